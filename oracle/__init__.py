@@ -1,0 +1,215 @@
+"""CPU oracle for OCP-MX block quantization -- TEST INFRASTRUCTURE ONLY.
+
+A plain, slow, double-precision C++ definition of what the GPU path computes (mx_oracle.cpp),
+loaded through ctypes. Only tests/, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of bench.py may import this package. The product library never
+imports, links or calls it, and the two share no code.
+
+Every function takes and returns numpy arrays in host memory. bf16 tensors travel as their raw
+uint16 bit patterns. Format ids: ``E2M1`` (MXFP4) and ``E4M3`` (MXFP8); scale layouts:
+``LINEAR`` ([M, K/32] row-major) and ``SWIZZLED`` (128x4 blocked, padded).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+E2M1 = 1
+E4M3 = 2
+LINEAR = 0
+SWIZZLED = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mx_oracle.cpp")
+_LIB = os.path.join(_HERE, "libmx_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile mx_oracle.cpp into libmx_oracle.so beside it (plain g++, no fast-math)."""
+    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["g++", "-std=c++17", "-O2", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off",
+             _SRC, "-o", tmp])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    p = ctypes.c_void_p
+    sig = {
+        "mxo_emax": (i32, [i32]),
+        "mxo_decode": (dbl, [i32, i32]),
+        "mxo_bf16_to_double": (dbl, [ctypes.c_uint16]),
+        "mxo_double_to_bf16": (ctypes.c_uint16, [dbl]),
+        "mxo_scale_byte": (i32, [i32, dbl]),
+        "mxo_quantize_block": (i32, [i32, p, i32, i32, p]),
+        "mxo_dequant_bf16": (ctypes.c_uint16, [i32, i32, i32]),
+        "mxo_swizzled_offset": (i64, [i64, i64, i64]),
+        "mxo_scales_shape": (None, [i64, i64, i32, p, p]),
+        "mxo_quantize": (None, [p, i64, i64, i32, i32, p, p]),
+        "mxo_qdq": (None, [p, i64, i64, i32, p]),
+        "mxo_rotate": (None, [p, i64, i64, p, i32, p]),
+        "mxo_rotate_quantize": (None, [p, i64, i64, p, i32, i32, i32, p, p]),
+        "mxo_rotate_qdq": (None, [p, i64, i64, p, i32, i32, p]),
+        "mxo_quantize_grouped": (None, [p, p, i32, i64, i32, i32, i64, p, p]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _bits(x) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    assert x.dtype == np.uint16, "bf16 tensors are passed as uint16 bit patterns"
+    return x
+
+
+# ----------------------------------------------------------------------------------------------
+# scalar helpers
+# ----------------------------------------------------------------------------------------------
+def emax(fmt: int) -> int:
+    return _load().mxo_emax(fmt)
+
+
+def decode(fmt: int, code: int) -> float:
+    """Value of one element code (sign included), scale 2^0."""
+    return _load().mxo_decode(fmt, code)
+
+
+def bf16_to_double(bits: int) -> float:
+    return _load().mxo_bf16_to_double(bits)
+
+
+def double_to_bf16(v: float) -> int:
+    """Round a double to bf16 once (nearest, ties to even); returns the bit pattern."""
+    return _load().mxo_double_to_bf16(v)
+
+
+def scale_byte(fmt: int, amax: float) -> int:
+    """E8M0 byte of a block with the given (finite, non-negative) abs-max."""
+    return _load().mxo_scale_byte(fmt, amax)
+
+
+def quantize_block(fmt: int, values, forced_byte: int = -1):
+    """Quantize one block of float64 values; returns (scale byte, unpacked codes uint8)."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    codes = np.zeros(v.size, dtype=np.uint8)
+    b = _load().mxo_quantize_block(fmt, _ptr(v), v.size, forced_byte, _ptr(codes))
+    return b, codes
+
+
+def dequant_bf16(fmt: int, code: int, scale: int) -> int:
+    return _load().mxo_dequant_bf16(fmt, code, scale)
+
+
+def swizzled_offset(r: int, c: int, padded_cols: int) -> int:
+    return _load().mxo_swizzled_offset(r, c, padded_cols)
+
+
+def scales_shape(M: int, K: int, layout: int):
+    rows = ctypes.c_int64()
+    cols = ctypes.c_int64()
+    _load().mxo_scales_shape(M, K, layout, ctypes.byref(rows), ctypes.byref(cols))
+    return rows.value, cols.value
+
+
+def grouped_scales_rows(counts, layout: int) -> int:
+    counts = [int(c) for c in counts]
+    if layout == LINEAR:
+        return sum(counts)
+    return sum(-(-c // 128) * 128 for c in counts)
+
+
+def code_bytes_per_row(fmt: int, K: int) -> int:
+    return K if fmt == E4M3 else K // 2
+
+
+# ----------------------------------------------------------------------------------------------
+# tensor operations
+# ----------------------------------------------------------------------------------------------
+def quantize(x_bits, fmt: int, layout: int):
+    """-> (codes uint8 [M, K or K/2], scales uint8 [rows, cols])."""
+    x = _bits(x_bits)
+    M, K = x.shape
+    codes = np.zeros((M, code_bytes_per_row(fmt, K)), dtype=np.uint8)
+    scales = np.zeros(scales_shape(M, K, layout), dtype=np.uint8)
+    _load().mxo_quantize(_ptr(x), M, K, fmt, layout, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def qdq(x_bits, fmt: int) -> np.ndarray:
+    """-> bf16 bits [M, K]."""
+    x = _bits(x_bits)
+    M, K = x.shape
+    out = np.zeros((M, K), dtype=np.uint16)
+    _load().mxo_qdq(_ptr(x), M, K, fmt, _ptr(out))
+    return out
+
+
+def rotate(x_bits, H_bits) -> np.ndarray:
+    """Pre-quantization rotated values y (float64 [M, K]), y_chunk = x_chunk @ H."""
+    x = _bits(x_bits)
+    H = _bits(H_bits)
+    M, K = x.shape
+    g = H.shape[0]
+    y = np.zeros((M, K), dtype=np.float64)
+    _load().mxo_rotate(_ptr(x), M, K, _ptr(H), g, _ptr(y))
+    return y
+
+
+def rotate_quantize(x_bits, H_bits, fmt: int, layout: int):
+    x = _bits(x_bits)
+    H = _bits(H_bits)
+    M, K = x.shape
+    codes = np.zeros((M, code_bytes_per_row(fmt, K)), dtype=np.uint8)
+    scales = np.zeros(scales_shape(M, K, layout), dtype=np.uint8)
+    _load().mxo_rotate_quantize(_ptr(x), M, K, _ptr(H), H.shape[0], fmt, layout, _ptr(codes),
+                                _ptr(scales))
+    return codes, scales
+
+
+def rotate_qdq(x_bits, H_bits, fmt: int) -> np.ndarray:
+    x = _bits(x_bits)
+    H = _bits(H_bits)
+    M, K = x.shape
+    out = np.zeros((M, K), dtype=np.uint16)
+    _load().mxo_rotate_qdq(_ptr(x), M, K, _ptr(H), H.shape[0], fmt, _ptr(out))
+    return out
+
+
+def quantize_grouped(x_bits, offsets, fmt: int, layout: int, scale_rows: int | None = None):
+    """Per-expert quantize. offsets: int64 [E+1] row offsets (host)."""
+    x = _bits(x_bits)
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    E = off.size - 1
+    M, K = x.shape
+    assert off[E] == M
+    counts = np.diff(off)
+    if scale_rows is None:
+        scale_rows = grouped_scales_rows(counts, layout)
+    cols = K // 32 if layout == LINEAR else -(-(K // 32) // 4) * 4
+    codes = np.zeros((M, code_bytes_per_row(fmt, K)), dtype=np.uint8)
+    scales = np.zeros((scale_rows, cols), dtype=np.uint8)
+    _load().mxo_quantize_grouped(_ptr(x), _ptr(off), E, K, fmt, layout, scale_rows, _ptr(codes),
+                                 _ptr(scales))
+    return codes, scales

@@ -1,0 +1,434 @@
+"""Pins for the CPU oracle: each test checks it against something other than itself.
+
+Sources of truth used here: the format definitions (spec constants and structure), closed forms
+worked by hand (tests/golden/), torch's CPU float8_e4m3fn / float8_e8m0fnu / bfloat16 casts
+(library routines), numpy/scipy routines, brute force and invariants.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from mx_microscaling_quantize_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16(values) -> np.ndarray:
+    return W.to_bf16_bits(np.asarray(values, dtype=np.float32))
+
+
+def all_finite_bf16() -> np.ndarray:
+    b = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    return b[((b >> 7) & 0xFF) != 0xFF]
+
+
+# ---------------------------------------------------------------------------------------------
+# element grids
+# ---------------------------------------------------------------------------------------------
+def test_e2m1_grid_from_spec_properties():
+    """E2M1: 8 magnitudes, strictly increasing; 0; min subnormal 0.5; min normal 1.0;
+    max normal 6.0; two values per binade (one mantissa bit); sign-magnitude codes."""
+    mags = [O.decode(O.E2M1, c) for c in range(8)]
+    assert mags[0] == 0.0
+    assert all(a < b for a, b in zip(mags, mags[1:]))
+    assert mags[1] == 0.5 and mags[2] == 1.0 and mags[7] == 6.0
+    for e in range(0, 3):  # binades [1,2), [2,4), [4,8)
+        inside = [m for m in mags if 2.0 ** e <= m < 2.0 ** (e + 1)]
+        assert len(inside) == 2 and inside[0] == 2.0 ** e
+        assert inside[1] - inside[0] == 2.0 ** (e - 1)
+    for c in range(8):
+        assert O.decode(O.E2M1, c | 8) == -mags[c]
+        assert math.copysign(1.0, O.decode(O.E2M1, c | 8)) == -1.0
+
+
+def test_e4m3_decode_matches_torch_all_bytes():
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            assert np.isnan(ref[c])  # the format's only NaN; the oracle never emits it
+            continue
+        assert O.decode(O.E4M3, c) == ref[c], hex(c)
+        assert math.copysign(1.0, O.decode(O.E4M3, c)) == math.copysign(1.0, ref[c])
+
+
+def test_e4m3_encode_matches_torch_cast_in_range():
+    """At scale byte 127 (s = 0) the element code is torch's RNE float8_e4m3fn cast, for every
+    finite bf16 value whose magnitude is below 464 (beyond, torch returns NaN, no saturation)."""
+    bits = all_finite_bf16()
+    vals = W.bf16_bits_to_float(bits).astype(np.float64)
+    keep = np.abs(vals) < 464
+    bits, vals = bits[keep], vals[keep]
+    _, codes = O.quantize_block(O.E4M3, vals, forced_byte=127)
+    ref = torch.from_numpy(vals.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
+    np.testing.assert_array_equal(codes, ref.numpy())
+
+
+def test_e4m3_saturates():
+    vals = np.array([464.0, 465.0, 480.0, 1e6, 3.0e38, -464.0, -1e30])
+    _, codes = O.quantize_block(O.E4M3, vals, forced_byte=127)
+    np.testing.assert_array_equal(codes, [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE])
+
+
+def test_e2m1_nearest_and_ties_brute_force():
+    """For t on a fine grid, the E2M1 code is a nearest grid point and, on ties, the even code."""
+    mags = np.array([O.decode(O.E2M1, c) for c in range(8)])
+    t = np.arange(-8 * 64, 8 * 64 + 1) / 64.0
+    _, codes = O.quantize_block(O.E2M1, t, forced_byte=127)
+    for ti, c in zip(t, codes):
+        m = mags[c & 7]
+        a = min(abs(ti), 6.0)
+        d = np.abs(mags - a)
+        assert abs(m - a) == d.min(), (ti, c)
+        if np.sum(d == d.min()) == 2:
+            assert (c & 1) == 0, (ti, c)
+        assert bool(c & 8) == (ti < 0 or (ti == 0 and math.copysign(1, ti) < 0)), (ti, c)
+
+
+def _read_worked_blocks(name):
+    blocks = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        parts = line.split()
+        if parts[0] == "block":
+            blocks.append((parts[1], int(parts[2]), []))
+        else:
+            blocks[-1][2].append((float(parts[0]), int(parts[1], 16)))
+    return blocks
+
+
+@pytest.mark.parametrize("fmt,name", [(O.E2M1, "e2m1_worked_blocks.txt"),
+                                      (O.E4M3, "e4m3_worked_blocks.txt")])
+def test_worked_blocks(fmt, name):
+    for bname, byte, entries in _read_worked_blocks(name):
+        v = np.zeros(32)
+        want = np.zeros(32, dtype=np.uint8)
+        for i, (val, code) in enumerate(entries):
+            v[i] = val
+            want[i] = code
+        assert bf16(v).astype(np.uint32).tolist() == bf16(v).tolist()
+        assert (W.bf16_bits_to_float(bf16(v)) == v.astype(np.float32)).all(), bname
+        got_byte, got = O.quantize_block(fmt, v)
+        assert got_byte == byte, bname
+        np.testing.assert_array_equal(got, want, err_msg=bname)
+        # the same block through the tensor entry point (packing / linear scale layout)
+        codes, scales = O.quantize(bf16(v).reshape(1, 32), fmt, O.LINEAR)
+        assert scales[0, 0] == byte
+        if fmt == O.E4M3:
+            np.testing.assert_array_equal(codes[0], want)
+        else:
+            np.testing.assert_array_equal(codes[0] & 0xF, want[0::2])
+            np.testing.assert_array_equal(codes[0] >> 4, want[1::2])
+
+
+# ---------------------------------------------------------------------------------------------
+# scales
+# ---------------------------------------------------------------------------------------------
+def test_scale_bytes_closed_form_table():
+    for line in open(os.path.join(GOLDEN, "scale_bytes.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        a, b2, b8 = line.split()
+        amax = 2.0 ** int(a[2:]) if a.startswith("2^") else float(a)
+        assert O.scale_byte(O.E2M1, amax) == int(b2), a
+        assert O.scale_byte(O.E4M3, amax) == int(b8), a
+        # through a whole block (amax placed at a varying position)
+        v = np.zeros(32)
+        v[int(b2) % 32] = -amax
+        assert O.quantize_block(O.E2M1, v)[0] == int(b2)
+        assert O.quantize_block(O.E4M3, v)[0] == int(b8)
+
+
+@pytest.mark.parametrize("fmt", [O.E2M1, O.E4M3])
+def test_scale_bracket_invariant_every_bf16_amax(fmt):
+    """For every non-negative finite bf16 amax: 2^(s+emax) <= amax < 2^(s+emax+1) unless the
+    scale is clamped at s = -127 (then amax < 2^(-127+emax+1)); decode via torch's e8m0."""
+    emax = 2 if fmt == O.E2M1 else 8
+    bits = all_finite_bf16()
+    bits = bits[bits < 0x8000]
+    vals = W.bf16_bits_to_float(bits).astype(np.float64)
+    e8 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).double().numpy()
+    for amax in vals:
+        byte = O.scale_byte(fmt, float(amax))
+        assert 0 <= byte <= 254
+        scale = e8[byte]
+        if amax == 0:
+            assert byte == 0
+            continue
+        lo = scale * 2.0 ** emax
+        if byte > 0:
+            assert lo <= amax < 2 * lo, (amax, byte)
+        else:
+            assert amax < 2 * lo, (amax, byte)
+            assert amax < 2.0 ** (-126 + emax) or lo <= amax
+
+
+def test_zero_block():
+    for fmt in (O.E2M1, O.E4M3):
+        b, codes = O.quantize_block(fmt, np.zeros(32))
+        assert b == 0 and not codes.any()
+        v = np.zeros(32)
+        v[3] = -0.0
+        b, codes = O.quantize_block(fmt, v)
+        sign = 0x8 if fmt == O.E2M1 else 0x80
+        assert b == 0 and codes[3] == sign and codes.sum() == sign
+
+
+def test_nan_and_inf_blocks():
+    for fmt, fill in ((O.E2M1, 0), (O.E4M3, 0x7F)):
+        for bad in (float("nan"), float("inf"), -float("inf")):
+            v = np.linspace(-1, 1, 32)
+            v[7] = bad
+            b, codes = O.quantize_block(fmt, v)
+            assert b == 0xFF and (codes == fill).all()
+            x = bf16(v).reshape(1, 32)
+            assert (O.qdq(x, fmt) == 0x7FC0).all()
+
+
+# ---------------------------------------------------------------------------------------------
+# round trip, dequantization, idempotence
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("fmt", [O.E2M1, O.E4M3])
+def test_every_representable_value_round_trips_at_scale_one(fmt):
+    n = 16 if fmt == O.E2M1 else 256
+    sign = 0x8 if fmt == O.E2M1 else 0x80
+    anchor = 6.0 if fmt == O.E2M1 else 448.0  # amax in [2^emax, 2^(emax+1)) forces s = 0
+    for c in range(n):
+        if fmt == O.E4M3 and (c & 0x7F) == 0x7F:
+            continue
+        v = np.zeros(32)
+        v[0] = anchor
+        v[1] = O.decode(fmt, c)
+        b, codes = O.quantize_block(fmt, v)
+        assert b == 127
+        assert codes[1] == c or (v[1] == 0 and (codes[1] & ~sign) == 0 and codes[1] == c)
+        x = bf16(v).reshape(1, 32)
+        out = O.qdq(x, fmt)
+        np.testing.assert_array_equal(out, x)
+
+
+def test_dequant_matches_torch_bf16_rounding():
+    """decode(code) * 2^s rounded once to bf16 == torch's float64 -> bfloat16 cast of the same
+    exact product (exact in float32, so torch's float path rounds it once)."""
+    for fmt, codes in ((O.E2M1, range(16)), (O.E4M3, [c for c in range(256) if c & 0x7F != 0x7F])):
+        for byte in list(range(0, 12)) + list(range(120, 135)) + list(range(240, 255)):
+            for c in codes:
+                exact = O.decode(fmt, c) * 2.0 ** (byte - 127)
+                want = torch.tensor([exact], dtype=torch.float64).to(torch.bfloat16)
+                want = int(want.view(torch.int16).item()) & 0xFFFF
+                assert O.dequant_bf16(fmt, c, byte) == want, (fmt, c, byte)
+
+
+def test_bf16_conversions_against_torch():
+    bits = all_finite_bf16()
+    for b in bits[::97]:
+        v = O.bf16_to_double(int(b))
+        t = torch.tensor([int(b)], dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+        assert v == t.double().item() and math.copysign(1, v) == math.copysign(1, t.item())
+        assert O.double_to_bf16(v) == b
+    rng = np.random.default_rng(5)
+    vals = rng.standard_normal(2000).astype(np.float32) * np.float32(2.0) ** rng.integers(
+        -140, 120, 2000).astype(np.float32)
+    want = W.to_bf16_bits(vals)
+    got = np.array([O.double_to_bf16(float(v)) for v in vals], dtype=np.uint16)
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("fmt", [O.E2M1, O.E4M3])
+def test_qdq_idempotent(fmt):
+    x = W.mxfp4_qdq_activation(64, 256)
+    y = O.qdq(x, fmt)
+    z = O.qdq(y, fmt)
+    np.testing.assert_array_equal(z, y)
+    x = W.mxfp4_qdq_weight(64, 256)
+    y = O.qdq(x, fmt)
+    np.testing.assert_array_equal(O.qdq(y, fmt), y)
+
+
+def test_qdq_equals_dequantized_codes():
+    x = W.mxfp8_linear_quant(8, 256)
+    for fmt in (O.E2M1, O.E4M3):
+        codes, scales = O.quantize(x, fmt, O.LINEAR)
+        out = O.qdq(x, fmt)
+        for r in range(8):
+            for k in range(0, 256, 7):
+                if fmt == O.E4M3:
+                    c = codes[r, k]
+                else:
+                    c = (codes[r, k // 2] >> (4 * (k % 2))) & 0xF
+                assert out[r, k] == O.dequant_bf16(fmt, int(c), int(scales[r, k // 32]))
+
+
+# ---------------------------------------------------------------------------------------------
+# layouts
+# ---------------------------------------------------------------------------------------------
+def to_blocked_reference(scales: torch.Tensor) -> torch.Tensor:
+    """The 128x4 blocked rearrangement written with tensor reshapes (pad, cut into 128x4 tiles,
+    row-block-major; inside a tile the 4 row-quarters of 32 rows are interleaved per row)."""
+    rows, cols = scales.shape
+    R = -(-rows // 128) * 128
+    C = -(-cols // 4) * 4
+    p = torch.zeros((R, C), dtype=scales.dtype)
+    p[:rows, :cols] = scales
+    t = p.view(R // 128, 128, C // 4, 4).permute(0, 2, 1, 3)   # [rb, cb, 128, 4]
+    t = t.reshape(-1, 4, 32, 4).transpose(1, 2)                # [tile, 32, 4 quarters, 4]
+    return t.reshape(-1)
+
+
+@pytest.mark.parametrize("M,K", [(1, 32), (5, 96), (128, 128), (130, 416), (300, 4096)])
+def test_swizzled_layout_matches_reshape_formulation_and_is_bijective(M, K):
+    x = W.mxfp8_linear_quant(M, K, stream=M)
+    for fmt in (O.E2M1, O.E4M3):
+        codes_l, lin = O.quantize(x, fmt, O.LINEAR)
+        codes_s, swz = O.quantize(x, fmt, O.SWIZZLED)
+        np.testing.assert_array_equal(codes_l, codes_s)
+        want = to_blocked_reference(torch.from_numpy(lin)).numpy()
+        np.testing.assert_array_equal(swz.reshape(-1), want)
+        R, C = swz.shape
+        assert R == -(-M // 128) * 128 and C == -(-(K // 32) // 4) * 4
+        offs = {O.swizzled_offset(r, c, C) for r in range(R) for c in range(C)}
+        assert offs == set(range(R * C))
+
+
+def test_e2m1_nibble_order():
+    v = np.zeros(32)
+    v[0], v[1] = 1.0, -6.0  # codes 0x2 and 0xF
+    codes, _ = O.quantize(bf16(v).reshape(1, 32), O.E2M1, O.LINEAR)
+    assert codes[0, 0] == 0xF2
+
+
+# ---------------------------------------------------------------------------------------------
+# rotation
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("g", [16, 32, 64, 128])
+def test_hadamard_input_generator(g):
+    import scipy.linalg
+    h = W.sylvester_hadamard(g)
+    np.testing.assert_array_equal(h, scipy.linalg.hadamard(g))
+    hn = h * g ** -0.5
+    np.testing.assert_allclose(hn @ hn.T, np.eye(g), atol=1e-15)
+    hb = W.bf16_bits_to_float(W.normalized_hadamard_bf16(g)).astype(np.float64)
+    assert np.all(np.abs(hb - hn) <= 2.0 ** -9 * np.abs(hn))
+    if g in (16, 64):
+        np.testing.assert_array_equal(hb, hn)
+
+
+@pytest.mark.parametrize("g", [16, 32, 64, 128])
+def test_rotation_against_numpy_matmul(g):
+    K = 256
+    x = W.rotation_sweep_input("attn_in", 6, K)
+    H = W.normalized_hadamard_bf16(g)
+    y = O.rotate(x, H)
+    xd = W.bf16_bits_to_float(x).astype(np.float64)
+    hd = W.bf16_bits_to_float(H).astype(np.float64)
+    want = (xd.reshape(6, K // g, g) @ hd).reshape(6, K)
+    np.testing.assert_allclose(y, want, rtol=0, atol=1e-12 * np.abs(xd).max())
+
+
+def test_rotation_identity_reduces_to_plain_path():
+    x = W.mxfp4_qdq_activation(8, 512)
+    for g in (16, 32, 64, 128):
+        eye = W.to_bf16_bits(np.eye(g))
+        np.testing.assert_array_equal(O.rotate(x, eye), W.bf16_bits_to_float(x))
+        for fmt in (O.E2M1, O.E4M3):
+            for layout in (O.LINEAR, O.SWIZZLED):
+                a = O.rotate_quantize(x, eye, fmt, layout)
+                b = O.quantize(x, fmt, layout)
+                np.testing.assert_array_equal(a[0], b[0])
+                np.testing.assert_array_equal(a[1], b[1])
+            np.testing.assert_array_equal(O.rotate_qdq(x, eye, fmt), O.qdq(x, fmt))
+
+
+def test_rotation_spike_gives_hadamard_row_and_norm_is_kept():
+    g = 64
+    H = W.normalized_hadamard_bf16(g)
+    hd = W.bf16_bits_to_float(H).astype(np.float64)
+    x = np.zeros((1, 128), dtype=np.float32)
+    x[0, 64 + 5] = 2.0
+    y = O.rotate(W.to_bf16_bits(x), H)
+    assert (y[0, :64] == 0).all()
+    np.testing.assert_array_equal(y[0, 64:], 2.0 * hd[5])
+    xr = W.rotation_sweep_input("o_proj_in", 4, 512)
+    y = O.rotate(xr, H)  # g = 64: bf16(64^-0.5) = 1/8 exactly, H orthonormal
+    xd = W.bf16_bits_to_float(xr).astype(np.float64)
+    for c in range(0, 512, 64):
+        np.testing.assert_allclose(np.linalg.norm(y[:, c:c + 64], axis=1),
+                                   np.linalg.norm(xd[:, c:c + 64], axis=1), rtol=1e-14)
+
+
+def test_rotate_quantize_is_quantize_of_rotated_values():
+    x = W.rotate_quant_activation(3, 256)
+    H = W.normalized_hadamard_bf16(32)
+    y = O.rotate(x, H)
+    codes, scales = O.rotate_quantize(x, H, O.E2M1, O.LINEAR)
+    for r in range(3):
+        for j in range(8):
+            b, c = O.quantize_block(O.E2M1, y[r, 32 * j:32 * j + 32])
+            assert scales[r, j] == b
+            packed = c[0::2] | (c[1::2] << 4)
+            np.testing.assert_array_equal(codes[r, 16 * j:16 * j + 16], packed)
+
+
+# ---------------------------------------------------------------------------------------------
+# grouped (MoE)
+# ---------------------------------------------------------------------------------------------
+def test_grouped_single_expert_equals_plain():
+    x = W.mxfp8_linear_quant(200, 256)
+    off = np.array([0, 200])
+    for fmt in (O.E2M1, O.E4M3):
+        for layout in (O.LINEAR, O.SWIZZLED):
+            a = O.quantize_grouped(x, off, fmt, layout)
+            b = O.quantize(x, fmt, layout)
+            np.testing.assert_array_equal(a[0], b[0])
+            np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_grouped_experts_are_independent_blocks():
+    counts = [0, 5, 128, 0, 130, 1]
+    off = np.concatenate([[0], np.cumsum(counts)])
+    x = W.mxfp8_linear_quant(int(off[-1]), 160)
+    codes, swz = O.quantize_grouped(x, off, O.E4M3, O.SWIZZLED)
+    assert swz.shape == (128 + 128 + 256 + 128, 8)
+    prow = 0
+    for e, n in enumerate(counts):
+        if n == 0:
+            continue
+        c, s = O.quantize(x[off[e]:off[e + 1]], O.E4M3, O.SWIZZLED)
+        np.testing.assert_array_equal(codes[off[e]:off[e + 1]], c)
+        flat = swz.reshape(-1)[prow * 8:(prow + s.shape[0]) * 8]
+        np.testing.assert_array_equal(flat, s.reshape(-1))
+        prow += s.shape[0]
+
+
+def test_workload_recipes():
+    x = W.mxfp8_linear_quant(128, 4096)
+    assert x.shape == (128, 4096) and x.dtype == np.uint16
+    f = W.bf16_bits_to_float(x)
+    for r in range(128):
+        j = (37 * r) % 128
+        assert (f[r, 32 * j:32 * j + 32] == 0).all()
+    assert 0.005 < (np.abs(f) > 6).mean() < 0.02
+    counts = W.moe_counts()
+    assert counts.sum() == 16384 and counts.size == 128 and counts.max() > 1000
+    np.testing.assert_array_equal(W.mxfp8_linear_quant(4, 64), W.mxfp8_linear_quant(4, 64))
+
+
+@pytest.mark.parametrize("g", [16, 32, 128])
+def test_rotation_orientation_with_non_symmetric_matrix(g):
+    """y_chunk = x_chunk @ H (row vector times matrix), checked with a random, non-symmetric H
+    against numpy's matmul; the transposed product must differ."""
+    rng = np.random.default_rng(g)
+    H = W.to_bf16_bits(rng.standard_normal((g, g)) / np.sqrt(g))
+    x = W.rotate_quant_activation(5, 2 * g)
+    y = O.rotate(x, H)
+    xd = W.bf16_bits_to_float(x).astype(np.float64).reshape(5, 2, g)
+    hd = W.bf16_bits_to_float(H).astype(np.float64)
+    np.testing.assert_allclose(y, (xd @ hd).reshape(5, 2 * g), rtol=0, atol=1e-12)
+    assert np.abs(y - (xd @ hd.T).reshape(5, 2 * g)).max() > 1e-3
