@@ -1,0 +1,155 @@
+/*
+ * mxq.h -- C ABI of libmxq: OCP-MX block quantization (MXFP4 / MXFP8) on one GB300 GPU.
+ *
+ * What the library computes (sources are the pages this library restates):
+ *  - "[Transform] [Quantization] Add QuTLASS support to vLLM" (vllm PR 24440), feature list:
+ *    abs-max block scales ("Multiple quantization schemes ... Abs-Max"), the MXFP4 format,
+ *    "Fused transform + quantization + scale computation", rotation matrices "loaded at
+ *    runtime, allowing any transformation", rotation sizes 16/32/64/128; review thread on
+ *    vllm/_custom_ops.py (`fusedQuantizeMx(a, b, ...)` returning packed E2M1 codes and E8M0
+ *    scales of shape `padded_rows x padded_cols`) and on vllm/qutlass_utils/utils.py
+ *    (`to_blocked`: the blocked scale layout block-scaled GEMMs consume).
+ *  - "use cute-dsl to speedup mxfp QDQ" (intel/neural-compressor PR 2548), Description:
+ *    MXFP4 / MXFP8 QDQ on contiguous input, group size 32, K divisible by 32, CUDA-Graph use.
+ *  - prhub summary of vllm PR 47229, code snippet of mxfp8_utils.py: MXFP8 (E4M3) quantize
+ *    with MXFP8_BLOCK_SIZE = 32 returning codes and scales, scales viewed as [M, K/32] when not
+ *    swizzled, or in the swizzled layout when `is_sf_swizzled_layout`.
+ *
+ * Arithmetic (the pages name the formats but print no formula; this is the OCP MX reading):
+ *  For every block of 32 consecutive elements along K of a bf16 row-major [M, K] matrix:
+ *    amax = max |v_i|;  s = clamp(floor(log2 amax) - emax, -127, 127)  (emax = 2 for E2M1,
+ *    8 for E4M3; an all-zero block gets s = -127);  E8M0 scale byte = s + 127;
+ *    code_i = v_i / 2^s rounded to nearest-even on the element grid, saturating at the largest
+ *    finite magnitude (6 for E2M1, 448 for E4M3), sign kept (also for zero);
+ *    QDQ output_i = bf16_round_nearest_even(decode(code_i) * 2^s).
+ *  A block holding a NaN or an infinity gets scale byte 0xFF; its codes are 0x7F (E4M3) or
+ *  0x0 (E2M1) and its QDQ outputs are the bf16 NaN 0x7FC0.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named x, y, codes, scales, H, row_offsets are DEVICE memory owned by the caller;
+ *    the library never allocates, frees or synchronizes, and never reads device memory on the
+ *    host. Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream) and is
+ *    asynchronous.
+ *  - Validation happens on the host before any launch; on error nothing is launched and the
+ *    status says why. After the launch, a launch failure maps to MX_ERR_CUDA.
+ *  - x, y, codes and (swizzled) scales must be 16-byte aligned; rows are contiguous.
+ *  - M == 0 or K == 0 is a valid empty call: nothing is launched, MX_OK is returned.
+ *  - Layouts: E4M3 codes are [M, K] bytes (float8_e4m3fn). E2M1 codes are [M, K/2] bytes, two
+ *    codes per byte, the lower K index in the low nibble. Linear scales are [M, K/32] bytes,
+ *    row-major. Swizzled scales are [ceil(M/128)*128, ceil(K/128)*4] bytes: the scale matrix is
+ *    padded with zero bytes and cut into 128x4 tiles of 512 bytes, stored row-block-major; scale
+ *    (r, c) of a tile sits at byte (r % 32) * 16 + (r / 32) * 4 + c. Every byte, pads
+ *    included, is written by each call.
+ */
+#ifndef MXQ_H
+#define MXQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int mx_status;
+
+/* status codes */
+#define MX_OK 0
+#define MX_ERR_NULL 1        /* a required pointer is NULL */
+#define MX_ERR_SHAPE 2       /* negative size, K % 32 != 0, K % g != 0, bad expert count */
+#define MX_ERR_ALIGN 3       /* a pointer is not 16-byte aligned */
+#define MX_ERR_UNSUPPORTED 4 /* unknown format / layout / rounding, group != 32, bad g */
+#define MX_ERR_CUDA 5        /* the CUDA runtime reported an error at launch */
+
+/* element formats */
+#define MX_FMT_E2M1 1 /* MXFP4: 1 sign, 2 exponent, 1 mantissa bit */
+#define MX_FMT_E4M3 2 /* MXFP8: 1 sign, 4 exponent, 3 mantissa bits ("fn": max 448, no Inf) */
+
+/* scale layouts */
+#define MX_SCALES_LINEAR 0   /* [M, K/32] row-major */
+#define MX_SCALES_SWIZZLED 1 /* 128x4 blocked tiles, padded (see above) */
+
+/* rounding schemes */
+#define MX_ROUND_RNE 0 /* abs-max floor scale, round to nearest even, saturate */
+
+/* Text of a status code (static storage). */
+const char* mx_status_string(mx_status status);
+
+/*
+ * Shape of the scale matrix for an [M, K] input: linear [M, K/32]; swizzled
+ * [ceil(M/128)*128, ceil(K/128)*4]. Host only, launches nothing.
+ * Errors: MX_ERR_NULL (rows or cols NULL), MX_ERR_SHAPE (M < 0, K < 0, K % 32),
+ * MX_ERR_UNSUPPORTED (group != 32, unknown layout).
+ */
+mx_status mx_scales_shape(int64_t M, int64_t K, int group, int layout, int64_t* rows,
+                          int64_t* cols);
+
+/*
+ * Block quantize (pages: fusedQuantizeMx without the rotation; mxfp8_quantize).
+ * x: bf16 [M, K]. codes: see layouts. scales: per `layout`. fmt: MX_FMT_*. group: must be 32.
+ * rounding: MX_ROUND_RNE. Errors: see conventions.
+ */
+mx_status mx_quantize(const void* x, int64_t M, int64_t K, int fmt, int group, int layout,
+                      int rounding, void* codes, void* scales, void* stream);
+
+/*
+ * QDQ: quantize then dequantize, bf16 in, bf16 out (pages: mxfp4_qdq / mxfp8_qdq).
+ * If H is not NULL, every g-element chunk along K is first rotated, y_chunk = x_chunk * H
+ * (H: bf16 [g, g] row-major device matrix, g in {16, 32, 64, 128}, K % g == 0), and the
+ * rotated values are quantized; the output stays in the rotated basis. If H is NULL, g is
+ * ignored. y: bf16 [M, K], must not overlap x.
+ */
+mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int rounding,
+                 const void* H, int g, void* y, void* stream);
+
+/*
+ * Fused rotate + quantize (pages: fusedQuantizeMx(a, b) with b the runtime-loaded rotation).
+ * y_chunk = x_chunk * H for every g-chunk along K (bf16 products, fp32 accumulation on the
+ * tensor cores), then the block quantization above on the fp32 rotated values.
+ * H: bf16 [g, g] row-major, g in {16, 32, 64, 128}, K % g == 0. Other arguments as
+ * mx_quantize.
+ */
+mx_status mx_rotate_quantize(const void* x, int64_t M, int64_t K, const void* H, int g, int fmt,
+                             int group, int layout, int rounding, void* codes, void* scales,
+                             void* stream);
+
+/*
+ * Scale-matrix shape for a grouped call with E experts and M_total rows: linear
+ * [M_total, K/32]; swizzled [R, ceil(K/128)*4] with R = floor((M_total + 127*E) / 128) * 128,
+ * an upper bound of sum_e ceil(n_e/128)*128 valid for any split of M_total rows.
+ */
+mx_status mx_grouped_scales_shape(int64_t M_total, int E, int64_t K, int group, int layout,
+                                  int64_t* rows, int64_t* cols);
+
+/*
+ * Grouped (MoE expert) quantize. Rows [row_offsets[e], row_offsets[e+1]) of x belong to
+ * expert e (row_offsets: DEVICE int64 [E+1], row_offsets[0] = 0, row_offsets[E] = M_total,
+ * non-decreasing). Codes stay contiguous as for mx_quantize on the whole x. Linear scales are
+ * [M_total, K/32]. Swizzled scales give each expert its own run of 128-row tiles: expert e's
+ * rows start at padded row P_e = sum_{e' < e} ceil(n_e'/128) * 128; the buffer has
+ * mx_grouped_scales_shape() rows and all of it is written (rows past the last expert: zero).
+ * 1 <= E <= 1024. Offsets that break the contract give unspecified values but every access
+ * stays inside x, codes and scales.
+ */
+mx_status mx_quantize_grouped(const void* x, const int64_t* row_offsets, int E, int64_t M_total,
+                              int64_t K, int fmt, int group, int layout, int rounding,
+                              void* codes, void* scales, void* stream);
+
+/*
+ * Diagnostics: the rotated values y = x_chunk * H exactly as mx_rotate_quantize computes them
+ * before quantization (same device code), written as fp32 [M, K] to y_f32 (device).
+ */
+mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, int g, float* y_f32,
+                          void* stream);
+
+/*
+ * Device-side error word of the current device: bit 0 set if a kernel gave up waiting for
+ * its tensor-core work to complete (a bounded wait ran out; its outputs are then invalid).
+ * Synchronizes the device, returns the word in *flags and clears it.
+ */
+mx_status mx_device_errors(int* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXQ_H */

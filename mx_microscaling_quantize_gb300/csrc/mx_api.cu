@@ -1,0 +1,211 @@
+// mx_api.cu -- the extern "C" entry points declared in include/mxq.h: host-side validation,
+// shape arithmetic and launch selection. No allocation, no synchronization, no device reads.
+#include <cstdint>
+
+#include "mx_launch.h"
+#include "mxq.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+bool valid_fmt(int fmt) { return fmt == MX_FMT_E2M1 || fmt == MX_FMT_E4M3; }
+bool valid_layout(int layout) { return layout == MX_SCALES_LINEAR || layout == MX_SCALES_SWIZZLED; }
+bool valid_g(int g) { return g == 16 || g == 32 || g == 64 || g == 128; }
+
+// Checks shared by every call on an [M, K] bf16 input. Returns MX_OK to go on; *empty is set
+// when there is nothing to compute.
+mx_status check_common(int64_t M, int64_t K, int fmt, int group, int rounding, bool* empty) {
+  if (M < 0 || K < 0) return MX_ERR_SHAPE;
+  if (group != 32) return MX_ERR_UNSUPPORTED;
+  if (!valid_fmt(fmt)) return MX_ERR_UNSUPPORTED;
+  if (rounding != MX_ROUND_RNE) return MX_ERR_UNSUPPORTED;
+  if (K % 32 != 0) return MX_ERR_SHAPE;
+  // element indices are formed in int64: keep M * K far from overflow
+  if (K > 0 && M > (int64_t(1) << 40) / K) return MX_ERR_SHAPE;
+  *empty = (M == 0 || K == 0);
+  return MX_OK;
+}
+
+mx_status from_cuda(cudaError_t err) { return err == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
+
+mxq::RotArgs rot_args(const void* x, int64_t M, int64_t K, const void* H, void* out) {
+  mxq::RotArgs a{};
+  a.x = x;
+  a.H = H;
+  a.out = out;
+  a.M = M;
+  a.K = K;
+  a.col_tiles = ceil_div(K, mxq::kTileCols);
+  a.row_blocks = ceil_div(M, mxq::kTileRows);
+  return a;
+}
+
+mxq::StreamArgs stream_args(const void* x, int64_t M, int64_t K, void* out) {
+  mxq::StreamArgs a{};
+  a.x = x;
+  a.out = out;
+  a.M = M;
+  a.K = K;
+  a.col_tiles = ceil_div(K, mxq::kTileCols);
+  a.row_blocks = ceil_div(M, mxq::kTileRows);
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mx_status_string(mx_status status) {
+  switch (status) {
+    case MX_OK: return "MX_OK";
+    case MX_ERR_NULL: return "MX_ERR_NULL: a required pointer is NULL";
+    case MX_ERR_SHAPE: return "MX_ERR_SHAPE: invalid size (negative, K % 32, K % g, experts)";
+    case MX_ERR_ALIGN: return "MX_ERR_ALIGN: a buffer is not 16-byte aligned";
+    case MX_ERR_UNSUPPORTED: return "MX_ERR_UNSUPPORTED: format, layout, rounding, group or g";
+    case MX_ERR_CUDA: return "MX_ERR_CUDA: the CUDA runtime reported an error at launch";
+    default: return "unknown mx_status";
+  }
+}
+
+mx_status mx_scales_shape(int64_t M, int64_t K, int group, int layout, int64_t* rows,
+                          int64_t* cols) {
+  if (!rows || !cols) return MX_ERR_NULL;
+  if (M < 0 || K < 0 || K % 32 != 0) return MX_ERR_SHAPE;
+  if (group != 32 || !valid_layout(layout)) return MX_ERR_UNSUPPORTED;
+  if (layout == MX_SCALES_LINEAR) {
+    *rows = M;
+    *cols = K / 32;
+  } else {
+    *rows = ceil_div(M, mxq::kTileRows) * mxq::kTileRows;
+    *cols = ceil_div(K, mxq::kTileCols) * 4;
+  }
+  return MX_OK;
+}
+
+mx_status mx_grouped_scales_shape(int64_t M_total, int E, int64_t K, int group, int layout,
+                                  int64_t* rows, int64_t* cols) {
+  if (!rows || !cols) return MX_ERR_NULL;
+  if (M_total < 0 || K < 0 || K % 32 != 0 || E < 1 || E > 1024) return MX_ERR_SHAPE;
+  if (group != 32 || !valid_layout(layout)) return MX_ERR_UNSUPPORTED;
+  if (layout == MX_SCALES_LINEAR) {
+    *rows = M_total;
+    *cols = K / 32;
+  } else {
+    *rows = (M_total + int64_t(mxq::kTileRows - 1) * E) / mxq::kTileRows * mxq::kTileRows;
+    *cols = ceil_div(K, mxq::kTileCols) * 4;
+  }
+  return MX_OK;
+}
+
+mx_status mx_quantize(const void* x, int64_t M, int64_t K, int fmt, int group, int layout,
+                      int rounding, void* codes, void* scales, void* stream) {
+  bool empty = false;
+  mx_status st = check_common(M, K, fmt, group, rounding, &empty);
+  if (st != MX_OK) return st;
+  if (!valid_layout(layout)) return MX_ERR_UNSUPPORTED;
+  if (empty) return MX_OK;
+  if (!x || !codes || !scales) return MX_ERR_NULL;
+  if (!aligned16(x) || !aligned16(codes)) return MX_ERR_ALIGN;
+  if (layout == MX_SCALES_SWIZZLED && !aligned16(scales)) return MX_ERR_ALIGN;
+  mxq::StreamArgs a = stream_args(x, M, K, codes);
+  a.scales = static_cast<uint8_t*>(scales);
+  a.scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : a.col_tiles * 4;
+  return from_cuda(mxq::launch_stream(fmt, false, layout == MX_SCALES_SWIZZLED, false, a,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int rounding,
+                 const void* H, int g, void* y, void* stream) {
+  bool empty = false;
+  mx_status st = check_common(M, K, fmt, group, rounding, &empty);
+  if (st != MX_OK) return st;
+  if (H) {
+    if (!valid_g(g)) return MX_ERR_UNSUPPORTED;
+    if (K % g != 0) return MX_ERR_SHAPE;
+  }
+  if (empty) return MX_OK;
+  if (!x || !y) return MX_ERR_NULL;
+  if (!aligned16(x) || !aligned16(y)) return MX_ERR_ALIGN;
+  if (H) {
+    if (reinterpret_cast<uintptr_t>(H) & 1u) return MX_ERR_ALIGN;
+    return from_cuda(mxq::launch_rotate(fmt, mxq::kRotQdq, false, g, rot_args(x, M, K, H, y),
+                                        static_cast<cudaStream_t>(stream)));
+  }
+  return from_cuda(mxq::launch_stream(fmt, true, false, false, stream_args(x, M, K, y),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+mx_status mx_rotate_quantize(const void* x, int64_t M, int64_t K, const void* H, int g, int fmt,
+                             int group, int layout, int rounding, void* codes, void* scales,
+                             void* stream) {
+  bool empty = false;
+  mx_status st = check_common(M, K, fmt, group, rounding, &empty);
+  if (st != MX_OK) return st;
+  if (!valid_layout(layout) || !valid_g(g)) return MX_ERR_UNSUPPORTED;
+  if (K % g != 0) return MX_ERR_SHAPE;
+  if (empty) return MX_OK;
+  if (!x || !H || !codes || !scales) return MX_ERR_NULL;
+  if (!aligned16(x) || !aligned16(codes)) return MX_ERR_ALIGN;
+  if (layout == MX_SCALES_SWIZZLED && !aligned16(scales)) return MX_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(H) & 1u) return MX_ERR_ALIGN;
+  mxq::RotArgs a = rot_args(x, M, K, H, codes);
+  a.scales = static_cast<uint8_t*>(scales);
+  a.scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : a.col_tiles * 4;
+  return from_cuda(mxq::launch_rotate(fmt, mxq::kRotCodes, layout == MX_SCALES_SWIZZLED, g, a,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+mx_status mx_quantize_grouped(const void* x, const int64_t* row_offsets, int E, int64_t M_total,
+                              int64_t K, int fmt, int group, int layout, int rounding,
+                              void* codes, void* scales, void* stream) {
+  bool empty = false;
+  mx_status st = check_common(M_total, K, fmt, group, rounding, &empty);
+  if (st != MX_OK) return st;
+  if (!valid_layout(layout)) return MX_ERR_UNSUPPORTED;
+  if (E < 1 || E > 1024) return MX_ERR_SHAPE;
+  int64_t srows = 0, scols = 0;
+  st = mx_grouped_scales_shape(M_total, E, K, group, layout, &srows, &scols);
+  if (st != MX_OK) return st;
+  if (empty) return MX_OK;
+  if (!row_offsets || !x || !codes || !scales) return MX_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(row_offsets) & 7u) return MX_ERR_ALIGN;
+  if (!aligned16(x) || !aligned16(codes)) return MX_ERR_ALIGN;
+  if (layout == MX_SCALES_SWIZZLED && !aligned16(scales)) return MX_ERR_ALIGN;
+  mxq::StreamArgs a = stream_args(x, M_total, K, codes);
+  a.scales = static_cast<uint8_t*>(scales);
+  // every expert adds at most one partial 128-row block
+  a.row_blocks = layout == MX_SCALES_LINEAR ? ceil_div(M_total, mxq::kTileRows) + E
+                                            : srows / mxq::kTileRows;
+  a.scale_cols = scols;
+  a.offsets = row_offsets;
+  a.E = E;
+  return from_cuda(mxq::launch_stream(fmt, false, layout == MX_SCALES_SWIZZLED, true, a,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, int g, float* y_f32,
+                          void* stream) {
+  bool empty = false;
+  mx_status st = check_common(M, K, MX_FMT_E2M1, 32, MX_ROUND_RNE, &empty);
+  if (st != MX_OK) return st;
+  if (!valid_g(g)) return MX_ERR_UNSUPPORTED;
+  if (K % g != 0) return MX_ERR_SHAPE;
+  if (empty) return MX_OK;
+  if (!x || !H || !y_f32) return MX_ERR_NULL;
+  if (!aligned16(x) || !aligned16(y_f32)) return MX_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(H) & 1u) return MX_ERR_ALIGN;
+  return from_cuda(mxq::launch_rotate(MX_FMT_E2M1, mxq::kRotDebug, false, g,
+                                      rot_args(x, M, K, H, y_f32),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+mx_status mx_device_errors(int* flags) {
+  if (!flags) return MX_ERR_NULL;
+  unsigned int v = 0;
+  cudaError_t err = mxq::read_device_errors(&v);
+  *flags = (int)v;
+  return from_cuda(err);
+}
+
+}  // extern "C"

@@ -1,0 +1,54 @@
+// mx_launch.h -- host-side launch interface between the C ABI (mx_api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mxq {
+
+// Work is cut into tiles of 128 rows x 128 elements along K; a tile's 4x128 block scales form
+// exactly one 512-byte tile of the swizzled scale layout.
+constexpr int kTileRows = 128;
+constexpr int kTileCols = 128;
+
+struct StreamArgs {
+  const void* x;           // bf16 [M, K]
+  void* out;               // codes (quantize) or bf16 [M, K] (QDQ)
+  uint8_t* scales;         // quantize only
+  int64_t M;               // rows of x (all experts when grouped)
+  int64_t K;
+  int64_t col_tiles;       // ceil(K / 128)
+  int64_t row_blocks;      // 128-row blocks visited (grouped: padded-row bound / 128)
+  int64_t scale_cols;      // linear: K / 32; swizzled: col_tiles * 4
+  const int64_t* offsets;  // grouped only: device int64 [E + 1]
+  int E;
+};
+
+// fmt: 1 = E2M1, 2 = E4M3. qdq: write bf16 QDQ instead of codes + scales.
+cudaError_t launch_stream(int fmt, bool qdq, bool swizzled, bool grouped, const StreamArgs& a,
+                          cudaStream_t stream);
+
+enum RotOut { kRotCodes = 0, kRotQdq = 1, kRotDebug = 2 };
+
+struct RotArgs {
+  const void* x;      // bf16 [M, K]
+  const void* H;      // bf16 [g, g] row-major
+  void* out;          // codes, bf16 QDQ, or fp32 rotated values
+  uint8_t* scales;    // codes only
+  int64_t M;
+  int64_t K;
+  int64_t col_tiles;
+  int64_t row_blocks;
+  int64_t scale_cols;
+};
+
+cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const RotArgs& a,
+                          cudaStream_t stream);
+
+// Reads and clears the device error word of the current device (synchronizes).
+cudaError_t read_device_errors(unsigned int* flags);
+
+// Number of CTAs of `kernel` that fit on the current device at once (SMs x CTAs per SM).
+int resident_ctas(const void* kernel, int threads, size_t dyn_smem);
+
+}  // namespace mxq
