@@ -1,1 +1,203 @@
-"""OCP-MX block quantization (MXFP4 / MXFP8) for GB300."""
+"""OCP-MX block quantization (MXFP4 / MXFP8) on GB300: Python binding of libmxq.
+
+Every function here has the name of the C entry point it calls (include/mxq.h) and does
+argument marshalling only: it checks tensor device/dtype/shape, allocates outputs with torch
+when the caller passes none, and hands raw device pointers and the current CUDA stream to the
+library. All computation runs in the library's sm_103a kernels. If libmxq.so is missing the
+calls raise; there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+E2M1 = MXFP4 = 1
+E4M3 = MXFP8 = 2
+LINEAR = 0
+SWIZZLED = 1
+RNE = 0
+GROUP = 32
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmxq.so")
+_lib = None
+
+EXPORTS = (
+    "mx_status_string", "mx_scales_shape", "mx_grouped_scales_shape", "mx_quantize", "mx_qdq",
+    "mx_rotate_quantize", "mx_quantize_grouped", "mx_rotate_debug", "mx_device_errors",
+)
+
+
+class MXError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmxq (ctypes handle with argument types set)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is not built; run `python -m mx_microscaling_quantize_gb300._build` "
+            "(or __graft_entry__.build()) first")
+    L = ctypes.CDLL(LIB_PATH)
+    i32, i64, p = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
+    pi64 = ctypes.POINTER(ctypes.c_int64)
+    sigs = {
+        "mx_status_string": (ctypes.c_char_p, [i32]),
+        "mx_scales_shape": (i32, [i64, i64, i32, i32, pi64, pi64]),
+        "mx_grouped_scales_shape": (i32, [i64, i32, i64, i32, i32, pi64, pi64]),
+        "mx_quantize": (i32, [p, i64, i64, i32, i32, i32, i32, p, p, p]),
+        "mx_qdq": (i32, [p, i64, i64, i32, i32, i32, p, i32, p, p]),
+        "mx_rotate_quantize": (i32, [p, i64, i64, p, i32, i32, i32, i32, i32, p, p, p]),
+        "mx_quantize_grouped": (i32, [p, p, i32, i64, i64, i32, i32, i32, i32, p, p, p]),
+        "mx_rotate_debug": (i32, [p, i64, i64, p, i32, p, p]),
+        "mx_device_errors": (i32, [ctypes.POINTER(ctypes.c_int)]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def mx_status_string(status: int) -> str:
+    return lib().mx_status_string(status).decode()
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise MXError(status, mx_status_string(status))
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else stream
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _input(x: torch.Tensor, name: str = "x") -> tuple[int, int]:
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.bfloat16):
+        raise TypeError(f"{name} must be a CUDA bfloat16 tensor")
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D [M, K] tensor")
+    return x.shape[0], x.shape[1]
+
+
+def _rotation(H: torch.Tensor) -> int:
+    if not (isinstance(H, torch.Tensor) and H.is_cuda and H.dtype == torch.bfloat16):
+        raise TypeError("H must be a CUDA bfloat16 tensor")
+    if H.dim() != 2 or H.shape[0] != H.shape[1] or not H.is_contiguous():
+        raise ValueError("H must be a contiguous square [g, g] tensor")
+    return H.shape[0]
+
+
+def code_bytes_per_row(fmt: int, K: int) -> int:
+    return K if fmt == E4M3 else K // 2
+
+
+def _codes_out(codes, x, M, K, fmt):
+    if codes is None:
+        return torch.empty((M, code_bytes_per_row(fmt, K)), dtype=torch.uint8, device=x.device)
+    if codes.numel() * codes.element_size() != M * code_bytes_per_row(fmt, K):
+        raise ValueError("codes has the wrong size")
+    return codes
+
+
+def _scales_out(scales, x, rows, cols):
+    if scales is None:
+        return torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    if scales.numel() * scales.element_size() != rows * cols:
+        raise ValueError("scales has the wrong size")
+    return scales
+
+
+def mx_scales_shape(M: int, K: int, layout: int = LINEAR, group: int = GROUP) -> tuple[int, int]:
+    r, c = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().mx_scales_shape(M, K, group, layout, ctypes.byref(r), ctypes.byref(c)))
+    return r.value, c.value
+
+
+def mx_grouped_scales_shape(M_total: int, E: int, K: int, layout: int = SWIZZLED,
+                            group: int = GROUP) -> tuple[int, int]:
+    r, c = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().mx_grouped_scales_shape(M_total, E, K, group, layout, ctypes.byref(r),
+                                         ctypes.byref(c)))
+    return r.value, c.value
+
+
+def mx_quantize(x, fmt, layout=LINEAR, *, codes=None, scales=None, group=GROUP, rounding=RNE,
+                stream=None):
+    """Block quantize bf16 [M, K] -> (codes uint8, E8M0 scales uint8)."""
+    M, K = _input(x)
+    codes = _codes_out(codes, x, M, K, fmt)
+    scales = _scales_out(scales, x, *mx_scales_shape(M, K, layout, group))
+    _check(lib().mx_quantize(_ptr(x), M, K, fmt, group, layout, rounding, _ptr(codes),
+                             _ptr(scales), _stream_ptr(stream)))
+    return codes, scales
+
+
+def mx_qdq(x, fmt, H=None, *, y=None, group=GROUP, rounding=RNE, stream=None):
+    """Quantize-dequantize bf16 [M, K] -> bf16 [M, K]; with H, rotate each g-chunk first."""
+    M, K = _input(x)
+    g = _rotation(H) if H is not None else 0
+    if y is None:
+        y = torch.empty_like(x)
+    _check(lib().mx_qdq(_ptr(x), M, K, fmt, group, rounding, _ptr(H), g, _ptr(y),
+                        _stream_ptr(stream)))
+    return y
+
+
+def mx_rotate_quantize(x, H, fmt, layout=SWIZZLED, *, codes=None, scales=None, group=GROUP,
+                       rounding=RNE, stream=None):
+    """Rotate each g-chunk by H, then block quantize -> (codes, scales)."""
+    M, K = _input(x)
+    g = _rotation(H)
+    codes = _codes_out(codes, x, M, K, fmt)
+    scales = _scales_out(scales, x, *mx_scales_shape(M, K, layout, group))
+    _check(lib().mx_rotate_quantize(_ptr(x), M, K, _ptr(H), g, fmt, group, layout, rounding,
+                                    _ptr(codes), _ptr(scales), _stream_ptr(stream)))
+    return codes, scales
+
+
+def mx_quantize_grouped(x, row_offsets, fmt, layout=SWIZZLED, *, codes=None, scales=None,
+                        group=GROUP, rounding=RNE, stream=None):
+    """Per-expert block quantize; row_offsets: CUDA int64 [E + 1]."""
+    M, K = _input(x)
+    if not (row_offsets.is_cuda and row_offsets.dtype == torch.int64 and row_offsets.dim() == 1
+            and row_offsets.is_contiguous()):
+        raise TypeError("row_offsets must be a contiguous CUDA int64 [E + 1] tensor")
+    E = row_offsets.numel() - 1
+    codes = _codes_out(codes, x, M, K, fmt)
+    scales = _scales_out(scales, x, *mx_grouped_scales_shape(M, E, K, layout, group))
+    _check(lib().mx_quantize_grouped(_ptr(x), _ptr(row_offsets), E, M, K, fmt, group, layout,
+                                     rounding, _ptr(codes), _ptr(scales), _stream_ptr(stream)))
+    return codes, scales
+
+
+def mx_rotate_debug(x, H, *, y=None, stream=None):
+    """The fp32 rotated values the rotated kernels quantize (diagnostics)."""
+    M, K = _input(x)
+    g = _rotation(H)
+    if y is None:
+        y = torch.empty((M, K), dtype=torch.float32, device=x.device)
+    _check(lib().mx_rotate_debug(_ptr(x), M, K, _ptr(H), g, _ptr(y), _stream_ptr(stream)))
+    return y
+
+
+def mx_device_errors() -> int:
+    """Synchronize and return (then clear) the device error word."""
+    v = ctypes.c_int()
+    _check(lib().mx_device_errors(ctypes.byref(v)))
+    return v.value

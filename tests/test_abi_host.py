@@ -1,0 +1,149 @@
+"""Host-side checks of the C ABI: the library loads, exports what include/mxq.h declares, and
+rejects bad arguments before any launch. No call here reaches a kernel: every call either fails
+validation or is an empty call (M == 0 or K == 0), so fake pointers are never dereferenced."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import mx_microscaling_quantize_gb300 as mxq
+from mx_microscaling_quantize_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxq.h")
+
+OK, NULL, SHAPE, ALIGN, UNSUP = 0, 1, 2, 3, 4
+P = 1 << 20  # a 16-byte aligned fake device address, never dereferenced
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return mxq.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^(?:mx_status|const char\*)\s+(mx_\w+)\(", text, re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(mxq.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", mxq.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(L, name) is not None
+
+
+def test_macros_match_binding():
+    text = open(HEADER).read()
+    macros = dict(re.findall(r"#define (MX_\w+) (\d+)", text))
+    assert int(macros["MX_FMT_E2M1"]) == mxq.E2M1 and int(macros["MX_FMT_E4M3"]) == mxq.E4M3
+    assert int(macros["MX_SCALES_LINEAR"]) == mxq.LINEAR
+    assert int(macros["MX_SCALES_SWIZZLED"]) == mxq.SWIZZLED
+    assert int(macros["MX_ROUND_RNE"]) == mxq.RNE
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert mxq.mx_status_string(s).startswith("MX_")
+    assert "unknown" in mxq.mx_status_string(99)
+
+
+@pytest.mark.parametrize("M,K,layout,want", [
+    (1, 32, 0, (1, 1)), (1, 32, 1, (128, 4)), (128, 4096, 0, (128, 128)),
+    (129, 96, 1, (256, 4)), (300, 416, 1, (384, 16)), (0, 64, 1, (0, 4)),
+    (8192, 28672, 1, (8192, 896)),
+])
+def test_scales_shape(L, M, K, layout, want):
+    assert mxq.mx_scales_shape(M, K, layout) == want
+
+
+def test_grouped_scales_shape(L):
+    assert mxq.mx_grouped_scales_shape(16384, 128, 2048, mxq.SWIZZLED) == (32640, 64)
+    assert mxq.mx_grouped_scales_shape(16384, 128, 2048, mxq.LINEAR) == (16384, 64)
+    # the bound holds for every split of the rows: n_e = 1 for 127 experts, rest in one
+    counts = [1] * 127 + [16384 - 127]
+    need = sum(-(-c // 128) * 128 for c in counts)
+    assert need <= mxq.mx_grouped_scales_shape(16384, 128, 2048, mxq.SWIZZLED)[0]
+
+
+def shape_status(L, M, K, group=32, layout=0):
+    r, c = ctypes.c_int64(), ctypes.c_int64()
+    return L.mx_scales_shape(M, K, group, layout, ctypes.byref(r), ctypes.byref(c))
+
+
+def test_scales_shape_errors(L):
+    assert shape_status(L, -1, 32) == SHAPE
+    assert shape_status(L, 4, 48) == SHAPE
+    assert shape_status(L, 4, 64, group=16) == UNSUP
+    assert shape_status(L, 4, 64, layout=7) == UNSUP
+    assert L.mx_scales_shape(4, 64, 32, 0, None, None) == NULL
+
+
+def test_quantize_validation(L):
+    q = L.mx_quantize
+    assert q(P, -1, 64, 1, 32, 0, 0, P, P, None) == SHAPE
+    assert q(P, 4, 48, 1, 32, 0, 0, P, P, None) == SHAPE
+    assert q(P, 4, 64, 3, 32, 0, 0, P, P, None) == UNSUP
+    assert q(P, 4, 64, 1, 16, 0, 0, P, P, None) == UNSUP
+    assert q(P, 4, 64, 1, 32, 2, 0, P, P, None) == UNSUP
+    assert q(P, 4, 64, 1, 32, 0, 1, P, P, None) == UNSUP
+    assert q(None, 4, 64, 1, 32, 0, 0, P, P, None) == NULL
+    assert q(P, 4, 64, 1, 32, 0, 0, None, P, None) == NULL
+    assert q(P, 4, 64, 1, 32, 0, 0, P, None, None) == NULL
+    assert q(P + 8, 4, 64, 1, 32, 0, 0, P, P, None) == ALIGN
+    assert q(P, 4, 64, 1, 32, 0, 0, P + 4, P, None) == ALIGN
+    assert q(P, 4, 64, 1, 32, 1, 0, P, P + 1, None) == ALIGN
+    # empty calls launch nothing and succeed, even with NULL buffers
+    assert q(None, 0, 64, 1, 32, 0, 0, None, None, None) == OK
+    assert q(None, 5, 0, 2, 32, 1, 0, None, None, None) == OK
+    # absurd sizes are rejected, not overflowed
+    assert q(P, 1 << 40, 1 << 20, 1, 32, 0, 0, P, P, None) == SHAPE
+
+
+def test_qdq_and_rotation_validation(L):
+    assert L.mx_qdq(P, 4, 64, 1, 32, 0, P, 8, P, None) == UNSUP     # g = 8
+    assert L.mx_qdq(P, 4, 96, 1, 32, 0, P, 64, P, None) == SHAPE    # K % g
+    assert L.mx_qdq(P, 4, 64, 1, 32, 0, P + 1, 32, P, None) == ALIGN
+    assert L.mx_qdq(P, 4, 64, 1, 32, 0, None, 0, None, None) == NULL
+    assert L.mx_qdq(P, 4, 64, 1, 32, 0, None, 0, P + 2, None) == ALIGN
+    r = L.mx_rotate_quantize
+    assert r(P, 4, 64, P, 48, 1, 32, 1, 0, P, P, None) == UNSUP
+    assert r(P, 4, 192, P, 128, 1, 32, 1, 0, P, P, None) == SHAPE
+    assert r(P, 4, 64, None, 32, 1, 32, 1, 0, P, P, None) == NULL
+    assert r(P, 4, 64, P, 32, 1, 32, 1, 0, P, P + 8, None) == ALIGN
+    assert r(None, 0, 64, None, 32, 1, 32, 1, 0, None, None, None) == OK
+    d = L.mx_rotate_debug
+    assert d(P, 4, 64, P, 24, P, None) == UNSUP
+    assert d(P, 4, 64, None, 32, P, None) == NULL
+
+
+def test_grouped_validation(L):
+    g = L.mx_quantize_grouped
+    assert g(P, P, 0, 16, 64, 1, 32, 1, 0, P, P, None) == SHAPE       # E = 0
+    assert g(P, P, 1025, 16, 64, 1, 32, 1, 0, P, P, None) == SHAPE    # E > 1024
+    assert g(P, None, 4, 16, 64, 1, 32, 1, 0, P, P, None) == NULL
+    assert g(P, P + 4, 4, 16, 64, 1, 32, 1, 0, P, P, None) == ALIGN
+    assert g(P, P, 4, 16, 64, 1, 32, 1, 0, P, P + 8, None) == ALIGN
+    assert g(P, P, 4, 16, 48, 1, 32, 1, 0, P, P, None) == SHAPE
+    assert g(None, None, 4, 0, 64, 1, 32, 1, 0, None, None, None) == OK
+
+
+def test_device_errors_null(L):
+    assert L.mx_device_errors(None) == NULL
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(mxq, "_lib", None)
+    monkeypatch.setattr(mxq, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        mxq.lib()
