@@ -1,0 +1,456 @@
+"""Benchmark of the MX block quantize / QDQ hot path on GB300.
+
+Default workload (one step): MXFP4 (E2M1) QDQ, group 32, bf16 in / bf16 out, of the weight-like
+x[8192, 8192] (Student-t nu=4 * 0.02) and the activation-like x[4096, 8192] (N(0,1), 8 outlier
+columns * 100): two kernel launches, 402,653,184 algorithmic bytes (4 B per element). Inputs
+(192 MiB) and outputs (192 MiB) are larger than L2 (129 MB), so no flush runs between steps.
+
+Prints one JSON line: metric/value in algorithmic GB/s, a roofline object for the dominant
+kernel (CUDA-event launch times against the measured HBM copy bandwidth), the CPU oracle timed
+on the host cores (cpu_baseline), an end-to-end figure through the C ABI from pinned host
+buffers (e2e), SM clocks sampled during the timed region, and per-workload kernel figures for
+the other workloads (cold L2: a 256 MiB buffer is written between timed launches).
+
+--impl reference times the CPU oracle instead (bounded sample per step, all host cores).
+"""
+
+from __future__ import annotations
+
+import argparse
+import concurrent.futures
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MX quant/QDQ HBM GB/s and % of GB300 peak; Gelem/s vs CPU oracle"
+WORKLOAD = "mxfp4_qdq: E2M1 QDQ g32 of bf16 x[8192,8192] Student-t(4)*0.02 + x[4096,8192] N(0,1) w/ 8 outlier cols"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "mx_stream_qdq_e2m1_mxfp4_qdq_workload.md")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--quick", action="store_true",
+                   help="main timed loop only (no e2e, CPU baseline, extra workloads)")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; weak scaling, no data-path collective)
+# ---------------------------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------------------------
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("mx_stream.cu", "mx_device.cuh", "mx_launch.h"):
+        with open(os.path.join(ROOT, "mx_microscaling_quantize_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary, if the
+    kernel sources are unchanged since it was taken."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+).*?source_sha:\s*([0-9a-f]+)", text, re.S)
+    if not m or m.group(2) != kernel_source_hash():
+        return None
+    return int(m.group(1))
+
+
+def to_gpu(bits, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle timing (bounded samples)
+# ---------------------------------------------------------------------------------------------
+def oracle_qdq_rows(parts, threads):
+    """Run the oracle's QDQ on row chunks of each (bits) array with a thread pool."""
+    import oracle as O
+    jobs = []
+    for bits in parts:
+        step = max(1, bits.shape[0] // (threads * 4))
+        for r in range(0, bits.shape[0], step):
+            jobs.append(bits[r:r + step])
+    with concurrent.futures.ThreadPoolExecutor(threads) as pool:
+        list(pool.map(lambda b: O.qdq(b, O.E2M1), jobs))
+
+
+def cpu_sample(xw, xa, target_s=10.0):
+    """Rows of both tensors sized for about target_s seconds of oracle work on all cores."""
+    import oracle as O
+    threads = os.cpu_count() or 1
+    O.build()
+    probe = xw[:16]
+    t0 = time.perf_counter()
+    O.qdq(probe, O.E2M1)
+    per_elem = (time.perf_counter() - t0) / probe.size
+    elems = int(target_s * threads / per_elem)
+    frac = min(1.0, elems / (xw.size + xa.size))
+    rw = max(1, int(xw.shape[0] * frac))
+    ra = max(1, int(xa.shape[0] * frac))
+    return xw[:rw], xa[:ra], threads
+
+
+def time_oracle(sw, sa, threads):
+    t0 = time.perf_counter()
+    oracle_qdq_rows([sw, sa], threads)
+    dt = time.perf_counter() - t0
+    nbytes = 4 * (sw.size + sa.size)
+    return nbytes / dt / 1e9, dt
+
+
+# ---------------------------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    from mx_microscaling_quantize_gb300 import workloads as W
+    xw, xa = W.mxfp4_qdq_weight(), W.mxfp4_qdq_activation()
+    # bounded sample per step so that --steps K --warmup W ends within minutes
+    per_step_s = max(0.5, 120.0 / max(1, args.steps + args.warmup))
+    sw, sa, threads = cpu_sample(xw, xa, target_s=per_step_s)
+    for _ in range(args.warmup):
+        time_oracle(sw, sa, threads)
+    total = 0.0
+    for _ in range(args.steps):
+        total += time_oracle(sw, sa, threads)[1]
+    nbytes = 4 * (sw.size + sa.size)
+    value = nbytes * args.steps / total / 1e9
+    sample = (f"rows 0..{sw.shape[0]} of x[8192,8192] and 0..{sa.shape[0]} of x[4096,8192] "
+              f"({sw.size + sa.size} elements) per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": 8192,
+                   "parallelism": "none (CPU oracle)", "l2": "n/a"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gelem_per_s": value / 4,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------------
+def extra_workloads(dev, peak):
+    """Kernel-only figures of the other workloads: CUDA events around each launch, a 256 MiB
+    buffer written between launches so every launch starts with a cold L2."""
+    import torch
+    import mx_microscaling_quantize_gb300 as mxq
+    from mx_microscaling_quantize_gb300 import workloads as W
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+
+    def timed(fn, iters=10):
+        times = []
+        for i in range(iters + 2):
+            flush.fill_(i & 0xFF)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            e.synchronize()
+            if i >= 2:
+                times.append(s.elapsed_time(e) / 1e3)
+        return statistics.median(times)
+
+    def record(name, nbytes, elems, t, launches=1):
+        out[name] = {"GB/s": nbytes / t / 1e9, "frac_of_peak": nbytes / t / 1e9 / peak,
+                     "Gelem/s": elems / t / 1e9, "us": t * 1e6, "launches": launches}
+
+    # MXFP8 quantize, linear scales, x[128, 4096]
+    x = to_gpu(W.mxfp8_linear_quant(), dev)
+    c, s = mxq.mx_quantize(x, mxq.E4M3, mxq.LINEAR)
+    t = timed(lambda: mxq.mx_quantize(x, mxq.E4M3, mxq.LINEAR, codes=c, scales=s))
+    record("mxfp8_linear_quant[128,4096]", x.numel() * 3 + s.numel(), x.numel(), t)
+
+    # the two QDQ tensors separately, both formats
+    for name, bits in (("weight[8192,8192]", W.mxfp4_qdq_weight()),
+                       ("activation[4096,8192]", W.mxfp4_qdq_activation())):
+        x = to_gpu(bits, dev)
+        y = torch.empty_like(x)
+        for fmt, fname in ((mxq.E2M1, "mxfp4"), (mxq.E4M3, "mxfp8")):
+            t = timed(lambda: mxq.mx_qdq(x, fmt, y=y))
+            record(f"{fname}_qdq_{name}", 4 * x.numel(), x.numel(), t)
+        del x, y
+
+    # fused rotate + MXFP4 quantize, g = 32 Hadamard, swizzled scales
+    H = to_gpu(W.normalized_hadamard_bf16(32), dev)
+    for K in W.ROTATE_QUANT_K:
+        for M in W.ROTATE_QUANT_M:
+            x = to_gpu(W.rotate_quant_activation(M, K), dev)
+            c, s = mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED)
+            t = timed(lambda: mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, codes=c,
+                                                     scales=s))
+            record(f"rotate_quant_mxfp4_g32[{M},{K}]", 2 * x.numel() + c.numel() + s.numel(),
+                   x.numel(), t)
+            del x, c, s
+
+    # MoE MXFP8 grouped quantize, swizzled scales padded per expert
+    xb, off = W.moe_quant()
+    x = to_gpu(xb, dev)
+    offs = torch.from_numpy(off).to(dev)
+    c, s = mxq.mx_quantize_grouped(x, offs, mxq.E4M3, mxq.SWIZZLED)
+    used_rows = int(sum(-(-int(n) // 128) * 128 for n in np.diff(off)))
+    t = timed(lambda: mxq.mx_quantize_grouped(x, offs, mxq.E4M3, mxq.SWIZZLED, codes=c, scales=s))
+    record("moe_quant_mxfp8[16384,2048]x128", 3 * x.numel() + used_rows * s.shape[1], x.numel(), t)
+    del x, c, s
+
+    # rotation sweep: rotated QDQ, g in {16,32,64,128} x {MXFP4, MXFP8} on 3 layer inputs
+    for lname, M, K in W.ROTATION_SWEEP_LAYERS:
+        x = to_gpu(W.rotation_sweep_input(lname), dev)
+        y = torch.empty_like(x)
+        for g in W.ROTATION_SWEEP_G:
+            Hg = to_gpu(W.normalized_hadamard_bf16(g), dev)
+            for fmt, fname in ((mxq.E2M1, "mxfp4"), (mxq.E4M3, "mxfp8")):
+                t = timed(lambda: mxq.mx_qdq(x, fmt, Hg, y=y), iters=5)
+                record(f"rotated_qdq_{fname}_g{g}_{lname}[{M},{K}]", 4 * x.numel(), x.numel(), t)
+        del x, y
+    return out
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import mx_microscaling_quantize_gb300 as mxq
+    from mx_microscaling_quantize_gb300 import workloads as W
+
+    xw_b, xa_b = W.mxfp4_qdq_weight(), W.mxfp4_qdq_activation()
+    xw, xa = to_gpu(xw_b, dev), to_gpu(xa_b, dev)
+    yw, ya = torch.empty_like(xw), torch.empty_like(xa)
+    elems = xw.numel() + xa.numel()
+    step_bytes = 4 * elems  # bf16 in + bf16 out
+    stream = torch.cuda.current_stream()
+    peak, peak_src = hbm_peak()
+
+    def step():
+        mxq.mx_qdq(xw, mxq.E2M1, y=yw, stream=stream)
+        mxq.mx_qdq(xa, mxq.E2M1, y=ya, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_start.record(stream)
+        for i in range(K):
+            e = ev[i]
+            e[0].record(stream)
+            mxq.mx_qdq(xw, mxq.E2M1, y=yw, stream=stream)
+            e[1].record(stream)
+            e[2].record(stream)
+            mxq.mx_qdq(xa, mxq.E2M1, y=ya, stream=stream)
+            e[3].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world)
+    ms_per_step = ms_total / K
+    kern_s = sum(e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in ev) / 1e3
+    launches = 2 * K
+    value = step_bytes * world / (ms_per_step / 1e3) / 1e9
+    achieved = step_bytes * K / kern_s / 1e9  # algorithmic bytes / launch time, both launches
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "format": "E2M1 (MXFP4)", "group": 32,
+                   "elements_per_step": elems, "algorithmic_bytes_per_step": step_bytes,
+                   "global_batch": 1, "seq_len": 8192, "parallelism": f"replicas x{world}",
+                   "l2": "inputs+outputs 384 MiB per step > 129 MB L2; no flush"},
+        "gelem_per_s": elems * world / (ms_per_step / 1e3) / 1e9,
+        "gpu_launches": launches,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs (copy)",
+                     "kernel": "mx_stream_kernel<E2M1, QDQ>",
+                     "traffic": recorded_traffic(),
+                     "algorithmic_bytes_per_launch": {"weight": 4 * xw.numel(),
+                                                      "activation": 4 * xa.numel()}},
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.quick:
+        # end to end through the C ABI from pinned host buffers
+        hw = torch.from_numpy(xw_b.view(np.int16)).pin_memory()
+        ha = torch.from_numpy(xa_b.view(np.int16)).pin_memory()
+        ow = torch.empty_like(hw).pin_memory()
+        oa = torch.empty_like(ha).pin_memory()
+        E = min(K, 50)
+        for it in range(E + 3):
+            if it == 3:
+                torch.cuda.synchronize()
+                s0 = torch.cuda.Event(enable_timing=True)
+                s1 = torch.cuda.Event(enable_timing=True)
+                s0.record(stream)
+            xw.view(torch.int16).copy_(hw, non_blocking=True)
+            xa.view(torch.int16).copy_(ha, non_blocking=True)
+            step()
+            ow.copy_(yw.view(torch.int16), non_blocking=True)
+            oa.copy_(ya.view(torch.int16), non_blocking=True)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e2e_s = s0.elapsed_time(s1) / 1e3 / E
+        line["e2e"] = {"value": step_bytes / e2e_s / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": 2 * elems, "d2h_bytes_per_step": 2 * elems,
+                       "ms_per_step": e2e_s * 1e3}
+        line["workloads"] = extra_workloads(dev, peak)
+        sw, sa, threads = cpu_sample(xw_b, xa_b)
+        cpu_gbs, cpu_s = time_oracle(sw, sa, threads)
+        line["cpu_baseline"] = {
+            "value": cpu_gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {sw.shape[0]} rows of x[8192,8192] + first {sa.shape[0]} rows of "
+                      f"x[4096,8192], E2M1 QDQ, {cpu_s:.1f} s on {threads} threads",
+            "gelem_per_s": cpu_gbs / 4}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -48,7 +48,9 @@ cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const Rot
 // Reads and clears the device error word of the current device (synchronizes).
 cudaError_t read_device_errors(unsigned int* flags);
 
-// Number of CTAs of `kernel` that fit on the current device at once (SMs x CTAs per SM).
+// Number of CTAs of `kernel` that fit on the current device at once (SMs x CTAs per SM);
+// also raises the kernel's dynamic shared-memory limit when dyn_smem > 48 KiB. Cached per
+// (device, kernel, threads, dyn_smem).
 int resident_ctas(const void* kernel, int threads, size_t dyn_smem);
 
 }  // namespace mxq

@@ -244,7 +244,12 @@ __global__ void __launch_bounds__(kThreads) mx_rotate_kernel(RotArgs a) {
     }
     __syncwarp();
     if (t + gridDim.x < n_tiles) load_tile(t + gridDim.x);
-    if (!mbar_wait_bounded(mbar_u32, phase)) atomicOr(&g_device_errors, kErrWaitTimeout);
+    const bool timed_out = !mbar_wait_bounded(mbar_u32, phase);
+    // the give-up decision is taken by the whole CTA so that no thread skips a barrier
+    if (__syncthreads_or(timed_out)) {
+      if (tid == 0) atomicOr(&g_device_errors, kErrWaitTimeout);
+      break;
+    }
     phase ^= 1u;
     tc_fence_after();
 
@@ -335,8 +340,6 @@ cudaError_t launch_t(const RotArgs& a, cudaStream_t stream) {
   constexpr int smem = smem_request<G>();
   const int64_t n_tiles = a.row_blocks * a.col_tiles;
   if (n_tiles <= 0) return cudaSuccess;
-  cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err != cudaSuccess) return err;
   const int resident = resident_ctas(k, kThreads, smem);
   if (resident <= 0) return cudaErrorInvalidConfiguration;
   const int grid = (int)(n_tiles < resident ? n_tiles : resident);

@@ -9,6 +9,10 @@
 // vector. Swizzled scales of a tile are exactly one 512-byte tile of the 128x4 layout: they are
 // gathered in shared memory and written as 32 x 16-byte stores. Grouped (MoE) calls map each
 // 128-row block to its expert with a per-CTA prefix over the expert row counts.
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "mx_device.cuh"
 #include "mx_launch.h"
 
@@ -195,14 +199,30 @@ cudaError_t launch_stream(int fmt, bool qdq, bool swizzled, bool grouped, const 
 }
 
 int resident_ctas(const void* kernel, int threads, size_t dyn_smem) {
+  // (device, kernel, block shape) -> SMs x CTAs per SM, computed once per process
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, int, size_t>, int> cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const auto key = std::make_tuple(dev, kernel, threads, dyn_smem);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
   int sms = 0, per_sm = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dyn_smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem) !=
+          cudaSuccess) {
+    return 0;
+  }
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, dyn_smem) !=
       cudaSuccess) {
     return 0;
   }
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = sms * per_sm;
   return sms * per_sm;
 }
 

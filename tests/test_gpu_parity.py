@@ -1,0 +1,306 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the CPU oracle.
+
+Bar: bit-exact codes, E8M0 bytes and bf16 QDQ outputs on the non-rotated paths; the rotated
+paths follow the tolerance rules of mx_testlib (pre-quantization values within 1e-5 of the
+chunk norm, code differences only next to rounding midpoints, scale flips only next to powers
+of two). Inputs are the seeded synthetic workloads at sizes the oracle finishes in seconds
+(several tiles plus ragged tails), and the full workload sizes on sampled rows.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__
+import mx_microscaling_quantize_gb300 as mxq
+import oracle as O
+from mx_microscaling_quantize_gb300 import workloads as W
+import mx_testlib as T
+
+pytestmark = pytest.mark.gpu
+FMTS = [O.E2M1, O.E4M3]
+LAYOUTS = [O.LINEAR, O.SWIZZLED]
+GUARD = 4096
+CANARY = 0xA5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    __graft_entry__.build()
+    yield
+    assert mxq.mx_device_errors() == 0
+
+
+def quantize(xb, fmt, layout):
+    c, s = mxq.mx_quantize(T.to_gpu(xb), fmt, layout)
+    return T.u8(c), T.u8(s)
+
+
+def qdq(xb, fmt, H=None):
+    return T.bf16_bits(mxq.mx_qdq(T.to_gpu(xb), fmt, None if H is None else T.to_gpu(H)))
+
+
+def assert_quantize_exact(xb, fmt, layout):
+    c, s = quantize(xb, fmt, layout)
+    rc, rs = O.quantize(xb, fmt, layout)
+    np.testing.assert_array_equal(s, rs)
+    np.testing.assert_array_equal(c, rc)
+
+
+def guarded(nbytes):
+    """A uint8 device buffer with GUARD canary bytes on both sides; returns (full, inner)."""
+    full = torch.full((nbytes + 2 * GUARD,), CANARY, dtype=torch.uint8, device="cuda")
+    return full, full[GUARD:GUARD + nbytes]
+
+
+def assert_guards(full, nbytes):
+    f = full.cpu().numpy()
+    assert (f[:GUARD] == CANARY).all() and (f[GUARD + nbytes:] == CANARY).all()
+
+
+# ---------------------------------------------------------------------------------------------
+# converters, exhaustively
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("fmt", FMTS)
+def test_converter_sweep_bit_exact(fmt):
+    """Every finite bf16 value at its own scale and at every larger scale (s in [-127, 125]):
+    codes, scale bytes and QDQ outputs equal the oracle's."""
+    xs = T.converter_sweep()
+    assert_quantize_exact(xs, fmt, O.LINEAR)
+    np.testing.assert_array_equal(qdq(xs, fmt), O.qdq(xs, fmt))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_nan_and_inf_blocks(fmt):
+    v = np.random.default_rng(3).standard_normal((4, 256)).astype(np.float32)
+    v[0, 5], v[1, 40], v[2, 70], v[3, 255] = np.nan, np.inf, -np.inf, np.nan
+    xb = W.to_bf16_bits(v)
+    for layout in LAYOUTS:
+        assert_quantize_exact(xb, fmt, layout)
+    np.testing.assert_array_equal(qdq(xb, fmt), O.qdq(xb, fmt))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_signed_zero_and_subnormal_blocks(fmt):
+    v = np.zeros((2, 128), dtype=np.float32)
+    v[0, 1::2] = -0.0
+    v[1, :32] = -(2.0 ** -133)
+    v[1, 32:64] = np.float32(2.0 ** -130) * np.arange(32)
+    v[1, 64:] = -1e-38
+    xb = W.to_bf16_bits(v)
+    xb[0, 1::2] = 0x8000
+    assert_quantize_exact(xb, fmt, O.LINEAR)
+    np.testing.assert_array_equal(qdq(xb, fmt), O.qdq(xb, fmt))
+
+
+# ---------------------------------------------------------------------------------------------
+# non-rotated workloads
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("fmt", FMTS)
+def test_mxfp8_linear_quant_workload_full_size(fmt, layout):
+    """x[128, 4096] N(0,1) with 1% x50 outliers and an all-zero block per row."""
+    assert_quantize_exact(W.mxfp8_linear_quant(), fmt, layout)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_mxfp4_qdq_workload_small(fmt):
+    np.testing.assert_array_equal(qdq(W.mxfp4_qdq_weight(384, 8192), fmt),
+                                  O.qdq(W.mxfp4_qdq_weight(384, 8192), fmt))
+    xa = W.mxfp4_qdq_activation(300, 8192)
+    np.testing.assert_array_equal(qdq(xa, fmt), O.qdq(xa, fmt))
+
+
+@pytest.mark.parametrize("which", ["weight", "activation"])
+def test_mxfp4_qdq_workload_full_size_sampled_rows(which):
+    """The full tensors in the benchmark's launch: 40 sampled rows against the oracle, and
+    QDQ(QDQ(x)) == QDQ(x) over the whole output."""
+    xb = W.mxfp4_qdq_weight() if which == "weight" else W.mxfp4_qdq_activation()
+    xg = T.to_gpu(xb)
+    y = mxq.mx_qdq(xg, mxq.E2M1)
+    rows = np.sort(np.random.default_rng(11).choice(xb.shape[0], 40, replace=False))
+    yb = T.bf16_bits(y[torch.from_numpy(rows).cuda()])
+    np.testing.assert_array_equal(yb, O.qdq(xb[rows], O.E2M1))
+    assert torch.equal(mxq.mx_qdq(y, mxq.E2M1).view(torch.int16), y.view(torch.int16))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M", [1, 2, 127, 128, 129, 255])
+@pytest.mark.parametrize("K", [32, 64, 96, 160, 416])
+def test_edge_shapes_with_canaries(fmt, M, K):
+    xb = W.mxfp8_linear_quant(M, K, stream=M * 1000 + K)
+    x = T.to_gpu(xb)
+    for layout in LAYOUTS:
+        rows, cols = mxq.mx_scales_shape(M, K, layout)
+        cb = mxq.code_bytes_per_row(fmt, K) * M
+        cfull, codes = guarded(cb)
+        sfull, scales = guarded(rows * cols)
+        mxq.mx_quantize(x, fmt, layout, codes=codes, scales=scales)
+        rc, rs = O.quantize(xb, fmt, layout)
+        np.testing.assert_array_equal(T.u8(codes).reshape(rc.shape), rc)
+        np.testing.assert_array_equal(T.u8(scales).reshape(rs.shape), rs)
+        assert_guards(cfull, cb)
+        assert_guards(sfull, rows * cols)
+    yfull, ybytes = guarded(M * K * 2)
+    mxq.mx_qdq(x, fmt, y=ybytes.view(torch.bfloat16).view(M, K))
+    got = T.u8(ybytes).view(np.uint16).reshape(M, K)
+    np.testing.assert_array_equal(got, O.qdq(xb, fmt))
+    assert_guards(yfull, M * K * 2)
+
+
+def test_non_default_stream_and_repeat_calls():
+    xb = W.mxfp4_qdq_activation(256, 1024)
+    x = T.to_gpu(xb)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a = mxq.mx_qdq(x, mxq.E4M3)
+        c1, s1 = mxq.mx_quantize(x, mxq.E2M1, mxq.SWIZZLED)
+        c2, s2 = mxq.mx_quantize(x, mxq.E2M1, mxq.SWIZZLED)
+    s.synchronize()
+    np.testing.assert_array_equal(T.bf16_bits(a), O.qdq(xb, O.E4M3))
+    assert torch.equal(c1, c2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_qdq_idempotent_on_gpu(fmt):
+    x = T.to_gpu(W.rotation_sweep_input("attn_in", 512, 8192))
+    y = mxq.mx_qdq(x, fmt)
+    assert torch.equal(mxq.mx_qdq(y, fmt).view(torch.int16), y.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------------------------
+# grouped (MoE) quantize
+# ---------------------------------------------------------------------------------------------
+def grouped(xb, offsets, fmt, layout):
+    c, s = mxq.mx_quantize_grouped(T.to_gpu(xb), torch.from_numpy(offsets).cuda(), fmt, layout)
+    return T.u8(c), T.u8(s)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_moe_workload_full_size(layout):
+    """128 experts, Zipf(1.1) token counts summing to 16384, rows [n_e, 2048], MXFP8."""
+    xb, off = W.moe_quant()
+    c, s = grouped(xb, off, O.E4M3, layout)
+    rows = s.shape[0]
+    rc, rs = O.quantize_grouped(xb, off, O.E4M3, layout, scale_rows=rows)
+    np.testing.assert_array_equal(s, rs)
+    np.testing.assert_array_equal(c, rc)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("counts", [[0, 1, 127, 128, 129, 0, 300, 5],
+                                    [1000], [0, 0, 64], [128] * 6, [3] * 40])
+def test_grouped_edge_counts(fmt, counts):
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    xb = W.mxfp8_linear_quant(int(off[-1]), 160, stream=len(counts))
+    for layout in LAYOUTS:
+        c, s = grouped(xb, off, fmt, layout)
+        rc, rs = O.quantize_grouped(xb, off, fmt, layout, scale_rows=s.shape[0])
+        np.testing.assert_array_equal(s, rs)
+        np.testing.assert_array_equal(c, rc)
+
+
+def test_grouped_bad_offsets_stay_in_bounds():
+    """Offsets that break the contract (decreasing, beyond M) give unspecified values but no
+    access outside the buffers (canaries intact) and no error from the device."""
+    M, K, E = 200, 64, 4
+    off = np.array([0, 150, 20, 500, 200], dtype=np.int64)
+    x = T.to_gpu(W.mxfp8_linear_quant(M, K))
+    rows, cols = mxq.mx_grouped_scales_shape(M, E, K, mxq.SWIZZLED)
+    cfull, codes = guarded(M * K)
+    sfull, scales = guarded(rows * cols)
+    mxq.mx_quantize_grouped(x, torch.from_numpy(off).cuda(), mxq.E4M3, mxq.SWIZZLED, codes=codes,
+                            scales=scales)
+    torch.cuda.synchronize()
+    assert_guards(cfull, M * K)
+    assert_guards(sfull, rows * cols)
+
+
+# ---------------------------------------------------------------------------------------------
+# rotated path
+# ---------------------------------------------------------------------------------------------
+def rotation(g, kind="hadamard"):
+    if kind == "hadamard":
+        return W.normalized_hadamard_bf16(g)
+    if kind == "identity":
+        return W.to_bf16_bits(np.eye(g))
+    rng = np.random.default_rng(g)
+    return W.to_bf16_bits(rng.standard_normal((g, g)) / np.sqrt(g))
+
+
+@pytest.mark.parametrize("kind", ["hadamard", "random"])
+@pytest.mark.parametrize("g", [16, 32, 64, 128])
+def test_rotated_values_within_tolerance(g, kind):
+    xb = W.rotate_quant_activation(300, 1024)
+    H = rotation(g, kind)
+    y = mxq.mx_rotate_debug(T.to_gpu(xb), T.to_gpu(H)).cpu().numpy()
+    assert T.check_rotated_values(y, O.rotate(xb, H), g) <= 1.0
+
+
+@pytest.mark.parametrize("g", [16, 32, 64, 128])
+def test_identity_rotation_is_bit_exact(g):
+    """x * I is exact in fp32: the rotated kernels then equal the plain path bit for bit."""
+    xb = W.mxfp4_qdq_activation(200, 512)
+    H = T.to_gpu(rotation(g, "identity"))
+    x = T.to_gpu(xb)
+    for fmt in FMTS:
+        for layout in LAYOUTS:
+            c, s = mxq.mx_rotate_quantize(x, H, fmt, layout)
+            rc, rs = O.quantize(xb, fmt, layout)
+            np.testing.assert_array_equal(T.u8(s), rs)
+            np.testing.assert_array_equal(T.u8(c), rc)
+        np.testing.assert_array_equal(T.bf16_bits(mxq.mx_qdq(x, fmt, H)), O.qdq(xb, fmt))
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M,K", [(1, 8192), (16, 8192), (128, 1024), (300, 1024), (16, 28672)])
+def test_rotate_quantize_rules(fmt, layout, M, K):
+    """Fused rotate + quantize (g = 32 normalized Hadamard) on the activation workload."""
+    xb = W.rotate_quant_activation(M, K)
+    H = rotation(32)
+    c, s = mxq.mx_rotate_quantize(T.to_gpu(xb), T.to_gpu(H), fmt, layout)
+    c, s = T.u8(c), T.u8(s)
+    if layout == O.SWIZZLED:
+        assert not T.swizzle_pads(s, M, K).any()
+        s = T.unswizzle(s, M, K)
+    stats = T.check_rotated_codes(xb, H, fmt, c, s)
+    assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+
+
+@pytest.mark.parametrize("kind", ["hadamard", "random"])
+@pytest.mark.parametrize("g", [16, 32, 64, 128])
+@pytest.mark.parametrize("fmt", FMTS)
+def test_rotated_qdq_rules(fmt, g, kind):
+    """Rotated QDQ on the decoder-layer input recipe (Student-t nu=5)."""
+    xb = W.rotation_sweep_input("down_proj_in", 128, 2048)
+    H = rotation(g, kind)
+    out = qdq(xb, fmt, H)
+    stats = T.check_rotated_qdq(xb, H, fmt, out)
+    assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_rotate_quantize_full_size_sampled_rows(fmt):
+    """The largest activation of the rotate+quantize workload, x[8192, 28672], swizzled scales:
+    32 sampled rows through the rules."""
+    M, K = 8192, 28672
+    xb = W.rotate_quant_activation(M, K)
+    H = rotation(32)
+    c, s = mxq.mx_rotate_quantize(T.to_gpu(xb), T.to_gpu(H), fmt, mxq.SWIZZLED)
+    c, s = T.u8(c), T.unswizzle(T.u8(s), M, K)
+    rows = np.sort(np.random.default_rng(5).choice(M, 32, replace=False))
+    stats = T.check_rotated_codes(xb[rows], H, fmt, c[rows], s[rows])
+    assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+
+
+def test_rotation_sweep_full_size_sampled_rows():
+    """Rotated QDQ at the full down-projection input [4096, 28672], every g and format."""
+    xb = W.rotation_sweep_input("down_proj_in")
+    x = T.to_gpu(xb)
+    rows = np.sort(np.random.default_rng(9).choice(xb.shape[0], 8, replace=False))
+    for g in (16, 32, 64, 128):
+        H = rotation(g)
+        for fmt in FMTS:
+            out = T.bf16_bits(mxq.mx_qdq(x, fmt, T.to_gpu(H))[torch.from_numpy(rows).cuda()])
+            T.check_rotated_qdq(xb[rows], H, fmt, out)

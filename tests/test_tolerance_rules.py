@@ -1,0 +1,81 @@
+"""CPU checks of the rotated-path tolerance rules in mx_testlib: they accept the oracle's own
+results and the exemptions the rules allow, and reject codes or scales that are wrong."""
+
+import numpy as np
+import pytest
+
+import oracle as O
+from mx_microscaling_quantize_gb300 import workloads as W
+import mx_testlib as T
+
+
+def identity(g):
+    return W.to_bf16_bits(np.eye(g))
+
+
+@pytest.mark.parametrize("fmt", [O.E2M1, O.E4M3])
+def test_rules_accept_oracle_results(fmt):
+    x = W.rotate_quant_activation(4, 256)
+    H = W.normalized_hadamard_bf16(32)
+    c, s = O.rotate_quantize(x, H, fmt, O.LINEAR)
+    stats = T.check_rotated_codes(x, H, fmt, c, s)
+    assert stats["exempt_blocks"] == 0
+    assert T.check_rotated_qdq(x, H, fmt, O.rotate_qdq(x, H, fmt))["exempt_blocks"] == 0
+
+
+def test_rules_reject_a_wrong_code_away_from_midpoints():
+    x = W.rotate_quant_activation(4, 256)
+    H = W.normalized_hadamard_bf16(32)
+    c, s = O.rotate_quantize(x, H, O.E2M1, O.LINEAR)
+    y = O.rotate(x, H)
+    # pick an element whose scaled value is far from every midpoint and bump its code
+    t = y[0, :32] / 2.0 ** (int(s[0, 0]) - 127)
+    i = int(np.argmin(np.abs(np.abs(t) - 1.0)))  # |t| close to a grid point (1.0)
+    bad = c.copy()
+    nib = (bad[0, i // 2] >> (4 * (i % 2))) & 0xF
+    new = (nib & 0x8) | min((nib & 7) + 1, 7)
+    bad[0, i // 2] = (bad[0, i // 2] & (0xF0 if i % 2 == 0 else 0x0F)) | (new << (4 * (i % 2)))
+    with pytest.raises(AssertionError):
+        T.check_rotated_codes(x, H, O.E2M1, bad, s)
+    bad_s = s.copy()
+    bad_s[1, 3] += 1
+    with pytest.raises(AssertionError):
+        T.check_rotated_codes(x, H, O.E2M1, c, bad_s)
+    out = O.rotate_qdq(x, H, O.E2M1)
+    out[2, 40] ^= 0x0040
+    with pytest.raises(AssertionError):
+        T.check_rotated_qdq(x, H, O.E2M1, out)
+
+
+def test_rules_allow_midpoint_and_power_of_two_exemptions():
+    g = 32
+    v = np.zeros((1, 32))
+    v[0, 0] = 4.0     # amax exactly 2^2: E2M1 byte 127, a flip to 126 is allowed
+    v[0, 1] = 0.75    # exact midpoint of 0.5 and 1.0 at scale 1
+    x = W.to_bf16_bits(v)
+    H = identity(g)
+    c, s = O.rotate_quantize(x, H, O.E2M1, O.LINEAR)
+    alt = c.copy()
+    alt[0, 0] = (alt[0, 0] & 0x0F) | (0x1 << 4)  # element 1 -> 0.5 instead of 1.0
+    stats = T.check_rotated_codes(x, H, O.E2M1, alt, s)
+    assert stats["exempt_codes"] == 1
+    b, codes = O.quantize_block(O.E2M1, v[0], forced_byte=126)
+    packed = (codes[0::2] | (codes[1::2] << 4)).reshape(1, 16)
+    stats = T.check_rotated_codes(x, H, O.E2M1, packed, np.array([[126]], dtype=np.uint8))
+    assert stats["scale_flips"] == 1
+
+
+def test_unswizzle_inverts_oracle_layout():
+    x = W.mxfp8_linear_quant(200, 416)
+    _, lin = O.quantize(x, O.E4M3, O.LINEAR)
+    _, swz = O.quantize(x, O.E4M3, O.SWIZZLED)
+    np.testing.assert_array_equal(T.unswizzle(swz, 200, 416), lin)
+    assert not T.swizzle_pads(swz, 200, 416).any()
+
+
+def test_converter_sweep_covers_every_scale():
+    xs = T.converter_sweep()
+    _, s2 = O.quantize(xs[:400], O.E2M1, O.LINEAR)
+    assert xs.shape[1] == 2048 and xs.shape[0] > 4000
+    fin = T.finite_bf16()
+    assert np.isin(fin, xs).all()
