@@ -47,6 +47,9 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--quick", action="store_true",
                    help="main timed loop only (no e2e, CPU baseline, extra workloads)")
+    p.add_argument("--case", choices=sorted(CASES), default=None,
+                   help="run one other workload only (for profiler captures): warmup + steps "
+                        "launches, one JSON line with its kernel-only GB/s")
     return p.parse_args()
 
 
@@ -194,28 +197,22 @@ def oracle_qdq_rows(parts, threads):
         list(pool.map(lambda b: O.qdq(b, O.E2M1), jobs))
 
 
-def cpu_sample(xw, xa, target_s=10.0):
-    """Rows of both tensors sized for about target_s seconds of oracle work on all cores."""
+def time_oracle_for(xw, xa, min_seconds):
+    """Oracle QDQ of whole-row samples on all host cores, repeated until min_seconds elapsed
+    (at least once); returns (GB/s over algorithmic bytes, seconds, passes, threads)."""
     import oracle as O
-    threads = os.cpu_count() or 1
     O.build()
-    probe = xw[:16]
+    threads = os.cpu_count() or 1
     t0 = time.perf_counter()
-    O.qdq(probe, O.E2M1)
-    per_elem = (time.perf_counter() - t0) / probe.size
-    elems = int(target_s * threads / per_elem)
-    frac = min(1.0, elems / (xw.size + xa.size))
-    rw = max(1, int(xw.shape[0] * frac))
-    ra = max(1, int(xa.shape[0] * frac))
-    return xw[:rw], xa[:ra], threads
-
-
-def time_oracle(sw, sa, threads):
-    t0 = time.perf_counter()
-    oracle_qdq_rows([sw, sa], threads)
-    dt = time.perf_counter() - t0
-    nbytes = 4 * (sw.size + sa.size)
-    return nbytes / dt / 1e9, dt
+    passes = 0
+    while True:
+        oracle_qdq_rows([xw, xa], threads)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    nbytes = 4 * (xw.size + xa.size) * passes
+    return nbytes / dt / 1e9, dt, passes, threads
 
 
 # ---------------------------------------------------------------------------------------------
@@ -227,18 +224,17 @@ def run_reference(args):
         return
     from mx_microscaling_quantize_gb300 import workloads as W
     xw, xa = W.mxfp4_qdq_weight(), W.mxfp4_qdq_activation()
-    # bounded sample per step so that --steps K --warmup W ends within minutes
-    per_step_s = max(0.5, 120.0 / max(1, args.steps + args.warmup))
-    sw, sa, threads = cpu_sample(xw, xa, target_s=per_step_s)
+    # each step: one oracle pass over the whole workload on all host cores (about 0.3 s on
+    # 16 Grace cores), so that --steps K --warmup W ends within minutes
     for _ in range(args.warmup):
-        time_oracle(sw, sa, threads)
+        time_oracle_for(xw, xa, 0.0)
     total = 0.0
+    threads = os.cpu_count() or 1
     for _ in range(args.steps):
-        total += time_oracle(sw, sa, threads)[1]
-    nbytes = 4 * (sw.size + sa.size)
+        total += time_oracle_for(xw, xa, 0.0)[1]
+    nbytes = 4 * (xw.size + xa.size)
     value = nbytes * args.steps / total / 1e9
-    sample = (f"rows 0..{sw.shape[0]} of x[8192,8192] and 0..{sa.shape[0]} of x[4096,8192] "
-              f"({sw.size + sa.size} elements) per step")
+    sample = "the whole workload (both tensors) per step, row chunks over all host cores"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -333,6 +329,60 @@ def extra_workloads(dev, peak):
                 record(f"rotated_qdq_{fname}_g{g}_{lname}[{M},{K}]", 4 * x.numel(), x.numel(), t)
         del x, y
     return out
+
+
+CASES = {
+    "mxfp8_linear_quant": "E4M3 quantize, linear scales, x[128,4096]",
+    "rotate_quant": "E2M1 rotate(g=32 Hadamard)+quantize, swizzled, x[8192,8192]",
+    "rotated_qdq_g128": "E4M3 rotated QDQ g=128, x[4096,28672] Student-t(5)",
+    "moe_quant": "E4M3 grouped quantize, swizzled, 128 experts, x[16384,2048]",
+}
+
+
+def run_case(args):
+    """One workload, `warmup` untimed + `steps` timed launches back to back (no L2 flush)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    import __graft_entry__
+    __graft_entry__.build()
+    import mx_microscaling_quantize_gb300 as mxq
+    from mx_microscaling_quantize_gb300 import workloads as W
+    if args.case == "mxfp8_linear_quant":
+        x = to_gpu(W.mxfp8_linear_quant(), dev)
+        c, s = mxq.mx_quantize(x, mxq.E4M3, mxq.LINEAR)
+        fn = lambda: mxq.mx_quantize(x, mxq.E4M3, mxq.LINEAR, codes=c, scales=s)
+        nbytes = 3 * x.numel() + s.numel()
+    elif args.case == "rotate_quant":
+        x = to_gpu(W.rotate_quant_activation(8192, 8192), dev)
+        H = to_gpu(W.normalized_hadamard_bf16(32), dev)
+        c, s = mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED)
+        fn = lambda: mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, codes=c, scales=s)
+        nbytes = 2 * x.numel() + c.numel() + s.numel()
+    elif args.case == "rotated_qdq_g128":
+        x = to_gpu(W.rotation_sweep_input("down_proj_in"), dev)
+        H = to_gpu(W.normalized_hadamard_bf16(128), dev)
+        y = torch.empty_like(x)
+        fn = lambda: mxq.mx_qdq(x, mxq.E4M3, H, y=y)
+        nbytes = 4 * x.numel()
+    else:
+        xb, off = W.moe_quant()
+        x = to_gpu(xb, dev)
+        offs = torch.from_numpy(off).to(dev)
+        c, s = mxq.mx_quantize_grouped(x, offs, mxq.E4M3, mxq.SWIZZLED)
+        fn = lambda: mxq.mx_quantize_grouped(x, offs, mxq.E4M3, mxq.SWIZZLED, codes=c, scales=s)
+        nbytes = 3 * x.numel() + s.numel()
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    t = a.elapsed_time(b) / 1e3 / max(1, args.steps)
+    print(json.dumps({"case": args.case, "what": CASES[args.case], "us_per_launch": t * 1e6,
+                      "GB/s": nbytes / t / 1e9, "gpu_launches": args.steps}), flush=True)
 
 
 def run_ours(args):
@@ -430,12 +480,11 @@ def run_ours(args):
                        "h2d_bytes_per_step": 2 * elems, "d2h_bytes_per_step": 2 * elems,
                        "ms_per_step": e2e_s * 1e3}
         line["workloads"] = extra_workloads(dev, peak)
-        sw, sa, threads = cpu_sample(xw_b, xa_b)
-        cpu_gbs, cpu_s = time_oracle(sw, sa, threads)
+        cpu_gbs, cpu_s, passes, threads = time_oracle_for(xw_b, xa_b, 10.0)
         line["cpu_baseline"] = {
             "value": cpu_gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {sw.shape[0]} rows of x[8192,8192] + first {sa.shape[0]} rows of "
-                      f"x[4096,8192], E2M1 QDQ, {cpu_s:.1f} s on {threads} threads",
+            "sample": f"{passes} passes of the whole workload (E2M1 QDQ of x[8192,8192] and "
+                      f"x[4096,8192]) in {cpu_s:.1f} s, row chunks on {threads} threads",
             "gelem_per_s": cpu_gbs / 4}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -448,6 +497,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.case:
+        run_case(args)
     else:
         run_ours(args)
 
