@@ -48,9 +48,10 @@ cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const Rot
 // Reads and clears the device error word of the current device (synchronizes).
 cudaError_t read_device_errors(unsigned int* flags);
 
-// Number of CTAs of `kernel` that fit on the current device at once (SMs x CTAs per SM);
-// also raises the kernel's dynamic shared-memory limit when dyn_smem > 48 KiB. Cached per
-// (device, kernel, threads, dyn_smem).
-int resident_ctas(const void* kernel, int threads, size_t dyn_smem);
+// Number of CTAs of `kernel` that fit on the current device at once: SMs x CTAs per SM from
+// the kernel's registers and shared memory against the SM's limits, capped at max_per_sm when
+// positive. Also raises the kernel's dynamic shared-memory limit when dyn_smem > 48 KiB.
+// Cached per (device, kernel, threads, dyn_smem, max_per_sm).
+int resident_ctas(const void* kernel, int threads, size_t dyn_smem, int max_per_sm);
 
 }  // namespace mxq

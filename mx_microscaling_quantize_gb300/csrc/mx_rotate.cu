@@ -32,6 +32,7 @@ constexpr int kThreads = 128;
 constexpr int kALbo = kTileRows * 16 + 16;       // 2064
 constexpr int kASmem = (kTileCols / 8) * kALbo;  // 33024
 constexpr int kTmemCols = 128;
+constexpr int kMaxCtasPerSm = 512 / kTmemCols;  // TMEM columns per SM / columns per CTA
 constexpr uint32_t kErrWaitTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -340,7 +341,7 @@ cudaError_t launch_t(const RotArgs& a, cudaStream_t stream) {
   constexpr int smem = smem_request<G>();
   const int64_t n_tiles = a.row_blocks * a.col_tiles;
   if (n_tiles <= 0) return cudaSuccess;
-  const int resident = resident_ctas(k, kThreads, smem);
+  const int resident = resident_ctas(k, kThreads, smem, kMaxCtasPerSm);
   if (resident <= 0) return cudaErrorInvalidConfiguration;
   const int grid = (int)(n_tiles < resident ? n_tiles : resident);
   kern<<<grid, kThreads, smem, stream>>>(a);

@@ -9,6 +9,7 @@
 // vector. Swizzled scales of a tile are exactly one 512-byte tile of the 128x4 layout: they are
 // gathered in shared memory and written as 32 x 16-byte stores. Grouped (MoE) calls map each
 // 128-row block to its expert with a per-CTA prefix over the expert row counts.
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -174,7 +175,7 @@ cudaError_t launch_t(const StreamArgs& a, cudaStream_t stream) {
   const void* k = reinterpret_cast<const void*>(&mx_stream_kernel<FMT, QDQ, SWZ, GROUPED>);
   const int64_t n_tiles = a.row_blocks * a.col_tiles;
   if (n_tiles <= 0) return cudaSuccess;
-  const int resident = resident_ctas(k, kThreads, 0);
+  const int resident = resident_ctas(k, kThreads, 0, 0);
   if (resident <= 0) return cudaErrorInvalidConfiguration;
   const int grid = (int)(n_tiles < resident ? n_tiles : resident);
   mx_stream_kernel<FMT, QDQ, SWZ, GROUPED><<<grid, kThreads, 0, stream>>>(a);
@@ -198,29 +199,46 @@ cudaError_t launch_stream(int fmt, bool qdq, bool swizzled, bool grouped, const 
   return launch_fmt<kFmtE4M3>(qdq, swizzled, grouped, a, stream);
 }
 
-int resident_ctas(const void* kernel, int threads, size_t dyn_smem) {
-  // (device, kernel, block shape) -> SMs x CTAs per SM, computed once per process
+int resident_ctas(const void* kernel, int threads, size_t dyn_smem, int max_per_sm) {
+  // (device, kernel, block shape) -> SMs x CTAs per SM, computed once per process from the
+  // kernel's registers and shared memory against the SM's limits.
   static std::mutex mu;
-  static std::map<std::tuple<int, const void*, int, size_t>, int> cache;
+  static std::map<std::tuple<int, const void*, int, size_t, int>, int> cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  const auto key = std::make_tuple(dev, kernel, threads, dyn_smem);
+  const auto key = std::make_tuple(dev, kernel, threads, dyn_smem, max_per_sm);
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
-  int sms = 0, per_sm = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  int sms = 0, thr_sm = 0, regs_sm = 0, smem_sm = 0, smem_reserved = 0, blocks_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&blocks_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev) !=
+          cudaSuccess) {
+    return 0;
+  }
   if (dyn_smem > 48 * 1024 &&
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem) !=
           cudaSuccess) {
     return 0;
   }
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, dyn_smem) !=
-      cudaSuccess) {
-    return 0;
-  }
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return 0;
+  const int warps = (threads + 31) / 32;
+  const int regs_per_warp = ((fa.numRegs * 32 + 255) / 256) * 256;  // 256-register granules
+  int per_sm = blocks_sm;
+  per_sm = std::min(per_sm, thr_sm / (warps * 32));
+  if (regs_per_warp > 0) per_sm = std::min(per_sm, regs_sm / (regs_per_warp * warps));
+  const size_t smem_block = fa.sharedSizeBytes + dyn_smem + (size_t)smem_reserved;
+  per_sm = std::min(per_sm, (int)((size_t)smem_sm / smem_block));
+  if (max_per_sm > 0) per_sm = std::min(per_sm, max_per_sm);
   std::lock_guard<std::mutex> lock(mu);
   cache[key] = sms * per_sm;
   return sms * per_sm;
