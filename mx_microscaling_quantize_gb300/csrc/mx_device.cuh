@@ -3,13 +3,15 @@
 // Block scale: for a block with abs-max amax (fp32 bits, sign cleared) the E8M0 byte is
 // max(E - emax, 0) where E is amax's biased exponent: that is floor(log2 amax) - emax + 127
 // clamped below at 0 (s = -127), and 0 for an all-zero block. E = 255 (Inf/NaN) gives 0xFF.
-// Element codes come from the hardware's paired converters (round to nearest even, saturate
-// to the largest finite value); the sign bit is OR-ed in from the input so that values that
-// round to zero keep their sign.
+// Element codes come from the hardware's paired converters cvt.rn.satfinite.{e2m1x2,e4m3x2}:
+// round to nearest even, saturate to the largest finite value, and keep the sign of values
+// that round to zero (a property the exhaustive parity sweep checks against the oracle). The
+// first source of a paired conversion lands in the upper nibble / byte / half, so the higher K
+// index is passed first. Multiplying by 2^-s is exact (no overflow; an underflow only touches
+// values far below half the smallest code).
 #pragma once
 
 #include <cstdint>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace mxq {
@@ -49,146 +51,122 @@ __device__ __forceinline__ float scale_of(uint32_t byte) {
   return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
 }
 
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
 // ------------------------------------------------------------------------------------------
-// element conversions (lo = lower K index = low nibble / low byte / low half)
+// building blocks
 // ------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
-      : "=r"(r)
-      : "f"(hi), "f"(lo));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-__device__ __forceinline__ float half_bits_to_f32(uint32_t h) {
-  return __half2float(__ushort_as_half((unsigned short)h));
-}
-
-// one byte of two E2M1 codes -> two fp32 values (exact)
-__device__ __forceinline__ void e2m1x2_to_f32(uint32_t byte, float& lo, float& hi) {
-  uint32_t h2;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(h2)
-      : "r"(byte));
-  lo = half_bits_to_f32(h2 & 0xFFFFu);
-  hi = half_bits_to_f32(h2 >> 16);
-}
-
-// two E4M3 codes (low byte first) -> two fp32 values (exact)
-__device__ __forceinline__ void e4m3x2_to_f32(uint32_t pair, float& lo, float& hi) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)pair));
-  lo = half_bits_to_f32(h2 & 0xFFFFu);
-  hi = half_bits_to_f32(h2 >> 16);
-}
-
-// two fp32 -> packed bf16x2 (round to nearest even, subnormals kept)
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Sign bits of a bf16 pair placed where an E2M1 code byte / an E4M3 code pair keeps them.
-__device__ __forceinline__ uint32_t e2m1_signs_of_bf16x2(uint32_t w) {
-  return ((w >> 12) & 0x8u) | ((w >> 24) & 0x80u);
+// (lo, hi) *= s with one packed fp32 multiply (exact here: s is a power of two)
+__device__ __forceinline__ void mul2(float& lo, float& hi, float s) {
+  asm("{\n\t.reg .b64 p, q;\n\tmov.b64 p, {%0, %1};\n\tmov.b64 q, {%2, %2};\n\t"
+      "mul.rn.f32x2 p, p, q;\n\tmov.b64 {%0, %1}, p;\n\t}"
+      : "+f"(lo), "+f"(hi)
+      : "f"(s));
 }
-__device__ __forceinline__ uint32_t e4m3_signs_of_bf16x2(uint32_t w) {
-  return ((w >> 8) & 0x80u) | ((w >> 16) & 0x8000u);
+
+// abs-max of the 8 bf16 of a 16-byte vector as sign-free bf16 bits; NaN propagates (0x7FFF
+// sorts above every other pattern, Inf 0x7F80 above every finite one).
+__device__ __forceinline__ uint32_t absmax_bf16x8(const uint4& v) {
+  uint32_t a, b, m;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x), "r"(v.y));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z), "r"(v.w));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+  return max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
 }
-__device__ __forceinline__ uint32_t e2m1_signs_of_f32x2(float lo, float hi) {
-  return ((__float_as_uint(lo) >> 28) & 0x8u) | ((__float_as_uint(hi) >> 24) & 0x80u);
-}
-__device__ __forceinline__ uint32_t e4m3_signs_of_f32x2(float lo, float hi) {
-  return ((__float_as_uint(lo) >> 24) & 0x80u) | ((__float_as_uint(hi) >> 16) & 0x8000u);
+
+// abs-max of 32 fp32 values as sign-free fp32 bits; NaN propagates.
+__device__ __forceinline__ uint32_t absmax_f32x32(const float* y) {
+  float m[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(m[i]) : "f"(y[2 * i]), "f"(y[2 * i + 1]));
+  }
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(m[i]) : "f"(m[i]), "f"(m[i + w]));
+    }
+  }
+  return __float_as_uint(m[0]) & 0x7FFFFFFFu;
 }
 
 // ------------------------------------------------------------------------------------------
-// 8 bf16 elements (one 16-byte vector) -> codes / QDQ, given the block's scale.
+// 8 scaled fp32 values t[0..8) (lower K index first) -> codes
 // ------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t quant8_e2m1_bf16(const uint4& v, float inv) {
+__device__ __forceinline__ uint32_t codes8_e2m1(const float* t) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, %8, %7;\n\t"
+      "mov.b32 %0, {c0, c1, c2, c3};\n\t}"
+      : "=r"(r)
+      : "f"(t[0]), "f"(t[1]), "f"(t[2]), "f"(t[3]), "f"(t[4]), "f"(t[5]), "f"(t[6]), "f"(t[7]));
+  return r;
+}
+
+__device__ __forceinline__ uint2 codes8_e4m3(const float* t) {
+  uint32_t a, b;
+  asm("{\n\t.reg .b16 c0, c1, c2, c3;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 c0, %3, %2;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 c1, %5, %4;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 c2, %7, %6;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 c3, %9, %8;\n\t"
+      "mov.b32 %0, {c0, c1};\n\tmov.b32 %1, {c2, c3};\n\t}"
+      : "=r"(a), "=r"(b)
+      : "f"(t[0]), "f"(t[1]), "f"(t[2]), "f"(t[3]), "f"(t[4]), "f"(t[5]), "f"(t[6]), "f"(t[7]));
+  return make_uint2(a, b);
+}
+
+// ------------------------------------------------------------------------------------------
+// QDQ of two scaled values (lo = lower K index): round to the grid with the hardware
+// converter, decode exactly to f16x2, widen, multiply by the scale, round once to bf16x2.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t qdq2_e2m1(float tlo, float thi, float sc) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 c;\n\t.reg .b16 a, b;\n\t.reg .b32 h;\n\t.reg .f32 f0, f1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c, %2, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h, c;\n\t"
+      "mov.b32 {a, b}, h;\n\t"
+      "cvt.f32.f16 f0, a;\n\tcvt.f32.f16 f1, b;\n\t"
+      "mul.rn.f32 f0, f0, %3;\n\tmul.rn.f32 f1, f1, %3;\n\t"
+      "cvt.rn.bf16x2.f32 %0, f1, f0;\n\t}"
+      : "=r"(r)
+      : "f"(tlo), "f"(thi), "f"(sc));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t qdq2_e4m3(float tlo, float thi, float sc) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 c, a, b;\n\t.reg .b32 h;\n\t.reg .f32 f0, f1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 c, %2, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h, c;\n\t"
+      "mov.b32 {a, b}, h;\n\t"
+      "cvt.f32.f16 f0, a;\n\tcvt.f32.f16 f1, b;\n\t"
+      "mul.rn.f32 f0, f0, %3;\n\tmul.rn.f32 f1, f1, %3;\n\t"
+      "cvt.rn.bf16x2.f32 %0, f1, f0;\n\t}"
+      : "=r"(r)
+      : "f"(tlo), "f"(thi), "f"(sc));
+  return r;
+}
+
+template <int FMT>
+__device__ __forceinline__ uint32_t qdq2(float tlo, float thi, float sc) {
+  return FMT == kFmtE2M1 ? qdq2_e2m1(tlo, thi, sc) : qdq2_e4m3(tlo, thi, sc);
+}
+
+// 16-byte bf16 vector -> 8 fp32 values times `inv` (= 2^-s)
+__device__ __forceinline__ void scaled8_bf16(const uint4& v, float inv, float* t) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t out = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t b = cvt_e2m1x2(bf16_lo(w[i]) * inv, bf16_hi(w[i]) * inv) | e2m1_signs_of_bf16x2(w[i]);
-    out |= b << (8 * i);
+    t[2 * i] = bf16_lo(w[i]);
+    t[2 * i + 1] = bf16_hi(w[i]);
+    mul2(t[2 * i], t[2 * i + 1], inv);
   }
-  return out;
-}
-
-__device__ __forceinline__ uint2 quant8_e4m3_bf16(const uint4& v, float inv) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t p[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    p[i] = cvt_e4m3x2(bf16_lo(w[i]) * inv, bf16_hi(w[i]) * inv) | e4m3_signs_of_bf16x2(w[i]);
-  }
-  return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
-}
-
-// dequantize 8 E2M1 codes (4 bytes) under scale `sc` -> 8 bf16
-__device__ __forceinline__ uint4 dequant8_e2m1(uint32_t codes, float sc) {
-  uint32_t o[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float lo, hi;
-    e2m1x2_to_f32((codes >> (8 * i)) & 0xFFu, lo, hi);
-    o[i] = pack_bf16x2(lo * sc, hi * sc);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-// dequantize 8 E4M3 codes (8 bytes) under scale `sc` -> 8 bf16
-__device__ __forceinline__ uint4 dequant8_e4m3(uint2 codes, float sc) {
-  const uint32_t c[4] = {codes.x & 0xFFFFu, codes.x >> 16, codes.y & 0xFFFFu, codes.y >> 16};
-  uint32_t o[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float lo, hi;
-    e4m3x2_to_f32(c[i], lo, hi);
-    o[i] = pack_bf16x2(lo * sc, hi * sc);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-// ------------------------------------------------------------------------------------------
-// 8 fp32 elements -> codes (rotated path)
-// ------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t quant8_e2m1_f32(const float* y, float inv) {
-  uint32_t out = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = y[2 * i], hi = y[2 * i + 1];
-    uint32_t b = cvt_e2m1x2(lo * inv, hi * inv) | e2m1_signs_of_f32x2(lo, hi);
-    out |= b << (8 * i);
-  }
-  return out;
-}
-
-__device__ __forceinline__ uint2 quant8_e4m3_f32(const float* y, float inv) {
-  uint32_t p[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = y[2 * i], hi = y[2 * i + 1];
-    p[i] = cvt_e4m3x2(lo * inv, hi * inv) | e4m3_signs_of_f32x2(lo, hi);
-  }
-  return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }
 
 constexpr uint32_t kE4M3NaNx4 = 0x7F7F7F7Fu;

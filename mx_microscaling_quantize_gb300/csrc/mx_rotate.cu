@@ -274,19 +274,24 @@ __global__ void __launch_bounds__(kThreads) mx_rotate_kernel(RotArgs a) {
         }
         continue;
       }
-      uint32_t m = 0;
+      const uint32_t byte = scale_byte_from_amax_bits<FMT>(absmax_f32x32(y));
+      const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);  // a NaN / Inf block
+      {
+        const float inv = inv_scale_of(byte);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) m = max(m, __float_as_uint(y[i]) & 0x7FFFFFFFu);
-      const uint32_t byte = scale_byte_from_amax_bits<FMT>(m);
-      const float inv = inv_scale_of(byte);
+        for (int i = 0; i < 16; ++i) mul2(y[2 * i], y[2 * i + 1], inv);  // y <- y / 2^s
+      }
       if (OUT == kRotQdq) {
         const float sc = scale_of(byte);
         uint4 o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          if (FMT == kFmtE2M1) o[i] = dequant8_e2m1(quant8_e2m1_f32(y + 8 * i, inv), sc);
-          else o[i] = dequant8_e4m3(quant8_e4m3_f32(y + 8 * i, inv), sc);
-          if (byte == 255u) o[i] = make_uint4(kBf16NaNx2, kBf16NaNx2, kBf16NaNx2, kBf16NaNx2);
+          const float* t = y + 8 * i;
+          o[i] = make_uint4(qdq2<FMT>(t[0], t[1], sc), qdq2<FMT>(t[2], t[3], sc),
+                            qdq2<FMT>(t[4], t[5], sc), qdq2<FMT>(t[6], t[7], sc));
+          if (special && byte == 255u) {
+            o[i] = make_uint4(kBf16NaNx2, kBf16NaNx2, kBf16NaNx2, kBf16NaNx2);
+          }
         }
         if (row_ok) {
           uint4* dst = static_cast<uint4*>(a.out) + (e0 >> 3);
@@ -295,9 +300,9 @@ __global__ void __launch_bounds__(kThreads) mx_rotate_kernel(RotArgs a) {
         }
       } else {
         if (FMT == kFmtE2M1) {
-          uint4 c = make_uint4(quant8_e2m1_f32(y, inv), quant8_e2m1_f32(y + 8, inv),
-                               quant8_e2m1_f32(y + 16, inv), quant8_e2m1_f32(y + 24, inv));
-          if (byte == 255u) c = make_uint4(0u, 0u, 0u, 0u);
+          uint4 c = make_uint4(codes8_e2m1(y), codes8_e2m1(y + 8), codes8_e2m1(y + 16),
+                               codes8_e2m1(y + 24));
+          if (special && byte == 255u) c = make_uint4(0u, 0u, 0u, 0u);
           if (row_ok) {
             __stcs(reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + (e0 >> 1)), c);
           }
@@ -305,8 +310,8 @@ __global__ void __launch_bounds__(kThreads) mx_rotate_kernel(RotArgs a) {
           uint2 c[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            c[i] = quant8_e4m3_f32(y + 8 * i, inv);
-            if (byte == 255u) c[i] = make_uint2(kE4M3NaNx4, kE4M3NaNx4);
+            c[i] = codes8_e4m3(y + 8 * i);
+            if (special && byte == 255u) c[i] = make_uint2(kE4M3NaNx4, kE4M3NaNx4);
           }
           if (row_ok) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + e0);

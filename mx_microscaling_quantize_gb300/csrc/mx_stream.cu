@@ -3,7 +3,7 @@
 // One persistent grid walks tiles of 128 rows x 128 elements. A CTA of 256 threads reads a
 // tile as 2048 coalesced 16-byte vectors (a warp instruction covers 2 rows x 256 bytes, all
 // eight loads of a thread are in flight together), finds each 32-element block's abs-max with
-// a packed u16x2 max over the bf16 bit patterns plus two shuffles across the block's 4 lanes,
+// packed bf16x2 abs-max instructions plus two shuffles across the block's 4 lanes,
 // derives the E8M0 byte from the exponent field, converts in registers with the hardware
 // paired converters and writes codes (or the dequantized bf16) with one coalesced store per
 // vector. Swizzled scales of a tile are exactly one 512-byte tile of the 128x4 layout: they are
@@ -123,32 +123,29 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
 #pragma unroll
     for (int i = 0; i < kVecs; ++i) {
       const int r = i * 16 + rsub;
-      uint32_t m = max_u16x2(max_u16x2(v[i].x & 0x7FFF7FFFu, v[i].y & 0x7FFF7FFFu),
-                             max_u16x2(v[i].z & 0x7FFF7FFFu, v[i].w & 0x7FFF7FFFu));
-      m = max(m & 0xFFFFu, m >> 16);
+      uint32_t m = absmax_bf16x8(v[i]);
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
       const uint32_t byte = scale_byte_from_amax_bits<FMT>(m << 16);
       const bool ok = col_ok && r < rows_valid;
       const int64_t e0 = (row0 + r) * a.K + col;  // first element of this vector
-      const float inv = inv_scale_of(byte);
+      float t[8];
+      scaled8_bf16(v[i], inv_scale_of(byte), t);
+      const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);  // a NaN / Inf block
       if (QDQ) {
-        uint4 o;
-        if (byte == 255u) {
-          o = make_uint4(kBf16NaNx2, kBf16NaNx2, kBf16NaNx2, kBf16NaNx2);
-        } else if (FMT == kFmtE2M1) {
-          o = dequant8_e2m1(quant8_e2m1_bf16(v[i], inv), scale_of(byte));
-        } else {
-          o = dequant8_e4m3(quant8_e4m3_bf16(v[i], inv), scale_of(byte));
-        }
+        const float sc = scale_of(byte);
+        uint4 o = make_uint4(qdq2<FMT>(t[0], t[1], sc), qdq2<FMT>(t[2], t[3], sc),
+                             qdq2<FMT>(t[4], t[5], sc), qdq2<FMT>(t[6], t[7], sc));
+        if (special && byte == 255u) o = make_uint4(kBf16NaNx2, kBf16NaNx2, kBf16NaNx2, kBf16NaNx2);
         if (ok) __stcs(static_cast<uint4*>(a.out) + (e0 >> 3), o);
       } else {
         if (FMT == kFmtE2M1) {
-          const uint32_t c = byte == 255u ? 0u : quant8_e2m1_bf16(v[i], inv);
+          uint32_t c = codes8_e2m1(t);
+          if (special && byte == 255u) c = 0u;
           if (ok) __stcs(static_cast<unsigned int*>(a.out) + (e0 >> 3), c);
         } else {
-          uint2 c = quant8_e4m3_bf16(v[i], inv);
-          if (byte == 255u) c = make_uint2(kE4M3NaNx4, kE4M3NaNx4);
+          uint2 c = codes8_e4m3(t);
+          if (special && byte == 255u) c = make_uint2(kE4M3NaNx4, kE4M3NaNx4);
           if (ok) __stcs(static_cast<uint2*>(a.out) + (e0 >> 3), c);
         }
         if ((vec & 3) == 0) {
