@@ -8,6 +8,8 @@
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// x, y and codes are moved with 32-byte vector accesses
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool valid_fmt(int fmt) { return fmt == MX_FMT_E2M1 || fmt == MX_FMT_E4M3; }
 bool valid_layout(int layout) { return layout == MX_SCALES_LINEAR || layout == MX_SCALES_SWIZZLED; }
@@ -61,7 +63,7 @@ const char* mx_status_string(mx_status status) {
     case MX_OK: return "MX_OK";
     case MX_ERR_NULL: return "MX_ERR_NULL: a required pointer is NULL";
     case MX_ERR_SHAPE: return "MX_ERR_SHAPE: invalid size (negative, K % 32, K % g, experts)";
-    case MX_ERR_ALIGN: return "MX_ERR_ALIGN: a buffer is not 16-byte aligned";
+    case MX_ERR_ALIGN: return "MX_ERR_ALIGN: a buffer is misaligned (x, y, codes: 32 B; scales: 16 B)";
     case MX_ERR_UNSUPPORTED: return "MX_ERR_UNSUPPORTED: format, layout, rounding, group or g";
     case MX_ERR_CUDA: return "MX_ERR_CUDA: the CUDA runtime reported an error at launch";
     default: return "unknown mx_status";
@@ -106,7 +108,7 @@ mx_status mx_quantize(const void* x, int64_t M, int64_t K, int fmt, int group, i
   if (!valid_layout(layout)) return MX_ERR_UNSUPPORTED;
   if (empty) return MX_OK;
   if (!x || !codes || !scales) return MX_ERR_NULL;
-  if (!aligned16(x) || !aligned16(codes)) return MX_ERR_ALIGN;
+  if (!aligned32(x) || !aligned32(codes)) return MX_ERR_ALIGN;
   if (layout == MX_SCALES_SWIZZLED && !aligned16(scales)) return MX_ERR_ALIGN;
   mxq::StreamArgs a = stream_args(x, M, K, codes);
   a.scales = static_cast<uint8_t*>(scales);
@@ -126,7 +128,7 @@ mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int ro
   }
   if (empty) return MX_OK;
   if (!x || !y) return MX_ERR_NULL;
-  if (!aligned16(x) || !aligned16(y)) return MX_ERR_ALIGN;
+  if (!aligned32(x) || !aligned32(y)) return MX_ERR_ALIGN;
   if (H) {
     if (reinterpret_cast<uintptr_t>(H) & 1u) return MX_ERR_ALIGN;
     return from_cuda(mxq::launch_rotate(fmt, mxq::kRotQdq, false, g, rot_args(x, M, K, H, y),
@@ -146,7 +148,7 @@ mx_status mx_rotate_quantize(const void* x, int64_t M, int64_t K, const void* H,
   if (K % g != 0) return MX_ERR_SHAPE;
   if (empty) return MX_OK;
   if (!x || !H || !codes || !scales) return MX_ERR_NULL;
-  if (!aligned16(x) || !aligned16(codes)) return MX_ERR_ALIGN;
+  if (!aligned32(x) || !aligned32(codes)) return MX_ERR_ALIGN;
   if (layout == MX_SCALES_SWIZZLED && !aligned16(scales)) return MX_ERR_ALIGN;
   if (reinterpret_cast<uintptr_t>(H) & 1u) return MX_ERR_ALIGN;
   mxq::RotArgs a = rot_args(x, M, K, H, codes);
@@ -170,7 +172,7 @@ mx_status mx_quantize_grouped(const void* x, const int64_t* row_offsets, int E, 
   if (empty) return MX_OK;
   if (!row_offsets || !x || !codes || !scales) return MX_ERR_NULL;
   if (reinterpret_cast<uintptr_t>(row_offsets) & 7u) return MX_ERR_ALIGN;
-  if (!aligned16(x) || !aligned16(codes)) return MX_ERR_ALIGN;
+  if (!aligned32(x) || !aligned32(codes)) return MX_ERR_ALIGN;
   if (layout == MX_SCALES_SWIZZLED && !aligned16(scales)) return MX_ERR_ALIGN;
   mxq::StreamArgs a = stream_args(x, M_total, K, codes);
   a.scales = static_cast<uint8_t*>(scales);
@@ -193,7 +195,7 @@ mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, in
   if (K % g != 0) return MX_ERR_SHAPE;
   if (empty) return MX_OK;
   if (!x || !H || !y_f32) return MX_ERR_NULL;
-  if (!aligned16(x) || !aligned16(y_f32)) return MX_ERR_ALIGN;
+  if (!aligned32(x) || !aligned32(y_f32)) return MX_ERR_ALIGN;
   if (reinterpret_cast<uintptr_t>(H) & 1u) return MX_ERR_ALIGN;
   return from_cuda(mxq::launch_rotate(MX_FMT_E2M1, mxq::kRotDebug, false, g,
                                       rot_args(x, M, K, H, y_f32),

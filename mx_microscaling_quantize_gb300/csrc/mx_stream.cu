@@ -1,14 +1,15 @@
 // mx_stream.cu -- block quantize / QDQ without rotation (HBM-bound streaming kernels).
 //
-// One persistent grid walks tiles of 128 rows x 128 elements. A CTA of 256 threads reads a
-// tile as 2048 coalesced 16-byte vectors (a warp instruction covers 2 rows x 256 bytes, all
-// eight loads of a thread are in flight together), finds each 32-element block's abs-max with
-// packed bf16x2 abs-max instructions plus two shuffles across the block's 4 lanes,
-// derives the E8M0 byte from the exponent field, converts in registers with the hardware
-// paired converters and writes codes (or the dequantized bf16) with one coalesced store per
-// vector. Swizzled scales of a tile are exactly one 512-byte tile of the 128x4 layout: they are
-// gathered in shared memory and written as 32 x 16-byte stores. Grouped (MoE) calls map each
-// 128-row block to its expert with a per-CTA prefix over the expert row counts.
+// One persistent grid walks tiles of 128 rows x 128 elements. Each of the 256 threads of a CTA
+// owns two whole 32-element blocks of a tile (rows r and r + 64, block column tid % 4): it reads
+// each block with two 32-byte loads (a warp instruction covers 8 rows x 256 contiguous bytes and
+// fills every sector it touches), takes the abs-max with packed bf16x2 abs-max instructions,
+// derives the E8M0 byte from the exponent field once per block, converts in registers with the
+// hardware paired converters and writes the block's codes (16 or 32 bytes) or its dequantized
+// bf16 (two 32-byte stores). A tile's 4 x 128 block scales are exactly one 512-byte tile of the
+// swizzled layout: they are gathered in shared memory and written as 32 x 16-byte stores.
+// Grouped (MoE) calls map each 128-row block to its expert with a per-CTA prefix over the
+// expert row counts.
 #include <algorithm>
 #include <map>
 #include <mutex>
@@ -21,10 +22,95 @@ namespace mxq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kVecs = kTileRows * (kTileCols / 8) / kThreads;  // 16-byte vectors per thread: 8
 constexpr int kMaxExperts = 1024;
 
-__device__ __forceinline__ uint4 load_stream(const uint4* p) { return __ldcs(p); }
+__device__ __forceinline__ void load32B(const void* p, uint32_t* r) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ void store32B(void* p, const uint32_t* r) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
+// abs-max of one block (16 bf16x2 words) as sign-free bf16 bits; NaN propagates.
+__device__ __forceinline__ uint32_t absmax_block(const uint32_t* w) {
+  uint32_t m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[i]) : "r"(w[2 * i]), "r"(w[2 * i + 1]));
+  }
+#pragma unroll
+  for (int h = 4; h >= 1; h >>= 1) {
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[i]) : "r"(m[i]), "r"(m[i + h]));
+    }
+  }
+  return max(m[0] & 0x7FFFu, (m[0] >> 16) & 0x7FFFu);
+}
+
+// Quantize (or QDQ) one block held in w[16]; writes codes / bf16 through `out` when `ok`.
+// Returns the scale byte.
+template <int FMT, bool QDQ>
+__device__ __forceinline__ uint32_t block_kernel(const uint32_t* w, bool ok, void* out) {
+  const uint32_t byte = scale_byte_from_amax_bits<FMT>(absmax_block(w) << 16);
+  const float inv = inv_scale_of(byte);
+  const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);  // a NaN / Inf block in the warp
+  if (QDQ) {
+    const float sc = scale_of(byte);
+    uint32_t o[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float lo = bf16_lo(w[i]), hi = bf16_hi(w[i]);
+      mul2(lo, hi, inv);
+      o[i] = qdq2<FMT>(lo, hi, sc);
+    }
+    if (special && byte == 255u) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i] = kBf16NaNx2;
+    }
+    if (ok) {
+      store32B(out, o);
+      store32B(static_cast<uint8_t*>(out) + 32, o + 8);
+    }
+  } else {
+    uint32_t c[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float t[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        t[2 * i] = bf16_lo(w[4 * q + i]);
+        t[2 * i + 1] = bf16_hi(w[4 * q + i]);
+        mul2(t[2 * i], t[2 * i + 1], inv);
+      }
+      if (FMT == kFmtE2M1) {
+        c[q] = codes8_e2m1(t);
+      } else {
+        const uint2 p = codes8_e4m3(t);
+        c[2 * q] = p.x;
+        c[2 * q + 1] = p.y;
+      }
+    }
+    if (special && byte == 255u) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = FMT == kFmtE2M1 ? 0u : kE4M3NaNx4;
+    }
+    if (ok) {
+      if (FMT == kFmtE2M1) {
+        __stcs(static_cast<uint4*>(out), make_uint4(c[0], c[1], c[2], c[3]));
+      } else {
+        store32B(out, c);
+      }
+    }
+  }
+  return byte;
+}
 
 template <int FMT, bool QDQ, bool SWZ, bool GROUPED>
 __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
@@ -34,10 +120,10 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
   __shared__ int64_t s_warp[kThreads / 32];
 
   const int tid = threadIdx.x;
-  const int vec = tid & 15;  // 16-byte vector of the tile row
-  const int rsub = tid >> 4;
-  const int blk = vec >> 2;  // 32-element block of the tile row
-  const uint4* x = static_cast<const uint4*>(a.x);
+  const int bc = tid & 3;   // block column of the tile owned by this thread
+  const int br = tid >> 2;  // tile rows br and br + 64
+  const uint16_t* x = static_cast<const uint16_t*>(a.x);
+  constexpr int kCodeBytes = QDQ ? 64 : (FMT == kFmtE2M1 ? 16 : 32);  // output bytes per block
 
   if (GROUPED) {
     // expert e owns ceil(n_e / 128) padded row blocks; s_prefix[e] = blocks of experts < e.
@@ -109,51 +195,36 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
       rows_valid = a.M - row0;
     }
     rows_valid = rows_valid > kTileRows ? kTileRows : (rows_valid < 0 ? 0 : rows_valid);
-    const int64_t col = cb * kTileCols + vec * 8;
+    const int64_t col = cb * kTileCols + bc * 32;
     const bool col_ok = col < a.K;
 
-    uint4 v[kVecs];
+    // both blocks' loads in flight before any arithmetic
+    uint32_t w[2][16];
+    bool ok[2];
 #pragma unroll
-    for (int i = 0; i < kVecs; ++i) {
-      const int r = i * 16 + rsub;
-      v[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (col_ok && r < rows_valid) v[i] = load_stream(x + (((row0 + r) * a.K + col) >> 3));
-    }
-
-#pragma unroll
-    for (int i = 0; i < kVecs; ++i) {
-      const int r = i * 16 + rsub;
-      uint32_t m = absmax_bf16x8(v[i]);
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      const uint32_t byte = scale_byte_from_amax_bits<FMT>(m << 16);
-      const bool ok = col_ok && r < rows_valid;
-      const int64_t e0 = (row0 + r) * a.K + col;  // first element of this vector
-      float t[8];
-      scaled8_bf16(v[i], inv_scale_of(byte), t);
-      const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);  // a NaN / Inf block
-      if (QDQ) {
-        const float sc = scale_of(byte);
-        uint4 o = make_uint4(qdq2<FMT>(t[0], t[1], sc), qdq2<FMT>(t[2], t[3], sc),
-                             qdq2<FMT>(t[4], t[5], sc), qdq2<FMT>(t[6], t[7], sc));
-        if (special && byte == 255u) o = make_uint4(kBf16NaNx2, kBf16NaNx2, kBf16NaNx2, kBf16NaNx2);
-        if (ok) __stcs(static_cast<uint4*>(a.out) + (e0 >> 3), o);
+    for (int j = 0; j < 2; ++j) {
+      const int r = br + 64 * j;
+      ok[j] = col_ok && r < rows_valid;
+      if (ok[j]) {
+        const uint16_t* src = x + (row0 + r) * a.K + col;
+        load32B(src, w[j]);
+        load32B(src + 16, w[j] + 8);
       } else {
-        if (FMT == kFmtE2M1) {
-          uint32_t c = codes8_e2m1(t);
-          if (special && byte == 255u) c = 0u;
-          if (ok) __stcs(static_cast<unsigned int*>(a.out) + (e0 >> 3), c);
-        } else {
-          uint2 c = codes8_e4m3(t);
-          if (special && byte == 255u) c = make_uint2(kE4M3NaNx4, kE4M3NaNx4);
-          if (ok) __stcs(static_cast<uint2*>(a.out) + (e0 >> 3), c);
-        }
-        if ((vec & 3) == 0) {
-          if (SWZ) {
-            s_scale[buf][swizzle_in_tile(r, blk)] = (uint8_t)byte;  // pads: zero input -> 0
-          } else if (ok) {
-            a.scales[(row0 + r) * a.scale_cols + cb * 4 + blk] = (uint8_t)byte;
-          }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[j][i] = 0u;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int r = br + 64 * j;
+      const int64_t blk = ((row0 + r) * a.K + col) >> 5;  // block index in the flat input
+      void* dst = static_cast<uint8_t*>(a.out) + blk * kCodeBytes;
+      const uint32_t byte = block_kernel<FMT, QDQ>(w[j], ok[j], dst);
+      if (!QDQ) {
+        if (SWZ) {
+          s_scale[buf][swizzle_in_tile(r, bc)] = (uint8_t)byte;  // pads: zero input -> 0
+        } else if (ok[j]) {
+          a.scales[(row0 + r) * a.scale_cols + cb * 4 + bc] = (uint8_t)byte;
         }
       }
     }

@@ -101,6 +101,8 @@ def test_quantize_validation(L):
     assert q(P, 4, 64, 1, 32, 0, 0, None, P, None) == NULL
     assert q(P, 4, 64, 1, 32, 0, 0, P, None, None) == NULL
     assert q(P + 8, 4, 64, 1, 32, 0, 0, P, P, None) == ALIGN
+    assert q(P + 16, 4, 64, 1, 32, 0, 0, P, P, None) == ALIGN
+    assert q(P, 4, 64, 2, 32, 0, 0, P + 16, P, None) == ALIGN
     assert q(P, 4, 64, 1, 32, 0, 0, P + 4, P, None) == ALIGN
     assert q(P, 4, 64, 1, 32, 1, 0, P, P + 1, None) == ALIGN
     # empty calls launch nothing and succeed, even with NULL buffers
@@ -116,6 +118,7 @@ def test_qdq_and_rotation_validation(L):
     assert L.mx_qdq(P, 4, 64, 1, 32, 0, P + 1, 32, P, None) == ALIGN
     assert L.mx_qdq(P, 4, 64, 1, 32, 0, None, 0, None, None) == NULL
     assert L.mx_qdq(P, 4, 64, 1, 32, 0, None, 0, P + 2, None) == ALIGN
+    assert L.mx_qdq(P, 4, 64, 1, 32, 0, None, 0, P + 16, None) == ALIGN
     r = L.mx_rotate_quantize
     assert r(P, 4, 64, P, 48, 1, 32, 1, 0, P, P, None) == UNSUP
     assert r(P, 4, 192, P, 128, 1, 32, 1, 0, P, P, None) == SHAPE
