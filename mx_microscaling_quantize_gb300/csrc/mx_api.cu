@@ -204,9 +204,10 @@ mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, in
 
 mx_status mx_device_errors(int* flags) {
   if (!flags) return MX_ERR_NULL;
-  unsigned int v = 0;
+  unsigned int v = 0, w = 0;
   cudaError_t err = mxq::read_device_errors(&v);
-  *flags = (int)v;
+  if (err == cudaSuccess) err = mxq::read_stream_errors(&w);
+  *flags = (int)(v | w);
   return from_cuda(err);
 }
 

@@ -45,8 +45,10 @@ struct RotArgs {
 cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const RotArgs& a,
                           cudaStream_t stream);
 
-// Reads and clears the device error word of the current device (synchronizes).
+// Read and clear the device error words of the current device (the rotation kernels' and the
+// streaming kernels'); read_device_errors synchronizes the device first.
 cudaError_t read_device_errors(unsigned int* flags);
+cudaError_t read_stream_errors(unsigned int* flags);
 
 // Number of CTAs of `kernel` that fit on the current device at once: SMs x CTAs per SM from
 // the kernel's registers and shared memory against the SM's limits, capped at max_per_sm when
