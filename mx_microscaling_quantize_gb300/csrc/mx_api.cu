@@ -49,8 +49,6 @@ mxq::StreamArgs stream_args(const void* x, int64_t M, int64_t K, void* out) {
   a.out = out;
   a.M = M;
   a.K = K;
-  a.col_tiles = ceil_div(K, mxq::kTileCols);
-  a.row_blocks = ceil_div(M, mxq::kTileRows);
   return a;
 }
 
@@ -112,7 +110,8 @@ mx_status mx_quantize(const void* x, int64_t M, int64_t K, int fmt, int group, i
   if (layout == MX_SCALES_SWIZZLED && !aligned16(scales)) return MX_ERR_ALIGN;
   mxq::StreamArgs a = stream_args(x, M, K, codes);
   a.scales = static_cast<uint8_t*>(scales);
-  a.scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : a.col_tiles * 4;
+  a.scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : ceil_div(K, mxq::kTileCols) * 4;
+  a.scale_rows = layout == MX_SCALES_LINEAR ? M : ceil_div(M, mxq::kTileRows) * mxq::kTileRows;
   return from_cuda(mxq::launch_stream(fmt, false, layout == MX_SCALES_SWIZZLED, false, a,
                                       static_cast<cudaStream_t>(stream)));
 }
@@ -176,10 +175,8 @@ mx_status mx_quantize_grouped(const void* x, const int64_t* row_offsets, int E, 
   if (layout == MX_SCALES_SWIZZLED && !aligned16(scales)) return MX_ERR_ALIGN;
   mxq::StreamArgs a = stream_args(x, M_total, K, codes);
   a.scales = static_cast<uint8_t*>(scales);
-  // every expert adds at most one partial 128-row block
-  a.row_blocks = layout == MX_SCALES_LINEAR ? ceil_div(M_total, mxq::kTileRows) + E
-                                            : srows / mxq::kTileRows;
   a.scale_cols = scols;
+  a.scale_rows = srows;
   a.offsets = row_offsets;
   a.E = E;
   return from_cuda(mxq::launch_stream(fmt, false, layout == MX_SCALES_SWIZZLED, true, a,
@@ -204,10 +201,9 @@ mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, in
 
 mx_status mx_device_errors(int* flags) {
   if (!flags) return MX_ERR_NULL;
-  unsigned int v = 0, w = 0;
+  unsigned int v = 0;
   cudaError_t err = mxq::read_device_errors(&v);
-  if (err == cudaSuccess) err = mxq::read_stream_errors(&w);
-  *flags = (int)(v | w);
+  *flags = (int)v;
   return from_cuda(err);
 }
 

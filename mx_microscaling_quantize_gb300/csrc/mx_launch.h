@@ -17,9 +17,8 @@ struct StreamArgs {
   uint8_t* scales;         // quantize only
   int64_t M;               // rows of x (all experts when grouped)
   int64_t K;
-  int64_t col_tiles;       // ceil(K / 128)
-  int64_t row_blocks;      // 128-row blocks visited (grouped: padded-row bound / 128)
   int64_t scale_cols;      // linear: K / 32; swizzled: col_tiles * 4
+  int64_t scale_rows;      // rows of the scale buffer
   const int64_t* offsets;  // grouped only: device int64 [E + 1]
   int E;
 };
@@ -45,10 +44,8 @@ struct RotArgs {
 cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const RotArgs& a,
                           cudaStream_t stream);
 
-// Read and clear the device error words of the current device (the rotation kernels' and the
-// streaming kernels'); read_device_errors synchronizes the device first.
+// Reads and clears the device error word of the current device (synchronizes).
 cudaError_t read_device_errors(unsigned int* flags);
-cudaError_t read_stream_errors(unsigned int* flags);
 
 // Number of CTAs of `kernel` that fit on the current device at once: SMs x CTAs per SM from
 // the kernel's registers and shared memory against the SM's limits, capped at max_per_sm when
