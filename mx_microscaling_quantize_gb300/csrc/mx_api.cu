@@ -1,5 +1,6 @@
 // mx_api.cu -- the extern "C" entry points declared in include/mxq.h: host-side validation,
 // shape arithmetic and launch selection. No allocation, no synchronization, no device reads.
+#include <climits>
 #include <cstdint>
 
 #include "mx_launch.h"
@@ -28,6 +29,9 @@ mx_status check_common(int64_t M, int64_t K, int fmt, int group, int rounding, b
   *empty = (M == 0 || K == 0);
   return MX_OK;
 }
+
+// the rotation kernels address rows and columns through a 2-D tensor map (32-bit coordinates)
+bool fits_tensor_map(int64_t M, int64_t K) { return M <= INT32_MAX && K <= INT32_MAX; }
 
 mx_status from_cuda(cudaError_t err) { return err == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
 
@@ -123,7 +127,7 @@ mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int ro
   if (st != MX_OK) return st;
   if (H) {
     if (!valid_g(g)) return MX_ERR_UNSUPPORTED;
-    if (K % g != 0) return MX_ERR_SHAPE;
+    if (K % g != 0 || !fits_tensor_map(M, K)) return MX_ERR_SHAPE;
   }
   if (empty) return MX_OK;
   if (!x || !y) return MX_ERR_NULL;
@@ -144,7 +148,7 @@ mx_status mx_rotate_quantize(const void* x, int64_t M, int64_t K, const void* H,
   mx_status st = check_common(M, K, fmt, group, rounding, &empty);
   if (st != MX_OK) return st;
   if (!valid_layout(layout) || !valid_g(g)) return MX_ERR_UNSUPPORTED;
-  if (K % g != 0) return MX_ERR_SHAPE;
+  if (K % g != 0 || !fits_tensor_map(M, K)) return MX_ERR_SHAPE;
   if (empty) return MX_OK;
   if (!x || !H || !codes || !scales) return MX_ERR_NULL;
   if (!aligned32(x) || !aligned32(codes)) return MX_ERR_ALIGN;
@@ -189,7 +193,7 @@ mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, in
   mx_status st = check_common(M, K, MX_FMT_E2M1, 32, MX_ROUND_RNE, &empty);
   if (st != MX_OK) return st;
   if (!valid_g(g)) return MX_ERR_UNSUPPORTED;
-  if (K % g != 0) return MX_ERR_SHAPE;
+  if (K % g != 0 || !fits_tensor_map(M, K)) return MX_ERR_SHAPE;
   if (empty) return MX_OK;
   if (!x || !H || !y_f32) return MX_ERR_NULL;
   if (!aligned32(x) || !aligned32(y_f32)) return MX_ERR_ALIGN;

@@ -2,23 +2,31 @@
 //
 // The rotation multiplies every g-element chunk along K by a runtime-loaded g x g bf16 matrix
 // H (QuTLASS pull request, feature list: "Rotation matrices loaded at runtime, allowing any
-// transformation", sizes 16/32/64/128). For a tile of 128 rows x 128 elements that is
-// 128/g independent products [128 x g] * [g x g], issued as tcgen05.mma (kind::f16, bf16
-// operands, fp32 accumulation) by one thread, with both operands in shared memory and the
-// 128 x 128 fp32 result in tensor memory (TMEM). The epilogue reads TMEM with tcgen05.ld so
-// that thread r holds row r of the tile, i.e. four whole 32-element blocks, and quantizes
-// them in registers.
+// transformation", sizes 16/32/64/128). For a tile of 128 rows x 128 elements that is 128/g
+// independent products [128 x g] * [g x g]: tcgen05.mma (kind::f16, bf16 operands, fp32
+// accumulation in tensor memory), M = 128, N = g, K = 16 per instruction.
 //
-// Shared-memory operand layout (no swizzle, K-major "core matrices" of 8 rows x 16 bytes):
-//   A (x tile):  element (r, c) at (c / 8) * kALbo + r * 16 + (c % 8) * 2, so a thread that
-//                loaded 16 bytes (8 elements) of row r stores them with one 16-byte store;
-//                kALbo = 128 * 16 + 16 keeps those stores free of bank conflicts.
-//                Descriptor: leading (K-direction) byte offset kALbo, stride (8-row) 128.
-//   B (H^T):     element (n, k) = H[k][n] at (k / 8) * (g * 16) + n * 16 + (k % 8) * 2.
-//                Descriptor: leading byte offset g * 16, stride 128.
-// Per tile: registers -> A (st.shared), fence.proxy.async, barrier, one thread issues the
-// MMAs and commits to an mbarrier, every thread prefetches the next tile into registers,
-// waits on the mbarrier (bounded), reads TMEM, quantizes and stores.
+// One persistent CTA per SM, warp-specialized:
+//   warp 0       TMA producer: two 2-D boxes of 128 rows x 64 elements per tile, 128-byte
+//                swizzle, into a ring of kStages shared-memory stages (mbarrier complete_tx);
+//   warp 1       allocates 256 TMEM columns (two 128-column fp32 accumulators) and, from one
+//                lane, issues the tile's MMAs and commits them to the stage's "empty" barrier
+//                and to the accumulator's "full" barrier;
+//   warps 2..9   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//                32*(w%4) .. +31, i.e. tile rows; two warps share a quarter and split the four
+//                32-column blocks), abs-max, E8M0 scale, conversion, stores; then they free
+//                the accumulator for the MMA two tiles on.
+// Loads, MMAs and the epilogue of different tiles overlap. Operands: A (the x tile) in the
+// K-major 128-byte-swizzled layout the TMA writes (8-row groups 1024 bytes apart); B = H^T in
+// the K-major no-swizzle core-matrix layout, written once per CTA:
+//   element (n, k) = H[k][n] at (k / 8) * (g * 16) + n * 16 + (k % 8) * 2.
+// Every mbarrier wait is bounded (2 s); a wait that runs out sets the device error word and
+// the thread stops waiting from then on.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "mx_device.cuh"
 #include "mx_launch.h"
 
@@ -28,11 +36,14 @@ __device__ unsigned int g_device_errors;
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kALbo = kTileRows * 16 + 16;       // 2064
-constexpr int kASmem = (kTileCols / 8) * kALbo;  // 33024
-constexpr int kTmemCols = 128;
-constexpr int kMaxCtasPerSm = 512 / kTmemCols;  // TMEM columns per SM / columns per CTA
+constexpr int kStages = 4;
+constexpr int kBoxCols = 64;                  // bf16 per 128-byte swizzled row
+constexpr int kBoxBytes = kTileRows * 128;    // 16 KiB
+constexpr int kStageBytes = 2 * kBoxBytes;    // 128 rows x 128 elements
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue
+constexpr int kTmemCols = 256;                   // two 128-column accumulators
 constexpr uint32_t kErrWaitTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -42,7 +53,6 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_addr, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_addr),
                "r"(ncols));
@@ -62,17 +72,23 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-__device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(addr), "r"(count));
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, P;\n\t}"
       : "=r"(done)
-      : "r"(addr), "r"(parity)
+      : "r"(bar), "r"(parity)
       : "memory");
   return done != 0;
 }
@@ -81,30 +97,47 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for the mbarrier phase with the given parity; give up after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity) {
-  if (mbar_try_wait(addr, parity)) return true;
+// Wait for the phase of the given parity; gives up after kWaitLimitNs, and at once once this
+// thread has given up before (*failed). A give-up sets the device error word.
+__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, bool* failed) {
+  if (*failed || mbar_try_wait(bar, parity)) return;
   const unsigned long long t0 = global_ns();
-  while (!mbar_try_wait(addr, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *failed = true;
+      atomicOr(&g_device_errors, kErrWaitTimeout);
+      return;
+    }
   }
-  return true;
+}
+// 2-D tensor-map load of one box into shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
 }
 
-// Shared-memory matrix descriptor, no swizzle: start, leading and stride byte offsets (all
-// multiples of 16), bit 46 set (descriptor version of the 5th-generation tensor core).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptors (5th-generation tensor core format: start >> 4 at bits
+// 0-13, leading byte offset >> 4 at 16-29, stride byte offset >> 4 at 32-45, bit 46 set,
+// swizzle mode at 61-63).
+__device__ __forceinline__ uint64_t desc_noswizzle(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
          ((uint64_t)(sbo >> 4) << 32) | (1ull << 46);
 }
-
+// K-major, 128-byte swizzle: 8-row groups 1024 bytes apart (the leading offset is unused).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B bf16 (bits 7-9
 // and 10-12 = 1), both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
 }
-
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -112,13 +145,11 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
-__device__ __forceinline__ void mma_commit(uint32_t mbar_addr) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          mbar_addr)
-      : "memory");
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::
+                   "r"(bar)
+               : "memory");
 }
-
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* y) {
   uint32_t r[32];
@@ -136,207 +167,238 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* y) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(r[i]);
 }
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
+__device__ __forceinline__ void epilogue_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }
 
 // ------------------------------------------------------------------------------------------
-// kernel
+// epilogue of one 32-element block (32 fp32 rotated values y of one tile row)
 // ------------------------------------------------------------------------------------------
-template <int G>
-constexpr int smem_bytes() {
-  return kASmem + G * G * 2 + 16 + 2 * 512;
+template <int FMT, int OUT>
+__device__ __forceinline__ uint32_t epilogue_block(float* y, bool row_ok, void* out, int64_t e0) {
+  if (OUT == kRotDebug) {
+    if (row_ok) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + e0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+    }
+    return 0u;
+  }
+  const uint32_t byte = scale_byte_from_amax_bits<FMT>(absmax_f32x32(y));
+  const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);  // a NaN / Inf block in the warp
+  {
+    const float inv = inv_scale_of(byte);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mul2(y[2 * i], y[2 * i + 1], inv);  // y <- y / 2^s
+  }
+  if (OUT == kRotQdq) {
+    const float sc = scale_of(byte);
+    uint4 o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float* t = y + 8 * i;
+      o[i] = make_uint4(qdq2<FMT>(t[0], t[1], sc), qdq2<FMT>(t[2], t[3], sc),
+                        qdq2<FMT>(t[4], t[5], sc), qdq2<FMT>(t[6], t[7], sc));
+      if (special && byte == 255u) o[i] = make_uint4(kBf16NaNx2, kBf16NaNx2, kBf16NaNx2, kBf16NaNx2);
+    }
+    if (row_ok) {
+      uint4* dst = static_cast<uint4*>(out) + (e0 >> 3);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) __stcs(dst + i, o[i]);
+    }
+  } else if (FMT == kFmtE2M1) {
+    uint4 c = make_uint4(codes8_e2m1(y), codes8_e2m1(y + 8), codes8_e2m1(y + 16), codes8_e2m1(y + 24));
+    if (special && byte == 255u) c = make_uint4(0u, 0u, 0u, 0u);
+    if (row_ok) __stcs(reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + (e0 >> 1)), c);
+  } else {
+    uint2 c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      c[i] = codes8_e4m3(y + 8 * i);
+      if (special && byte == 255u) c[i] = make_uint2(kE4M3NaNx4, kE4M3NaNx4);
+    }
+    if (row_ok) {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + e0);
+      __stcs(dst, make_uint4(c[0].x, c[0].y, c[1].x, c[1].y));
+      __stcs(dst + 1, make_uint4(c[2].x, c[2].y, c[3].x, c[3].y));
+    }
+  }
+  return byte;
 }
-// Dynamic shared memory requested per CTA: at least 56 KiB so that no more than four CTAs
-// share an SM (four x 128 TMEM columns = the SM's 512), whatever g is.
+
 template <int G>
 constexpr int smem_request() {
-  return smem_bytes<G>() > 56 * 1024 ? smem_bytes<G>() : 56 * 1024;
+  // 1 KiB of slack for aligning the stage ring to 1024 bytes
+  return 1024 + kStages * kStageBytes + G * G * 2 + 2 * 512 + (2 * kStages + 4) * 8 + 16;
 }
 
 template <int FMT, int OUT, bool SWZ, int G>
-__global__ void __launch_bounds__(kThreads) mx_rotate_kernel(RotArgs a) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + kASmem;
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(sB + G * G * 2);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mbar + 1);
-  uint8_t* s_scale = reinterpret_cast<uint8_t*>(mbar + 2);  // [2][512]
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_rotate_kernel(const __grid_constant__ CUtensorMap tmap, RotArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sA = smem;                                  // kStages x (two swizzled boxes)
+  uint8_t* sB = smem + kStages * kStageBytes;          // H^T, core-matrix layout
+  uint8_t* s_scale = sB + G * G * 2;                   // [2][512] swizzled scale tiles
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_scale + 2 * 512);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
 
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const uint4* x = static_cast<const uint4*>(a.x);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint16_t* H = static_cast<const uint16_t*>(a.H);
-
-  if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
-  }
-  if (tid == 0) mbar_init(smem_u32(mbar), 1);
-  // B = H^T in K-major core-matrix layout (coalesced reads of H's rows).
   for (int idx = tid; idx < G * G; idx += kThreads) {
     const int k = idx / G, n = idx % G;
     *reinterpret_cast<uint16_t*>(sB + (k / 8) * (G * 16) + n * 16 + (k % 8) * 2) = H[idx];
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(tfull + b), 1);
+      mbar_init(smem_u32(tempty + b), kEpiWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t sA_u32 = smem_u32(sA);
-  const uint32_t sB_u32 = smem_u32(sB);
-  const uint32_t mbar_u32 = smem_u32(mbar);
-  constexpr uint32_t idesc = idesc_bf16_f32(kTileRows, G);
-
-  const int lvec = tid & 15;  // loader: 16-byte vector of the row
-  const int lrow = tid >> 4;  // loader: rows lrow + 8 i
+  const uint32_t sA_u32 = smem_u32(sA), sB_u32 = smem_u32(sB);
   const int64_t n_tiles = a.row_blocks * a.col_tiles;
+  bool failed = false;
 
-  uint4 v[16];
-  auto load_tile = [&](int64_t t) {
-    const int64_t rb = t / a.col_tiles;
-    const int64_t cb = t - rb * a.col_tiles;
-    const int64_t row0 = rb * kTileRows;
-    const int64_t col = cb * kTileCols + lvec * 8;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int64_t row = row0 + i * 8 + lrow;
-      v[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (row < a.M && col < a.K) v[i] = __ldcs(x + ((row * a.K + col) >> 3));
-    }
-  };
-
-  int64_t t = blockIdx.x;
-  if (t < n_tiles) load_tile(t);
-  uint32_t phase = 0;
-  int buf = 0;
-  int64_t prev_tile = -1;
-  for (; t < n_tiles; t += gridDim.x) {
-    const int64_t rb = t / a.col_tiles;
-    const int64_t cb = t - rb * a.col_tiles;
-    const int64_t row0 = rb * kTileRows;
-    const int64_t kc64 = a.K - cb * kTileCols;
-    const int kc = kc64 > kTileCols ? kTileCols : (int)kc64;  // valid columns (multiple of 32, g)
-    const bool row_ok = row0 + tid < a.M;
-
-#pragma unroll
-    for (int i = 0; i < 16; ++i) st_shared_v4(sA_u32 + lvec * kALbo + (i * 8 + lrow) * 16, v[i]);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (SWZ && OUT == kRotCodes && prev_tile >= 0 && tid < 32) {
-      uint4* dst = reinterpret_cast<uint4*>(a.scales + prev_tile * 512);
-      dst[tid] = reinterpret_cast<const uint4*>(s_scale + (buf ^ 1) * 512)[tid];
-    }
-    if (tid == 0) {
-      for (int j = 0; j < kc / G; ++j) {
-#pragma unroll
-        for (int s = 0; s < G / 16; ++s) {
-          const uint64_t ad = smem_desc(sA_u32 + (j * (G / 8) + 2 * s) * kALbo, kALbo, 128);
-          const uint64_t bd = smem_desc(sB_u32 + (2 * s) * (G * 16), G * 16, 128);
-          mma_bf16(tmem + (uint32_t)(j * G), ad, bd, idesc, s > 0 ? 1u : 0u);
-        }
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+      int it = 0;
+      for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+        const int s = it % kStages;
+        if (it >= kStages) mbar_wait(smem_u32(empty + s), ((it / kStages) & 1) ^ 1, &failed);
+        const int64_t rb = t / a.col_tiles, cb = t - rb * a.col_tiles;
+        const uint32_t dst = sA_u32 + s * kStageBytes;
+        mbar_arrive_expect_tx(smem_u32(full + s), kStageBytes);
+        tma_load_2d(dst, &tmap, (int)(cb * kTileCols), (int)(rb * kTileRows), smem_u32(full + s));
+        tma_load_2d(dst + kBoxBytes, &tmap, (int)(cb * kTileCols + kBoxCols), (int)(rb * kTileRows),
+                    smem_u32(full + s));
       }
-      mma_commit(mbar_u32);
     }
-    __syncwarp();
-    if (t + gridDim.x < n_tiles) load_tile(t + gridDim.x);
-    const bool timed_out = !mbar_wait_bounded(mbar_u32, phase);
-    // the give-up decision is taken by the whole CTA so that no thread skips a barrier
-    if (__syncthreads_or(timed_out)) {
-      if (tid == 0) atomicOr(&g_device_errors, kErrWaitTimeout);
-      break;
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kTileRows, G);
+      int it = 0;
+      for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+        const int s = it % kStages, acc = it & 1;
+        const int64_t cb = t % a.col_tiles;
+        const int64_t kc64 = a.K - cb * kTileCols;
+        const int kc = kc64 > kTileCols ? kTileCols : (int)kc64;  // multiple of 32 and of g
+        mbar_wait(smem_u32(full + s), (it / kStages) & 1, &failed);
+        if (it >= 2) mbar_wait(smem_u32(tempty + acc), ((it >> 1) & 1) ^ 1, &failed);
+        tc_fence_after();
+        for (int j = 0; j < kc / G; ++j) {
+#pragma unroll
+          for (int ks = 0; ks < G / 16; ++ks) {
+            const int col = j * G + ks * 16;  // first K column of this MMA in the tile
+            const uint32_t a_addr = sA_u32 + s * kStageBytes + (col / kBoxCols) * kBoxBytes +
+                                    (col % kBoxCols) * 2;
+            const uint64_t bd = desc_noswizzle(sB_u32 + 2 * ks * (G * 16), G * 16, 128);
+            mma_bf16(tmem + (uint32_t)(acc * 128 + j * G), desc_sw128(a_addr), bd, idesc,
+                     ks > 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(smem_u32(empty + s));   // stage free once these MMAs have read it
+        mma_commit(smem_u32(tfull + acc));  // accumulator ready
+      }
     }
-    phase ^= 1u;
-    tc_fence_after();
-
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+  } else {
+    // ---------------- epilogue warps ----------------
+    const int e = warp - 2;
+    const int quad = warp & 3;          // TMEM lanes 32*quad .. +31 = tile rows
+    const int half = e >> 2;            // column blocks 2*half, 2*half + 1
+    const int r = quad * 32 + lane;     // tile row of this thread
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    int it = 0;
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const int64_t rb = t / a.col_tiles, cb = t - rb * a.col_tiles;
+      const int64_t row0 = rb * kTileRows;
+      const int64_t kc64 = a.K - cb * kTileCols;
+      const int kc = kc64 > kTileCols ? kTileCols : (int)kc64;
+      const bool row_ok = row0 + r < a.M;
+      uint8_t* tile_scales = s_scale + (it & 1) * 512;
+      mbar_wait(smem_u32(tfull + acc), (it >> 1) & 1, &failed);
+      tc_fence_after();
 #pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      if (q * 32 >= kc) {
-        if (SWZ && OUT == kRotCodes) s_scale[buf * 512 + swizzle_in_tile(tid, q)] = 0;
-        continue;
+      for (int qq = 0; qq < 2; ++qq) {
+        const int q = 2 * half + qq;
+        if (q * 32 >= kc) {
+          if (SWZ && OUT == kRotCodes) tile_scales[swizzle_in_tile(r, q)] = 0;
+          continue;
+        }
+        float y[32];
+        tmem_ld32(lane_base + (uint32_t)(acc * 128 + q * 32), y);
+        const int64_t e0 = (row0 + r) * a.K + cb * kTileCols + q * 32;  // block's first element
+        const uint32_t byte = epilogue_block<FMT, OUT>(y, row_ok, a.out, e0);
+        if (OUT == kRotCodes) {
+          if (SWZ) tile_scales[swizzle_in_tile(r, q)] = (uint8_t)byte;  // pad rows: 0
+          else if (row_ok) a.scales[(row0 + r) * a.scale_cols + cb * 4 + q] = (uint8_t)byte;
+        }
       }
-      float y[32];
-      tmem_ld32(lane_base + (uint32_t)(q * 32), y);
-      const int64_t e0 = (row0 + tid) * a.K + cb * kTileCols + q * 32;  // first element
-      if (OUT == kRotDebug) {
-        if (row_ok) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + e0);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            dst[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
-          }
-        }
-        continue;
-      }
-      const uint32_t byte = scale_byte_from_amax_bits<FMT>(absmax_f32x32(y));
-      const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);  // a NaN / Inf block
-      {
-        const float inv = inv_scale_of(byte);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) mul2(y[2 * i], y[2 * i + 1], inv);  // y <- y / 2^s
-      }
-      if (OUT == kRotQdq) {
-        const float sc = scale_of(byte);
-        uint4 o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float* t = y + 8 * i;
-          o[i] = make_uint4(qdq2<FMT>(t[0], t[1], sc), qdq2<FMT>(t[2], t[3], sc),
-                            qdq2<FMT>(t[4], t[5], sc), qdq2<FMT>(t[6], t[7], sc));
-          if (special && byte == 255u) {
-            o[i] = make_uint4(kBf16NaNx2, kBf16NaNx2, kBf16NaNx2, kBf16NaNx2);
-          }
-        }
-        if (row_ok) {
-          uint4* dst = static_cast<uint4*>(a.out) + (e0 >> 3);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) __stcs(dst + i, o[i]);
-        }
-      } else {
-        if (FMT == kFmtE2M1) {
-          uint4 c = make_uint4(codes8_e2m1(y), codes8_e2m1(y + 8), codes8_e2m1(y + 16),
-                               codes8_e2m1(y + 24));
-          if (special && byte == 255u) c = make_uint4(0u, 0u, 0u, 0u);
-          if (row_ok) {
-            __stcs(reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + (e0 >> 1)), c);
-          }
-        } else {
-          uint2 c[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            c[i] = codes8_e4m3(y + 8 * i);
-            if (special && byte == 255u) c[i] = make_uint2(kE4M3NaNx4, kE4M3NaNx4);
-          }
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + e0);
-            __stcs(dst, make_uint4(c[0].x, c[0].y, c[1].x, c[1].y));
-            __stcs(dst + 1, make_uint4(c[2].x, c[2].y, c[3].x, c[3].y));
-          }
-        }
-        if (SWZ) {
-          s_scale[buf * 512 + swizzle_in_tile(tid, q)] = (uint8_t)byte;  // pad rows: 0
-        } else if (row_ok) {
-          a.scales[(row0 + tid) * a.scale_cols + cb * 4 + q] = (uint8_t)byte;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(tempty + acc));  // accumulator free for tile it + 2
+      if (SWZ && OUT == kRotCodes) {
+        epilogue_sync();  // the tile's 512 scale bytes are complete
+        if (e == 0) {
+          uint4* dst = reinterpret_cast<uint4*>(a.scales + t * 512);
+          dst[lane] = reinterpret_cast<const uint4*>(tile_scales)[lane];
         }
       }
     }
-    tc_fence_before();
-    prev_tile = t;
-    buf ^= 1;
   }
+  tc_fence_before();
   __syncthreads();
-  if (SWZ && OUT == kRotCodes && prev_tile >= 0 && tid < 32) {
-    uint4* dst = reinterpret_cast<uint4*>(a.scales + prev_tile * 512);
-    dst[tid] = reinterpret_cast<const uint4*>(s_scale + (buf ^ 1) * 512)[tid];
-  }
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------
+// Tensor map of x: 2-D [M rows, K columns] bf16, boxes of 128 rows x 64 columns, 128-byte
+// swizzle, zero fill out of bounds (pad rows and a short last column tile read zeros).
+cudaError_t make_tensor_map(CUtensorMap* map, const RotArgs& a) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  });
+  if (!encode) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+  const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBoxCols, (cuuint32_t)kTileRows};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.x), dims,
+                            strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <int FMT, int OUT, bool SWZ, int G>
@@ -346,10 +408,13 @@ cudaError_t launch_t(const RotArgs& a, cudaStream_t stream) {
   constexpr int smem = smem_request<G>();
   const int64_t n_tiles = a.row_blocks * a.col_tiles;
   if (n_tiles <= 0) return cudaSuccess;
-  const int resident = resident_ctas(k, kThreads, smem, kMaxCtasPerSm);
+  CUtensorMap map;
+  cudaError_t err = make_tensor_map(&map, a);
+  if (err != cudaSuccess) return err;
+  const int resident = resident_ctas(k, kThreads, smem, 1);
   if (resident <= 0) return cudaErrorInvalidConfiguration;
   const int grid = (int)(n_tiles < resident ? n_tiles : resident);
-  kern<<<grid, kThreads, smem, stream>>>(a);
+  kern<<<grid, kThreads, smem, stream>>>(map, a);
   return cudaGetLastError();
 }
 
