@@ -12,10 +12,10 @@
 //   warp 1       allocates 256 TMEM columns (two 128-column fp32 accumulators) and, from one
 //                lane, issues the tile's MMAs and commits them to the stage's "empty" barrier
 //                and to the accumulator's "full" barrier;
-//   warps 2..9   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
-//                32*(w%4) .. +31, i.e. tile rows; two warps share a quarter and split the four
-//                32-column blocks), abs-max, E8M0 scale, conversion, stores; then they free
-//                the accumulator for the MMA two tiles on.
+//   warps 2..17  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//                32*(w%4) .. +31, i.e. tile rows; the four warps of a quarter take one
+//                32-column block each), abs-max, E8M0 scale, conversion, stores; then they
+//                free the accumulator for the MMA two tiles on.
 // Loads, MMAs and the epilogue of different tiles overlap. Operands: A (the x tile) in the
 // K-major 128-byte-swizzled layout the TMA writes (8-row groups 1024 bytes apart); B = H^T in
 // the K-major no-swizzle core-matrix layout, written once per CTA:
@@ -40,7 +40,7 @@ constexpr int kStages = 4;
 constexpr int kBoxCols = 64;                  // bf16 per 128-byte swizzled row
 constexpr int kBoxBytes = kTileRows * 128;    // 16 KiB
 constexpr int kStageBytes = 2 * kBoxBytes;    // 128 rows x 128 elements
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue
 constexpr int kTmemCols = 256;                   // two 128-column accumulators
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue warps ----------------
     const int e = warp - 2;
     const int quad = warp & 3;          // TMEM lanes 32*quad .. +31 = tile rows
-    const int half = e >> 2;            // column blocks 2*half, 2*half + 1
+    const int q = e >> 2;               // the 32-column block of the tile this warp converts
     const int r = quad * 32 + lane;     // tile row of this thread
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     int it = 0;
@@ -338,13 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* tile_scales = s_scale + (it & 1) * 512;
       mbar_wait(smem_u32(tfull + acc), (it >> 1) & 1, &failed);
       tc_fence_after();
-#pragma unroll 1
-      for (int qq = 0; qq < 2; ++qq) {
-        const int q = 2 * half + qq;
-        if (q * 32 >= kc) {
-          if (SWZ && OUT == kRotCodes) tile_scales[swizzle_in_tile(r, q)] = 0;
-          continue;
-        }
+      if (q * 32 >= kc) {
+        if (SWZ && OUT == kRotCodes) tile_scales[swizzle_in_tile(r, q)] = 0;
+      } else {
         float y[32];
         tmem_ld32(lane_base + (uint32_t)(acc * 128 + q * 32), y);
         const int64_t e0 = (row0 + r) * a.K + cb * kTileCols + q * 32;  // block's first element
