@@ -9,13 +9,13 @@
 // One persistent CTA per SM, warp-specialized:
 //   warp 0       TMA producer: two 2-D boxes of 128 rows x 64 elements per tile, 128-byte
 //                swizzle, into a ring of kStages shared-memory stages (mbarrier complete_tx);
-//   warp 1       allocates 256 TMEM columns (two 128-column fp32 accumulators) and, from one
+//   warp 1       allocates 512 TMEM columns (four 128-column fp32 accumulators) and, from one
 //                lane, issues the tile's MMAs and commits them to the stage's "empty" barrier
 //                and to the accumulator's "full" barrier;
 //   warps 2..17  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
 //                32*(w%4) .. +31, i.e. tile rows; the four warps of a quarter take one
 //                32-column block each), abs-max, E8M0 scale, conversion, stores; then they
-//                free the accumulator for the MMA two tiles on.
+//                free the accumulator for the MMA four tiles on.
 // Loads, MMAs and the epilogue of different tiles overlap. Operands: A (the x tile) in the
 // K-major 128-byte-swizzled layout the TMA writes (8-row groups 1024 bytes apart); B = H^T in
 // the K-major no-swizzle core-matrix layout, written once per CTA:
@@ -36,14 +36,14 @@ __device__ unsigned int g_device_errors;
 
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kAcc = 4;  // fp32 accumulators in TMEM (128 columns each)
 constexpr int kBoxCols = 64;                  // bf16 per 128-byte swizzled row
 constexpr int kBoxBytes = kTileRows * 128;    // 16 KiB
 constexpr int kStageBytes = 2 * kBoxBytes;    // 128 rows x 128 elements
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue
-constexpr int kTmemCols = 256;                   // two 128-column accumulators
+constexpr int kTmemCols = 128 * kAcc;             // all 512 columns of the SM
 constexpr uint32_t kErrWaitTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -226,15 +226,22 @@ __device__ __forceinline__ uint32_t epilogue_block(float* y, bool row_ok, void* 
   return byte;
 }
 
+// shared-memory stages in flight: as many 32 KiB tiles as fit beside H^T
 template <int G>
-constexpr int smem_request() {
+__host__ __device__ constexpr int stages() {
+  return G == 128 ? 5 : 6;
+}
+template <int G>
+__host__ __device__ constexpr int smem_request() {
   // 1 KiB of slack for aligning the stage ring to 1024 bytes
-  return 1024 + kStages * kStageBytes + G * G * 2 + 2 * 512 + (2 * kStages + 4) * 8 + 16;
+  return 1024 + stages<G>() * kStageBytes + G * G * 2 + 2 * 512 + (2 * stages<G>() + 2 * kAcc) * 8 +
+         16;
 }
 
 template <int FMT, int OUT, bool SWZ, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_rotate_kernel(const __grid_constant__ CUtensorMap tmap, RotArgs a) {
+  constexpr int kStages = stages<G>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;                                  // kStages x (two swizzled boxes)
@@ -243,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(s_scale + 2 * 512);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tempty = tfull + kAcc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + kAcc);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint16_t* H = static_cast<const uint16_t*>(a.H);
@@ -257,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(full + s), 1);
       mbar_init(smem_u32(empty + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kAcc; ++b) {
       mbar_init(smem_u32(tfull + b), 1);
       mbar_init(smem_u32(tempty + b), kEpiWarps);
     }
@@ -298,12 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(kTileRows, G);
       int it = 0;
       for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
-        const int s = it % kStages, acc = it & 1;
+        const int s = it % kStages, acc = it % kAcc;
         const int64_t cb = t % a.col_tiles;
         const int64_t kc64 = a.K - cb * kTileCols;
         const int kc = kc64 > kTileCols ? kTileCols : (int)kc64;  // multiple of 32 and of g
         mbar_wait(smem_u32(full + s), (it / kStages) & 1, &failed);
-        if (it >= 2) mbar_wait(smem_u32(tempty + acc), ((it >> 1) & 1) ^ 1, &failed);
+        if (it >= kAcc) mbar_wait(smem_u32(tempty + acc), ((it / kAcc) & 1) ^ 1, &failed);
         tc_fence_after();
         for (int j = 0; j < kc / G; ++j) {
 #pragma unroll
@@ -329,14 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     int it = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
-      const int acc = it & 1;
+      const int acc = it % kAcc;
       const int64_t rb = t / a.col_tiles, cb = t - rb * a.col_tiles;
       const int64_t row0 = rb * kTileRows;
       const int64_t kc64 = a.K - cb * kTileCols;
       const int kc = kc64 > kTileCols ? kTileCols : (int)kc64;
       const bool row_ok = row0 + r < a.M;
       uint8_t* tile_scales = s_scale + (it & 1) * 512;
-      mbar_wait(smem_u32(tfull + acc), (it >> 1) & 1, &failed);
+      mbar_wait(smem_u32(tfull + acc), (it / kAcc) & 1, &failed);
       tc_fence_after();
       if (q * 32 >= kc) {
         if (SWZ && OUT == kRotCodes) tile_scales[swizzle_in_tile(r, q)] = 0;
@@ -352,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(tempty + acc));  // accumulator free for tile it + 2
+      if (lane == 0) mbar_arrive(smem_u32(tempty + acc));  // accumulator free for tile it + kAcc
       if (SWZ && OUT == kRotCodes) {
         epilogue_sync();  // the tile's 512 scale bytes are complete
         if (e == 0) {
