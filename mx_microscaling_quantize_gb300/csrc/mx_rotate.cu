@@ -120,6 +120,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 2-D tensor-map store of one box from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// all committed bulk stores have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// all committed bulk stores are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Shared-memory matrix descriptors (5th-generation tensor core format: start >> 4 at bits
 // 0-13, leading byte offset >> 4 at 16-29, stride byte offset >> 4 at 32-45, bit 46 set,
 // swizzle mode at 61-63).
@@ -169,6 +184,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* y) {
 }
 __device__ __forceinline__ void epilogue_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+}
+
+// ------------------------------------------------------------------------------------------
+// QDQ of one 32-element block of rotated values -> 32 bf16 in o[4]
+// ------------------------------------------------------------------------------------------
+template <int FMT>
+__device__ __forceinline__ void qdq_block_vals(float* y, uint4* o) {
+  const uint32_t byte = scale_byte_from_amax_bits<FMT>(absmax_f32x32(y));
+  const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);  // a NaN / Inf block in the warp
+  const float inv = inv_scale_of(byte), sc = scale_of(byte);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) mul2(y[2 * i], y[2 * i + 1], inv);  // y <- y / 2^s
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float* t = y + 8 * i;
+    o[i] = make_uint4(qdq2<FMT>(t[0], t[1], sc), qdq2<FMT>(t[2], t[3], sc),
+                      qdq2<FMT>(t[4], t[5], sc), qdq2<FMT>(t[6], t[7], sc));
+    if (special && byte == 255u) o[i] = make_uint4(kBf16NaNx2, kBf16NaNx2, kBf16NaNx2, kBf16NaNx2);
+  }
 }
 
 // ------------------------------------------------------------------------------------------
@@ -227,25 +261,32 @@ __device__ __forceinline__ uint32_t epilogue_block(float* y, bool row_ok, void* 
 }
 
 // shared-memory stages in flight: as many 32 KiB tiles as fit beside H^T
-template <int G>
+template <int G, int OUT>
 __host__ __device__ constexpr int stages() {
-  return G == 128 ? 5 : 6;
+  return (G == 128 || OUT == kRotQdq) ? 5 : 6;
 }
-template <int G>
+// QDQ outputs are staged in shared memory (one 32 KiB tile) and written back with TMA stores
+template <int OUT>
+__host__ __device__ constexpr int out_stage_bytes() {
+  return OUT == kRotQdq ? kStageBytes : 0;
+}
+template <int G, int OUT>
 __host__ __device__ constexpr int smem_request() {
   // 1 KiB of slack for aligning the stage ring to 1024 bytes
-  return 1024 + stages<G>() * kStageBytes + G * G * 2 + 2 * 512 + (2 * stages<G>() + 2 * kAcc) * 8 +
-         16;
+  return 1024 + stages<G, OUT>() * kStageBytes + out_stage_bytes<OUT>() + G * G * 2 + 2 * 512 +
+         (2 * stages<G, OUT>() + 2 * kAcc) * 8 + 16;
 }
 
 template <int FMT, int OUT, bool SWZ, int G>
 __global__ void __launch_bounds__(kThreads, 1)
-    mx_rotate_kernel(const __grid_constant__ CUtensorMap tmap, RotArgs a) {
-  constexpr int kStages = stages<G>();
+    mx_rotate_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap ymap,
+                     RotArgs a) {
+  constexpr int kStages = stages<G, OUT>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;                                  // kStages x (two swizzled boxes)
-  uint8_t* sB = smem + kStages * kStageBytes;          // H^T, core-matrix layout
+  uint8_t* sOut = smem + kStages * kStageBytes;        // QDQ output tile (two swizzled boxes)
+  uint8_t* sB = sOut + out_stage_bytes<OUT>();         // H^T, core-matrix layout
   uint8_t* s_scale = sB + G * G * 2;                   // [2][512] swizzled scale tiles
   uint64_t* full = reinterpret_cast<uint64_t*>(s_scale + 2 * 512);
   uint64_t* empty = full + kStages;
@@ -345,7 +386,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* tile_scales = s_scale + (it & 1) * 512;
       mbar_wait(smem_u32(tfull + acc), (it / kAcc) & 1, &failed);
       tc_fence_after();
-      if (q * 32 >= kc) {
+      const bool active = q * 32 < kc;  // this warp's 32 columns exist in the tile
+      if (OUT == kRotQdq) {
+        uint4 o[4];
+        if (active) {
+          float y[32];
+          tmem_ld32(lane_base + (uint32_t)(acc * 128 + q * 32), y);
+          qdq_block_vals<FMT>(y, o);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(tempty + acc));  // accumulator free for tile it + kAcc
+        // the previous tile's TMA store has read the staging tile before anyone overwrites it
+        if (e == 0 && lane == 0) bulk_wait_read();
+        epilogue_sync();
+        if (active) {
+          // row r, 16-byte chunk c of box q/2 sits at chunk c ^ (r % 8) (128-byte swizzle)
+          uint8_t* box = sOut + (q >> 1) * kBoxBytes + r * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int c = (q & 1) * 4 + k;
+            *reinterpret_cast<uint4*>(box + ((c ^ (r & 7)) << 4)) = o[k];
+          }
+        }
+        fence_proxy_async_smem();
+        epilogue_sync();
+        if (e == 0 && lane == 0) {
+          const uint32_t src = smem_u32(sOut);
+          tma_store_2d(&ymap, (int)(cb * kTileCols), (int)row0, src);  // rows >= M are clipped
+          if (kc > kBoxCols) tma_store_2d(&ymap, (int)(cb * kTileCols + kBoxCols), (int)row0, src + kBoxBytes);
+          bulk_commit();
+        }
+        continue;
+      }
+      if (!active) {
         if (SWZ && OUT == kRotCodes) tile_scales[swizzle_in_tile(r, q)] = 0;
       } else {
         float y[32];
@@ -369,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  if (OUT == kRotQdq && warp == 2 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -378,9 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------
-// Tensor map of x: 2-D [M rows, K columns] bf16, boxes of 128 rows x 64 columns, 128-byte
-// swizzle, zero fill out of bounds (pad rows and a short last column tile read zeros).
-cudaError_t make_tensor_map(CUtensorMap* map, const RotArgs& a) {
+// Tensor map of a bf16 [M rows, K columns] matrix (x, or the QDQ output y): boxes of 128 rows
+// x 64 columns, 128-byte swizzle; loads read zeros out of bounds (pad rows, a short last column
+// tile), stores drop what falls out of bounds.
+cudaError_t make_tensor_map(CUtensorMap* map, const void* base, int64_t M, int64_t K) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -393,11 +469,11 @@ cudaError_t make_tensor_map(CUtensorMap* map, const RotArgs& a) {
     }
   });
   if (!encode) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
-  const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
   const cuuint32_t box[2] = {(cuuint32_t)kBoxCols, (cuuint32_t)kTileRows};
   const cuuint32_t elem_strides[2] = {1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.x), dims,
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                             strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -408,16 +484,22 @@ template <int FMT, int OUT, bool SWZ, int G>
 cudaError_t launch_t(const RotArgs& a, cudaStream_t stream) {
   auto kern = mx_rotate_kernel<FMT, OUT, SWZ, G>;
   const void* k = reinterpret_cast<const void*>(kern);
-  constexpr int smem = smem_request<G>();
+  constexpr int smem = smem_request<G, OUT>();
   const int64_t n_tiles = a.row_blocks * a.col_tiles;
   if (n_tiles <= 0) return cudaSuccess;
-  CUtensorMap map;
-  cudaError_t err = make_tensor_map(&map, a);
+  CUtensorMap map, ymap;
+  cudaError_t err = make_tensor_map(&map, a.x, a.M, a.K);
   if (err != cudaSuccess) return err;
+  if (OUT == kRotQdq) {
+    err = make_tensor_map(&ymap, a.out, a.M, a.K);
+    if (err != cudaSuccess) return err;
+  } else {
+    ymap = map;  // unused
+  }
   const int resident = resident_ctas(k, kThreads, smem, 1);
   if (resident <= 0) return cudaErrorInvalidConfiguration;
   const int grid = (int)(n_tiles < resident ? n_tiles : resident);
-  kern<<<grid, kThreads, smem, stream>>>(map, a);
+  kern<<<grid, kThreads, smem, stream>>>(map, ymap, a);
   return cudaGetLastError();
 }
 
