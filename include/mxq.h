@@ -32,8 +32,8 @@
  *    asynchronous.
  *  - Validation happens on the host before any launch; on error nothing is launched and the
  *    status says why. After the launch, a launch failure maps to MX_ERR_CUDA.
- *  - x, y and codes must be 32-byte aligned, swizzled scales 16-byte aligned; rows are
- *    contiguous.
+ *  - x, y and codes must be 32-byte aligned, H and swizzled scales 16-byte aligned; rows
+ *    are contiguous.
  *  - M == 0 or K == 0 is a valid empty call: nothing is launched, MX_OK is returned.
  *  - Layouts: E4M3 codes are [M, K] bytes (float8_e4m3fn). E2M1 codes are [M, K/2] bytes, two
  *    codes per byte, the lower K index in the low nibble. Linear scales are [M, K/32] bytes,
@@ -57,7 +57,7 @@ typedef int mx_status;
 #define MX_OK 0
 #define MX_ERR_NULL 1        /* a required pointer is NULL */
 #define MX_ERR_SHAPE 2       /* negative size, K % 32 != 0, K % g != 0, bad expert count */
-#define MX_ERR_ALIGN 3       /* a pointer is misaligned (x, y, codes: 32 B; scales: 16 B) */
+#define MX_ERR_ALIGN 3       /* misaligned pointer (x, y, codes: 32 B; H, scales: 16 B) */
 #define MX_ERR_UNSUPPORTED 4 /* unknown format / layout / rounding, group != 32, bad g */
 #define MX_ERR_CUDA 5        /* the CUDA runtime reported an error at launch */
 

@@ -65,7 +65,7 @@ const char* mx_status_string(mx_status status) {
     case MX_OK: return "MX_OK";
     case MX_ERR_NULL: return "MX_ERR_NULL: a required pointer is NULL";
     case MX_ERR_SHAPE: return "MX_ERR_SHAPE: invalid size (negative, K % 32, K % g, experts)";
-    case MX_ERR_ALIGN: return "MX_ERR_ALIGN: a buffer is misaligned (x, y, codes: 32 B; scales: 16 B)";
+    case MX_ERR_ALIGN: return "MX_ERR_ALIGN: a buffer is misaligned (x, y, codes: 32 B; H, scales: 16 B)";
     case MX_ERR_UNSUPPORTED: return "MX_ERR_UNSUPPORTED: format, layout, rounding, group or g";
     case MX_ERR_CUDA: return "MX_ERR_CUDA: the CUDA runtime reported an error at launch";
     default: return "unknown mx_status";
@@ -133,7 +133,7 @@ mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int ro
   if (!x || !y) return MX_ERR_NULL;
   if (!aligned32(x) || !aligned32(y)) return MX_ERR_ALIGN;
   if (H) {
-    if (reinterpret_cast<uintptr_t>(H) & 1u) return MX_ERR_ALIGN;
+    if (!aligned16(H)) return MX_ERR_ALIGN;
     return from_cuda(mxq::launch_rotate(fmt, mxq::kRotQdq, false, g, rot_args(x, M, K, H, y),
                                         static_cast<cudaStream_t>(stream)));
   }
@@ -153,7 +153,7 @@ mx_status mx_rotate_quantize(const void* x, int64_t M, int64_t K, const void* H,
   if (!x || !H || !codes || !scales) return MX_ERR_NULL;
   if (!aligned32(x) || !aligned32(codes)) return MX_ERR_ALIGN;
   if (layout == MX_SCALES_SWIZZLED && !aligned16(scales)) return MX_ERR_ALIGN;
-  if (reinterpret_cast<uintptr_t>(H) & 1u) return MX_ERR_ALIGN;
+  if (!aligned16(H)) return MX_ERR_ALIGN;
   mxq::RotArgs a = rot_args(x, M, K, H, codes);
   a.scales = static_cast<uint8_t*>(scales);
   a.scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : a.col_tiles * 4;
@@ -197,7 +197,7 @@ mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, in
   if (empty) return MX_OK;
   if (!x || !H || !y_f32) return MX_ERR_NULL;
   if (!aligned32(x) || !aligned32(y_f32)) return MX_ERR_ALIGN;
-  if (reinterpret_cast<uintptr_t>(H) & 1u) return MX_ERR_ALIGN;
+  if (!aligned16(H)) return MX_ERR_ALIGN;
   return from_cuda(mxq::launch_rotate(MX_FMT_E2M1, mxq::kRotDebug, false, g,
                                       rot_args(x, M, K, H, y_f32),
                                       static_cast<cudaStream_t>(stream)));

@@ -274,7 +274,7 @@ template <int G, int OUT>
 __host__ __device__ constexpr int smem_request() {
   // 1 KiB of slack for aligning the stage ring to 1024 bytes
   return 1024 + stages<G, OUT>() * kStageBytes + out_stage_bytes<OUT>() + G * G * 2 + 2 * 512 +
-         (2 * stages<G, OUT>() + 2 * kAcc) * 8 + 16;
+         (2 * stages<G, OUT>() + 2 * kAcc + 1) * 8 + 16;
 }
 
 template <int FMT, int OUT, bool SWZ, int G>
@@ -292,14 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + kAcc;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + kAcc);
+  uint64_t* h_ready = tempty + kAcc;  // B = H^T staged
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(h_ready + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint16_t* H = static_cast<const uint16_t*>(a.H);
-  for (int idx = tid; idx < G * G; idx += kThreads) {
-    const int k = idx / G, n = idx % G;
-    *reinterpret_cast<uint16_t*>(sB + (k / 8) * (G * 16) + n * 16 + (k % 8) * 2) = H[idx];
-  }
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(full + s), 1);
@@ -309,16 +305,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(tfull + b), 1);
       mbar_init(smem_u32(tempty + b), kEpiWarps);
     }
+    mbar_init(smem_u32(h_ready), kEpiWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (warp >= 2) {
+    // The epilogue warps stage B = H^T (all 16-byte loads in flight first) while the producer
+    // already streams the first tiles; the MMA thread waits on h_ready.
+    constexpr int kVecs = G * G / 8;
+    constexpr int kPer = (kVecs + kEpiThreads - 1) / kEpiThreads;
+    const uint4* H = static_cast<const uint4*>(a.H);
+    const int et = tid - 64;
+    uint4 hv[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int v = et + i * kEpiThreads;
+      if (v < kVecs) hv[i] = H[v];
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int v = et + i * kEpiThreads;
+      if (v < kVecs) {
+        const int k = (v * 8) / G, n0 = (v * 8) % G;  // H[k][n0 .. n0 + 7]
+        const uint32_t w[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          *reinterpret_cast<uint16_t*>(sB + (k / 8) * (G * 16) + (n0 + j) * 16 + (k % 8) * 2) =
+              (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(h_ready));
+  }
   const uint32_t tmem = *tmem_slot;
   const uint32_t sA_u32 = smem_u32(sA), sB_u32 = smem_u32(sB);
   const int64_t n_tiles = a.row_blocks * a.col_tiles;
@@ -344,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kTileRows, G);
+      mbar_wait(smem_u32(h_ready), 0, &failed);
       int it = 0;
       for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
         const int s = it % kStages, acc = it % kAcc;

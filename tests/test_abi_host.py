@@ -116,6 +116,7 @@ def test_qdq_and_rotation_validation(L):
     assert L.mx_qdq(P, 4, 64, 1, 32, 0, P, 8, P, None) == UNSUP     # g = 8
     assert L.mx_qdq(P, 4, 96, 1, 32, 0, P, 64, P, None) == SHAPE    # K % g
     assert L.mx_qdq(P, 4, 64, 1, 32, 0, P + 1, 32, P, None) == ALIGN
+    assert L.mx_qdq(P, 4, 64, 1, 32, 0, P + 8, 32, P, None) == ALIGN
     assert L.mx_qdq(P, 4, 64, 1, 32, 0, None, 0, None, None) == NULL
     assert L.mx_qdq(P, 4, 64, 1, 32, 0, None, 0, P + 2, None) == ALIGN
     assert L.mx_qdq(P, 4, 64, 1, 32, 0, None, 0, P + 16, None) == ALIGN
