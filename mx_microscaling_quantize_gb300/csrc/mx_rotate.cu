@@ -127,6 +127,12 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int 
                "r"(x), "r"(y), "r"(src)
                : "memory");
 }
+// shared -> global bulk copy in the current bulk group (16-byte aligned, size % 16 == 0)
+__device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // all committed bulk stores have finished reading shared memory
 __device__ __forceinline__ void bulk_wait_read() {
@@ -187,93 +193,59 @@ __device__ __forceinline__ void epilogue_sync() {
 }
 
 // ------------------------------------------------------------------------------------------
-// QDQ of one 32-element block of rotated values -> 32 bf16 in o[4]
+// one 32-element block of rotated values -> its output bytes and scale byte
 // ------------------------------------------------------------------------------------------
-template <int FMT>
-__device__ __forceinline__ void qdq_block_vals(float* y, uint4* o) {
-  const uint32_t byte = scale_byte_from_amax_bits<FMT>(absmax_f32x32(y));
-  const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);  // a NaN / Inf block in the warp
-  const float inv = inv_scale_of(byte), sc = scale_of(byte);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) mul2(y[2 * i], y[2 * i + 1], inv);  // y <- y / 2^s
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float* t = y + 8 * i;
-    o[i] = make_uint4(qdq2<FMT>(t[0], t[1], sc), qdq2<FMT>(t[2], t[3], sc),
-                      qdq2<FMT>(t[4], t[5], sc), qdq2<FMT>(t[6], t[7], sc));
-    if (special && byte == 255u) o[i] = make_uint4(kBf16NaNx2, kBf16NaNx2, kBf16NaNx2, kBf16NaNx2);
-  }
+// Output bytes per block: QDQ 64 (bf16), E4M3 codes 32, E2M1 codes 16.
+template <int FMT, int OUT>
+__host__ __device__ constexpr int block_out_words() {
+  return OUT == kRotQdq ? 16 : (FMT == kFmtE4M3 ? 8 : 4);
 }
 
-// ------------------------------------------------------------------------------------------
-// epilogue of one 32-element block (32 fp32 rotated values y of one tile row)
-// ------------------------------------------------------------------------------------------
 template <int FMT, int OUT>
-__device__ __forceinline__ uint32_t epilogue_block(float* y, bool row_ok, void* out, int64_t e0) {
-  if (OUT == kRotDebug) {
-    if (row_ok) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + e0);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dst[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
-    }
-    return 0u;
-  }
+__device__ __forceinline__ uint32_t block_outputs(float* y, uint32_t* out) {
   const uint32_t byte = scale_byte_from_amax_bits<FMT>(absmax_f32x32(y));
   const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);  // a NaN / Inf block in the warp
-  {
-    const float inv = inv_scale_of(byte);
+  const float inv = inv_scale_of(byte);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) mul2(y[2 * i], y[2 * i + 1], inv);  // y <- y / 2^s
-  }
+  for (int i = 0; i < 16; ++i) mul2(y[2 * i], y[2 * i + 1], inv);  // y <- y / 2^s
   if (OUT == kRotQdq) {
     const float sc = scale_of(byte);
-    uint4 o[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float* t = y + 8 * i;
-      o[i] = make_uint4(qdq2<FMT>(t[0], t[1], sc), qdq2<FMT>(t[2], t[3], sc),
-                        qdq2<FMT>(t[4], t[5], sc), qdq2<FMT>(t[6], t[7], sc));
-      if (special && byte == 255u) o[i] = make_uint4(kBf16NaNx2, kBf16NaNx2, kBf16NaNx2, kBf16NaNx2);
-    }
-    if (row_ok) {
-      uint4* dst = static_cast<uint4*>(out) + (e0 >> 3);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) __stcs(dst + i, o[i]);
-    }
+    for (int i = 0; i < 16; ++i) out[i] = qdq2<FMT>(y[2 * i], y[2 * i + 1], sc);
   } else if (FMT == kFmtE2M1) {
-    uint4 c = make_uint4(codes8_e2m1(y), codes8_e2m1(y + 8), codes8_e2m1(y + 16), codes8_e2m1(y + 24));
-    if (special && byte == 255u) c = make_uint4(0u, 0u, 0u, 0u);
-    if (row_ok) __stcs(reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + (e0 >> 1)), c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = codes8_e2m1(y + 8 * i);
   } else {
-    uint2 c[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      c[i] = codes8_e4m3(y + 8 * i);
-      if (special && byte == 255u) c[i] = make_uint2(kE4M3NaNx4, kE4M3NaNx4);
+      const uint2 c = codes8_e4m3(y + 8 * i);
+      out[2 * i] = c.x;
+      out[2 * i + 1] = c.y;
     }
-    if (row_ok) {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + e0);
-      __stcs(dst, make_uint4(c[0].x, c[0].y, c[1].x, c[1].y));
-      __stcs(dst + 1, make_uint4(c[2].x, c[2].y, c[3].x, c[3].y));
-    }
+  }
+  if (special && byte == 255u) {
+    const uint32_t fill = OUT == kRotQdq ? kBf16NaNx2 : (FMT == kFmtE2M1 ? 0u : kE4M3NaNx4);
+#pragma unroll
+    for (int i = 0; i < block_out_words<FMT, OUT>(); ++i) out[i] = fill;
   }
   return byte;
 }
 
-// shared-memory stages in flight: as many 32 KiB tiles as fit beside H^T
+// shared-memory stages in flight: as many 32 KiB tiles as fit beside H^T and the output tile
 template <int G, int OUT>
 __host__ __device__ constexpr int stages() {
-  return (G == 128 || OUT == kRotQdq) ? 5 : 6;
+  return (G == 128 || OUT != kRotCodes) ? 5 : 6;
 }
-// QDQ outputs are staged in shared memory (one 32 KiB tile) and written back with TMA stores
-template <int OUT>
+// Output tile staged in shared memory and written back with TMA: 128 rows of 128 bf16 (QDQ),
+// 128 E4M3 bytes or 64 E2M1 bytes.
+template <int FMT, int OUT>
 __host__ __device__ constexpr int out_stage_bytes() {
-  return OUT == kRotQdq ? kStageBytes : 0;
+  return OUT == kRotDebug ? 0 : kTileRows * block_out_words<FMT, OUT>() * 4 * 4;
 }
-template <int G, int OUT>
+template <int FMT, int G, int OUT>
 __host__ __device__ constexpr int smem_request() {
   // 1 KiB of slack for aligning the stage ring to 1024 bytes
-  return 1024 + stages<G, OUT>() * kStageBytes + out_stage_bytes<OUT>() + G * G * 2 + 2 * 512 +
+  return 1024 + stages<G, OUT>() * kStageBytes + out_stage_bytes<FMT, OUT>() + G * G * 2 + 512 +
          (2 * stages<G, OUT>() + 2 * kAcc + 1) * 8 + 16;
 }
 
@@ -285,10 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;                                  // kStages x (two swizzled boxes)
-  uint8_t* sOut = smem + kStages * kStageBytes;        // QDQ output tile (two swizzled boxes)
-  uint8_t* sB = sOut + out_stage_bytes<OUT>();         // H^T, core-matrix layout
-  uint8_t* s_scale = sB + G * G * 2;                   // [2][512] swizzled scale tiles
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_scale + 2 * 512);
+  uint8_t* sOut = smem + kStages * kStageBytes;        // output tile, written back by TMA
+  uint8_t* sB = sOut + out_stage_bytes<FMT, OUT>();    // H^T, core-matrix layout
+  uint8_t* s_scale = sB + G * G * 2;                   // the tile's swizzled scales
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_scale + 512);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + kAcc;
@@ -397,11 +369,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- epilogue warps ----------------
+    // Thread (quad, lane) owns tile row r = 32 * quad + lane and, in warp quarter q, the
+    // 32-column block q. Each tile: read the block's fp32 values from TMEM, free the
+    // accumulator, convert, write the block's output bytes into the staged output tile, then
+    // one thread writes the tile (and the swizzled scale tile) back with TMA / bulk stores.
     const int e = warp - 2;
     const int quad = warp & 3;          // TMEM lanes 32*quad .. +31 = tile rows
     const int q = e >> 2;               // the 32-column block of the tile this warp converts
     const int r = quad * 32 + lane;     // tile row of this thread
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    constexpr int kWords = block_out_words<FMT, OUT>();
     int it = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
       const int acc = it % kAcc;
@@ -410,67 +387,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t kc64 = a.K - cb * kTileCols;
       const int kc = kc64 > kTileCols ? kTileCols : (int)kc64;
       const bool row_ok = row0 + r < a.M;
-      uint8_t* tile_scales = s_scale + (it & 1) * 512;
+      const bool active = q * 32 < kc;  // this warp's 32 columns exist in the tile
       mbar_wait(smem_u32(tfull + acc), (it / kAcc) & 1, &failed);
       tc_fence_after();
-      const bool active = q * 32 < kc;  // this warp's 32 columns exist in the tile
-      if (OUT == kRotQdq) {
-        uint4 o[4];
-        if (active) {
-          float y[32];
-          tmem_ld32(lane_base + (uint32_t)(acc * 128 + q * 32), y);
-          qdq_block_vals<FMT>(y, o);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(tempty + acc));  // accumulator free for tile it + kAcc
-        // the previous tile's TMA store has read the staging tile before anyone overwrites it
-        if (e == 0 && lane == 0) bulk_wait_read();
-        epilogue_sync();
-        if (active) {
-          // row r, 16-byte chunk c of box q/2 sits at chunk c ^ (r % 8) (128-byte swizzle)
-          uint8_t* box = sOut + (q >> 1) * kBoxBytes + r * 128;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int c = (q & 1) * 4 + k;
-            *reinterpret_cast<uint4*>(box + ((c ^ (r & 7)) << 4)) = o[k];
-          }
-        }
-        fence_proxy_async_smem();
-        epilogue_sync();
-        if (e == 0 && lane == 0) {
-          const uint32_t src = smem_u32(sOut);
-          tma_store_2d(&ymap, (int)(cb * kTileCols), (int)row0, src);  // rows >= M are clipped
-          if (kc > kBoxCols) tma_store_2d(&ymap, (int)(cb * kTileCols + kBoxCols), (int)row0, src + kBoxBytes);
-          bulk_commit();
-        }
-        continue;
-      }
-      if (!active) {
-        if (SWZ && OUT == kRotCodes) tile_scales[swizzle_in_tile(r, q)] = 0;
-      } else {
-        float y[32];
-        tmem_ld32(lane_base + (uint32_t)(acc * 128 + q * 32), y);
-        const int64_t e0 = (row0 + r) * a.K + cb * kTileCols + q * 32;  // block's first element
-        const uint32_t byte = epilogue_block<FMT, OUT>(y, row_ok, a.out, e0);
-        if (OUT == kRotCodes) {
-          if (SWZ) tile_scales[swizzle_in_tile(r, q)] = (uint8_t)byte;  // pad rows: 0
-          else if (row_ok) a.scales[(row0 + r) * a.scale_cols + cb * 4 + q] = (uint8_t)byte;
-        }
-      }
+      float y[32];
+      if (active) tmem_ld32(lane_base + (uint32_t)(acc * 128 + q * 32), y);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(tempty + acc));  // accumulator free for tile it + kAcc
-      if (SWZ && OUT == kRotCodes) {
-        epilogue_sync();  // the tile's 512 scale bytes are complete
-        if (e == 0) {
-          uint4* dst = reinterpret_cast<uint4*>(a.scales + t * 512);
-          dst[lane] = reinterpret_cast<const uint4*>(tile_scales)[lane];
+      if (OUT == kRotDebug) {
+        if (active && row_ok) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) +
+                                                  (row0 + r) * a.K + cb * kTileCols + q * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) dst[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
         }
+        continue;
+      }
+      uint32_t o[kWords];
+      uint32_t byte = 0;  // pad rows / columns of the swizzled scale tile stay zero
+      if (active) byte = block_outputs<FMT, OUT>(y, o);
+      if (!SWZ && active && row_ok) a.scales[(row0 + r) * a.scale_cols + cb * 4 + q] = (uint8_t)byte;
+      // the previous tile's stores have read the staged tiles before anyone overwrites them
+      if (e == 0 && lane == 0) bulk_wait_read();
+      epilogue_sync();
+      if (active) {
+        if (OUT == kRotQdq) {
+          // two 128-byte-swizzled boxes of 64 bf16 per row: chunk c of row r at c ^ (r % 8)
+          uint8_t* row = sOut + (q >> 1) * kBoxBytes + r * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int c = (q & 1) * 4 + k;
+            *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
+                make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+          }
+        } else if (FMT == kFmtE4M3) {
+          // one 128-byte-swizzled box of 128 code bytes per row
+          uint8_t* row = sOut + r * 128;
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int c = 2 * q + k;
+            *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
+                make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+          }
+        } else {
+          // one 64-byte-swizzled box of 64 code bytes per row: chunk c at c ^ ((r / 2) % 4)
+          *reinterpret_cast<uint4*>(sOut + r * 64 + ((q ^ ((r >> 1) & 3)) << 4)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      if (SWZ) s_scale[swizzle_in_tile(r, q)] = (uint8_t)byte;
+      fence_proxy_async_smem();
+      epilogue_sync();
+      if (e == 0 && lane == 0) {
+        const uint32_t src = smem_u32(sOut);
+        if (OUT == kRotQdq) {  // rows >= M and columns >= K are dropped by the TMA
+          tma_store_2d(&ymap, (int)(cb * kTileCols), (int)row0, src);
+          if (kc > kBoxCols) tma_store_2d(&ymap, (int)(cb * kTileCols + kBoxCols), (int)row0, src + kBoxBytes);
+        } else if (FMT == kFmtE4M3) {
+          tma_store_2d(&ymap, (int)(cb * kTileCols), (int)row0, src);
+        } else {
+          tma_store_2d(&ymap, (int)(cb * kTileCols / 2), (int)row0, src);
+        }
+        if (SWZ) bulk_store_s2g(a.scales + t * 512, smem_u32(s_scale), 512);
+        bulk_commit();
       }
     }
   }
-  if (OUT == kRotQdq && warp == 2 && lane == 0) bulk_wait_all();
+  if (OUT != kRotDebug && warp == 2 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -480,10 +464,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------
-// Tensor map of a bf16 [M rows, K columns] matrix (x, or the QDQ output y): boxes of 128 rows
-// x 64 columns, 128-byte swizzle; loads read zeros out of bounds (pad rows, a short last column
-// tile), stores drop what falls out of bounds.
-cudaError_t make_tensor_map(CUtensorMap* map, const void* base, int64_t M, int64_t K) {
+// Tensor map of a row-major [rows, cols] matrix of 1- or 2-byte elements, boxes of box_rows x
+// box_cols, the given swizzle; loads read zeros out of bounds, stores drop what falls outside.
+cudaError_t make_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                            CUtensorMapDataType type, int elem_bytes, int box_cols,
+                            CUtensorMapSwizzle swizzle) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -496,14 +481,13 @@ cudaError_t make_tensor_map(CUtensorMap* map, const void* base, int64_t M, int64
     }
   });
   if (!encode) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kBoxCols, (cuuint32_t)kTileRows};
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * elem_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)kTileRows};
   const cuuint32_t elem_strides[2] = {1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                            strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = encode(map, type, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -511,18 +495,26 @@ template <int FMT, int OUT, bool SWZ, int G>
 cudaError_t launch_t(const RotArgs& a, cudaStream_t stream) {
   auto kern = mx_rotate_kernel<FMT, OUT, SWZ, G>;
   const void* k = reinterpret_cast<const void*>(kern);
-  constexpr int smem = smem_request<G, OUT>();
+  constexpr int smem = smem_request<FMT, G, OUT>();
   const int64_t n_tiles = a.row_blocks * a.col_tiles;
   if (n_tiles <= 0) return cudaSuccess;
   CUtensorMap map, ymap;
-  cudaError_t err = make_tensor_map(&map, a.x, a.M, a.K);
+  cudaError_t err = make_tensor_map(&map, a.x, a.M, a.K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                    kBoxCols, CU_TENSOR_MAP_SWIZZLE_128B);
   if (err != cudaSuccess) return err;
-  if (OUT == kRotQdq) {
-    err = make_tensor_map(&ymap, a.out, a.M, a.K);
-    if (err != cudaSuccess) return err;
+  if (OUT == kRotQdq) {  // bf16 [M, K]
+    err = make_tensor_map(&ymap, a.out, a.M, a.K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kBoxCols,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  } else if (OUT == kRotCodes && FMT == kFmtE4M3) {  // E4M3 bytes [M, K]
+    err = make_tensor_map(&ymap, a.out, a.M, a.K, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  } else if (OUT == kRotCodes) {  // E2M1 bytes [M, K / 2]
+    err = make_tensor_map(&ymap, a.out, a.M, a.K / 2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64,
+                          CU_TENSOR_MAP_SWIZZLE_64B);
   } else {
     ymap = map;  // unused
   }
+  if (err != cudaSuccess) return err;
   const int resident = resident_ctas(k, kThreads, smem, 1);
   if (resident <= 0) return cudaErrorInvalidConfiguration;
   const int grid = (int)(n_tiles < resident ? n_tiles : resident);
