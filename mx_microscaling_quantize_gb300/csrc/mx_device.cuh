@@ -95,16 +95,18 @@ __device__ __forceinline__ uint32_t absmax_f32x32(const float* y) {
 // ------------------------------------------------------------------------------------------
 // 8 scaled fp32 values t[0..8) (lower K index first) -> codes
 // ------------------------------------------------------------------------------------------
+// The four code bytes are widened and shifted into place; the vector form of mov from four
+// 8-bit registers is not used (one kernel was seen to get zeros from it).
 __device__ __forceinline__ uint32_t codes8_e2m1(const float* t) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 c0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 c1, %4, %3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 c2, %6, %5;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 c3, %8, %7;\n\t"
-      "mov.b32 %0, {c0, c1, c2, c3};\n\t}"
-      : "=r"(r)
-      : "f"(t[0]), "f"(t[1]), "f"(t[2]), "f"(t[3]), "f"(t[4]), "f"(t[5]), "f"(t[6]), "f"(t[7]));
+  uint32_t r = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t b;
+    asm("{\n\t.reg .b8 c;\n\tcvt.rn.satfinite.e2m1x2.f32 c, %1, %2;\n\tcvt.u32.u8 %0, c;\n\t}"
+        : "=r"(b)
+        : "f"(t[2 * j + 1]), "f"(t[2 * j]));
+    r |= b << (8 * j);
+  }
   return r;
 }
 

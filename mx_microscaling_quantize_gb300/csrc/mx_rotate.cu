@@ -407,7 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t o[kWords];
       uint32_t byte = 0;  // pad rows / columns of the swizzled scale tile stay zero
       if (active) byte = block_outputs<FMT, OUT>(y, o);
-      if (!SWZ && active && row_ok) a.scales[(row0 + r) * a.scale_cols + cb * 4 + q] = (uint8_t)byte;
+      if (OUT == kRotCodes && !SWZ && active && row_ok) {
+        a.scales[(row0 + r) * a.scale_cols + cb * 4 + q] = (uint8_t)byte;  // linear scales
+      }
       // the previous tile's stores have read the staged tiles before anyone overwrites them
       if (e == 0 && lane == 0) bulk_wait_read();
       epilogue_sync();
@@ -436,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
-      if (SWZ) s_scale[swizzle_in_tile(r, q)] = (uint8_t)byte;
+      if (OUT == kRotCodes && SWZ) s_scale[swizzle_in_tile(r, q)] = (uint8_t)byte;
       fence_proxy_async_smem();
       epilogue_sync();
       if (e == 0 && lane == 0) {
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           tma_store_2d(&ymap, (int)(cb * kTileCols / 2), (int)row0, src);
         }
-        if (SWZ) bulk_store_s2g(a.scales + t * 512, smem_u32(s_scale), 512);
+        if (OUT == kRotCodes && SWZ) bulk_store_s2g(a.scales + t * 512, smem_u32(s_scale), 512);
         bulk_commit();
       }
     }
