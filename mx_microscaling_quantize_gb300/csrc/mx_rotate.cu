@@ -134,9 +134,9 @@ __device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t src, uint32_t
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// all committed bulk stores have finished reading shared memory
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// all committed bulk store groups but the most recent one have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // all committed bulk stores are complete
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -232,12 +232,12 @@ __device__ __forceinline__ uint32_t block_outputs(float* y, uint32_t* out) {
 }
 
 // shared-memory stages in flight: as many 32 KiB tiles as fit beside H^T and the output tile
-template <int G, int OUT>
+template <int FMT, int G, int OUT>
 __host__ __device__ constexpr int stages() {
-  return (G == 128 || OUT != kRotCodes) ? 5 : 6;
+  return OUT == kRotQdq ? 4 : ((G == 128 || OUT == kRotDebug || FMT == kFmtE4M3) ? 5 : 6);
 }
 // Output tile staged in shared memory and written back with TMA: 128 rows of 128 bf16 (QDQ),
-// 128 E4M3 bytes or 64 E2M1 bytes.
+// 128 E4M3 bytes or 64 E2M1 bytes. Two such buffers alternate between tiles.
 template <int FMT, int OUT>
 __host__ __device__ constexpr int out_stage_bytes() {
   return OUT == kRotDebug ? 0 : kTileRows * block_out_words<FMT, OUT>() * 4 * 4;
@@ -245,22 +245,24 @@ __host__ __device__ constexpr int out_stage_bytes() {
 template <int FMT, int G, int OUT>
 __host__ __device__ constexpr int smem_request() {
   // 1 KiB of slack for aligning the stage ring to 1024 bytes
-  return 1024 + stages<G, OUT>() * kStageBytes + out_stage_bytes<FMT, OUT>() + G * G * 2 + 512 +
-         (2 * stages<G, OUT>() + 2 * kAcc + 1) * 8 + 16;
+  return 1024 + stages<FMT, G, OUT>() * kStageBytes + 2 * out_stage_bytes<FMT, OUT>() + G * G * 2 +
+         2 * 512 + (2 * stages<FMT, G, OUT>() + 2 * kAcc + 1) * 8 + 16;
 }
+constexpr int kMaxSmemPerCta = 232448;  // opt-in dynamic shared memory limit of the SM
 
 template <int FMT, int OUT, bool SWZ, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_rotate_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap ymap,
                      RotArgs a) {
-  constexpr int kStages = stages<G, OUT>();
+  constexpr int kStages = stages<FMT, G, OUT>();
+  static_assert(smem_request<FMT, G, OUT>() <= kMaxSmemPerCta, "shared memory budget");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;                                  // kStages x (two swizzled boxes)
-  uint8_t* sOut = smem + kStages * kStageBytes;        // output tile, written back by TMA
-  uint8_t* sB = sOut + out_stage_bytes<FMT, OUT>();    // H^T, core-matrix layout
-  uint8_t* s_scale = sB + G * G * 2;                   // the tile's swizzled scales
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_scale + 512);
+  uint8_t* sOut = smem + kStages * kStageBytes;        // [2] output tiles, written back by TMA
+  uint8_t* sB = sOut + 2 * out_stage_bytes<FMT, OUT>();  // H^T, core-matrix layout
+  uint8_t* s_scale = sB + G * G * 2;                     // [2][512] swizzled scale tiles
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_scale + 2 * 512);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + kAcc;
@@ -410,13 +412,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (OUT == kRotCodes && !SWZ && active && row_ok) {
         a.scales[(row0 + r) * a.scale_cols + cb * 4 + q] = (uint8_t)byte;  // linear scales
       }
-      // the previous tile's stores have read the staged tiles before anyone overwrites them
-      if (e == 0 && lane == 0) bulk_wait_read();
+      // staged tiles alternate; the stores issued two tiles ago (same buffers) have read them
+      uint8_t* out_tile = sOut + (it & 1) * out_stage_bytes<FMT, OUT>();
+      uint8_t* scale_tile = s_scale + (it & 1) * 512;
+      if (e == 0 && lane == 0) bulk_wait_read_all_but_one();
       epilogue_sync();
       if (active) {
         if (OUT == kRotQdq) {
           // two 128-byte-swizzled boxes of 64 bf16 per row: chunk c of row r at c ^ (r % 8)
-          uint8_t* row = sOut + (q >> 1) * kBoxBytes + r * 128;
+          uint8_t* row = out_tile + (q >> 1) * kBoxBytes + r * 128;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int c = (q & 1) * 4 + k;
@@ -425,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else if (FMT == kFmtE4M3) {
           // one 128-byte-swizzled box of 128 code bytes per row
-          uint8_t* row = sOut + r * 128;
+          uint8_t* row = out_tile + r * 128;
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             const int c = 2 * q + k;
@@ -434,15 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           // one 64-byte-swizzled box of 64 code bytes per row: chunk c at c ^ ((r / 2) % 4)
-          *reinterpret_cast<uint4*>(sOut + r * 64 + ((q ^ ((r >> 1) & 3)) << 4)) =
+          *reinterpret_cast<uint4*>(out_tile + r * 64 + ((q ^ ((r >> 1) & 3)) << 4)) =
               make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
-      if (OUT == kRotCodes && SWZ) s_scale[swizzle_in_tile(r, q)] = (uint8_t)byte;
+      if (OUT == kRotCodes && SWZ) scale_tile[swizzle_in_tile(r, q)] = (uint8_t)byte;
       fence_proxy_async_smem();
       epilogue_sync();
       if (e == 0 && lane == 0) {
-        const uint32_t src = smem_u32(sOut);
+        const uint32_t src = smem_u32(out_tile);
         if (OUT == kRotQdq) {  // rows >= M and columns >= K are dropped by the TMA
           tma_store_2d(&ymap, (int)(cb * kTileCols), (int)row0, src);
           if (kc > kBoxCols) tma_store_2d(&ymap, (int)(cb * kTileCols + kBoxCols), (int)row0, src + kBoxBytes);
@@ -451,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           tma_store_2d(&ymap, (int)(cb * kTileCols / 2), (int)row0, src);
         }
-        if (OUT == kRotCodes && SWZ) bulk_store_s2g(a.scales + t * 512, smem_u32(s_scale), 512);
+        if (OUT == kRotCodes && SWZ) bulk_store_s2g(a.scales + t * 512, smem_u32(scale_tile), 512);
         bulk_commit();
       }
     }
