@@ -2,8 +2,8 @@
 //
 // The input [M, K] is contiguous and K % 32 == 0, so it is a flat sequence of 32-element
 // blocks; codes and QDQ outputs are flat sequences too, and linear scales are indexed by the
-// flat block number. A persistent grid walks the blocks with a grid stride: consecutive
-// threads own consecutive blocks (a warp moves 2 KiB of contiguous input with 32-byte vector
+// flat block number. A persistent grid walks the blocks with a grid stride (grouped calls: one
+// contiguous range per CTA): consecutive threads own consecutive blocks (a warp moves 2 KiB of contiguous input with 32-byte vector
 // loads), and each thread loads its next block before working on the current one. A thread
 // takes the block's abs-max with packed bf16x2 abs-max instructions, derives the E8M0 byte
 // from the exponent field, converts in registers with the hardware paired converters, and
@@ -183,18 +183,31 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
   const uint8_t* x = static_cast<const uint8_t*>(a.x);
   const int64_t cblk = a.K >> 5;  // blocks per row
   const int64_t nblk = a.M * cblk;
-  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  // Plain calls walk the blocks with a grid stride. Grouped calls give each CTA one contiguous
+  // range, so that a thread's row advances by only kThreads / (K/32) rows per step and its
+  // expert can be tracked incrementally instead of searched for every block.
+  int64_t b, b_end, stride;
+  if (GROUPED) {
+    const int64_t per_cta = ((nblk + gridDim.x - 1) / gridDim.x + kThreads - 1) / kThreads * kThreads;
+    b = (int64_t)blockIdx.x * per_cta + tid;
+    b_end = (int64_t)(blockIdx.x + 1) * per_cta < nblk ? (int64_t)(blockIdx.x + 1) * per_cta : nblk;
+    stride = kThreads;
+  } else {
+    b = (int64_t)blockIdx.x * kThreads + tid;
+    b_end = nblk;
+    stride = (int64_t)gridDim.x * kThreads;
+  }
   const int64_t row_step = stride / cblk, col_step = stride - row_step * cblk;
-  int64_t b = (int64_t)blockIdx.x * kThreads + tid;
   int64_t row = b / cblk, col = b - row * cblk;  // advanced incrementally below
+  int e = GROUPED ? last_not_above(s_off, a.E, row) : 0;  // expert of `row` (grouped)
   uint32_t cur[16], nxt[16];
-  if (b < nblk) {
+  if (b < b_end) {
     load32B(x + b * 64, cur);
     load32B(x + b * 64 + 32, cur + 8);
   }
-  for (; b < nblk; b += stride) {
+  for (; b < b_end; b += stride) {
     const int64_t bn = b + stride;
-    if (bn < nblk) {  // next block in flight while this one is converted
+    if (bn < b_end) {  // next block in flight while this one is converted
       load32B(x + bn * 64, nxt);
       load32B(x + bn * 64 + 32, nxt + 8);
     }
@@ -207,7 +220,7 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
         int64_t pr = row;
         bool ok = true;
         if (GROUPED) {
-          const int e = last_not_above(s_off, a.E, row);
+          while (e + 1 < a.E && row >= s_off[e + 1]) ++e;  // rows only grow within a thread
           ok = row >= s_off[e] && row < s_off[e + 1];
           pr = s_prow[e] + (row - s_off[e]);
           ok = ok && pr < a.scale_rows;
@@ -228,7 +241,8 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
   if (SWZ && !QDQ) {
     // zero the pad bytes of the swizzled buffer: whole pad rows, and columns past K/32
     const int64_t cp = a.scale_cols;
-    for (int64_t pr = (int64_t)blockIdx.x * kThreads + tid; pr < a.scale_rows; pr += stride) {
+    const int64_t pad_stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t pr = (int64_t)blockIdx.x * kThreads + tid; pr < a.scale_rows; pr += pad_stride) {
       int64_t data_cols = pr < a.M ? cblk : 0;
       if (GROUPED) {
         data_cols = 0;
