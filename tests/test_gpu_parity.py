@@ -304,3 +304,44 @@ def test_rotation_sweep_full_size_sampled_rows():
         for fmt in FMTS:
             out = T.bf16_bits(mxq.mx_qdq(x, fmt, T.to_gpu(H))[torch.from_numpy(rows).cuda()])
             T.check_rotated_qdq(xb[rows], H, fmt, out)
+
+
+def test_calls_capture_into_a_cuda_graph():
+    """The entry points allocate and synchronize nothing, so they can be captured in a CUDA
+    graph (the CuTe QDQ page's requirement); replays equal eager calls bit for bit."""
+    xb = W.rotation_sweep_input("attn_in", 512, 2048)
+    x = T.to_gpu(xb)
+    H = T.to_gpu(rotation(32))
+    xm, off = W.moe_quant(E=8, tokens=700, K=256)
+    xg, offs = T.to_gpu(xm), torch.from_numpy(off).cuda()
+    # warm up on a side stream (first calls set kernel attributes), then capture
+    y = torch.empty_like(x)
+    yr = torch.empty_like(x)
+    c, s = mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED)
+    cg, sg = mxq.mx_quantize_grouped(xg, offs, mxq.E4M3, mxq.SWIZZLED)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        mxq.mx_qdq(x, mxq.E2M1, y=y)
+        mxq.mx_qdq(x, mxq.E4M3, H, y=yr)
+        mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, codes=c, scales=s)
+        mxq.mx_quantize_grouped(xg, offs, mxq.E4M3, mxq.SWIZZLED, codes=cg, scales=sg)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (y, yr, c, s, cg, sg)]
+    for t in (y, yr, c, s, cg, sg):
+        t.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        mxq.mx_qdq(x, mxq.E2M1, y=y)
+        mxq.mx_qdq(x, mxq.E4M3, H, y=yr)
+        mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, codes=c, scales=s)
+        mxq.mx_quantize_grouped(xg, offs, mxq.E4M3, mxq.SWIZZLED, codes=cg, scales=sg)
+    for _ in range(2):
+        for t in (y, yr, c, s, cg, sg):
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for got, want in zip((y, yr, c, s, cg, sg), eager):
+            assert torch.equal(got.view(torch.uint8), want.view(torch.uint8))
+    np.testing.assert_array_equal(T.bf16_bits(y), O.qdq(xb, O.E2M1))
