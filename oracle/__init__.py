@@ -60,6 +60,7 @@ def _load():
         "mxo_scales_shape": (None, [i64, i64, i32, p, p]),
         "mxo_quantize": (None, [p, i64, i64, i32, i32, p, p]),
         "mxo_qdq": (None, [p, i64, i64, i32, p]),
+        "mxo_dequantize": (None, [p, p, i64, i64, i32, i32, p]),
         "mxo_rotate": (None, [p, i64, i64, p, i32, p]),
         "mxo_rotate_quantize": (None, [p, i64, i64, p, i32, i32, i32, p, p]),
         "mxo_rotate_qdq": (None, [p, i64, i64, p, i32, i32, p]),
@@ -163,6 +164,19 @@ def qdq(x_bits, fmt: int) -> np.ndarray:
     M, K = x.shape
     out = np.zeros((M, K), dtype=np.uint16)
     _load().mxo_qdq(_ptr(x), M, K, fmt, _ptr(out))
+    return out
+
+
+def dequantize(codes, scales, K: int, fmt: int, layout: int) -> np.ndarray:
+    """codes [M, K or K/2] uint8 and scales (linear [M, K/32] or swizzled) -> bf16 bits [M, K].
+    Scale byte 0xFF and E4M3 NaN codes give the bf16 NaN 0x7FC0."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    M = c.shape[0]
+    assert c.shape[1] == code_bytes_per_row(fmt, K)
+    s = np.ascontiguousarray(scales, dtype=np.uint8)
+    assert s.shape == scales_shape(M, K, layout)
+    out = np.zeros((M, K), dtype=np.uint16)
+    _load().mxo_dequantize(_ptr(c), _ptr(s), M, K, fmt, layout, _ptr(out))
     return out
 
 

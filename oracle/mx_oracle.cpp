@@ -189,8 +189,11 @@ int quantize_block(const ElementFormat& f, const double* v, int n, int forced_by
   return byte;
 }
 
+// Value of one code at scale 2^0. E4M3 S.1111.111 (0x7F, 0xFF) is the format's NaN.
 double decode_code(const ElementFormat& f, int code) {
-  double mag = f.magnitude[code & (f.sign_bit - 1)];
+  int magnitude_code = code & (f.sign_bit - 1);
+  if (magnitude_code >= f.n_magnitudes) return NAN;
+  double mag = f.magnitude[magnitude_code];
   return (code & f.sign_bit) ? -mag : mag;
 }
 
@@ -251,6 +254,29 @@ void qdq_rows(const ElementFormat& f, const double* v, int64_t rows, int64_t K, 
       int byte = quantize_block(f, v + r * K + j * 32, 32, -1, block_codes);
       for (int i = 0; i < 32; ++i) {
         out[r * K + j * 32 + i] = dequant_to_bf16(f, block_codes[i], byte);
+      }
+    }
+  }
+}
+
+// Dequantize [rows, K] codes (E4M3: one byte each; E2M1: two per byte, the lower K index in the
+// low nibble) under their block scales (linear [rows, K/32] or swizzled) into bf16.
+void dequantize_rows(const ElementFormat& f, const uint8_t* codes, const uint8_t* scales,
+                     int64_t rows, int64_t K, int layout, int64_t padded_cols, uint16_t* out) {
+  const int64_t groups = K / 32;
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t j = 0; j < groups; ++j) {
+      int byte = (layout == 0) ? scales[r * groups + j] : scales[swizzled_offset(r, j, padded_cols)];
+      for (int i = 0; i < 32; ++i) {
+        int64_t k = j * 32 + i;
+        int code;
+        if (f.sign_bit == 0x80) {
+          code = codes[r * K + k];
+        } else {
+          uint8_t b = codes[r * (K / 2) + k / 2];
+          code = (k % 2 == 0) ? (b & 0x0F) : (b >> 4);
+        }
+        out[r * K + k] = dequant_to_bf16(f, code, byte);
       }
     }
   }
@@ -333,6 +359,14 @@ void mxo_quantize(const uint16_t* x, int64_t M, int64_t K, int fmt, int layout, 
 void mxo_qdq(const uint16_t* x, int64_t M, int64_t K, int fmt, uint16_t* out) {
   std::vector<double> v = decode_rows(x, M, K);
   qdq_rows(*format_of(fmt), v.data(), M, K, out);
+}
+
+// codes / scales as mxo_quantize writes them -> bf16 bits [M, K].
+void mxo_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int64_t K, int fmt,
+                    int layout, uint16_t* out) {
+  int64_t srows, scols;
+  mxo_scales_shape(M, K, layout, &srows, &scols);
+  dequantize_rows(*format_of(fmt), codes, scales, M, K, layout, scols, out);
 }
 
 void mxo_rotate(const uint16_t* x, int64_t M, int64_t K, const uint16_t* H, int g, double* y) {

@@ -50,7 +50,8 @@ def test_e4m3_decode_matches_torch_all_bytes():
     ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
     for c in range(256):
         if c & 0x7F == 0x7F:
-            assert np.isnan(ref[c])  # the format's only NaN; the oracle never emits it
+            assert np.isnan(ref[c])  # the format's only NaN; quantization never emits it
+            assert np.isnan(O.decode(O.E4M3, c))
             continue
         assert O.decode(O.E4M3, c) == ref[c], hex(c)
         assert math.copysign(1.0, O.decode(O.E4M3, c)) == math.copysign(1.0, ref[c])
@@ -264,6 +265,84 @@ def test_qdq_equals_dequantized_codes():
                 else:
                     c = (codes[r, k // 2] >> (4 * (k % 2))) & 0xF
                 assert out[r, k] == O.dequant_bf16(fmt, int(c), int(scales[r, k // 32]))
+
+
+# ---------------------------------------------------------------------------------------------
+# dequantization of stored codes and scales
+# ---------------------------------------------------------------------------------------------
+E2M1_SPEC_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # OCP MX E2M1 magnitudes, codes 0..7
+
+
+def torch_bf16_bits(values: torch.Tensor) -> np.ndarray:
+    return values.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("layout", [O.LINEAR, O.SWIZZLED])
+@pytest.mark.parametrize("M,K", [(1, 32), (130, 416), (64, 4096)])
+def test_dequantize_of_quantize_is_qdq(M, K, layout):
+    x = W.mxfp4_qdq_activation(M, K) if K % 1024 == 0 else W.mxfp8_linear_quant(M, K, stream=K)
+    for fmt in (O.E2M1, O.E4M3):
+        codes, scales = O.quantize(x, fmt, layout)
+        np.testing.assert_array_equal(O.dequantize(codes, scales, K, fmt, layout), O.qdq(x, fmt))
+
+
+def test_dequantize_e4m3_every_code_and_scale_against_torch():
+    """Random E4M3 bytes (NaN codes included) under every E8M0 byte: torch's float8_e4m3fn and
+    float8_e8m0fnu decodes, multiplied in float64 (exact) and cast once to bfloat16."""
+    rng = np.random.default_rng(21)
+    M, K = 256, 1024
+    codes = rng.integers(0, 256, (M, K), dtype=np.uint8)
+    codes[0, :256] = np.arange(256, dtype=np.uint8)
+    scales = rng.integers(0, 256, (M, K // 32), dtype=np.uint8)
+    scales[1:, 0] = np.arange(255, dtype=np.uint8)
+    v = torch.from_numpy(codes).view(torch.float8_e4m3fn).double()
+    s = torch.from_numpy(scales).view(torch.float8_e8m0fnu).double().repeat_interleave(32, dim=1)
+    want = torch_bf16_bits(v * s)
+    got = O.dequantize(codes, scales, K, O.E4M3, O.LINEAR)
+    nan = np.isnan((v * s).numpy())
+    assert nan.any() and (got[nan] == 0x7FC0).all()
+    np.testing.assert_array_equal(got[~nan], want[~nan])
+    assert (got == 0x7F80).any() and (got == 0x0000).any()  # overflow to Inf and underflow hit
+
+
+def test_dequantize_e2m1_nibbles_against_spec_table():
+    """Packed E2M1 bytes: the even K index in the low nibble, magnitudes from the OCP table,
+    sign bit 0x8; scales read through the 128x4 blocked layout give the same values."""
+    rng = np.random.default_rng(22)
+    M, K = 200, 640
+    packed = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    scales = rng.integers(0, 256, (M, K // 32), dtype=np.uint8)
+    nib = np.empty((M, K), dtype=np.int64)
+    nib[:, 0::2] = packed & 0xF
+    nib[:, 1::2] = packed >> 4
+    table = np.array(E2M1_SPEC_VALUES + [-v for v in E2M1_SPEC_VALUES])
+    v = torch.from_numpy(table[nib])
+    s = torch.from_numpy(scales).view(torch.float8_e8m0fnu).double().repeat_interleave(32, dim=1)
+    want = torch_bf16_bits(v * s)
+    want[np.isnan((v * s).numpy())] = 0x7FC0
+    np.testing.assert_array_equal(O.dequantize(packed, scales, K, O.E2M1, O.LINEAR), want)
+    swz = to_blocked_reference(torch.from_numpy(scales)).numpy()
+    swz = swz.reshape(O.scales_shape(M, K, O.SWIZZLED))
+    np.testing.assert_array_equal(O.dequantize(packed, swz, K, O.E2M1, O.SWIZZLED), want)
+
+
+def test_dequantize_subnormal_and_overflow_closed_forms():
+    """Worked by hand: bf16 subnormals are m * 2^-133. E4M3 0x0F = 1.875 * 2^-6 under 2^-127 is
+    1.875 * 2^-133 -> 2 * 2^-133 (0x0002); 0x0C = 1.5 * 2^-133 ties to even -> 0x0002; 0x09 ->
+    0x0001; 0x01 = 2^-136 -> +0; 0x8F -> 0x8002. E2M1 6 * 2^127 overflows to Inf (0x7F80,
+    0xFF80 for code 0xF); E4M3 448 * 2^119 = 1.75 * 2^127 is exact: 0x7F60."""
+    cases = [(O.E4M3, 0x0F, 0, 0x0002), (O.E4M3, 0x0C, 0, 0x0002), (O.E4M3, 0x09, 0, 0x0001),
+             (O.E4M3, 0x01, 0, 0x0000), (O.E4M3, 0x8F, 0, 0x8002), (O.E2M1, 0x7, 254, 0x7F80),
+             (O.E2M1, 0xF, 254, 0xFF80), (O.E4M3, 0x7E, 246, 0x7F60), (O.E2M1, 0x1, 0, 0x0020),
+             (O.E4M3, 0x7F, 127, 0x7FC0), (O.E2M1, 0x2, 255, 0x7FC0)]
+    for fmt, code, byte, want in cases:
+        K = 32
+        if fmt == O.E4M3:
+            codes = np.full((1, K), code, dtype=np.uint8)
+        else:
+            codes = np.full((1, K // 2), code | (code << 4), dtype=np.uint8)
+        out = O.dequantize(codes, np.full((1, 1), byte, dtype=np.uint8), K, fmt, O.LINEAR)
+        assert (out == want).all(), (fmt, hex(code), byte, hex(int(out[0, 0])))
 
 
 # ---------------------------------------------------------------------------------------------
