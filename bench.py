@@ -254,19 +254,26 @@ def run_reference(args):
 # our arm
 # ---------------------------------------------------------------------------------------------
 def extra_workloads(dev, peak):
-    """Kernel-only figures of the other workloads: CUDA events around each launch, a 256 MiB
-    buffer written between launches so every launch starts with a cold L2."""
+    """Kernel-only figures of the other workloads: CUDA events around each launch. Between
+    launches a 256 MiB buffer is written (no line of the workload stays in L2) and another
+    256 MiB buffer is read, so that the dirty lines of that write are written back before the
+    timed launch instead of during it: each launch starts from a cold, clean L2."""
     import torch
     import mx_microscaling_quantize_gb300 as mxq
     from mx_microscaling_quantize_gb300 import workloads as W
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clean = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
     out = {}
 
-    def timed(fn, iters=10):
+    def timed(fn, iters=30):
+        # The event timestamps advance in steps of about 2 us on this GPU, so a single launch
+        # reads as a multiple of the step; the mean over launches that start at random phases
+        # of the step is unbiased where a median is not.
         times = []
         for i in range(iters + 2):
             flush.fill_(i & 0xFF)
+            clean.max()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record()
             fn()
@@ -274,7 +281,7 @@ def extra_workloads(dev, peak):
             e.synchronize()
             if i >= 2:
                 times.append(s.elapsed_time(e) / 1e3)
-        return statistics.median(times)
+        return statistics.fmean(times)
 
     def record(name, nbytes, elems, t, launches=1):
         out[name] = {"GB/s": nbytes / t / 1e9, "frac_of_peak": nbytes / t / 1e9 / peak,
@@ -308,6 +315,31 @@ def extra_workloads(dev, peak):
                    x.numel(), t)
             del x, c, s
 
+    # weight-side rotate + quantize of the 70B layer weights, g = 32, swizzled scales
+    for N, K in W.WEIGHT_SHAPES:
+        x = to_gpu(W.weight_rotate_quant(N, K), dev)
+        for fmt, fname in ((mxq.E2M1, "mxfp4"), (mxq.E4M3, "mxfp8")):
+            c, s = mxq.mx_rotate_quantize(x, H, fmt, mxq.SWIZZLED)
+            t = timed(lambda: mxq.mx_rotate_quantize(x, H, fmt, mxq.SWIZZLED, codes=c, scales=s),
+                      iters=15)
+            record(f"weight_rotate_quant_{fname}_g32[{N},{K}]",
+                   2 * x.numel() + c.numel() + s.numel(), x.numel(), t)
+            del c, s
+        del x
+
+    # dequantize stored codes + scales of the QDQ weight x[8192, 8192]
+    x = to_gpu(W.mxfp4_qdq_weight(), dev)
+    y = torch.empty_like(x)
+    K = x.shape[1]
+    for fmt, fname in ((mxq.E2M1, "mxfp4"), (mxq.E4M3, "mxfp8")):
+        for layout, lname in ((mxq.LINEAR, "linear"), (mxq.SWIZZLED, "swizzled")):
+            c, s = mxq.mx_quantize(x, fmt, layout)
+            t = timed(lambda: mxq.mx_dequantize(c, s, K, fmt, layout, y=y))
+            record(f"dequant_{fname}_{lname}[8192,8192]", c.numel() + x.numel() // 32
+                   + 2 * x.numel(), x.numel(), t)
+            del c, s
+    del x, y
+
     # MoE MXFP8 grouped quantize, swizzled scales padded per expert
     xb, off = W.moe_quant()
     x = to_gpu(xb, dev)
@@ -325,7 +357,7 @@ def extra_workloads(dev, peak):
         for g in W.ROTATION_SWEEP_G:
             Hg = to_gpu(W.normalized_hadamard_bf16(g), dev)
             for fmt, fname in ((mxq.E2M1, "mxfp4"), (mxq.E4M3, "mxfp8")):
-                t = timed(lambda: mxq.mx_qdq(x, fmt, Hg, y=y), iters=5)
+                t = timed(lambda: mxq.mx_qdq(x, fmt, Hg, y=y), iters=15)
                 record(f"rotated_qdq_{fname}_g{g}_{lname}[{M},{K}]", 4 * x.numel(), x.numel(), t)
         del x, y
     return out
@@ -336,6 +368,8 @@ CASES = {
     "rotate_quant": "E2M1 rotate(g=32 Hadamard)+quantize, swizzled, x[8192,8192]",
     "rotated_qdq_g128": "E4M3 rotated QDQ g=128, x[4096,28672] Student-t(5)",
     "moe_quant": "E4M3 grouped quantize, swizzled, 128 experts, x[16384,2048]",
+    "dequant_mxfp4": "E2M1 dequantize, swizzled scales, codes of the weight x[8192,8192]",
+    "weight_rotate_quant": "E4M3 rotate(g=32)+quantize, swizzled, weight [57344,8192]",
 }
 
 
@@ -364,6 +398,19 @@ def run_case(args):
         y = torch.empty_like(x)
         fn = lambda: mxq.mx_qdq(x, mxq.E4M3, H, y=y)
         nbytes = 4 * x.numel()
+    elif args.case == "dequant_mxfp4":
+        x = to_gpu(W.mxfp4_qdq_weight(), dev)
+        c, s = mxq.mx_quantize(x, mxq.E2M1, mxq.SWIZZLED)
+        y = torch.empty_like(x)
+        K = x.shape[1]
+        fn = lambda: mxq.mx_dequantize(c, s, K, mxq.E2M1, mxq.SWIZZLED, y=y)
+        nbytes = c.numel() + s.numel() + 2 * x.numel()
+    elif args.case == "weight_rotate_quant":
+        x = to_gpu(W.weight_rotate_quant(57344, 8192), dev)
+        H = to_gpu(W.normalized_hadamard_bf16(32), dev)
+        c, s = mxq.mx_rotate_quantize(x, H, mxq.E4M3, mxq.SWIZZLED)
+        fn = lambda: mxq.mx_rotate_quantize(x, H, mxq.E4M3, mxq.SWIZZLED, codes=c, scales=s)
+        nbytes = 2 * x.numel() + c.numel() + s.numel()
     else:
         xb, off = W.moe_quant()
         x = to_gpu(xb, dev)

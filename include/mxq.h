@@ -103,6 +103,22 @@ mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int ro
                  const void* H, int g, void* y, void* stream);
 
 /*
+ * Dequantize stored MX data to bf16 (pages: the QuTLASS review thread on vLLM's MXFP4 test,
+ * which dequantizes packed E2M1 codes with their E8M0 scales, `_dq_fp4(b_e2m1, b_e8m0, ...)`,
+ * before a reference matmul; the dequantize half of mxfp4_qdq / mxfp8_qdq).
+ * y_i = bf16_round_nearest_even(decode(code_i) * 2^(scale_byte - 127)) for every element, so
+ * mx_dequantize(mx_quantize(x)) == mx_qdq(x) bit for bit. Any code and scale byte is accepted:
+ * scale byte 0xFF (E8M0 NaN) and E4M3 codes S.1111.111 give the bf16 NaN 0x7FC0, products
+ * above the bf16 range give +-Inf, tiny products round to bf16 subnormals or signed zero.
+ * codes: E2M1 [M, K/2] or E4M3 [M, K] bytes (32-byte aligned), laid out as mx_quantize writes
+ * them. scales: linear [M, K/32] or swizzled (16-byte aligned) as returned by
+ * mx_scales_shape(); pad bytes are not read. y: bf16 [M, K] (32-byte aligned), must not
+ * overlap the inputs. Errors: see conventions.
+ */
+mx_status mx_dequantize(const void* codes, const void* scales, int64_t M, int64_t K, int fmt,
+                        int group, int layout, void* y, void* stream);
+
+/*
  * Fused rotate + quantize (pages: fusedQuantizeMx(a, b) with b the runtime-loaded rotation).
  * y_chunk = x_chunk * H for every g-chunk along K (bf16 products, fp32 accumulation on the
  * tensor cores), then the block quantization above on the fp32 rotated values.

@@ -27,7 +27,8 @@ _lib = None
 
 EXPORTS = (
     "mx_status_string", "mx_scales_shape", "mx_grouped_scales_shape", "mx_quantize", "mx_qdq",
-    "mx_rotate_quantize", "mx_quantize_grouped", "mx_rotate_debug", "mx_device_errors",
+    "mx_rotate_quantize", "mx_quantize_grouped", "mx_dequantize", "mx_rotate_debug",
+    "mx_device_errors",
 )
 
 
@@ -57,6 +58,7 @@ def lib() -> ctypes.CDLL:
         "mx_qdq": (i32, [p, i64, i64, i32, i32, i32, p, i32, p, p]),
         "mx_rotate_quantize": (i32, [p, i64, i64, p, i32, i32, i32, i32, i32, p, p, p]),
         "mx_quantize_grouped": (i32, [p, p, i32, i64, i64, i32, i32, i32, i32, p, p, p]),
+        "mx_dequantize": (i32, [p, p, i64, i64, i32, i32, i32, p, p]),
         "mx_rotate_debug": (i32, [p, i64, i64, p, i32, p, p]),
         "mx_device_errors": (i32, [ctypes.POINTER(ctypes.c_int)]),
     }
@@ -184,6 +186,30 @@ def mx_quantize_grouped(x, row_offsets, fmt, layout=SWIZZLED, *, codes=None, sca
     _check(lib().mx_quantize_grouped(_ptr(x), _ptr(row_offsets), E, M, K, fmt, group, layout,
                                      rounding, _ptr(codes), _ptr(scales), _stream_ptr(stream)))
     return codes, scales
+
+
+def mx_dequantize(codes, scales, K, fmt, layout=LINEAR, *, y=None, group=GROUP, stream=None):
+    """Stored codes (uint8 [M, K or K/2]) and E8M0 scales -> bf16 [M, K]."""
+    if not (isinstance(codes, torch.Tensor) and codes.is_cuda and codes.dim() == 2
+            and codes.is_contiguous() and codes.element_size() == 1):
+        raise TypeError("codes must be a contiguous CUDA 2-D tensor of bytes")
+    if not (isinstance(scales, torch.Tensor) and scales.is_cuda and scales.is_contiguous()
+            and scales.element_size() == 1):
+        raise TypeError("scales must be a contiguous CUDA tensor of bytes")
+    M = codes.shape[0]
+    if codes.shape[1] != code_bytes_per_row(fmt, K):
+        raise ValueError("codes has the wrong row length for K and fmt")
+    rows, cols = mx_scales_shape(M, K, layout, group)
+    if scales.numel() != rows * cols:
+        raise ValueError("scales has the wrong size")
+    if y is None:
+        y = torch.empty((M, K), dtype=torch.bfloat16, device=codes.device)
+    elif not (y.is_cuda and y.dtype == torch.bfloat16 and y.numel() == M * K
+              and y.is_contiguous()):
+        raise ValueError("y must be a contiguous CUDA bfloat16 tensor of M * K elements")
+    _check(lib().mx_dequantize(_ptr(codes), _ptr(scales), M, K, fmt, group, layout, _ptr(y),
+                               _stream_ptr(stream)))
+    return y
 
 
 def mx_rotate_debug(x, H, *, y=None, stream=None):

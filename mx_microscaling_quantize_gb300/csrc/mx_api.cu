@@ -141,6 +141,27 @@ mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int ro
                                       static_cast<cudaStream_t>(stream)));
 }
 
+mx_status mx_dequantize(const void* codes, const void* scales, int64_t M, int64_t K, int fmt,
+                        int group, int layout, void* y, void* stream) {
+  bool empty = false;
+  mx_status st = check_common(M, K, fmt, group, MX_ROUND_RNE, &empty);
+  if (st != MX_OK) return st;
+  if (!valid_layout(layout)) return MX_ERR_UNSUPPORTED;
+  if (empty) return MX_OK;
+  if (!codes || !scales || !y) return MX_ERR_NULL;
+  if (!aligned32(codes) || !aligned32(y)) return MX_ERR_ALIGN;
+  if (layout == MX_SCALES_SWIZZLED && !aligned16(scales)) return MX_ERR_ALIGN;
+  mxq::DequantArgs a{};
+  a.codes = codes;
+  a.scales = static_cast<const uint8_t*>(scales);
+  a.y = y;
+  a.M = M;
+  a.K = K;
+  a.scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : ceil_div(K, mxq::kTileCols) * 4;
+  return from_cuda(mxq::launch_dequant(fmt, layout == MX_SCALES_SWIZZLED, a,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 mx_status mx_rotate_quantize(const void* x, int64_t M, int64_t K, const void* H, int g, int fmt,
                              int group, int layout, int rounding, void* codes, void* scales,
                              void* stream) {

@@ -174,6 +174,32 @@ __device__ __forceinline__ void scaled8_bf16(const uint4& v, float inv, float* t
 constexpr uint32_t kE4M3NaNx4 = 0x7F7F7F7Fu;
 constexpr uint32_t kBf16NaNx2 = 0x7FC07FC0u;
 
+// Byte offset of scale (padded row pr, column c) in the 128x4 tiles (cp padded columns).
+__device__ __forceinline__ int64_t swizzled_offset(int64_t pr, int64_t c, int64_t cp) {
+  return ((pr >> 7) * (cp >> 2) + (c >> 2)) * 512 + (pr & 31) * 16 + ((pr >> 5) & 3) * 4 + (c & 3);
+}
+
+// 32-byte vector load through the non-coherent path, not kept in L1 (streamed once).
+__device__ __forceinline__ void load32B(const void* p, uint32_t* r) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ void load16B(const void* p, uint32_t* r) {
+  asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "l"(p));
+}
+
+// 32-byte vector store, evict-first (written once, not re-read by this kernel).
+__device__ __forceinline__ void store32B(void* p, const uint32_t* r) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 // Swizzled scale position of (r, c) inside one 128x4 tile.
 __device__ __forceinline__ int swizzle_in_tile(int r, int c) {
   return (r & 31) * 16 + (r >> 5) * 4 + c;

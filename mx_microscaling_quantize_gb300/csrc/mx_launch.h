@@ -27,6 +27,17 @@ struct StreamArgs {
 cudaError_t launch_stream(int fmt, bool qdq, bool swizzled, bool grouped, const StreamArgs& a,
                           cudaStream_t stream);
 
+struct DequantArgs {
+  const void* codes;      // E2M1 [M, K/2] or E4M3 [M, K] bytes
+  const uint8_t* scales;  // linear [M, K/32] or swizzled (scale_cols padded columns)
+  void* y;                // bf16 [M, K]
+  int64_t M;
+  int64_t K;
+  int64_t scale_cols;
+};
+
+cudaError_t launch_dequant(int fmt, bool swizzled, const DequantArgs& a, cudaStream_t stream);
+
 enum RotOut { kRotCodes = 0, kRotQdq = 1, kRotDebug = 2 };
 
 struct RotArgs {

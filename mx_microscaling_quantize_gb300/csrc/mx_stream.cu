@@ -10,7 +10,7 @@
 // writes the block's codes (16 or 32 bytes) or dequantized bf16 (two 32-byte stores) and its
 // scale byte: at the flat block index (linear) or at its place in the 128x4 tiles (swizzled;
 // the row/column of the block are advanced incrementally, grouped calls map the row to its
-// expert's padded row). A final row pass writes zeros into the swizzled pad bytes.
+// expert's padded row). A final pass over the whole grid writes zeros into the pad bytes.
 #include <algorithm>
 #include <map>
 #include <mutex>
@@ -25,19 +25,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxExperts = 1024;
-
-__device__ __forceinline__ void load32B(const void* p, uint32_t* r) {
-  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7])
-               : "l"(p));
-}
-
-__device__ __forceinline__ void store32B(void* p, const uint32_t* r) {
-  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]),
-               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
-}
 
 // abs-max of one block (16 bf16x2 words) as sign-free bf16 bits; NaN propagates.
 __device__ __forceinline__ uint32_t absmax_block(const uint32_t* w) {
@@ -112,12 +99,6 @@ __device__ __forceinline__ uint32_t block_kernel(const uint32_t* w, bool ok, voi
     }
   }
   return byte;
-}
-
-// Row range of tile t: first input row and number of valid rows (0..128); column block cb.
-// Byte offset of scale (padded row pr, column c) in the 128x4 tiles (cp padded columns).
-__device__ __forceinline__ int64_t swizzled_offset(int64_t pr, int64_t c, int64_t cp) {
-  return ((pr >> 7) * (cp >> 2) + (c >> 2)) * 512 + (pr & 31) * 16 + ((pr >> 5) & 3) * 4 + (c & 3);
 }
 
 // largest e in [0, n) with v[e] <= key (v[0] <= key assumed)
@@ -239,26 +220,43 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
   }
 
   if (SWZ && !QDQ) {
-    // zero the pad bytes of the swizzled buffer: whole pad rows, and columns past K/32
-    const int64_t cp = a.scale_cols;
-    const int64_t pad_stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t pr = (int64_t)blockIdx.x * kThreads + tid; pr < a.scale_rows; pr += pad_stride) {
-      int64_t data_cols = pr < a.M ? cblk : 0;
-      if (GROUPED) {
-        data_cols = 0;
-        if (pr < s_prow[a.E]) {
-          const int e = last_not_above(s_prow, a.E, pr);
-          const int64_t n = s_off[e + 1] > s_off[e] ? s_off[e + 1] - s_off[e] : 0;
-          if (pr - s_prow[e] < n) data_cols = cblk;
+    // Zero the pad bytes of the swizzled buffer, spread over every thread of the grid as a flat
+    // list of items: (A) in each data row, the bytes past column K/32 of its last 4-byte word
+    // (only when K/32 % 4 != 0); (B) every 4-byte word of every pad row (rows past M, or past
+    // an expert's rows inside its last 128-row block).
+    const int64_t cp = a.scale_cols, cp4 = cp >> 2;
+    const int64_t nthr = (int64_t)gridDim.x * kThreads;
+    const int64_t t0 = (int64_t)blockIdx.x * kThreads + tid;
+    if (cblk & 3) {
+      const int64_t c4 = cblk & ~int64_t(3);
+      for (int64_t r = t0; r < a.M; r += nthr) {
+        int64_t pr = r;
+        if (GROUPED) {
+          const int ex = last_not_above(s_off, a.E, r);
+          if (r >= s_off[ex + 1]) continue;  // rows outside every expert have no scales
+          pr = s_prow[ex] + (r - s_off[ex]);
+          if (pr >= a.scale_rows) continue;
         }
-      }
-      for (int64_t c4 = data_cols & ~int64_t(3); c4 < cp; c4 += 4) {
         uint8_t* run = a.scales + swizzled_offset(pr, c4, cp);
-        if (c4 >= data_cols) {
-          *reinterpret_cast<uint32_t*>(run) = 0u;
-        } else {
-          for (int64_t c = data_cols; c < c4 + 4; ++c) run[c - c4] = 0;
+        for (int64_t c = cblk; c < c4 + 4; ++c) run[c - c4] = 0;
+      }
+    }
+    if (!GROUPED) {
+      const int64_t pad_rows = a.scale_rows - a.M;
+      for (int64_t i = t0; i < pad_rows * cp4; i += nthr) {
+        const int64_t pr = a.M + i % pad_rows, c4 = (i / pad_rows) * 4;
+        *reinterpret_cast<uint32_t*>(a.scales + swizzled_offset(pr, c4, cp)) = 0u;
+      }
+    } else {
+      for (int64_t i = t0; i < a.scale_rows * cp4; i += nthr) {
+        const int64_t pr = i % a.scale_rows, c4 = (i / a.scale_rows) * 4;
+        bool pad = true;
+        if (pr < s_prow[a.E]) {
+          const int ex = last_not_above(s_prow, a.E, pr);
+          const int64_t n = s_off[ex + 1] > s_off[ex] ? s_off[ex + 1] - s_off[ex] : 0;
+          pad = pr - s_prow[ex] >= n;
         }
+        if (pad) *reinterpret_cast<uint32_t*>(a.scales + swizzled_offset(pr, c4, cp)) = 0u;
       }
     }
   }
@@ -269,8 +267,12 @@ cudaError_t launch_t(const StreamArgs& a, cudaStream_t stream) {
   const void* k = reinterpret_cast<const void*>(&mx_stream_kernel<FMT, QDQ, SWZ, GROUPED>);
   const int64_t nblk = a.M * (a.K >> 5);
   int64_t need = (nblk + kThreads - 1) / kThreads;
-  const int64_t pad_need = (a.scale_rows + kThreads - 1) / kThreads;
-  if (SWZ && pad_need > need) need = pad_need;
+  if (SWZ && !QDQ) {  // enough threads for the pad items as well (see the kernel's pad pass)
+    const int64_t cp4 = a.scale_cols / 4;
+    const int64_t items = GROUPED ? a.scale_rows * cp4 : (a.scale_rows - a.M) * cp4;
+    const int64_t pad_need = (items + kThreads - 1) / kThreads;
+    if (pad_need > need) need = pad_need;
+  }
   if (need <= 0) return cudaSuccess;
   const int resident = resident_ctas(k, kThreads, 0, 0);
   if (resident <= 0) return cudaErrorInvalidConfiguration;

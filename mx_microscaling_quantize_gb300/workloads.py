@@ -17,6 +17,9 @@ Workloads (shapes from the pages; value distributions chosen as weight-like / ac
     ranks mapped through a seeded permutation; rows [n_e, 2048] N(0,1) concatenated by expert.
   * rotation_sweep: one decoder layer's inputs at 4096 tokens: [4096, 8192] attention input,
     [4096, 8192] O-projection input, [4096, 28672] down-projection input, Student-t(nu=5).
+  * weight_rotate_quant: weight-side rotate + quantize of the 70B layer weights [N, K] =
+    (8192, 8192), (57344, 8192), (8192, 28672), N(0,1) * 0.02, drawn in 2048-row chunks with one
+    child stream each so that any row range can be drawn alone.
 The rotation matrix is an input too: the normalized Sylvester Hadamard H_g * g^-0.5 rounded to
 bf16, the construction the QuTLASS benchmark loads at run time.
 """
@@ -27,7 +30,8 @@ import numpy as np
 import torch
 
 SEED_BASE = 1000
-WORKLOADS = ("mxfp8_linear_quant", "mxfp4_qdq", "rotate_quant", "moe_quant", "rotation_sweep")
+WORKLOADS = ("mxfp8_linear_quant", "mxfp4_qdq", "rotate_quant", "moe_quant", "rotation_sweep",
+             "weight_rotate_quant")
 
 
 def _rng(workload: str, stream: int = 0) -> np.random.Generator:
@@ -132,3 +136,22 @@ def rotation_sweep_input(name: str, M: int | None = None, K: int | None = None,
     K = K0 if K is None else K
     rng = _rng("rotation_sweep", 3 * stream + idx)
     return to_bf16_bits(rng.standard_t(5.0, size=(M, K)))
+
+
+WEIGHT_SHAPES = ((8192, 8192), (57344, 8192), (8192, 28672))
+WEIGHT_CHUNK_ROWS = 2048
+
+
+def weight_rotate_quant(N: int, K: int, r0: int = 0, r1: int | None = None) -> np.ndarray:
+    """Rows [r0, r1) of the weight-like [N, K] matrix N(0,1) * 0.02 (bf16 bits)."""
+    r1 = N if r1 is None else r1
+    assert 0 <= r0 <= r1 <= N
+    out = np.empty((r1 - r0, K), dtype=np.uint16)
+    for chunk in range(r0 // WEIGHT_CHUNK_ROWS, -(-r1 // WEIGHT_CHUNK_ROWS)):
+        lo = chunk * WEIGHT_CHUNK_ROWS
+        hi = min(lo + WEIGHT_CHUNK_ROWS, N)
+        rng = _rng("weight_rotate_quant", (N * 1_000_003 + K) * 4096 + chunk)
+        block = rng.standard_normal((hi - lo, K), dtype=np.float32) * np.float32(0.02)
+        a, b = max(lo, r0), min(hi, r1)
+        out[a - r0:b - r0] = to_bf16_bits(block[a - lo:b - lo])
+    return out

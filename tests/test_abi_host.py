@@ -142,6 +142,23 @@ def test_grouped_validation(L):
     assert g(None, None, 4, 0, 64, 1, 32, 1, 0, None, None, None) == OK
 
 
+def test_dequantize_validation(L):
+    d = L.mx_dequantize  # (codes, scales, M, K, fmt, group, layout, y, stream)
+    assert d(P, P, -1, 64, 1, 32, 0, P, None) == SHAPE
+    assert d(P, P, 4, 48, 1, 32, 0, P, None) == SHAPE
+    assert d(P, P, 4, 64, 3, 32, 0, P, None) == UNSUP
+    assert d(P, P, 4, 64, 1, 16, 0, P, None) == UNSUP
+    assert d(P, P, 4, 64, 1, 32, 2, P, None) == UNSUP
+    assert d(None, P, 4, 64, 1, 32, 0, P, None) == NULL
+    assert d(P, None, 4, 64, 1, 32, 0, P, None) == NULL
+    assert d(P, P, 4, 64, 1, 32, 0, None, None) == NULL
+    assert d(P + 16, P, 4, 64, 2, 32, 0, P, None) == ALIGN
+    assert d(P, P, 4, 64, 2, 32, 0, P + 16, None) == ALIGN
+    assert d(P, P + 8, 4, 64, 2, 32, 1, P, None) == ALIGN
+    assert d(None, None, 0, 64, 1, 32, 1, None, None) == OK
+    assert d(P, P, 1 << 40, 1 << 20, 1, 32, 0, P, None) == SHAPE
+
+
 def test_device_errors_null(L):
     assert L.mx_device_errors(None) == NULL
 

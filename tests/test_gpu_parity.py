@@ -169,6 +169,70 @@ def test_qdq_idempotent_on_gpu(fmt):
 
 
 # ---------------------------------------------------------------------------------------------
+# dequantize stored codes + scales
+# ---------------------------------------------------------------------------------------------
+def dequantize(codes, scales, K, fmt, layout):
+    y = mxq.mx_dequantize(torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda(), K,
+                          fmt, layout)
+    return T.bf16_bits(y)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_dequantize_every_code_under_every_scale_byte(fmt):
+    """Row r holds every code of the format under scale byte r (0..255): subnormal results,
+    overflow to Inf, E8M0 NaN and E4M3 NaN codes included."""
+    if fmt == O.E4M3:
+        K = 256
+        codes = np.tile(np.arange(256, dtype=np.uint8), (256, 1))
+    else:
+        K = 32
+        nib = np.arange(32) % 16
+        codes = np.tile((nib[0::2] | (nib[1::2] << 4)).astype(np.uint8), (256, 1))
+    scales = np.repeat(np.arange(256, dtype=np.uint8), K // 32).reshape(256, K // 32)
+    np.testing.assert_array_equal(dequantize(codes, scales, K, fmt, O.LINEAR),
+                                  O.dequantize(codes, scales, K, fmt, O.LINEAR))
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M,K", [(1, 32), (3, 96), (129, 416), (300, 4096), (1000, 2048)])
+def test_dequantize_random_bytes_bit_exact(fmt, layout, M, K):
+    rng = np.random.default_rng(M * 7 + K)
+    codes = rng.integers(0, 256, (M, O.code_bytes_per_row(fmt, K)), dtype=np.uint8)
+    scales = rng.integers(0, 256, O.scales_shape(M, K, layout), dtype=np.uint8)
+    np.testing.assert_array_equal(dequantize(codes, scales, K, fmt, layout),
+                                  O.dequantize(codes, scales, K, fmt, layout))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M,K", [(1, 32), (127, 160), (255, 416)])
+def test_dequantize_edge_shapes_with_canaries(fmt, M, K):
+    xb = W.mxfp8_linear_quant(M, K, stream=M * 1000 + K + 1)
+    for layout in LAYOUTS:
+        c, s = mxq.mx_quantize(T.to_gpu(xb), fmt, layout)
+        yfull, ybytes = guarded(M * K * 2)
+        mxq.mx_dequantize(c, s, K, fmt, layout, y=ybytes.view(torch.bfloat16).view(M, K))
+        got = T.u8(ybytes).view(np.uint16).reshape(M, K)
+        np.testing.assert_array_equal(got, O.qdq(xb, fmt))
+        assert_guards(yfull, M * K * 2)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("fmt", FMTS)
+def test_dequantize_of_quantize_is_qdq_full_size(fmt, layout):
+    """The MXFP4 QDQ weight workload x[8192, 8192]: dequantize(quantize(x)) equals the GPU QDQ
+    bit for bit over the whole tensor, and the oracle's QDQ on 32 sampled rows."""
+    xb = W.mxfp4_qdq_weight()
+    x = T.to_gpu(xb)
+    c, s = mxq.mx_quantize(x, fmt, layout)
+    y = mxq.mx_dequantize(c, s, x.shape[1], fmt, layout)
+    assert torch.equal(y.view(torch.int16), mxq.mx_qdq(x, fmt).view(torch.int16))
+    rows = np.sort(np.random.default_rng(12).choice(xb.shape[0], 32, replace=False))
+    np.testing.assert_array_equal(T.bf16_bits(y[torch.from_numpy(rows).cuda()]),
+                                  O.qdq(xb[rows], fmt))
+
+
+# ---------------------------------------------------------------------------------------------
 # grouped (MoE) quantize
 # ---------------------------------------------------------------------------------------------
 def grouped(xb, offsets, fmt, layout):
@@ -292,6 +356,24 @@ def test_rotate_quantize_full_size_sampled_rows(fmt):
     rows = np.sort(np.random.default_rng(5).choice(M, 32, replace=False))
     stats = T.check_rotated_codes(xb[rows], H, fmt, c[rows], s[rows])
     assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+
+
+@pytest.mark.parametrize("N,K", W.WEIGHT_SHAPES)
+def test_weight_rotate_quantize_full_size_sampled_rows(N, K):
+    """Weight-side rotate + quantize of the 70B layer weights (the same H as the activations),
+    swizzled scales, both formats, g = 32 and g = 128: 16 sampled rows through the rules."""
+    xb = W.weight_rotate_quant(N, K)
+    x = T.to_gpu(xb)
+    rows = np.sort(np.random.default_rng(N + K).choice(N, 16, replace=False))
+    rows_t = torch.from_numpy(rows).cuda()
+    for g in (32, 128):
+        H = rotation(g)
+        for fmt in FMTS:
+            c, s = mxq.mx_rotate_quantize(x, T.to_gpu(H), fmt, mxq.SWIZZLED)
+            s = T.unswizzle(T.u8(s), N, K)
+            stats = T.check_rotated_codes(xb[rows], H, fmt, T.u8(c[rows_t]), s[rows])
+            assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+            del c
 
 
 def test_rotation_sweep_full_size_sampled_rows():

@@ -486,6 +486,14 @@ def test_grouped_experts_are_independent_blocks():
         prow += s.shape[0]
 
 
+def test_weight_generator_row_ranges_match_the_whole():
+    full = W.weight_rotate_quant(5000, 64)
+    for r0, r1 in ((0, 1), (2047, 2049), (4095, 5000), (100, 4200)):
+        np.testing.assert_array_equal(W.weight_rotate_quant(5000, 64, r0, r1), full[r0:r1])
+    v = W.bf16_bits_to_float(full)
+    assert abs(v.std() - 0.02) < 0.001 and abs(v.mean()) < 0.001
+
+
 def test_workload_recipes():
     x = W.mxfp8_linear_quant(128, 4096)
     assert x.shape == (128, 4096) and x.dtype == np.uint16
