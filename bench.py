@@ -5,11 +5,14 @@ x[8192, 8192] (Student-t nu=4 * 0.02) and the activation-like x[4096, 8192] (N(0
 columns * 100): two kernel launches, 402,653,184 algorithmic bytes (4 B per element). Inputs
 (192 MiB) and outputs (192 MiB) are larger than L2 (129 MB), so no flush runs between steps.
 
-Prints one JSON line: metric/value in algorithmic GB/s, a roofline object for the dominant
-kernel (CUDA-event launch times against the measured HBM copy bandwidth), the CPU oracle timed
-on the host cores (cpu_baseline), an end-to-end figure through the C ABI from pinned host
-buffers (e2e), SM clocks sampled during the timed region, and per-workload kernel figures for
-the other workloads (cold L2: a 256 MiB buffer is written between timed launches).
+Prints one JSON line: metric/value in algorithmic GB/s over the CUDA-event-timed region of K
+steps (every 10th step also brackets each launch with events, for the per-launch durations), a
+roofline object for the kernel (against the measured HBM copy bandwidth), the CPU oracle timed
+on the host cores (cpu_baseline), an end-to-end figure through the same calls with the inputs
+copied in from, and the outputs back to, pinned host memory every step (e2e; copies in both
+directions pipelined over two buffer sets), SM clocks sampled during the timed region, and
+per-workload kernel figures for the other workloads (cold L2: a 256 MiB buffer is written
+between timed launches; mean of the launches, since event timestamps advance in ~2 us steps).
 
 --impl reference times the CPU oracle instead (bounded sample per step, all host cores).
 """
@@ -254,16 +257,16 @@ def run_reference(args):
 # our arm
 # ---------------------------------------------------------------------------------------------
 def extra_workloads(dev, peak):
-    """Kernel-only figures of the other workloads: CUDA events around each launch. Between
-    launches a 256 MiB buffer is written (no line of the workload stays in L2) and another
-    256 MiB buffer is read, so that the dirty lines of that write are written back before the
-    timed launch instead of during it: each launch starts from a cold, clean L2."""
+    """Kernel-only figures of the other workloads: CUDA events around each launch, a 256 MiB
+    buffer written between launches so that every launch starts with a cold L2. The launch
+    then also pays for writing back the dirty lines that buffer left in L2, which stands in
+    for the write-back of its own outputs: those are still in L2 when the launch ends, so a
+    single launch timed from a clean L2 would leave out the cost of its writes."""
     import torch
     import mx_microscaling_quantize_gb300 as mxq
     from mx_microscaling_quantize_gb300 import workloads as W
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    clean = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
     out = {}
 
     def timed(fn, iters=30):
@@ -273,7 +276,6 @@ def extra_workloads(dev, peak):
         times = []
         for i in range(iters + 2):
             flush.fill_(i & 0xFF)
-            clean.max()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record()
             fn()
@@ -432,6 +434,66 @@ def run_case(args):
                       "GB/s": nbytes / t / 1e9, "gpu_launches": args.steps}), flush=True)
 
 
+def end_to_end(mxq, xw_b, xa_b, dev, steps):
+    """The same step through the public call with the inputs in pinned host memory and the
+    outputs read back to pinned host memory, every step: host-to-device copies on one stream,
+    the two QDQ calls on another, device-to-host copies on a third, two device buffer sets so
+    that step i+1's inbound copies overlap step i's outbound ones (the host link is full
+    duplex). Timed from the first inbound copy to the last outbound one."""
+    import torch
+    hw = torch.from_numpy(xw_b.view(np.int16)).pin_memory()
+    ha = torch.from_numpy(xa_b.view(np.int16)).pin_memory()
+    ow = torch.empty_like(hw).pin_memory()
+    oa = torch.empty_like(ha).pin_memory()
+    bufs = [[torch.empty(t.shape, dtype=torch.int16, device=dev) for t in (hw, ha, hw, ha)]
+            for _ in range(2)]
+    s_in, s_qdq, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event(enable_timing=False)
+    loaded = [ev() for _ in range(2)]
+    computed = [ev() for _ in range(2)]
+    drained = [ev() for _ in range(2)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def run(n, timed):
+        torch.cuda.synchronize()
+        for i in range(n):
+            j = i % 2
+            xw, xa, yw, ya = bufs[j]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(computed[j])  # buffer set j no longer read by step i-2
+                if timed and i == 0:
+                    t0.record(s_in)
+                xw.copy_(hw, non_blocking=True)
+                xa.copy_(ha, non_blocking=True)
+                loaded[j].record(s_in)
+            with torch.cuda.stream(s_qdq):
+                s_qdq.wait_event(loaded[j])
+                if i >= 2:
+                    s_qdq.wait_event(drained[j])  # outputs of step i-2 already copied out
+                mxq.mx_qdq(xw.view(torch.bfloat16), mxq.E2M1, y=yw.view(torch.bfloat16),
+                           stream=s_qdq)
+                mxq.mx_qdq(xa.view(torch.bfloat16), mxq.E2M1, y=ya.view(torch.bfloat16),
+                           stream=s_qdq)
+                computed[j].record(s_qdq)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(computed[j])
+                ow.copy_(yw, non_blocking=True)
+                oa.copy_(ya, non_blocking=True)
+                drained[j].record(s_out)
+        if timed:
+            t1.record(s_out)
+        torch.cuda.synchronize()
+
+    run(3, False)
+    run(steps, True)
+    sec = t0.elapsed_time(t1) / 1e3 / steps
+    elems = hw.numel() + ha.numel()
+    return {"value": 4 * elems / sec / 1e9, "unit": "GB/s", "h2d_bytes_per_step": 2 * elems,
+            "d2h_bytes_per_step": 2 * elems, "ms_per_step": sec * 1e3,
+            "pipeline": "2 buffer sets; H2D, QDQ and D2H on 3 streams"}
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_setup(args.gpus)
@@ -459,7 +521,12 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    # Every SAMPLE-th step brackets each of its two launches with CUDA events (the roofline's
+    # per-launch durations); the other steps run with no event between kernels, since an event
+    # at a kernel boundary makes the stream drain there and would slow the whole-job figure.
+    sample = 10
+    sampled = list(range(0, K, sample))
+    ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(4)] for i in sampled}
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -467,22 +534,30 @@ def run_ours(args):
     with ClockSampler(local) as clocks:
         t_start.record(stream)
         for i in range(K):
-            e = ev[i]
-            e[0].record(stream)
+            e = ev.get(i)
+            if e:
+                e[0].record(stream)
             mxq.mx_qdq(xw, mxq.E2M1, y=yw, stream=stream)
-            e[1].record(stream)
-            e[2].record(stream)
+            if e:
+                e[1].record(stream)
+                e[2].record(stream)
             mxq.mx_qdq(xa, mxq.E2M1, y=ya, stream=stream)
-            e[3].record(stream)
+            if e:
+                e[3].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
     ms_total = max_over_ranks(t_start.elapsed_time(t_end), world)
     ms_per_step = ms_total / K
-    kern_s = sum(e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in ev) / 1e3
+    t_weight = statistics.fmean(ev[i][0].elapsed_time(ev[i][1]) for i in sampled) / 1e3
+    t_act = statistics.fmean(ev[i][2].elapsed_time(ev[i][3]) for i in sampled) / 1e3
     launches = 2 * K
     value = step_bytes * world / (ms_per_step / 1e3) / 1e9
-    achieved = step_bytes * K / kern_s / 1e9  # algorithmic bytes / launch time, both launches
+    # Average launch duration of the kernel: the event-timed region holds nothing but its
+    # launches, back to back, so bytes of all launches / region time is the byte-weighted
+    # average (kernel boundaries included). launch_us keeps the sampled event-bracketed
+    # durations, which read a little longer: the brackets make the stream drain.
+    achieved = step_bytes * K / (ms_total / 1e3) / 1e9
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -497,35 +572,16 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs (copy)",
                      "kernel": "mx_stream_kernel<E2M1, QDQ>",
+                     "launch_us": {"weight": t_weight * 1e6, "activation": t_act * 1e6,
+                                   "region_per_step": ms_per_step * 1e3,
+                                   "sampled_steps": len(sampled)},
                      "traffic": recorded_traffic(),
                      "algorithmic_bytes_per_launch": {"weight": 4 * xw.numel(),
                                                       "activation": 4 * xa.numel()}},
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.quick:
-        # end to end through the C ABI from pinned host buffers
-        hw = torch.from_numpy(xw_b.view(np.int16)).pin_memory()
-        ha = torch.from_numpy(xa_b.view(np.int16)).pin_memory()
-        ow = torch.empty_like(hw).pin_memory()
-        oa = torch.empty_like(ha).pin_memory()
-        E = min(K, 50)
-        for it in range(E + 3):
-            if it == 3:
-                torch.cuda.synchronize()
-                s0 = torch.cuda.Event(enable_timing=True)
-                s1 = torch.cuda.Event(enable_timing=True)
-                s0.record(stream)
-            xw.view(torch.int16).copy_(hw, non_blocking=True)
-            xa.view(torch.int16).copy_(ha, non_blocking=True)
-            step()
-            ow.copy_(yw.view(torch.int16), non_blocking=True)
-            oa.copy_(ya.view(torch.int16), non_blocking=True)
-        s1.record(stream)
-        torch.cuda.synchronize()
-        e2e_s = s0.elapsed_time(s1) / 1e3 / E
-        line["e2e"] = {"value": step_bytes / e2e_s / 1e9, "unit": "GB/s",
-                       "h2d_bytes_per_step": 2 * elems, "d2h_bytes_per_step": 2 * elems,
-                       "ms_per_step": e2e_s * 1e3}
+        line["e2e"] = end_to_end(mxq, xw_b, xa_b, dev, min(K, 50))
         line["workloads"] = extra_workloads(dev, peak)
         cpu_gbs, cpu_s, passes, threads = time_oracle_for(xw_b, xa_b, 10.0)
         line["cpu_baseline"] = {

@@ -138,8 +138,20 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read_all_but_one() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
-// all committed bulk stores are complete
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// all committed bulk stores have finished reading shared memory (their global writes complete
+// on their own; the kernel's end makes them visible to later work)
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Both 64-column boxes of tile t (128 rows x 128 columns) into one ring stage.
+__device__ __forceinline__ void load_tile(const RotArgs& a, const CUtensorMap* map, uint32_t dst,
+                                          uint32_t bar, int64_t t) {
+  const int64_t rb = t / a.col_tiles, cb = t - rb * a.col_tiles;
+  mbar_arrive_expect_tx(bar, kStageBytes);
+  tma_load_2d(dst, map, (int)(cb * kTileCols), (int)(rb * kTileRows), bar);
+  tma_load_2d(dst + kBoxBytes, map, (int)(cb * kTileCols + kBoxCols), (int)(rb * kTileRows), bar);
+}
 
 // Shared-memory matrix descriptors (5th-generation tensor core format: start >> 4 at bits
 // 0-13, leading byte offset >> 4 at 16-29, stride byte offset >> 4 at 32-45, bit 46 set,
@@ -270,7 +282,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(h_ready + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t n_tiles = a.row_blocks * a.col_tiles;
+  const uint32_t sA_u32 = smem_u32(sA), sB_u32 = smem_u32(sB);
+  // Thread 0 initializes the barriers and is also the TMA producer: it fills the first stages
+  // of the ring at once (they wait for nothing), so that the first loads are in flight while
+  // the block allocates tensor memory and stages H.
+  int first_loads = 0;
   if (tid == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+    if (OUT != kRotDebug) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&ymap)) : "memory");
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(full + s), 1);
       mbar_init(smem_u32(empty + s), 1);
@@ -281,6 +303,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(h_ready), kEpiWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int64_t t = blockIdx.x; t < n_tiles && first_loads < kStages; t += gridDim.x) {
+      load_tile(a, &tmap, sA_u32 + first_loads * kStageBytes, smem_u32(full + first_loads), t);
+      ++first_loads;
+    }
+  }
+  // The epilogue warps stage B = H^T: the 16-byte loads of H are issued before the block-wide
+  // barrier, the shared-memory writes and the arrival on h_ready (initialized by thread 0)
+  // after it.
+  constexpr int kVecs = G * G / 8;
+  constexpr int kPer = (kVecs + kEpiThreads - 1) / kEpiThreads;
+  uint4 hv[kPer];
+  if (warp >= 2) {
+    const uint4* H = static_cast<const uint4*>(a.H);
+    const int et = tid - 64;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int v = et + i * kEpiThreads;
+      if (v < kVecs) hv[i] = H[v];
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -290,18 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp >= 2) {
-    // The epilogue warps stage B = H^T (all 16-byte loads in flight first) while the producer
-    // already streams the first tiles; the MMA thread waits on h_ready.
-    constexpr int kVecs = G * G / 8;
-    constexpr int kPer = (kVecs + kEpiThreads - 1) / kEpiThreads;
-    const uint4* H = static_cast<const uint4*>(a.H);
     const int et = tid - 64;
-    uint4 hv[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int v = et + i * kEpiThreads;
-      if (v < kVecs) hv[i] = H[v];
-    }
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int v = et + i * kEpiThreads;
@@ -320,24 +350,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(smem_u32(h_ready));
   }
   const uint32_t tmem = *tmem_slot;
-  const uint32_t sA_u32 = smem_u32(sA), sB_u32 = smem_u32(sB);
-  const int64_t n_tiles = a.row_blocks * a.col_tiles;
   bool failed = false;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
-      int it = 0;
-      for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+      int it = first_loads;  // the first stages were issued before the block-wide barrier
+      for (int64_t t = blockIdx.x + (int64_t)it * gridDim.x; t < n_tiles; t += gridDim.x, ++it) {
         const int s = it % kStages;
-        if (it >= kStages) mbar_wait(smem_u32(empty + s), ((it / kStages) & 1) ^ 1, &failed);
-        const int64_t rb = t / a.col_tiles, cb = t - rb * a.col_tiles;
-        const uint32_t dst = sA_u32 + s * kStageBytes;
-        mbar_arrive_expect_tx(smem_u32(full + s), kStageBytes);
-        tma_load_2d(dst, &tmap, (int)(cb * kTileCols), (int)(rb * kTileRows), smem_u32(full + s));
-        tma_load_2d(dst + kBoxBytes, &tmap, (int)(cb * kTileCols + kBoxCols), (int)(rb * kTileRows),
-                    smem_u32(full + s));
+        mbar_wait(smem_u32(empty + s), ((it / kStages) & 1) ^ 1, &failed);
+        load_tile(a, &tmap, sA_u32 + s * kStageBytes, smem_u32(full + s), t);
       }
     }
   } else if (warp == 1) {
@@ -460,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  if (OUT != kRotDebug && warp == 2 && lane == 0) bulk_wait_all();
+  if (OUT != kRotDebug && warp == 2 && lane == 0) bulk_wait_read_all();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -220,10 +220,11 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
   }
 
   if (SWZ && !QDQ) {
-    // Zero the pad bytes of the swizzled buffer, spread over every thread of the grid as a flat
-    // list of items: (A) in each data row, the bytes past column K/32 of its last 4-byte word
-    // (only when K/32 % 4 != 0); (B) every 4-byte word of every pad row (rows past M, or past
-    // an expert's rows inside its last 128-row block).
+    // Zero the pad bytes of the swizzled buffer, spread over every thread of the grid: (A) in
+    // each data row, the bytes past column K/32 of its last 4-byte word (only when
+    // K/32 % 4 != 0); (B) every 4-byte word of every pad row (rows past M: a flat list of
+    // (row, word) items, so that a few wide pad rows do not serialize on a few threads; rows
+    // past an expert's rows inside its last 128-row block: one thread per scale row).
     const int64_t cp = a.scale_cols, cp4 = cp >> 2;
     const int64_t nthr = (int64_t)gridDim.x * kThreads;
     const int64_t t0 = (int64_t)blockIdx.x * kThreads + tid;
@@ -248,15 +249,20 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
         *reinterpret_cast<uint32_t*>(a.scales + swizzled_offset(pr, c4, cp)) = 0u;
       }
     } else {
-      for (int64_t i = t0; i < a.scale_rows * cp4; i += nthr) {
-        const int64_t pr = i % a.scale_rows, c4 = (i / a.scale_rows) * 4;
+      // pad rows lie between the experts' rows: one thread per scale row finds out whether
+      // its row is one (a search over the experts' padded row offsets) and zeroes it
+      for (int64_t pr = t0; pr < a.scale_rows; pr += nthr) {
         bool pad = true;
         if (pr < s_prow[a.E]) {
           const int ex = last_not_above(s_prow, a.E, pr);
           const int64_t n = s_off[ex + 1] > s_off[ex] ? s_off[ex + 1] - s_off[ex] : 0;
           pad = pr - s_prow[ex] >= n;
         }
-        if (pad) *reinterpret_cast<uint32_t*>(a.scales + swizzled_offset(pr, c4, cp)) = 0u;
+        if (pad) {
+          for (int64_t c4 = 0; c4 < cp; c4 += 4) {
+            *reinterpret_cast<uint32_t*>(a.scales + swizzled_offset(pr, c4, cp)) = 0u;
+          }
+        }
       }
     }
   }
@@ -269,7 +275,7 @@ cudaError_t launch_t(const StreamArgs& a, cudaStream_t stream) {
   int64_t need = (nblk + kThreads - 1) / kThreads;
   if (SWZ && !QDQ) {  // enough threads for the pad items as well (see the kernel's pad pass)
     const int64_t cp4 = a.scale_cols / 4;
-    const int64_t items = GROUPED ? a.scale_rows * cp4 : (a.scale_rows - a.M) * cp4;
+    const int64_t items = GROUPED ? a.scale_rows : (a.scale_rows - a.M) * cp4;
     const int64_t pad_need = (items + kThreads - 1) / kThreads;
     if (pad_need > need) need = pad_need;
   }
