@@ -65,6 +65,11 @@ def _load():
         "mxo_rotate_quantize": (None, [p, i64, i64, p, i32, i32, i32, p, p]),
         "mxo_rotate_qdq": (None, [p, i64, i64, p, i32, i32, p]),
         "mxo_quantize_grouped": (None, [p, p, i32, i64, i32, i32, i64, p, p]),
+        "mxo_nvfp4_scales_shape": (None, [i64, i64, i32, p, p]),
+        "mxo_nvfp4_block": (i32, [p, i32, ctypes.c_float, p]),
+        "mxo_nvfp4_dequant_bf16": (ctypes.c_uint16, [i32, i32, ctypes.c_float]),
+        "mxo_nvfp4_quantize": (None, [p, i64, i64, p, i32, ctypes.c_float, i32, p, p]),
+        "mxo_nvfp4_qdq": (None, [p, i64, i64, p, i32, ctypes.c_float, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -227,3 +232,48 @@ def quantize_grouped(x_bits, offsets, fmt: int, layout: int, scale_rows: int | N
     _load().mxo_quantize_grouped(_ptr(x), _ptr(off), E, K, fmt, layout, scale_rows, _ptr(codes),
                                  _ptr(scales))
     return codes, scales
+
+
+# ----------------------------------------------------------------------------------------------
+# NVFP4: E2M1 codes in blocks of 16, E4M3 block scales under an fp32 global scale gs
+# ----------------------------------------------------------------------------------------------
+def nvfp4_scales_shape(M: int, K: int, layout: int):
+    rows = ctypes.c_int64()
+    cols = ctypes.c_int64()
+    _load().mxo_nvfp4_scales_shape(M, K, layout, ctypes.byref(rows), ctypes.byref(cols))
+    return rows.value, cols.value
+
+
+def nvfp4_block(values, gs: float):
+    """One block of fp32 values -> (E4M3 scale byte, unpacked E2M1 codes)."""
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    codes = np.zeros(v.size, dtype=np.uint8)
+    b = _load().mxo_nvfp4_block(_ptr(v), v.size, float(np.float32(gs)), _ptr(codes))
+    return b, codes
+
+
+def nvfp4_dequant_bf16(code: int, scale: int, gs: float) -> int:
+    return _load().mxo_nvfp4_dequant_bf16(code, scale, float(np.float32(gs)))
+
+
+def nvfp4_quantize(x_bits, gs: float, layout: int, H_bits=None):
+    """-> (codes uint8 [M, K/2], E4M3 scales uint8 [rows, cols]); H_bits rotates each g-chunk."""
+    x = _bits(x_bits)
+    M, K = x.shape
+    H = None if H_bits is None else _bits(H_bits)
+    codes = np.zeros((M, K // 2), dtype=np.uint8)
+    scales = np.zeros(nvfp4_scales_shape(M, K, layout), dtype=np.uint8)
+    _load().mxo_nvfp4_quantize(_ptr(x), M, K, None if H is None else _ptr(H),
+                               0 if H is None else H.shape[0], float(np.float32(gs)), layout,
+                               _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def nvfp4_qdq(x_bits, gs: float, H_bits=None) -> np.ndarray:
+    x = _bits(x_bits)
+    M, K = x.shape
+    H = None if H_bits is None else _bits(H_bits)
+    out = np.zeros((M, K), dtype=np.uint16)
+    _load().mxo_nvfp4_qdq(_ptr(x), M, K, None if H is None else _ptr(H),
+                          0 if H is None else H.shape[0], float(np.float32(gs)), _ptr(out))
+    return out

@@ -305,6 +305,94 @@ std::vector<double> rotate_rows(const uint16_t* x, int64_t rows, int64_t K, cons
   return y;
 }
 
+// ---------------------------------------------------------------------------------------------
+// NVFP4: E2M1 elements in blocks of 16 along K, one E4M3 scale per block under a per-tensor fp32
+// global scale gs. The QuTLASS page names the format ("Support for both NVFP4 and MXFP4") and
+// the call fusedQuantizeNv(a, H, global_scale) whose blocked scales are viewed as [-1, K/16]
+// (review thread on benchmarks/kernels/bench_nvfp4_qutlass.py), but prints no scale rule. The
+// reading taken is the usual two-level one, with every step an fp32 operation (round to nearest
+// even), in this order:
+//   r6 = gs / 6;  s_f = amax * r6;  sc = E4M3(s_f) (nearest even, saturating at 448);
+//   enc = gs / decode(sc) (0 when decode(sc) == 0);  code_i = E2M1(v_i * enc);
+//   QDQ: dq = decode(sc) / gs (0 when decode(sc) == 0);  y_i = bf16(decode(code_i) * dq).
+// A block holding a NaN or an infinity gets scale byte 0x7F (the E4M3 NaN), codes 0 and QDQ
+// outputs 0x7FC0. Values v_i are fp32 (bf16 inputs widen exactly; rotated values are rounded to
+// fp32 once).
+// ---------------------------------------------------------------------------------------------
+int e4m3_code_of_nonneg(float v) { return nearest_magnitude_code(kE4M3, (double)v); }
+
+// Quantize one block of n fp32 values; writes unpacked E2M1 codes, returns the E4M3 scale byte.
+int nvfp4_block(const float* v, int n, float gs, uint8_t* codes) {
+  bool special = false;
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    if (std::isnan(v[i]) || std::isinf(v[i])) special = true;
+    else if (std::fabs(v[i]) > amax) amax = std::fabs(v[i]);
+  }
+  if (special) {
+    for (int i = 0; i < n; ++i) codes[i] = 0;
+    return 0x7F;
+  }
+  const float r6 = gs / 6.0f;
+  const float s_f = amax * r6;
+  const int sc = e4m3_code_of_nonneg(s_f);
+  const float s_dec = (float)kE4M3.magnitude[sc];
+  const float enc = (s_dec == 0.0f) ? 0.0f : gs / s_dec;
+  for (int i = 0; i < n; ++i) {
+    const float t = v[i] * enc;
+    int code = nearest_magnitude_code(kE2M1, std::fabs((double)t));
+    if (std::signbit(t)) code |= 0x8;
+    codes[i] = (uint8_t)code;
+  }
+  return sc;
+}
+
+uint16_t nvfp4_dequant_to_bf16(int code, int scale_byte, float gs) {
+  if (scale_byte == 0x7F || scale_byte == 0xFF) return 0x7FC0;
+  const float s_dec = (float)kE4M3.magnitude[scale_byte & 0x7F];
+  const float dq = (s_dec == 0.0f) ? 0.0f : s_dec / gs;
+  const float y = (float)decode_code(kE2M1, code) * dq;
+  return double_to_bf16_rne((double)y);
+}
+
+// rows of fp32 values [rows, K] -> packed codes [rows, K/2], scales (linear [rows, K/16] or
+// swizzled with padded_cols columns) and/or QDQ bf16 (either output may be null)
+void nvfp4_rows(const float* v, int64_t rows, int64_t K, float gs, int layout, int64_t padded_cols,
+                uint8_t* codes, uint8_t* scales, uint16_t* qdq) {
+  const int64_t groups = K / 16;
+  uint8_t bc[16];
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t j = 0; j < groups; ++j) {
+      const int sc = nvfp4_block(v + r * K + j * 16, 16, gs, bc);
+      if (scales) {
+        if (layout == 0) scales[r * groups + j] = (uint8_t)sc;
+        else scales[swizzled_offset(r, j, padded_cols)] = (uint8_t)sc;
+      }
+      for (int i = 0; i < 16; ++i) {
+        const int64_t k = j * 16 + i;
+        if (codes) {
+          uint8_t& b = codes[r * (K / 2) + k / 2];
+          if (k % 2 == 0) b = (uint8_t)((b & 0xF0) | bc[i]);
+          else b = (uint8_t)((b & 0x0F) | (bc[i] << 4));
+        }
+        if (qdq) qdq[r * K + k] = nvfp4_dequant_to_bf16(bc[i], sc, gs);
+      }
+    }
+  }
+}
+
+std::vector<float> bf16_rows_to_float(const uint16_t* x, int64_t n) {
+  std::vector<float> v((size_t)n);
+  for (int64_t i = 0; i < n; ++i) v[(size_t)i] = (float)bf16_to_double(x[i]);
+  return v;
+}
+
+std::vector<float> doubles_to_float(const std::vector<double>& y) {
+  std::vector<float> v(y.size());
+  for (size_t i = 0; i < y.size(); ++i) v[i] = (float)y[i];
+  return v;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------------------------
@@ -410,6 +498,42 @@ void mxo_quantize_grouped(const uint16_t* x, const int64_t* offsets, int E, int6
     padded_row += ceil_div(n, 128) * 128;
   }
   (void)M_total;
+}
+
+// NVFP4 (see the reading above). Scale shapes: linear [M, K/16]; swizzled
+// [ceil(M/128)*128, ceil(K/16/4)*4] (pads zeroed here). H may be null (no rotation).
+void mxo_nvfp4_scales_shape(int64_t M, int64_t K, int layout, int64_t* rows, int64_t* cols) {
+  if (layout == 0) {
+    *rows = M;
+    *cols = K / 16;
+  } else {
+    *rows = ceil_div(M, 128) * 128;
+    *cols = ceil_div(K / 16, 4) * 4;
+  }
+}
+
+int mxo_nvfp4_block(const float* v, int n, float gs, uint8_t* codes) {
+  return nvfp4_block(v, n, gs, codes);
+}
+
+uint16_t mxo_nvfp4_dequant_bf16(int code, int scale_byte, float gs) {
+  return nvfp4_dequant_to_bf16(code, scale_byte, gs);
+}
+
+void mxo_nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, const uint16_t* H, int g, float gs,
+                        int layout, uint8_t* codes, uint8_t* scales) {
+  int64_t srows, scols;
+  mxo_nvfp4_scales_shape(M, K, layout, &srows, &scols);
+  std::memset(scales, 0, (size_t)(srows * scols));
+  std::memset(codes, 0, (size_t)(M * (K / 2)));
+  std::vector<float> v = H ? doubles_to_float(rotate_rows(x, M, K, H, g)) : bf16_rows_to_float(x, M * K);
+  nvfp4_rows(v.data(), M, K, gs, layout, scols, codes, scales, nullptr);
+}
+
+void mxo_nvfp4_qdq(const uint16_t* x, int64_t M, int64_t K, const uint16_t* H, int g, float gs,
+                   uint16_t* out) {
+  std::vector<float> v = H ? doubles_to_float(rotate_rows(x, M, K, H, g)) : bf16_rows_to_float(x, M * K);
+  nvfp4_rows(v.data(), M, K, gs, 0, 0, nullptr, nullptr, out);
 }
 
 }  // extern "C"

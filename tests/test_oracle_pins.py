@@ -346,6 +346,92 @@ def test_dequantize_subnormal_and_overflow_closed_forms():
 
 
 # ---------------------------------------------------------------------------------------------
+# NVFP4 (two-level reading: E4M3 block scale of 16 under an fp32 global scale)
+# ---------------------------------------------------------------------------------------------
+def read_nvfp4_golden():
+    out = []
+    for line in open(os.path.join(GOLDEN, "nvfp4_worked_blocks.txt")):
+        if not line.strip() or line.startswith("#"):
+            continue
+        name, gs, vals, sc, codes, qdq = [f.strip() for f in line.split("|")]
+        out.append((name, float(gs), [float(v) for v in vals.split()], int(sc, 16),
+                    [int(c, 16) for c in codes.split()], [int(q, 16) for q in qdq.split()]))
+    return out
+
+
+@pytest.mark.parametrize("case", read_nvfp4_golden(), ids=lambda c: c[0])
+def test_nvfp4_worked_blocks(case):
+    name, gs, vals, sc, codes, qdq = case
+    b, c = O.nvfp4_block(vals, gs)
+    assert b == sc and list(c) == codes
+    x = bf16(vals).reshape(1, 16)
+    x = np.concatenate([x, x], axis=1)  # K = 32: two identical blocks
+    np.testing.assert_array_equal(O.nvfp4_qdq(x, gs)[0, :16], np.array(qdq, dtype=np.uint16))
+    cq, sq = O.nvfp4_quantize(x, gs, O.LINEAR)
+    assert list(sq[0]) == [sc, sc]
+    assert [(cq[0, k // 2] >> (4 * (k % 2))) & 0xF for k in range(16)] == codes
+
+
+def test_nvfp4_special_block():
+    v = [1.0] * 16
+    v[3] = float("nan")
+    b, c = O.nvfp4_block(v, 1.0)
+    assert b == 0x7F and not c.any()
+    assert O.nvfp4_dequant_bf16(2, 0x7F, 1.0) == 0x7FC0
+
+
+def test_nvfp4_scale_is_torch_e4m3_cast_of_the_fp32_scale():
+    """The scale byte is torch's RNE float8_e4m3fn cast of s_f = amax * (gs / 6) (fp32 ops in
+    numpy), for scales inside the E4M3 range."""
+    rng = np.random.default_rng(31)
+    for _ in range(400):
+        v = (rng.standard_normal(16) * 2.0 ** rng.integers(-20, 20)).astype(np.float32)
+        gs = np.float32(2.0 ** rng.uniform(-8, 12))
+        s_f = np.abs(v).max() * (gs / np.float32(6.0))
+        if s_f >= 448:
+            continue
+        want = torch.tensor([float(s_f)], dtype=torch.float32).to(torch.float8_e4m3fn)
+        b, _ = O.nvfp4_block(v, gs)
+        assert b == int(want.view(torch.uint8).item()), (s_f, b)
+
+
+def test_nvfp4_codes_are_mx_e2m1_rounding_of_the_scaled_values():
+    """Codes = the (pinned) MX E2M1 rounding at scale 2^0 of t = v * (gs / decode(sc))."""
+    rng = np.random.default_rng(32)
+    e4m3 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    for _ in range(300):
+        v = (rng.standard_normal(16) * 2.0 ** rng.integers(-10, 10)).astype(np.float32)
+        gs = np.float32(2.0 ** rng.uniform(-6, 10))
+        b, codes = O.nvfp4_block(v, gs)
+        s_dec = np.float32(e4m3[b])
+        enc = gs / s_dec if s_dec != 0 else np.float32(0)
+        t = (v * enc).astype(np.float64)
+        byte, want = O.quantize_block(O.E2M1, t, forced_byte=127)
+        assert byte == 127
+        np.testing.assert_array_equal(codes, want)
+
+
+def test_nvfp4_identity_rotation_and_layouts():
+    x = W.mxfp4_qdq_activation(130, 256)
+    gs = np.float32(448 * 6) / np.float32(W.bf16_bits_to_float(x).__abs__().max())
+    eye = W.to_bf16_bits(np.eye(32))
+    c0, s0 = O.nvfp4_quantize(x, gs, O.LINEAR)
+    c1, s1 = O.nvfp4_quantize(x, gs, O.LINEAR, H_bits=eye)
+    np.testing.assert_array_equal(c0, c1)
+    np.testing.assert_array_equal(s0, s1)
+    np.testing.assert_array_equal(O.nvfp4_qdq(x, gs), O.nvfp4_qdq(x, gs, H_bits=eye))
+    _, sw = O.nvfp4_quantize(x, gs, O.SWIZZLED)
+    want = to_blocked_reference(torch.from_numpy(s0)).numpy()
+    np.testing.assert_array_equal(sw.reshape(-1), want)
+    # QDQ output is the dequantization of the stored codes and scales
+    q = O.nvfp4_qdq(x, gs)
+    for r in range(0, 130, 13):
+        for k in range(0, 256, 11):
+            code = (c0[r, k // 2] >> (4 * (k % 2))) & 0xF
+            assert q[r, k] == O.nvfp4_dequant_bf16(int(code), int(s0[r, k // 16]), float(gs))
+
+
+# ---------------------------------------------------------------------------------------------
 # layouts
 # ---------------------------------------------------------------------------------------------
 def to_blocked_reference(scales: torch.Tensor) -> torch.Tensor:
