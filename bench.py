@@ -342,6 +342,26 @@ def extra_workloads(dev, peak):
             del c, s
     del x, y
 
+    # NVFP4 (16-element blocks, E4M3 scales under a global scale): plain quantize and QDQ of
+    # the QDQ weight, and rotate(g = 16) + quantize of the largest activation
+    x = to_gpu(W.mxfp4_qdq_weight(), dev)
+    gs = torch.tensor([448.0 * 6.0], device=dev) / x.float().abs().max()
+    c, s = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED)
+    t = timed(lambda: mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, codes=c, scales=s))
+    record("nvfp4_quant[8192,8192]", 2 * x.numel() + c.numel() + x.numel() // 16, x.numel(), t)
+    y = torch.empty_like(x)
+    t = timed(lambda: mxq.mx_qdq_nvfp4(x, gs, y=y))
+    record("nvfp4_qdq[8192,8192]", 4 * x.numel(), x.numel(), t)
+    del x, y, c, s
+    x = to_gpu(W.rotate_quant_activation(8192, 28672), dev)
+    H16 = to_gpu(W.normalized_hadamard_bf16(16), dev)
+    c, s = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, H16)
+    t = timed(lambda: mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, H16, codes=c, scales=s),
+              iters=15)
+    record("nvfp4_rotate_quant_g16[8192,28672]", 2 * x.numel() + c.numel() + x.numel() // 16,
+           x.numel(), t)
+    del x, c, s
+
     # MoE MXFP8 grouped quantize, swizzled scales padded per expert
     xb, off = W.moe_quant()
     x = to_gpu(xb, dev)
@@ -372,6 +392,8 @@ CASES = {
     "moe_quant": "E4M3 grouped quantize, swizzled, 128 experts, x[16384,2048]",
     "dequant_mxfp4": "E2M1 dequantize, swizzled scales, codes of the weight x[8192,8192]",
     "weight_rotate_quant": "E4M3 rotate(g=32)+quantize, swizzled, weight [57344,8192]",
+    "nvfp4_quant": "NVFP4 quantize, swizzled E4M3 scales, weight x[8192,8192]",
+    "nvfp4_rotate_quant": "NVFP4 rotate(g=16)+quantize, swizzled, x[8192,28672]",
 }
 
 
@@ -413,6 +435,19 @@ def run_case(args):
         c, s = mxq.mx_rotate_quantize(x, H, mxq.E4M3, mxq.SWIZZLED)
         fn = lambda: mxq.mx_rotate_quantize(x, H, mxq.E4M3, mxq.SWIZZLED, codes=c, scales=s)
         nbytes = 2 * x.numel() + c.numel() + s.numel()
+    elif args.case == "nvfp4_quant":
+        x = to_gpu(W.mxfp4_qdq_weight(), dev)
+        gs = torch.tensor([448.0 * 6.0], device=dev) / x.float().abs().max()
+        c, s = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED)
+        fn = lambda: mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, codes=c, scales=s)
+        nbytes = 2 * x.numel() + c.numel() + x.numel() // 16
+    elif args.case == "nvfp4_rotate_quant":
+        x = to_gpu(W.rotate_quant_activation(8192, 28672), dev)
+        H = to_gpu(W.normalized_hadamard_bf16(16), dev)
+        gs = torch.tensor([448.0 * 6.0 / 8.0], device=dev)
+        c, s = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, H)
+        fn = lambda: mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, H, codes=c, scales=s)
+        nbytes = 2 * x.numel() + c.numel() + x.numel() // 16
     else:
         xb, off = W.moe_quant()
         x = to_gpu(xb, dev)

@@ -152,6 +152,36 @@ mx_status mx_quantize_grouped(const void* x, const int64_t* row_offsets, int E, 
                               void* codes, void* scales, void* stream);
 
 /*
+ * NVFP4 (pages: the QuTLASS feature list, "Support for both NVFP4 and MXFP4", and its review
+ * thread on benchmarks/kernels/bench_nvfp4_qutlass.py: fusedQuantizeNv(a, H, global_scale)
+ * returning E2M1 codes and blocked scales viewed as [-1, K/16]). E2M1 codes in blocks of 16
+ * along K, one E4M3 scale byte per block, under a per-tensor fp32 global scale gs. The pages
+ * print no scale rule; the reading is the usual two-level one, every step one fp32 operation
+ * rounded to nearest even, in this order, per block with abs-max amax:
+ *   s_f = amax * (gs / 6);  scale byte = E4M3(s_f), saturating at 448;
+ *   enc = gs / decode(scale);  code_i = E2M1(v_i * enc)  (enc = 0 when decode(scale) == 0);
+ *   QDQ: y_i = bf16(decode(code_i) * (decode(scale) / gs))  (0 factor likewise).
+ * A block holding a NaN or an infinity gets scale byte 0x7F, codes 0 and QDQ outputs 0x7FC0.
+ * With H (bf16 [g, g], g in {16, 32, 64, 128}, K % g == 0) every g-chunk is first rotated,
+ * y_chunk = x_chunk * H (fp32 accumulation on the tensor cores), as in mx_rotate_quantize.
+ * global_scale: DEVICE pointer to one fp32 value, 4-byte aligned, read by the kernel (so it may
+ * come from an earlier kernel on the same stream); it must be positive and finite, and
+ * gs / 2^-9 must not overflow fp32 (gs < 1.7e38 * 2^-9), else results are unspecified.
+ * K % 32 == 0. Codes: [M, K/2] bytes (32-byte aligned), the lower K index in the low nibble.
+ * Scales: linear [M, K/16] (2-byte aligned) or swizzled [ceil(M/128)*128, ceil(K/64)*4]
+ * (16-byte aligned; 128x4 tiles as for the MX scales, pads zero), see mx_nvfp4_scales_shape.
+ */
+mx_status mx_nvfp4_scales_shape(int64_t M, int64_t K, int layout, int64_t* rows, int64_t* cols);
+
+mx_status mx_quantize_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g,
+                            const float* global_scale, int layout, void* codes, void* scales,
+                            void* stream);
+
+/* NVFP4 QDQ (see above): bf16 y [M, K], 32-byte aligned, must not overlap x. */
+mx_status mx_qdq_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g,
+                       const float* global_scale, void* y, void* stream);
+
+/*
  * Diagnostics: the rotated values y = x_chunk * H exactly as mx_rotate_quantize computes them
  * before quantization (same device code), written as fp32 [M, K] to y_f32 (device).
  */

@@ -27,8 +27,8 @@ _lib = None
 
 EXPORTS = (
     "mx_status_string", "mx_scales_shape", "mx_grouped_scales_shape", "mx_quantize", "mx_qdq",
-    "mx_rotate_quantize", "mx_quantize_grouped", "mx_dequantize", "mx_rotate_debug",
-    "mx_device_errors",
+    "mx_rotate_quantize", "mx_quantize_grouped", "mx_dequantize", "mx_nvfp4_scales_shape",
+    "mx_quantize_nvfp4", "mx_qdq_nvfp4", "mx_rotate_debug", "mx_device_errors",
 )
 
 
@@ -59,6 +59,9 @@ def lib() -> ctypes.CDLL:
         "mx_rotate_quantize": (i32, [p, i64, i64, p, i32, i32, i32, i32, i32, p, p, p]),
         "mx_quantize_grouped": (i32, [p, p, i32, i64, i64, i32, i32, i32, i32, p, p, p]),
         "mx_dequantize": (i32, [p, p, i64, i64, i32, i32, i32, p, p]),
+        "mx_nvfp4_scales_shape": (i32, [i64, i64, i32, pi64, pi64]),
+        "mx_quantize_nvfp4": (i32, [p, i64, i64, p, i32, p, i32, p, p, p]),
+        "mx_qdq_nvfp4": (i32, [p, i64, i64, p, i32, p, p, p]),
         "mx_rotate_debug": (i32, [p, i64, i64, p, i32, p, p]),
         "mx_device_errors": (i32, [ctypes.POINTER(ctypes.c_int)]),
     }
@@ -209,6 +212,43 @@ def mx_dequantize(codes, scales, K, fmt, layout=LINEAR, *, y=None, group=GROUP, 
         raise ValueError("y must be a contiguous CUDA bfloat16 tensor of M * K elements")
     _check(lib().mx_dequantize(_ptr(codes), _ptr(scales), M, K, fmt, group, layout, _ptr(y),
                                _stream_ptr(stream)))
+    return y
+
+
+def mx_nvfp4_scales_shape(M: int, K: int, layout: int = SWIZZLED) -> tuple[int, int]:
+    r, c = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().mx_nvfp4_scales_shape(M, K, layout, ctypes.byref(r), ctypes.byref(c)))
+    return r.value, c.value
+
+
+def _global_scale(gs) -> None:
+    if not (isinstance(gs, torch.Tensor) and gs.is_cuda and gs.dtype == torch.float32
+            and gs.numel() == 1):
+        raise TypeError("global_scale must be a CUDA float32 tensor of one element")
+
+
+def mx_quantize_nvfp4(x, global_scale, layout=SWIZZLED, H=None, *, codes=None, scales=None,
+                      stream=None):
+    """NVFP4 quantize (optionally rotating each g-chunk by H first) -> (codes, E4M3 scales)."""
+    M, K = _input(x)
+    _global_scale(global_scale)
+    g = _rotation(H) if H is not None else 0
+    codes = _codes_out(codes, x, M, K, E2M1)
+    scales = _scales_out(scales, x, *mx_nvfp4_scales_shape(M, K, layout))
+    _check(lib().mx_quantize_nvfp4(_ptr(x), M, K, _ptr(H), g, _ptr(global_scale), layout,
+                                   _ptr(codes), _ptr(scales), _stream_ptr(stream)))
+    return codes, scales
+
+
+def mx_qdq_nvfp4(x, global_scale, H=None, *, y=None, stream=None):
+    """NVFP4 quantize-dequantize bf16 [M, K] -> bf16 [M, K] (optionally rotated)."""
+    M, K = _input(x)
+    _global_scale(global_scale)
+    g = _rotation(H) if H is not None else 0
+    if y is None:
+        y = torch.empty_like(x)
+    _check(lib().mx_qdq_nvfp4(_ptr(x), M, K, _ptr(H), g, _ptr(global_scale), _ptr(y),
+                              _stream_ptr(stream)))
     return y
 
 

@@ -3,6 +3,7 @@
 #include <climits>
 #include <cstdint>
 
+#include "mx_device.cuh"
 #include "mx_launch.h"
 #include "mxq.h"
 
@@ -205,6 +206,93 @@ mx_status mx_quantize_grouped(const void* x, const int64_t* row_offsets, int E, 
   a.offsets = row_offsets;
   a.E = E;
   return from_cuda(mxq::launch_stream(fmt, false, layout == MX_SCALES_SWIZZLED, true, a,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+mx_status mx_nvfp4_scales_shape(int64_t M, int64_t K, int layout, int64_t* rows, int64_t* cols) {
+  if (!rows || !cols) return MX_ERR_NULL;
+  if (M < 0 || K < 0 || K % 32 != 0) return MX_ERR_SHAPE;
+  if (!valid_layout(layout)) return MX_ERR_UNSUPPORTED;
+  if (layout == MX_SCALES_LINEAR) {
+    *rows = M;
+    *cols = K / 16;
+  } else {
+    *rows = ceil_div(M, mxq::kTileRows) * mxq::kTileRows;
+    *cols = ceil_div(K, 64) * 4;
+  }
+  return MX_OK;
+}
+
+namespace {
+
+// Shared by the two NVFP4 calls: validation of x, H and the global scale. Returns MX_OK to go
+// on; *empty is set when there is nothing to compute.
+mx_status check_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g,
+                      const float* global_scale, bool* empty) {
+  mx_status st = check_common(M, K, MX_FMT_E2M1, 32, MX_ROUND_RNE, empty);
+  if (st != MX_OK) return st;
+  if (H) {
+    if (!valid_g(g)) return MX_ERR_UNSUPPORTED;
+    if (K % g != 0 || !fits_tensor_map(M, K)) return MX_ERR_SHAPE;
+  }
+  if (*empty) return MX_OK;
+  if (!x || !global_scale) return MX_ERR_NULL;
+  if (!aligned32(x) || (reinterpret_cast<uintptr_t>(global_scale) & 3u)) return MX_ERR_ALIGN;
+  if (H && !aligned16(H)) return MX_ERR_ALIGN;
+  return MX_OK;
+}
+
+}  // namespace
+
+mx_status mx_quantize_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g,
+                            const float* global_scale, int layout, void* codes, void* scales,
+                            void* stream) {
+  if (!valid_layout(layout)) return MX_ERR_UNSUPPORTED;
+  bool empty = false;
+  mx_status st = check_nvfp4(x, M, K, H, g, global_scale, &empty);
+  if (st != MX_OK || empty) return st;
+  if (!codes || !scales) return MX_ERR_NULL;
+  if (!aligned32(codes)) return MX_ERR_ALIGN;
+  if (layout == MX_SCALES_SWIZZLED ? !aligned16(scales)
+                                   : (reinterpret_cast<uintptr_t>(scales) & 1u) != 0) {
+    return MX_ERR_ALIGN;
+  }
+  int64_t srows = 0, scols = 0;
+  mx_nvfp4_scales_shape(M, K, layout, &srows, &scols);
+  const bool swz = layout == MX_SCALES_SWIZZLED;
+  if (H) {
+    mxq::RotArgs a = rot_args(x, M, K, H, codes);
+    a.scales = static_cast<uint8_t*>(scales);
+    a.scale_cols = scols;
+    a.gscale = global_scale;
+    return from_cuda(mxq::launch_rotate(mxq::kFmtNVFP4, mxq::kRotCodes, swz, g, a,
+                                        static_cast<cudaStream_t>(stream)));
+  }
+  mxq::StreamArgs a = stream_args(x, M, K, codes);
+  a.scales = static_cast<uint8_t*>(scales);
+  a.scale_cols = scols;
+  a.scale_rows = srows;
+  a.gscale = global_scale;
+  return from_cuda(mxq::launch_stream(mxq::kFmtNVFP4, false, swz, false, a,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+mx_status mx_qdq_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g,
+                       const float* global_scale, void* y, void* stream) {
+  bool empty = false;
+  mx_status st = check_nvfp4(x, M, K, H, g, global_scale, &empty);
+  if (st != MX_OK || empty) return st;
+  if (!y) return MX_ERR_NULL;
+  if (!aligned32(y)) return MX_ERR_ALIGN;
+  if (H) {
+    mxq::RotArgs a = rot_args(x, M, K, H, y);
+    a.gscale = global_scale;
+    return from_cuda(mxq::launch_rotate(mxq::kFmtNVFP4, mxq::kRotQdq, false, g, a,
+                                        static_cast<cudaStream_t>(stream)));
+  }
+  mxq::StreamArgs a = stream_args(x, M, K, y);
+  a.gscale = global_scale;
+  return from_cuda(mxq::launch_stream(mxq::kFmtNVFP4, true, false, false, a,
                                       static_cast<cudaStream_t>(stream)));
 }
 

@@ -18,6 +18,7 @@ namespace mxq {
 
 constexpr int kFmtE2M1 = 1;
 constexpr int kFmtE4M3 = 2;
+constexpr int kFmtNVFP4 = 3;  // E2M1 elements, 16-element blocks, E4M3 scales, fp32 global scale
 
 template <int FMT>
 struct FormatTraits;
@@ -28,6 +29,10 @@ struct FormatTraits<kFmtE2M1> {
 template <>
 struct FormatTraits<kFmtE4M3> {
   static constexpr uint32_t emax = 8;
+};
+template <>
+struct FormatTraits<kFmtNVFP4> {  // element format E2M1; the block scale is not a power of two
+  static constexpr uint32_t emax = 2;
 };
 
 // ------------------------------------------------------------------------------------------
@@ -73,6 +78,23 @@ __device__ __forceinline__ uint32_t absmax_bf16x8(const uint4& v) {
   asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z), "r"(v.w));
   asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
   return max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
+}
+
+// abs-max of 16 fp32 values as sign-free fp32 bits; NaN propagates.
+__device__ __forceinline__ uint32_t absmax_f32x16(const float* y) {
+  float m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(m[i]) : "f"(y[2 * i]), "f"(y[2 * i + 1]));
+  }
+#pragma unroll
+  for (int w = 4; w >= 1; w >>= 1) {
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(m[i]) : "f"(m[i]), "f"(m[i + w]));
+    }
+  }
+  return __float_as_uint(m[0]) & 0x7FFFFFFFu;
 }
 
 // abs-max of 32 fp32 values as sign-free fp32 bits; NaN propagates.
@@ -198,6 +220,54 @@ __device__ __forceinline__ void store32B(void* p, const uint32_t* r) {
   asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]),
                "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                : "memory");
+}
+
+// ------------------------------------------------------------------------------------------
+// NVFP4 block scales. For a block of 16 values with abs-max amax under the global scale gs,
+// every step is one fp32 operation rounded to nearest even, in this order:
+//   s_f = amax * r6 (r6 = gs / 6);  sc = E4M3(s_f), saturating at 448;
+//   enc = gs / decode(sc);  code_i = E2M1(v_i * enc);
+//   QDQ: y_i = bf16(decode(code_i) * dq), dq = decode(sc) / gs;
+// enc and dq are 0 when decode(sc) is 0. A block holding a NaN or an infinity gets scale byte
+// 0x7F (the E4M3 NaN), codes 0 and QDQ outputs 0x7FC0 (the caller applies these fills).
+// ------------------------------------------------------------------------------------------
+struct NvScales {
+  uint32_t bytes;  // E4M3 scale bytes of two consecutive blocks, the first in the low byte
+  float enc[2];
+  float dq[2];
+  bool special[2];
+};
+
+// two E4M3 bytes (low byte first) -> exact fp32 values (every finite E4M3 value is an f16)
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t pair, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 c, a, b;\n\t.reg .b32 h;\n\tcvt.u16.u32 c, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h, c;\n\tmov.b32 {a, b}, h;\n\t"
+      "cvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(pair));
+}
+
+// amax0/amax1: sign-free fp32 bits of the two blocks' abs-max (Inf/NaN at or above 0x7F800000)
+__device__ __forceinline__ NvScales nv_scales(uint32_t amax0, uint32_t amax1, float gs, float r6) {
+  NvScales n;
+  const float s0 = __fmul_rn(__uint_as_float(amax0), r6);
+  const float s1 = __fmul_rn(__uint_as_float(amax1), r6);
+  uint32_t pair;
+  asm("{\n\t.reg .b16 c;\n\tcvt.rn.satfinite.e4m3x2.f32 c, %1, %2;\n\tcvt.u32.u16 %0, c;\n\t}"
+      : "=r"(pair)
+      : "f"(s1), "f"(s0));
+  n.special[0] = amax0 >= 0x7F800000u;
+  n.special[1] = amax1 >= 0x7F800000u;
+  if (n.special[0]) pair = (pair & 0xFF00u) | 0x007Fu;
+  if (n.special[1]) pair = (pair & 0x00FFu) | 0x7F00u;
+  float d0, d1;
+  e4m3x2_to_f32(pair, d0, d1);
+  n.enc[0] = d0 == 0.0f ? 0.0f : __fdiv_rn(gs, d0);
+  n.enc[1] = d1 == 0.0f ? 0.0f : __fdiv_rn(gs, d1);
+  n.dq[0] = d0 == 0.0f ? 0.0f : __fdiv_rn(d0, gs);
+  n.dq[1] = d1 == 0.0f ? 0.0f : __fdiv_rn(d1, gs);
+  n.bytes = pair;
+  return n;
 }
 
 // Swizzled scale position of (r, c) inside one 128x4 tile.

@@ -21,9 +21,11 @@ struct StreamArgs {
   int64_t scale_rows;      // rows of the scale buffer
   const int64_t* offsets;  // grouped only: device int64 [E + 1]
   int E;
+  const float* gscale;     // NVFP4 only: device fp32 global scale
 };
 
-// fmt: 1 = E2M1, 2 = E4M3. qdq: write bf16 QDQ instead of codes + scales.
+// fmt: 1 = E2M1, 2 = E4M3, 3 = NVFP4 (not grouped). qdq: write bf16 QDQ instead of codes +
+// scales.
 cudaError_t launch_stream(int fmt, bool qdq, bool swizzled, bool grouped, const StreamArgs& a,
                           cudaStream_t stream);
 
@@ -50,6 +52,7 @@ struct RotArgs {
   int64_t col_tiles;
   int64_t row_blocks;
   int64_t scale_cols;
+  const float* gscale;  // NVFP4 only: device fp32 global scale
 };
 
 cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const RotArgs& a,

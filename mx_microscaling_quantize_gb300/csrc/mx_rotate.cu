@@ -213,6 +213,31 @@ __host__ __device__ constexpr int block_out_words() {
   return OUT == kRotQdq ? 16 : (FMT == kFmtE4M3 ? 8 : 4);
 }
 
+// NVFP4 (two 16-element blocks per 32 values): returns both E4M3 scale bytes, low byte first.
+template <int OUT>
+__device__ __forceinline__ uint32_t nv_block_outputs(float* y, uint32_t* out, float gs, float r6) {
+  const NvScales n = nv_scales(absmax_f32x16(y), absmax_f32x16(y + 16), gs, r6);
+  const bool special = __any_sync(0xFFFFFFFFu, n.special[0] || n.special[1]);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) mul2(y[2 * i], y[2 * i + 1], n.enc[i >> 3]);  // y <- y * enc
+  if (OUT == kRotQdq) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) out[i] = qdq2_e2m1(y[2 * i], y[2 * i + 1], n.dq[i >> 3]);
+    if (special) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) out[i] = n.special[i >> 3] ? kBf16NaNx2 : out[i];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = codes8_e2m1(y + 8 * i);
+    if (special) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) out[i] = n.special[i >> 1] ? 0u : out[i];
+    }
+  }
+  return n.bytes;
+}
+
 template <int FMT, int OUT>
 __device__ __forceinline__ uint32_t block_outputs(float* y, uint32_t* out) {
   const uint32_t byte = scale_byte_from_amax_bits<FMT>(absmax_f32x32(y));
@@ -254,11 +279,17 @@ template <int FMT, int OUT>
 __host__ __device__ constexpr int out_stage_bytes() {
   return OUT == kRotDebug ? 0 : kTileRows * block_out_words<FMT, OUT>() * 4 * 4;
 }
+// Swizzled scale tiles staged per 128x128 tile when codes are written: one 512-byte 128x4 tile
+// (4 scale columns) for the MX formats, two for NVFP4 (8 scale columns of 16-element blocks).
+template <int FMT, int OUT>
+__host__ __device__ constexpr int scale_stage_bytes() {
+  return OUT != kRotCodes ? 0 : (FMT == kFmtNVFP4 ? 1024 : 512);
+}
 template <int FMT, int G, int OUT>
 __host__ __device__ constexpr int smem_request() {
   // 1 KiB of slack for aligning the stage ring to 1024 bytes
   return 1024 + stages<FMT, G, OUT>() * kStageBytes + 2 * out_stage_bytes<FMT, OUT>() + G * G * 2 +
-         2 * 512 + (2 * stages<FMT, G, OUT>() + 2 * kAcc + 1) * 8 + 16;
+         2 * scale_stage_bytes<FMT, OUT>() + (2 * stages<FMT, G, OUT>() + 2 * kAcc + 1) * 8 + 16;
 }
 constexpr int kMaxSmemPerCta = 232448;  // opt-in dynamic shared memory limit of the SM
 
@@ -273,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sA = smem;                                  // kStages x (two swizzled boxes)
   uint8_t* sOut = smem + kStages * kStageBytes;        // [2] output tiles, written back by TMA
   uint8_t* sB = sOut + 2 * out_stage_bytes<FMT, OUT>();  // H^T, core-matrix layout
-  uint8_t* s_scale = sB + G * G * 2;                     // [2][512] swizzled scale tiles
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_scale + 2 * 512);
+  uint8_t* s_scale = sB + G * G * 2;  // [2][scale_stage_bytes] swizzled scale tiles
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_scale + 2 * scale_stage_bytes<FMT, OUT>());
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + kAcc;
@@ -403,6 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quad * 32 + lane;     // tile row of this thread
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     constexpr int kWords = block_out_words<FMT, OUT>();
+    constexpr bool kNv = FMT == kFmtNVFP4;
+    float gs = 0.0f, r6 = 0.0f;  // NVFP4 global scale and gs / 6
+    if (kNv && OUT != kRotDebug) {
+      gs = __ldg(a.gscale);
+      r6 = __fdiv_rn(gs, 6.0f);
+    }
     int it = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
       const int acc = it % kAcc;
@@ -430,13 +467,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint32_t o[kWords];
       uint32_t byte = 0;  // pad rows / columns of the swizzled scale tile stay zero
-      if (active) byte = block_outputs<FMT, OUT>(y, o);
-      if (OUT == kRotCodes && !SWZ && active && row_ok) {
-        a.scales[(row0 + r) * a.scale_cols + cb * 4 + q] = (uint8_t)byte;  // linear scales
+      if (active) {
+        if constexpr (kNv) byte = nv_block_outputs<OUT>(y, o, gs, r6);
+        else byte = block_outputs<FMT, OUT>(y, o);
+      }
+      if (OUT == kRotCodes && !SWZ && active && row_ok) {  // linear scales
+        if (kNv) {
+          *reinterpret_cast<uint16_t*>(a.scales + (row0 + r) * a.scale_cols + cb * 8 + 2 * q) =
+              (uint16_t)byte;
+        } else {
+          a.scales[(row0 + r) * a.scale_cols + cb * 4 + q] = (uint8_t)byte;
+        }
       }
       // staged tiles alternate; the stores issued two tiles ago (same buffers) have read them
       uint8_t* out_tile = sOut + (it & 1) * out_stage_bytes<FMT, OUT>();
-      uint8_t* scale_tile = s_scale + (it & 1) * 512;
+      uint8_t* scale_tile = s_scale + (it & 1) * scale_stage_bytes<FMT, OUT>();
       if (e == 0 && lane == 0) bulk_wait_read_all_but_one();
       epilogue_sync();
       if (active) {
@@ -464,7 +509,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
-      if (OUT == kRotCodes && SWZ) scale_tile[swizzle_in_tile(r, q)] = (uint8_t)byte;
+      if (OUT == kRotCodes && SWZ) {
+        if (kNv) {  // scale columns 2q, 2q + 1: 128x4 tile q / 2, adjacent bytes
+          *reinterpret_cast<uint16_t*>(scale_tile + (q >> 1) * 512 +
+                                       swizzle_in_tile(r, (2 * q) & 3)) = (uint16_t)byte;
+        } else {
+          scale_tile[swizzle_in_tile(r, q)] = (uint8_t)byte;
+        }
+      }
       fence_proxy_async_smem();
       epilogue_sync();
       if (e == 0 && lane == 0) {
@@ -477,7 +529,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           tma_store_2d(&ymap, (int)(cb * kTileCols / 2), (int)row0, src);
         }
-        if (OUT == kRotCodes && SWZ) bulk_store_s2g(a.scales + t * 512, smem_u32(scale_tile), 512);
+        if (OUT == kRotCodes && SWZ) {
+          if (kNv) {  // 128x4 tiles 2 cb and 2 cb + 1 of row block rb (the second may not exist)
+            const int64_t per_rb = a.scale_cols / 4, first = 2 * cb;
+            const uint32_t bytes = first + 1 < per_rb ? 1024u : 512u;
+            bulk_store_s2g(a.scales + (rb * per_rb + first) * 512, smem_u32(scale_tile), bytes);
+          } else {
+            bulk_store_s2g(a.scales + t * 512, smem_u32(scale_tile), 512);
+          }
+        }
         bulk_commit();
       }
     }
@@ -572,6 +632,7 @@ cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const Rot
                           cudaStream_t stream) {
   if (out_kind == kRotDebug) return launch_g<kFmtE2M1, kRotDebug, false>(g, a, stream);
   if (fmt == kFmtE2M1) return launch_fmt<kFmtE2M1>(out_kind, swizzled, g, a, stream);
+  if (fmt == kFmtNVFP4) return launch_fmt<kFmtNVFP4>(out_kind, swizzled, g, a, stream);
   return launch_fmt<kFmtE4M3>(out_kind, swizzled, g, a, stream);
 }
 

@@ -101,6 +101,62 @@ __device__ __forceinline__ uint32_t block_kernel(const uint32_t* w, bool ok, voi
   return byte;
 }
 
+// abs-max of 8 bf16x2 words (one 16-element block) as sign-free bf16 bits; NaN propagates.
+__device__ __forceinline__ uint32_t absmax_words8(const uint32_t* w) {
+  uint32_t m[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[i]) : "r"(w[2 * i]), "r"(w[2 * i + 1]));
+  }
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[0]) : "r"(m[0]), "r"(m[2]));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[1]) : "r"(m[1]), "r"(m[3]));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[0]) : "r"(m[0]), "r"(m[1]));
+  return max(m[0] & 0x7FFFu, (m[0] >> 16) & 0x7FFFu);
+}
+
+// NVFP4: the 32 values in w[16] are two 16-element blocks. Writes their codes (16 bytes) or
+// QDQ bf16 (64 bytes) through `out`; returns the two E4M3 scale bytes (first in the low byte).
+template <bool QDQ>
+__device__ __forceinline__ uint32_t nv_block_kernel(const uint32_t* w, void* out, float gs,
+                                                    float r6) {
+  const NvScales n = nv_scales(absmax_words8(w) << 16, absmax_words8(w + 8) << 16, gs, r6);
+  const bool special = __any_sync(__activemask(), n.special[0] || n.special[1]);
+  if (QDQ) {
+    uint32_t o[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float lo = bf16_lo(w[i]), hi = bf16_hi(w[i]);
+      mul2(lo, hi, n.enc[i >> 3]);
+      o[i] = qdq2_e2m1(lo, hi, n.dq[i >> 3]);
+    }
+    if (special) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i] = n.special[i >> 3] ? kBf16NaNx2 : o[i];
+    }
+    store32B(out, o);
+    store32B(static_cast<uint8_t*>(out) + 32, o + 8);
+  } else {
+    uint32_t c[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float t[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        t[2 * i] = bf16_lo(w[4 * q + i]);
+        t[2 * i + 1] = bf16_hi(w[4 * q + i]);
+        mul2(t[2 * i], t[2 * i + 1], n.enc[q >> 1]);
+      }
+      c[q] = codes8_e2m1(t);
+    }
+    if (special) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) c[q] = n.special[q >> 1] ? 0u : c[q];
+    }
+    __stcs(static_cast<uint4*>(out), make_uint4(c[0], c[1], c[2], c[3]));
+  }
+  return n.bytes;
+}
+
 // largest e in [0, n) with v[e] <= key (v[0] <= key assumed)
 __device__ __forceinline__ int last_not_above(const int64_t* v, int n, int64_t key) {
   int lo = 0, hi = n;
@@ -118,7 +174,13 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
   __shared__ int64_t s_prow[GROUPED ? kMaxExperts + 1 : 1];  // first padded scale row of e
   __shared__ int64_t s_warp[kThreads / 32];
   const int tid = threadIdx.x;
-  constexpr int kCodeBytes = QDQ ? 64 : (FMT == kFmtE2M1 ? 16 : 32);  // output bytes per block
+  constexpr bool kNv = FMT == kFmtNVFP4;
+  constexpr int kCodeBytes = QDQ ? 64 : (FMT == kFmtE4M3 ? 32 : 16);  // output bytes per block
+  float gs = 0.0f, r6 = 0.0f;  // NVFP4 global scale and gs / 6
+  if (kNv) {
+    gs = __ldg(a.gscale);
+    r6 = __fdiv_rn(gs, 6.0f);
+  }
 
   if (GROUPED) {
     // expert e owns ceil(n_e / 128) * 128 padded scale rows; s_prow is their prefix sum
@@ -192,9 +254,17 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
       load32B(x + bn * 64, nxt);
       load32B(x + bn * 64 + 32, nxt + 8);
     }
-    const uint32_t byte =
-        block_kernel<FMT, QDQ>(cur, true, static_cast<uint8_t*>(a.out) + b * kCodeBytes);
-    if (!QDQ) {
+    uint32_t byte;
+    if constexpr (kNv) {
+      byte = nv_block_kernel<QDQ>(cur, static_cast<uint8_t*>(a.out) + b * kCodeBytes, gs, r6);
+    } else {
+      byte = block_kernel<FMT, QDQ>(cur, true, static_cast<uint8_t*>(a.out) + b * kCodeBytes);
+    }
+    if (kNv && !QDQ) {
+      // two scale bytes, NVFP4 blocks 2 * col and 2 * col + 1: adjacent in both layouts
+      const int64_t off = SWZ ? swizzled_offset(row, 2 * col, a.scale_cols) : 2 * b;
+      *reinterpret_cast<uint16_t*>(a.scales + off) = (uint16_t)byte;
+    } else if (!QDQ) {
       if (!SWZ) {
         a.scales[b] = (uint8_t)byte;  // linear [M, K/32] == flat block order
       } else {
@@ -226,10 +296,11 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
     // (row, word) items, so that a few wide pad rows do not serialize on a few threads; rows
     // past an expert's rows inside its last 128-row block: one thread per scale row).
     const int64_t cp = a.scale_cols, cp4 = cp >> 2;
+    const int64_t dcols = kNv ? 2 * cblk : cblk;  // scale columns holding data
     const int64_t nthr = (int64_t)gridDim.x * kThreads;
     const int64_t t0 = (int64_t)blockIdx.x * kThreads + tid;
-    if (cblk & 3) {
-      const int64_t c4 = cblk & ~int64_t(3);
+    if (dcols & 3) {
+      const int64_t c4 = dcols & ~int64_t(3);
       for (int64_t r = t0; r < a.M; r += nthr) {
         int64_t pr = r;
         if (GROUPED) {
@@ -239,7 +310,7 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
           if (pr >= a.scale_rows) continue;
         }
         uint8_t* run = a.scales + swizzled_offset(pr, c4, cp);
-        for (int64_t c = cblk; c < c4 + 4; ++c) run[c - c4] = 0;
+        for (int64_t c = dcols; c < c4 + 4; ++c) run[c - c4] = 0;
       }
     }
     if (!GROUPED) {
@@ -290,8 +361,12 @@ cudaError_t launch_t(const StreamArgs& a, cudaStream_t stream) {
 template <int FMT>
 cudaError_t launch_fmt(bool qdq, bool swz, bool grouped, const StreamArgs& a, cudaStream_t st) {
   if (qdq) return launch_t<FMT, true, false, false>(a, st);
-  if (grouped) {
-    return swz ? launch_t<FMT, false, true, true>(a, st) : launch_t<FMT, false, false, true>(a, st);
+  if constexpr (FMT != kFmtNVFP4) {
+    if (grouped) {
+      return swz ? launch_t<FMT, false, true, true>(a, st) : launch_t<FMT, false, false, true>(a, st);
+    }
+  } else {
+    if (grouped) return cudaErrorInvalidValue;
   }
   return swz ? launch_t<FMT, false, true, false>(a, st) : launch_t<FMT, false, false, false>(a, st);
 }
@@ -301,6 +376,7 @@ cudaError_t launch_fmt(bool qdq, bool swz, bool grouped, const StreamArgs& a, cu
 cudaError_t launch_stream(int fmt, bool qdq, bool swizzled, bool grouped, const StreamArgs& a,
                           cudaStream_t stream) {
   if (fmt == kFmtE2M1) return launch_fmt<kFmtE2M1>(qdq, swizzled, grouped, a, stream);
+  if (fmt == kFmtNVFP4) return launch_fmt<kFmtNVFP4>(qdq, swizzled, grouped, a, stream);
   return launch_fmt<kFmtE4M3>(qdq, swizzled, grouped, a, stream);
 }
 

@@ -235,3 +235,93 @@ def check_rotated_qdq(x_bits, H_bits, fmt, out_gpu_bits):
         assert ok, f"rotated QDQ block (row {r}, block {j}) outside tolerance"
         exempt += 1
     return {"blocks": M * K // 32, "exempt_blocks": exempt}
+
+
+# ---------------------------------------------------------------------------------------------
+# NVFP4: rotated-path tolerance rules (blocks of 16, E4M3 scale under the global scale gs)
+# ---------------------------------------------------------------------------------------------
+_E4M3_VALUES = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+_E2M1_VALUES = np.array([O.decode(O.E2M1, c) for c in range(16)])
+
+
+def e4m3_cast(v: np.ndarray) -> np.ndarray:
+    """Non-negative fp32 values -> E4M3 bytes, nearest even, saturating at 448."""
+    v = np.minimum(np.asarray(v, dtype=np.float32), np.float32(448.0))
+    return torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def nvfp4_scale_candidates(amax: float, tb: float, gs: np.float32) -> set:
+    """Scale bytes reachable by rounding s_f = amax' * (gs / 6) for amax' within tb of amax."""
+    f = np.float32
+    r6 = f(gs) / f(6.0)
+    lo = f(max(amax - tb, 0.0)) * r6 * f(1 - 2.0 ** -22)
+    hi = f(amax + tb) * r6 * f(1 + 2.0 ** -22)
+    b_lo, b_hi = e4m3_cast(np.array([lo, hi]))
+    return set(range(int(b_lo), int(b_hi) + 1))
+
+
+def _nvfp4_block_ok(yb, tb, gs, gpu_codes, gpu_byte, ref_byte) -> tuple[bool, int]:
+    f = np.float32
+    if gpu_byte != ref_byte and gpu_byte not in nvfp4_scale_candidates(np.abs(yb).max(), tb.max(), gs):
+        return False, 0
+    s_dec = f(_E4M3_VALUES[gpu_byte])
+    enc = f(gs) / s_dec if s_dec != 0 else f(0.0)
+    t = yb.astype(np.float32) * enc
+    _, rc = O.quantize_block(O.E2M1, t.astype(np.float64), forced_byte=127)
+    diff = np.nonzero(rc != gpu_codes)[0]
+    for i in diff:
+        a, b = _E2M1_VALUES[rc[i]], _E2M1_VALUES[gpu_codes[i]]
+        if not _neighbours(O.E2M1, _E2M1_VALUES, a, b):
+            return False, 0
+        slack = float(tb[i]) * float(enc) * 1.001 + 4 * float(np.spacing(np.float32(abs(t[i]))))
+        if abs(float(t[i]) - (a + b) / 2) > slack:
+            return False, 0
+    return True, len(diff)
+
+
+def check_rotated_nvfp4(x_bits, H_bits, gs, codes_gpu, scales_gpu_linear):
+    y = O.rotate(x_bits, H_bits)
+    tol = rotation_tolerance(y, H_bits.shape[0])
+    M, K = y.shape
+    rc, rs = O.nvfp4_quantize(x_bits, gs, O.LINEAR, H_bits=H_bits)
+    gc, rce = unpack_codes(codes_gpu, O.E2M1), unpack_codes(rc, O.E2M1)
+    bad = np.nonzero((rs != scales_gpu_linear) | (gc != rce).reshape(M, K // 16, 16).any(axis=2))
+    flips = 0
+    for r, j in zip(*bad):
+        sl = slice(16 * j, 16 * j + 16)
+        ok, _ = _nvfp4_block_ok(y[r, sl], tol[r, sl], gs, gc[r, sl], int(scales_gpu_linear[r, j]),
+                                int(rs[r, j]))
+        assert ok, (f"NVFP4 block (row {r}, block {j}) outside tolerance: gpu scale "
+                    f"{scales_gpu_linear[r, j]:#x} ref {rs[r, j]:#x}")
+        flips += int(scales_gpu_linear[r, j] != rs[r, j])
+    return {"blocks": M * K // 16, "exempt_blocks": len(bad[0]), "scale_flips": flips}
+
+
+def check_rotated_nvfp4_qdq(x_bits, H_bits, gs, out_gpu_bits):
+    y = O.rotate(x_bits, H_bits)
+    tol = rotation_tolerance(y, H_bits.shape[0])
+    M, K = y.shape
+    ref = O.nvfp4_qdq(x_bits, gs, H_bits=H_bits)
+    _, rs = O.nvfp4_quantize(x_bits, gs, O.LINEAR, H_bits=H_bits)
+    bad = np.nonzero((ref != out_gpu_bits).reshape(M, K // 16, 16).any(axis=2))
+    for r, j in zip(*bad):
+        sl = slice(16 * j, 16 * j + 16)
+        yb, tb, ob = y[r, sl], tol[r, sl], out_gpu_bits[r, sl]
+        ok = False
+        for b in sorted(nvfp4_scale_candidates(np.abs(yb).max(), tb.max(), gs) | {int(rs[r, j])}):
+            table = {c: O.nvfp4_dequant_bf16(c, b, float(gs)) for c in range(16)}
+            codes = []
+            for i in range(16):
+                cands = [c for c in range(16) if table[c] == ob[i]]
+                if not cands:
+                    break
+                codes.append(cands[0])
+            if len(codes) == 16:
+                # among codes with equal outputs (e.g. +0 / -0) any is fine: try the ref's first
+                _, rc = O.nvfp4_block(yb.astype(np.float32), gs)
+                codes = [int(rc[i]) if table[int(rc[i])] == ob[i] else codes[i] for i in range(16)]
+                if _nvfp4_block_ok(yb, tb, gs, np.array(codes), b, int(rs[r, j]))[0]:
+                    ok = True
+                    break
+        assert ok, f"rotated NVFP4 QDQ block (row {r}, block {j}) outside tolerance"
+    return {"blocks": M * K // 16, "exempt_blocks": len(bad[0])}

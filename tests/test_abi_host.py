@@ -159,6 +159,30 @@ def test_dequantize_validation(L):
     assert d(P, P, 1 << 40, 1 << 20, 1, 32, 0, P, None) == SHAPE
 
 
+def test_nvfp4_shapes_and_validation(L):
+    assert mxq.mx_nvfp4_scales_shape(1, 32, mxq.SWIZZLED) == (128, 4)
+    assert mxq.mx_nvfp4_scales_shape(300, 416, mxq.SWIZZLED) == (384, 28)
+    assert mxq.mx_nvfp4_scales_shape(300, 416, mxq.LINEAR) == (300, 26)
+    q = L.mx_quantize_nvfp4  # (x, M, K, H, g, gs, layout, codes, scales, stream)
+    assert q(P, 4, 48, None, 0, P, 0, P, P, None) == SHAPE
+    assert q(P, 4, 64, None, 0, P, 2, P, P, None) == UNSUP
+    assert q(P, 4, 64, P, 8, P, 0, P, P, None) == UNSUP
+    assert q(P, 4, 96, P, 64, P, 0, P, P, None) == SHAPE
+    assert q(P, 4, 64, None, 0, None, 0, P, P, None) == NULL
+    assert q(None, 4, 64, None, 0, P, 0, P, P, None) == NULL
+    assert q(P, 4, 64, None, 0, P, 0, None, P, None) == NULL
+    assert q(P, 4, 64, None, 0, P + 2, 0, P, P, None) == ALIGN
+    assert q(P, 4, 64, None, 0, P, 0, P + 16, P, None) == ALIGN
+    assert q(P, 4, 64, None, 0, P, 0, P, P + 1, None) == ALIGN
+    assert q(P, 4, 64, None, 0, P, 1, P, P + 2, None) == ALIGN
+    assert q(P, 4, 64, P + 8, 32, P, 1, P, P, None) == ALIGN
+    assert q(None, 0, 64, None, 0, None, 1, None, None, None) == OK
+    d = L.mx_qdq_nvfp4  # (x, M, K, H, g, gs, y, stream)
+    assert d(P, 4, 64, None, 0, P, None, None) == NULL
+    assert d(P, 4, 64, None, 0, P, P + 16, None) == ALIGN
+    assert d(P, -1, 64, None, 0, P, P, None) == SHAPE
+
+
 def test_device_errors_null(L):
     assert L.mx_device_errors(None) == NULL
 

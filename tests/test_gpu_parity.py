@@ -233,6 +233,125 @@ def test_dequantize_of_quantize_is_qdq_full_size(fmt, layout):
 
 
 # ---------------------------------------------------------------------------------------------
+# NVFP4 (16-element blocks, E4M3 scales under a global scale)
+# ---------------------------------------------------------------------------------------------
+def gs_of(xb) -> np.float32:
+    """The usual global scale 448 * 6 / amax(x) (1 for an all-zero x: gs must be finite)."""
+    amax = np.float32(np.abs(W.bf16_bits_to_float(xb)).max())
+    return np.float32(448 * 6) / amax if amax > 0 else np.float32(1.0)
+
+
+def gs_tensor(gs):
+    return torch.tensor([float(gs)], dtype=torch.float32, device="cuda")
+
+
+def nv_quantize(xb, gs, layout, H=None):
+    c, s = mxq.mx_quantize_nvfp4(T.to_gpu(xb), gs_tensor(gs), layout,
+                                 None if H is None else T.to_gpu(H))
+    return T.u8(c), T.u8(s)
+
+
+def nv_qdq(xb, gs, H=None):
+    return T.bf16_bits(mxq.mx_qdq_nvfp4(T.to_gpu(xb), gs_tensor(gs),
+                                        None if H is None else T.to_gpu(H)))
+
+
+def assert_nvfp4_exact(xb, gs, H=None, layouts=LAYOUTS):
+    for layout in layouts:
+        c, s = nv_quantize(xb, gs, layout, H)
+        rc, rs = O.nvfp4_quantize(xb, gs, layout, H_bits=H)
+        np.testing.assert_array_equal(s, rs)
+        np.testing.assert_array_equal(c, rc)
+    np.testing.assert_array_equal(nv_qdq(xb, gs, H), O.nvfp4_qdq(xb, gs, H_bits=H))
+
+
+@pytest.mark.parametrize("M,K", [(1, 32), (3, 96), (127, 160), (129, 416), (300, 4096), (64, 8192)])
+def test_nvfp4_bit_exact(M, K):
+    xb = W.mxfp4_qdq_activation(M, K) if K % 1024 == 0 else W.mxfp8_linear_quant(M, K, stream=M + K)
+    for gs in (gs_of(xb), np.float32(1.0), np.float32(37.5)):
+        assert_nvfp4_exact(xb, gs)
+
+
+def test_nvfp4_special_underflow_and_saturation():
+    v = np.random.default_rng(41).standard_normal((4, 256)).astype(np.float32)
+    v[0, 5], v[1, 40], v[2, 70], v[3, 255] = np.nan, np.inf, -np.inf, np.nan
+    v[3, :16] = 0.0
+    v[3, 16:32] = -1e-30
+    xb = W.to_bf16_bits(v)
+    for gs in (np.float32(100.0), np.float32(1e-10), np.float32(6e6), np.float32(1e30)):
+        assert_nvfp4_exact(xb, gs)
+
+
+def test_nvfp4_every_scale_byte():
+    """gs = 6 makes s_f the block abs-max itself, so the converter sweep (every finite bf16 at
+    its own and every larger scale) reaches every E4M3 scale byte, saturation included."""
+    xs = T.converter_sweep()
+    assert_nvfp4_exact(xs, np.float32(6.0), layouts=[O.LINEAR])
+    _, s = nv_quantize(xs, np.float32(6.0), O.LINEAR)
+    assert set(np.unique(s)) >= set(range(0, 0x7F))
+
+
+def test_nvfp4_full_size_sampled_rows():
+    xb = W.mxfp4_qdq_weight()
+    gs = gs_of(xb)
+    x = T.to_gpu(xb)
+    c, s = mxq.mx_quantize_nvfp4(x, gs_tensor(gs), mxq.SWIZZLED)
+    y = mxq.mx_qdq_nvfp4(x, gs_tensor(gs))
+    rows = np.sort(np.random.default_rng(13).choice(xb.shape[0], 24, replace=False))
+    rc, rs = O.nvfp4_quantize(xb[rows], gs, O.LINEAR)
+    M, K = xb.shape
+    np.testing.assert_array_equal(T.unswizzle(T.u8(s), M, 2 * K)[rows], rs)
+    np.testing.assert_array_equal(T.u8(c)[rows], rc)
+    np.testing.assert_array_equal(T.bf16_bits(y[torch.from_numpy(rows).cuda()]),
+                                  O.nvfp4_qdq(xb[rows], gs))
+
+
+@pytest.mark.parametrize("g", [16, 32, 64, 128])
+def test_nvfp4_exact_rotations_bit_exact(g):
+    """Identity and signed-permutation H make the rotation exact in fp32: the rotated NVFP4
+    kernels then equal the oracle bit for bit."""
+    xb = W.mxfp4_qdq_activation(200, 512)
+    gs = gs_of(xb)
+    assert_nvfp4_exact(xb, gs, rotation(g, "identity"))
+    rng = np.random.default_rng(g)
+    P = np.zeros((g, g))
+    P[np.arange(g), rng.permutation(g)] = rng.choice([-1.0, 1.0], g)
+    Hp = W.to_bf16_bits(P)
+    assert_nvfp4_exact(xb, gs, Hp)
+    # the signed permutation moves values across blocks: not the plain path's result
+    assert not np.array_equal(O.nvfp4_qdq(xb, gs, H_bits=Hp), O.nvfp4_qdq(xb, gs))
+
+
+@pytest.mark.parametrize("g", [16, 32, 64, 128])
+def test_nvfp4_rotated_hadamard_rules(g):
+    xb = W.rotate_quant_activation(300, 1024)
+    H = rotation(g)
+    gs = np.float32(448 * 6) / np.float32(np.abs(O.rotate(xb, H)).max())
+    M, K = xb.shape
+    for layout in LAYOUTS:
+        c, s = nv_quantize(xb, gs, layout, H)
+        if layout == O.SWIZZLED:
+            assert not T.swizzle_pads(s, M, 2 * K).any()
+            s = T.unswizzle(s, M, 2 * K)
+        stats = T.check_rotated_nvfp4(xb, H, gs, c, s)
+        assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+    stats = T.check_rotated_nvfp4_qdq(xb, H, gs, nv_qdq(xb, gs, H))
+    assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+
+
+def test_nvfp4_rotated_full_size_sampled_rows():
+    M, K = 8192, 28672
+    xb = W.rotate_quant_activation(M, K)
+    H = rotation(16)
+    gs = np.float32(448 * 6 / 8.0)  # rotated N(0,1) values stay well below 8
+    c, s = nv_quantize(xb, gs, O.SWIZZLED, H)
+    s = T.unswizzle(s, M, 2 * K)
+    rows = np.sort(np.random.default_rng(17).choice(M, 12, replace=False))
+    stats = T.check_rotated_nvfp4(xb[rows], H, gs, c[rows], s[rows])
+    assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+
+
+# ---------------------------------------------------------------------------------------------
 # grouped (MoE) quantize
 # ---------------------------------------------------------------------------------------------
 def grouped(xb, offsets, fmt, layout):

@@ -79,3 +79,40 @@ def test_converter_sweep_covers_every_scale():
     assert xs.shape[1] == 2048 and xs.shape[0] > 4000
     fin = T.finite_bf16()
     assert np.isin(fin, xs).all()
+
+
+def nvfp4_gs(x_bits) -> np.float32:
+    return np.float32(448 * 6) / np.float32(np.abs(W.bf16_bits_to_float(x_bits)).max())
+
+
+def test_nvfp4_rules_accept_oracle_and_reject_planted_errors():
+    x = W.rotate_quant_activation(4, 256)
+    H = W.normalized_hadamard_bf16(32)
+    gs = nvfp4_gs(x)
+    c, s = O.nvfp4_quantize(x, gs, O.LINEAR, H_bits=H)
+    assert T.check_rotated_nvfp4(x, H, gs, c, s)["exempt_blocks"] == 0
+    assert T.check_rotated_nvfp4_qdq(x, H, gs, O.nvfp4_qdq(x, gs, H_bits=H))["exempt_blocks"] == 0
+    # a code two grid steps away
+    bad = c.copy()
+    nib = bad[1, 3] & 0xF
+    bad[1, 3] = (bad[1, 3] & 0xF0) | ((nib & 0x8) | ((nib & 7) + 2 if (nib & 7) < 6 else 0))
+    with pytest.raises(AssertionError):
+        T.check_rotated_nvfp4(x, H, gs, bad, s)
+    # a scale byte far from the rounding of s_f
+    bad_s = s.copy()
+    bad_s[2, 5] = min(int(bad_s[2, 5]) + 3, 0x7E)
+    with pytest.raises(AssertionError):
+        T.check_rotated_nvfp4(x, H, gs, c, bad_s)
+    # a QDQ output that no allowed code gives
+    q = O.nvfp4_qdq(x, gs, H_bits=H)
+    q[3, 17] ^= 0x0040
+    with pytest.raises(AssertionError):
+        T.check_rotated_nvfp4_qdq(x, H, gs, q)
+
+
+def test_nvfp4_scale_candidates_bracket_the_rounding():
+    gs = np.float32(6.0)  # r6 = 1: s_f = amax
+    assert T.nvfp4_scale_candidates(1.0, 0.0, gs) == {0x38}          # 1.0 exactly
+    # 1.0625 is the midpoint of 1.0 (0x38) and 1.125 (0x39): a tolerance around it allows both
+    assert T.nvfp4_scale_candidates(1.0625, 1e-6, gs) == {0x38, 0x39}
+    assert T.nvfp4_scale_candidates(1.03, 1e-6, gs) == {0x38}
