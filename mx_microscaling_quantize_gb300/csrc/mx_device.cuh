@@ -247,35 +247,19 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint32_t pair, float& lo, float& h
       : "r"(pair));
 }
 
-// Scale bytes of two blocks (first in the low byte) from the sign-free fp32 bits of their
-// abs-max (Inf/NaN at or above 0x7F800000: scale 0x7F and *_special set).
-__device__ __forceinline__ uint32_t nv_scale_bytes(uint32_t amax0, uint32_t amax1, float r6,
-                                                   bool* special) {
+// amax0/amax1: sign-free fp32 bits of the two blocks' abs-max (Inf/NaN at or above 0x7F800000)
+__device__ __forceinline__ NvScales nv_scales(uint32_t amax0, uint32_t amax1, float gs, float r6) {
+  NvScales n;
   const float s0 = __fmul_rn(__uint_as_float(amax0), r6);
   const float s1 = __fmul_rn(__uint_as_float(amax1), r6);
   uint32_t pair;
   asm("{\n\t.reg .b16 c;\n\tcvt.rn.satfinite.e4m3x2.f32 c, %1, %2;\n\tcvt.u32.u16 %0, c;\n\t}"
       : "=r"(pair)
       : "f"(s1), "f"(s0));
-  special[0] = amax0 >= 0x7F800000u;
-  special[1] = amax1 >= 0x7F800000u;
-  if (special[0]) pair = (pair & 0xFF00u) | 0x007Fu;
-  if (special[1]) pair = (pair & 0x00FFu) | 0x7F00u;
-  return pair;
-}
-
-// enc = gs / decode(byte) and dq = decode(byte) / gs of one scale byte (0 when it decodes to 0)
-__device__ __forceinline__ void nv_factors(uint32_t byte, float gs, float& enc, float& dq) {
-  float d, unused;
-  e4m3x2_to_f32(byte, d, unused);
-  enc = d == 0.0f ? 0.0f : __fdiv_rn(gs, d);
-  dq = d == 0.0f ? 0.0f : __fdiv_rn(d, gs);
-}
-
-// amax0/amax1: sign-free fp32 bits of the two blocks' abs-max (Inf/NaN at or above 0x7F800000)
-__device__ __forceinline__ NvScales nv_scales(uint32_t amax0, uint32_t amax1, float gs, float r6) {
-  NvScales n;
-  const uint32_t pair = nv_scale_bytes(amax0, amax1, r6, n.special);
+  n.special[0] = amax0 >= 0x7F800000u;
+  n.special[1] = amax1 >= 0x7F800000u;
+  if (n.special[0]) pair = (pair & 0xFF00u) | 0x007Fu;
+  if (n.special[1]) pair = (pair & 0x00FFu) | 0x7F00u;
   float d0, d1;
   e4m3x2_to_f32(pair, d0, d1);
   n.enc[0] = d0 == 0.0f ? 0.0f : __fdiv_rn(gs, d0);

@@ -116,19 +116,10 @@ __device__ __forceinline__ uint32_t absmax_words8(const uint32_t* w) {
 
 // NVFP4: the 32 values in w[16] are two 16-element blocks. Writes their codes (16 bytes) or
 // QDQ bf16 (64 bytes) through `out`; returns the two E4M3 scale bytes (first in the low byte).
-// t_enc / t_dq: gs / decode(b) and decode(b) / gs for every scale byte b < 128 (shared memory,
-// the same IEEE divisions done once per CTA).
 template <bool QDQ>
-__device__ __forceinline__ uint32_t nv_block_kernel(const uint32_t* w, void* out, float r6,
-                                                    const float* t_enc, const float* t_dq) {
-  NvScales n;
-  n.bytes = nv_scale_bytes(absmax_words8(w) << 16, absmax_words8(w + 8) << 16, r6, n.special);
-  n.enc[0] = t_enc[n.bytes & 0x7Fu];
-  n.enc[1] = t_enc[(n.bytes >> 8) & 0x7Fu];
-  if (QDQ) {
-    n.dq[0] = t_dq[n.bytes & 0x7Fu];
-    n.dq[1] = t_dq[(n.bytes >> 8) & 0x7Fu];
-  }
+__device__ __forceinline__ uint32_t nv_block_kernel(const uint32_t* w, void* out, float gs,
+                                                    float r6) {
+  const NvScales n = nv_scales(absmax_words8(w) << 16, absmax_words8(w + 8) << 16, gs, r6);
   const bool special = __any_sync(__activemask(), n.special[0] || n.special[1]);
   if (QDQ) {
     uint32_t o[16];
@@ -185,13 +176,10 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
   const int tid = threadIdx.x;
   constexpr bool kNv = FMT == kFmtNVFP4;
   constexpr int kCodeBytes = QDQ ? 64 : (FMT == kFmtE4M3 ? 32 : 16);  // output bytes per block
-  __shared__ float s_enc[kNv ? 128 : 1], s_dq[kNv ? 128 : 1];  // NVFP4 per-scale-byte factors
-  float r6 = 0.0f;                                               // NVFP4 gs / 6
+  float gs = 0.0f, r6 = 0.0f;  // NVFP4 global scale and gs / 6
   if (kNv) {
-    const float gs = __ldg(a.gscale);
+    gs = __ldg(a.gscale);
     r6 = __fdiv_rn(gs, 6.0f);
-    if (tid < 128) nv_factors((uint32_t)tid, gs, s_enc[tid], s_dq[tid]);
-    __syncthreads();
   }
 
   if (GROUPED) {
@@ -268,8 +256,7 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
     }
     uint32_t byte;
     if constexpr (kNv) {
-      byte = nv_block_kernel<QDQ>(cur, static_cast<uint8_t*>(a.out) + b * kCodeBytes, r6, s_enc,
-                                  s_dq);
+      byte = nv_block_kernel<QDQ>(cur, static_cast<uint8_t*>(a.out) + b * kCodeBytes, gs, r6);
     } else {
       byte = block_kernel<FMT, QDQ>(cur, true, static_cast<uint8_t*>(a.out) + b * kCodeBytes);
     }
