@@ -70,6 +70,7 @@ def _load():
         "mxo_nvfp4_dequant_bf16": (ctypes.c_uint16, [i32, i32, ctypes.c_float]),
         "mxo_nvfp4_quantize": (None, [p, i64, i64, p, i32, ctypes.c_float, i32, p, p]),
         "mxo_nvfp4_qdq": (None, [p, i64, i64, p, i32, ctypes.c_float, p]),
+        "mxo_nvfp4_dequantize": (None, [p, p, i64, i64, ctypes.c_float, i32, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -277,3 +278,13 @@ def nvfp4_qdq(x_bits, gs: float, H_bits=None) -> np.ndarray:
     _load().mxo_nvfp4_qdq(_ptr(x), M, K, None if H is None else _ptr(H),
                           0 if H is None else H.shape[0], float(np.float32(gs)), _ptr(out))
     return out
+
+
+def nvfp4_dequantize(codes, scales, K: int, gs: float, layout: int) -> np.ndarray:
+    """Stored NVFP4 codes [M, K/2] + E4M3 scales (linear or swizzled) -> bf16 bits [M, K]."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    s = np.ascontiguousarray(scales, dtype=np.uint8)
+    M = c.shape[0]
+    y = np.zeros((M, K), dtype=np.uint16)
+    _load().mxo_nvfp4_dequantize(_ptr(c), _ptr(s), M, K, float(np.float32(gs)), layout, _ptr(y))
+    return y

@@ -347,9 +347,12 @@ int nvfp4_block(const float* v, int n, float gs, uint8_t* codes) {
   return sc;
 }
 
+// decode(sc) is the signed E4M3 value of the scale byte (the quantizer only writes
+// non-negative ones; stored data given to the dequantize may carry the sign bit).
 uint16_t nvfp4_dequant_to_bf16(int code, int scale_byte, float gs) {
   if (scale_byte == 0x7F || scale_byte == 0xFF) return 0x7FC0;
-  const float s_dec = (float)kE4M3.magnitude[scale_byte & 0x7F];
+  const float s_mag = (float)kE4M3.magnitude[scale_byte & 0x7F];
+  const float s_dec = (scale_byte & 0x80) ? -s_mag : s_mag;
   const float dq = (s_dec == 0.0f) ? 0.0f : s_dec / gs;
   const float y = (float)decode_code(kE2M1, code) * dq;
   return double_to_bf16_rne((double)y);
@@ -534,6 +537,23 @@ void mxo_nvfp4_qdq(const uint16_t* x, int64_t M, int64_t K, const uint16_t* H, i
                    uint16_t* out) {
   std::vector<float> v = H ? doubles_to_float(rotate_rows(x, M, K, H, g)) : bf16_rows_to_float(x, M * K);
   nvfp4_rows(v.data(), M, K, gs, 0, 0, nullptr, nullptr, out);
+}
+
+// Stored NVFP4 data -> bf16: element k of row r is dequantized with the scale of its 16-element
+// block (linear [M, K/16] or swizzled as mxo_nvfp4_scales_shape says).
+void mxo_nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int64_t K,
+                          float gs, int layout, uint16_t* y) {
+  int64_t srows, scols;
+  mxo_nvfp4_scales_shape(M, K, layout, &srows, &scols);
+  for (int64_t r = 0; r < M; ++r) {
+    for (int64_t k = 0; k < K; ++k) {
+      const uint8_t b = codes[r * (K / 2) + k / 2];
+      const int code = (k % 2 == 0) ? (b & 0x0F) : (b >> 4);
+      const int64_t j = k / 16;
+      const int sc = layout == 0 ? scales[r * (K / 16) + j] : scales[swizzled_offset(r, j, scols)];
+      y[r * K + k] = nvfp4_dequant_to_bf16(code, sc, gs);
+    }
+  }
 }
 
 }  // extern "C"

@@ -431,6 +431,42 @@ def test_nvfp4_identity_rotation_and_layouts():
             assert q[r, k] == O.nvfp4_dequant_bf16(int(code), int(s0[r, k // 16]), float(gs))
 
 
+def test_nvfp4_dequantize_every_code_and_scale_in_fp32_steps():
+    """All 16 E2M1 codes under all 256 E4M3 scale bytes and three global scales: decode(code)
+    from the OCP value table, decode(scale) by torch's float8_e4m3fn (sign included), then the
+    two fp32 operations of the reading, dq = decode(scale) / gs and decode(code) * dq, in
+    numpy float32 (correctly rounded), and torch's float32 -> bfloat16 cast; NaN scale bytes
+    (0x7F, 0xFF) give 0x7FC0."""
+    K = 32
+    codes = np.tile(np.array([(2 * i) | ((2 * i + 1) << 4) for i in range(8)], np.uint8), (256, 2))
+    scales = np.repeat(np.arange(256, dtype=np.uint8)[:, None], 2, axis=1)
+    table = np.array(E2M1_SPEC_VALUES + [-v for v in E2M1_SPEC_VALUES], dtype=np.float32)
+    code_val = np.tile(table, (256, 2))
+    s_dec = torch.from_numpy(scales).view(torch.float8_e4m3fn).float().numpy()
+    for gs in (1.0, 0.3712, 2.0 ** -10 * 3.0):
+        g32 = np.float32(gs)
+        dq = np.where(s_dec == 0, np.float32(0), s_dec / g32).astype(np.float32)
+        y = (code_val * np.repeat(dq, 16, axis=1)).astype(np.float32)
+        want = torch_bf16_bits(torch.from_numpy(y))
+        nan = np.isnan(y)
+        want[nan] = 0x7FC0
+        got = O.nvfp4_dequantize(codes, scales, K, gs, O.LINEAR)
+        assert nan[0x7F].all() and nan[0xFF].all() and nan.sum() == 2 * K
+        np.testing.assert_array_equal(got, want)
+        assert (got[0x85] != got[0x05]).any()  # the scale's sign bit is honoured
+
+
+@pytest.mark.parametrize("rotated", [False, True])
+def test_nvfp4_dequantize_of_quantize_is_qdq(rotated):
+    x = W.mxfp4_qdq_activation(130, 512)
+    H = W.normalized_hadamard_bf16(32) if rotated else None
+    gs = np.float32(448 * 6) / np.float32(np.abs(W.bf16_bits_to_float(x)).max())
+    q = O.nvfp4_qdq(x, gs, H_bits=H)
+    for layout in (O.LINEAR, O.SWIZZLED):
+        c, s = O.nvfp4_quantize(x, gs, layout, H_bits=H)
+        np.testing.assert_array_equal(O.nvfp4_dequantize(c, s, 512, gs, layout), q)
+
+
 # ---------------------------------------------------------------------------------------------
 # layouts
 # ---------------------------------------------------------------------------------------------
