@@ -71,6 +71,7 @@ def _load():
         "mxo_nvfp4_quantize": (None, [p, i64, i64, p, i32, ctypes.c_float, i32, p, p]),
         "mxo_nvfp4_qdq": (None, [p, i64, i64, p, i32, ctypes.c_float, p]),
         "mxo_nvfp4_dequantize": (None, [p, p, i64, i64, ctypes.c_float, i32, p]),
+        "mxo_nvfp4_quantize_grouped": (None, [p, p, i32, i64, p, i32, i64, p, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -288,3 +289,23 @@ def nvfp4_dequantize(codes, scales, K: int, gs: float, layout: int) -> np.ndarra
     y = np.zeros((M, K), dtype=np.uint16)
     _load().mxo_nvfp4_dequantize(_ptr(c), _ptr(s), M, K, float(np.float32(gs)), layout, _ptr(y))
     return y
+
+
+def nvfp4_quantize_grouped(x_bits, offsets, gs, layout: int, scale_rows: int | None = None):
+    """Per-expert NVFP4 quantize. offsets: int64 [E+1] row offsets; gs: fp32 [E] global scales
+    (one per expert). -> (codes [M, K/2], scales: linear [M, K/16] or per-expert padded
+    swizzled [scale_rows, ceil(K/64)*4])."""
+    x = _bits(x_bits)
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    g = np.ascontiguousarray(gs, dtype=np.float32)
+    E = off.size - 1
+    M, K = x.shape
+    assert off[E] == M and g.size == E
+    if scale_rows is None:
+        scale_rows = grouped_scales_rows(np.diff(off), layout)
+    cols = nvfp4_scales_shape(0, K, layout)[1]
+    codes = np.zeros((M, K // 2), dtype=np.uint8)
+    scales = np.zeros((scale_rows, cols), dtype=np.uint8)
+    _load().mxo_nvfp4_quantize_grouped(_ptr(x), _ptr(off), E, K, _ptr(g), layout, scale_rows,
+                                       _ptr(codes), _ptr(scales))
+    return codes, scales

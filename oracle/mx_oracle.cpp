@@ -539,6 +539,29 @@ void mxo_nvfp4_qdq(const uint16_t* x, int64_t M, int64_t K, const uint16_t* H, i
   nvfp4_rows(v.data(), M, K, gs, 0, 0, nullptr, nullptr, out);
 }
 
+// Grouped (MoE) NVFP4 quantize: rows [offsets[e], offsets[e+1]) are expert e's input, quantized
+// under that expert's own global scale gs[e]. Codes stay in row order. Linear scales are
+// [M_total, K/16] in row order; swizzled scales give each expert its own run of 128-row tiles
+// starting at padded row P_e = sum_{e' < e} ceil(n_e' / 128) * 128 (pads zero), as for the MX
+// grouped layout.
+void mxo_nvfp4_quantize_grouped(const uint16_t* x, const int64_t* offsets, int E, int64_t K,
+                                const float* gs, int layout, int64_t scale_rows, uint8_t* codes,
+                                uint8_t* scales) {
+  int64_t srows, scols;
+  mxo_nvfp4_scales_shape(0, K, layout, &srows, &scols);
+  std::memset(scales, 0, (size_t)(scale_rows * scols));
+  std::memset(codes, 0, (size_t)(offsets[E] * (K / 2)));
+  int64_t padded_row = 0;
+  for (int e = 0; e < E; ++e) {
+    const int64_t r0 = offsets[e], n = offsets[e + 1] - offsets[e];
+    std::vector<float> v = bf16_rows_to_float(x + r0 * K, n * K);
+    const int64_t scale_row0 = (layout == 0) ? r0 : padded_row;
+    nvfp4_rows(v.data(), n, K, gs[e], layout, scols, codes + r0 * (K / 2),
+               scales + scale_row0 * scols, nullptr);
+    padded_row += ceil_div(n, 128) * 128;
+  }
+}
+
 // Stored NVFP4 data -> bf16: element k of row r is dequantized with the scale of its 16-element
 // block (linear [M, K/16] or swizzled as mxo_nvfp4_scales_shape says).
 void mxo_nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int64_t K,

@@ -608,6 +608,35 @@ def test_grouped_experts_are_independent_blocks():
         prow += s.shape[0]
 
 
+def test_nvfp4_grouped_experts_are_independent_blocks():
+    """Each expert's codes and scales are the plain NVFP4 quantization of its own rows under its
+    own global scale; swizzled scales sit in the expert's own run of 128-row tiles, pads zero;
+    one expert covering every row is the plain call."""
+    counts = [0, 5, 128, 0, 130, 1]
+    off = np.concatenate([[0], np.cumsum(counts)])
+    x = W.mxfp8_linear_quant(int(off[-1]), 192)
+    gs = np.array([1.0, 3.0, 0.25, 7.0, 448 * 6 / 40.0, 0.5], dtype=np.float32)
+    codes, swz = O.nvfp4_quantize_grouped(x, off, gs, O.SWIZZLED)
+    cl, lin = O.nvfp4_quantize_grouped(x, off, gs, O.LINEAR)
+    np.testing.assert_array_equal(codes, cl)
+    assert swz.shape == (128 + 128 + 256 + 128, 12) and lin.shape == (264, 12)
+    prow = 0
+    for e, n in enumerate(counts):
+        if n == 0:
+            continue
+        c, s = O.nvfp4_quantize(x[off[e]:off[e + 1]], gs[e], O.SWIZZLED)
+        _, sl = O.nvfp4_quantize(x[off[e]:off[e + 1]], gs[e], O.LINEAR)
+        np.testing.assert_array_equal(codes[off[e]:off[e + 1]], c)
+        np.testing.assert_array_equal(lin[off[e]:off[e + 1]], sl)
+        flat = swz.reshape(-1)[prow * 12:(prow + s.shape[0]) * 12]
+        np.testing.assert_array_equal(flat, s.reshape(-1))
+        prow += s.shape[0]
+    one = O.nvfp4_quantize_grouped(x, np.array([0, off[-1]]), gs[4:5], O.SWIZZLED)
+    plain = O.nvfp4_quantize(x, gs[4], O.SWIZZLED)
+    np.testing.assert_array_equal(one[0], plain[0])
+    np.testing.assert_array_equal(one[1], plain[1])
+
+
 def test_weight_generator_row_ranges_match_the_whole():
     full = W.weight_rotate_quant(5000, 64)
     for r0, r1 in ((0, 1), (2047, 2049), (4095, 5000), (100, 4200)):
