@@ -352,6 +352,10 @@ def extra_workloads(dev, peak):
     y = torch.empty_like(x)
     t = timed(lambda: mxq.mx_qdq_nvfp4(x, gs, y=y))
     record("nvfp4_qdq[8192,8192]", 4 * x.numel(), x.numel(), t)
+    K = x.shape[1]
+    t = timed(lambda: mxq.mx_dequantize_nvfp4(c, s, K, gs, mxq.SWIZZLED, y=y))
+    record("nvfp4_dequant_swizzled[8192,8192]", c.numel() + x.numel() // 16 + 2 * x.numel(),
+           x.numel(), t)
     del x, y, c, s
     x = to_gpu(W.rotate_quant_activation(8192, 28672), dev)
     H16 = to_gpu(W.normalized_hadamard_bf16(16), dev)
@@ -370,6 +374,15 @@ def extra_workloads(dev, peak):
     used_rows = int(sum(-(-int(n) // 128) * 128 for n in np.diff(off)))
     t = timed(lambda: mxq.mx_quantize_grouped(x, offs, mxq.E4M3, mxq.SWIZZLED, codes=c, scales=s))
     record("moe_quant_mxfp8[16384,2048]x128", 3 * x.numel() + used_rows * s.shape[1], x.numel(), t)
+    del c, s
+    # the same expert inputs in NVFP4, one global scale per expert
+    gse = torch.stack([448.0 * 6.0 / x[int(off[e]):int(off[e + 1])].float().abs().max()
+                       if off[e + 1] > off[e] else torch.ones((), device=dev)
+                       for e in range(len(off) - 1)]).float().contiguous()
+    c, s = mxq.mx_quantize_nvfp4_grouped(x, offs, gse, mxq.SWIZZLED)
+    t = timed(lambda: mxq.mx_quantize_nvfp4_grouped(x, offs, gse, mxq.SWIZZLED, codes=c, scales=s))
+    record("moe_quant_nvfp4[16384,2048]x128", 2 * x.numel() + c.numel() + used_rows * s.shape[1],
+           x.numel(), t)
     del x, c, s
 
     # rotation sweep: rotated QDQ, g in {16,32,64,128} x {MXFP4, MXFP8} on 3 layer inputs
@@ -394,6 +407,7 @@ CASES = {
     "weight_rotate_quant": "E4M3 rotate(g=32)+quantize, swizzled, weight [57344,8192]",
     "nvfp4_quant": "NVFP4 quantize, swizzled E4M3 scales, weight x[8192,8192]",
     "nvfp4_rotate_quant": "NVFP4 rotate(g=16)+quantize, swizzled, x[8192,28672]",
+    "nvfp4_dequant": "NVFP4 dequantize, swizzled E4M3 scales, codes of the weight x[8192,8192]",
 }
 
 
@@ -441,6 +455,14 @@ def run_case(args):
         c, s = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED)
         fn = lambda: mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, codes=c, scales=s)
         nbytes = 2 * x.numel() + c.numel() + x.numel() // 16
+    elif args.case == "nvfp4_dequant":
+        x = to_gpu(W.mxfp4_qdq_weight(), dev)
+        gs = torch.tensor([448.0 * 6.0], device=dev) / x.float().abs().max()
+        c, s = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED)
+        y = torch.empty_like(x)
+        K = x.shape[1]
+        fn = lambda: mxq.mx_dequantize_nvfp4(c, s, K, gs, mxq.SWIZZLED, y=y)
+        nbytes = c.numel() + x.numel() // 16 + 2 * x.numel()
     elif args.case == "nvfp4_rotate_quant":
         x = to_gpu(W.rotate_quant_activation(8192, 28672), dev)
         H = to_gpu(W.normalized_hadamard_bf16(16), dev)

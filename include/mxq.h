@@ -182,6 +182,38 @@ mx_status mx_qdq_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g
                        const float* global_scale, void* y, void* stream);
 
 /*
+ * Grouped (MoE expert) NVFP4 quantize: rows [row_offsets[e], row_offsets[e+1]) of x are expert
+ * e's input and are quantized as by mx_quantize_nvfp4 (no rotation) under that expert's own
+ * global scale global_scales[e] (DEVICE fp32 [E], 4-byte aligned, each positive and finite;
+ * pass E equal values for one shared scale). row_offsets: DEVICE int64 [E+1] with the contract
+ * of mx_quantize_grouped. Codes stay contiguous [M_total, K/2]. Linear scales are
+ * [M_total, K/16] (2-byte aligned); swizzled scales give each expert its own run of 128-row
+ * tiles starting at padded row P_e = sum_{e' < e} ceil(n_e'/128) * 128, in a buffer of
+ * mx_nvfp4_grouped_scales_shape() bytes that is written whole (pads zero; 16-byte aligned).
+ * 1 <= E <= 1024, K % 32 == 0.
+ */
+mx_status mx_nvfp4_grouped_scales_shape(int64_t M_total, int E, int64_t K, int layout,
+                                        int64_t* rows, int64_t* cols);
+
+mx_status mx_quantize_nvfp4_grouped(const void* x, const int64_t* row_offsets, int E,
+                                    int64_t M_total, int64_t K, const float* global_scales,
+                                    int layout, void* codes, void* scales, void* stream);
+
+/*
+ * NVFP4 dequantize (the dequantize half of NVFP4 QDQ; see the NVFP4 reading above):
+ * y_i = bf16(decode(code_i) * (decode(scale) / gs)) with each 16-element block's E4M3 scale
+ * byte decoded as a signed E4M3 value (0 factor when it decodes to zero), every step one fp32
+ * operation rounded to nearest even, so mx_dequantize_nvfp4(mx_quantize_nvfp4(x)) ==
+ * mx_qdq_nvfp4(x) bit for bit (same H, same gs). Scale bytes 0x7F / 0xFF (the E4M3 NaN) give
+ * 0x7FC0 for their block. codes: [M, K/2] bytes (32-byte aligned). scales: linear [M, K/16]
+ * (2-byte aligned) or swizzled as mx_nvfp4_scales_shape() (16-byte aligned; pads not read).
+ * global_scale: DEVICE pointer to one positive finite fp32 value (4-byte aligned). y: bf16
+ * [M, K] (32-byte aligned), must not overlap the inputs. K % 32 == 0. Errors: see conventions.
+ */
+mx_status mx_dequantize_nvfp4(const void* codes, const void* scales, int64_t M, int64_t K,
+                              const float* global_scale, int layout, void* y, void* stream);
+
+/*
  * Diagnostics: the rotated values y = x_chunk * H exactly as mx_rotate_quantize computes them
  * before quantization (same device code), written as fp32 [M, K] to y_f32 (device).
  */

@@ -28,7 +28,8 @@ _lib = None
 EXPORTS = (
     "mx_status_string", "mx_scales_shape", "mx_grouped_scales_shape", "mx_quantize", "mx_qdq",
     "mx_rotate_quantize", "mx_quantize_grouped", "mx_dequantize", "mx_nvfp4_scales_shape",
-    "mx_quantize_nvfp4", "mx_qdq_nvfp4", "mx_rotate_debug", "mx_device_errors",
+    "mx_quantize_nvfp4", "mx_qdq_nvfp4", "mx_dequantize_nvfp4", "mx_nvfp4_grouped_scales_shape",
+    "mx_quantize_nvfp4_grouped", "mx_rotate_debug", "mx_device_errors",
 )
 
 
@@ -62,6 +63,9 @@ def lib() -> ctypes.CDLL:
         "mx_nvfp4_scales_shape": (i32, [i64, i64, i32, pi64, pi64]),
         "mx_quantize_nvfp4": (i32, [p, i64, i64, p, i32, p, i32, p, p, p]),
         "mx_qdq_nvfp4": (i32, [p, i64, i64, p, i32, p, p, p]),
+        "mx_dequantize_nvfp4": (i32, [p, p, i64, i64, p, i32, p, p]),
+        "mx_nvfp4_grouped_scales_shape": (i32, [i64, i32, i64, i32, pi64, pi64]),
+        "mx_quantize_nvfp4_grouped": (i32, [p, p, i32, i64, i64, p, i32, p, p, p]),
         "mx_rotate_debug": (i32, [p, i64, i64, p, i32, p, p]),
         "mx_device_errors": (i32, [ctypes.POINTER(ctypes.c_int)]),
     }
@@ -249,6 +253,60 @@ def mx_qdq_nvfp4(x, global_scale, H=None, *, y=None, stream=None):
         y = torch.empty_like(x)
     _check(lib().mx_qdq_nvfp4(_ptr(x), M, K, _ptr(H), g, _ptr(global_scale), _ptr(y),
                               _stream_ptr(stream)))
+    return y
+
+
+def mx_nvfp4_grouped_scales_shape(M_total: int, E: int, K: int,
+                                  layout: int = SWIZZLED) -> tuple[int, int]:
+    r, c = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().mx_nvfp4_grouped_scales_shape(M_total, E, K, layout, ctypes.byref(r),
+                                               ctypes.byref(c)))
+    return r.value, c.value
+
+
+def mx_quantize_nvfp4_grouped(x, row_offsets, global_scales, layout=SWIZZLED, *, codes=None,
+                              scales=None, stream=None):
+    """Per-expert NVFP4 quantize; row_offsets: CUDA int64 [E + 1]; global_scales: CUDA fp32 [E]."""
+    M, K = _input(x)
+    if not (row_offsets.is_cuda and row_offsets.dtype == torch.int64 and row_offsets.dim() == 1
+            and row_offsets.is_contiguous()):
+        raise TypeError("row_offsets must be a contiguous CUDA int64 [E + 1] tensor")
+    E = row_offsets.numel() - 1
+    if not (isinstance(global_scales, torch.Tensor) and global_scales.is_cuda
+            and global_scales.dtype == torch.float32 and global_scales.numel() == E
+            and global_scales.is_contiguous()):
+        raise TypeError("global_scales must be a contiguous CUDA float32 tensor of E elements")
+    codes = _codes_out(codes, x, M, K, E2M1)
+    scales = _scales_out(scales, x, *mx_nvfp4_grouped_scales_shape(M, E, K, layout))
+    _check(lib().mx_quantize_nvfp4_grouped(_ptr(x), _ptr(row_offsets), E, M, K,
+                                           _ptr(global_scales), layout, _ptr(codes),
+                                           _ptr(scales), _stream_ptr(stream)))
+    return codes, scales
+
+
+def mx_dequantize_nvfp4(codes, scales, K, global_scale, layout=SWIZZLED, *, y=None,
+                        stream=None):
+    """Stored NVFP4 codes (uint8 [M, K/2]) and E4M3 scales -> bf16 [M, K]."""
+    if not (isinstance(codes, torch.Tensor) and codes.is_cuda and codes.dim() == 2
+            and codes.is_contiguous() and codes.element_size() == 1):
+        raise TypeError("codes must be a contiguous CUDA 2-D tensor of bytes")
+    if not (isinstance(scales, torch.Tensor) and scales.is_cuda and scales.is_contiguous()
+            and scales.element_size() == 1):
+        raise TypeError("scales must be a contiguous CUDA tensor of bytes")
+    _global_scale(global_scale)
+    M = codes.shape[0]
+    if codes.shape[1] != K // 2:
+        raise ValueError("codes has the wrong row length for K")
+    rows, cols = mx_nvfp4_scales_shape(M, K, layout)
+    if scales.numel() != rows * cols:
+        raise ValueError("scales has the wrong size")
+    if y is None:
+        y = torch.empty((M, K), dtype=torch.bfloat16, device=codes.device)
+    elif not (y.is_cuda and y.dtype == torch.bfloat16 and y.numel() == M * K
+              and y.is_contiguous()):
+        raise ValueError("y must be a contiguous CUDA bfloat16 tensor of M * K elements")
+    _check(lib().mx_dequantize_nvfp4(_ptr(codes), _ptr(scales), M, K, _ptr(global_scale), layout,
+                                     _ptr(y), _stream_ptr(stream)))
     return y
 
 

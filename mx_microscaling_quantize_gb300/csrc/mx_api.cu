@@ -296,6 +296,77 @@ mx_status mx_qdq_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g
                                       static_cast<cudaStream_t>(stream)));
 }
 
+mx_status mx_nvfp4_grouped_scales_shape(int64_t M_total, int E, int64_t K, int layout,
+                                        int64_t* rows, int64_t* cols) {
+  if (!rows || !cols) return MX_ERR_NULL;
+  if (M_total < 0 || K < 0 || K % 32 != 0 || E < 1 || E > 1024) return MX_ERR_SHAPE;
+  if (!valid_layout(layout)) return MX_ERR_UNSUPPORTED;
+  if (layout == MX_SCALES_LINEAR) {
+    *rows = M_total;
+    *cols = K / 16;
+  } else {
+    *rows = (M_total + int64_t(mxq::kTileRows - 1) * E) / mxq::kTileRows * mxq::kTileRows;
+    *cols = ceil_div(K, 64) * 4;
+  }
+  return MX_OK;
+}
+
+mx_status mx_quantize_nvfp4_grouped(const void* x, const int64_t* row_offsets, int E,
+                                    int64_t M_total, int64_t K, const float* global_scales,
+                                    int layout, void* codes, void* scales, void* stream) {
+  bool empty = false;
+  mx_status st = check_common(M_total, K, MX_FMT_E2M1, 32, MX_ROUND_RNE, &empty);
+  if (st != MX_OK) return st;
+  int64_t srows = 0, scols = 0;
+  st = mx_nvfp4_grouped_scales_shape(M_total, E, K, layout, &srows, &scols);
+  if (st != MX_OK) return st;
+  if (empty) return MX_OK;
+  if (!x || !row_offsets || !global_scales || !codes || !scales) return MX_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(row_offsets) & 7u) return MX_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(global_scales) & 3u) return MX_ERR_ALIGN;
+  if (!aligned32(x) || !aligned32(codes)) return MX_ERR_ALIGN;
+  if (layout == MX_SCALES_SWIZZLED ? !aligned16(scales)
+                                   : (reinterpret_cast<uintptr_t>(scales) & 1u) != 0) {
+    return MX_ERR_ALIGN;
+  }
+  mxq::StreamArgs a = stream_args(x, M_total, K, codes);
+  a.scales = static_cast<uint8_t*>(scales);
+  a.scale_cols = scols;
+  a.scale_rows = srows;
+  a.offsets = row_offsets;
+  a.E = E;
+  a.gscale = global_scales;
+  return from_cuda(mxq::launch_stream(mxq::kFmtNVFP4, false, layout == MX_SCALES_SWIZZLED, true,
+                                      a, static_cast<cudaStream_t>(stream)));
+}
+
+mx_status mx_dequantize_nvfp4(const void* codes, const void* scales, int64_t M, int64_t K,
+                              const float* global_scale, int layout, void* y, void* stream) {
+  if (!valid_layout(layout)) return MX_ERR_UNSUPPORTED;
+  bool empty = false;
+  mx_status st = check_common(M, K, MX_FMT_E2M1, 32, MX_ROUND_RNE, &empty);
+  if (st != MX_OK || empty) return st;
+  if (!codes || !scales || !global_scale || !y) return MX_ERR_NULL;
+  if (!aligned32(codes) || !aligned32(y)) return MX_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(global_scale) & 3u) return MX_ERR_ALIGN;
+  if (layout == MX_SCALES_SWIZZLED ? !aligned16(scales)
+                                   : (reinterpret_cast<uintptr_t>(scales) & 1u) != 0) {
+    return MX_ERR_ALIGN;
+  }
+  int64_t srows = 0, scols = 0;
+  mx_nvfp4_scales_shape(M, K, layout, &srows, &scols);
+  mxq::DequantArgs a{};
+  a.codes = codes;
+  a.scales = static_cast<const uint8_t*>(scales);
+  a.y = y;
+  a.M = M;
+  a.K = K;
+  a.scale_cols = scols;
+  a.gscale = global_scale;
+  return from_cuda(mxq::launch_dequant(mxq::kFmtNVFP4, layout == MX_SCALES_SWIZZLED, a,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, int g, float* y_f32,
                           void* stream) {
   bool empty = false;

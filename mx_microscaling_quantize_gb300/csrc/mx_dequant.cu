@@ -9,6 +9,9 @@
 // whenever it is at least 2^-149 in magnitude, which covers every code down to 2^-9 * 2^-127)
 // and rounded once to bf16, which is where subnormal results and overflow to infinity happen.
 // Scale byte 0xFF (the E8M0 NaN) and E4M3 NaN codes give the bf16 NaN 0x7FC0.
+// NVFP4 data is the same packed E2M1 stream with one E4M3 scale per 16 elements: a thread's
+// 32-element chunk holds two blocks whose scale bytes are adjacent in both layouts; each block's
+// factor is decode(scale) / gs (one IEEE division), applied like the MX power of two.
 #include "mx_device.cuh"
 #include "mx_launch.h"
 
@@ -57,15 +60,15 @@ __device__ __forceinline__ uint32_t canonical_nan2(uint32_t w) {
 
 template <int FMT>
 struct CodeBlock {
-  static constexpr int kWords = FMT == kFmtE2M1 ? 4 : 8;  // 32-bit words of codes per block
+  static constexpr int kWords = FMT == kFmtE4M3 ? 8 : 4;  // 32-bit words of codes per block
   uint32_t w[kWords];
-  uint32_t scale;
+  uint32_t scale;  // NVFP4: the two blocks' E4M3 bytes, first in the low byte
 };
 
 template <int FMT>
 __device__ __forceinline__ void load_block(const uint8_t* codes, int64_t b, CodeBlock<FMT>& cb) {
-  if (FMT == kFmtE2M1) load16B(codes + b * 16, cb.w);
-  else load32B(codes + b * 32, cb.w);
+  if (FMT == kFmtE4M3) load32B(codes + b * 32, cb.w);
+  else load16B(codes + b * 16, cb.w);
 }
 
 template <int FMT, bool SWZ>
@@ -78,8 +81,13 @@ __global__ void __launch_bounds__(kThreads) mx_dequant_kernel(DequantArgs a) {
   const int64_t row_step = stride / cblk, col_step = stride - row_step * cblk;
   int64_t row = b / cblk, col = b - row * cblk;  // advanced incrementally (swizzled scales)
   auto scale_at = [&](int64_t r, int64_t c, int64_t flat) -> uint32_t {
+    if (FMT == kFmtNVFP4) {  // scale columns 2c and 2c + 1: adjacent bytes, 2-byte aligned
+      const int64_t off = SWZ ? swizzled_offset(r, 2 * c, a.scale_cols) : 2 * flat;
+      return __ldg(reinterpret_cast<const uint16_t*>(a.scales + off));
+    }
     return SWZ ? __ldg(a.scales + swizzled_offset(r, c, a.scale_cols)) : __ldg(a.scales + flat);
   };
+  const float gs = FMT == kFmtNVFP4 ? __ldg(a.gscale) : 0.0f;
   CodeBlock<FMT> cur, nxt;
   if (b < nblk) {
     load_block<FMT>(codes, b, cur);
@@ -97,22 +105,36 @@ __global__ void __launch_bounds__(kThreads) mx_dequant_kernel(DequantArgs a) {
       load_block<FMT>(codes, bn, nxt);
       nxt.scale = scale_at(row, col, bn);
     }
-    const float sc = scale_of(cur.scale);
+    float sc0, sc1;  // factors of elements 0-15 and 16-31 (one MX scale: equal)
+    if (FMT == kFmtNVFP4) {
+      float d0, d1;
+      e4m3x2_to_f32(cur.scale, d0, d1);
+      sc0 = d0 == 0.0f ? 0.0f : __fdiv_rn(d0, gs);
+      sc1 = d1 == 0.0f ? 0.0f : __fdiv_rn(d1, gs);
+    } else {
+      sc0 = sc1 = scale_of(cur.scale);
+    }
     uint32_t o[16];
     uint32_t nan_codes = 0;
 #pragma unroll
     for (int i = 0; i < CodeBlock<FMT>::kWords; ++i) {
       const uint32_t w = cur.w[i];
-      if (FMT == kFmtE2M1) {
+      if (FMT != kFmtE4M3) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[4 * i + j] = dq2_e2m1((w >> (8 * j)) & 0xFFu, sc);
+        for (int j = 0; j < 4; ++j) o[4 * i + j] = dq2_e2m1((w >> (8 * j)) & 0xFFu, i < 2 ? sc0 : sc1);
       } else {
-        o[2 * i] = dq2_e4m3(w & 0xFFFFu, sc);
-        o[2 * i + 1] = dq2_e4m3(w >> 16, sc);
+        o[2 * i] = dq2_e4m3(w & 0xFFFFu, sc0);
+        o[2 * i + 1] = dq2_e4m3(w >> 16, sc0);
         nan_codes |= (w & 0x7F7F7F7Fu) + 0x01010101u;  // a byte reaches 0x80 iff it is S.1111.111
       }
     }
-    if (cur.scale == 255u) {
+    if (FMT == kFmtNVFP4) {
+      const bool nan0 = (cur.scale & 0x7Fu) == 0x7Fu, nan1 = ((cur.scale >> 8) & 0x7Fu) == 0x7Fu;
+      if (nan0 || nan1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = (i < 8 ? nan0 : nan1) ? kBf16NaNx2 : o[i];
+      }
+    } else if (cur.scale == 255u) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) o[i] = kBf16NaNx2;
     } else if (FMT == kFmtE4M3 && (nan_codes & 0x80808080u)) {
@@ -143,6 +165,9 @@ cudaError_t launch_t(const DequantArgs& a, cudaStream_t stream) {
 cudaError_t launch_dequant(int fmt, bool swizzled, const DequantArgs& a, cudaStream_t stream) {
   if (fmt == kFmtE2M1) {
     return swizzled ? launch_t<kFmtE2M1, true>(a, stream) : launch_t<kFmtE2M1, false>(a, stream);
+  }
+  if (fmt == kFmtNVFP4) {
+    return swizzled ? launch_t<kFmtNVFP4, true>(a, stream) : launch_t<kFmtNVFP4, false>(a, stream);
   }
   return swizzled ? launch_t<kFmtE4M3, true>(a, stream) : launch_t<kFmtE4M3, false>(a, stream);
 }

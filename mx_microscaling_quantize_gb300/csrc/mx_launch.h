@@ -21,23 +21,25 @@ struct StreamArgs {
   int64_t scale_rows;      // rows of the scale buffer
   const int64_t* offsets;  // grouped only: device int64 [E + 1]
   int E;
-  const float* gscale;     // NVFP4 only: device fp32 global scale
+  const float* gscale;     // NVFP4 only: device fp32 global scale (grouped: one per expert)
 };
 
-// fmt: 1 = E2M1, 2 = E4M3, 3 = NVFP4 (not grouped). qdq: write bf16 QDQ instead of codes +
+// fmt: 1 = E2M1, 2 = E4M3, 3 = NVFP4. qdq: write bf16 QDQ instead of codes +
 // scales.
 cudaError_t launch_stream(int fmt, bool qdq, bool swizzled, bool grouped, const StreamArgs& a,
                           cudaStream_t stream);
 
 struct DequantArgs {
   const void* codes;      // E2M1 [M, K/2] or E4M3 [M, K] bytes
-  const uint8_t* scales;  // linear [M, K/32] or swizzled (scale_cols padded columns)
+  const uint8_t* scales;  // linear [M, K/32] (NVFP4: [M, K/16]) or swizzled (scale_cols columns)
   void* y;                // bf16 [M, K]
   int64_t M;
   int64_t K;
   int64_t scale_cols;
+  const float* gscale;    // NVFP4 only: device fp32 global scale
 };
 
+// fmt: 1 = E2M1, 2 = E4M3, 3 = NVFP4 (E2M1 codes, E4M3 scales per 16 elements).
 cudaError_t launch_dequant(int fmt, bool swizzled, const DequantArgs& a, cudaStream_t stream);
 
 enum RotOut { kRotCodes = 0, kRotQdq = 1, kRotDebug = 2 };

@@ -173,13 +173,17 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
   __shared__ int64_t s_off[GROUPED ? kMaxExperts + 1 : 1];   // clamped first row of expert e
   __shared__ int64_t s_prow[GROUPED ? kMaxExperts + 1 : 1];  // first padded scale row of e
   __shared__ int64_t s_warp[kThreads / 32];
-  const int tid = threadIdx.x;
   constexpr bool kNv = FMT == kFmtNVFP4;
+  __shared__ float s_gs[GROUPED && kNv ? kMaxExperts : 1];  // NVFP4 grouped: gs of expert e
+  const int tid = threadIdx.x;
   constexpr int kCodeBytes = QDQ ? 64 : (FMT == kFmtE4M3 ? 32 : 16);  // output bytes per block
-  float gs = 0.0f, r6 = 0.0f;  // NVFP4 global scale and gs / 6
-  if (kNv) {
+  float gs = 0.0f, r6 = 0.0f;  // NVFP4 global scale and gs / 6 (grouped: of the current expert)
+  if (kNv && !GROUPED) {
     gs = __ldg(a.gscale);
     r6 = __fdiv_rn(gs, 6.0f);
+  }
+  if (kNv && GROUPED) {
+    for (int e = tid; e < a.E; e += kThreads) s_gs[e] = __ldg(a.gscale + e);
   }
 
   if (GROUPED) {
@@ -243,6 +247,7 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
   const int64_t row_step = stride / cblk, col_step = stride - row_step * cblk;
   int64_t row = b / cblk, col = b - row * cblk;  // advanced incrementally below
   int e = GROUPED ? last_not_above(s_off, a.E, row) : 0;  // expert of `row` (grouped)
+  int e_gs = -1;                                          // expert whose gs / r6 are loaded
   uint32_t cur[16], nxt[16];
   if (b < b_end) {
     load32B(x + b * 64, cur);
@@ -254,29 +259,36 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
       load32B(x + bn * 64, nxt);
       load32B(x + bn * 64 + 32, nxt + 8);
     }
+    if (GROUPED) {
+      while (e + 1 < a.E && row >= s_off[e + 1]) ++e;  // rows only grow within a thread
+      if (kNv && e != e_gs) {
+        e_gs = e;
+        gs = s_gs[e];
+        r6 = __fdiv_rn(gs, 6.0f);
+      }
+    }
     uint32_t byte;
     if constexpr (kNv) {
       byte = nv_block_kernel<QDQ>(cur, static_cast<uint8_t*>(a.out) + b * kCodeBytes, gs, r6);
     } else {
       byte = block_kernel<FMT, QDQ>(cur, true, static_cast<uint8_t*>(a.out) + b * kCodeBytes);
     }
-    if (kNv && !QDQ) {
-      // two scale bytes, NVFP4 blocks 2 * col and 2 * col + 1: adjacent in both layouts
-      const int64_t off = SWZ ? swizzled_offset(row, 2 * col, a.scale_cols) : 2 * b;
-      *reinterpret_cast<uint16_t*>(a.scales + off) = (uint16_t)byte;
-    } else if (!QDQ) {
-      if (!SWZ) {
-        a.scales[b] = (uint8_t)byte;  // linear [M, K/32] == flat block order
+    if (!QDQ) {
+      // scale position: linear = flat block order; swizzled = the row's (padded) tile row.
+      // NVFP4: two scale bytes, blocks 2 * col and 2 * col + 1, adjacent in both layouts.
+      int64_t pr = row;
+      bool ok = true;
+      if (GROUPED && SWZ) {
+        ok = row >= s_off[e] && row < s_off[e + 1];
+        pr = s_prow[e] + (row - s_off[e]);
+        ok = ok && pr < a.scale_rows;
+      }
+      if (kNv) {
+        const int64_t off = SWZ ? swizzled_offset(pr, 2 * col, a.scale_cols) : 2 * b;
+        if (ok) *reinterpret_cast<uint16_t*>(a.scales + off) = (uint16_t)byte;
       } else {
-        int64_t pr = row;
-        bool ok = true;
-        if (GROUPED) {
-          while (e + 1 < a.E && row >= s_off[e + 1]) ++e;  // rows only grow within a thread
-          ok = row >= s_off[e] && row < s_off[e + 1];
-          pr = s_prow[e] + (row - s_off[e]);
-          ok = ok && pr < a.scale_rows;
-        }
-        if (ok) a.scales[swizzled_offset(pr, col, a.scale_cols)] = (uint8_t)byte;
+        const int64_t off = SWZ ? swizzled_offset(pr, col, a.scale_cols) : b;
+        if (ok) a.scales[off] = (uint8_t)byte;
       }
     }
 #pragma unroll
@@ -361,12 +373,8 @@ cudaError_t launch_t(const StreamArgs& a, cudaStream_t stream) {
 template <int FMT>
 cudaError_t launch_fmt(bool qdq, bool swz, bool grouped, const StreamArgs& a, cudaStream_t st) {
   if (qdq) return launch_t<FMT, true, false, false>(a, st);
-  if constexpr (FMT != kFmtNVFP4) {
-    if (grouped) {
-      return swz ? launch_t<FMT, false, true, true>(a, st) : launch_t<FMT, false, false, true>(a, st);
-    }
-  } else {
-    if (grouped) return cudaErrorInvalidValue;
+  if (grouped) {
+    return swz ? launch_t<FMT, false, true, true>(a, st) : launch_t<FMT, false, false, true>(a, st);
   }
   return swz ? launch_t<FMT, false, true, false>(a, st) : launch_t<FMT, false, false, false>(a, st);
 }

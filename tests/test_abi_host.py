@@ -181,6 +181,35 @@ def test_nvfp4_shapes_and_validation(L):
     assert d(P, 4, 64, None, 0, P, None, None) == NULL
     assert d(P, 4, 64, None, 0, P, P + 16, None) == ALIGN
     assert d(P, -1, 64, None, 0, P, P, None) == SHAPE
+    assert mxq.mx_nvfp4_grouped_scales_shape(300, 4, 416, mxq.SWIZZLED) == (768, 28)
+    assert mxq.mx_nvfp4_grouped_scales_shape(300, 4, 416, mxq.LINEAR) == (300, 26)
+    gq = L.mx_quantize_nvfp4_grouped  # (x, off, E, M, K, gs, layout, codes, scales, stream)
+    assert gq(P, P, 0, 4, 64, P, 0, P, P, None) == SHAPE
+    assert gq(P, P, 1025, 4, 64, P, 0, P, P, None) == SHAPE
+    assert gq(P, P, 2, 4, 48, P, 0, P, P, None) == SHAPE
+    assert gq(P, P, 2, 4, 64, P, 2, P, P, None) == UNSUP
+    assert gq(P, P, 2, 4, 64, None, 0, P, P, None) == NULL
+    assert gq(P, None, 2, 4, 64, P, 0, P, P, None) == NULL
+    assert gq(P, P + 4, 2, 4, 64, P, 0, P, P, None) == ALIGN
+    assert gq(P, P, 2, 4, 64, P + 2, 0, P, P, None) == ALIGN
+    assert gq(P, P, 2, 4, 64, P, 0, P, P + 1, None) == ALIGN
+    assert gq(P, P, 2, 4, 64, P, 1, P, P + 2, None) == ALIGN
+    assert gq(None, None, 2, 0, 64, None, 1, None, None, None) == OK
+    u = L.mx_dequantize_nvfp4  # (codes, scales, M, K, gs, layout, y, stream)
+    assert u(P, P, 4, 48, P, 0, P, None) == SHAPE
+    assert u(P, P, -1, 64, P, 0, P, None) == SHAPE
+    assert u(P, P, 4, 64, P, 2, P, None) == UNSUP
+    assert u(None, P, 4, 64, P, 0, P, None) == NULL
+    assert u(P, None, 4, 64, P, 0, P, None) == NULL
+    assert u(P, P, 4, 64, None, 0, P, None) == NULL
+    assert u(P, P, 4, 64, P, 0, None, None) == NULL
+    assert u(P + 16, P, 4, 64, P, 0, P, None) == ALIGN
+    assert u(P, P, 4, 64, P, 0, P + 16, None) == ALIGN
+    assert u(P, P + 1, 4, 64, P, 0, P, None) == ALIGN
+    assert u(P, P + 2, 4, 64, P, 1, P, None) == ALIGN
+    assert u(P, P, 4, 64, P + 2, 0, P, None) == ALIGN
+    assert u(None, None, 0, 64, None, 1, None, None) == OK
+    assert u(P, P, 1 << 40, 1 << 20, P, 0, P, None) == SHAPE
 
 
 def test_device_errors_null(L):

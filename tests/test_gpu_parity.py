@@ -306,6 +306,68 @@ def test_nvfp4_full_size_sampled_rows():
                                   O.nvfp4_qdq(xb[rows], gs))
 
 
+def nv_dequantize(codes, scales, K, gs, layout):
+    y = mxq.mx_dequantize_nvfp4(torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda(),
+                                K, gs_tensor(gs), layout)
+    return T.bf16_bits(y)
+
+
+def test_nvfp4_dequantize_every_code_under_every_scale_byte():
+    """Row r holds all 16 E2M1 codes in both of its blocks under E4M3 scale byte r (0..255:
+    subnormal scales, the sign bit and the two NaN bytes included), for three global scales."""
+    K = 32
+    nib = np.arange(32) % 16
+    codes = np.tile((nib[0::2] | (nib[1::2] << 4)).astype(np.uint8), (256, 1))
+    scales = np.repeat(np.arange(256, dtype=np.uint8)[:, None], 2, axis=1)
+    for gs in (np.float32(1.0), np.float32(0.3712), np.float32(2.0 ** -10 * 3)):
+        np.testing.assert_array_equal(nv_dequantize(codes, scales, K, gs, O.LINEAR),
+                                      O.nvfp4_dequantize(codes, scales, K, gs, O.LINEAR))
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("M,K", [(1, 32), (3, 96), (129, 416), (300, 4096), (1000, 2048)])
+def test_nvfp4_dequantize_random_bytes_bit_exact(layout, M, K):
+    rng = np.random.default_rng(M * 11 + K)
+    codes = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    scales = rng.integers(0, 256, O.nvfp4_scales_shape(M, K, layout), dtype=np.uint8)
+    gs = np.float32(448 * 6 / 3.5)
+    np.testing.assert_array_equal(nv_dequantize(codes, scales, K, gs, layout),
+                                  O.nvfp4_dequantize(codes, scales, K, gs, layout))
+
+
+@pytest.mark.parametrize("M,K", [(1, 32), (127, 160), (255, 416)])
+def test_nvfp4_dequantize_edge_shapes_with_canaries(M, K):
+    xb = W.mxfp8_linear_quant(M, K, stream=M * 1000 + K + 2)
+    gs = gs_of(xb)
+    for layout in LAYOUTS:
+        c, s = mxq.mx_quantize_nvfp4(T.to_gpu(xb), gs_tensor(gs), layout)
+        yfull, ybytes = guarded(M * K * 2)
+        mxq.mx_dequantize_nvfp4(c, s, K, gs_tensor(gs), layout,
+                                y=ybytes.view(torch.bfloat16).view(M, K))
+        got = T.u8(ybytes).view(np.uint16).reshape(M, K)
+        np.testing.assert_array_equal(got, O.nvfp4_qdq(xb, gs))
+        assert_guards(yfull, M * K * 2)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_nvfp4_dequantize_of_quantize_is_qdq_full_size(layout):
+    """x[8192, 8192] (the MXFP4 QDQ weight workload), plain and rotated (normalized Hadamard,
+    g = 16): dequantize(quantize(x)) equals the GPU QDQ bit for bit over the whole tensor; the
+    plain one also equals the oracle's QDQ on 24 sampled rows."""
+    xb = W.mxfp4_qdq_weight()
+    x = T.to_gpu(xb)
+    gs = gs_of(xb)
+    for H in (None, T.to_gpu(W.normalized_hadamard_bf16(16))):
+        c, s = mxq.mx_quantize_nvfp4(x, gs_tensor(gs), layout, H)
+        y = mxq.mx_dequantize_nvfp4(c, s, x.shape[1], gs_tensor(gs), layout)
+        q = mxq.mx_qdq_nvfp4(x, gs_tensor(gs), H)
+        assert torch.equal(y.view(torch.int16), q.view(torch.int16))
+        if H is None:
+            rows = np.sort(np.random.default_rng(14).choice(xb.shape[0], 24, replace=False))
+            np.testing.assert_array_equal(T.bf16_bits(y[torch.from_numpy(rows).cuda()]),
+                                          O.nvfp4_qdq(xb[rows], gs))
+
+
 @pytest.mark.parametrize("g", [16, 32, 64, 128])
 def test_nvfp4_exact_rotations_bit_exact(g):
     """Identity and signed-permutation H make the rotation exact in fp32: the rotated NVFP4
@@ -383,6 +445,49 @@ def test_grouped_edge_counts(fmt, counts):
         np.testing.assert_array_equal(c, rc)
 
 
+def nv_grouped(xb, offsets, gs, layout):
+    c, s = mxq.mx_quantize_nvfp4_grouped(T.to_gpu(xb), torch.from_numpy(offsets).cuda(),
+                                         torch.from_numpy(np.asarray(gs, np.float32)).cuda(),
+                                         layout)
+    return T.u8(c), T.u8(s)
+
+
+def expert_global_scales(xb, off):
+    """448 * 6 / amax of each expert's rows (1 for an expert without rows or all zeros)."""
+    v = np.abs(W.bf16_bits_to_float(xb))
+    gs = []
+    for e in range(len(off) - 1):
+        amax = np.float32(v[off[e]:off[e + 1]].max()) if off[e + 1] > off[e] else np.float32(0)
+        gs.append(np.float32(448 * 6) / amax if amax > 0 else np.float32(1.0))
+    return np.array(gs, np.float32)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_nvfp4_moe_workload_full_size(layout):
+    """The MoE workload (128 experts, Zipf(1.1) counts summing to 16384, rows [n_e, 2048]) in
+    NVFP4 with one global scale per expert: bit-exact codes and scales, pads included."""
+    xb, off = W.moe_quant()
+    gs = expert_global_scales(xb, off)
+    c, s = nv_grouped(xb, off, gs, layout)
+    rc, rs = O.nvfp4_quantize_grouped(xb, off, gs, layout, scale_rows=s.shape[0])
+    np.testing.assert_array_equal(s, rs)
+    np.testing.assert_array_equal(c, rc)
+
+
+@pytest.mark.parametrize("counts", [[0, 1, 127, 128, 129, 0, 300, 5],
+                                    [1000], [0, 0, 64], [128] * 6, [3] * 40])
+def test_nvfp4_grouped_edge_counts(counts):
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    for K in (160, 192):  # K/16 % 4 != 0 (partial last scale word) and == 0
+        xb = W.mxfp8_linear_quant(int(off[-1]), K, stream=len(counts) + K)
+        gs = expert_global_scales(xb, off) * np.float32(0.75)
+        for layout in LAYOUTS:
+            c, s = nv_grouped(xb, off, gs, layout)
+            rc, rs = O.nvfp4_quantize_grouped(xb, off, gs, layout, scale_rows=s.shape[0])
+            np.testing.assert_array_equal(s, rs)
+            np.testing.assert_array_equal(c, rc)
+
+
 def test_grouped_bad_offsets_stay_in_bounds():
     """Offsets that break the contract (decreasing, beyond M) give unspecified values but no
     access outside the buffers (canaries intact) and no error from the device."""
@@ -396,6 +501,15 @@ def test_grouped_bad_offsets_stay_in_bounds():
                             scales=scales)
     torch.cuda.synchronize()
     assert_guards(cfull, M * K)
+    assert_guards(sfull, rows * cols)
+    rows, cols = mxq.mx_nvfp4_grouped_scales_shape(M, E, K, mxq.SWIZZLED)
+    cfull, codes = guarded(M * K // 2)
+    sfull, scales = guarded(rows * cols)
+    mxq.mx_quantize_nvfp4_grouped(x, torch.from_numpy(off).cuda(),
+                                  torch.ones(E, dtype=torch.float32, device="cuda"), mxq.SWIZZLED,
+                                  codes=codes, scales=scales)
+    torch.cuda.synchronize()
+    assert_guards(cfull, M * K // 2)
     assert_guards(sfull, rows * cols)
 
 
