@@ -11,8 +11,9 @@ roofline object for the kernel (against the measured HBM copy bandwidth), the CP
 on the host cores (cpu_baseline), an end-to-end figure through the same calls with the inputs
 copied in from, and the outputs back to, pinned host memory every step (e2e; copies in both
 directions pipelined over two buffer sets), SM clocks sampled during the timed region, and
-per-workload kernel figures for the other workloads (cold L2: a 256 MiB buffer is written
-between timed launches; mean of the launches, since event timestamps advance in ~2 us steps).
+per-workload kernel figures for the other workloads, cold (a 256 MiB buffer is written before
+each timed launch; mean of the launches, since event timestamps advance in ~2 us steps) and
+steady (launches back to back over copies of the buffers that together exceed 3x L2).
 
 --impl reference times the CPU oracle instead (bounded sample per step, all host cores).
 """
@@ -257,16 +258,22 @@ def run_reference(args):
 # our arm
 # ---------------------------------------------------------------------------------------------
 def extra_workloads(dev, peak):
-    """Kernel-only figures of the other workloads: CUDA events around each launch, a 256 MiB
-    buffer written between launches so that every launch starts with a cold L2. The launch
-    then also pays for writing back the dirty lines that buffer left in L2, which stands in
-    for the write-back of its own outputs: those are still in L2 when the launch ends, so a
-    single launch timed from a clean L2 would leave out the cost of its writes."""
+    """Kernel-only figures of the other workloads, two ways (CUDA events on the launching
+    stream both times):
+    - cold: single launches, a 256 MiB buffer written before each so that it starts with a
+      cold L2. The launch then also pays for writing back the dirty lines that buffer left,
+      up to the whole L2 (129 MB), which stands in for the write-back of its own outputs
+      (still in L2 when it ends); for a launch that writes less than L2 this overcharges.
+    - steady: launches back to back, cycling over enough copies of the buffers (inputs and
+      outputs) that the copies together are at least three times L2, so no launch finds its
+      inputs in L2 and each pays for the write-back of what the launch before it wrote, as in
+      a stream of such calls; the mean over the loop."""
     import torch
     import mx_microscaling_quantize_gb300 as mxq
     from mx_microscaling_quantize_gb300 import workloads as W
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    l2_bytes = 129 * 10 ** 6
     out = {}
 
     def timed(fn, iters=30):
@@ -285,15 +292,48 @@ def extra_workloads(dev, peak):
                 times.append(s.elapsed_time(e) / 1e3)
         return statistics.fmean(times)
 
-    def record(name, nbytes, elems, t, launches=1):
-        out[name] = {"GB/s": nbytes / t / 1e9, "frac_of_peak": nbytes / t / 1e9 / peak,
-                     "Gelem/s": elems / t / 1e9, "us": t * 1e6, "launches": launches}
+    def steady(fns, iters):
+        for fn in fns:
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for i in range(iters):
+            fns[i % len(fns)]()
+        e.record()
+        e.synchronize()
+        return s.elapsed_time(e) / 1e3 / iters
+
+    def measure(name, nbytes, elems, make, footprint, iters=30):
+        """make(k) -> a launch closure over buffer set k (k = 0: the given buffers, k > 0:
+        copies); footprint: bytes of one set's inputs and outputs."""
+        fns = [make(0)]
+        t_cold = timed(fns[0], iters)
+        sets = max(1, min(64, -(-3 * l2_bytes // footprint)))
+        fns += [make(k) for k in range(1, sets)]
+        t_steady = steady(fns, max(2 * iters, 2 * sets))
+        out[name] = {"GB/s": nbytes / t_cold / 1e9, "frac_of_peak": nbytes / t_cold / 1e9 / peak,
+                     "Gelem/s": elems / t_cold / 1e9, "us": t_cold * 1e6, "launches": 1,
+                     "steady_GB/s": nbytes / t_steady / 1e9,
+                     "steady_frac": nbytes / t_steady / 1e9 / peak,
+                     "steady_us": t_steady * 1e6, "steady_sets": sets}
+        del fns
+
+    def copy_of(t, k):
+        return t if k == 0 else t.clone()
+
+    def empty_of(t, k):
+        return t if k == 0 else torch.empty_like(t)
 
     # MXFP8 quantize, linear scales, x[128, 4096]
     x = to_gpu(W.mxfp8_linear_quant(), dev)
     c, s = mxq.mx_quantize(x, mxq.E4M3, mxq.LINEAR)
-    t = timed(lambda: mxq.mx_quantize(x, mxq.E4M3, mxq.LINEAR, codes=c, scales=s))
-    record("mxfp8_linear_quant[128,4096]", x.numel() * 3 + s.numel(), x.numel(), t)
+
+    def make(k, x=x, c=c, s=s):
+        xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+        return lambda: mxq.mx_quantize(xk, mxq.E4M3, mxq.LINEAR, codes=ck, scales=sk)
+    nb = 3 * x.numel() + s.numel()
+    measure("mxfp8_linear_quant[128,4096]", nb, x.numel(), make, nb)
 
     # the two QDQ tensors separately, both formats
     for name, bits in (("weight[8192,8192]", W.mxfp4_qdq_weight()),
@@ -301,8 +341,10 @@ def extra_workloads(dev, peak):
         x = to_gpu(bits, dev)
         y = torch.empty_like(x)
         for fmt, fname in ((mxq.E2M1, "mxfp4"), (mxq.E4M3, "mxfp8")):
-            t = timed(lambda: mxq.mx_qdq(x, fmt, y=y))
-            record(f"{fname}_qdq_{name}", 4 * x.numel(), x.numel(), t)
+            def make(k, x=x, y=y, fmt=fmt):
+                xk, yk = copy_of(x, k), empty_of(y, k)
+                return lambda: mxq.mx_qdq(xk, fmt, y=yk)
+            measure(f"{fname}_qdq_{name}", 4 * x.numel(), x.numel(), make, 4 * x.numel())
         del x, y
 
     # fused rotate + MXFP4 quantize, g = 32 Hadamard, swizzled scales
@@ -311,10 +353,13 @@ def extra_workloads(dev, peak):
         for M in W.ROTATE_QUANT_M:
             x = to_gpu(W.rotate_quant_activation(M, K), dev)
             c, s = mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED)
-            t = timed(lambda: mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, codes=c,
-                                                     scales=s))
-            record(f"rotate_quant_mxfp4_g32[{M},{K}]", 2 * x.numel() + c.numel() + s.numel(),
-                   x.numel(), t)
+
+            def make(k, x=x, c=c, s=s):
+                xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+                return lambda: mxq.mx_rotate_quantize(xk, H, mxq.E2M1, mxq.SWIZZLED, codes=ck,
+                                                      scales=sk)
+            nb = 2 * x.numel() + c.numel() + s.numel()
+            measure(f"rotate_quant_mxfp4_g32[{M},{K}]", nb, x.numel(), make, nb)
             del x, c, s
 
     # weight-side rotate + quantize of the 70B layer weights, g = 32, swizzled scales
@@ -322,10 +367,13 @@ def extra_workloads(dev, peak):
         x = to_gpu(W.weight_rotate_quant(N, K), dev)
         for fmt, fname in ((mxq.E2M1, "mxfp4"), (mxq.E4M3, "mxfp8")):
             c, s = mxq.mx_rotate_quantize(x, H, fmt, mxq.SWIZZLED)
-            t = timed(lambda: mxq.mx_rotate_quantize(x, H, fmt, mxq.SWIZZLED, codes=c, scales=s),
-                      iters=15)
-            record(f"weight_rotate_quant_{fname}_g32[{N},{K}]",
-                   2 * x.numel() + c.numel() + s.numel(), x.numel(), t)
+
+            def make(k, x=x, c=c, s=s, fmt=fmt):
+                xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+                return lambda: mxq.mx_rotate_quantize(xk, H, fmt, mxq.SWIZZLED, codes=ck,
+                                                      scales=sk)
+            nb = 2 * x.numel() + c.numel() + s.numel()
+            measure(f"weight_rotate_quant_{fname}_g32[{N},{K}]", nb, x.numel(), make, nb, iters=15)
             del c, s
         del x
 
@@ -336,53 +384,75 @@ def extra_workloads(dev, peak):
     for fmt, fname in ((mxq.E2M1, "mxfp4"), (mxq.E4M3, "mxfp8")):
         for layout, lname in ((mxq.LINEAR, "linear"), (mxq.SWIZZLED, "swizzled")):
             c, s = mxq.mx_quantize(x, fmt, layout)
-            t = timed(lambda: mxq.mx_dequantize(c, s, K, fmt, layout, y=y))
-            record(f"dequant_{fname}_{lname}[8192,8192]", c.numel() + x.numel() // 32
-                   + 2 * x.numel(), x.numel(), t)
-            del c, s
-    del x, y
 
-    # NVFP4 (16-element blocks, E4M3 scales under a global scale): plain quantize and QDQ of
-    # the QDQ weight, and rotate(g = 16) + quantize of the largest activation
-    x = to_gpu(W.mxfp4_qdq_weight(), dev)
+            def make(k, c=c, s=s, fmt=fmt, layout=layout):
+                ck, sk, yk = copy_of(c, k), copy_of(s, k), empty_of(y, k)
+                return lambda: mxq.mx_dequantize(ck, sk, K, fmt, layout, y=yk)
+            nb = c.numel() + x.numel() // 32 + 2 * x.numel()
+            measure(f"dequant_{fname}_{lname}[8192,8192]", nb, x.numel(), make, nb)
+            del c, s
+    del y
+
+    # NVFP4 (16-element blocks, E4M3 scales under a global scale): plain quantize, QDQ and
+    # dequantize of the QDQ weight, and rotate(g = 16) + quantize of the largest activation
     gs = torch.tensor([448.0 * 6.0], device=dev) / x.float().abs().max()
     c, s = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED)
-    t = timed(lambda: mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, codes=c, scales=s))
-    record("nvfp4_quant[8192,8192]", 2 * x.numel() + c.numel() + x.numel() // 16, x.numel(), t)
+
+    def make(k, x=x, c=c, s=s):
+        xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+        return lambda: mxq.mx_quantize_nvfp4(xk, gs, mxq.SWIZZLED, codes=ck, scales=sk)
+    nb = 2 * x.numel() + c.numel() + x.numel() // 16
+    measure("nvfp4_quant[8192,8192]", nb, x.numel(), make, nb)
     y = torch.empty_like(x)
-    t = timed(lambda: mxq.mx_qdq_nvfp4(x, gs, y=y))
-    record("nvfp4_qdq[8192,8192]", 4 * x.numel(), x.numel(), t)
-    K = x.shape[1]
-    t = timed(lambda: mxq.mx_dequantize_nvfp4(c, s, K, gs, mxq.SWIZZLED, y=y))
-    record("nvfp4_dequant_swizzled[8192,8192]", c.numel() + x.numel() // 16 + 2 * x.numel(),
-           x.numel(), t)
+
+    def make(k, x=x, y=y):
+        xk, yk = copy_of(x, k), empty_of(y, k)
+        return lambda: mxq.mx_qdq_nvfp4(xk, gs, y=yk)
+    measure("nvfp4_qdq[8192,8192]", 4 * x.numel(), x.numel(), make, 4 * x.numel())
+
+    def make(k, c=c, s=s, y=y):
+        ck, sk, yk = copy_of(c, k), copy_of(s, k), empty_of(y, k)
+        return lambda: mxq.mx_dequantize_nvfp4(ck, sk, K, gs, mxq.SWIZZLED, y=yk)
+    nb = c.numel() + x.numel() // 16 + 2 * x.numel()
+    measure("nvfp4_dequant_swizzled[8192,8192]", nb, x.numel(), make, nb)
     del x, y, c, s
     x = to_gpu(W.rotate_quant_activation(8192, 28672), dev)
     H16 = to_gpu(W.normalized_hadamard_bf16(16), dev)
     c, s = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, H16)
-    t = timed(lambda: mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, H16, codes=c, scales=s),
-              iters=15)
-    record("nvfp4_rotate_quant_g16[8192,28672]", 2 * x.numel() + c.numel() + x.numel() // 16,
-           x.numel(), t)
+
+    def make(k, x=x, c=c, s=s):
+        xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+        return lambda: mxq.mx_quantize_nvfp4(xk, gs, mxq.SWIZZLED, H16, codes=ck, scales=sk)
+    nb = 2 * x.numel() + c.numel() + x.numel() // 16
+    measure("nvfp4_rotate_quant_g16[8192,28672]", nb, x.numel(), make, nb, iters=15)
     del x, c, s
 
-    # MoE MXFP8 grouped quantize, swizzled scales padded per expert
+    # MoE grouped quantize, swizzled scales padded per expert: MXFP8, and the same expert
+    # inputs in NVFP4 with one global scale per expert
     xb, off = W.moe_quant()
     x = to_gpu(xb, dev)
     offs = torch.from_numpy(off).to(dev)
     c, s = mxq.mx_quantize_grouped(x, offs, mxq.E4M3, mxq.SWIZZLED)
     used_rows = int(sum(-(-int(n) // 128) * 128 for n in np.diff(off)))
-    t = timed(lambda: mxq.mx_quantize_grouped(x, offs, mxq.E4M3, mxq.SWIZZLED, codes=c, scales=s))
-    record("moe_quant_mxfp8[16384,2048]x128", 3 * x.numel() + used_rows * s.shape[1], x.numel(), t)
+
+    def make(k, x=x, c=c, s=s):
+        xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+        return lambda: mxq.mx_quantize_grouped(xk, offs, mxq.E4M3, mxq.SWIZZLED, codes=ck,
+                                               scales=sk)
+    nb = 3 * x.numel() + used_rows * s.shape[1]
+    measure("moe_quant_mxfp8[16384,2048]x128", nb, x.numel(), make, nb)
     del c, s
-    # the same expert inputs in NVFP4, one global scale per expert
     gse = torch.stack([448.0 * 6.0 / x[int(off[e]):int(off[e + 1])].float().abs().max()
                        if off[e + 1] > off[e] else torch.ones((), device=dev)
                        for e in range(len(off) - 1)]).float().contiguous()
     c, s = mxq.mx_quantize_nvfp4_grouped(x, offs, gse, mxq.SWIZZLED)
-    t = timed(lambda: mxq.mx_quantize_nvfp4_grouped(x, offs, gse, mxq.SWIZZLED, codes=c, scales=s))
-    record("moe_quant_nvfp4[16384,2048]x128", 2 * x.numel() + c.numel() + used_rows * s.shape[1],
-           x.numel(), t)
+
+    def make(k, x=x, c=c, s=s):
+        xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+        return lambda: mxq.mx_quantize_nvfp4_grouped(xk, offs, gse, mxq.SWIZZLED, codes=ck,
+                                                     scales=sk)
+    nb = 2 * x.numel() + c.numel() + used_rows * s.shape[1]
+    measure("moe_quant_nvfp4[16384,2048]x128", nb, x.numel(), make, nb)
     del x, c, s
 
     # rotation sweep: rotated QDQ, g in {16,32,64,128} x {MXFP4, MXFP8} on 3 layer inputs
@@ -392,8 +462,11 @@ def extra_workloads(dev, peak):
         for g in W.ROTATION_SWEEP_G:
             Hg = to_gpu(W.normalized_hadamard_bf16(g), dev)
             for fmt, fname in ((mxq.E2M1, "mxfp4"), (mxq.E4M3, "mxfp8")):
-                t = timed(lambda: mxq.mx_qdq(x, fmt, Hg, y=y), iters=15)
-                record(f"rotated_qdq_{fname}_g{g}_{lname}[{M},{K}]", 4 * x.numel(), x.numel(), t)
+                def make(k, x=x, y=y, Hg=Hg, fmt=fmt):
+                    xk, yk = copy_of(x, k), empty_of(y, k)
+                    return lambda: mxq.mx_qdq(xk, fmt, Hg, y=yk)
+                measure(f"rotated_qdq_{fname}_g{g}_{lname}[{M},{K}]", 4 * x.numel(), x.numel(),
+                        make, 4 * x.numel(), iters=15)
         del x, y
     return out
 

@@ -10,6 +10,7 @@ calls raise; there is no fallback.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 
 import torch
@@ -86,9 +87,18 @@ def _check(status: int) -> None:
         raise MXError(status, mx_status_string(status))
 
 
-def _stream_ptr(stream) -> int | None:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_ptr(stream, t: torch.Tensor) -> int:
+    """The cudaStream_t to launch on: `stream` (a torch.cuda.Stream or a raw handle), or when
+    None the current stream of t's device (read without building a Stream object, which costs
+    microseconds per call)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        dev = t.get_device()
+        if _raw_stream is not None:
+            return _raw_stream(dev)
+        return torch.cuda.current_stream(dev).cuda_stream
     return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else stream
 
 
@@ -132,12 +142,14 @@ def _scales_out(scales, x, rows, cols):
     return scales
 
 
+@functools.lru_cache(maxsize=4096)
 def mx_scales_shape(M: int, K: int, layout: int = LINEAR, group: int = GROUP) -> tuple[int, int]:
     r, c = ctypes.c_int64(), ctypes.c_int64()
     _check(lib().mx_scales_shape(M, K, group, layout, ctypes.byref(r), ctypes.byref(c)))
     return r.value, c.value
 
 
+@functools.lru_cache(maxsize=4096)
 def mx_grouped_scales_shape(M_total: int, E: int, K: int, layout: int = SWIZZLED,
                             group: int = GROUP) -> tuple[int, int]:
     r, c = ctypes.c_int64(), ctypes.c_int64()
@@ -153,7 +165,7 @@ def mx_quantize(x, fmt, layout=LINEAR, *, codes=None, scales=None, group=GROUP, 
     codes = _codes_out(codes, x, M, K, fmt)
     scales = _scales_out(scales, x, *mx_scales_shape(M, K, layout, group))
     _check(lib().mx_quantize(_ptr(x), M, K, fmt, group, layout, rounding, _ptr(codes),
-                             _ptr(scales), _stream_ptr(stream)))
+                             _ptr(scales), _stream_ptr(stream, x)))
     return codes, scales
 
 
@@ -164,7 +176,7 @@ def mx_qdq(x, fmt, H=None, *, y=None, group=GROUP, rounding=RNE, stream=None):
     if y is None:
         y = torch.empty_like(x)
     _check(lib().mx_qdq(_ptr(x), M, K, fmt, group, rounding, _ptr(H), g, _ptr(y),
-                        _stream_ptr(stream)))
+                        _stream_ptr(stream, x)))
     return y
 
 
@@ -176,7 +188,7 @@ def mx_rotate_quantize(x, H, fmt, layout=SWIZZLED, *, codes=None, scales=None, g
     codes = _codes_out(codes, x, M, K, fmt)
     scales = _scales_out(scales, x, *mx_scales_shape(M, K, layout, group))
     _check(lib().mx_rotate_quantize(_ptr(x), M, K, _ptr(H), g, fmt, group, layout, rounding,
-                                    _ptr(codes), _ptr(scales), _stream_ptr(stream)))
+                                    _ptr(codes), _ptr(scales), _stream_ptr(stream, x)))
     return codes, scales
 
 
@@ -191,7 +203,7 @@ def mx_quantize_grouped(x, row_offsets, fmt, layout=SWIZZLED, *, codes=None, sca
     codes = _codes_out(codes, x, M, K, fmt)
     scales = _scales_out(scales, x, *mx_grouped_scales_shape(M, E, K, layout, group))
     _check(lib().mx_quantize_grouped(_ptr(x), _ptr(row_offsets), E, M, K, fmt, group, layout,
-                                     rounding, _ptr(codes), _ptr(scales), _stream_ptr(stream)))
+                                     rounding, _ptr(codes), _ptr(scales), _stream_ptr(stream, x)))
     return codes, scales
 
 
@@ -215,10 +227,11 @@ def mx_dequantize(codes, scales, K, fmt, layout=LINEAR, *, y=None, group=GROUP, 
               and y.is_contiguous()):
         raise ValueError("y must be a contiguous CUDA bfloat16 tensor of M * K elements")
     _check(lib().mx_dequantize(_ptr(codes), _ptr(scales), M, K, fmt, group, layout, _ptr(y),
-                               _stream_ptr(stream)))
+                               _stream_ptr(stream, codes)))
     return y
 
 
+@functools.lru_cache(maxsize=4096)
 def mx_nvfp4_scales_shape(M: int, K: int, layout: int = SWIZZLED) -> tuple[int, int]:
     r, c = ctypes.c_int64(), ctypes.c_int64()
     _check(lib().mx_nvfp4_scales_shape(M, K, layout, ctypes.byref(r), ctypes.byref(c)))
@@ -240,7 +253,7 @@ def mx_quantize_nvfp4(x, global_scale, layout=SWIZZLED, H=None, *, codes=None, s
     codes = _codes_out(codes, x, M, K, E2M1)
     scales = _scales_out(scales, x, *mx_nvfp4_scales_shape(M, K, layout))
     _check(lib().mx_quantize_nvfp4(_ptr(x), M, K, _ptr(H), g, _ptr(global_scale), layout,
-                                   _ptr(codes), _ptr(scales), _stream_ptr(stream)))
+                                   _ptr(codes), _ptr(scales), _stream_ptr(stream, x)))
     return codes, scales
 
 
@@ -252,10 +265,11 @@ def mx_qdq_nvfp4(x, global_scale, H=None, *, y=None, stream=None):
     if y is None:
         y = torch.empty_like(x)
     _check(lib().mx_qdq_nvfp4(_ptr(x), M, K, _ptr(H), g, _ptr(global_scale), _ptr(y),
-                              _stream_ptr(stream)))
+                              _stream_ptr(stream, x)))
     return y
 
 
+@functools.lru_cache(maxsize=4096)
 def mx_nvfp4_grouped_scales_shape(M_total: int, E: int, K: int,
                                   layout: int = SWIZZLED) -> tuple[int, int]:
     r, c = ctypes.c_int64(), ctypes.c_int64()
@@ -280,7 +294,7 @@ def mx_quantize_nvfp4_grouped(x, row_offsets, global_scales, layout=SWIZZLED, *,
     scales = _scales_out(scales, x, *mx_nvfp4_grouped_scales_shape(M, E, K, layout))
     _check(lib().mx_quantize_nvfp4_grouped(_ptr(x), _ptr(row_offsets), E, M, K,
                                            _ptr(global_scales), layout, _ptr(codes),
-                                           _ptr(scales), _stream_ptr(stream)))
+                                           _ptr(scales), _stream_ptr(stream, x)))
     return codes, scales
 
 
@@ -306,7 +320,7 @@ def mx_dequantize_nvfp4(codes, scales, K, global_scale, layout=SWIZZLED, *, y=No
               and y.is_contiguous()):
         raise ValueError("y must be a contiguous CUDA bfloat16 tensor of M * K elements")
     _check(lib().mx_dequantize_nvfp4(_ptr(codes), _ptr(scales), M, K, _ptr(global_scale), layout,
-                                     _ptr(y), _stream_ptr(stream)))
+                                     _ptr(y), _stream_ptr(stream, codes)))
     return y
 
 
@@ -316,7 +330,7 @@ def mx_rotate_debug(x, H, *, y=None, stream=None):
     g = _rotation(H)
     if y is None:
         y = torch.empty((M, K), dtype=torch.float32, device=x.device)
-    _check(lib().mx_rotate_debug(_ptr(x), M, K, _ptr(H), g, _ptr(y), _stream_ptr(stream)))
+    _check(lib().mx_rotate_debug(_ptr(x), M, K, _ptr(H), g, _ptr(y), _stream_ptr(stream, x)))
     return y
 
 

@@ -186,6 +186,30 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
     for (int e = tid; e < a.E; e += kThreads) s_gs[e] = __ldg(a.gscale + e);
   }
 
+  const uint8_t* x = static_cast<const uint8_t*>(a.x);
+  const int64_t cblk = a.K >> 5;  // blocks per row
+  const int64_t nblk = a.M * cblk;
+  // Plain calls walk the blocks with a grid stride. Grouped calls give each CTA one contiguous
+  // range, so that a thread's row advances by only kThreads / (K/32) rows per step and its
+  // expert can be tracked incrementally instead of searched for every block.
+  int64_t b, b_end, stride;
+  if (GROUPED) {
+    const int64_t per_cta = ((nblk + gridDim.x - 1) / gridDim.x + kThreads - 1) / kThreads * kThreads;
+    b = (int64_t)blockIdx.x * per_cta + tid;
+    b_end = (int64_t)(blockIdx.x + 1) * per_cta < nblk ? (int64_t)(blockIdx.x + 1) * per_cta : nblk;
+    stride = kThreads;
+  } else {
+    b = (int64_t)blockIdx.x * kThreads + tid;
+    b_end = nblk;
+    stride = (int64_t)gridDim.x * kThreads;
+  }
+  const int64_t row_step = stride / cblk, col_step = stride - row_step * cblk;
+  int64_t row = b / cblk, col = b - row * cblk;  // advanced incrementally below
+  uint32_t cur[16], nxt[16];
+  if (b < b_end) {  // the first block's load is in flight during the grouped prologue
+    load32B(x + b * 64, cur);
+    load32B(x + b * 64 + 32, cur + 8);
+  }
   if (GROUPED) {
     // expert e owns ceil(n_e / 128) * 128 padded scale rows; s_prow is their prefix sum
     int64_t nb[4];
@@ -227,32 +251,8 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
     __syncthreads();
   }
 
-  const uint8_t* x = static_cast<const uint8_t*>(a.x);
-  const int64_t cblk = a.K >> 5;  // blocks per row
-  const int64_t nblk = a.M * cblk;
-  // Plain calls walk the blocks with a grid stride. Grouped calls give each CTA one contiguous
-  // range, so that a thread's row advances by only kThreads / (K/32) rows per step and its
-  // expert can be tracked incrementally instead of searched for every block.
-  int64_t b, b_end, stride;
-  if (GROUPED) {
-    const int64_t per_cta = ((nblk + gridDim.x - 1) / gridDim.x + kThreads - 1) / kThreads * kThreads;
-    b = (int64_t)blockIdx.x * per_cta + tid;
-    b_end = (int64_t)(blockIdx.x + 1) * per_cta < nblk ? (int64_t)(blockIdx.x + 1) * per_cta : nblk;
-    stride = kThreads;
-  } else {
-    b = (int64_t)blockIdx.x * kThreads + tid;
-    b_end = nblk;
-    stride = (int64_t)gridDim.x * kThreads;
-  }
-  const int64_t row_step = stride / cblk, col_step = stride - row_step * cblk;
-  int64_t row = b / cblk, col = b - row * cblk;  // advanced incrementally below
   int e = GROUPED ? last_not_above(s_off, a.E, row) : 0;  // expert of `row` (grouped)
   int e_gs = -1;                                          // expert whose gs / r6 are loaded
-  uint32_t cur[16], nxt[16];
-  if (b < b_end) {
-    load32B(x + b * 64, cur);
-    load32B(x + b * 64 + 32, cur + 8);
-  }
   for (; b < b_end; b += stride) {
     const int64_t bn = b + stride;
     if (bn < b_end) {  // next block in flight while this one is converted
