@@ -21,7 +21,8 @@
 // the K-major no-swizzle core-matrix layout, written once per CTA:
 //   element (n, k) = H[k][n] at (k / 8) * (g * 16) + n * 16 + (k % 8) * 2.
 // Every mbarrier wait is bounded (2 s); a wait that runs out sets the device error word and
-// the thread stops waiting from then on.
+// the thread stops waiting from then on. Calls with very few rows go to a plain FMA kernel
+// instead (mx_rotate_small_kernel, below), which is faster at those sizes.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -339,19 +340,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++first_loads;
     }
   }
-  // The epilogue warps stage B = H^T: the 16-byte loads of H are issued before the block-wide
-  // barrier, the shared-memory writes and the arrival on h_ready (initialized by thread 0)
-  // after it.
-  constexpr int kVecs = G * G / 8;
-  constexpr int kPer = (kVecs + kEpiThreads - 1) / kEpiThreads;
-  uint4 hv[kPer];
+  // The epilogue warps stage B = H^T one 16-byte core-matrix row at a time: row c of the
+  // layout (k-group c / G, column n = c % G) holds H[8 (c / G) + t][n], t = 0..7, and sits at
+  // byte 16 c, so consecutive threads write consecutive 16 bytes (no bank conflicts). Its eight
+  // 2-byte loads (consecutive threads: consecutive columns of a row of H) are issued before
+  // the block-wide barrier; the packing, the shared-memory writes and the arrival on h_ready
+  // (initialized by thread 0) come after it.
+  constexpr int kChunks = G * G / 8;
+  constexpr int kPer = (kChunks + kEpiThreads - 1) / kEpiThreads;
+  uint16_t hv[kPer][8];
   if (warp >= 2) {
-    const uint4* H = static_cast<const uint4*>(a.H);
+    const uint16_t* H = static_cast<const uint16_t*>(a.H);
     const int et = tid - 64;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-      const int v = et + i * kEpiThreads;
-      if (v < kVecs) hv[i] = H[v];
+      const int c = et + i * kEpiThreads;
+      if (c < kChunks) {
+        const int k0 = (c / G) * 8, n = c % G;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) hv[i][t] = __ldg(H + (k0 + t) * G + n);
+      }
     }
   }
   if (warp == 1) {
@@ -365,15 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = tid - 64;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-      const int v = et + i * kEpiThreads;
-      if (v < kVecs) {
-        const int k = (v * 8) / G, n0 = (v * 8) % G;  // H[k][n0 .. n0 + 7]
-        const uint32_t w[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+      const int c = et + i * kEpiThreads;
+      if (c < kChunks) {
+        uint32_t w[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          *reinterpret_cast<uint16_t*>(sB + (k / 8) * (G * 16) + (n0 + j) * 16 + (k % 8) * 2) =
-              (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
-        }
+        for (int t = 0; t < 4; ++t) w[t] = (uint32_t)hv[i][2 * t] | ((uint32_t)hv[i][2 * t + 1] << 16);
+        *reinterpret_cast<uint4*>(sB + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
     fence_proxy_async_smem();
@@ -550,6 +555,181 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------------------------------
+// Few rows (M <= kSmallRows, M * g <= kSmallWork): the same rotation and quantization with
+// plain fp32 FMAs, one CTA per 128-column tile, x and H staged in shared memory. At these
+// sizes the tensor-core kernel's fixed latency chain (tensor memory allocation, TMA load, MMA,
+// tensor-memory read, TMA store) is most of a call, while the arithmetic is a few thousand
+// FMAs per thread. Thread (r, cg) computes columns
+// 8 cg .. 8 cg + 7 of the tile for row r, y_j = sum_i x[r][c0 + i] * H[i][j - c0] with c0 the
+// start of the column's g-chunk, accumulated in fp32 in increasing i; the four threads of a
+// 32-element block (two of a 16-element NVFP4 block) combine their abs-max with shuffles. The
+// CTA writes the tile's swizzled scale tile(s) whole (pad rows zero) from shared memory.
+// ------------------------------------------------------------------------------------------
+constexpr int kSmallRows = 16;
+constexpr int kSmallThreads = kSmallRows * 16;
+// The FMA kernel takes a call when M <= kSmallRows and M * g <= kSmallWork: measured in CUDA
+// graphs on GB300 it is then faster than the tensor-core kernel (M = 1: 1.7 vs 3.7 us at
+// g = 32, 3.4 vs 4.3 us at g = 128), while at M = 16, g = 128 its 8 g FMAs per thread make it
+// slower (4.8 vs 4.3 us at K = 8192, 7.8 vs 5.3 us at K = 28672).
+constexpr int kSmallWork = 512;
+
+// abs-max of 8 fp32 values as sign-free fp32 bits; NaN propagates.
+__device__ __forceinline__ uint32_t absmax_f32x8(const float* y) {
+  float m[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(m[i]) : "f"(y[2 * i]), "f"(y[2 * i + 1]));
+  }
+  asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(m[0]) : "f"(m[0]), "f"(m[2]));
+  asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(m[1]) : "f"(m[1]), "f"(m[3]));
+  asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(m[0]) : "f"(m[0]), "f"(m[1]));
+  return __float_as_uint(m[0]) & 0x7FFFFFFFu;
+}
+
+template <int FMT, int OUT, bool SWZ, int G>
+__global__ void __launch_bounds__(kSmallThreads)
+    mx_rotate_small_kernel(RotArgs a) {
+  constexpr bool kNv = FMT == kFmtNVFP4;
+  constexpr int kScaleTiles = kNv ? 2 : 1;  // 128x4 scale tiles per 128 columns
+  constexpr int kHv = (G * G / 8 + kSmallThreads - 1) / kSmallThreads;  // 16-byte H loads
+  __shared__ __align__(16) uint16_t s_h[G * G];                        // H, row-major
+  __shared__ __align__(16) uint16_t s_x[kSmallRows * kTileCols];        // the tile's rows of x
+  __shared__ __align__(16) uint8_t s_scale[SWZ && OUT == kRotCodes ? kScaleTiles * 512 : 16];
+  const int tid = threadIdx.x, r = tid >> 4, cg = tid & 15;
+  const int64_t cb = blockIdx.x;
+  const int64_t col = cb * kTileCols + cg * 8;
+  const bool ok = r < a.M && col < a.K;
+
+  // stage H and x[r][col .. col + 7] (every 16-byte load issued before one barrier)
+  uint4 hreg[kHv];
+#pragma unroll
+  for (int i = 0; i < kHv; ++i) {
+    const int v = tid + i * kSmallThreads;
+    if (v < G * G / 8) hreg[i] = __ldg(static_cast<const uint4*>(a.H) + v);
+  }
+  uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+  if (ok) xv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + r * a.K + col));
+#pragma unroll
+  for (int i = 0; i < kHv; ++i) {
+    const int v = tid + i * kSmallThreads;
+    if (v < G * G / 8) reinterpret_cast<uint4*>(s_h)[v] = hreg[i];
+  }
+  reinterpret_cast<uint4*>(s_x)[tid] = xv;  // row r, columns 8 cg .. 8 cg + 7 of the tile
+  if (SWZ && OUT == kRotCodes) {
+    for (int i = tid; i < kScaleTiles * 128; i += kSmallThreads) {
+      reinterpret_cast<uint32_t*>(s_scale)[i] = 0u;
+    }
+  }
+  __syncthreads();
+
+  // rotation: 8 outputs of row r, chunk start c0 = col - jj0 (inside the tile: G divides 128)
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  if (ok) {
+    const int jj0 = (int)(col % G);
+    const uint16_t* xr = s_x + r * kTileCols + cg * 8 - jj0;
+#pragma unroll 4
+    for (int i0 = 0; i0 < G; i0 += 8) {
+      const uint4 xq = *reinterpret_cast<const uint4*>(xr + i0);
+      const uint32_t xw[4] = {xq.x, xq.y, xq.z, xq.w};
+#pragma unroll
+      for (int ii = 0; ii < 8; ++ii) {
+        const float xi = (ii & 1) ? bf16_hi(xw[ii >> 1]) : bf16_lo(xw[ii >> 1]);
+        const uint4 hq = *reinterpret_cast<const uint4*>(s_h + (i0 + ii) * G + jj0);
+        const uint32_t hw[4] = {hq.x, hq.y, hq.z, hq.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[2 * j] = fmaf(xi, bf16_lo(hw[j]), acc[2 * j]);
+          acc[2 * j + 1] = fmaf(xi, bf16_hi(hw[j]), acc[2 * j + 1]);
+        }
+      }
+    }
+  }
+
+  if (OUT == kRotDebug) {
+    if (ok) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + r * a.K + col);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    return;
+  }
+
+  // block scale: abs-max over the 4 threads of a 32-element block (2 of a 16-element block)
+  uint32_t amax = absmax_f32x8(acc);
+  amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  if (!kNv) amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  uint32_t byte;
+  uint32_t o[4];
+  if constexpr (kNv) {
+    const float gs = __ldg(a.gscale);
+    const float r6 = __fdiv_rn(gs, 6.0f);
+    const NvScales n = nv_scales(amax, amax, gs, r6);
+    byte = n.bytes & 0xFFu;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mul2(acc[2 * i], acc[2 * i + 1], n.enc[0]);
+    if (OUT == kRotQdq) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = n.special[0] ? kBf16NaNx2 : qdq2_e2m1(acc[2 * i], acc[2 * i + 1], n.dq[0]);
+    } else {
+      o[0] = n.special[0] ? 0u : codes8_e2m1(acc);
+    }
+  } else {
+    byte = scale_byte_from_amax_bits<FMT>(amax);
+    const float inv = inv_scale_of(byte);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mul2(acc[2 * i], acc[2 * i + 1], inv);
+    if (OUT == kRotQdq) {
+      const float sc = scale_of(byte);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = qdq2<FMT>(acc[2 * i], acc[2 * i + 1], sc);
+      if (byte == 255u) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = kBf16NaNx2;
+      }
+    } else if (FMT == kFmtE2M1) {
+      o[0] = byte == 255u ? 0u : codes8_e2m1(acc);
+    } else {
+      const uint2 c = codes8_e4m3(acc);
+      o[0] = byte == 255u ? kE4M3NaNx4 : c.x;
+      o[1] = byte == 255u ? kE4M3NaNx4 : c.y;
+    }
+  }
+
+  // element outputs
+  if (ok) {
+    if (OUT == kRotQdq) {
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + r * a.K + col) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+    } else if (FMT == kFmtE4M3) {
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.out) + r * a.K + col) = make_uint2(o[0], o[1]);
+    } else {
+      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.out) + r * (a.K / 2) + col / 2) = o[0];
+    }
+  }
+  if (OUT != kRotCodes) return;
+
+  // scales: one thread per block writes its byte
+  const int per_block = kNv ? 2 : 4;  // threads per scale block
+  const int sc_col = cg / per_block;  // scale column within the tile
+  const bool writer = ok && (cg % per_block) == 0;
+  if (!SWZ) {
+    if (writer) a.scales[r * a.scale_cols + cb * (kNv ? 8 : 4) + sc_col] = (uint8_t)byte;
+    return;
+  }
+  __syncthreads();  // the staged tile(s) are zero
+  if (writer) s_scale[(sc_col >> 2) * 512 + swizzle_in_tile(r, sc_col & 3)] = (uint8_t)byte;
+  __syncthreads();
+  const int64_t per_rb = a.scale_cols / 4;  // 128x4 tiles per row block
+  const int64_t first = cb * kScaleTiles;
+  const int words = (first + kScaleTiles <= per_rb ? kScaleTiles : 1) * 32;  // 16-byte words
+  if (tid < words) {
+    reinterpret_cast<uint4*>(a.scales + first * 512)[tid] = reinterpret_cast<const uint4*>(s_scale)[tid];
+  }
+}
+
+// ------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------
 // Tensor map of a row-major [rows, cols] matrix of 1- or 2-byte elements, boxes of box_rows x
@@ -581,6 +761,11 @@ cudaError_t make_tensor_map(CUtensorMap* map, const void* base, int64_t rows, in
 
 template <int FMT, int OUT, bool SWZ, int G>
 cudaError_t launch_t(const RotArgs& a, cudaStream_t stream) {
+  if (a.M <= kSmallRows && a.M * G <= kSmallWork) {  // few rows: the FMA kernel
+    if (a.col_tiles <= 0) return cudaSuccess;
+    mx_rotate_small_kernel<FMT, OUT, SWZ, G><<<(unsigned)a.col_tiles, kSmallThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
   auto kern = mx_rotate_kernel<FMT, OUT, SWZ, G>;
   const void* k = reinterpret_cast<const void*>(kern);
   constexpr int smem = smem_request<FMT, G, OUT>();

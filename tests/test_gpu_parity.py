@@ -577,6 +577,87 @@ def test_rotated_qdq_rules(fmt, g, kind):
     assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
 
 
+def few_rows_K(g):
+    """A K with a partial last 128-column tile where g allows one (K % g == 0)."""
+    return {16: 288, 32: 288, 64: 320, 128: 384}[g]
+
+
+@pytest.mark.parametrize("kind", ["hadamard", "random"])
+@pytest.mark.parametrize("g", [16, 32, 64, 128])
+@pytest.mark.parametrize("M", [1, 3, 16])
+def test_few_rows_rotated_paths(M, g, kind):
+    """Calls with at most 16 rows (decode-sized) run on the FMA kernel: rotated values within
+    tolerance, rotate+quantize in both layouts (swizzled pads zero, canary bands intact) and
+    rotated QDQ under the rules, for both MX formats."""
+    K = few_rows_K(g)
+    xb = W.rotate_quant_activation(M, K, stream=M * 1000 + g)
+    H = rotation(g, kind)
+    x, Hd = T.to_gpu(xb), T.to_gpu(H)
+    y = mxq.mx_rotate_debug(x, Hd).cpu().numpy()
+    assert T.check_rotated_values(y, O.rotate(xb, H), g) <= 1.0
+    for fmt in FMTS:
+        for layout in LAYOUTS:
+            rows, cols = mxq.mx_scales_shape(M, K, layout)
+            nc = M * O.code_bytes_per_row(fmt, K)
+            cfull, codes = guarded(nc)
+            sfull, scales = guarded(rows * cols)
+            mxq.mx_rotate_quantize(x, Hd, fmt, layout, codes=codes, scales=scales)
+            c = T.u8(codes).reshape(M, -1)
+            s = T.u8(scales).reshape(rows, cols)
+            assert_guards(cfull, nc)
+            assert_guards(sfull, rows * cols)
+            if layout == O.SWIZZLED:
+                assert not T.swizzle_pads(s, M, K).any()
+                s = T.unswizzle(s, M, K)
+            stats = T.check_rotated_codes(xb, H, fmt, c, s)
+            assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+        yfull, ybytes = guarded(M * K * 2)
+        mxq.mx_qdq(x, fmt, Hd, y=ybytes.view(torch.bfloat16).view(M, K))
+        assert_guards(yfull, M * K * 2)
+        T.check_rotated_qdq(xb, H, fmt, T.u8(ybytes).view(np.uint16).reshape(M, K))
+
+
+@pytest.mark.parametrize("g", [16, 32, 64, 128])
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_few_rows_identity_rotation_is_bit_exact(M, g):
+    """x * I is exact in fp32 on the FMA kernel too: codes, scales (both layouts) and QDQ equal
+    the plain path's oracle bit for bit, MX and NVFP4 (quantize and QDQ)."""
+    K = few_rows_K(g)
+    xb = W.mxfp8_linear_quant(M, K, stream=M * 100 + g)
+    H = T.to_gpu(rotation(g, "identity"))
+    x = T.to_gpu(xb)
+    for fmt in FMTS:
+        for layout in LAYOUTS:
+            c, s = mxq.mx_rotate_quantize(x, H, fmt, layout)
+            rc, rs = O.quantize(xb, fmt, layout)
+            np.testing.assert_array_equal(T.u8(s), rs)
+            np.testing.assert_array_equal(T.u8(c), rc)
+        np.testing.assert_array_equal(T.bf16_bits(mxq.mx_qdq(x, fmt, H)), O.qdq(xb, fmt))
+    gs = gs_of(xb)
+    for layout in LAYOUTS:
+        c, s = mxq.mx_quantize_nvfp4(x, gs_tensor(gs), layout, H)
+        rc, rs = O.nvfp4_quantize(xb, gs, layout)
+        np.testing.assert_array_equal(T.u8(s), rs)
+        np.testing.assert_array_equal(T.u8(c), rc)
+    np.testing.assert_array_equal(T.bf16_bits(mxq.mx_qdq_nvfp4(x, gs_tensor(gs), H)),
+                                  O.nvfp4_qdq(xb, gs))
+
+
+@pytest.mark.parametrize("g", [16, 32, 64, 128])
+def test_few_rows_nvfp4_hadamard_rules(g):
+    M, K = 7, few_rows_K(g)
+    xb = W.rotate_quant_activation(M, K, stream=g + 3)
+    H = rotation(g)
+    gs = np.float32(448 * 6 / 8.0)
+    for layout in LAYOUTS:
+        c, s = nv_quantize(xb, gs, layout, H)
+        if layout == O.SWIZZLED:
+            s = T.unswizzle(s, M, 2 * K)
+        stats = T.check_rotated_nvfp4(xb, H, gs, c, s)
+        assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+    T.check_rotated_nvfp4_qdq(xb, H, gs, nv_qdq(xb, gs, H))
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_rotate_quantize_full_size_sampled_rows(fmt):
     """The largest activation of the rotate+quantize workload, x[8192, 28672], swizzled scales:
