@@ -73,6 +73,8 @@ __device__ __forceinline__ void load_block(const uint8_t* codes, int64_t b, Code
 
 template <int FMT, bool SWZ>
 __global__ void __launch_bounds__(kThreads) mx_dequant_kernel(DequantArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
   const uint8_t* codes = static_cast<const uint8_t*>(a.codes);
   const int64_t cblk = a.K >> 5;
   const int64_t nblk = a.M * cblk;
@@ -83,11 +85,11 @@ __global__ void __launch_bounds__(kThreads) mx_dequant_kernel(DequantArgs a) {
   auto scale_at = [&](int64_t r, int64_t c, int64_t flat) -> uint32_t {
     if (FMT == kFmtNVFP4) {  // scale columns 2c and 2c + 1: adjacent bytes, 2-byte aligned
       const int64_t off = SWZ ? swizzled_offset(r, 2 * c, a.scale_cols) : 2 * flat;
-      return __ldg(reinterpret_cast<const uint16_t*>(a.scales + off));
+      return load_u16(a.scales + off);
     }
-    return SWZ ? __ldg(a.scales + swizzled_offset(r, c, a.scale_cols)) : __ldg(a.scales + flat);
+    return load_u8(a.scales + (SWZ ? swizzled_offset(r, c, a.scale_cols) : flat));
   };
-  const float gs = FMT == kFmtNVFP4 ? __ldg(a.gscale) : 0.0f;
+  const float gs = FMT == kFmtNVFP4 ? load_f32(a.gscale) : 0.0f;
   CodeBlock<FMT> cur, nxt;
   if (b < nblk) {
     load_block<FMT>(codes, b, cur);
@@ -156,8 +158,7 @@ cudaError_t launch_t(const DequantArgs& a, cudaStream_t stream) {
   const int resident = resident_ctas(k, kThreads, 0, 0);
   if (resident <= 0) return cudaErrorInvalidConfiguration;
   const int grid = (int)(need < resident ? need : resident);
-  mx_dequant_kernel<FMT, SWZ><<<grid, kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(&mx_dequant_kernel<FMT, SWZ>, dim3(grid), dim3(kThreads), 0, stream, a);
 }
 
 }  // namespace

@@ -201,18 +201,56 @@ __device__ __forceinline__ int64_t swizzled_offset(int64_t pr, int64_t c, int64_
   return ((pr >> 7) * (cp >> 2) + (c >> 2)) * 512 + (pr & 31) * 16 + ((pr >> 5) & 3) * 4 + (c & 3);
 }
 
-// 32-byte vector load through the non-coherent path, not kept in L1 (streamed once).
+// Loads of kernel inputs. Every one is a coherent ld.global, never the non-coherent (.nc,
+// __ldg) path: a kernel launched with programmatic stream serialization (see pdl_wait) runs
+// while the kernel before it may still be writing what it reads, and .nc loads are defined
+// only for data that stays unchanged for the whole life of the kernel (the compiler may also
+// schedule them early). Each is an asm volatile, so it stays after pdl_wait in program order.
+// 32-byte vector load, not kept in L1 (streamed once).
 __device__ __forceinline__ void load32B(const void* p, uint32_t* r) {
-  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+  asm volatile("ld.global.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                  "=r"(r[6]), "=r"(r[7])
                : "l"(p));
 }
 
 __device__ __forceinline__ void load16B(const void* p, uint32_t* r) {
-  asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "l"(p));
+}
+
+// 16-byte vector load (kept in L1: small operands read by many threads, such as H)
+__device__ __forceinline__ uint4 load_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float load_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t load_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t load_u8(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ int64_t load_s64(const int64_t* p) {
+  int64_t v;
+  asm volatile("ld.global.s64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
 }
 
 // 32-byte vector store, evict-first (written once, not re-read by this kernel).
@@ -269,6 +307,18 @@ __device__ __forceinline__ NvScales nv_scales(uint32_t amax0, uint32_t amax1, fl
   n.bytes = pair;
   return n;
 }
+
+// Programmatic dependent launch. Every kernel of the library is launched with programmatic
+// stream serialization (launch_pdl): its CTAs may be scheduled while the kernel before it on
+// the stream is still finishing. Each kernel lets the next one be scheduled as soon as all of
+// its own CTAs are running, and waits for the previous kernel to complete (with its memory
+// visible) before its first global memory access, so stream order is kept; only set-up that
+// touches nothing in global memory (shared memory, barriers, kernel parameters) runs earlier.
+// Without a programmatic dependency both instructions have no effect.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Swizzled scale position of (r, c) inside one 128x4 tile.
 __device__ __forceinline__ int swizzle_in_tile(int r, int c) {

@@ -139,10 +139,10 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read_all_but_one() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
-// all committed bulk stores have finished reading shared memory (their global writes complete
-// on their own; the kernel's end makes them visible to later work)
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// all committed bulk stores have completed, their global writes included (the kernel ends
+// after this, so a dependent kernel that stops waiting at its pdl_wait sees every output)
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Both 64-column boxes of tile t (128 rows x 128 columns) into one ring stage.
@@ -319,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Thread 0 initializes the barriers and is also the TMA producer: it fills the first stages
   // of the ring at once (they wait for nothing), so that the first loads are in flight while
   // the block allocates tensor memory and stages H.
+  pdl_launch_dependents();
   int first_loads = 0;
   if (tid == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
@@ -335,6 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(h_ready), kEpiWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // Everything above touches only shared memory and kernel parameters; x, H, the outputs and
+  // tensor memory are used only once the kernel before this one on the stream has completed.
+  pdl_wait();
+  if (tid == 0) {
     for (int64_t t = blockIdx.x; t < n_tiles && first_loads < kStages; t += gridDim.x) {
       load_tile(a, &tmap, sA_u32 + first_loads * kStageBytes, smem_u32(full + first_loads), t);
       ++first_loads;
@@ -348,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (initialized by thread 0) come after it.
   constexpr int kChunks = G * G / 8;
   constexpr int kPer = (kChunks + kEpiThreads - 1) / kEpiThreads;
-  uint16_t hv[kPer][8];
+  uint32_t hv[kPer][8];
   if (warp >= 2) {
     const uint16_t* H = static_cast<const uint16_t*>(a.H);
     const int et = tid - 64;
@@ -358,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (c < kChunks) {
         const int k0 = (c / G) * 8, n = c % G;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) hv[i][t] = __ldg(H + (k0 + t) * G + n);
+        for (int t = 0; t < 8; ++t) hv[i][t] = load_u16(H + (k0 + t) * G + n);
       }
     }
   }
@@ -377,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (c < kChunks) {
         uint32_t w[4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) w[t] = (uint32_t)hv[i][2 * t] | ((uint32_t)hv[i][2 * t + 1] << 16);
+        for (int t = 0; t < 4; ++t) w[t] = hv[i][2 * t] | (hv[i][2 * t + 1] << 16);
         *reinterpret_cast<uint4*>(sB + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
@@ -442,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kNv = FMT == kFmtNVFP4;
     float gs = 0.0f, r6 = 0.0f;  // NVFP4 global scale and gs / 6
     if (kNv && OUT != kRotDebug) {
-      gs = __ldg(a.gscale);
+      gs = load_f32(a.gscale);
       r6 = __fdiv_rn(gs, 6.0f);
     }
     int it = 0;
@@ -547,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  if (OUT != kRotDebug && warp == 2 && lane == 0) bulk_wait_read_all();
+  if (OUT != kRotDebug && warp == 2 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -599,16 +605,18 @@ __global__ void __launch_bounds__(kSmallThreads)
   const int64_t cb = blockIdx.x;
   const int64_t col = cb * kTileCols + cg * 8;
   const bool ok = r < a.M && col < a.K;
+  pdl_launch_dependents();
+  pdl_wait();
 
   // stage H and x[r][col .. col + 7] (every 16-byte load issued before one barrier)
   uint4 hreg[kHv];
 #pragma unroll
   for (int i = 0; i < kHv; ++i) {
     const int v = tid + i * kSmallThreads;
-    if (v < G * G / 8) hreg[i] = __ldg(static_cast<const uint4*>(a.H) + v);
+    if (v < G * G / 8) hreg[i] = load_v4(static_cast<const uint4*>(a.H) + v);
   }
   uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-  if (ok) xv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + r * a.K + col));
+  if (ok) xv = load_v4(static_cast<const uint16_t*>(a.x) + r * a.K + col);
 #pragma unroll
   for (int i = 0; i < kHv; ++i) {
     const int v = tid + i * kSmallThreads;
@@ -663,7 +671,7 @@ __global__ void __launch_bounds__(kSmallThreads)
   uint32_t byte;
   uint32_t o[4];
   if constexpr (kNv) {
-    const float gs = __ldg(a.gscale);
+    const float gs = load_f32(a.gscale);
     const float r6 = __fdiv_rn(gs, 6.0f);
     const NvScales n = nv_scales(amax, amax, gs, r6);
     byte = n.bytes & 0xFFu;
@@ -763,8 +771,8 @@ template <int FMT, int OUT, bool SWZ, int G>
 cudaError_t launch_t(const RotArgs& a, cudaStream_t stream) {
   if (a.M <= kSmallRows && a.M * G <= kSmallWork) {  // few rows: the FMA kernel
     if (a.col_tiles <= 0) return cudaSuccess;
-    mx_rotate_small_kernel<FMT, OUT, SWZ, G><<<(unsigned)a.col_tiles, kSmallThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(&mx_rotate_small_kernel<FMT, OUT, SWZ, G>, dim3((unsigned)a.col_tiles),
+                      dim3(kSmallThreads), 0, stream, a);
   }
   auto kern = mx_rotate_kernel<FMT, OUT, SWZ, G>;
   const void* k = reinterpret_cast<const void*>(kern);
@@ -791,8 +799,7 @@ cudaError_t launch_t(const RotArgs& a, cudaStream_t stream) {
   const int resident = resident_ctas(k, kThreads, smem, 1);
   if (resident <= 0) return cudaErrorInvalidConfiguration;
   const int grid = (int)(n_tiles < resident ? n_tiles : resident);
-  kern<<<grid, kThreads, smem, stream>>>(map, ymap, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, map, ymap, a);
 }
 
 template <int FMT, int OUT, bool SWZ>

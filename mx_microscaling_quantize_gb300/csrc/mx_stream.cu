@@ -177,13 +177,15 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
   __shared__ float s_gs[GROUPED && kNv ? kMaxExperts : 1];  // NVFP4 grouped: gs of expert e
   const int tid = threadIdx.x;
   constexpr int kCodeBytes = QDQ ? 64 : (FMT == kFmtE4M3 ? 32 : 16);  // output bytes per block
+  pdl_launch_dependents();
+  pdl_wait();
   float gs = 0.0f, r6 = 0.0f;  // NVFP4 global scale and gs / 6 (grouped: of the current expert)
   if (kNv && !GROUPED) {
-    gs = __ldg(a.gscale);
+    gs = load_f32(a.gscale);
     r6 = __fdiv_rn(gs, 6.0f);
   }
   if (kNv && GROUPED) {
-    for (int e = tid; e < a.E; e += kThreads) s_gs[e] = __ldg(a.gscale + e);
+    for (int e = tid; e < a.E; e += kThreads) s_gs[e] = load_f32(a.gscale + e);
   }
 
   const uint8_t* x = static_cast<const uint8_t*>(a.x);
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
       const int e = tid * 4 + j;
       nb[j] = 0;
       if (e < a.E) {
-        int64_t lo = a.offsets[e], hi = a.offsets[e + 1];
+        int64_t lo = load_s64(a.offsets + e), hi = load_s64(a.offsets + e + 1);
         lo = lo < 0 ? 0 : (lo > a.M ? a.M : lo);
         hi = hi < lo ? lo : (hi > a.M ? a.M : hi);
         s_off[e] = lo;
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
       }
     }
     if (tid == 0) {
-      const int64_t end = a.offsets[a.E];
+      const int64_t end = load_s64(a.offsets + a.E);
       s_off[a.E] = end < 0 ? 0 : (end > a.M ? a.M : end);
     }
     int64_t incl = local;
@@ -366,8 +368,8 @@ cudaError_t launch_t(const StreamArgs& a, cudaStream_t stream) {
   const int resident = resident_ctas(k, kThreads, 0, 0);
   if (resident <= 0) return cudaErrorInvalidConfiguration;
   const int grid = (int)(need < resident ? need : resident);
-  mx_stream_kernel<FMT, QDQ, SWZ, GROUPED><<<grid, kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(&mx_stream_kernel<FMT, QDQ, SWZ, GROUPED>, dim3(grid), dim3(kThreads), 0,
+                    stream, a);
 }
 
 template <int FMT>

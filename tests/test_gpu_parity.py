@@ -702,6 +702,64 @@ def test_rotation_sweep_full_size_sampled_rows():
             T.check_rotated_qdq(xb[rows], H, fmt, out)
 
 
+def test_dependent_calls_keep_stream_order():
+    """Every kernel is launched with programmatic stream serialization (it may be scheduled
+    while the kernel before it finishes) and waits for that kernel before touching global
+    memory. A chain of calls in which each reads what the one before wrote (and some overwrite
+    what an earlier one read) gives the same bytes back to back, eagerly and in a CUDA graph, as
+    with a synchronization after every call."""
+    M, K = 4096, 8192
+    x = T.to_gpu(W.rotation_sweep_input("attn_in", M, K))
+    H = T.to_gpu(rotation(32))
+    H128 = T.to_gpu(rotation(128))
+    gs = torch.tensor([448.0 * 6 / 8.0], device="cuda")
+    a, b, d = (torch.empty_like(x) for _ in range(3))
+    c4, s4 = mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED)
+    c8, s8 = mxq.mx_quantize(x, mxq.E4M3, mxq.LINEAR)
+    cn, sn = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED)
+    small = torch.empty((8, K), dtype=torch.bfloat16, device="cuda")
+    cs, ss = mxq.mx_rotate_quantize(x[:8], H, mxq.E2M1, mxq.SWIZZLED)
+    outs = (a, b, d, c4, s4, c8, s8, cn, sn, small, cs, ss)
+
+    def chain(sync):
+        steps = [
+            lambda: mxq.mx_qdq(x, mxq.E4M3, H128, y=a),
+            lambda: mxq.mx_qdq(a, mxq.E2M1, y=b),
+            lambda: mxq.mx_rotate_quantize(b, H, mxq.E2M1, mxq.SWIZZLED, codes=c4, scales=s4),
+            lambda: mxq.mx_dequantize(c4, s4, K, mxq.E2M1, mxq.SWIZZLED, y=d),
+            lambda: mxq.mx_qdq(d, mxq.E4M3, H, y=a),
+            lambda: mxq.mx_quantize(a, mxq.E4M3, mxq.LINEAR, codes=c8, scales=s8),
+            lambda: mxq.mx_dequantize(c8, s8, K, mxq.E4M3, mxq.LINEAR, y=b),
+            lambda: mxq.mx_quantize_nvfp4(b, gs, mxq.SWIZZLED, codes=cn, scales=sn),
+            lambda: mxq.mx_dequantize_nvfp4(cn, sn, K, gs, mxq.SWIZZLED, y=d),
+            lambda: mxq.mx_qdq(d[:8], mxq.E2M1, H, y=small),
+            lambda: mxq.mx_rotate_quantize(small, H, mxq.E2M1, mxq.SWIZZLED, codes=cs, scales=ss),
+        ]
+        for step in steps:
+            step()
+            if sync:
+                torch.cuda.synchronize()
+
+    chain(True)
+    want = [t.clone() for t in outs]
+    for t in outs:
+        t.zero_()
+    chain(False)
+    torch.cuda.synchronize()
+    for got, ref in zip(outs, want):
+        assert torch.equal(got.view(torch.uint8), ref.view(torch.uint8))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        chain(False)
+    for t in outs:
+        t.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    for got, ref in zip(outs, want):
+        assert torch.equal(got.view(torch.uint8), ref.view(torch.uint8))
+    assert mxq.mx_device_errors() == 0
+
+
 def test_calls_capture_into_a_cuda_graph():
     """The entry points allocate and synchronize nothing, so they can be captured in a CUDA
     graph (the CuTe QDQ page's requirement); replays equal eager calls bit for bit."""
