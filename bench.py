@@ -481,6 +481,7 @@ CASES = {
     "nvfp4_quant": "NVFP4 quantize, swizzled E4M3 scales, weight x[8192,8192]",
     "nvfp4_rotate_quant": "NVFP4 rotate(g=16)+quantize, swizzled, x[8192,28672]",
     "nvfp4_dequant": "NVFP4 dequantize, swizzled E4M3 scales, codes of the weight x[8192,8192]",
+    "rotate_quant_decode": "E2M1 rotate(g=32)+quantize, swizzled, x[16,28672] (FMA kernel)",
 }
 
 
@@ -528,6 +529,12 @@ def run_case(args):
         c, s = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED)
         fn = lambda: mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, codes=c, scales=s)
         nbytes = 2 * x.numel() + c.numel() + x.numel() // 16
+    elif args.case == "rotate_quant_decode":
+        x = to_gpu(W.rotate_quant_activation(16, 28672), dev)
+        H = to_gpu(W.normalized_hadamard_bf16(32), dev)
+        c, s = mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED)
+        fn = lambda: mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, codes=c, scales=s)
+        nbytes = 2 * x.numel() + c.numel() + s.numel()
     elif args.case == "nvfp4_dequant":
         x = to_gpu(W.mxfp4_qdq_weight(), dev)
         gs = torch.tensor([448.0 * 6.0], device=dev) / x.float().abs().max()
