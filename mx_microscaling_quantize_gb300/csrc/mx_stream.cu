@@ -253,18 +253,33 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
     __syncthreads();
   }
 
-  int e = GROUPED ? last_not_above(s_off, a.E, row) : 0;  // expert of `row` (grouped)
-  int e_gs = -1;                                          // expert whose gs / r6 are loaded
+  // Grouped: the expert of `row` and, in registers, its first row, end row and first padded
+  // scale row (and NVFP4 global scale); reloaded from shared memory only when `row` leaves it.
+  int e = GROUPED ? last_not_above(s_off, a.E, row) : 0;
+  int64_t e_lo = 0, e_hi = 0, e_prow = 0;
+  if (GROUPED) {
+    e_lo = s_off[e];
+    e_hi = s_off[e + 1];
+    e_prow = s_prow[e];
+    if (kNv) {
+      gs = s_gs[e];
+      r6 = __fdiv_rn(gs, 6.0f);
+    }
+  }
   for (; b < b_end; b += stride) {
     const int64_t bn = b + stride;
     if (bn < b_end) {  // next block in flight while this one is converted
       load32B(x + bn * 64, nxt);
       load32B(x + bn * 64 + 32, nxt + 8);
     }
-    if (GROUPED) {
-      while (e + 1 < a.E && row >= s_off[e + 1]) ++e;  // rows only grow within a thread
-      if (kNv && e != e_gs) {
-        e_gs = e;
+    if (GROUPED && row >= e_hi && e + 1 < a.E) {  // rows only grow within a thread
+      do {
+        ++e;
+      } while (e + 1 < a.E && row >= s_off[e + 1]);
+      e_lo = s_off[e];
+      e_hi = s_off[e + 1];
+      e_prow = s_prow[e];
+      if (kNv) {
         gs = s_gs[e];
         r6 = __fdiv_rn(gs, 6.0f);
       }
@@ -281,9 +296,8 @@ __global__ void __launch_bounds__(kThreads) mx_stream_kernel(StreamArgs a) {
       int64_t pr = row;
       bool ok = true;
       if (GROUPED && SWZ) {
-        ok = row >= s_off[e] && row < s_off[e + 1];
-        pr = s_prow[e] + (row - s_off[e]);
-        ok = ok && pr < a.scale_rows;
+        pr = e_prow + (row - e_lo);
+        ok = row >= e_lo && row < e_hi && pr < a.scale_rows;
       }
       if (kNv) {
         const int64_t off = SWZ ? swizzled_offset(pr, 2 * col, a.scale_cols) : 2 * b;
