@@ -658,6 +658,69 @@ def test_few_rows_nvfp4_hadamard_rules(g):
     T.check_rotated_nvfp4_qdq(xb, H, gs, nv_qdq(xb, gs, H))
 
 
+@pytest.mark.parametrize("M,g", [(16, 32), (17, 32), (8, 64), (9, 64), (4, 128), (5, 128),
+                                 (16, 16), (17, 16)])
+def test_rotated_dispatch_boundary(M, g):
+    """Both sides of the switch between the FMA kernel (M <= 16 and M * g <= 512) and the
+    tensor-core kernel: rotate+quantize (both formats and layouts), rotated QDQ and rotated
+    NVFP4 follow the oracle under the rules."""
+    K = few_rows_K(g) + 2 * 128
+    xb = W.rotate_quant_activation(M, K, stream=7 * M + g)
+    H = rotation(g)
+    x, Hd = T.to_gpu(xb), T.to_gpu(H)
+    for fmt in FMTS:
+        for layout in LAYOUTS:
+            c, s = mxq.mx_rotate_quantize(x, Hd, fmt, layout)
+            c, s = T.u8(c), T.u8(s)
+            if layout == O.SWIZZLED:
+                assert not T.swizzle_pads(s, M, K).any()
+                s = T.unswizzle(s, M, K)
+            stats = T.check_rotated_codes(xb, H, fmt, c, s)
+            assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+        T.check_rotated_qdq(xb, H, fmt, qdq(xb, fmt, H))
+    gs = np.float32(448 * 6 / 8.0)
+    c, s = nv_quantize(xb, gs, O.SWIZZLED, H)
+    stats = T.check_rotated_nvfp4(xb, H, gs, c, T.unswizzle(s, M, 2 * K))
+    assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+    T.check_rotated_nvfp4_qdq(xb, H, gs, nv_qdq(xb, gs, H))
+
+
+def test_random_shapes_every_entry_point():
+    """Seeded random shapes (M from 1 to 300, K a random multiple of max(g, 32)): plain
+    quantize, QDQ and dequantize of both formats and layouts and NVFP4 quantize / QDQ /
+    dequantize bit-exact against the oracle; rotate+quantize and rotated QDQ under the rules."""
+    rng = np.random.default_rng(2024)
+    for case in range(16):
+        M = int(rng.choice([1, 2, 7, 16, 17, 100, 129, 300]))
+        g = int(rng.choice([16, 32, 64, 128]))
+        K = int(rng.integers(1, 12)) * max(g, 32)
+        xb = W.rotate_quant_activation(M, K, stream=1000 + case)
+        x = T.to_gpu(xb)
+        for fmt in FMTS:
+            for layout in LAYOUTS:
+                c, s = mxq.mx_quantize(x, fmt, layout)
+                rc, rs = O.quantize(xb, fmt, layout)
+                np.testing.assert_array_equal(T.u8(c), rc)
+                np.testing.assert_array_equal(T.u8(s), rs)
+                np.testing.assert_array_equal(T.bf16_bits(mxq.mx_dequantize(c, s, K, fmt, layout)),
+                                              O.qdq(xb, fmt))
+            np.testing.assert_array_equal(T.bf16_bits(mxq.mx_qdq(x, fmt)), O.qdq(xb, fmt))
+        gs = gs_of(xb)
+        assert_nvfp4_exact(xb, gs)
+        c, s = mxq.mx_quantize_nvfp4(x, gs_tensor(gs), mxq.SWIZZLED)
+        np.testing.assert_array_equal(
+            T.bf16_bits(mxq.mx_dequantize_nvfp4(c, s, K, gs_tensor(gs), mxq.SWIZZLED)),
+            O.nvfp4_qdq(xb, gs))
+        H = rotation(g)
+        fmt = FMTS[case % 2]
+        c, s = mxq.mx_rotate_quantize(x, T.to_gpu(H), fmt, mxq.SWIZZLED)
+        s = T.u8(s)
+        assert not T.swizzle_pads(s, M, K).any()
+        stats = T.check_rotated_codes(xb, H, fmt, T.u8(c), T.unswizzle(s, M, K))
+        assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, (M, K, g, stats)
+        T.check_rotated_qdq(xb, H, fmt, qdq(xb, fmt, H))
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_rotate_quantize_full_size_sampled_rows(fmt):
     """The largest activation of the rotate+quantize workload, x[8192, 28672], swizzled scales:
