@@ -71,8 +71,11 @@ __device__ __forceinline__ void load_block(const uint8_t* codes, int64_t b, Code
   else load16B(codes + b * 16, cb.w);
 }
 
+// Minimum of one CTA per SM: the compiler may then use 55-79 registers (4 or 3 CTAs per SM
+// instead of 5 at 48), which measured 5-8% faster back to back (E2M1 swizzled x[8192,8192]
+// 29.6 -> 28.2 us, NVFP4 30.6 -> 28.2 us).
 template <int FMT, bool SWZ>
-__global__ void __launch_bounds__(kThreads) mx_dequant_kernel(DequantArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) mx_dequant_kernel(DequantArgs a) {
   pdl_launch_dependents();
   pdl_wait();
   const uint8_t* codes = static_cast<const uint8_t*>(a.codes);
