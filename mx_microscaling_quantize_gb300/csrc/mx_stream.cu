@@ -3,14 +3,17 @@
 // The input [M, K] is contiguous and K % 32 == 0, so it is a flat sequence of 32-element
 // blocks; codes and QDQ outputs are flat sequences too, and linear scales are indexed by the
 // flat block number. A persistent grid walks the blocks with a grid stride (grouped calls: one
-// contiguous range per CTA): consecutive threads own consecutive blocks (a warp moves 2 KiB of contiguous input with 32-byte vector
-// loads), and each thread loads its next block before working on the current one. A thread
+// contiguous range per CTA): consecutive threads own consecutive blocks (a warp moves 2 KiB of
+// contiguous input with 32-byte vector loads), and each thread loads its next block before
+// working on the current one. A thread
 // takes the block's abs-max with packed bf16x2 abs-max instructions, derives the E8M0 byte
 // from the exponent field, converts in registers with the hardware paired converters, and
 // writes the block's codes (16 or 32 bytes) or dequantized bf16 (two 32-byte stores) and its
 // scale byte: at the flat block index (linear) or at its place in the 128x4 tiles (swizzled;
 // the row/column of the block are advanced incrementally, grouped calls map the row to its
 // expert's padded row). A final pass over the whole grid writes zeros into the pad bytes.
+// NVFP4 (E2M1 codes, one E4M3 scale per 16 elements under an fp32 global scale) runs on the
+// same kernel: a thread's 32 elements are two NVFP4 blocks.
 #include <algorithm>
 #include <map>
 #include <mutex>
