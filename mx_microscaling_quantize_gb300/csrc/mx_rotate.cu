@@ -111,22 +111,28 @@ __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, bool* f
     }
   }
 }
+// L2 policy for data touched once (inputs read once, outputs written once): evict first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 // 2-D tensor-map load of one box into shared memory, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(l2_evict_first_policy())
       : "memory");
 }
 
 // 2-D tensor-map store of one box from shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(src)
-               : "memory");
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src), "l"(l2_evict_first_policy())
+      : "memory");
 }
 // shared -> global bulk copy in the current bulk group (16-byte aligned, size % 16 == 0)
 __device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t src, uint32_t bytes) {
