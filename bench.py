@@ -267,7 +267,10 @@ def extra_workloads(dev, peak):
     - steady: launches back to back, cycling over enough copies of the buffers (inputs and
       outputs) that the copies together are at least three times L2, so no launch finds its
       inputs in L2 and each pays for the write-back of what the launch before it wrote, as in
-      a stream of such calls; the mean over the loop."""
+      a stream of such calls; the mean over the loop.
+    - graph (calls under 32 MiB of traffic only, which the two above time as launch latency):
+      device time per call of 100 calls captured in one CUDA graph and replayed (the small
+      buffer copies then partly sit in L2)."""
     import torch
     import mx_microscaling_quantize_gb300 as mxq
     from mx_microscaling_quantize_gb300 import workloads as W
@@ -304,6 +307,31 @@ def extra_workloads(dev, peak):
         e.synchronize()
         return s.elapsed_time(e) / 1e3 / iters
 
+    def graph_time(fns, calls=100):
+        """Device time per call of `calls` launches (cycling over fns) captured in one CUDA graph
+        and replayed: what a call costs inside a captured serving step, without host launches."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for fn in fns:
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(calls):
+                fns[i % len(fns)]()
+        graph.replay()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(5):
+            graph.replay()
+        e.record()
+        e.synchronize()
+        del graph
+        return s.elapsed_time(e) / 1e3 / (5 * calls)
+
     def measure(name, nbytes, elems, make, footprint, iters=30):
         """make(k) -> a launch closure over buffer set k (k = 0: the given buffers, k > 0:
         copies); footprint: bytes of one set's inputs and outputs."""
@@ -317,6 +345,8 @@ def extra_workloads(dev, peak):
                      "steady_GB/s": nbytes / t_steady / 1e9,
                      "steady_frac": nbytes / t_steady / 1e9 / peak,
                      "steady_us": t_steady * 1e6, "steady_sets": sets}
+        if footprint < (32 << 20):  # small calls: launch-bound above; device time in a graph
+            out[name]["graph_us"] = graph_time(fns) * 1e6
         del fns
 
     def copy_of(t, k):

@@ -753,6 +753,40 @@ def test_weight_rotate_quantize_full_size_sampled_rows(N, K):
             del c
 
 
+@pytest.mark.parametrize("K", W.ROTATE_QUANT_K)
+@pytest.mark.parametrize("M", W.ROTATE_QUANT_M)
+def test_rotate_quant_workload_grid(M, K):
+    """The fused rotate + MXFP4 quantize workload at every one of its (M, K) sizes (g = 32
+    normalized Hadamard, swizzled scales, rows padded to 128): all rows up to M = 128, 24 sampled
+    rows beyond, under the rules; swizzle pads zero over the whole buffer."""
+    xb = W.rotate_quant_activation(M, K)
+    H = rotation(32)
+    c, s = mxq.mx_rotate_quantize(T.to_gpu(xb), T.to_gpu(H), mxq.E2M1, mxq.SWIZZLED)
+    s = T.u8(s)
+    assert not T.swizzle_pads(s, M, K).any()
+    s = T.unswizzle(s, M, K)
+    rows = np.arange(M) if M <= 128 else np.sort(
+        np.random.default_rng(M + K).choice(M, 24, replace=False))
+    rows_t = torch.from_numpy(rows).cuda()
+    stats = T.check_rotated_codes(xb[rows], H, O.E2M1, T.u8(c[rows_t]), s[rows])
+    assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+
+
+@pytest.mark.parametrize("layer", [n for n, _, _ in W.ROTATION_SWEEP_LAYERS])
+def test_rotation_sweep_every_layer_sampled_rows(layer):
+    """The rotation-size sweep on each of the three decoder-layer inputs at full size: every g
+    in {16, 32, 64, 128} and both formats, 8 sampled rows under the rules."""
+    xb = W.rotation_sweep_input(layer)
+    x = T.to_gpu(xb)
+    rows = np.sort(np.random.default_rng(len(layer)).choice(xb.shape[0], 8, replace=False))
+    rows_t = torch.from_numpy(rows).cuda()
+    for g in W.ROTATION_SWEEP_G:
+        H = rotation(g)
+        for fmt in FMTS:
+            out = T.bf16_bits(mxq.mx_qdq(x, fmt, T.to_gpu(H))[rows_t])
+            T.check_rotated_qdq(xb[rows], H, fmt, out)
+
+
 def test_rotation_sweep_full_size_sampled_rows():
     """Rotated QDQ at the full down-projection input [4096, 28672], every g and format."""
     xb = W.rotation_sweep_input("down_proj_in")
