@@ -227,6 +227,15 @@ mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, in
  */
 mx_status mx_device_errors(int* flags);
 
+/*
+ * Failure-detection self-test (no counterpart on the pages): launches one thread that waits on
+ * an mbarrier nothing ever arrives at, with the same bounded-wait routine the tensor-core
+ * kernel uses for every wait, given up after limit_ns nanoseconds (1 .. 100,000,000). The wait
+ * gives up, sets bit 0 of the device error word (read it with mx_device_errors) and the kernel
+ * returns; the context stays usable. Errors: MX_ERR_SHAPE (limit out of range), MX_ERR_CUDA.
+ */
+mx_status mx_selftest_bounded_wait(int64_t limit_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,6 +31,7 @@ EXPORTS = (
     "mx_rotate_quantize", "mx_quantize_grouped", "mx_dequantize", "mx_nvfp4_scales_shape",
     "mx_quantize_nvfp4", "mx_qdq_nvfp4", "mx_dequantize_nvfp4", "mx_nvfp4_grouped_scales_shape",
     "mx_quantize_nvfp4_grouped", "mx_rotate_debug", "mx_device_errors",
+    "mx_selftest_bounded_wait",
 )
 
 
@@ -69,6 +70,7 @@ def lib() -> ctypes.CDLL:
         "mx_quantize_nvfp4_grouped": (i32, [p, p, i32, i64, i64, p, i32, p, p, p]),
         "mx_rotate_debug": (i32, [p, i64, i64, p, i32, p, p]),
         "mx_device_errors": (i32, [ctypes.POINTER(ctypes.c_int)]),
+        "mx_selftest_bounded_wait": (i32, [i64, p]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -339,3 +341,14 @@ def mx_device_errors() -> int:
     v = ctypes.c_int()
     _check(lib().mx_device_errors(ctypes.byref(v)))
     return v.value
+
+
+def mx_selftest_bounded_wait(limit_ns: int = 1_000_000, *, stream=None, device: int = 0) -> None:
+    """Run one bounded wait that nothing completes (it gives up after limit_ns and sets the
+    device error word; read it with mx_device_errors())."""
+    st = stream
+    if st is None:
+        st = _raw_stream(device) if _raw_stream is not None else torch.cuda.current_stream(device).cuda_stream
+    elif isinstance(st, torch.cuda.Stream):
+        st = st.cuda_stream
+    _check(lib().mx_selftest_bounded_wait(limit_ns, st))

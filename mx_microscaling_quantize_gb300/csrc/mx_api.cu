@@ -383,6 +383,12 @@ mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, in
                                       static_cast<cudaStream_t>(stream)));
 }
 
+mx_status mx_selftest_bounded_wait(int64_t limit_ns, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 100000000) return MX_ERR_SHAPE;
+  return from_cuda(mxq::launch_wait_selftest((unsigned long long)limit_ns,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 mx_status mx_device_errors(int* flags) {
   if (!flags) return MX_ERR_NULL;
   unsigned int v = 0;

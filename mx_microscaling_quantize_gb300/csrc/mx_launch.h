@@ -81,6 +81,9 @@ cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const Rot
 // Reads and clears the device error word of the current device (synchronizes).
 cudaError_t read_device_errors(unsigned int* flags);
 
+// One wait on an mbarrier that nothing arrives at, given up after limit_ns (sets the error word).
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);
+
 // Number of CTAs of `kernel` that fit on the current device at once: SMs x CTAs per SM from
 // the kernel's registers and shared memory against the SM's limits, capped at max_per_sm when
 // positive. Also raises the kernel's dynamic shared-memory limit when dyn_smem > 48 KiB.

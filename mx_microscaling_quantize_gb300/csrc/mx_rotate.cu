@@ -98,13 +98,15 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for the phase of the given parity; gives up after kWaitLimitNs, and at once once this
-// thread has given up before (*failed). A give-up sets the device error word.
-__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, bool* failed) {
+// Wait for the phase of the given parity; gives up after limit_ns (kWaitLimitNs in the
+// kernels), and at once once this thread has given up before (*failed). A give-up sets the
+// device error word.
+__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, bool* failed,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (*failed || mbar_try_wait(bar, parity)) return;
   const unsigned long long t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       *failed = true;
       atomicOr(&g_device_errors, kErrWaitTimeout);
       return;
@@ -743,6 +745,19 @@ __global__ void __launch_bounds__(kSmallThreads)
   }
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing ever arrives at,
+// with the kernels' wait routine and a short limit; the wait gives up and sets the device error
+// word, and the kernel returns.
+__global__ void mx_wait_selftest_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    bool failed = false;
+    mbar_wait(smem_u32(&bar), 0, &failed, limit_ns);
+  }
+}
+
 // ------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------
@@ -832,6 +847,11 @@ cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const Rot
   if (fmt == kFmtE2M1) return launch_fmt<kFmtE2M1>(out_kind, swizzled, g, a, stream);
   if (fmt == kFmtNVFP4) return launch_fmt<kFmtNVFP4>(out_kind, swizzled, g, a, stream);
   return launch_fmt<kFmtE4M3>(out_kind, swizzled, g, a, stream);
+}
+
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream) {
+  mx_wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t read_device_errors(unsigned int* flags) {

@@ -216,6 +216,12 @@ def test_device_errors_null(L):
     assert L.mx_device_errors(None) == NULL
 
 
+def test_selftest_bounded_wait_validation(L):
+    assert L.mx_selftest_bounded_wait(0, None) == SHAPE
+    assert L.mx_selftest_bounded_wait(-5, None) == SHAPE
+    assert L.mx_selftest_bounded_wait(100_000_001, None) == SHAPE
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mxq, "_lib", None)
     monkeypatch.setattr(mxq, "LIB_PATH", str(tmp_path / "missing.so"))

@@ -857,6 +857,20 @@ def test_dependent_calls_keep_stream_order():
     assert mxq.mx_device_errors() == 0
 
 
+def test_bounded_wait_gives_up_and_reports():
+    """Failure detection without a fault: a wait that nothing completes (the tensor-core
+    kernel's bounded-wait routine, 1 ms limit) gives up, the device error word reports it once
+    (reading clears it), and the context still computes correct results afterwards."""
+    assert mxq.mx_device_errors() == 0
+    mxq.mx_selftest_bounded_wait(1_000_000)
+    assert mxq.mx_device_errors() == 1
+    assert mxq.mx_device_errors() == 0
+    xb = W.rotate_quant_activation(256, 1024, stream=77)
+    H = rotation(32, "identity")
+    np.testing.assert_array_equal(qdq(xb, O.E2M1, H), O.qdq(xb, O.E2M1))
+    assert mxq.mx_device_errors() == 0
+
+
 def test_calls_capture_into_a_cuda_graph():
     """The entry points allocate and synchronize nothing, so they can be captured in a CUDA
     graph (the CuTe QDQ page's requirement); replays equal eager calls bit for bit."""
