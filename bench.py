@@ -512,6 +512,9 @@ CASES = {
     "nvfp4_rotate_quant": "NVFP4 rotate(g=16)+quantize, swizzled, x[8192,28672]",
     "nvfp4_dequant": "NVFP4 dequantize, swizzled E4M3 scales, codes of the weight x[8192,8192]",
     "rotate_quant_decode": "E2M1 rotate(g=32)+quantize, swizzled, x[16,28672] (FMA kernel)",
+    "moe_quant_nvfp4": "NVFP4 grouped quantize, swizzled, 128 experts, per-expert scales, x[16384,2048]",
+    "qdq_vs_copy": "MXFP4 QDQ of the weight and activation, each followed by an elementwise "
+                   "copy of the same bytes (torch.mul(x, 1, out=y)) for profiler comparisons",
 }
 
 
@@ -559,6 +562,26 @@ def run_case(args):
         c, s = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED)
         fn = lambda: mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, codes=c, scales=s)
         nbytes = 2 * x.numel() + c.numel() + x.numel() // 16
+    elif args.case == "qdq_vs_copy":
+        # the reference copy is a torch elementwise kernel (2 bytes in, 2 out per element, like
+        # QDQ); it is profiled beside the QDQ launches, never part of the library's path
+        xw, xa = to_gpu(W.mxfp4_qdq_weight(), dev), to_gpu(W.mxfp4_qdq_activation(), dev)
+        yw, ya, cw, ca = (torch.empty_like(t) for t in (xw, xa, xw, xa))
+
+        def fn():
+            mxq.mx_qdq(xw, mxq.E2M1, y=yw)
+            torch.mul(xw, 1.0, out=cw)
+            mxq.mx_qdq(xa, mxq.E2M1, y=ya)
+            torch.mul(xa, 1.0, out=ca)
+        nbytes = 8 * (xw.numel() + xa.numel())
+    elif args.case == "moe_quant_nvfp4":
+        xb, off = W.moe_quant()
+        x = to_gpu(xb, dev)
+        offs = torch.from_numpy(off).to(dev)
+        gse = torch.full((len(off) - 1,), 100.0, device=dev)
+        c, s = mxq.mx_quantize_nvfp4_grouped(x, offs, gse, mxq.SWIZZLED)
+        fn = lambda: mxq.mx_quantize_nvfp4_grouped(x, offs, gse, mxq.SWIZZLED, codes=c, scales=s)
+        nbytes = 2 * x.numel() + c.numel() + s.numel()
     elif args.case == "rotate_quant_decode":
         x = to_gpu(W.rotate_quant_activation(16, 28672), dev)
         H = to_gpu(W.normalized_hadamard_bf16(32), dev)
@@ -598,7 +621,9 @@ def run_case(args):
     torch.cuda.synchronize()
     t = a.elapsed_time(b) / 1e3 / max(1, args.steps)
     print(json.dumps({"case": args.case, "what": CASES[args.case], "us_per_launch": t * 1e6,
-                      "GB/s": nbytes / t / 1e9, "gpu_launches": args.steps}), flush=True)
+                      "GB/s": nbytes / t / 1e9,
+                      "gpu_launches": args.steps * (2 if args.case == "qdq_vs_copy" else 1)}),
+          flush=True)
 
 
 def end_to_end(mxq, xw_b, xa_b, dev, steps):
