@@ -515,6 +515,8 @@ CASES = {
     "moe_quant_nvfp4": "NVFP4 grouped quantize, swizzled, 128 experts, per-expert scales, x[16384,2048]",
     "qdq_vs_copy": "MXFP4 QDQ of the weight and activation, each followed by an elementwise "
                    "copy of the same bytes (torch.mul(x, 1, out=y)) for profiler comparisons",
+    "quant_vs_cast": "MXFP8 quantize and dequantize of the weight x[8192,8192], each followed by "
+                     "torch's plain bf16 <-> float8_e4m3fn cast of the same bytes",
 }
 
 
@@ -574,6 +576,22 @@ def run_case(args):
             mxq.mx_qdq(xa, mxq.E2M1, y=ya)
             torch.mul(xa, 1.0, out=ca)
         nbytes = 8 * (xw.numel() + xa.numel())
+    elif args.case == "quant_vs_cast":
+        # torch's casts move the same bytes per element as the MXFP8 quantize (2 in, 1 out) and
+        # dequantize (1 in, 2 out) without the block scales; profiled beside them only
+        x = to_gpu(W.mxfp4_qdq_weight(), dev)
+        c, s = mxq.mx_quantize(x, mxq.E4M3, mxq.LINEAR)
+        y = torch.empty_like(x)
+        f8 = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=dev)
+        yb = torch.empty_like(x)
+        K = x.shape[1]
+
+        def fn():
+            mxq.mx_quantize(x, mxq.E4M3, mxq.LINEAR, codes=c, scales=s)
+            f8.copy_(x)
+            mxq.mx_dequantize(c, s, K, mxq.E4M3, mxq.LINEAR, y=y)
+            yb.copy_(f8)
+        nbytes = 6 * x.numel() + 2 * s.numel()
     elif args.case == "moe_quant_nvfp4":
         xb, off = W.moe_quant()
         x = to_gpu(xb, dev)
@@ -622,7 +640,8 @@ def run_case(args):
     t = a.elapsed_time(b) / 1e3 / max(1, args.steps)
     print(json.dumps({"case": args.case, "what": CASES[args.case], "us_per_launch": t * 1e6,
                       "GB/s": nbytes / t / 1e9,
-                      "gpu_launches": args.steps * (2 if args.case == "qdq_vs_copy" else 1)}),
+                      "gpu_launches": args.steps * (2 if args.case in ("qdq_vs_copy",
+                                                                       "quant_vs_cast") else 1)}),
           flush=True)
 
 
