@@ -658,6 +658,35 @@ def test_few_rows_nvfp4_hadamard_rules(g):
     T.check_rotated_nvfp4_qdq(xb, H, gs, nv_qdq(xb, gs, H))
 
 
+@pytest.mark.parametrize("g", [16, 32, 128])
+@pytest.mark.parametrize("M", [5, 40])
+def test_rotated_nan_and_inf_inputs(M, g):
+    """NaN and +-Inf inputs on both rotation kernels (M = 5: the FMA kernel for g <= 64; M = 40
+    and g = 128: the tensor-core kernel): every chunk holding one rotates to NaN/Inf values, its
+    blocks get scale byte 0xFF with the fill codes (QDQ: 0x7FC0), exactly as in the oracle; the
+    other chunks follow the rules."""
+    K = 512
+    v = np.random.default_rng(M * 10 + g).standard_normal((M, K)).astype(np.float32)
+    v[0, 3], v[M - 1, 200], v[M // 2, 511] = np.nan, np.inf, -np.inf
+    v[1, 130], v[1, 131] = np.inf, -np.inf
+    xb = W.to_bf16_bits(v)
+    H = rotation(g)
+    x, Hd = T.to_gpu(xb), T.to_gpu(H)
+    for fmt in FMTS:
+        c, s = mxq.mx_rotate_quantize(x, Hd, fmt, mxq.LINEAR)
+        c, s = T.u8(c), T.u8(s)
+        _, rs = O.rotate_quantize(xb, H, fmt, O.LINEAR)
+        special = rs == 255
+        assert special.any() and (s[special] == 255).all() and (s[~special] != 255).all()
+        stats = T.check_rotated_codes(xb, H, fmt, c, s)
+        assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+        out = qdq(xb, fmt, H)
+        ref = O.rotate_qdq(xb, H, fmt)
+        nan_ref = np.repeat(special, 32, axis=1)
+        np.testing.assert_array_equal(out[nan_ref], ref[nan_ref])
+        T.check_rotated_qdq(xb, H, fmt, out)
+
+
 @pytest.mark.parametrize("M,g", [(16, 32), (17, 32), (8, 64), (9, 64), (4, 128), (5, 128),
                                  (16, 16), (17, 16)])
 def test_rotated_dispatch_boundary(M, g):
