@@ -54,6 +54,8 @@ def parse_args():
     p.add_argument("--case", choices=sorted(CASES), default=None,
                    help="run one other workload only (for profiler captures): warmup + steps "
                         "launches, one JSON line with its kernel-only GB/s")
+    p.add_argument("--tiles-per-sm", type=int, default=8,
+                   help="rotate_quant_tiles: x[128, 128 * SMs * n] gives exactly n tiles per SM")
     return p.parse_args()
 
 
@@ -517,6 +519,8 @@ CASES = {
                    "copy of the same bytes (torch.mul(x, 1, out=y)) for profiler comparisons",
     "quant_vs_cast": "MXFP8 quantize and dequantize of the weight x[8192,8192], each followed by "
                      "torch's plain bf16 <-> float8_e4m3fn cast of the same bytes",
+    "rotate_quant_tiles": "E2M1 rotate(g=32)+quantize, swizzled, x[128, 128 * SMs * n]: exactly "
+                          "n = --tiles-per-sm tiles per SM, launches cycling over input copies",
 }
 
 
@@ -592,6 +596,22 @@ def run_case(args):
             mxq.mx_dequantize(c, s, K, mxq.E4M3, mxq.LINEAR, y=y)
             yb.copy_(f8)
         nbytes = 6 * x.numel() + 2 * s.numel()
+    elif args.case == "rotate_quant_tiles":
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        n = max(1, args.tiles_per_sm)
+        M, K = 128, 128 * sms * n
+        H = to_gpu(W.normalized_hadamard_bf16(32), dev)
+        copies = max(1, -(-400 // (6 * n * sms // 152)))  # together well above L2
+        xs = [to_gpu(W.rotate_quant_activation(M, K, stream=i), dev) for i in range(copies)]
+        outs = [mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED) for x in xs]
+        calls = [(x, c, s) for x, (c, s) in zip(xs, outs)]
+        it = [0]
+
+        def fn():
+            x, c, s = calls[it[0] % len(calls)]
+            it[0] += 1
+            mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, codes=c, scales=s)
+        nbytes = 2 * M * K + M * K // 2 + outs[0][1].numel()
     elif args.case == "moe_quant_nvfp4":
         xb, off = W.moe_quant()
         x = to_gpu(xb, dev)
