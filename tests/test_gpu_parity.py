@@ -488,6 +488,69 @@ def test_nvfp4_grouped_edge_counts(counts):
             np.testing.assert_array_equal(c, rc)
 
 
+def test_grouped_maximum_expert_count():
+    """1024 experts (the limit; the prologue's per-thread share of the expert scan is then
+    full), random counts with many empty experts, MXFP8 and NVFP4, both layouts."""
+    rng = np.random.default_rng(1024)
+    counts = rng.integers(0, 6, 1024) * (rng.random(1024) < 0.6)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    xb = W.mxfp8_linear_quant(int(off[-1]), 96, stream=1024)
+    gs = expert_global_scales(xb, off)
+    for layout in LAYOUTS:
+        c, s = grouped(xb, off, O.E4M3, layout)
+        rc, rs = O.quantize_grouped(xb, off, O.E4M3, layout, scale_rows=s.shape[0])
+        np.testing.assert_array_equal(s, rs)
+        np.testing.assert_array_equal(c, rc)
+        c, s = nv_grouped(xb, off, gs, layout)
+        rc, rs = O.nvfp4_quantize_grouped(xb, off, gs, layout, scale_rows=s.shape[0])
+        np.testing.assert_array_equal(s, rs)
+        np.testing.assert_array_equal(c, rc)
+
+
+def test_nvfp4_calls_capture_into_a_cuda_graph():
+    """NVFP4 quantize (plain and rotated), QDQ, dequantize and grouped quantize captured in one
+    CUDA graph replay bit-identically to eager calls."""
+    xb = W.rotation_sweep_input("attn_in", 256, 1024)
+    x = T.to_gpu(xb)
+    H = T.to_gpu(rotation(16))
+    gs = gs_tensor(gs_of(xb))
+    xm, off = W.moe_quant(E=8, tokens=700, K=256)
+    xg, offs = T.to_gpu(xm), torch.from_numpy(off).cuda()
+    gse = torch.full((8,), 50.0, device="cuda")
+    c, s = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED)
+    cr, sr = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, H)
+    y, yd = torch.empty_like(x), torch.empty_like(x)
+    cg, sg = mxq.mx_quantize_nvfp4_grouped(xg, offs, gse, mxq.SWIZZLED)
+    K = x.shape[1]
+
+    def calls():
+        mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, codes=c, scales=s)
+        mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, H, codes=cr, scales=sr)
+        mxq.mx_qdq_nvfp4(x, gs, H, y=y)
+        mxq.mx_dequantize_nvfp4(c, s, K, gs, mxq.SWIZZLED, y=yd)
+        mxq.mx_quantize_nvfp4_grouped(xg, offs, gse, mxq.SWIZZLED, codes=cg, scales=sg)
+
+    outs = (c, s, cr, sr, y, yd, cg, sg)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        calls()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in outs]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        calls()
+    for _ in range(2):
+        for t in outs:
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for got, want in zip(outs, eager):
+            assert torch.equal(got.view(torch.uint8), want.view(torch.uint8))
+    np.testing.assert_array_equal(T.bf16_bits(yd), O.nvfp4_qdq(xb, gs_of(xb)))
+
+
 def test_grouped_bad_offsets_stay_in_bounds():
     """Offsets that break the contract (decreasing, beyond M) give unspecified values but no
     access outside the buffers (canaries intact) and no error from the device."""
