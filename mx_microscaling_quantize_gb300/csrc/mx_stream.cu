@@ -335,8 +335,9 @@ __global__ void __launch_bounds__(kThreads, stream_min_ctas<FMT, QDQ, GROUPED>()
     // Zero the pad bytes of the swizzled buffer, spread over every thread of the grid: (A) in
     // each data row, the bytes past column K/32 of its last 4-byte word (only when
     // K/32 % 4 != 0); (B) every 4-byte word of every pad row (rows past M: a flat list of
-    // (row, word) items, so that a few wide pad rows do not serialize on a few threads; rows
-    // past an expert's rows inside its last 128-row block: one thread per scale row).
+    // (row, word) items, so that a few wide pad rows do not serialize on a few threads;
+    // grouped: the rows past the last expert as one contiguous range, the rows past an
+    // expert's rows inside its last 128-row block one thread per row).
     const int64_t cp = a.scale_cols, cp4 = cp >> 2;
     const int64_t dcols = kNv ? 2 * cblk : cblk;  // scale columns holding data
     const int64_t nthr = (int64_t)gridDim.x * kThreads;
@@ -362,16 +363,23 @@ __global__ void __launch_bounds__(kThreads, stream_min_ctas<FMT, QDQ, GROUPED>()
         *reinterpret_cast<uint32_t*>(a.scales + swizzled_offset(pr, c4, cp)) = 0u;
       }
     } else {
-      // pad rows lie between the experts' rows: one thread per scale row finds out whether
-      // its row is one (a search over the experts' padded row offsets) and zeroes it
-      for (int64_t pr = t0; pr < a.scale_rows; pr += nthr) {
-        bool pad = true;
-        if (pr < s_prow[a.E]) {
-          const int ex = last_not_above(s_prow, a.E, pr);
-          const int64_t n = s_off[ex + 1] > s_off[ex] ? s_off[ex + 1] - s_off[ex] : 0;
-          pad = pr - s_prow[ex] >= n;
-        }
-        if (pad) {
+      // Rows past the last expert's padded range are whole 128-row blocks, whose tiles form
+      // one contiguous byte range at the end of the buffer (tiles are row-block-major): zeroed
+      // with 16-byte stores spread over the grid. Pad rows inside an expert's last block lie
+      // between data rows: one thread per (expert, row of its last block) zeroes the row when
+      // it is one (no search: measured 0.2-0.6 us faster than a search per scale row).
+      const int64_t used = s_prow[a.E] < a.scale_rows ? s_prow[a.E] : a.scale_rows;
+      uint4* tail = reinterpret_cast<uint4*>(a.scales + used * cp);
+      const int64_t tail_vecs = (a.scale_rows - used) * cp / 16;
+      for (int64_t i = t0; i < tail_vecs; i += nthr) tail[i] = make_uint4(0u, 0u, 0u, 0u);
+      // inner pad rows: item (e, k) is row k of expert e's last 128-row block, a pad row when
+      // k >= n_e mod 128 (the expert's padded range ends with ceil(n_e/128)*128 - n_e of them)
+      for (int64_t j = t0; j < (int64_t)a.E * kTileRows; j += nthr) {
+        const int ex = (int)(j / kTileRows), k = (int)(j % kTileRows);
+        const int64_t n = s_off[ex + 1] > s_off[ex] ? s_off[ex + 1] - s_off[ex] : 0;
+        const int64_t last = s_prow[ex + 1] - kTileRows;  // first row of the last block
+        const int64_t pr = last + k;
+        if (n > 0 && pr >= s_prow[ex] + n && pr < used) {
           for (int64_t c4 = 0; c4 < cp; c4 += 4) {
             *reinterpret_cast<uint32_t*>(a.scales + swizzled_offset(pr, c4, cp)) = 0u;
           }
