@@ -11,7 +11,8 @@
 // writes the block's codes (16 or 32 bytes) or dequantized bf16 (two 32-byte stores) and its
 // scale byte: at the flat block index (linear) or at its place in the 128x4 tiles (swizzled;
 // the row/column of the block are advanced incrementally, grouped calls map the row to its
-// expert's padded row). A final pass over the whole grid writes zeros into the pad bytes.
+// expert's padded row). After the main loop a pass spread over the whole grid writes zeros
+// into the pad bytes.
 // NVFP4 (E2M1 codes, one E4M3 scale per 16 elements under an fp32 global scale) runs on the
 // same kernel: a thread's 32 elements are two NVFP4 blocks.
 #include <algorithm>
@@ -171,6 +172,74 @@ __device__ __forceinline__ int last_not_above(const int64_t* v, int n, int64_t k
   return lo;
 }
 
+// Pad bytes of a grouped call's swizzled scale buffer, spread evenly over every thread of the
+// grid (s_off: clamped first row of each expert and the end; s_prow: first padded scale row of
+// each expert and the total):
+//  (A) in each data row, the bytes past the last data column of its last 4-byte word (only when
+//      the data columns are not a multiple of 4);
+//  (B) the rows past the last expert's padded range: whole 128-row blocks, whose tiles form one
+//      contiguous byte range at the end of the buffer (tiles are row-block-major), zeroed with
+//      16-byte stores;
+//  (C) the pad rows inside each expert's last 128-row block (those at or past its row count):
+//      one warp per (expert, 4-byte word of the row) task, 4-byte stores into one tile.
+// Runs after the main loop. Its cost is the work of the warps that get a task, so the inner
+// pad rows are split into short per-warp tasks with 32-bit index arithmetic inside a tile:
+// measured 0.5-0.6 us less per call than one thread per pad row writing the row's words in a
+// loop (x[16384, 2048], 128 experts), and faster than running the same pass before the main
+// loop, where it delays the loop's loads.
+template <bool kNv>
+__device__ __forceinline__ void zero_grouped_pads(const StreamArgs& a, const int64_t* s_off,
+                                                  const int64_t* s_prow, int64_t cblk) {
+  const int64_t cp = a.scale_cols, cp4 = cp >> 2;
+  const int64_t dcols = kNv ? 2 * cblk : cblk;  // scale columns holding data
+  const int64_t nthr = (int64_t)gridDim.x * kThreads;
+  const int64_t t0 = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  const int64_t used = s_prow[a.E] < a.scale_rows ? s_prow[a.E] : a.scale_rows;
+  if (dcols & 3) {  // (A)
+    const int64_t c4 = dcols & ~int64_t(3);
+    for (int64_t r = t0; r < a.M; r += nthr) {
+      const int ex = last_not_above(s_off, a.E, r);
+      if (r < s_off[ex] || r >= s_off[ex + 1]) continue;  // rows outside every expert
+      const int64_t pr = s_prow[ex] + (r - s_off[ex]);
+      if (pr >= a.scale_rows) continue;
+      uint8_t* run = a.scales + swizzled_offset(pr, c4, cp);
+      for (int64_t c = dcols; c < c4 + 4; ++c) run[c - c4] = 0;
+    }
+  }
+  uint4* tail = reinterpret_cast<uint4*>(a.scales + used * cp);  // (B)
+  const int64_t tail_vecs = (a.scale_rows - used) * cp / 16;
+  for (int64_t i = t0; i < tail_vecs; i += nthr) tail[i] = make_uint4(0u, 0u, 0u, 0u);
+  // (C) one warp per (expert, 4-byte word) task; lane l takes rows l, l + 32, ... of the
+  // expert's last 128-row block, whose word sits in one 512-byte tile
+  const int lane = (int)(threadIdx.x & 31);
+  const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+  const int64_t tasks = (int64_t)a.E * cp4;
+  for (int64_t t = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < tasks;
+       t += nwarps) {
+    int ex;
+    int64_t w;
+    if (tasks <= 0xFFFFFFFFll) {
+      ex = (int)((uint32_t)t % (uint32_t)a.E);
+      w = (uint32_t)t / (uint32_t)a.E;
+    } else {
+      ex = (int)(t % a.E);
+      w = t / a.E;
+    }
+    const int64_t n = s_off[ex + 1] > s_off[ex] ? s_off[ex + 1] - s_off[ex] : 0;
+    if (n == 0) continue;
+    const int64_t last = s_prow[ex + 1] - kTileRows;  // first row of the last block (>= 0)
+    const int64_t first_pad = s_prow[ex] + n;
+    uint8_t* tile = a.scales + ((last >> 7) * cp4 + w) * 512;
+#pragma unroll
+    for (int k = lane; k < kTileRows; k += 32) {
+      const int64_t pr = last + k;
+      if (pr >= first_pad && pr < used) {
+        *reinterpret_cast<uint32_t*>(tile + (k & 31) * 16 + (k >> 5) * 4) = 0u;
+      }
+    }
+  }
+}
+
 // Register budget per instantiation (the grid is sized from the resulting occupancy): QDQ
 // kernels are given room for more registers (66, 3 CTAs per SM), which measured 2-3% faster
 // than the 50-register, 4-CTA build (x[8192,8192] 44.9 -> 44.0 us, x[4096,8192] 22.8 -> 22.1 us
@@ -197,9 +266,6 @@ __global__ void __launch_bounds__(kThreads, stream_min_ctas<FMT, QDQ, GROUPED>()
   if (kNv && !GROUPED) {
     gs = load_f32(a.gscale);
     r6 = __fdiv_rn(gs, 6.0f);
-  }
-  if (kNv && GROUPED) {
-    for (int e = tid; e < a.E; e += kThreads) s_gs[e] = load_f32(a.gscale + e);
   }
 
   const uint8_t* x = static_cast<const uint8_t*>(a.x);
@@ -236,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, stream_min_ctas<FMT, QDQ, GROUPED>()
       nb[j] = 0;
       if (e < a.E) {
         int64_t lo = load_s64(a.offsets + e), hi = load_s64(a.offsets + e + 1);
+        if (kNv) s_gs[e] = load_f32(a.gscale + e);
         lo = lo < 0 ? 0 : (lo > a.M ? a.M : lo);
         hi = hi < lo ? lo : (hi > a.M ? a.M : hi);
         s_off[e] = lo;
@@ -331,13 +398,13 @@ __global__ void __launch_bounds__(kThreads, stream_min_ctas<FMT, QDQ, GROUPED>()
     }
   }
 
-  if (SWZ && !QDQ) {
+  if (SWZ && !QDQ && GROUPED) zero_grouped_pads<kNv>(a, s_off, s_prow, cblk);
+  if (SWZ && !QDQ && !GROUPED) {
     // Zero the pad bytes of the swizzled buffer, spread over every thread of the grid: (A) in
     // each data row, the bytes past column K/32 of its last 4-byte word (only when
     // K/32 % 4 != 0); (B) every 4-byte word of every pad row (rows past M: a flat list of
-    // (row, word) items, so that a few wide pad rows do not serialize on a few threads;
-    // grouped: the rows past the last expert as one contiguous range, the rows past an
-    // expert's rows inside its last 128-row block one thread per row).
+    // (row, word) items, so that a few wide pad rows do not serialize on a few threads).
+    // Grouped calls write their pad bytes with zero_grouped_pads.
     const int64_t cp = a.scale_cols, cp4 = cp >> 2;
     const int64_t dcols = kNv ? 2 * cblk : cblk;  // scale columns holding data
     const int64_t nthr = (int64_t)gridDim.x * kThreads;
@@ -345,46 +412,14 @@ __global__ void __launch_bounds__(kThreads, stream_min_ctas<FMT, QDQ, GROUPED>()
     if (dcols & 3) {
       const int64_t c4 = dcols & ~int64_t(3);
       for (int64_t r = t0; r < a.M; r += nthr) {
-        int64_t pr = r;
-        if (GROUPED) {
-          const int ex = last_not_above(s_off, a.E, r);
-          if (r >= s_off[ex + 1]) continue;  // rows outside every expert have no scales
-          pr = s_prow[ex] + (r - s_off[ex]);
-          if (pr >= a.scale_rows) continue;
-        }
-        uint8_t* run = a.scales + swizzled_offset(pr, c4, cp);
+        uint8_t* run = a.scales + swizzled_offset(r, c4, cp);
         for (int64_t c = dcols; c < c4 + 4; ++c) run[c - c4] = 0;
       }
     }
-    if (!GROUPED) {
-      const int64_t pad_rows = a.scale_rows - a.M;
-      for (int64_t i = t0; i < pad_rows * cp4; i += nthr) {
-        const int64_t pr = a.M + i % pad_rows, c4 = (i / pad_rows) * 4;
-        *reinterpret_cast<uint32_t*>(a.scales + swizzled_offset(pr, c4, cp)) = 0u;
-      }
-    } else {
-      // Rows past the last expert's padded range are whole 128-row blocks, whose tiles form
-      // one contiguous byte range at the end of the buffer (tiles are row-block-major): zeroed
-      // with 16-byte stores spread over the grid. Pad rows inside an expert's last block lie
-      // between data rows: one thread per (expert, row of its last block) zeroes the row when
-      // it is one (no search: measured 0.2-0.6 us faster than a search per scale row).
-      const int64_t used = s_prow[a.E] < a.scale_rows ? s_prow[a.E] : a.scale_rows;
-      uint4* tail = reinterpret_cast<uint4*>(a.scales + used * cp);
-      const int64_t tail_vecs = (a.scale_rows - used) * cp / 16;
-      for (int64_t i = t0; i < tail_vecs; i += nthr) tail[i] = make_uint4(0u, 0u, 0u, 0u);
-      // inner pad rows: item (e, k) is row k of expert e's last 128-row block, a pad row when
-      // k >= n_e mod 128 (the expert's padded range ends with ceil(n_e/128)*128 - n_e of them)
-      for (int64_t j = t0; j < (int64_t)a.E * kTileRows; j += nthr) {
-        const int ex = (int)(j / kTileRows), k = (int)(j % kTileRows);
-        const int64_t n = s_off[ex + 1] > s_off[ex] ? s_off[ex + 1] - s_off[ex] : 0;
-        const int64_t last = s_prow[ex + 1] - kTileRows;  // first row of the last block
-        const int64_t pr = last + k;
-        if (n > 0 && pr >= s_prow[ex] + n && pr < used) {
-          for (int64_t c4 = 0; c4 < cp; c4 += 4) {
-            *reinterpret_cast<uint32_t*>(a.scales + swizzled_offset(pr, c4, cp)) = 0u;
-          }
-        }
-      }
+    const int64_t pad_rows = a.scale_rows - a.M;
+    for (int64_t i = t0; i < pad_rows * cp4; i += nthr) {
+      const int64_t pr = a.M + i % pad_rows, c4 = (i / pad_rows) * 4;
+      *reinterpret_cast<uint32_t*>(a.scales + swizzled_offset(pr, c4, cp)) = 0u;
     }
   }
 }

@@ -551,11 +551,13 @@ def test_nvfp4_calls_capture_into_a_cuda_graph():
     np.testing.assert_array_equal(T.bf16_bits(yd), O.nvfp4_qdq(xb, gs_of(xb)))
 
 
-def test_grouped_bad_offsets_stay_in_bounds():
-    """Offsets that break the contract (decreasing, beyond M) give unspecified values but no
-    access outside the buffers (canaries intact) and no error from the device."""
+@pytest.mark.parametrize("first", [0, 30])
+def test_grouped_bad_offsets_stay_in_bounds(first):
+    """Offsets that break the contract (decreasing, beyond M, first offset above 0 with rows
+    before it) give unspecified values but no access outside the buffers (canaries intact) and
+    no error from the device. K = 64: two scale columns, so the partial-word pad pass runs."""
     M, K, E = 200, 64, 4
-    off = np.array([0, 150, 20, 500, 200], dtype=np.int64)
+    off = np.array([first, 150, 20, 500, 200], dtype=np.int64)
     x = T.to_gpu(W.mxfp8_linear_quant(M, K))
     rows, cols = mxq.mx_grouped_scales_shape(M, E, K, mxq.SWIZZLED)
     cfull, codes = guarded(M * K)
