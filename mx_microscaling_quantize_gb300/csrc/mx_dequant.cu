@@ -71,12 +71,36 @@ __device__ __forceinline__ void load_block(const uint8_t* codes, int64_t b, Code
   else load16B(codes + b * 16, cb.w);
 }
 
+// Iterations per warp whose codes are prefetched into L2 before pdl_wait. Measured on GB300
+// (steady, back to back, x[8192, 8192]): 4 spans took E4M3 linear from 35.1 to 34.2 us and
+// E2M1 swizzled from 28.4 to 28.0 us; 1 or 2 spans changed nothing measurable.
+constexpr int kPrefetchSpans = 4;
+
 // Minimum of one CTA per SM: the compiler may then use 55-79 registers (4 or 3 CTAs per SM
 // instead of 5 at 48), which measured 5-8% faster back to back (E2M1 swizzled x[8192,8192]
 // 29.6 -> 28.2 us, NVFP4 30.6 -> 28.2 us).
 template <int FMT, bool SWZ>
 __global__ void __launch_bounds__(kThreads, 1) mx_dequant_kernel(DequantArgs a) {
   pdl_launch_dependents();
+  {
+    // L2 prefetch (before pdl_wait: a hint, see prefetch_l2) of the codes of this warp's first
+    // kPrefetchSpans iterations, 32 blocks each: 2 KiB (E2M1) or 4 KiB (E4M3) per warp.
+    const int64_t nblk0 = a.M * (a.K >> 5);
+    const int64_t w0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31u);
+    const int64_t ws = (int64_t)gridDim.x * kThreads;
+    constexpr int kCodeBytes = FMT == kFmtE4M3 ? 32 : 16;
+    if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+      for (int d = 0; d < kPrefetchSpans; ++d) {
+        const int64_t s0 = w0 + d * ws;
+        if (s0 < nblk0) {
+          const int64_t n = nblk0 - s0 < 32 ? nblk0 - s0 : 32;
+          prefetch_l2(static_cast<const uint8_t*>(a.codes) + s0 * kCodeBytes,
+                      (uint32_t)(n * kCodeBytes));
+        }
+      }
+    }
+  }
   pdl_wait();
   const uint8_t* codes = static_cast<const uint8_t*>(a.codes);
   const int64_t cblk = a.K >> 5;
