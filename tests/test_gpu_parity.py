@@ -910,7 +910,17 @@ def test_dependent_calls_keep_stream_order():
     cn, sn = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED)
     small = torch.empty((8, K), dtype=torch.bfloat16, device="cuda")
     cs, ss = mxq.mx_rotate_quantize(x[:8], H, mxq.E2M1, mxq.SWIZZLED)
-    outs = (a, b, d, c4, s4, c8, s8, cn, sn, small, cs, ss)
+    # grouped calls: 8 experts of uneven sizes; the offsets are rewritten by a torch kernel in
+    # the chain itself, so a grouped call's offset loads also depend on the launch before it
+    counts = [700, 0, 1, 129, 2000, 300, 5, 961]
+    off_src = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int64,
+                           device="cuda")
+    offs = torch.zeros_like(off_src)
+    gse = torch.full((len(counts),), 448.0 * 6 / 8.0, device="cuda")
+    cg, sg = mxq.mx_quantize_grouped(x, off_src, mxq.E4M3, mxq.SWIZZLED)
+    cgl, sgl = mxq.mx_quantize_grouped(x, off_src, mxq.E4M3, mxq.LINEAR)
+    cng, sng = mxq.mx_quantize_nvfp4_grouped(x, off_src, gse, mxq.SWIZZLED)
+    outs = (a, b, d, c4, s4, c8, s8, cn, sn, small, cs, ss, offs, cg, sg, cgl, sgl, cng, sng)
 
     def chain(sync):
         steps = [
@@ -923,6 +933,12 @@ def test_dependent_calls_keep_stream_order():
             lambda: mxq.mx_dequantize(c8, s8, K, mxq.E4M3, mxq.LINEAR, y=b),
             lambda: mxq.mx_quantize_nvfp4(b, gs, mxq.SWIZZLED, codes=cn, scales=sn),
             lambda: mxq.mx_dequantize_nvfp4(cn, sn, K, gs, mxq.SWIZZLED, y=d),
+            lambda: offs.copy_(off_src),
+            lambda: mxq.mx_quantize_grouped(d, offs, mxq.E4M3, mxq.SWIZZLED, codes=cg, scales=sg),
+            lambda: mxq.mx_quantize_grouped(d, offs, mxq.E4M3, mxq.LINEAR, codes=cgl, scales=sgl),
+            lambda: mxq.mx_dequantize(cgl, sgl, K, mxq.E4M3, mxq.LINEAR, y=a),
+            lambda: mxq.mx_quantize_nvfp4_grouped(a, offs, gse, mxq.SWIZZLED, codes=cng,
+                                                  scales=sng),
             lambda: mxq.mx_qdq(d[:8], mxq.E2M1, H, y=small),
             lambda: mxq.mx_rotate_quantize(small, H, mxq.E2M1, mxq.SWIZZLED, codes=cs, scales=ss),
         ]
