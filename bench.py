@@ -754,8 +754,10 @@ def run_ours(args):
     K = args.steps
     # Every SAMPLE-th step brackets each of its two launches with CUDA events (the roofline's
     # per-launch durations); the other steps run with no event between kernels, since an event
-    # at a kernel boundary makes the stream drain there and would slow the whole-job figure.
-    sample = 10
+    # at a kernel boundary makes the stream drain there and would slow the whole-job figure
+    # (sampling every 10th step cost about 2.5% of it; every 100th leaves 200 sampled steps of
+    # the default 20000).
+    sample = max(1, min(100, K // 20))
     sampled = list(range(0, K, sample))
     ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(4)] for i in sampled}
     t_start = torch.cuda.Event(enable_timing=True)
