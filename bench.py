@@ -487,6 +487,29 @@ def extra_workloads(dev, peak):
     measure("moe_quant_nvfp4[16384,2048]x128", nb, x.numel(), make, nb)
     del x, c, s
 
+    # rotate+quantize with linear scales (the layout of mxfp8_quantize without swizzling)
+    x = to_gpu(W.rotate_quant_activation(8192, 28672), dev)
+    H32 = to_gpu(W.normalized_hadamard_bf16(32), dev)
+    for fmt, fname, cb in ((mxq.E2M1, "mxfp4", 0.5), (mxq.E4M3, "mxfp8", 1.0)):
+        c, s = mxq.mx_rotate_quantize(x, H32, fmt, mxq.LINEAR)
+
+        def make(k, x=x, c=c, s=s, fmt=fmt):
+            xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+            return lambda: mxq.mx_rotate_quantize(xk, H32, fmt, mxq.LINEAR, codes=ck, scales=sk)
+        nb = 2 * x.numel() + c.numel() + s.numel()
+        measure(f"rotate_quant_{fname}_g32_linear[8192,28672]", nb, x.numel(), make, nb, iters=15)
+        del c, s
+    H16 = to_gpu(W.normalized_hadamard_bf16(16), dev)
+    gsx = (448.0 * 6.0 / x.float().abs().max()).reshape(1).float().contiguous()
+    c, s = mxq.mx_quantize_nvfp4(x, gsx, mxq.LINEAR, H16)
+
+    def make(k, x=x, c=c, s=s):
+        xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+        return lambda: mxq.mx_quantize_nvfp4(xk, gsx, mxq.LINEAR, H16, codes=ck, scales=sk)
+    nb = 2 * x.numel() + c.numel() + s.numel()
+    measure("nvfp4_rotate_quant_g16_linear[8192,28672]", nb, x.numel(), make, nb, iters=15)
+    del x, c, s
+
     # rotation sweep: rotated QDQ, g in {16,32,64,128} x {MXFP4, MXFP8} on 3 layer inputs
     for lname, M, K in W.ROTATION_SWEEP_LAYERS:
         x = to_gpu(W.rotation_sweep_input(lname), dev)

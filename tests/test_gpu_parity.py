@@ -614,6 +614,30 @@ def test_identity_rotation_is_bit_exact(g):
         np.testing.assert_array_equal(T.bf16_bits(mxq.mx_qdq(x, fmt, H)), O.qdq(xb, fmt))
 
 
+@pytest.mark.parametrize("K,g", [(96, 16), (96, 32), (160, 32), (192, 64), (416, 32)])
+def test_identity_rotation_partial_column_tile(K, g):
+    """K % 128 != 0 on the tensor-core kernel (M > 16): the last 128-column tile is partial, so
+    its staged scales cover fewer than 4 (MX) / 8 (NVFP4) columns and the linear scale rows
+    are not 4-byte aligned. With H = I the results equal the plain path bit for bit, both
+    layouts, MX and NVFP4."""
+    H = T.to_gpu(rotation(g, "identity"))
+    for M in (129, 200):
+        xb = W.mxfp8_linear_quant(M, K, stream=K + g)
+        x = T.to_gpu(xb)
+        for fmt in FMTS:
+            for layout in LAYOUTS:
+                c, s = mxq.mx_rotate_quantize(x, H, fmt, layout)
+                rc, rs = O.quantize(xb, fmt, layout)
+                np.testing.assert_array_equal(T.u8(s), rs)
+                np.testing.assert_array_equal(T.u8(c), rc)
+        gs = gs_of(xb)
+        for layout in LAYOUTS:
+            c, s = nv_quantize(xb, gs, layout, rotation(g, "identity"))
+            rc, rs = O.nvfp4_quantize(xb, gs, layout)
+            np.testing.assert_array_equal(s, rs)
+            np.testing.assert_array_equal(c, rc)
+
+
 @pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("M,K", [(1, 8192), (16, 8192), (128, 1024), (300, 1024), (16, 28672)])
