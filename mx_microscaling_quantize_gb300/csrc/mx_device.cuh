@@ -285,25 +285,58 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint32_t pair, float& lo, float& h
       : "r"(pair));
 }
 
-// amax0/amax1: sign-free fp32 bits of the two blocks' abs-max (Inf/NaN at or above 0x7F800000)
-__device__ __forceinline__ NvScales nv_scales(uint32_t amax0, uint32_t amax1, float gs, float r6) {
-  NvScales n;
+// amax0/amax1: sign-free fp32 bits of the two blocks' abs-max (Inf/NaN at or above 0x7F800000).
+// Returns the two E4M3 scale bytes (first in the low byte; 0x7F for a block holding a NaN or an
+// infinity) and sets the blocks' special flags.
+__device__ __forceinline__ uint32_t nv_scale_pair(uint32_t amax0, uint32_t amax1, float r6,
+                                                  bool* special) {
   const float s0 = __fmul_rn(__uint_as_float(amax0), r6);
   const float s1 = __fmul_rn(__uint_as_float(amax1), r6);
   uint32_t pair;
   asm("{\n\t.reg .b16 c;\n\tcvt.rn.satfinite.e4m3x2.f32 c, %1, %2;\n\tcvt.u32.u16 %0, c;\n\t}"
       : "=r"(pair)
       : "f"(s1), "f"(s0));
-  n.special[0] = amax0 >= 0x7F800000u;
-  n.special[1] = amax1 >= 0x7F800000u;
-  if (n.special[0]) pair = (pair & 0xFF00u) | 0x007Fu;
-  if (n.special[1]) pair = (pair & 0x00FFu) | 0x7F00u;
+  special[0] = amax0 >= 0x7F800000u;
+  special[1] = amax1 >= 0x7F800000u;
+  if (special[0]) pair = (pair & 0xFF00u) | 0x007Fu;
+  if (special[1]) pair = (pair & 0x00FFu) | 0x7F00u;
+  return pair;
+}
+
+__device__ __forceinline__ NvScales nv_scales(uint32_t amax0, uint32_t amax1, float gs, float r6) {
+  NvScales n;
+  const uint32_t pair = nv_scale_pair(amax0, amax1, r6, n.special);
   float d0, d1;
   e4m3x2_to_f32(pair, d0, d1);
   n.enc[0] = d0 == 0.0f ? 0.0f : __fdiv_rn(gs, d0);
   n.enc[1] = d1 == 0.0f ? 0.0f : __fdiv_rn(gs, d1);
   n.dq[0] = d0 == 0.0f ? 0.0f : __fdiv_rn(d0, gs);
   n.dq[1] = d1 == 0.0f ? 0.0f : __fdiv_rn(d1, gs);
+  n.bytes = pair;
+  return n;
+}
+
+// The per-scale-byte factors of one global scale, for b in [0, 128): enc = gs / decode(b) and
+// dq = decode(b) / gs (0 where decode(b) is 0), the same fp32 divisions nv_scales performs, so
+// that a kernel can tabulate them once and look them up (nv_scales_tab) with identical results.
+__device__ __forceinline__ void nv_factors_of_byte(uint32_t b, float gs, float& enc, float& dq) {
+  float d, unused;
+  e4m3x2_to_f32(b, d, unused);
+  enc = d == 0.0f ? 0.0f : __fdiv_rn(gs, d);
+  dq = d == 0.0f ? 0.0f : __fdiv_rn(d, gs);
+}
+
+// nv_scales with the factors looked up in tables t_enc / t_dq built by nv_factors_of_byte
+// (indexed by the byte's low 7 bits; a special block's 0x7F reads the NaN entry, and its outputs
+// are replaced by the caller anyway).
+__device__ __forceinline__ NvScales nv_scales_tab(uint32_t amax0, uint32_t amax1, float r6,
+                                                  const float* t_enc, const float* t_dq) {
+  NvScales n;
+  const uint32_t pair = nv_scale_pair(amax0, amax1, r6, n.special);
+  n.enc[0] = t_enc[pair & 0x7Fu];
+  n.enc[1] = t_enc[(pair >> 8) & 0x7Fu];
+  n.dq[0] = t_dq[pair & 0x7Fu];
+  n.dq[1] = t_dq[(pair >> 8) & 0x7Fu];
   n.bytes = pair;
   return n;
 }
