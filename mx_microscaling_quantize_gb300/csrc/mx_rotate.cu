@@ -15,8 +15,12 @@
 //   warps 2..17  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
 //                32*(w%4) .. +31, i.e. tile rows; the four warps of a quarter take one
 //                32-column block each), abs-max, E8M0 scale, conversion, stores; then they
-//                free the accumulator for the MMA four tiles on.
-// Loads, MMAs and the epilogue of different tiles overlap. Operands: A (the x tile) in the
+//                free the accumulator for the MMA four tiles on. Outputs and scales (both
+//                layouts) are staged per tile in shared memory and written back with TMA /
+//                bulk stores (linear scales: one store per tile row); NVFP4 factors come from
+//                per-CTA tables of all 128 scale bytes.
+// Loads, MMAs and the epilogue of different tiles overlap; each CTA prefetches its first two
+// tiles into L2 before waiting for the kernel before it on the stream. Operands: A (the x tile) in the
 // K-major 128-byte-swizzled layout the TMA writes (8-row groups 1024 bytes apart); B = H^T in
 // the K-major no-swizzle core-matrix layout, written once per CTA:
 //   element (n, k) = H[k][n] at (k / 8) * (g * 16) + n * 16 + (k % 8) * 2.
