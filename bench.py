@@ -221,6 +221,24 @@ def time_oracle_for(xw, xa, min_seconds):
     return nbytes / dt / 1e9, dt, passes, threads
 
 
+def time_oracle_one_core(xw, min_seconds, rows=256):
+    """Oracle QDQ of the weight's first `rows` rows on one host core (one oracle call per pass,
+    no thread pool), repeated until min_seconds elapsed (at least once); returns (GB/s over
+    algorithmic bytes, seconds, passes, rows)."""
+    import oracle as O
+    O.build()
+    sample = np.ascontiguousarray(xw[:rows])
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        O.qdq(sample, O.E2M1)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    return 4 * sample.size * passes / dt / 1e9, dt, passes, rows
+
+
 # ---------------------------------------------------------------------------------------------
 # reference arm: the CPU oracle
 # ---------------------------------------------------------------------------------------------
@@ -845,6 +863,11 @@ def run_ours(args):
             "sample": f"{passes} passes of the whole workload (E2M1 QDQ of x[8192,8192] and "
                       f"x[4096,8192]) in {cpu_s:.1f} s, row chunks on {threads} threads",
             "gelem_per_s": cpu_gbs / 4}
+        one_gbs, one_s, one_passes, one_rows = time_oracle_one_core(xw_b, 2.0)
+        line["cpu_baseline"]["single_core"] = {
+            "value": one_gbs, "unit": "GB/s", "cores": 1,
+            "sample": f"{one_passes} passes of the weight's first {one_rows} rows "
+                      f"(E2M1 QDQ of x[{one_rows},8192]) in {one_s:.1f} s on one thread"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
