@@ -64,6 +64,9 @@ def _load():
         "mxo_rotate": (None, [p, i64, i64, p, i32, p]),
         "mxo_rotate_quantize": (None, [p, i64, i64, p, i32, i32, i32, p, p]),
         "mxo_rotate_qdq": (None, [p, i64, i64, p, i32, i32, p]),
+        "mxo_quantize_values": (None, [p, i64, i64, i32, i32, p, p]),
+        "mxo_qdq_values": (None, [p, i64, i64, i32, p]),
+        "mxo_nvfp4_values": (None, [p, i64, i64, ctypes.c_float, i32, p, p, p]),
         "mxo_quantize_grouped": (None, [p, p, i32, i64, i32, i32, i64, p, p]),
         "mxo_nvfp4_scales_shape": (None, [i64, i64, i32, p, p]),
         "mxo_nvfp4_block": (i32, [p, i32, ctypes.c_float, p]),
@@ -218,6 +221,32 @@ def rotate_qdq(x_bits, H_bits, fmt: int) -> np.ndarray:
     return out
 
 
+def _values(v) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    assert v.ndim == 2
+    return v
+
+
+def quantize_values(v, fmt: int, layout: int):
+    """Quantize float64 values [M, K] (rotated values from ``rotate``, for instance): the same
+    steps as ``quantize`` after its bf16 decode. -> (codes, scales)."""
+    v = _values(v)
+    M, K = v.shape
+    codes = np.zeros((M, code_bytes_per_row(fmt, K)), dtype=np.uint8)
+    scales = np.zeros(scales_shape(M, K, layout), dtype=np.uint8)
+    _load().mxo_quantize_values(_ptr(v), M, K, fmt, layout, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def qdq_values(v, fmt: int) -> np.ndarray:
+    """QDQ of float64 values [M, K] -> bf16 bits [M, K] (``qdq`` after its bf16 decode)."""
+    v = _values(v)
+    M, K = v.shape
+    out = np.zeros((M, K), dtype=np.uint16)
+    _load().mxo_qdq_values(_ptr(v), M, K, fmt, _ptr(out))
+    return out
+
+
 def quantize_grouped(x_bits, offsets, fmt: int, layout: int, scale_rows: int | None = None):
     """Per-expert quantize. offsets: int64 [E+1] row offsets (host)."""
     x = _bits(x_bits)
@@ -279,6 +308,21 @@ def nvfp4_qdq(x_bits, gs: float, H_bits=None) -> np.ndarray:
     _load().mxo_nvfp4_qdq(_ptr(x), M, K, None if H is None else _ptr(H),
                           0 if H is None else H.shape[0], float(np.float32(gs)), _ptr(out))
     return out
+
+
+def nvfp4_values(v, gs: float, layout: int, codes=True, scales=True, qdq=True):
+    """NVFP4 of float64 values [M, K] (rotated values from ``rotate``, for instance), each
+    rounded to fp32 once first: -> (codes [M, K/2], scales, QDQ bf16 bits [M, K]), None for an
+    output not asked for."""
+    v = _values(v)
+    M, K = v.shape
+    c = np.zeros((M, K // 2), dtype=np.uint8) if codes else None
+    s = np.zeros(nvfp4_scales_shape(M, K, layout), dtype=np.uint8) if scales else None
+    q = np.zeros((M, K), dtype=np.uint16) if qdq else None
+    _load().mxo_nvfp4_values(_ptr(v), M, K, float(np.float32(gs)), layout,
+                             None if c is None else _ptr(c), None if s is None else _ptr(s),
+                             None if q is None else _ptr(q))
+    return c, s, q
 
 
 def nvfp4_dequantize(codes, scales, K: int, gs: float, layout: int) -> np.ndarray:

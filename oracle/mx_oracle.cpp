@@ -289,16 +289,19 @@ std::vector<double> decode_rows(const uint16_t* x, int64_t rows, int64_t K) {
 }
 
 // y = x_chunk * H for every g-element chunk along K; H is g x g row-major (H[i*g + j]).
+// Every output y_j = sum over i = 0 .. g-1 of x_i * H[i][j], added in increasing i starting
+// from 0: the loop takes input i in turn and adds x_i times row i of H to the whole chunk.
 std::vector<double> rotate_rows(const uint16_t* x, int64_t rows, int64_t K, const uint16_t* H, int g) {
   std::vector<double> h((size_t)g * g);
   for (int i = 0; i < g * g; ++i) h[(size_t)i] = bf16_to_double(H[i]);
-  std::vector<double> y((size_t)(rows * K));
+  std::vector<double> y((size_t)(rows * K), 0.0);
   for (int64_t r = 0; r < rows; ++r) {
     for (int64_t c0 = 0; c0 < K; c0 += g) {
-      for (int j = 0; j < g; ++j) {
-        double acc = 0.0;
-        for (int i = 0; i < g; ++i) acc += bf16_to_double(x[r * K + c0 + i]) * h[(size_t)i * g + j];
-        y[(size_t)(r * K + c0 + j)] = acc;
+      double* yc = y.data() + r * K + c0;
+      for (int i = 0; i < g; ++i) {
+        const double xi = bf16_to_double(x[r * K + c0 + i]);
+        const double* hrow = h.data() + (size_t)i * g;
+        for (int j = 0; j < g; ++j) yc[j] += xi * hrow[j];
       }
     }
   }
@@ -480,6 +483,20 @@ void mxo_rotate_qdq(const uint16_t* x, int64_t M, int64_t K, const uint16_t* H, 
   qdq_rows(*format_of(fmt), y.data(), M, K, out);
 }
 
+// Quantize / QDQ of values given as doubles, [M, K] row-major (the rotated values mxo_rotate
+// returns, for instance): the same steps as mxo_quantize / mxo_qdq after the bf16 decode.
+void mxo_quantize_values(const double* v, int64_t M, int64_t K, int fmt, int layout, uint8_t* codes,
+                         uint8_t* scales) {
+  int64_t srows, scols;
+  mxo_scales_shape(M, K, layout, &srows, &scols);
+  std::memset(scales, 0, (size_t)(srows * scols));
+  quantize_rows(*format_of(fmt), v, M, K, 0, layout, scols, codes, scales);
+}
+
+void mxo_qdq_values(const double* v, int64_t M, int64_t K, int fmt, uint16_t* out) {
+  qdq_rows(*format_of(fmt), v, M, K, out);
+}
+
 // Grouped (MoE) quantize: rows [offsets[e], offsets[e+1]) belong to expert e. Codes stay
 // contiguous. Linear scales are [M_total, K/32]. Swizzled scales give every expert its own
 // run of 128-row blocks: expert e starts at padded row P_e = sum_{e'<e} ceil(n_e'/128)*128.
@@ -537,6 +554,20 @@ void mxo_nvfp4_qdq(const uint16_t* x, int64_t M, int64_t K, const uint16_t* H, i
                    uint16_t* out) {
   std::vector<float> v = H ? doubles_to_float(rotate_rows(x, M, K, H, g)) : bf16_rows_to_float(x, M * K);
   nvfp4_rows(v.data(), M, K, gs, 0, 0, nullptr, nullptr, out);
+}
+
+// NVFP4 of values given as doubles [M, K] (rotated values, for instance), each rounded to fp32
+// once first; any of codes, scales, qdq may be null. Scales as mxo_nvfp4_quantize lays them out
+// (pads zeroed here).
+void mxo_nvfp4_values(const double* y, int64_t M, int64_t K, float gs, int layout, uint8_t* codes,
+                      uint8_t* scales, uint16_t* qdq) {
+  int64_t srows, scols;
+  mxo_nvfp4_scales_shape(M, K, layout, &srows, &scols);
+  if (scales) std::memset(scales, 0, (size_t)(srows * scols));
+  if (codes) std::memset(codes, 0, (size_t)(M * (K / 2)));
+  std::vector<float> v((size_t)(M * K));
+  for (int64_t i = 0; i < M * K; ++i) v[(size_t)i] = (float)y[i];
+  nvfp4_rows(v.data(), M, K, gs, layout, scols, codes, scales, qdq);
 }
 
 // Grouped (MoE) NVFP4 quantize: rows [offsets[e], offsets[e+1]) are expert e's input, quantized
