@@ -13,6 +13,9 @@ re-quantized by the oracle under the GPU's scale and held to the same element ru
 
 from __future__ import annotations
 
+import concurrent.futures
+import os
+
 import numpy as np
 import torch
 
@@ -110,6 +113,53 @@ def converter_sweep(K: int = 2048) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------------------------
+# whole outputs on all host cores: the oracle over row chunks in a thread pool (its ctypes calls
+# and numpy's array operations run without the interpreter lock)
+# ---------------------------------------------------------------------------------------------
+THREADS = os.cpu_count() or 1
+
+
+def rows_per_job(M: int, K: int, target_elems: int = 1 << 21) -> int:
+    """Rows of one job: about target_elems elements, at least enough jobs for every thread."""
+    by_size = max(1, target_elems // max(K, 1))
+    by_threads = max(1, -(-M // (2 * THREADS)))
+    return max(1, min(by_size, by_threads))
+
+
+def map_row_chunks(fn, M: int, K: int, target_elems: int = 1 << 21) -> list:
+    """fn(r0, r1) over consecutive row ranges covering [0, M); results in row order. An
+    exception in any job is raised here."""
+    step = rows_per_job(M, K, target_elems)
+    ranges = [(r0, min(M, r0 + step)) for r0 in range(0, M, step)]
+    if len(ranges) == 1:
+        return [fn(*ranges[0])]
+    with concurrent.futures.ThreadPoolExecutor(THREADS) as pool:
+        return list(pool.map(lambda rr: fn(*rr), ranges))
+
+
+def assert_rows_equal(got: np.ndarray, ref_fn, what: str = "output"):
+    """got [M, ...] equals ref_fn(r0, r1) on every row range, element for element."""
+    M = got.shape[0]
+    width = int(np.prod(got.shape[1:])) if got.ndim > 1 else 1
+
+    def job(r0, r1):
+        ref = ref_fn(r0, r1)
+        g = got[r0:r1]
+        if not np.array_equal(g, ref.reshape(g.shape)):
+            bad = np.argwhere(g != ref.reshape(g.shape))
+            i = tuple(int(v) for v in bad[0])
+            raise AssertionError(f"{what}: {len(bad)} elements differ from the oracle in rows "
+                                 f"[{r0}, {r1}); first at {(i[0] + r0,) + i[1:]}: "
+                                 f"got {g[i]} want {ref.reshape(g.shape)[i]}")
+    map_row_chunks(job, M, width)
+
+
+def oracle_qdq_rows(x_bits, fmt):
+    """ref_fn for assert_rows_equal: the oracle's QDQ of rows [r0, r1) of x."""
+    return lambda r0, r1: O.qdq(x_bits[r0:r1], fmt)
+
+
+# ---------------------------------------------------------------------------------------------
 # rotated-path tolerance rules
 # ---------------------------------------------------------------------------------------------
 def _grid(fmt):
@@ -117,6 +167,26 @@ def _grid(fmt):
     vals = np.array([O.decode(fmt, c) if not (fmt == O.E4M3 and (c & 0x7F) == 0x7F) else np.nan
                      for c in range(n)])
     return vals
+
+
+_GRIDS = {}
+_DQ_TABLES = {}
+
+
+def grid_values(fmt) -> np.ndarray:
+    if fmt not in _GRIDS:
+        _GRIDS[fmt] = _grid(fmt)
+    return _GRIDS[fmt]
+
+
+def dequant_table(fmt, byte) -> np.ndarray:
+    """bf16 bits of every code of the format dequantized under scale byte `byte` (oracle)."""
+    key = (fmt, byte)
+    if key not in _DQ_TABLES:
+        n = 16 if fmt == O.E2M1 else 256
+        _DQ_TABLES[key] = np.array([O.dequant_bf16(fmt, c, byte) for c in range(n)],
+                                   dtype=np.uint16)
+    return _DQ_TABLES[key]
 
 
 def _neighbours(fmt, vals, a, b) -> bool:
@@ -145,13 +215,20 @@ def check_rotated_values(y_gpu: np.ndarray, y_ref: np.ndarray, g: int) -> float:
 
 
 def _allowed_bytes(fmt, yb, tb, ref_byte):
-    amax = np.abs(yb).max()
+    """Scale bytes the GPU may give a block: the oracle's, and one step off only where the
+    oracle's abs-max lies within the block's tolerance of the power of two that the step
+    crosses. amax in [2^k, 2^(k+1)) gives the oracle byte of exponent k; a GPU value within tol
+    of it may fall below 2^k (one byte lower, only if amax is that close to 2^k) or reach
+    2^(k+1) (one byte higher, only if amax is that close to 2^(k+1))."""
+    amax = float(np.abs(yb).max())
     allowed = {ref_byte}
     if amax > 0:
         k = np.floor(np.log2(amax))
-        for p in (2.0 ** k, 2.0 ** (k + 1)):
-            if abs(amax - p) <= tb.max():
-                allowed |= {ref_byte - 1, ref_byte + 1}
+        tmax = float(tb.max())
+        if amax - 2.0 ** k <= tmax:
+            allowed.add(ref_byte - 1)
+        if 2.0 ** (k + 1) - amax <= tmax:
+            allowed.add(ref_byte + 1)
     return allowed
 
 
@@ -172,69 +249,105 @@ def _block_ok(fmt, vals, yb, tb, gpu_codes, gpu_byte, ref_byte) -> tuple[bool, i
     return True, len(diff)
 
 
-def check_rotated_codes(x_bits, H_bits, fmt, codes_gpu, scales_gpu_linear):
-    """Apply the rules to GPU codes/scales (linear layout). Returns a dict of counts; raises
-    AssertionError with the first offending block."""
-    y = O.rotate(x_bits, H_bits)
-    g = H_bits.shape[0]
-    tol = rotation_tolerance(y, g)
-    M, K = y.shape
-    rc, rs = O.rotate_quantize(x_bits, H_bits, fmt, O.LINEAR)
-    gc = unpack_codes(codes_gpu, fmt)
+def _codes_chunk(fmt, vals, y, tol, gc_packed, sg, r0):
+    """Rules on one row chunk: y/tol the oracle's rotated values and tolerances, gc_packed and
+    sg the GPU's codes and linear scales of the same rows."""
+    n, K = y.shape
+    rc, rs = O.quantize_values(y, fmt, O.LINEAR)
+    gc = unpack_codes(gc_packed, fmt)
     rce = unpack_codes(rc, fmt)
-    vals = _grid(fmt)
-    bad_blocks = np.nonzero((rs != scales_gpu_linear) |
-                            (gc != rce).reshape(M, K // 32, 32).any(axis=2))
-    exempt_codes = 0
-    flips = 0
-    for r, j in zip(*bad_blocks):
-        sl = slice(32 * j, 32 * j + 32)
-        ok, n = _block_ok(fmt, vals, y[r, sl], tol[r, sl], gc[r, sl], int(scales_gpu_linear[r, j]),
-                          int(rs[r, j]))
-        assert ok, (f"block (row {r}, block {j}) outside tolerance: gpu byte "
-                    f"{scales_gpu_linear[r, j]} ref byte {rs[r, j]}")
-        exempt_codes += n
-        flips += int(scales_gpu_linear[r, j] != rs[r, j])
-    return {"blocks": M * K // 32, "exempt_blocks": len(bad_blocks[0]), "exempt_codes": exempt_codes,
-            "scale_flips": flips}
-
-
-def check_rotated_qdq(x_bits, H_bits, fmt, out_gpu_bits):
-    """Rules for rotated QDQ: blocks that differ from the oracle must equal the dequantization of
-    codes allowed by the rules under an allowed scale."""
-    y = O.rotate(x_bits, H_bits)
-    g = H_bits.shape[0]
-    tol = rotation_tolerance(y, g)
-    M, K = y.shape
-    ref = O.rotate_qdq(x_bits, H_bits, fmt)
-    _, rs = O.rotate_quantize(x_bits, H_bits, fmt, O.LINEAR)
-    vals = _grid(fmt)
-    bad = np.nonzero((ref != out_gpu_bits).reshape(M, K // 32, 32).any(axis=2))
-    exempt = 0
+    bad = np.nonzero((rs != sg) | (gc != rce).reshape(n, K // 32, 32).any(axis=2))
+    exempt_codes = flips = 0
     for r, j in zip(*bad):
         sl = slice(32 * j, 32 * j + 32)
-        yb, tb, ob = y[r, sl], tol[r, sl], out_gpu_bits[r, sl]
+        ok, k = _block_ok(fmt, vals, y[r, sl], tol[r, sl], gc[r, sl], int(sg[r, j]), int(rs[r, j]))
+        assert ok, (f"block (row {r0 + r}, block {j}) outside tolerance: gpu byte "
+                    f"{sg[r, j]} ref byte {rs[r, j]}")
+        exempt_codes += k
+        flips += int(sg[r, j] != rs[r, j])
+    return np.array([n * K // 32, len(bad[0]), exempt_codes, flips])
+
+
+def _qdq_chunk(fmt, vals, y, tol, og, r0):
+    """Rules for rotated QDQ on one row chunk: blocks that differ from the oracle must equal
+    the dequantization of codes allowed by the rules under an allowed scale."""
+    n, K = y.shape
+    ref = O.qdq_values(y, fmt)
+    bad = np.nonzero((ref != og).reshape(n, K // 32, 32).any(axis=2))
+    for r, j in zip(*bad):
+        sl = slice(32 * j, 32 * j + 32)
+        yb, tb, ob = y[r, sl], tol[r, sl], og[r, sl]
+        ref_byte, _ = O.quantize_block(fmt, yb)
         ok = False
-        for b in sorted(_allowed_bytes(fmt, yb, tb, int(rs[r, j]))):
+        for b in sorted(_allowed_bytes(fmt, yb, tb, ref_byte)):
             # the GPU codes implied by its outputs under scale b
             _, rc = O.quantize_block(fmt, yb, forced_byte=b)
+            table = dequant_table(fmt, b)
             codes = rc.copy()
             good = True
-            for i in range(32):
-                if O.dequant_bf16(fmt, int(rc[i]), b) == ob[i]:
-                    continue
-                cands = [c for c in range(len(vals)) if not np.isnan(vals[c])
-                         and O.dequant_bf16(fmt, c, b) == ob[i]]
+            for i in np.nonzero(table[rc] != ob)[0]:
+                cands = [c for c in np.nonzero(table == ob[i])[0] if not np.isnan(vals[c])]
                 if not cands:
                     good = False
                     break
                 codes[i] = cands[0]
-            if good and _block_ok(fmt, vals, yb, tb, codes, b, int(rs[r, j]))[0]:
+            if good and _block_ok(fmt, vals, yb, tb, codes, b, ref_byte)[0]:
                 ok = True
                 break
-        assert ok, f"rotated QDQ block (row {r}, block {j}) outside tolerance"
-        exempt += 1
-    return {"blocks": M * K // 32, "exempt_blocks": exempt}
+        assert ok, f"rotated QDQ block (row {r0 + r}, block {j}) outside tolerance"
+    return np.array([n * K // 32, len(bad[0])])
+
+
+def check_rotated_codes(x_bits, H_bits, fmt, codes_gpu, scales_gpu_linear):
+    """Apply the rules to GPU codes/scales (linear layout) over every row (the oracle on row
+    chunks, all host cores). Returns a dict of counts; raises AssertionError with the first
+    offending block."""
+    return check_rotated_multi(x_bits, H_bits, codes={fmt: (codes_gpu, scales_gpu_linear)})[fmt]
+
+
+def check_rotated_qdq(x_bits, H_bits, fmt, out_gpu_bits):
+    return check_rotated_multi(x_bits, H_bits, qdq={fmt: out_gpu_bits})[("qdq", fmt)]
+
+
+def check_rotated_multi(x_bits, H_bits, codes=None, qdq=None, nvfp4=None, nvfp4_qdq=None):
+    """Every rule check of one input and one rotation at once, each row chunk rotated once by
+    the oracle: codes {fmt: (codes, linear scales)}, qdq {fmt: bf16 bits}, nvfp4 {gs: (codes,
+    linear scales)}, nvfp4_qdq {gs: bf16 bits}. Returns {fmt: codes stats, ("qdq", fmt): ...,
+    ("nvfp4", gs): ..., ("nvfp4_qdq", gs): ...}."""
+    codes, qdq = codes or {}, qdq or {}
+    nvfp4, nvfp4_qdq = nvfp4 or {}, nvfp4_qdq or {}
+    x = np.ascontiguousarray(x_bits)
+    M, K = x.shape
+    g = H_bits.shape[0]
+    for fmt in set(codes) | set(qdq):
+        grid_values(fmt)
+
+    def job(r0, r1):
+        y = O.rotate(x[r0:r1], H_bits)
+        tol = rotation_tolerance(y, g)
+        out = {}
+        for fmt, (c, s) in codes.items():
+            out[fmt] = _codes_chunk(fmt, grid_values(fmt), y, tol, c[r0:r1], s[r0:r1], r0)
+        for fmt, o in qdq.items():
+            out[("qdq", fmt)] = _qdq_chunk(fmt, grid_values(fmt), y, tol, o[r0:r1], r0)
+        for gs, (c, s) in nvfp4.items():
+            out[("nvfp4", gs)] = _nvfp4_codes_chunk(y, tol, gs, c[r0:r1], s[r0:r1], r0)
+        for gs, o in nvfp4_qdq.items():
+            out[("nvfp4_qdq", gs)] = _nvfp4_qdq_chunk(y, tol, gs, o[r0:r1], r0)
+        return out
+
+    parts = map_row_chunks(job, M, K, target_elems=1 << 20)
+    total = {k: sum(p[k] for p in parts) for k in parts[0]}
+    stats = {}
+    for k, v in total.items():
+        if k in codes:
+            stats[k] = {"blocks": int(v[0]), "exempt_blocks": int(v[1]),
+                        "exempt_codes": int(v[2]), "scale_flips": int(v[3])}
+        elif k[0] == "nvfp4":
+            stats[k] = {"blocks": int(v[0]), "exempt_blocks": int(v[1]), "scale_flips": int(v[2])}
+        else:
+            stats[k] = {"blocks": int(v[0]), "exempt_blocks": int(v[1])}
+    return stats
 
 
 # ---------------------------------------------------------------------------------------------
@@ -279,34 +392,28 @@ def _nvfp4_block_ok(yb, tb, gs, gpu_codes, gpu_byte, ref_byte) -> tuple[bool, in
     return True, len(diff)
 
 
-def check_rotated_nvfp4(x_bits, H_bits, gs, codes_gpu, scales_gpu_linear):
-    y = O.rotate(x_bits, H_bits)
-    tol = rotation_tolerance(y, H_bits.shape[0])
-    M, K = y.shape
-    rc, rs = O.nvfp4_quantize(x_bits, gs, O.LINEAR, H_bits=H_bits)
-    gc, rce = unpack_codes(codes_gpu, O.E2M1), unpack_codes(rc, O.E2M1)
-    bad = np.nonzero((rs != scales_gpu_linear) | (gc != rce).reshape(M, K // 16, 16).any(axis=2))
+def _nvfp4_codes_chunk(y, tol, gs, gc_packed, sg, r0):
+    n, K = y.shape
+    rc, rs, _ = O.nvfp4_values(y, gs, O.LINEAR, qdq=False)
+    gc, rce = unpack_codes(gc_packed, O.E2M1), unpack_codes(rc, O.E2M1)
+    bad = np.nonzero((rs != sg) | (gc != rce).reshape(n, K // 16, 16).any(axis=2))
     flips = 0
     for r, j in zip(*bad):
         sl = slice(16 * j, 16 * j + 16)
-        ok, _ = _nvfp4_block_ok(y[r, sl], tol[r, sl], gs, gc[r, sl], int(scales_gpu_linear[r, j]),
-                                int(rs[r, j]))
-        assert ok, (f"NVFP4 block (row {r}, block {j}) outside tolerance: gpu scale "
-                    f"{scales_gpu_linear[r, j]:#x} ref {rs[r, j]:#x}")
-        flips += int(scales_gpu_linear[r, j] != rs[r, j])
-    return {"blocks": M * K // 16, "exempt_blocks": len(bad[0]), "scale_flips": flips}
+        ok, _ = _nvfp4_block_ok(y[r, sl], tol[r, sl], gs, gc[r, sl], int(sg[r, j]), int(rs[r, j]))
+        assert ok, (f"NVFP4 block (row {r0 + r}, block {j}) outside tolerance: gpu scale "
+                    f"{sg[r, j]:#x} ref {rs[r, j]:#x}")
+        flips += int(sg[r, j] != rs[r, j])
+    return np.array([n * K // 16, len(bad[0]), flips])
 
 
-def check_rotated_nvfp4_qdq(x_bits, H_bits, gs, out_gpu_bits):
-    y = O.rotate(x_bits, H_bits)
-    tol = rotation_tolerance(y, H_bits.shape[0])
-    M, K = y.shape
-    ref = O.nvfp4_qdq(x_bits, gs, H_bits=H_bits)
-    _, rs = O.nvfp4_quantize(x_bits, gs, O.LINEAR, H_bits=H_bits)
-    bad = np.nonzero((ref != out_gpu_bits).reshape(M, K // 16, 16).any(axis=2))
+def _nvfp4_qdq_chunk(y, tol, gs, og, r0):
+    n, K = y.shape
+    _, rs, ref = O.nvfp4_values(y, gs, O.LINEAR, codes=False)
+    bad = np.nonzero((ref != og).reshape(n, K // 16, 16).any(axis=2))
     for r, j in zip(*bad):
         sl = slice(16 * j, 16 * j + 16)
-        yb, tb, ob = y[r, sl], tol[r, sl], out_gpu_bits[r, sl]
+        yb, tb, ob = y[r, sl], tol[r, sl], og[r, sl]
         ok = False
         for b in sorted(nvfp4_scale_candidates(np.abs(yb).max(), tb.max(), gs) | {int(rs[r, j])}):
             table = {c: O.nvfp4_dequant_bf16(c, b, float(gs)) for c in range(16)}
@@ -323,5 +430,14 @@ def check_rotated_nvfp4_qdq(x_bits, H_bits, gs, out_gpu_bits):
                 if _nvfp4_block_ok(yb, tb, gs, np.array(codes), b, int(rs[r, j]))[0]:
                     ok = True
                     break
-        assert ok, f"rotated NVFP4 QDQ block (row {r}, block {j}) outside tolerance"
-    return {"blocks": M * K // 16, "exempt_blocks": len(bad[0])}
+        assert ok, f"rotated NVFP4 QDQ block (row {r0 + r}, block {j}) outside tolerance"
+    return np.array([n * K // 16, len(bad[0])])
+
+
+def check_rotated_nvfp4(x_bits, H_bits, gs, codes_gpu, scales_gpu_linear):
+    return check_rotated_multi(x_bits, H_bits,
+                               nvfp4={gs: (codes_gpu, scales_gpu_linear)})[("nvfp4", gs)]
+
+
+def check_rotated_nvfp4_qdq(x_bits, H_bits, gs, out_gpu_bits):
+    return check_rotated_multi(x_bits, H_bits, nvfp4_qdq={gs: out_gpu_bits})[("nvfp4_qdq", gs)]

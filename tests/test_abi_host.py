@@ -222,6 +222,18 @@ def test_selftest_bounded_wait_validation(L):
     assert L.mx_selftest_bounded_wait(100_000_001, None) == SHAPE
 
 
+def test_selftest_rotate_give_up_validation(L):
+    f = L.mx_selftest_rotate_give_up
+    assert f(P, 128, 256, P, 32, P, P, 0, None) == SHAPE            # limit out of range
+    assert f(P, 128, 256, P, 32, P, P, 100_000_001, None) == SHAPE
+    assert f(P, 16, 256, P, 32, P, P, 1000, None) == SHAPE          # the few-row kernel's call
+    assert f(P, 0, 256, P, 32, P, P, 1000, None) == SHAPE           # empty
+    assert f(P, 128, 96, P, 64, P, P, 1000, None) == SHAPE          # K % g
+    assert f(P, 128, 256, P, 48, P, P, 1000, None) == UNSUP         # g
+    assert f(None, 128, 256, P, 32, P, P, 1000, None) == NULL
+    assert f(P + 16, 128, 256, P, 32, P, P, 1000, None) == ALIGN    # x 32-byte aligned
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mxq, "_lib", None)
     monkeypatch.setattr(mxq, "LIB_PATH", str(tmp_path / "missing.so"))

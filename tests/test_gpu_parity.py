@@ -4,8 +4,11 @@ Bar: bit-exact codes, E8M0 bytes and bf16 QDQ outputs on the non-rotated paths; 
 paths follow the tolerance rules of mx_testlib (pre-quantization values within 1e-5 of the
 chunk norm, code differences only next to rounding midpoints, scale flips only next to powers
 of two). Inputs are the seeded synthetic workloads at sizes the oracle finishes in seconds
-(several tiles plus ragged tails), and the full workload sizes on sampled rows.
+(several tiles plus ragged tails), and every workload at its full size, whole outputs: the
+oracle runs over row chunks on all host cores (mx_testlib.map_row_chunks).
 """
+
+import functools
 
 import numpy as np
 import pytest
@@ -29,6 +32,22 @@ def built():
     __graft_entry__.build()
     yield
     assert mxq.mx_device_errors() == 0
+
+
+@functools.lru_cache(maxsize=2)
+def full_input(name, *args):
+    """A full-size workload input, drawn once for the tests that share it (bf16 bits, read
+    only)."""
+    x = getattr(W, name)(*args)
+    x.setflags(write=False)
+    return x
+
+
+def assert_quantize_rows(xb, fmt, codes, scales_linear):
+    """GPU codes and linear scales of x equal the oracle's over every row (row chunks)."""
+    T.assert_rows_equal(codes, lambda r0, r1: O.quantize(xb[r0:r1], fmt, O.LINEAR)[0], "codes")
+    T.assert_rows_equal(scales_linear, lambda r0, r1: O.quantize(xb[r0:r1], fmt, O.LINEAR)[1],
+                        "scales")
 
 
 def quantize(xb, fmt, layout):
@@ -111,17 +130,17 @@ def test_mxfp4_qdq_workload_small(fmt):
     np.testing.assert_array_equal(qdq(xa, fmt), O.qdq(xa, fmt))
 
 
+@pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("which", ["weight", "activation"])
-def test_mxfp4_qdq_workload_full_size_sampled_rows(which):
-    """The full tensors in the benchmark's launch: 40 sampled rows against the oracle, and
+def test_mxfp4_qdq_workload_full_size(which, fmt):
+    """The full tensors of the benchmark's step, x[8192, 8192] and x[4096, 8192]: every QDQ
+    output equals the oracle's (MXFP4, the workload's format, and MXFP8), and
     QDQ(QDQ(x)) == QDQ(x) over the whole output."""
-    xb = W.mxfp4_qdq_weight() if which == "weight" else W.mxfp4_qdq_activation()
+    xb = full_input("mxfp4_qdq_weight") if which == "weight" else full_input("mxfp4_qdq_activation")
     xg = T.to_gpu(xb)
-    y = mxq.mx_qdq(xg, mxq.E2M1)
-    rows = np.sort(np.random.default_rng(11).choice(xb.shape[0], 40, replace=False))
-    yb = T.bf16_bits(y[torch.from_numpy(rows).cuda()])
-    np.testing.assert_array_equal(yb, O.qdq(xb[rows], O.E2M1))
-    assert torch.equal(mxq.mx_qdq(y, mxq.E2M1).view(torch.int16), y.view(torch.int16))
+    y = mxq.mx_qdq(xg, fmt)
+    T.assert_rows_equal(T.bf16_bits(y), T.oracle_qdq_rows(xb, fmt), "QDQ")
+    assert torch.equal(mxq.mx_qdq(y, fmt).view(torch.int16), y.view(torch.int16))
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -220,16 +239,21 @@ def test_dequantize_edge_shapes_with_canaries(fmt, M, K):
 @pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("fmt", FMTS)
 def test_dequantize_of_quantize_is_qdq_full_size(fmt, layout):
-    """The MXFP4 QDQ weight workload x[8192, 8192]: dequantize(quantize(x)) equals the GPU QDQ
-    bit for bit over the whole tensor, and the oracle's QDQ on 32 sampled rows."""
-    xb = W.mxfp4_qdq_weight()
+    """The MXFP4 QDQ weight workload x[8192, 8192]: the codes and scales of the quantize call
+    (swizzle pads zero) and the bf16 output of dequantize(quantize(x)) equal the oracle's over
+    the whole tensor, and the latter equals the GPU QDQ bit for bit."""
+    xb = full_input("mxfp4_qdq_weight")
     x = T.to_gpu(xb)
+    M, K = xb.shape
     c, s = mxq.mx_quantize(x, fmt, layout)
-    y = mxq.mx_dequantize(c, s, x.shape[1], fmt, layout)
+    y = mxq.mx_dequantize(c, s, K, fmt, layout)
     assert torch.equal(y.view(torch.int16), mxq.mx_qdq(x, fmt).view(torch.int16))
-    rows = np.sort(np.random.default_rng(12).choice(xb.shape[0], 32, replace=False))
-    np.testing.assert_array_equal(T.bf16_bits(y[torch.from_numpy(rows).cuda()]),
-                                  O.qdq(xb[rows], fmt))
+    s = T.u8(s)
+    if layout == O.SWIZZLED:
+        assert not T.swizzle_pads(s, M, K).any()
+        s = T.unswizzle(s, M, K)
+    assert_quantize_rows(xb, fmt, T.u8(c), s)
+    T.assert_rows_equal(T.bf16_bits(y), T.oracle_qdq_rows(xb, fmt), "dequantize")
 
 
 # ---------------------------------------------------------------------------------------------
@@ -291,19 +315,21 @@ def test_nvfp4_every_scale_byte():
     assert set(np.unique(s)) >= set(range(0, 0x7F))
 
 
-def test_nvfp4_full_size_sampled_rows():
-    xb = W.mxfp4_qdq_weight()
+def test_nvfp4_full_size():
+    """NVFP4 quantize (swizzled scales, pads zero) and QDQ of the weight x[8192, 8192]: codes,
+    E4M3 scale bytes and bf16 outputs equal the oracle's over the whole tensor."""
+    xb = full_input("mxfp4_qdq_weight")
     gs = gs_of(xb)
     x = T.to_gpu(xb)
     c, s = mxq.mx_quantize_nvfp4(x, gs_tensor(gs), mxq.SWIZZLED)
     y = mxq.mx_qdq_nvfp4(x, gs_tensor(gs))
-    rows = np.sort(np.random.default_rng(13).choice(xb.shape[0], 24, replace=False))
-    rc, rs = O.nvfp4_quantize(xb[rows], gs, O.LINEAR)
     M, K = xb.shape
-    np.testing.assert_array_equal(T.unswizzle(T.u8(s), M, 2 * K)[rows], rs)
-    np.testing.assert_array_equal(T.u8(c)[rows], rc)
-    np.testing.assert_array_equal(T.bf16_bits(y[torch.from_numpy(rows).cuda()]),
-                                  O.nvfp4_qdq(xb[rows], gs))
+    s = T.u8(s)
+    assert not T.swizzle_pads(s, M, 2 * K).any()
+    ref = lambda r0, r1: O.nvfp4_quantize(xb[r0:r1], gs, O.LINEAR)
+    T.assert_rows_equal(T.unswizzle(s, M, 2 * K), lambda r0, r1: ref(r0, r1)[1], "NVFP4 scales")
+    T.assert_rows_equal(T.u8(c), lambda r0, r1: ref(r0, r1)[0], "NVFP4 codes")
+    T.assert_rows_equal(T.bf16_bits(y), lambda r0, r1: O.nvfp4_qdq(xb[r0:r1], gs), "NVFP4 QDQ")
 
 
 def nv_dequantize(codes, scales, K, gs, layout):
@@ -353,8 +379,8 @@ def test_nvfp4_dequantize_edge_shapes_with_canaries(M, K):
 def test_nvfp4_dequantize_of_quantize_is_qdq_full_size(layout):
     """x[8192, 8192] (the MXFP4 QDQ weight workload), plain and rotated (normalized Hadamard,
     g = 16): dequantize(quantize(x)) equals the GPU QDQ bit for bit over the whole tensor; the
-    plain one also equals the oracle's QDQ on 24 sampled rows."""
-    xb = W.mxfp4_qdq_weight()
+    plain one also equals the oracle's QDQ over the whole tensor."""
+    xb = full_input("mxfp4_qdq_weight")
     x = T.to_gpu(xb)
     gs = gs_of(xb)
     for H in (None, T.to_gpu(W.normalized_hadamard_bf16(16))):
@@ -363,9 +389,8 @@ def test_nvfp4_dequantize_of_quantize_is_qdq_full_size(layout):
         q = mxq.mx_qdq_nvfp4(x, gs_tensor(gs), H)
         assert torch.equal(y.view(torch.int16), q.view(torch.int16))
         if H is None:
-            rows = np.sort(np.random.default_rng(14).choice(xb.shape[0], 24, replace=False))
-            np.testing.assert_array_equal(T.bf16_bits(y[torch.from_numpy(rows).cuda()]),
-                                          O.nvfp4_qdq(xb[rows], gs))
+            T.assert_rows_equal(T.bf16_bits(y), lambda r0, r1: O.nvfp4_qdq(xb[r0:r1], gs),
+                                "NVFP4 dequantize")
 
 
 @pytest.mark.parametrize("g", [16, 32, 64, 128])
@@ -401,16 +426,20 @@ def test_nvfp4_rotated_hadamard_rules(g):
     assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
 
 
-def test_nvfp4_rotated_full_size_sampled_rows():
+def test_nvfp4_rotated_full_size():
+    """Rotate (normalized Hadamard, g = 16) + NVFP4 quantize, swizzled scales, and rotated NVFP4
+    QDQ of the largest activation x[8192, 28672]: every block under the NVFP4 rules."""
     M, K = 8192, 28672
-    xb = W.rotate_quant_activation(M, K)
+    xb = full_input("rotate_quant_activation", M, K)
     H = rotation(16)
     gs = np.float32(448 * 6 / 8.0)  # rotated N(0,1) values stay well below 8
     c, s = nv_quantize(xb, gs, O.SWIZZLED, H)
-    s = T.unswizzle(s, M, 2 * K)
-    rows = np.sort(np.random.default_rng(17).choice(M, 12, replace=False))
-    stats = T.check_rotated_nvfp4(xb[rows], H, gs, c[rows], s[rows])
-    assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+    assert not T.swizzle_pads(s, M, 2 * K).any()
+    q = nv_qdq(xb, gs, H)
+    st = T.check_rotated_multi(xb, H, nvfp4={gs: (c, T.unswizzle(s, M, 2 * K))},
+                               nvfp4_qdq={gs: q})
+    for v in st.values():
+        assert v["exempt_blocks"] <= 0.01 * v["blocks"] + 2, st
 
 
 # ---------------------------------------------------------------------------------------------
@@ -839,82 +868,72 @@ def test_random_shapes_every_entry_point():
         T.check_rotated_qdq(xb, H, fmt, qdq(xb, fmt, H))
 
 
-@pytest.mark.parametrize("fmt", FMTS)
-def test_rotate_quantize_full_size_sampled_rows(fmt):
-    """The largest activation of the rotate+quantize workload, x[8192, 28672], swizzled scales:
-    32 sampled rows through the rules."""
+def test_rotate_quantize_full_size_other_format_and_layout():
+    """The largest activation of the rotate+quantize workload, x[8192, 28672], g = 32: MXFP8
+    with swizzled scales and MXFP4 with linear scales (MXFP4 swizzled is the workload grid
+    below), every block under the rules."""
     M, K = 8192, 28672
-    xb = W.rotate_quant_activation(M, K)
+    xb = full_input("rotate_quant_activation", M, K)
     H = rotation(32)
-    c, s = mxq.mx_rotate_quantize(T.to_gpu(xb), T.to_gpu(H), fmt, mxq.SWIZZLED)
-    c, s = T.u8(c), T.unswizzle(T.u8(s), M, K)
-    rows = np.sort(np.random.default_rng(5).choice(M, 32, replace=False))
-    stats = T.check_rotated_codes(xb[rows], H, fmt, c[rows], s[rows])
-    assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+    x, Hd = T.to_gpu(xb), T.to_gpu(H)
+    c8, s8 = mxq.mx_rotate_quantize(x, Hd, mxq.E4M3, mxq.SWIZZLED)
+    s8 = T.u8(s8)
+    assert not T.swizzle_pads(s8, M, K).any()
+    c4, s4 = mxq.mx_rotate_quantize(x, Hd, mxq.E2M1, mxq.LINEAR)
+    st = T.check_rotated_multi(xb, H, codes={O.E4M3: (T.u8(c8), T.unswizzle(s8, M, K)),
+                                             O.E2M1: (T.u8(c4), T.u8(s4))})
+    for v in st.values():
+        assert v["exempt_blocks"] <= 0.01 * v["blocks"] + 2, st
 
 
 @pytest.mark.parametrize("N,K", W.WEIGHT_SHAPES)
-def test_weight_rotate_quantize_full_size_sampled_rows(N, K):
+def test_weight_rotate_quantize_full_size(N, K):
     """Weight-side rotate + quantize of the 70B layer weights (the same H as the activations),
-    swizzled scales, both formats, g = 32 and g = 128: 16 sampled rows through the rules."""
+    swizzled scales, both formats, g = 32 and g = 128: every block of the whole weight under
+    the rules."""
     xb = W.weight_rotate_quant(N, K)
     x = T.to_gpu(xb)
-    rows = np.sort(np.random.default_rng(N + K).choice(N, 16, replace=False))
-    rows_t = torch.from_numpy(rows).cuda()
     for g in (32, 128):
         H = rotation(g)
+        outs = {}
         for fmt in FMTS:
             c, s = mxq.mx_rotate_quantize(x, T.to_gpu(H), fmt, mxq.SWIZZLED)
-            s = T.unswizzle(T.u8(s), N, K)
-            stats = T.check_rotated_codes(xb[rows], H, fmt, T.u8(c[rows_t]), s[rows])
-            assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
+            s = T.u8(s)
+            assert not T.swizzle_pads(s, N, K).any()
+            outs[fmt] = (T.u8(c), T.unswizzle(s, N, K))
             del c
+        st = T.check_rotated_multi(xb, H, codes=outs)
+        for v in st.values():
+            assert v["exempt_blocks"] <= 0.01 * v["blocks"] + 2, (g, st)
 
 
 @pytest.mark.parametrize("K", W.ROTATE_QUANT_K)
 @pytest.mark.parametrize("M", W.ROTATE_QUANT_M)
 def test_rotate_quant_workload_grid(M, K):
     """The fused rotate + MXFP4 quantize workload at every one of its (M, K) sizes (g = 32
-    normalized Hadamard, swizzled scales, rows padded to 128): all rows up to M = 128, 24 sampled
-    rows beyond, under the rules; swizzle pads zero over the whole buffer."""
-    xb = W.rotate_quant_activation(M, K)
+    normalized Hadamard, swizzled scales, rows padded to 128): every row under the rules,
+    swizzle pads zero over the whole buffer."""
+    xb = full_input("rotate_quant_activation", M, K)
     H = rotation(32)
     c, s = mxq.mx_rotate_quantize(T.to_gpu(xb), T.to_gpu(H), mxq.E2M1, mxq.SWIZZLED)
     s = T.u8(s)
     assert not T.swizzle_pads(s, M, K).any()
-    s = T.unswizzle(s, M, K)
-    rows = np.arange(M) if M <= 128 else np.sort(
-        np.random.default_rng(M + K).choice(M, 24, replace=False))
-    rows_t = torch.from_numpy(rows).cuda()
-    stats = T.check_rotated_codes(xb[rows], H, O.E2M1, T.u8(c[rows_t]), s[rows])
+    stats = T.check_rotated_codes(xb, H, O.E2M1, T.u8(c), T.unswizzle(s, M, K))
     assert stats["exempt_blocks"] <= 0.01 * stats["blocks"] + 2, stats
 
 
 @pytest.mark.parametrize("layer", [n for n, _, _ in W.ROTATION_SWEEP_LAYERS])
-def test_rotation_sweep_every_layer_sampled_rows(layer):
-    """The rotation-size sweep on each of the three decoder-layer inputs at full size: every g
-    in {16, 32, 64, 128} and both formats, 8 sampled rows under the rules."""
+def test_rotation_sweep_full_size(layer):
+    """The rotation-size sweep on each of the three decoder-layer inputs at full size: rotated
+    QDQ for every g in {16, 32, 64, 128} and both formats, every block under the rules."""
     xb = W.rotation_sweep_input(layer)
     x = T.to_gpu(xb)
-    rows = np.sort(np.random.default_rng(len(layer)).choice(xb.shape[0], 8, replace=False))
-    rows_t = torch.from_numpy(rows).cuda()
     for g in W.ROTATION_SWEEP_G:
         H = rotation(g)
-        for fmt in FMTS:
-            out = T.bf16_bits(mxq.mx_qdq(x, fmt, T.to_gpu(H))[rows_t])
-            T.check_rotated_qdq(xb[rows], H, fmt, out)
-
-
-def test_rotation_sweep_full_size_sampled_rows():
-    """Rotated QDQ at the full down-projection input [4096, 28672], every g and format."""
-    xb = W.rotation_sweep_input("down_proj_in")
-    x = T.to_gpu(xb)
-    rows = np.sort(np.random.default_rng(9).choice(xb.shape[0], 8, replace=False))
-    for g in (16, 32, 64, 128):
-        H = rotation(g)
-        for fmt in FMTS:
-            out = T.bf16_bits(mxq.mx_qdq(x, fmt, T.to_gpu(H))[torch.from_numpy(rows).cuda()])
-            T.check_rotated_qdq(xb[rows], H, fmt, out)
+        outs = {fmt: T.bf16_bits(mxq.mx_qdq(x, fmt, T.to_gpu(H))) for fmt in FMTS}
+        st = T.check_rotated_multi(xb, H, qdq=outs)
+        for v in st.values():
+            assert v["exempt_blocks"] <= 0.01 * v["blocks"] + 2, (g, st)
 
 
 def test_dependent_calls_keep_stream_order():
@@ -1002,6 +1021,32 @@ def test_bounded_wait_gives_up_and_reports():
     xb = W.rotate_quant_activation(256, 1024, stream=77)
     H = rotation(32, "identity")
     np.testing.assert_array_equal(qdq(xb, O.E2M1, H), O.qdq(xb, O.E2M1))
+    assert mxq.mx_device_errors() == 0
+
+
+def test_rotate_kernel_give_up_drains_and_reports():
+    """Failure detection in the tensor-core kernel itself, without a fault: every mbarrier wait
+    of a rotate+quantize call limited to 1 ns, 20 us and 1 ms (x[4096, 8192], 1024 tiles over
+    the persistent CTAs) runs out while the pipeline is busy. Each call still ends (no role
+    issues more work once its wait ran out, and loads, MMAs and stores in flight are waited
+    for before tensor memory is freed), the error word reports the give-up at least for the
+    1 ns limit, and afterwards the same context computes correct results."""
+    assert mxq.mx_device_errors() == 0
+    xb = W.rotate_quant_activation(4096, 8192, stream=79)
+    x, H = T.to_gpu(xb), T.to_gpu(rotation(32))
+    for limit in (1, 20_000, 1_000_000):
+        mxq.mx_selftest_rotate_give_up(x, H, limit)
+        errors = mxq.mx_device_errors()  # synchronizes: the call has ended
+        assert errors in (0, 1)
+        if limit == 1:
+            assert errors == 1
+    xs = W.rotate_quant_activation(256, 1024, stream=80)
+    Hi = rotation(32, "identity")
+    np.testing.assert_array_equal(qdq(xs, O.E2M1, Hi), O.qdq(xs, O.E2M1))
+    c, s = mxq.mx_rotate_quantize(T.to_gpu(xs), T.to_gpu(Hi), mxq.E4M3, mxq.SWIZZLED)
+    rc, rs = O.quantize(xs, O.E4M3, O.SWIZZLED)
+    np.testing.assert_array_equal(T.u8(c), rc)
+    np.testing.assert_array_equal(T.u8(s), rs)
     assert mxq.mx_device_errors() == 0
 
 

@@ -116,3 +116,81 @@ def test_nvfp4_scale_candidates_bracket_the_rounding():
     # 1.0625 is the midpoint of 1.0 (0x38) and 1.125 (0x39): a tolerance around it allows both
     assert T.nvfp4_scale_candidates(1.0625, 1e-6, gs) == {0x38, 0x39}
     assert T.nvfp4_scale_candidates(1.03, 1e-6, gs) == {0x38}
+
+
+def _packed_e2m1(codes):
+    return (codes[0::2] | (codes[1::2] << 4)).reshape(1, -1).astype(np.uint8)
+
+
+def test_scale_flip_only_toward_the_nearby_power_of_two():
+    """A block's abs-max within tolerance of 2^k (the bottom of its binade) lets the GPU's
+    scale byte be one lower, never one higher; within tolerance of 2^(k+1) (the top), one
+    higher, never one lower. Planted flips in the wrong direction are rejected even though the
+    codes are exactly what the oracle gives under the planted byte."""
+    g = 32
+    # bottom of the binade: amax = 4.0 exactly (E2M1 byte 127)
+    v = np.zeros((1, 32))
+    v[0, 0], v[0, 1] = 4.0, 0.75
+    x = W.to_bf16_bits(v)
+    H = identity(g)
+    _, s = O.rotate_quantize(x, H, O.E2M1, O.LINEAR)
+    assert int(s[0, 0]) == 127
+    for byte, ok in ((126, True), (128, False)):
+        _, codes = O.quantize_block(O.E2M1, v[0], forced_byte=byte)
+        sb = np.array([[byte]], dtype=np.uint8)
+        if ok:
+            assert T.check_rotated_codes(x, H, O.E2M1, _packed_e2m1(codes), sb)["scale_flips"] == 1
+        else:
+            with pytest.raises(AssertionError):
+                T.check_rotated_codes(x, H, O.E2M1, _packed_e2m1(codes), sb)
+    # top of the binade: every element 7.9375 * (1 + 2^-7) = 7.99951..., 4.9e-4 below 8; with
+    # g = 128 the chunk norm is about 90.5 (tolerance 9.05e-4); H = (1 + 2^-7) I is exact in
+    # bf16. The flip is planted in the first of the row's four blocks.
+    g = 128
+    v = np.full((1, 128), 7.9375)
+    x = W.to_bf16_bits(v)
+    H = W.to_bf16_bits(np.eye(g) * (1.0 + 2.0 ** -7))
+    y = O.rotate(x, H)
+    assert 0 < 8.0 - y.max() < 1e-5 * np.linalg.norm(y)
+    c, s = O.rotate_quantize(x, H, O.E2M1, O.LINEAR)
+    assert (s == 127).all()
+    for byte, ok in ((128, True), (126, False)):
+        _, codes = O.quantize_block(O.E2M1, y[0, :32], forced_byte=byte)
+        cb, sb = c.copy(), s.copy()
+        cb[0, :16] = _packed_e2m1(codes)[0]
+        sb[0, 0] = byte
+        if ok:
+            assert T.check_rotated_codes(x, H, O.E2M1, cb, sb)["scale_flips"] == 1
+        else:
+            with pytest.raises(AssertionError):
+                T.check_rotated_codes(x, H, O.E2M1, cb, sb)
+    # QDQ outputs follow the same rule: that block dequantized under byte 126 is rejected,
+    # under 128 accepted
+    for byte, ok in ((128, True), (126, False)):
+        _, codes = O.quantize_block(O.E2M1, y[0, :32], forced_byte=byte)
+        out = O.rotate_qdq(x, H, O.E2M1)
+        out[0, :32] = [O.dequant_bf16(O.E2M1, int(cd), byte) for cd in codes]
+        if ok:
+            assert T.check_rotated_qdq(x, H, O.E2M1, out)["exempt_blocks"] == 1
+        else:
+            with pytest.raises(AssertionError):
+                T.check_rotated_qdq(x, H, O.E2M1, out)
+
+
+def test_chunked_checks_cover_every_row():
+    """The whole-output checks split rows over a thread pool: a planted error in the last row
+    of a many-row input is still found, and per-chunk counts add up to the whole."""
+    x = W.rotate_quant_activation(97, 256, stream=5)
+    H = W.normalized_hadamard_bf16(32)
+    c, s = O.rotate_quantize(x, H, O.E4M3, O.LINEAR)
+    stats = T.check_rotated_codes(x, H, O.E4M3, c, s)
+    assert stats["blocks"] == 97 * 256 // 32 and stats["exempt_blocks"] == 0
+    bad = c.copy()
+    bad[96, 200] ^= 0x03
+    with pytest.raises(AssertionError, match="row 96"):
+        T.check_rotated_codes(x, H, O.E4M3, bad, s)
+    q = O.qdq(x, O.E2M1)
+    T.assert_rows_equal(q, T.oracle_qdq_rows(x, O.E2M1))
+    q[96, 255] ^= 1
+    with pytest.raises(AssertionError, match="rows"):
+        T.assert_rows_equal(q, T.oracle_qdq_rows(x, O.E2M1))
