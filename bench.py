@@ -6,8 +6,11 @@ columns * 100): two kernel launches, 402,653,184 algorithmic bytes (4 B per elem
 (192 MiB) and outputs (192 MiB) are larger than L2 (129 MB), so no flush runs between steps.
 
 Prints one JSON line: metric/value in algorithmic GB/s over the CUDA-event-timed region of K
-steps (every 10th step also brackets each launch with events, for the per-launch durations), a
-roofline object for the kernel (against the measured HBM copy bandwidth), the CPU oracle timed
+steps, launched back to back with no event between them (an event at a kernel boundary makes
+the stream drain there); after that region, a separate pass brackets each launch of some more
+steps with events for the per-launch durations. A roofline object for the kernel (against the
+measured HBM copy bandwidth, with the DRAM traffic per launch that an ncu capture recorded in
+profiles/mx_stream_qdq_traffic.json while the kernel's sources are unchanged), the CPU oracle timed
 on the host cores (cpu_baseline), an end-to-end figure through the same calls with the inputs
 copied in from, and the outputs back to, pinned host memory every step (e2e; copies in both
 directions pipelined over two buffer sets), SM clocks sampled during the timed region, and
@@ -25,7 +28,6 @@ import concurrent.futures
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -40,7 +42,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MX quant/QDQ HBM GB/s and % of GB300 peak; Gelem/s vs CPU oracle"
 WORKLOAD = "mxfp4_qdq: E2M1 QDQ g32 of bf16 x[8192,8192] Student-t(4)*0.02 + x[4096,8192] N(0,1) w/ 8 outlier cols"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "mx_stream_qdq_e2m1_mxfp4_qdq_workload.md")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "mx_stream_qdq_traffic.json")
 
 
 def parse_args():
@@ -171,16 +173,17 @@ def kernel_source_hash():
 
 
 def recorded_traffic():
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary, if the
-    kernel sources are unchanged since it was taken."""
+    """DRAM bytes per launch of the dominant kernel from the committed ncu record (read + write,
+    --cache-control none), if the kernel's sources are unchanged since it was taken; else
+    None."""
     try:
-        text = open(PROFILE_SUMMARY).read()
-    except OSError:
+        with open(TRAFFIC_RECORD) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    m = re.search(r"traffic_bytes_per_launch:\s*(\d+).*?source_sha:\s*([0-9a-f]+)", text, re.S)
-    if not m or m.group(2) != kernel_source_hash():
+    if rec.get("source_sha") != kernel_source_hash():
         return None
-    return int(m.group(1))
+    return rec
 
 
 def to_gpu(bits, dev):
@@ -793,45 +796,42 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     K = args.steps
-    # Every SAMPLE-th step brackets each of its two launches with CUDA events (the roofline's
-    # per-launch durations); the other steps run with no event between kernels, since an event
-    # at a kernel boundary makes the stream drain there and would slow the whole-job figure
-    # (sampling every 10th step cost about 2.5% of it; every 100th leaves 200 sampled steps of
-    # the default 20000).
-    sample = max(1, min(100, K // 20))
-    sampled = list(range(0, K, sample))
-    ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(4)] for i in sampled}
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         t_start.record(stream)
-        for i in range(K):
-            e = ev.get(i)
-            if e:
-                e[0].record(stream)
+        for _ in range(K):
             mxq.mx_qdq(xw, mxq.E2M1, y=yw, stream=stream)
-            if e:
-                e[1].record(stream)
-                e[2].record(stream)
             mxq.mx_qdq(xa, mxq.E2M1, y=ya, stream=stream)
-            if e:
-                e[3].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
     ms_total = max_over_ranks(t_start.elapsed_time(t_end), world)
     ms_per_step = ms_total / K
-    t_weight = statistics.fmean(ev[i][0].elapsed_time(ev[i][1]) for i in sampled) / 1e3
-    t_act = statistics.fmean(ev[i][2].elapsed_time(ev[i][3]) for i in sampled) / 1e3
+    # Per-launch durations, after the timed region: each launch of these steps is bracketed by
+    # events (which make the stream drain at every kernel boundary, so they read a little longer
+    # than the launches of the timed region).
+    n_sampled = min(200, max(20, K))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_sampled)]
+    for e in ev:
+        e[0].record(stream)
+        mxq.mx_qdq(xw, mxq.E2M1, y=yw, stream=stream)
+        e[1].record(stream)
+        e[2].record(stream)
+        mxq.mx_qdq(xa, mxq.E2M1, y=ya, stream=stream)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    t_weight = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    t_act = statistics.fmean(e[2].elapsed_time(e[3]) for e in ev) / 1e3
     launches = 2 * K
     value = step_bytes * world / (ms_per_step / 1e3) / 1e9
-    # Average launch duration of the kernel: the event-timed region holds nothing but its
-    # launches, back to back, so bytes of all launches / region time is the byte-weighted
-    # average (kernel boundaries included). launch_us keeps the sampled event-bracketed
-    # durations, which read a little longer: the brackets make the stream drain.
+    # Average launch duration of the kernel: the timed region holds nothing but its launches,
+    # back to back, so bytes of all launches / region time is the byte-weighted average
+    # (kernel boundaries included).
     achieved = step_bytes * K / (ms_total / 1e3) / 1e9
+    traffic = recorded_traffic()
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -848,10 +848,14 @@ def run_ours(args):
                      "kernel": "mx_stream_kernel<E2M1, QDQ>",
                      "launch_us": {"weight": t_weight * 1e6, "activation": t_act * 1e6,
                                    "region_per_step": ms_per_step * 1e3,
-                                   "sampled_steps": len(sampled)},
-                     "traffic": recorded_traffic(),
-                     "algorithmic_bytes_per_launch": {"weight": 4 * xw.numel(),
-                                                      "activation": 4 * xa.numel()}},
+                                   "bracketed_steps": n_sampled,
+                                   "note": "event-bracketed launches after the timed region"},
+                     "traffic": None if traffic is None else traffic["traffic_bytes_per_launch"],
+                     "traffic_detail": None if traffic is None else {
+                         "method": traffic["method"], "launches": traffic["launches"]},
+                     "algorithmic_bytes_per_launch": (4 * xw.numel() + 4 * xa.numel()) // 2,
+                     "algorithmic_bytes_by_tensor": {"weight": 4 * xw.numel(),
+                                                     "activation": 4 * xa.numel()}},
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.quick:
