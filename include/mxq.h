@@ -236,6 +236,22 @@ mx_status mx_device_errors(int* flags);
  */
 mx_status mx_selftest_bounded_wait(int64_t limit_ns, void* stream);
 
+/*
+ * Give-up self-test of the tensor-core rotation kernel (no counterpart on the pages): the call
+ * mx_rotate_quantize(x, M, K, H, g, MX_FMT_E2M1, 32, MX_SCALES_SWIZZLED, MX_ROUND_RNE, codes,
+ * scales, stream) makes, with every mbarrier wait of the kernel limited to limit_ns
+ * nanoseconds (1 .. 100,000,000) instead of 2 s, so that waits run out while the pipeline is
+ * busy. A role whose wait ran out stops issuing work, and the kernel still waits for its loads,
+ * MMAs and stores in flight before it frees tensor memory and exits: the call ends, the device
+ * error word reports the give-up (mx_device_errors) and the context stays usable. codes and
+ * scales then hold unspecified bytes. Shapes as mx_rotate_quantize, except that calls the
+ * few-row kernel would take (M <= 16 and M * g <= 512) and empty calls are MX_ERR_SHAPE.
+ * Errors: MX_ERR_SHAPE (limit or shape), MX_ERR_NULL, MX_ERR_ALIGN, MX_ERR_UNSUPPORTED (g),
+ * MX_ERR_CUDA.
+ */
+mx_status mx_selftest_rotate_give_up(const void* x, int64_t M, int64_t K, const void* H, int g,
+                                     void* codes, void* scales, int64_t limit_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,7 @@ EXPORTS = (
     "mx_rotate_quantize", "mx_quantize_grouped", "mx_dequantize", "mx_nvfp4_scales_shape",
     "mx_quantize_nvfp4", "mx_qdq_nvfp4", "mx_dequantize_nvfp4", "mx_nvfp4_grouped_scales_shape",
     "mx_quantize_nvfp4_grouped", "mx_rotate_debug", "mx_device_errors",
-    "mx_selftest_bounded_wait",
+    "mx_selftest_bounded_wait", "mx_selftest_rotate_give_up",
 )
 
 
@@ -71,6 +71,7 @@ def lib() -> ctypes.CDLL:
         "mx_rotate_debug": (i32, [p, i64, i64, p, i32, p, p]),
         "mx_device_errors": (i32, [ctypes.POINTER(ctypes.c_int)]),
         "mx_selftest_bounded_wait": (i32, [i64, p]),
+        "mx_selftest_rotate_give_up": (i32, [p, i64, i64, p, i32, p, p, i64, p]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -352,3 +353,17 @@ def mx_selftest_bounded_wait(limit_ns: int = 1_000_000, *, stream=None, device: 
     elif isinstance(st, torch.cuda.Stream):
         st = st.cuda_stream
     _check(lib().mx_selftest_bounded_wait(limit_ns, st))
+
+
+def mx_selftest_rotate_give_up(x, H, limit_ns: int, *, stream=None):
+    """The tensor-core rotate + MXFP4 quantize (swizzled scales) with every wait of the kernel
+    limited to limit_ns: waits run out while the pipeline is busy, the kernel stops issuing
+    work, drains what is in flight and returns; the device error word reports it (read it with
+    mx_device_errors()). Returns the (unspecified) codes and scales buffers."""
+    M, K = _input(x)
+    g = _rotation(H)
+    codes = _codes_out(None, x, M, K, E2M1)
+    scales = _scales_out(None, x, *mx_scales_shape(M, K, SWIZZLED))
+    _check(lib().mx_selftest_rotate_give_up(_ptr(x), M, K, _ptr(H), g, _ptr(codes), _ptr(scales),
+                                            limit_ns, _stream_ptr(stream, x)))
+    return codes, scales

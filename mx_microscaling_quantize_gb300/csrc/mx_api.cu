@@ -389,6 +389,29 @@ mx_status mx_selftest_bounded_wait(int64_t limit_ns, void* stream) {
                                              static_cast<cudaStream_t>(stream)));
 }
 
+mx_status mx_selftest_rotate_give_up(const void* x, int64_t M, int64_t K, const void* H, int g,
+                                     void* codes, void* scales, int64_t limit_ns, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 100000000) return MX_ERR_SHAPE;
+  bool empty = false;
+  mx_status st = check_common(M, K, MX_FMT_E2M1, 32, MX_ROUND_RNE, &empty);
+  if (st != MX_OK) return st;
+  if (!valid_g(g)) return MX_ERR_UNSUPPORTED;
+  // the tensor-core kernel takes every call but the few-row ones (M <= 16 and M * g <= 512)
+  if (K % g != 0 || !fits_tensor_map(M, K) || empty || (M <= 16 && M * g <= 512)) {
+    return MX_ERR_SHAPE;
+  }
+  if (!x || !H || !codes || !scales) return MX_ERR_NULL;
+  if (!aligned32(x) || !aligned32(codes) || !aligned16(scales) || !aligned16(H)) {
+    return MX_ERR_ALIGN;
+  }
+  mxq::RotArgs a = rot_args(x, M, K, H, codes);
+  a.scales = static_cast<uint8_t*>(scales);
+  a.scale_cols = a.col_tiles * 4;
+  a.wait_limit_ns = (unsigned long long)limit_ns;
+  return from_cuda(mxq::launch_rotate(MX_FMT_E2M1, mxq::kRotCodes, true, g, a,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
 mx_status mx_device_errors(int* flags) {
   if (!flags) return MX_ERR_NULL;
   unsigned int v = 0;

@@ -75,6 +75,9 @@ struct RotArgs {
   int64_t row_blocks;
   int64_t scale_cols;
   const float* gscale;  // NVFP4 only: device fp32 global scale
+  // Limit of each mbarrier wait in the tensor-core rotation kernel, ns; 0 = the default (2 s).
+  // Only the give-up self-test sets it.
+  unsigned long long wait_limit_ns;
 };
 
 cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const RotArgs& a,

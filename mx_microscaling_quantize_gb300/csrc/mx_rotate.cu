@@ -25,7 +25,12 @@
 // the K-major no-swizzle core-matrix layout, written once per CTA:
 //   element (n, k) = H[k][n] at (k / 8) * (g * 16) + n * 16 + (k % 8) * 2.
 // Every mbarrier wait is bounded (2 s); a wait that runs out sets the device error word and
-// the thread stops waiting from then on. Calls with very few rows go to a plain FMA kernel
+// the thread stops waiting from then on. A role whose wait ran out stops issuing work: the
+// producer issues no more loads, the MMA thread no more MMAs, and the epilogue warps (the whole
+// warp, since tcgen05.ld is warp-collective) skip their tensor-memory reads and stores while
+// still taking part in every epilogue barrier. Before the block deallocates tensor memory and
+// exits, the producer waits for its loads still in flight, the MMA thread for its last commit
+// and the storing thread for its bulk stores. Calls with very few rows go to a plain FMA kernel
 // instead (mx_rotate_small_kernel, below), which is faster at those sizes.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -440,30 +445,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
+  const unsigned long long limit = a.wait_limit_ns ? a.wait_limit_ns : kWaitLimitNs;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      int it = first_loads;  // the first stages were issued before the block-wide barrier
-      for (int64_t t = blockIdx.x + (int64_t)it * gridDim.x; t < n_tiles; t += gridDim.x, ++it) {
-        const int s = it % kStages;
-        mbar_wait(smem_u32(empty + s), ((it / kStages) & 1) ^ 1, &failed);
+      int issued = first_loads;  // the first stages were issued before the block-wide barrier
+      for (int64_t t = blockIdx.x + (int64_t)issued * gridDim.x; t < n_tiles; t += gridDim.x) {
+        const int s = issued % kStages;
+        mbar_wait(smem_u32(empty + s), ((issued / kStages) & 1) ^ 1, &failed, limit);
+        if (failed) break;
         load_tile(a, &tmap, sA_u32 + s * kStageBytes, smem_u32(full + s), t);
+        ++issued;
+      }
+      // Every load issued has landed before the block can exit: wait for the most recent load
+      // of each stage (the earlier ones were consumed before their stage was refilled). After
+      // a normal run these phases completed long ago and the waits return at once.
+      bool drain_failed = false;
+      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i) {
+        mbar_wait(smem_u32(full + i % kStages), (i / kStages) & 1, &drain_failed);
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kTileRows, G);
-      mbar_wait(smem_u32(h_ready), 0, &failed);
+      mbar_wait(smem_u32(h_ready), 0, &failed, limit);
       int it = 0;
       for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
         const int s = it % kStages, acc = it % kAcc;
         const int64_t cb = t % a.col_tiles;
         const int64_t kc64 = a.K - cb * kTileCols;
         const int kc = kc64 > kTileCols ? kTileCols : (int)kc64;  // multiple of 32 and of g
-        mbar_wait(smem_u32(full + s), (it / kStages) & 1, &failed);
-        if (it >= kAcc) mbar_wait(smem_u32(tempty + acc), ((it / kAcc) & 1) ^ 1, &failed);
+        mbar_wait(smem_u32(full + s), (it / kStages) & 1, &failed, limit);
+        if (it >= kAcc) mbar_wait(smem_u32(tempty + acc), ((it / kAcc) & 1) ^ 1, &failed, limit);
+        if (failed) break;
         tc_fence_after();
         for (int j = 0; j < kc / G; ++j) {
 #pragma unroll
@@ -478,6 +494,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(smem_u32(empty + s));   // stage free once these MMAs have read it
         mma_commit(smem_u32(tfull + acc));  // accumulator ready
+      }
+      // `it` tiles were committed; the last commit tracks every MMA this thread issued, so its
+      // completion means no MMA still reads shared memory or writes tensor memory.
+      if (it > 0) {
+        bool drain_failed = false;
+        mbar_wait(smem_u32(tfull + (it - 1) % kAcc), ((it - 1) / kAcc) & 1, &drain_failed);
       }
     }
   } else {
@@ -509,15 +531,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kc = kc64 > kTileCols ? kTileCols : (int)kc64;
       const bool row_ok = row0 + r < a.M;
       const bool active = q * 32 < kc;  // this warp's 32 columns exist in the tile
-      mbar_wait(smem_u32(tfull + acc), (it / kAcc) & 1, &failed);
+      mbar_wait(smem_u32(tfull + acc), (it / kAcc) & 1, &failed, limit);
+      // tcgen05.ld is warp-collective: once any lane's wait ran out, the whole warp skips it
+      failed = __any_sync(0xFFFFFFFFu, failed);
+      const bool work = active && !failed;
       tc_fence_after();
       float y[32];
-      if (active) tmem_ld32(lane_base + (uint32_t)(acc * 128 + q * 32), y);
+      if (work) tmem_ld32(lane_base + (uint32_t)(acc * 128 + q * 32), y);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(tempty + acc));  // accumulator free for tile it + kAcc
       if (OUT == kRotDebug) {
-        if (active && row_ok) {
+        if (work && row_ok) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) +
                                                   (row0 + r) * a.K + cb * kTileCols + q * 32);
 #pragma unroll
@@ -527,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint32_t o[kWords];
       uint32_t byte = 0;  // pad rows / columns of the swizzled scale tile stay zero
-      if (active) {
+      if (work) {
         if constexpr (kNv) byte = nv_block_outputs<OUT>(y, o, r6, t_enc, t_dq);
         else byte = block_outputs<FMT, OUT>(y, o);
       }
@@ -536,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* scale_tile = s_scale + (it & 1) * scale_stage_bytes<FMT, OUT>();
       if (e == 0 && lane == 0) bulk_wait_read_all_but_one();
       epilogue_sync();
-      if (active) {
+      if (work) {
         if (OUT == kRotQdq) {
           // two 128-byte-swizzled boxes of 64 bf16 per row: chunk c of row r at c ^ (r % 8)
           uint8_t* row = out_tile + (q >> 1) * kBoxBytes + r * 128;
@@ -568,13 +593,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           scale_tile[swizzle_in_tile(r, q)] = (uint8_t)byte;
         }
-      } else if (OUT == kRotCodes && active) {  // linear: the tile's scales of row r, in order
+      } else if (OUT == kRotCodes && work) {  // linear: the tile's scales of row r, in order
         if (kNv) *reinterpret_cast<uint16_t*>(scale_tile + r * 8 + 2 * q) = (uint16_t)byte;
         else scale_tile[r * 4 + q] = (uint8_t)byte;
       }
       fence_proxy_async_smem();
       epilogue_sync();
-      if (OUT == kRotCodes && !SWZ && q == 0 && row_ok) {
+      if (OUT == kRotCodes && !SWZ && q == 0 && row_ok && !failed) {
         // Linear scales: one thread per tile row writes the row's scale bytes of this tile
         // (4 MX / 8 NVFP4 bytes, fewer in a partial last column tile) with one store when the
         // destination allows it, instead of one 1- or 2-byte store per 32-element block.
@@ -596,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < nbytes; ++i) dst[i] = src[i];
         }
       }
-      if (e == 0 && lane == 0) {
+      if (e == 0 && lane == 0 && !failed) {
         const uint32_t src = smem_u32(out_tile);
         if (OUT == kRotQdq) {  // rows >= M and columns >= K are dropped by the TMA
           tma_store_2d(&ymap, (int)(cb * kTileCols), (int)row0, src);
