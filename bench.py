@@ -550,6 +550,8 @@ def extra_workloads(dev, peak):
 CASES = {
     "mxfp8_linear_quant": "E4M3 quantize, linear scales, x[128,4096]",
     "rotate_quant": "E2M1 rotate(g=32 Hadamard)+quantize, swizzled, x[8192,8192]",
+    "rotate_quant_hadamard": "the same call with rot_kind ROT_HADAMARD (in-register fast "
+                             "Walsh-Hadamard transform on the streaming layout)",
     "rotated_qdq_g128": "E4M3 rotated QDQ g=128, x[4096,28672] Student-t(5)",
     "moe_quant": "E4M3 grouped quantize, swizzled, 128 experts, x[16384,2048]",
     "dequant_mxfp4": "E2M1 dequantize, swizzled scales, codes of the weight x[8192,8192]",
@@ -565,7 +567,74 @@ CASES = {
                      "torch's plain bf16 <-> float8_e4m3fn cast of the same bytes",
     "rotate_quant_tiles": "E2M1 rotate(g=32)+quantize, swizzled, x[128, 128 * SMs * n]: exactly "
                           "n = --tiles-per-sm tiles per SM, launches cycling over input copies",
+    "nonrotated_sweep": "every non-rotated kernel at full workload size (quantize, QDQ, "
+                        "dequantize, NVFP4, grouped MoE, the x[128,4096] MXFP8 quantize), each "
+                        "launched --steps times back to back, in turn (for per-kernel ncu "
+                        "captures; one JSON line with each variant's mean us per launch)",
 }
+
+
+def nonrotated_variants(dev):
+    """(name, launch closure, algorithmic bytes per launch) of every non-rotated kernel variant
+    at its full workload size."""
+    import torch
+    import mx_microscaling_quantize_gb300 as mxq
+    from mx_microscaling_quantize_gb300 import workloads as W
+    out = []
+    xw = to_gpu(W.mxfp4_qdq_weight(), dev)
+    xa = to_gpu(W.mxfp4_qdq_activation(), dev)
+    n = xw.numel()
+    K = xw.shape[1]
+    for fmt, fname, cb in ((mxq.E2M1, "mxfp4", 0.5), (mxq.E4M3, "mxfp8", 1.0)):
+        for layout, lname in ((mxq.LINEAR, "linear"), (mxq.SWIZZLED, "swizzled")):
+            c, s = mxq.mx_quantize(xw, fmt, layout)
+            out.append((f"quant_{fname}_{lname}[8192,8192]",
+                        lambda c=c, s=s, fmt=fmt, layout=layout:
+                        mxq.mx_quantize(xw, fmt, layout, codes=c, scales=s),
+                        int(2 * n + cb * n + n // 32)))
+            y = torch.empty_like(xw)
+            out.append((f"dequant_{fname}_{lname}[8192,8192]",
+                        lambda c=c, s=s, y=y, fmt=fmt, layout=layout:
+                        mxq.mx_dequantize(c, s, K, fmt, layout, y=y),
+                        int(2 * n + cb * n + n // 32)))
+        for x, tname in ((xw, "weight[8192,8192]"), (xa, "activation[4096,8192]")):
+            y = torch.empty_like(x)
+            out.append((f"qdq_{fname}_{tname}", lambda x=x, y=y, fmt=fmt: mxq.mx_qdq(x, fmt, y=y),
+                        4 * x.numel()))
+    gs = torch.tensor([448.0 * 6.0], device=dev) / xw.float().abs().max()
+    for layout, lname in ((mxq.LINEAR, "linear"), (mxq.SWIZZLED, "swizzled")):
+        c, s = mxq.mx_quantize_nvfp4(xw, gs, layout)
+        out.append((f"nvfp4_quant_{lname}[8192,8192]",
+                    lambda c=c, s=s, layout=layout:
+                    mxq.mx_quantize_nvfp4(xw, gs, layout, codes=c, scales=s),
+                    int(2.5 * n + n // 16)))
+        y = torch.empty_like(xw)
+        out.append((f"nvfp4_dequant_{lname}[8192,8192]",
+                    lambda c=c, s=s, y=y, layout=layout:
+                    mxq.mx_dequantize_nvfp4(c, s, K, gs, layout, y=y), int(2.5 * n + n // 16)))
+    y = torch.empty_like(xw)
+    out.append(("nvfp4_qdq[8192,8192]", lambda y=y: mxq.mx_qdq_nvfp4(xw, gs, y=y), 4 * n))
+    xb, off = W.moe_quant()
+    xm = to_gpu(xb, dev)
+    offs = torch.from_numpy(off).to(dev)
+    used = int(sum(-(-int(k) // 128) * 128 for k in np.diff(off)))
+    c, s = mxq.mx_quantize_grouped(xm, offs, mxq.E4M3, mxq.SWIZZLED)
+    out.append(("moe_quant_mxfp8[16384,2048]x128",
+                lambda c=c, s=s: mxq.mx_quantize_grouped(xm, offs, mxq.E4M3, mxq.SWIZZLED,
+                                                          codes=c, scales=s),
+                3 * xm.numel() + used * s.shape[1]))
+    gse = torch.full((len(off) - 1,), 100.0, device=dev)
+    c, s = mxq.mx_quantize_nvfp4_grouped(xm, offs, gse, mxq.SWIZZLED)
+    out.append(("moe_quant_nvfp4[16384,2048]x128",
+                lambda c=c, s=s: mxq.mx_quantize_nvfp4_grouped(xm, offs, gse, mxq.SWIZZLED,
+                                                                codes=c, scales=s),
+                int(2.5 * xm.numel()) + used * s.shape[1]))
+    x1 = to_gpu(W.mxfp8_linear_quant(), dev)
+    c, s = mxq.mx_quantize(x1, mxq.E4M3, mxq.LINEAR)
+    out.append(("quant_mxfp8_linear[128,4096]",
+                lambda c=c, s=s: mxq.mx_quantize(x1, mxq.E4M3, mxq.LINEAR, codes=c, scales=s),
+                3 * x1.numel() + s.numel()))
+    return out
 
 
 def run_case(args):
@@ -576,6 +645,25 @@ def run_case(args):
     __graft_entry__.build()
     import mx_microscaling_quantize_gb300 as mxq
     from mx_microscaling_quantize_gb300 import workloads as W
+    if args.case == "nonrotated_sweep":
+        variants = nonrotated_variants(dev)
+        for _, fn, _ in variants:  # warm-up: one launch of each
+            fn()
+        torch.cuda.synchronize()
+        res = {}
+        for name, fn, nbytes in variants:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(max(1, args.steps)):
+                fn()
+            b.record()
+            b.synchronize()
+            t = a.elapsed_time(b) / 1e3 / max(1, args.steps)
+            res[name] = {"us_per_launch": t * 1e6, "GB/s": nbytes / t / 1e9,
+                         "algorithmic_bytes": nbytes}
+        print(json.dumps({"case": args.case, "what": CASES[args.case], "variants": res,
+                          "gpu_launches": len(variants) * (1 + max(1, args.steps))}), flush=True)
+        return
     if args.case == "mxfp8_linear_quant":
         x = to_gpu(W.mxfp8_linear_quant(), dev)
         c, s = mxq.mx_quantize(x, mxq.E4M3, mxq.LINEAR)
@@ -586,6 +674,13 @@ def run_case(args):
         H = to_gpu(W.normalized_hadamard_bf16(32), dev)
         c, s = mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED)
         fn = lambda: mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, codes=c, scales=s)
+        nbytes = 2 * x.numel() + c.numel() + s.numel()
+    elif args.case == "rotate_quant_hadamard":
+        x = to_gpu(W.rotate_quant_activation(8192, 8192), dev)
+        H = to_gpu(W.normalized_hadamard_bf16(32), dev)
+        c, s = mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, rot_kind=mxq.ROT_HADAMARD)
+        fn = lambda: mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, codes=c, scales=s,
+                                            rot_kind=mxq.ROT_HADAMARD)
         nbytes = 2 * x.numel() + c.numel() + s.numel()
     elif args.case == "rotated_qdq_g128":
         x = to_gpu(W.rotation_sweep_input("down_proj_in"), dev)
@@ -791,16 +886,23 @@ def run_ours(args):
         mxq.mx_qdq(xw, mxq.E2M1, y=yw, stream=stream)
         mxq.mx_qdq(xa, mxq.E2M1, y=ya, stream=stream)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-
     K = args.steps
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
+    sleep = getattr(torch.cuda, "_sleep", None)
     with ClockSampler(local) as clocks:
+        # The warm-up runs once the clock sampler is up, right before the timed region, so that
+        # the region does not start on a GPU that sat idle while the sampler started.
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        # A short device-side wait (about 50 us) ahead of the region's first event: the host
+        # queues the first launches meanwhile, so the region starts with its work already
+        # submitted instead of on a host launch.
+        if sleep is not None:
+            sleep(100_000)
         t_start.record(stream)
         for _ in range(K):
             mxq.mx_qdq(xw, mxq.E2M1, y=yw, stream=stream)

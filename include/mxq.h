@@ -72,6 +72,24 @@ typedef int mx_status;
 /* rounding schemes */
 #define MX_ROUND_RNE 0 /* abs-max floor scale, round to nearest even, saturate */
 
+/*
+ * Rotation kinds (argument rot_kind of the rotating calls; ignored where H is NULL).
+ *  MX_ROT_DENSE: H is any bf16 [g, g] matrix; the product runs on the tensor cores (calls
+ *    with at most 16 rows and M * g <= 512: fp32 FMAs).
+ *  MX_ROT_HADAMARD: the caller states that H = c * S_g, where S_g is the Sylvester Hadamard
+ *    matrix of order g (S_1 = [1], S_2n = [[S_n, S_n], [S_n, -S_n]], entry (i, j) =
+ *    (-1)^popcount(i & j)) and c = H[0][0], e.g. the normalized hadamard(g) * g^-0.5 rounded
+ *    to bf16. The product is then a fast Walsh-Hadamard transform in registers (log2 g
+ *    butterfly stages in fp32, then a multiplication by c) on the streaming kernel. Every
+ *    CTA checks the statement on the bit patterns of H on the device; where it does not hold
+ *    the call computes sum_i x_i H[i][j] with fp32 FMAs instead, so the results are correct
+ *    for any H (only slower).
+ * Both kinds compute the same rotation up to fp32 rounding (well inside the 1e-5 normwise
+ * tolerance of the rotated path).
+ */
+#define MX_ROT_DENSE 0
+#define MX_ROT_HADAMARD 1
+
 /* Text of a status code (static storage). */
 const char* mx_status_string(mx_status status);
 
@@ -95,12 +113,12 @@ mx_status mx_quantize(const void* x, int64_t M, int64_t K, int fmt, int group, i
 /*
  * QDQ: quantize then dequantize, bf16 in, bf16 out (pages: mxfp4_qdq / mxfp8_qdq).
  * If H is not NULL, every g-element chunk along K is first rotated, y_chunk = x_chunk * H
- * (H: bf16 [g, g] row-major device matrix, g in {16, 32, 64, 128}, K % g == 0), and the
- * rotated values are quantized; the output stays in the rotated basis. If H is NULL, g is
- * ignored. y: bf16 [M, K], must not overlap x.
+ * (H: bf16 [g, g] row-major device matrix, g in {16, 32, 64, 128}, K % g == 0, rot_kind an
+ * MX_ROT_* value), and the rotated values are quantized; the output stays in the rotated
+ * basis. If H is NULL, g and rot_kind are ignored. y: bf16 [M, K], must not overlap x.
  */
 mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int rounding,
-                 const void* H, int g, void* y, void* stream);
+                 const void* H, int g, int rot_kind, void* y, void* stream);
 
 /*
  * Dequantize stored MX data to bf16 (pages: the QuTLASS review thread on vLLM's MXFP4 test,
@@ -120,14 +138,14 @@ mx_status mx_dequantize(const void* codes, const void* scales, int64_t M, int64_
 
 /*
  * Fused rotate + quantize (pages: fusedQuantizeMx(a, b) with b the runtime-loaded rotation).
- * y_chunk = x_chunk * H for every g-chunk along K (bf16 products, fp32 accumulation on the
- * tensor cores), then the block quantization above on the fp32 rotated values.
- * H: bf16 [g, g] row-major, g in {16, 32, 64, 128}, K % g == 0. Other arguments as
- * mx_quantize.
+ * y_chunk = x_chunk * H for every g-chunk along K (bf16 products, fp32 accumulation; see
+ * MX_ROT_* for how), then the block quantization above on the fp32 rotated values.
+ * H: bf16 [g, g] row-major, g in {16, 32, 64, 128}, K % g == 0. rot_kind: MX_ROT_*. Other
+ * arguments as mx_quantize.
  */
-mx_status mx_rotate_quantize(const void* x, int64_t M, int64_t K, const void* H, int g, int fmt,
-                             int group, int layout, int rounding, void* codes, void* scales,
-                             void* stream);
+mx_status mx_rotate_quantize(const void* x, int64_t M, int64_t K, const void* H, int g,
+                             int rot_kind, int fmt, int group, int layout, int rounding,
+                             void* codes, void* scales, void* stream);
 
 /*
  * Scale-matrix shape for a grouped call with E experts and M_total rows: linear
@@ -163,7 +181,8 @@ mx_status mx_quantize_grouped(const void* x, const int64_t* row_offsets, int E, 
  *   QDQ: y_i = bf16(decode(code_i) * (decode(scale) / gs))  (0 factor likewise).
  * A block holding a NaN or an infinity gets scale byte 0x7F, codes 0 and QDQ outputs 0x7FC0.
  * With H (bf16 [g, g], g in {16, 32, 64, 128}, K % g == 0) every g-chunk is first rotated,
- * y_chunk = x_chunk * H (fp32 accumulation on the tensor cores), as in mx_rotate_quantize.
+ * y_chunk = x_chunk * H (fp32 accumulation; rot_kind as in mx_rotate_quantize, ignored without
+ * H), as in mx_rotate_quantize.
  * global_scale: DEVICE pointer to one fp32 value, 4-byte aligned, read by the kernel (so it may
  * come from an earlier kernel on the same stream); it must be positive and finite, and
  * gs / 2^-9 must not overflow fp32 (gs < 1.7e38 * 2^-9), else results are unspecified.
@@ -174,11 +193,11 @@ mx_status mx_quantize_grouped(const void* x, const int64_t* row_offsets, int E, 
 mx_status mx_nvfp4_scales_shape(int64_t M, int64_t K, int layout, int64_t* rows, int64_t* cols);
 
 mx_status mx_quantize_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g,
-                            const float* global_scale, int layout, void* codes, void* scales,
-                            void* stream);
+                            int rot_kind, const float* global_scale, int layout, void* codes,
+                            void* scales, void* stream);
 
 /* NVFP4 QDQ (see above): bf16 y [M, K], 32-byte aligned, must not overlap x. */
-mx_status mx_qdq_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g,
+mx_status mx_qdq_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g, int rot_kind,
                        const float* global_scale, void* y, void* stream);
 
 /*
@@ -215,10 +234,11 @@ mx_status mx_dequantize_nvfp4(const void* codes, const void* scales, int64_t M, 
 
 /*
  * Diagnostics: the rotated values y = x_chunk * H exactly as mx_rotate_quantize computes them
- * before quantization (same device code), written as fp32 [M, K] to y_f32 (device).
+ * before quantization with the same rot_kind (same device code), written as fp32 [M, K] to
+ * y_f32 (device, 32-byte aligned).
  */
-mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, int g, float* y_f32,
-                          void* stream);
+mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, int g, int rot_kind,
+                          float* y_f32, void* stream);
 
 /*
  * Device-side error word of the current device: bit 0 set if a kernel gave up waiting for

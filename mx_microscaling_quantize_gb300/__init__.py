@@ -21,6 +21,8 @@ LINEAR = 0
 SWIZZLED = 1
 RNE = 0
 GROUP = 32
+ROT_DENSE = 0     # any H: tensor-core product
+ROT_HADAMARD = 1  # H = H[0][0] * Sylvester (stated by the caller, checked on the device)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmxq.so")
@@ -58,17 +60,17 @@ def lib() -> ctypes.CDLL:
         "mx_scales_shape": (i32, [i64, i64, i32, i32, pi64, pi64]),
         "mx_grouped_scales_shape": (i32, [i64, i32, i64, i32, i32, pi64, pi64]),
         "mx_quantize": (i32, [p, i64, i64, i32, i32, i32, i32, p, p, p]),
-        "mx_qdq": (i32, [p, i64, i64, i32, i32, i32, p, i32, p, p]),
-        "mx_rotate_quantize": (i32, [p, i64, i64, p, i32, i32, i32, i32, i32, p, p, p]),
+        "mx_qdq": (i32, [p, i64, i64, i32, i32, i32, p, i32, i32, p, p]),
+        "mx_rotate_quantize": (i32, [p, i64, i64, p, i32, i32, i32, i32, i32, i32, p, p, p]),
         "mx_quantize_grouped": (i32, [p, p, i32, i64, i64, i32, i32, i32, i32, p, p, p]),
         "mx_dequantize": (i32, [p, p, i64, i64, i32, i32, i32, p, p]),
         "mx_nvfp4_scales_shape": (i32, [i64, i64, i32, pi64, pi64]),
-        "mx_quantize_nvfp4": (i32, [p, i64, i64, p, i32, p, i32, p, p, p]),
-        "mx_qdq_nvfp4": (i32, [p, i64, i64, p, i32, p, p, p]),
+        "mx_quantize_nvfp4": (i32, [p, i64, i64, p, i32, i32, p, i32, p, p, p]),
+        "mx_qdq_nvfp4": (i32, [p, i64, i64, p, i32, i32, p, p, p]),
         "mx_dequantize_nvfp4": (i32, [p, p, i64, i64, p, i32, p, p]),
         "mx_nvfp4_grouped_scales_shape": (i32, [i64, i32, i64, i32, pi64, pi64]),
         "mx_quantize_nvfp4_grouped": (i32, [p, p, i32, i64, i64, p, i32, p, p, p]),
-        "mx_rotate_debug": (i32, [p, i64, i64, p, i32, p, p]),
+        "mx_rotate_debug": (i32, [p, i64, i64, p, i32, i32, p, p]),
         "mx_device_errors": (i32, [ctypes.POINTER(ctypes.c_int)]),
         "mx_selftest_bounded_wait": (i32, [i64, p]),
         "mx_selftest_rotate_give_up": (i32, [p, i64, i64, p, i32, p, p, i64, p]),
@@ -172,26 +174,28 @@ def mx_quantize(x, fmt, layout=LINEAR, *, codes=None, scales=None, group=GROUP, 
     return codes, scales
 
 
-def mx_qdq(x, fmt, H=None, *, y=None, group=GROUP, rounding=RNE, stream=None):
-    """Quantize-dequantize bf16 [M, K] -> bf16 [M, K]; with H, rotate each g-chunk first."""
+def mx_qdq(x, fmt, H=None, *, y=None, group=GROUP, rounding=RNE, rot_kind=ROT_DENSE,
+           stream=None):
+    """Quantize-dequantize bf16 [M, K] -> bf16 [M, K]; with H, rotate each g-chunk first
+    (rot_kind: ROT_DENSE or ROT_HADAMARD)."""
     M, K = _input(x)
     g = _rotation(H) if H is not None else 0
     if y is None:
         y = torch.empty_like(x)
-    _check(lib().mx_qdq(_ptr(x), M, K, fmt, group, rounding, _ptr(H), g, _ptr(y),
+    _check(lib().mx_qdq(_ptr(x), M, K, fmt, group, rounding, _ptr(H), g, rot_kind, _ptr(y),
                         _stream_ptr(stream, x)))
     return y
 
 
 def mx_rotate_quantize(x, H, fmt, layout=SWIZZLED, *, codes=None, scales=None, group=GROUP,
-                       rounding=RNE, stream=None):
+                       rounding=RNE, rot_kind=ROT_DENSE, stream=None):
     """Rotate each g-chunk by H, then block quantize -> (codes, scales)."""
     M, K = _input(x)
     g = _rotation(H)
     codes = _codes_out(codes, x, M, K, fmt)
     scales = _scales_out(scales, x, *mx_scales_shape(M, K, layout, group))
-    _check(lib().mx_rotate_quantize(_ptr(x), M, K, _ptr(H), g, fmt, group, layout, rounding,
-                                    _ptr(codes), _ptr(scales), _stream_ptr(stream, x)))
+    _check(lib().mx_rotate_quantize(_ptr(x), M, K, _ptr(H), g, rot_kind, fmt, group, layout,
+                                    rounding, _ptr(codes), _ptr(scales), _stream_ptr(stream, x)))
     return codes, scales
 
 
@@ -248,26 +252,26 @@ def _global_scale(gs) -> None:
 
 
 def mx_quantize_nvfp4(x, global_scale, layout=SWIZZLED, H=None, *, codes=None, scales=None,
-                      stream=None):
+                      rot_kind=ROT_DENSE, stream=None):
     """NVFP4 quantize (optionally rotating each g-chunk by H first) -> (codes, E4M3 scales)."""
     M, K = _input(x)
     _global_scale(global_scale)
     g = _rotation(H) if H is not None else 0
     codes = _codes_out(codes, x, M, K, E2M1)
     scales = _scales_out(scales, x, *mx_nvfp4_scales_shape(M, K, layout))
-    _check(lib().mx_quantize_nvfp4(_ptr(x), M, K, _ptr(H), g, _ptr(global_scale), layout,
-                                   _ptr(codes), _ptr(scales), _stream_ptr(stream, x)))
+    _check(lib().mx_quantize_nvfp4(_ptr(x), M, K, _ptr(H), g, rot_kind, _ptr(global_scale),
+                                   layout, _ptr(codes), _ptr(scales), _stream_ptr(stream, x)))
     return codes, scales
 
 
-def mx_qdq_nvfp4(x, global_scale, H=None, *, y=None, stream=None):
+def mx_qdq_nvfp4(x, global_scale, H=None, *, y=None, rot_kind=ROT_DENSE, stream=None):
     """NVFP4 quantize-dequantize bf16 [M, K] -> bf16 [M, K] (optionally rotated)."""
     M, K = _input(x)
     _global_scale(global_scale)
     g = _rotation(H) if H is not None else 0
     if y is None:
         y = torch.empty_like(x)
-    _check(lib().mx_qdq_nvfp4(_ptr(x), M, K, _ptr(H), g, _ptr(global_scale), _ptr(y),
+    _check(lib().mx_qdq_nvfp4(_ptr(x), M, K, _ptr(H), g, rot_kind, _ptr(global_scale), _ptr(y),
                               _stream_ptr(stream, x)))
     return y
 
@@ -327,13 +331,14 @@ def mx_dequantize_nvfp4(codes, scales, K, global_scale, layout=SWIZZLED, *, y=No
     return y
 
 
-def mx_rotate_debug(x, H, *, y=None, stream=None):
+def mx_rotate_debug(x, H, *, y=None, rot_kind=ROT_DENSE, stream=None):
     """The fp32 rotated values the rotated kernels quantize (diagnostics)."""
     M, K = _input(x)
     g = _rotation(H)
     if y is None:
         y = torch.empty((M, K), dtype=torch.float32, device=x.device)
-    _check(lib().mx_rotate_debug(_ptr(x), M, K, _ptr(H), g, _ptr(y), _stream_ptr(stream, x)))
+    _check(lib().mx_rotate_debug(_ptr(x), M, K, _ptr(H), g, rot_kind, _ptr(y),
+                                 _stream_ptr(stream, x)))
     return y
 
 

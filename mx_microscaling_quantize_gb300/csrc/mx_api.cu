@@ -16,6 +16,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool valid_fmt(int fmt) { return fmt == MX_FMT_E2M1 || fmt == MX_FMT_E4M3; }
 bool valid_layout(int layout) { return layout == MX_SCALES_LINEAR || layout == MX_SCALES_SWIZZLED; }
 bool valid_g(int g) { return g == 16 || g == 32 || g == 64 || g == 128; }
+bool valid_rot_kind(int k) { return k == MX_ROT_DENSE || k == MX_ROT_HADAMARD; }
 
 // Checks shared by every call on an [M, K] bf16 input. Returns MX_OK to go on; *empty is set
 // when there is nothing to compute.
@@ -122,12 +123,12 @@ mx_status mx_quantize(const void* x, int64_t M, int64_t K, int fmt, int group, i
 }
 
 mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int rounding,
-                 const void* H, int g, void* y, void* stream) {
+                 const void* H, int g, int rot_kind, void* y, void* stream) {
   bool empty = false;
   mx_status st = check_common(M, K, fmt, group, rounding, &empty);
   if (st != MX_OK) return st;
   if (H) {
-    if (!valid_g(g)) return MX_ERR_UNSUPPORTED;
+    if (!valid_g(g) || !valid_rot_kind(rot_kind)) return MX_ERR_UNSUPPORTED;
     if (K % g != 0 || !fits_tensor_map(M, K)) return MX_ERR_SHAPE;
   }
   if (empty) return MX_OK;
@@ -135,6 +136,12 @@ mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int ro
   if (!aligned32(x) || !aligned32(y)) return MX_ERR_ALIGN;
   if (H) {
     if (!aligned16(H)) return MX_ERR_ALIGN;
+    if (rot_kind == MX_ROT_HADAMARD) {
+      mxq::StreamArgs a = stream_args(x, M, K, y);
+      a.H = H;
+      return from_cuda(mxq::launch_hadamard(fmt, mxq::kRotQdq, false, g, a,
+                                            static_cast<cudaStream_t>(stream)));
+    }
     return from_cuda(mxq::launch_rotate(fmt, mxq::kRotQdq, false, g, rot_args(x, M, K, H, y),
                                         static_cast<cudaStream_t>(stream)));
   }
@@ -163,19 +170,28 @@ mx_status mx_dequantize(const void* codes, const void* scales, int64_t M, int64_
                                        static_cast<cudaStream_t>(stream)));
 }
 
-mx_status mx_rotate_quantize(const void* x, int64_t M, int64_t K, const void* H, int g, int fmt,
-                             int group, int layout, int rounding, void* codes, void* scales,
-                             void* stream) {
+mx_status mx_rotate_quantize(const void* x, int64_t M, int64_t K, const void* H, int g,
+                             int rot_kind, int fmt, int group, int layout, int rounding,
+                             void* codes, void* scales, void* stream) {
   bool empty = false;
   mx_status st = check_common(M, K, fmt, group, rounding, &empty);
   if (st != MX_OK) return st;
-  if (!valid_layout(layout) || !valid_g(g)) return MX_ERR_UNSUPPORTED;
+  if (!valid_layout(layout) || !valid_g(g) || !valid_rot_kind(rot_kind)) return MX_ERR_UNSUPPORTED;
   if (K % g != 0 || !fits_tensor_map(M, K)) return MX_ERR_SHAPE;
   if (empty) return MX_OK;
   if (!x || !H || !codes || !scales) return MX_ERR_NULL;
   if (!aligned32(x) || !aligned32(codes)) return MX_ERR_ALIGN;
   if (layout == MX_SCALES_SWIZZLED && !aligned16(scales)) return MX_ERR_ALIGN;
   if (!aligned16(H)) return MX_ERR_ALIGN;
+  if (rot_kind == MX_ROT_HADAMARD) {
+    mxq::StreamArgs a = stream_args(x, M, K, codes);
+    a.scales = static_cast<uint8_t*>(scales);
+    a.scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : ceil_div(K, mxq::kTileCols) * 4;
+    a.scale_rows = layout == MX_SCALES_LINEAR ? M : ceil_div(M, mxq::kTileRows) * mxq::kTileRows;
+    a.H = H;
+    return from_cuda(mxq::launch_hadamard(fmt, mxq::kRotCodes, layout == MX_SCALES_SWIZZLED, g, a,
+                                          static_cast<cudaStream_t>(stream)));
+  }
   mxq::RotArgs a = rot_args(x, M, K, H, codes);
   a.scales = static_cast<uint8_t*>(scales);
   a.scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : a.col_tiles * 4;
@@ -227,12 +243,12 @@ namespace {
 
 // Shared by the two NVFP4 calls: validation of x, H and the global scale. Returns MX_OK to go
 // on; *empty is set when there is nothing to compute.
-mx_status check_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g,
+mx_status check_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g, int rot_kind,
                       const float* global_scale, bool* empty) {
   mx_status st = check_common(M, K, MX_FMT_E2M1, 32, MX_ROUND_RNE, empty);
   if (st != MX_OK) return st;
   if (H) {
-    if (!valid_g(g)) return MX_ERR_UNSUPPORTED;
+    if (!valid_g(g) || !valid_rot_kind(rot_kind)) return MX_ERR_UNSUPPORTED;
     if (K % g != 0 || !fits_tensor_map(M, K)) return MX_ERR_SHAPE;
   }
   if (*empty) return MX_OK;
@@ -245,11 +261,11 @@ mx_status check_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g,
 }  // namespace
 
 mx_status mx_quantize_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g,
-                            const float* global_scale, int layout, void* codes, void* scales,
-                            void* stream) {
+                            int rot_kind, const float* global_scale, int layout, void* codes,
+                            void* scales, void* stream) {
   if (!valid_layout(layout)) return MX_ERR_UNSUPPORTED;
   bool empty = false;
-  mx_status st = check_nvfp4(x, M, K, H, g, global_scale, &empty);
+  mx_status st = check_nvfp4(x, M, K, H, g, rot_kind, global_scale, &empty);
   if (st != MX_OK || empty) return st;
   if (!codes || !scales) return MX_ERR_NULL;
   if (!aligned32(codes)) return MX_ERR_ALIGN;
@@ -260,6 +276,16 @@ mx_status mx_quantize_nvfp4(const void* x, int64_t M, int64_t K, const void* H, 
   int64_t srows = 0, scols = 0;
   mx_nvfp4_scales_shape(M, K, layout, &srows, &scols);
   const bool swz = layout == MX_SCALES_SWIZZLED;
+  if (H && rot_kind == MX_ROT_HADAMARD) {
+    mxq::StreamArgs a = stream_args(x, M, K, codes);
+    a.scales = static_cast<uint8_t*>(scales);
+    a.scale_cols = scols;
+    a.scale_rows = srows;
+    a.gscale = global_scale;
+    a.H = H;
+    return from_cuda(mxq::launch_hadamard(mxq::kFmtNVFP4, mxq::kRotCodes, swz, g, a,
+                                          static_cast<cudaStream_t>(stream)));
+  }
   if (H) {
     mxq::RotArgs a = rot_args(x, M, K, H, codes);
     a.scales = static_cast<uint8_t*>(scales);
@@ -277,13 +303,20 @@ mx_status mx_quantize_nvfp4(const void* x, int64_t M, int64_t K, const void* H, 
                                       static_cast<cudaStream_t>(stream)));
 }
 
-mx_status mx_qdq_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g,
+mx_status mx_qdq_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g, int rot_kind,
                        const float* global_scale, void* y, void* stream) {
   bool empty = false;
-  mx_status st = check_nvfp4(x, M, K, H, g, global_scale, &empty);
+  mx_status st = check_nvfp4(x, M, K, H, g, rot_kind, global_scale, &empty);
   if (st != MX_OK || empty) return st;
   if (!y) return MX_ERR_NULL;
   if (!aligned32(y)) return MX_ERR_ALIGN;
+  if (H && rot_kind == MX_ROT_HADAMARD) {
+    mxq::StreamArgs a = stream_args(x, M, K, y);
+    a.gscale = global_scale;
+    a.H = H;
+    return from_cuda(mxq::launch_hadamard(mxq::kFmtNVFP4, mxq::kRotQdq, false, g, a,
+                                          static_cast<cudaStream_t>(stream)));
+  }
   if (H) {
     mxq::RotArgs a = rot_args(x, M, K, H, y);
     a.gscale = global_scale;
@@ -367,17 +400,23 @@ mx_status mx_dequantize_nvfp4(const void* codes, const void* scales, int64_t M, 
                                        static_cast<cudaStream_t>(stream)));
 }
 
-mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, int g, float* y_f32,
-                          void* stream) {
+mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, int g, int rot_kind,
+                          float* y_f32, void* stream) {
   bool empty = false;
   mx_status st = check_common(M, K, MX_FMT_E2M1, 32, MX_ROUND_RNE, &empty);
   if (st != MX_OK) return st;
-  if (!valid_g(g)) return MX_ERR_UNSUPPORTED;
+  if (!valid_g(g) || !valid_rot_kind(rot_kind)) return MX_ERR_UNSUPPORTED;
   if (K % g != 0 || !fits_tensor_map(M, K)) return MX_ERR_SHAPE;
   if (empty) return MX_OK;
   if (!x || !H || !y_f32) return MX_ERR_NULL;
   if (!aligned32(x) || !aligned32(y_f32)) return MX_ERR_ALIGN;
   if (!aligned16(H)) return MX_ERR_ALIGN;
+  if (rot_kind == MX_ROT_HADAMARD) {
+    mxq::StreamArgs a = stream_args(x, M, K, y_f32);
+    a.H = H;
+    return from_cuda(mxq::launch_hadamard(MX_FMT_E2M1, mxq::kRotDebug, false, g, a,
+                                          static_cast<cudaStream_t>(stream)));
+  }
   return from_cuda(mxq::launch_rotate(MX_FMT_E2M1, mxq::kRotDebug, false, g,
                                       rot_args(x, M, K, H, y_f32),
                                       static_cast<cudaStream_t>(stream)));

@@ -341,6 +341,91 @@ __device__ __forceinline__ NvScales nv_scales_tab(uint32_t amax0, uint32_t amax1
   return n;
 }
 
+// ------------------------------------------------------------------------------------------
+// One thread's 32 fp32 values (rotated values, lower K index first) -> output words.
+// ------------------------------------------------------------------------------------------
+// MX: one 32-element block. Writes 16 words of bf16 QDQ output or the block's codes (E2M1: 4
+// words, E4M3: 8) into out; returns the E8M0 byte. A block holding a NaN or an infinity gets
+// byte 0xFF and the fill outputs (QDQ 0x7FC0, E2M1 codes 0, E4M3 codes 0x7F). Every lane of
+// the warp must call it (the NaN check is a warp vote).
+template <int FMT, bool QDQ>
+__device__ __forceinline__ uint32_t mx_block_f32(float* y, uint32_t* out) {
+  const uint32_t byte = scale_byte_from_amax_bits<FMT>(absmax_f32x32(y));
+  const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);
+  const float inv = inv_scale_of(byte);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) mul2(y[2 * i], y[2 * i + 1], inv);  // y <- y / 2^s
+  if (QDQ) {
+    const float sc = scale_of(byte);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) out[i] = qdq2<FMT>(y[2 * i], y[2 * i + 1], sc);
+  } else if (FMT == kFmtE2M1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = codes8_e2m1(y + 8 * i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint2 c = codes8_e4m3(y + 8 * i);
+      out[2 * i] = c.x;
+      out[2 * i + 1] = c.y;
+    }
+  }
+  if (special && byte == 255u) {
+    const uint32_t fill = QDQ ? kBf16NaNx2 : (FMT == kFmtE2M1 ? 0u : kE4M3NaNx4);
+#pragma unroll
+    for (int i = 0; i < (QDQ ? 16 : (FMT == kFmtE2M1 ? 4 : 8)); ++i) out[i] = fill;
+  }
+  return byte;
+}
+
+// NVFP4: two 16-element blocks under the scales n (from nv_scales or nv_scales_tab). Writes 16
+// words of bf16 QDQ output or 4 words of E2M1 codes; a NaN/Inf block gets 0x7FC0 / codes 0.
+// Every lane of the warp must call it.
+template <bool QDQ>
+__device__ __forceinline__ void nv_block_f32(float* y, uint32_t* out, const NvScales& n) {
+  const bool special = __any_sync(0xFFFFFFFFu, n.special[0] || n.special[1]);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) mul2(y[2 * i], y[2 * i + 1], n.enc[i >> 3]);  // y <- y * enc
+  if (QDQ) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) out[i] = qdq2_e2m1(y[2 * i], y[2 * i + 1], n.dq[i >> 3]);
+    if (special) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) out[i] = n.special[i >> 3] ? kBf16NaNx2 : out[i];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = codes8_e2m1(y + 8 * i);
+    if (special) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) out[i] = n.special[i >> 1] ? 0u : out[i];
+    }
+  }
+}
+
+// Zeroes the pad bytes of a swizzled scale buffer of a plain (not grouped) call, spread over
+// every thread of the grid (t0: this thread's index, nthr: the grid's threads): (A) in each of
+// the M data rows, the bytes past column dcols of its last 4-byte word (only when dcols % 4 !=
+// 0); (B) every 4-byte word of every pad row (rows M .. scale_rows - 1, as a flat list of
+// (row, word) items so that a few wide pad rows do not serialize on a few threads).
+__device__ __forceinline__ void zero_swizzled_pads(uint8_t* scales, int64_t M, int64_t dcols,
+                                                   int64_t scale_rows, int64_t cp, int64_t t0,
+                                                   int64_t nthr) {
+  const int64_t cp4 = cp >> 2;
+  if (dcols & 3) {
+    const int64_t c4 = dcols & ~int64_t(3);
+    for (int64_t r = t0; r < M; r += nthr) {
+      uint8_t* run = scales + swizzled_offset(r, c4, cp);
+      for (int64_t c = dcols; c < c4 + 4; ++c) run[c - c4] = 0;
+    }
+  }
+  const int64_t pad_rows = scale_rows - M;
+  for (int64_t i = t0; i < pad_rows * cp4; i += nthr) {
+    const int64_t pr = M + i % pad_rows, c4 = (i / pad_rows) * 4;
+    *reinterpret_cast<uint32_t*>(scales + swizzled_offset(pr, c4, cp)) = 0u;
+  }
+}
+
 // Programmatic dependent launch. Every kernel of the library is launched with programmatic
 // stream serialization (launch_pdl): its CTAs may be scheduled while the kernel before it on
 // the stream is still finishing. Each kernel lets the next one be scheduled as soon as all of

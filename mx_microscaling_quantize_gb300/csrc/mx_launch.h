@@ -42,6 +42,7 @@ struct StreamArgs {
   const int64_t* offsets;  // grouped only: device int64 [E + 1]
   int E;
   const float* gscale;     // NVFP4 only: device fp32 global scale (grouped: one per expert)
+  const void* H;           // Hadamard-rotated calls only: bf16 [g, g] row-major
 };
 
 // fmt: 1 = E2M1, 2 = E4M3, 3 = NVFP4. qdq: write bf16 QDQ instead of codes +
@@ -63,6 +64,12 @@ struct DequantArgs {
 cudaError_t launch_dequant(int fmt, bool swizzled, const DequantArgs& a, cudaStream_t stream);
 
 enum RotOut { kRotCodes = 0, kRotQdq = 1, kRotDebug = 2 };
+
+// Rotate + quantize / QDQ / debug values on the streaming layout with a fast Walsh-Hadamard
+// transform (H stated to be H[0][0] * Sylvester; checked on the device, dense FMA product
+// otherwise). fmt as launch_stream; out_kind a RotOut; a.H and g the rotation.
+cudaError_t launch_hadamard(int fmt, int out_kind, bool swizzled, int g, const StreamArgs& a,
+                            cudaStream_t stream);
 
 struct RotArgs {
   const void* x;      // bf16 [M, K]

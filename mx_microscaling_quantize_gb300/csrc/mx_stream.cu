@@ -436,28 +436,9 @@ __global__ void __launch_bounds__(kThreads, stream_min_ctas<FMT, QDQ, GROUPED>()
   }
 
   if (SWZ && !QDQ && GROUPED) zero_grouped_pads<kNv>(a, s_off, s_prow, cblk);
-  if (SWZ && !QDQ && !GROUPED) {
-    // Zero the pad bytes of the swizzled buffer, spread over every thread of the grid: (A) in
-    // each data row, the bytes past column K/32 of its last 4-byte word (only when
-    // K/32 % 4 != 0); (B) every 4-byte word of every pad row (rows past M: a flat list of
-    // (row, word) items, so that a few wide pad rows do not serialize on a few threads).
-    // Grouped calls write their pad bytes with zero_grouped_pads.
-    const int64_t cp = a.scale_cols, cp4 = cp >> 2;
-    const int64_t dcols = kNv ? 2 * cblk : cblk;  // scale columns holding data
-    const int64_t nthr = (int64_t)gridDim.x * kThreads;
-    const int64_t t0 = (int64_t)blockIdx.x * kThreads + tid;
-    if (dcols & 3) {
-      const int64_t c4 = dcols & ~int64_t(3);
-      for (int64_t r = t0; r < a.M; r += nthr) {
-        uint8_t* run = a.scales + swizzled_offset(r, c4, cp);
-        for (int64_t c = dcols; c < c4 + 4; ++c) run[c - c4] = 0;
-      }
-    }
-    const int64_t pad_rows = a.scale_rows - a.M;
-    for (int64_t i = t0; i < pad_rows * cp4; i += nthr) {
-      const int64_t pr = a.M + i % pad_rows, c4 = (i / pad_rows) * 4;
-      *reinterpret_cast<uint32_t*>(a.scales + swizzled_offset(pr, c4, cp)) = 0u;
-    }
+  if (SWZ && !QDQ && !GROUPED) {  // grouped calls write their pad bytes with zero_grouped_pads
+    zero_swizzled_pads(a.scales, a.M, kNv ? 2 * cblk : cblk, a.scale_rows, a.scale_cols,
+                       (int64_t)blockIdx.x * kThreads + tid, (int64_t)gridDim.x * kThreads);
   }
 }
 

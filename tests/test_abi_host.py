@@ -50,6 +50,8 @@ def test_macros_match_binding():
     assert int(macros["MX_SCALES_LINEAR"]) == mxq.LINEAR
     assert int(macros["MX_SCALES_SWIZZLED"]) == mxq.SWIZZLED
     assert int(macros["MX_ROUND_RNE"]) == mxq.RNE
+    assert int(macros["MX_ROT_DENSE"]) == mxq.ROT_DENSE
+    assert int(macros["MX_ROT_HADAMARD"]) == mxq.ROT_HADAMARD
 
 
 def test_status_strings(L):
@@ -113,22 +115,29 @@ def test_quantize_validation(L):
 
 
 def test_qdq_and_rotation_validation(L):
-    assert L.mx_qdq(P, 4, 64, 1, 32, 0, P, 8, P, None) == UNSUP     # g = 8
-    assert L.mx_qdq(P, 4, 96, 1, 32, 0, P, 64, P, None) == SHAPE    # K % g
-    assert L.mx_qdq(P, 4, 64, 1, 32, 0, P + 1, 32, P, None) == ALIGN
-    assert L.mx_qdq(P, 4, 64, 1, 32, 0, P + 8, 32, P, None) == ALIGN
-    assert L.mx_qdq(P, 4, 64, 1, 32, 0, None, 0, None, None) == NULL
-    assert L.mx_qdq(P, 4, 64, 1, 32, 0, None, 0, P + 2, None) == ALIGN
-    assert L.mx_qdq(P, 4, 64, 1, 32, 0, None, 0, P + 16, None) == ALIGN
-    r = L.mx_rotate_quantize
-    assert r(P, 4, 64, P, 48, 1, 32, 1, 0, P, P, None) == UNSUP
-    assert r(P, 4, 192, P, 128, 1, 32, 1, 0, P, P, None) == SHAPE
-    assert r(P, 4, 64, None, 32, 1, 32, 1, 0, P, P, None) == NULL
-    assert r(P, 4, 64, P, 32, 1, 32, 1, 0, P, P + 8, None) == ALIGN
-    assert r(None, 0, 64, None, 32, 1, 32, 1, 0, None, None, None) == OK
-    d = L.mx_rotate_debug
-    assert d(P, 4, 64, P, 24, P, None) == UNSUP
-    assert d(P, 4, 64, None, 32, P, None) == NULL
+    q = L.mx_qdq  # (x, M, K, fmt, group, rounding, H, g, rot_kind, y, stream)
+    for rk in (0, 1):  # MX_ROT_DENSE, MX_ROT_HADAMARD
+        assert q(P, 4, 64, 1, 32, 0, P, 8, rk, P, None) == UNSUP     # g = 8
+        assert q(P, 4, 96, 1, 32, 0, P, 64, rk, P, None) == SHAPE    # K % g
+        assert q(P, 4, 64, 1, 32, 0, P + 1, 32, rk, P, None) == ALIGN
+        assert q(P, 4, 64, 1, 32, 0, P + 8, 32, rk, P, None) == ALIGN
+    assert q(P, 4, 64, 1, 32, 0, P, 32, 2, P, None) == UNSUP         # unknown rot_kind
+    assert q(P, 4, 64, 1, 32, 0, None, 0, 7, None, None) == NULL     # no H: rot_kind ignored
+    assert q(P, 4, 64, 1, 32, 0, None, 0, 0, P + 2, None) == ALIGN
+    assert q(P, 4, 64, 1, 32, 0, None, 0, 0, P + 16, None) == ALIGN
+    r = L.mx_rotate_quantize  # (x, M, K, H, g, rot_kind, fmt, group, layout, rnd, codes, scales, s)
+    for rk in (0, 1):
+        assert r(P, 4, 64, P, 48, rk, 1, 32, 1, 0, P, P, None) == UNSUP
+        assert r(P, 4, 192, P, 128, rk, 1, 32, 1, 0, P, P, None) == SHAPE
+        assert r(P, 4, 64, None, 32, rk, 1, 32, 1, 0, P, P, None) == NULL
+        assert r(P, 4, 64, P, 32, rk, 1, 32, 1, 0, P, P + 8, None) == ALIGN
+        assert r(None, 0, 64, None, 32, rk, 1, 32, 1, 0, None, None, None) == OK
+    assert r(P, 4, 64, P, 32, -1, 1, 32, 1, 0, P, P, None) == UNSUP
+    d = L.mx_rotate_debug  # (x, M, K, H, g, rot_kind, y, stream)
+    assert d(P, 4, 64, P, 24, 0, P, None) == UNSUP
+    assert d(P, 4, 64, P, 32, 3, P, None) == UNSUP
+    assert d(P, 4, 64, None, 32, 1, P, None) == NULL
+    assert d(P, 4, 64, P, 32, 1, P + 16, None) == ALIGN
 
 
 def test_grouped_validation(L):
@@ -163,24 +172,27 @@ def test_nvfp4_shapes_and_validation(L):
     assert mxq.mx_nvfp4_scales_shape(1, 32, mxq.SWIZZLED) == (128, 4)
     assert mxq.mx_nvfp4_scales_shape(300, 416, mxq.SWIZZLED) == (384, 28)
     assert mxq.mx_nvfp4_scales_shape(300, 416, mxq.LINEAR) == (300, 26)
-    q = L.mx_quantize_nvfp4  # (x, M, K, H, g, gs, layout, codes, scales, stream)
-    assert q(P, 4, 48, None, 0, P, 0, P, P, None) == SHAPE
-    assert q(P, 4, 64, None, 0, P, 2, P, P, None) == UNSUP
-    assert q(P, 4, 64, P, 8, P, 0, P, P, None) == UNSUP
-    assert q(P, 4, 96, P, 64, P, 0, P, P, None) == SHAPE
-    assert q(P, 4, 64, None, 0, None, 0, P, P, None) == NULL
-    assert q(None, 4, 64, None, 0, P, 0, P, P, None) == NULL
-    assert q(P, 4, 64, None, 0, P, 0, None, P, None) == NULL
-    assert q(P, 4, 64, None, 0, P + 2, 0, P, P, None) == ALIGN
-    assert q(P, 4, 64, None, 0, P, 0, P + 16, P, None) == ALIGN
-    assert q(P, 4, 64, None, 0, P, 0, P, P + 1, None) == ALIGN
-    assert q(P, 4, 64, None, 0, P, 1, P, P + 2, None) == ALIGN
-    assert q(P, 4, 64, P + 8, 32, P, 1, P, P, None) == ALIGN
-    assert q(None, 0, 64, None, 0, None, 1, None, None, None) == OK
-    d = L.mx_qdq_nvfp4  # (x, M, K, H, g, gs, y, stream)
-    assert d(P, 4, 64, None, 0, P, None, None) == NULL
-    assert d(P, 4, 64, None, 0, P, P + 16, None) == ALIGN
-    assert d(P, -1, 64, None, 0, P, P, None) == SHAPE
+    q = L.mx_quantize_nvfp4  # (x, M, K, H, g, rot_kind, gs, layout, codes, scales, stream)
+    assert q(P, 4, 48, None, 0, 0, P, 0, P, P, None) == SHAPE
+    assert q(P, 4, 64, None, 0, 0, P, 2, P, P, None) == UNSUP
+    assert q(P, 4, 64, P, 8, 0, P, 0, P, P, None) == UNSUP
+    assert q(P, 4, 64, P, 32, 2, P, 0, P, P, None) == UNSUP          # unknown rot_kind
+    assert q(P, 4, 96, P, 64, 1, P, 0, P, P, None) == SHAPE
+    assert q(P, 4, 64, None, 0, 0, None, 0, P, P, None) == NULL
+    assert q(None, 4, 64, None, 0, 0, P, 0, P, P, None) == NULL
+    assert q(P, 4, 64, None, 0, 0, P, 0, None, P, None) == NULL
+    assert q(P, 4, 64, None, 0, 0, P + 2, 0, P, P, None) == ALIGN
+    assert q(P, 4, 64, None, 0, 0, P, 0, P + 16, P, None) == ALIGN
+    assert q(P, 4, 64, None, 0, 0, P, 0, P, P + 1, None) == ALIGN
+    assert q(P, 4, 64, None, 0, 0, P, 1, P, P + 2, None) == ALIGN
+    for rk in (0, 1):
+        assert q(P, 4, 64, P + 8, 32, rk, P, 1, P, P, None) == ALIGN
+    assert q(None, 0, 64, None, 0, 0, None, 1, None, None, None) == OK
+    d = L.mx_qdq_nvfp4  # (x, M, K, H, g, rot_kind, gs, y, stream)
+    assert d(P, 4, 64, None, 0, 0, P, None, None) == NULL
+    assert d(P, 4, 64, None, 0, 0, P, P + 16, None) == ALIGN
+    assert d(P, -1, 64, None, 0, 0, P, P, None) == SHAPE
+    assert d(P, 4, 64, P, 32, 5, P, P, None) == UNSUP
     assert mxq.mx_nvfp4_grouped_scales_shape(300, 4, 416, mxq.SWIZZLED) == (768, 28)
     assert mxq.mx_nvfp4_grouped_scales_shape(300, 4, 416, mxq.LINEAR) == (300, 26)
     gq = L.mx_quantize_nvfp4_grouped  # (x, off, E, M, K, gs, layout, codes, scales, stream)
