@@ -569,14 +569,18 @@ CASES = {
                           "n = --tiles-per-sm tiles per SM, launches cycling over input copies",
     "nonrotated_sweep": "every non-rotated kernel at full workload size (quantize, QDQ, "
                         "dequantize, NVFP4, grouped MoE, the x[128,4096] MXFP8 quantize), each "
-                        "launched --steps times back to back, in turn (for per-kernel ncu "
-                        "captures; one JSON line with each variant's mean us per launch)",
+                        "launched --steps times back to back over buffer copies that exceed 3x "
+                        "L2, in turn (for per-kernel ncu captures; one JSON line with each "
+                        "variant's mean us per launch)",
 }
 
 
 def nonrotated_variants(dev):
-    """(name, launch closure, algorithmic bytes per launch) of every non-rotated kernel variant
-    at its full workload size."""
+    """(name, make, algorithmic bytes per launch, bytes of one buffer set) of every non-rotated
+    kernel variant at its full workload size; make(k) returns a launch closure over buffer set k
+    (k = 0: the workload's own input; k > 0: copies). Outputs are torch.empty buffers and the
+    dequantize inputs random code / scale bytes, so that building the variants launches no
+    kernel of the library."""
     import torch
     import mx_microscaling_quantize_gb300 as mxq
     from mx_microscaling_quantize_gb300 import workloads as W
@@ -584,56 +588,99 @@ def nonrotated_variants(dev):
     xw = to_gpu(W.mxfp4_qdq_weight(), dev)
     xa = to_gpu(W.mxfp4_qdq_activation(), dev)
     n = xw.numel()
-    K = xw.shape[1]
+    M, K = xw.shape
+    gen = torch.Generator(device=dev).manual_seed(7)
+
+    def rnd_bytes(shape):
+        return torch.randint(0, 256, shape, dtype=torch.uint8, device=dev, generator=gen)
+
+    def cpy(t, k):
+        return t if k == 0 else t.clone()
+
     for fmt, fname, cb in ((mxq.E2M1, "mxfp4", 0.5), (mxq.E4M3, "mxfp8", 1.0)):
+        cshape = (M, mxq.code_bytes_per_row(fmt, K))
         for layout, lname in ((mxq.LINEAR, "linear"), (mxq.SWIZZLED, "swizzled")):
-            c, s = mxq.mx_quantize(xw, fmt, layout)
-            out.append((f"quant_{fname}_{lname}[8192,8192]",
-                        lambda c=c, s=s, fmt=fmt, layout=layout:
-                        mxq.mx_quantize(xw, fmt, layout, codes=c, scales=s),
-                        int(2 * n + cb * n + n // 32)))
-            y = torch.empty_like(xw)
-            out.append((f"dequant_{fname}_{lname}[8192,8192]",
-                        lambda c=c, s=s, y=y, fmt=fmt, layout=layout:
-                        mxq.mx_dequantize(c, s, K, fmt, layout, y=y),
-                        int(2 * n + cb * n + n // 32)))
-        for x, tname in ((xw, "weight[8192,8192]"), (xa, "activation[4096,8192]")):
-            y = torch.empty_like(x)
-            out.append((f"qdq_{fname}_{tname}", lambda x=x, y=y, fmt=fmt: mxq.mx_qdq(x, fmt, y=y),
-                        4 * x.numel()))
+            sshape = mxq.mx_scales_shape(M, K, layout)
+            nb = int(2 * n + cb * n + n // 32)
+
+            def make_q(k, fmt=fmt, layout=layout, cshape=cshape, sshape=sshape):
+                x = cpy(xw, k)
+                c = torch.empty(cshape, dtype=torch.uint8, device=dev)
+                s_ = torch.empty(sshape, dtype=torch.uint8, device=dev)
+                return lambda: mxq.mx_quantize(x, fmt, layout, codes=c, scales=s_)
+            out.append((f"quant_{fname}_{lname}[8192,8192]", make_q, nb, nb))
+            codes0, scales0 = rnd_bytes(cshape), rnd_bytes(sshape)
+
+            def make_d(k, fmt=fmt, layout=layout, codes0=codes0, scales0=scales0):
+                c, s_ = cpy(codes0, k), cpy(scales0, k)
+                y = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+                return lambda: mxq.mx_dequantize(c, s_, K, fmt, layout, y=y)
+            out.append((f"dequant_{fname}_{lname}[8192,8192]", make_d, nb, nb))
+        for x0, tname in ((xw, "weight[8192,8192]"), (xa, "activation[4096,8192]")):
+            def make_qdq(k, x0=x0, fmt=fmt):
+                x = cpy(x0, k)
+                y = torch.empty_like(x)
+                return lambda: mxq.mx_qdq(x, fmt, y=y)
+            out.append((f"qdq_{fname}_{tname}", make_qdq, 4 * x0.numel(), 4 * x0.numel()))
     gs = torch.tensor([448.0 * 6.0], device=dev) / xw.float().abs().max()
+    nb4 = int(2.5 * n + n // 16)
     for layout, lname in ((mxq.LINEAR, "linear"), (mxq.SWIZZLED, "swizzled")):
-        c, s = mxq.mx_quantize_nvfp4(xw, gs, layout)
-        out.append((f"nvfp4_quant_{lname}[8192,8192]",
-                    lambda c=c, s=s, layout=layout:
-                    mxq.mx_quantize_nvfp4(xw, gs, layout, codes=c, scales=s),
-                    int(2.5 * n + n // 16)))
-        y = torch.empty_like(xw)
-        out.append((f"nvfp4_dequant_{lname}[8192,8192]",
-                    lambda c=c, s=s, y=y, layout=layout:
-                    mxq.mx_dequantize_nvfp4(c, s, K, gs, layout, y=y), int(2.5 * n + n // 16)))
-    y = torch.empty_like(xw)
-    out.append(("nvfp4_qdq[8192,8192]", lambda y=y: mxq.mx_qdq_nvfp4(xw, gs, y=y), 4 * n))
+        sshape = mxq.mx_nvfp4_scales_shape(M, K, layout)
+
+        def make_q4(k, layout=layout, sshape=sshape):
+            x = cpy(xw, k)
+            c = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+            s_ = torch.empty(sshape, dtype=torch.uint8, device=dev)
+            return lambda: mxq.mx_quantize_nvfp4(x, gs, layout, codes=c, scales=s_)
+        out.append((f"nvfp4_quant_{lname}[8192,8192]", make_q4, nb4, nb4))
+        codes0 = rnd_bytes((M, K // 2))
+        scales0 = rnd_bytes(sshape) & 0x77  # finite E4M3 scale bytes
+
+        def make_d4(k, layout=layout, codes0=codes0, scales0=scales0):
+            c, s_ = cpy(codes0, k), cpy(scales0, k)
+            y = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+            return lambda: mxq.mx_dequantize_nvfp4(c, s_, K, gs, layout, y=y)
+        out.append((f"nvfp4_dequant_{lname}[8192,8192]", make_d4, nb4, nb4))
+
+    def make_qdq4(k):
+        x = cpy(xw, k)
+        y = torch.empty_like(x)
+        return lambda: mxq.mx_qdq_nvfp4(x, gs, y=y)
+    out.append(("nvfp4_qdq[8192,8192]", make_qdq4, 4 * n, 4 * n))
     xb, off = W.moe_quant()
     xm = to_gpu(xb, dev)
     offs = torch.from_numpy(off).to(dev)
+    E = len(off) - 1
     used = int(sum(-(-int(k) // 128) * 128 for k in np.diff(off)))
-    c, s = mxq.mx_quantize_grouped(xm, offs, mxq.E4M3, mxq.SWIZZLED)
-    out.append(("moe_quant_mxfp8[16384,2048]x128",
-                lambda c=c, s=s: mxq.mx_quantize_grouped(xm, offs, mxq.E4M3, mxq.SWIZZLED,
-                                                          codes=c, scales=s),
-                3 * xm.numel() + used * s.shape[1]))
-    gse = torch.full((len(off) - 1,), 100.0, device=dev)
-    c, s = mxq.mx_quantize_nvfp4_grouped(xm, offs, gse, mxq.SWIZZLED)
-    out.append(("moe_quant_nvfp4[16384,2048]x128",
-                lambda c=c, s=s: mxq.mx_quantize_nvfp4_grouped(xm, offs, gse, mxq.SWIZZLED,
-                                                                codes=c, scales=s),
-                int(2.5 * xm.numel()) + used * s.shape[1]))
+    srows, scols = mxq.mx_grouped_scales_shape(xm.shape[0], E, xm.shape[1], mxq.SWIZZLED)
+    nb8 = 3 * xm.numel() + used * scols
+
+    def make_moe8(k):
+        x = cpy(xm, k)
+        c = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+        s_ = torch.empty((srows, scols), dtype=torch.uint8, device=dev)
+        return lambda: mxq.mx_quantize_grouped(x, offs, mxq.E4M3, mxq.SWIZZLED, codes=c, scales=s_)
+    out.append(("moe_quant_mxfp8[16384,2048]x128", make_moe8, nb8, nb8))
+    gse = torch.full((E,), 100.0, device=dev)
+    srows4, scols4 = mxq.mx_nvfp4_grouped_scales_shape(xm.shape[0], E, xm.shape[1], mxq.SWIZZLED)
+    nbm4 = int(2.5 * xm.numel()) + used * scols4
+
+    def make_moe4(k):
+        x = cpy(xm, k)
+        c = torch.empty((x.shape[0], x.shape[1] // 2), dtype=torch.uint8, device=dev)
+        s_ = torch.empty((srows4, scols4), dtype=torch.uint8, device=dev)
+        return lambda: mxq.mx_quantize_nvfp4_grouped(x, offs, gse, mxq.SWIZZLED, codes=c,
+                                                     scales=s_)
+    out.append(("moe_quant_nvfp4[16384,2048]x128", make_moe4, nbm4, nbm4))
     x1 = to_gpu(W.mxfp8_linear_quant(), dev)
-    c, s = mxq.mx_quantize(x1, mxq.E4M3, mxq.LINEAR)
-    out.append(("quant_mxfp8_linear[128,4096]",
-                lambda c=c, s=s: mxq.mx_quantize(x1, mxq.E4M3, mxq.LINEAR, codes=c, scales=s),
-                3 * x1.numel() + s.numel()))
+    nb1 = 3 * x1.numel() + x1.numel() // 32
+
+    def make_c1(k):
+        x = cpy(x1, k)
+        c = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+        s_ = torch.empty((x.shape[0], x.shape[1] // 32), dtype=torch.uint8, device=dev)
+        return lambda: mxq.mx_quantize(x, mxq.E4M3, mxq.LINEAR, codes=c, scales=s_)
+    out.append(("quant_mxfp8_linear[128,4096]", make_c1, nb1, nb1))
     return out
 
 
@@ -646,23 +693,37 @@ def run_case(args):
     import mx_microscaling_quantize_gb300 as mxq
     from mx_microscaling_quantize_gb300 import workloads as W
     if args.case == "nonrotated_sweep":
-        variants = nonrotated_variants(dev)
-        for _, fn, _ in variants:  # warm-up: one launch of each
-            fn()
-        torch.cuda.synchronize()
+        # Each variant: its own buffer sets, together at least three times L2 (so that no launch
+        # finds its input in L2), one warm-up launch per set, then --steps launches cycling over
+        # the sets. No kernel of the library runs outside these launches, so under a profiler
+        # the launches come in this order: every variant's warm-up launches, then its timed ones,
+        # variant after variant.
+        l2 = 129 * 10 ** 6
         res = {}
-        for name, fn, nbytes in variants:
+        order = []
+        for name, make, nbytes, footprint in nonrotated_variants(dev):
+            sets = max(1, min(64, -(-3 * l2 // footprint)))
+            fns = [make(k) for k in range(sets)]
+            for fn in fns:
+                fn()
+            torch.cuda.synchronize()
+            steps = max(1, args.steps)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            for _ in range(max(1, args.steps)):
-                fn()
+            for i in range(steps):
+                fns[i % sets]()
             b.record()
             b.synchronize()
-            t = a.elapsed_time(b) / 1e3 / max(1, args.steps)
+            t = a.elapsed_time(b) / 1e3 / steps
             res[name] = {"us_per_launch": t * 1e6, "GB/s": nbytes / t / 1e9,
-                         "algorithmic_bytes": nbytes}
+                         "algorithmic_bytes": nbytes, "warmup_launches": sets,
+                         "timed_launches": steps}
+            order.append(name)
+            del fns
         print(json.dumps({"case": args.case, "what": CASES[args.case], "variants": res,
-                          "gpu_launches": len(variants) * (1 + max(1, args.steps))}), flush=True)
+                          "launch_order": order,
+                          "gpu_launches": sum(v["warmup_launches"] + v["timed_launches"]
+                                              for v in res.values())}), flush=True)
         return
     if args.case == "mxfp8_linear_quant":
         x = to_gpu(W.mxfp8_linear_quant(), dev)

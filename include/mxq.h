@@ -79,11 +79,12 @@ typedef int mx_status;
  *  MX_ROT_HADAMARD: the caller states that H = c * S_g, where S_g is the Sylvester Hadamard
  *    matrix of order g (S_1 = [1], S_2n = [[S_n, S_n], [S_n, -S_n]], entry (i, j) =
  *    (-1)^popcount(i & j)) and c = H[0][0], e.g. the normalized hadamard(g) * g^-0.5 rounded
- *    to bf16. The product is then a fast Walsh-Hadamard transform in registers (log2 g
- *    butterfly stages in fp32, then a multiplication by c) on the streaming kernel. Every
- *    CTA checks the statement on the bit patterns of H on the device; where it does not hold
- *    the call computes sum_i x_i H[i][j] with fp32 FMAs instead, so the results are correct
- *    for any H (only slower).
+ *    to bf16. For g <= 64 the product is then a fast Walsh-Hadamard transform in registers
+ *    (log2 g butterfly stages in fp32, then a multiplication by c) on the streaming kernel.
+ *    Every CTA checks the statement on the bit patterns of H on the device; where it does not
+ *    hold the call computes sum_i x_i H[i][j] with fp32 FMAs instead, so the results are
+ *    correct for any H (only slower). For g = 128 the call runs as MX_ROT_DENSE (faster
+ *    there).
  * Both kinds compute the same rotation up to fp32 rounding (well inside the 1e-5 normwise
  * tolerance of the rotated path).
  */

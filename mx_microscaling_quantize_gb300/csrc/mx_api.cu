@@ -17,6 +17,10 @@ bool valid_fmt(int fmt) { return fmt == MX_FMT_E2M1 || fmt == MX_FMT_E4M3; }
 bool valid_layout(int layout) { return layout == MX_SCALES_LINEAR || layout == MX_SCALES_SWIZZLED; }
 bool valid_g(int g) { return g == 16 || g == 32 || g == 64 || g == 128; }
 bool valid_rot_kind(int k) { return k == MX_ROT_DENSE || k == MX_ROT_HADAMARD; }
+// The Walsh-Hadamard kernel takes MX_ROT_HADAMARD calls for g <= 64. For g = 128 its two
+// shuffle stages made it 19-42% slower than the tensor-core kernel on every measured shape, so
+// those calls run there (which takes any H).
+bool use_fwht(int rot_kind, int g) { return rot_kind == MX_ROT_HADAMARD && g <= 64; }
 
 // Checks shared by every call on an [M, K] bf16 input. Returns MX_OK to go on; *empty is set
 // when there is nothing to compute.
@@ -136,7 +140,7 @@ mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int ro
   if (!aligned32(x) || !aligned32(y)) return MX_ERR_ALIGN;
   if (H) {
     if (!aligned16(H)) return MX_ERR_ALIGN;
-    if (rot_kind == MX_ROT_HADAMARD) {
+    if (use_fwht(rot_kind, g)) {
       mxq::StreamArgs a = stream_args(x, M, K, y);
       a.H = H;
       return from_cuda(mxq::launch_hadamard(fmt, mxq::kRotQdq, false, g, a,
@@ -183,7 +187,7 @@ mx_status mx_rotate_quantize(const void* x, int64_t M, int64_t K, const void* H,
   if (!aligned32(x) || !aligned32(codes)) return MX_ERR_ALIGN;
   if (layout == MX_SCALES_SWIZZLED && !aligned16(scales)) return MX_ERR_ALIGN;
   if (!aligned16(H)) return MX_ERR_ALIGN;
-  if (rot_kind == MX_ROT_HADAMARD) {
+  if (use_fwht(rot_kind, g)) {
     mxq::StreamArgs a = stream_args(x, M, K, codes);
     a.scales = static_cast<uint8_t*>(scales);
     a.scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : ceil_div(K, mxq::kTileCols) * 4;
@@ -276,7 +280,7 @@ mx_status mx_quantize_nvfp4(const void* x, int64_t M, int64_t K, const void* H, 
   int64_t srows = 0, scols = 0;
   mx_nvfp4_scales_shape(M, K, layout, &srows, &scols);
   const bool swz = layout == MX_SCALES_SWIZZLED;
-  if (H && rot_kind == MX_ROT_HADAMARD) {
+  if (H && use_fwht(rot_kind, g)) {
     mxq::StreamArgs a = stream_args(x, M, K, codes);
     a.scales = static_cast<uint8_t*>(scales);
     a.scale_cols = scols;
@@ -310,7 +314,7 @@ mx_status mx_qdq_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g
   if (st != MX_OK || empty) return st;
   if (!y) return MX_ERR_NULL;
   if (!aligned32(y)) return MX_ERR_ALIGN;
-  if (H && rot_kind == MX_ROT_HADAMARD) {
+  if (H && use_fwht(rot_kind, g)) {
     mxq::StreamArgs a = stream_args(x, M, K, y);
     a.gscale = global_scale;
     a.H = H;
@@ -411,7 +415,7 @@ mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, in
   if (!x || !H || !y_f32) return MX_ERR_NULL;
   if (!aligned32(x) || !aligned32(y_f32)) return MX_ERR_ALIGN;
   if (!aligned16(H)) return MX_ERR_ALIGN;
-  if (rot_kind == MX_ROT_HADAMARD) {
+  if (use_fwht(rot_kind, g)) {
     mxq::StreamArgs a = stream_args(x, M, K, y_f32);
     a.H = H;
     return from_cuda(mxq::launch_hadamard(MX_FMT_E2M1, mxq::kRotDebug, false, g, a,

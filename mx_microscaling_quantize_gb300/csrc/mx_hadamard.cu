@@ -12,14 +12,16 @@
 // so the results are the rotation's for any H, only slower.
 //
 // Layout: as in mx_stream.cu, the input is a flat sequence of 32-element blocks, a persistent
-// grid walks them with a grid stride, consecutive threads own consecutive blocks (a warp moves
-// 2 KiB of contiguous input) and each thread loads its next block before working on the
-// current one. A chunk never crosses a row (K % g == 0) and starts at a multiple of g in the
-// flat order, so a g = 16 or 32 chunk lies inside one thread's block and a g = 64 / 128 chunk
-// spans 2 / 4 consecutive lanes, whose butterfly stages exchange values with shuffles. The
-// loop's trip count is the same for every lane of a warp (lanes past the end compute on zeros
-// and store nothing), so the shuffles always have the whole warp. After the rotation the
-// block's fp32 values take the same quantization steps as in the tensor-core kernel.
+// grid walks them with a grid stride and consecutive threads own consecutive blocks (a warp moves
+// 2 KiB of contiguous input) and each thread loads its next block before working on the current
+// one. A chunk never
+// crosses a row (K % g == 0) and starts at a multiple of g in the flat order, so a g = 16 or 32
+// chunk lies inside one thread's block and a g = 64 / 128 chunk spans 2 / 4 consecutive lanes,
+// whose butterfly stages exchange values with shuffles. The loop's trip count is the same for
+// every lane of a warp (lanes past the end compute on zeros and store nothing), so the shuffles
+// always have the whole warp. After the rotation the block's fp32 values take the same
+// quantization steps as in the tensor-core kernel; for the MX formats the factor c is folded
+// into the power-of-two scaling (exact, see mx_hadamard_block).
 #include "mx_device.cuh"
 #include "mx_launch.h"
 
@@ -52,23 +54,35 @@ __device__ __forceinline__ bool is_scaled_sylvester(const uint16_t* H, uint32_t 
   return __syncthreads_and(ok) != 0;
 }
 
+// (a0, a1) <- (a0 + b0, a1 + b1) and (b0, b1) <- (a0 - b0, a1 - b1) with packed fp32 operations
+// (each element rounded once, as the scalar operations would).
+__device__ __forceinline__ void addsub2(float& a0, float& a1, float& b0, float& b1) {
+  asm("{\n\t.reg .b64 a, b, s, d;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 b, {%2, %3};\n\t"
+      "add.rn.f32x2 s, a, b;\n\tsub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, s;\n\t"
+      "mov.b64 {%2, %3}, d;\n\t}"
+      : "+f"(a0), "+f"(a1), "+f"(b0), "+f"(b1));
+}
+
 // v <- S_G v over every G-chunk of the warp's values (unnormalized fast Walsh-Hadamard
 // transform). Stage h pairs the elements i and i + h of a chunk ((i & h) == 0) into
-// (v_i + v_{i+h}, v_i - v_{i+h}). Stages inside a thread first; for G = 64 / 128 the element
+// (v_i + v_{i+h}, v_i - v_{i+h}); stage 1 pairs neighbours (scalar), stages h >= 2 take two
+// neighbouring pairs at once (packed). Stages inside a thread first; for G = 64 / 128 the element
 // index i = 32 * (lane within the chunk) + t, so stage h = 32 / 64 pairs lane bit 1 / 2: the
 // lower lane keeps its value plus its partner's, the upper lane its partner's minus its own.
 template <int G>
 __device__ __forceinline__ void fwht(float* v, int lane) {
   constexpr int kIn = G < 32 ? G : 32;
 #pragma unroll
-  for (int h = 1; h < kIn; h <<= 1) {
+  for (int i = 0; i < 32; i += 2) {
+    const float a = v[i], b = v[i + 1];
+    v[i] = a + b;
+    v[i + 1] = a - b;
+  }
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if ((i & h) == 0) {
-        const float a = v[i], b = v[i + h];
-        v[i] = a + b;
-        v[i + h] = a - b;
-      }
+  for (int h = 2; h < kIn; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      if ((i & h) == 0) addsub2(v[i], v[i + 1], v[i + h], v[i + h + 1]);
     }
   }
 #pragma unroll
@@ -135,11 +149,63 @@ __device__ __forceinline__ void dense_rotate(float* v, const uint16_t* H, int la
   for (int j = 0; j < 32; ++j) v[j] = acc[j];
 }
 
-// L2 prefetch spans (2 KiB each) per warp before pdl_wait, as in the streaming kernels.
-constexpr int kPrefetchSpans = 1;
+// MX block of the unscaled transform s (y = c * s): returns the E8M0 byte and writes the QDQ
+// output or the codes. The abs-max of y is |c| * max |s_j| rounded once (rounding is monotonic
+// and symmetric, so this is max_j |fl(c s_j)|), and the values are scaled by q = c * 2^-s in one
+// multiplication: fl(s_j q) = fl(c s_j) * 2^-s exactly while q is a normal number (the scaling
+// by a power of two is exact); otherwise the two multiplications are done in turn.
+template <int FMT, bool QDQ>
+__device__ __forceinline__ uint32_t mx_hadamard_block(float* v, float c, uint32_t* out) {
+  const float amax_s = __uint_as_float(absmax_f32x32(v));
+  const float amax = __fmul_rn(fabsf(c), amax_s);
+  const uint32_t byte = scale_byte_from_amax_bits<FMT>(__float_as_uint(amax) & 0x7FFFFFFFu);
+  const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);
+  const float inv = inv_scale_of(byte);
+  const float q = __fmul_rn(c, inv);
+  if (fabsf(q) >= 1.17549435e-38f || c == 0.0f) {  // q normal (or zero): one exact step
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mul2(v[2 * i], v[2 * i + 1], q);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      mul2(v[2 * i], v[2 * i + 1], c);
+      mul2(v[2 * i], v[2 * i + 1], inv);
+    }
+  }
+  if (QDQ) {
+    const float sc = scale_of(byte);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) out[i] = qdq2<FMT>(v[2 * i], v[2 * i + 1], sc);
+  } else if (FMT == kFmtE2M1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = codes8_e2m1(v + 8 * i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint2 cc = codes8_e4m3(v + 8 * i);
+      out[2 * i] = cc.x;
+      out[2 * i + 1] = cc.y;
+    }
+  }
+  if (special && byte == 255u) {
+    const uint32_t fill = QDQ ? kBf16NaNx2 : (FMT == kFmtE2M1 ? 0u : kE4M3NaNx4);
+#pragma unroll
+    for (int i = 0; i < (QDQ ? 16 : (FMT == kFmtE2M1 ? 4 : 8)); ++i) out[i] = fill;
+  }
+  return byte;
+}
+
+// CTAs per SM the register budget is set for: QDQ (two 32-byte stores per block, the widest
+// epilogue) 2, which measured 6-8% faster than 3 (its 80-register build spills); codes 3, 5-10%
+// faster than 2 (rotated MXFP8 x[8192, 28672]: 115.2 -> 109.1 us).
+template <int OUT>
+__host__ __device__ constexpr int hadamard_min_ctas() {
+  return OUT == kRotQdq ? 2 : 3;
+}
 
 template <int FMT, int OUT, bool SWZ, int G>
-__global__ void __launch_bounds__(kThreads, 2) mx_hadamard_kernel(StreamArgs a) {
+__global__ void __launch_bounds__(kThreads, hadamard_min_ctas<OUT>())
+    mx_hadamard_kernel(StreamArgs a) {
   constexpr bool kNv = FMT == kFmtNVFP4;
   constexpr bool kQdq = OUT == kRotQdq;
   // output bytes per 32-element block: QDQ bf16 64, E4M3 codes 32, E2M1 codes 16, debug fp32 128
@@ -152,18 +218,9 @@ __global__ void __launch_bounds__(kThreads, 2) mx_hadamard_kernel(StreamArgs a) 
   const int64_t nblk = a.M * cblk;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   pdl_launch_dependents();
-  {
-    const int64_t w0 = (int64_t)blockIdx.x * kThreads + (tid & ~31);
-    if (lane == 0) {
-#pragma unroll
-      for (int d = 0; d < kPrefetchSpans; ++d) {
-        const int64_t s0 = w0 + d * stride;
-        if (s0 < nblk) {
-          const int64_t n = nblk - s0 < 32 ? nblk - s0 : 32;
-          prefetch_l2(x + s0 * 64, (uint32_t)(n * 64));
-        }
-      }
-    }
+  if (lane == 0) {  // the warp's first 2 KiB into L2 (a hint, see prefetch_l2)
+    const int64_t s0 = (int64_t)blockIdx.x * kThreads + (tid & ~31);
+    if (s0 < nblk) prefetch_l2(x + s0 * 64, (uint32_t)((nblk - s0 < 32 ? nblk - s0 : 32) * 64));
   }
   pdl_wait();
 
@@ -181,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 2) mx_hadamard_kernel(StreamArgs a) 
   const uint32_t c_bits = load_u16(H);
   const float c = __uint_as_float(c_bits << 16);
   const bool hadamard = is_scaled_sylvester<G>(H, c_bits);
+  const float cm = hadamard ? c : 1.0f;  // the dense product already holds the rotated values
   float gs = 0.0f, r6 = 0.0f;
   if (kNv && OUT != kRotDebug) {
     gs = load_f32(a.gscale);
@@ -206,13 +264,13 @@ __global__ void __launch_bounds__(kThreads, 2) mx_hadamard_kernel(StreamArgs a) 
     }
     if (hadamard) {
       fwht<G>(v, lane);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) mul2(v[2 * i], v[2 * i + 1], c);
     } else {
       dense_rotate<G>(v, H, lane, s_dense[tid >> 5]);
     }
     uint8_t* dst = static_cast<uint8_t*>(a.out) + b * kOutBytes;
     if constexpr (OUT == kRotDebug) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mul2(v[2 * i], v[2 * i + 1], cm);
       if (valid) {
         float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
@@ -222,11 +280,13 @@ __global__ void __launch_bounds__(kThreads, 2) mx_hadamard_kernel(StreamArgs a) 
       uint32_t o[16];
       uint32_t byte;
       if constexpr (kNv) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mul2(v[2 * i], v[2 * i + 1], cm);
         const NvScales n = nv_scales(absmax_f32x16(v), absmax_f32x16(v + 16), gs, r6);
         nv_block_f32<kQdq>(v, o, n);
         byte = n.bytes;
       } else {
-        byte = mx_block_f32<FMT, kQdq>(v, o);
+        byte = mx_hadamard_block<FMT, kQdq>(v, cm, o);
       }
       if (valid) {
         if (kQdq) {
@@ -288,7 +348,7 @@ cudaError_t launch_g(int g, const StreamArgs& a, cudaStream_t st) {
     case 16: return launch_t<FMT, OUT, SWZ, 16>(a, st);
     case 32: return launch_t<FMT, OUT, SWZ, 32>(a, st);
     case 64: return launch_t<FMT, OUT, SWZ, 64>(a, st);
-    default: return launch_t<FMT, OUT, SWZ, 128>(a, st);
+    default: return cudaErrorInvalidValue;  // g = 128 calls run on the tensor-core kernel
   }
 }
 

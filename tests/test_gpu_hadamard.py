@@ -6,7 +6,8 @@ so the rotated-path tolerance rules of mx_testlib apply unchanged: pre-quantizat
 within 1e-5 of the chunk norm, codes different only next to rounding midpoints, scale bytes one
 step off only next to the power of two that the step crosses. A matrix that is not a scaled
 Sylvester Hadamard takes the kernel's dense fp32-FMA product instead; with H = I that product
-is exact, so the results equal the plain path's bit for bit.
+is exact, so the results equal the plain path's bit for bit. With g = 128 the Hadamard-hinted
+calls run on the tensor-core kernel (faster there), and the same tests hold for them.
 """
 
 import numpy as np
