@@ -400,19 +400,22 @@ def extra_workloads(dev, peak):
             measure(f"{fname}_qdq_{name}", 4 * x.numel(), x.numel(), make, 4 * x.numel())
         del x, y
 
-    # fused rotate + MXFP4 quantize, g = 32 Hadamard, swizzled scales
+    # fused rotate + MXFP4 quantize, g = 32 Hadamard, swizzled scales: on the tensor cores
+    # (rot_kind ROT_DENSE, any H) and with the Hadamard statement (ROT_HADAMARD: in-register
+    # Walsh-Hadamard transform)
     H = to_gpu(W.normalized_hadamard_bf16(32), dev)
+    kinds = ((mxq.ROT_DENSE, ""), (mxq.ROT_HADAMARD, "_hadamard"))
     for K in W.ROTATE_QUANT_K:
         for M in W.ROTATE_QUANT_M:
             x = to_gpu(W.rotate_quant_activation(M, K), dev)
             c, s = mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED)
-
-            def make(k, x=x, c=c, s=s):
-                xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
-                return lambda: mxq.mx_rotate_quantize(xk, H, mxq.E2M1, mxq.SWIZZLED, codes=ck,
-                                                      scales=sk)
-            nb = 2 * x.numel() + c.numel() + s.numel()
-            measure(f"rotate_quant_mxfp4_g32[{M},{K}]", nb, x.numel(), make, nb)
+            for rk, kname in kinds:
+                def make(k, x=x, c=c, s=s, rk=rk):
+                    xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+                    return lambda: mxq.mx_rotate_quantize(xk, H, mxq.E2M1, mxq.SWIZZLED, codes=ck,
+                                                          scales=sk, rot_kind=rk)
+                nb = 2 * x.numel() + c.numel() + s.numel()
+                measure(f"rotate_quant_mxfp4_g32{kname}[{M},{K}]", nb, x.numel(), make, nb)
             del x, c, s
 
     # weight-side rotate + quantize of the 70B layer weights, g = 32, swizzled scales
@@ -420,13 +423,14 @@ def extra_workloads(dev, peak):
         x = to_gpu(W.weight_rotate_quant(N, K), dev)
         for fmt, fname in ((mxq.E2M1, "mxfp4"), (mxq.E4M3, "mxfp8")):
             c, s = mxq.mx_rotate_quantize(x, H, fmt, mxq.SWIZZLED)
-
-            def make(k, x=x, c=c, s=s, fmt=fmt):
-                xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
-                return lambda: mxq.mx_rotate_quantize(xk, H, fmt, mxq.SWIZZLED, codes=ck,
-                                                      scales=sk)
-            nb = 2 * x.numel() + c.numel() + s.numel()
-            measure(f"weight_rotate_quant_{fname}_g32[{N},{K}]", nb, x.numel(), make, nb, iters=15)
+            for rk, kname in kinds:
+                def make(k, x=x, c=c, s=s, fmt=fmt, rk=rk):
+                    xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+                    return lambda: mxq.mx_rotate_quantize(xk, H, fmt, mxq.SWIZZLED, codes=ck,
+                                                          scales=sk, rot_kind=rk)
+                nb = 2 * x.numel() + c.numel() + s.numel()
+                measure(f"weight_rotate_quant_{fname}_g32{kname}[{N},{K}]", nb, x.numel(), make,
+                        nb, iters=15)
             del c, s
         del x
 
@@ -538,11 +542,13 @@ def extra_workloads(dev, peak):
         for g in W.ROTATION_SWEEP_G:
             Hg = to_gpu(W.normalized_hadamard_bf16(g), dev)
             for fmt, fname in ((mxq.E2M1, "mxfp4"), (mxq.E4M3, "mxfp8")):
-                def make(k, x=x, y=y, Hg=Hg, fmt=fmt):
-                    xk, yk = copy_of(x, k), empty_of(y, k)
-                    return lambda: mxq.mx_qdq(xk, fmt, Hg, y=yk)
-                measure(f"rotated_qdq_{fname}_g{g}_{lname}[{M},{K}]", 4 * x.numel(), x.numel(),
-                        make, 4 * x.numel(), iters=15)
+                # ROT_HADAMARD with g = 128 runs on the tensor cores, as ROT_DENSE
+                for rk, kname in (kinds if g <= 64 else kinds[:1]):
+                    def make(k, x=x, y=y, Hg=Hg, fmt=fmt, rk=rk):
+                        xk, yk = copy_of(x, k), empty_of(y, k)
+                        return lambda: mxq.mx_qdq(xk, fmt, Hg, y=yk, rot_kind=rk)
+                    measure(f"rotated_qdq_{fname}_g{g}{kname}_{lname}[{M},{K}]", 4 * x.numel(),
+                            x.numel(), make, 4 * x.numel(), iters=15)
         del x, y
     return out
 
