@@ -573,6 +573,10 @@ CASES = {
                      "torch's plain bf16 <-> float8_e4m3fn cast of the same bytes",
     "rotate_quant_tiles": "E2M1 rotate(g=32)+quantize, swizzled, x[128, 128 * SMs * n]: exactly "
                           "n = --tiles-per-sm tiles per SM, launches cycling over input copies",
+    "gemm": "block-scaled GEMM consumer C = dequant(A) dequant(B)^T (bf16 out) on the quantized "
+            "activation and weight workloads, MXFP4 and MXFP8, swizzled scales, at the o_proj, "
+            "down_proj, square and decode shapes; beside it torch.matmul (cuBLAS bf16) of the "
+            "dequantized operands, alone and after the two mx_dequantize calls",
     "nonrotated_sweep": "every non-rotated kernel at full workload size (quantize, QDQ, "
                         "dequantize, NVFP4, grouped MoE, the x[128,4096] MXFP8 quantize), each "
                         "launched --steps times back to back over buffer copies that exceed 3x "
@@ -731,6 +735,9 @@ def run_case(args):
                           "gpu_launches": sum(v["warmup_launches"] + v["timed_launches"]
                                               for v in res.values())}), flush=True)
         return
+    if args.case == "gemm":
+        run_gemm_case(args, dev)
+        return
     if args.case == "mxfp8_linear_quant":
         x = to_gpu(W.mxfp8_linear_quant(), dev)
         c, s = mxq.mx_quantize(x, mxq.E4M3, mxq.LINEAR)
@@ -868,6 +875,66 @@ def run_case(args):
                       "GB/s": nbytes / t / 1e9,
                       "gpu_launches": args.steps * (2 if args.case in ("qdq_vs_copy",
                                                                        "quant_vs_cast") else 1)}),
+          flush=True)
+
+
+def run_gemm_case(args, dev):
+    """TFLOP/s (2 M N K per call) of mx_gemm, launches back to back after --warmup, against the
+    measured bf16 tensor peak; the same product through cuBLAS on bf16 operands for context."""
+    import torch
+    import mx_microscaling_quantize_gb300 as mxq
+    from mx_microscaling_quantize_gb300 import workloads as W
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = peaks.get("bf16_tflops", 1900.0)
+    shapes = [("o_proj", 4096, 8192, 8192), ("down_proj", 1024, 8192, 28672),
+              ("square", 8192, 8192, 8192), ("decode", 16, 8192, 8192)]
+    steps = max(1, args.steps)
+
+    def clock(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            fn()
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b) / 1e3 / steps
+
+    res = {}
+    launches = 0
+    for name, M, N, K in shapes:
+        xa = to_gpu(W.mxfp4_qdq_activation(M, K), dev)
+        xw = to_gpu(W.weight_rotate_quant(N, K), dev)
+        for fmt, fname in ((mxq.E2M1, "mxfp4"), (mxq.E4M3, "mxfp8")):
+            ca, sa = mxq.mx_quantize(xa, fmt, mxq.SWIZZLED)
+            cw, sw = mxq.mx_quantize(xw, fmt, mxq.SWIZZLED)
+            c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            t = clock(lambda: mxq.mx_gemm(ca, sa, cw, sw, K, fmt, mxq.SWIZZLED, c=c))
+            da = mxq.mx_dequantize(ca, sa, K, fmt, mxq.SWIZZLED)
+            dw = mxq.mx_dequantize(cw, sw, K, fmt, mxq.SWIZZLED)
+            t_mm = clock(lambda: torch.matmul(da, dw.t(), out=c))
+
+            def two_step():
+                mxq.mx_dequantize(ca, sa, K, fmt, mxq.SWIZZLED, y=da)
+                mxq.mx_dequantize(cw, sw, K, fmt, mxq.SWIZZLED, y=dw)
+                torch.matmul(da, dw.t(), out=c)
+            t_two = clock(two_step)
+            launches += 4 + 3 * (max(3, args.warmup) + steps)
+            flops = 2.0 * M * N * K
+            res[f"{name}_{fname}"] = {
+                "M": M, "N": N, "K": K, "us": t * 1e6, "TFLOP/s": flops / t / 1e12,
+                "frac_of_bf16_peak": flops / t / 1e12 / peak,
+                "cublas_bf16_us": t_mm * 1e6, "cublas_bf16_TFLOP/s": flops / t_mm / 1e12,
+                "dequant_then_cublas_us": t_two * 1e6}
+            del ca, sa, cw, sw, c, da, dw
+        del xa, xw
+        torch.cuda.empty_cache()
+    print(json.dumps({"case": args.case, "what": CASES[args.case], "bf16_peak_TFLOP/s": peak,
+                      "peak_source": "measured bf16_tflops (cuBLAS burst)" if peaks else
+                      "fallback", "steps": steps, "shapes": res, "gpu_launches": launches}),
           flush=True)
 
 

@@ -234,6 +234,26 @@ mx_status mx_dequantize_nvfp4(const void* codes, const void* scales, int64_t M, 
                               const float* global_scale, int layout, void* y, void* stream);
 
 /*
+ * Block-scaled GEMM consumer (pages: the QuTLASS review thread on vLLM's MXFP4 test, which runs
+ * matmul_mxf4_bf16_tn(a_e2m1, b_e2m1, a_e8m0, b_e8m0, alpha) on the quantizer's outputs and
+ * compares it with the matmul of the dequantized operands `_dq_fp4(...)`):
+ *   C[i][j] = alpha * sum_k dequant(A)[i][k] * dequant(B)[j][k]   ("TN": both K-major),
+ * dequant as in mx_dequantize (decode(code) * 2^(scale_byte - 127) rounded to bf16 once: exact
+ * for every E2M1 value and for E4M3 unless below the bf16 range), products exact, sums in fp32
+ * on the tensor cores, C rounded to bf16 once. A: codes [M, K/2] (E2M1) or [M, K] (E4M3) with
+ * scales [M, K/32] (linear) or the 128x4 blocked layout of mx_scales_shape(M, K) (swizzled), as
+ * mx_quantize writes them; B likewise with N rows; both in the same fmt and layout. C: bf16
+ * [M, N] row-major, must not overlap the inputs. K % 64 == 0 (K > 0), N % 8 == 0; codes and C
+ * 16-byte aligned, swizzled scales 16-byte aligned. A scale byte 0xFF makes its 32 values NaN.
+ * M <= 8,388,480 (65,535 tiles of 128 rows). M == 0 or N == 0 is a no-op returning MX_OK.
+ * Errors: see conventions; K not a positive multiple of 64, N % 8 or M too large ->
+ * MX_ERR_SHAPE.
+ */
+mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes,
+                  const void* b_scales, int64_t M, int64_t N, int64_t K, int fmt, int group,
+                  int layout, float alpha, void* c, void* stream);
+
+/*
  * Diagnostics: the rotated values y = x_chunk * H exactly as mx_rotate_quantize computes them
  * before quantization with the same rot_kind (same device code), written as fp32 [M, K] to
  * y_f32 (device, 32-byte aligned).

@@ -33,7 +33,7 @@ EXPORTS = (
     "mx_rotate_quantize", "mx_quantize_grouped", "mx_dequantize", "mx_nvfp4_scales_shape",
     "mx_quantize_nvfp4", "mx_qdq_nvfp4", "mx_dequantize_nvfp4", "mx_nvfp4_grouped_scales_shape",
     "mx_quantize_nvfp4_grouped", "mx_rotate_debug", "mx_device_errors",
-    "mx_selftest_bounded_wait", "mx_selftest_rotate_give_up",
+    "mx_selftest_bounded_wait", "mx_selftest_rotate_give_up", "mx_gemm",
 )
 
 
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
         "mx_device_errors": (i32, [ctypes.POINTER(ctypes.c_int)]),
         "mx_selftest_bounded_wait": (i32, [i64, p]),
         "mx_selftest_rotate_give_up": (i32, [p, i64, i64, p, i32, p, p, i64, p]),
+        "mx_gemm": (i32, [p, p, p, p, i64, i64, i64, i32, i32, i32, ctypes.c_float, p, p]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -372,3 +373,22 @@ def mx_selftest_rotate_give_up(x, H, limit_ns: int, *, stream=None):
     _check(lib().mx_selftest_rotate_give_up(_ptr(x), M, K, _ptr(H), g, _ptr(codes), _ptr(scales),
                                             limit_ns, _stream_ptr(stream, x)))
     return codes, scales
+
+
+def mx_gemm(a_codes, a_scales, b_codes, b_scales, K: int, fmt, layout=SWIZZLED, alpha: float = 1.0,
+            *, c=None, group=GROUP, stream=None):
+    """C[M, N] = alpha * dequant(A) @ dequant(B)^T (bf16) from MX codes and E8M0 scales as
+    mx_quantize returns them (A: [M, K/2 or K] codes, B: [N, ...])."""
+    for t in (a_codes, a_scales, b_codes, b_scales):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.uint8
+                and t.is_contiguous()):
+            raise TypeError("codes and scales must be contiguous CUDA uint8 tensors")
+    M, N = a_codes.shape[0], b_codes.shape[0]
+    if a_codes.numel() != M * code_bytes_per_row(fmt, K) or \
+            b_codes.numel() != N * code_bytes_per_row(fmt, K):
+        raise ValueError("codes do not match K and the format")
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
+    _check(lib().mx_gemm(_ptr(a_codes), _ptr(a_scales), _ptr(b_codes), _ptr(b_scales), M, N, K,
+                         fmt, group, layout, alpha, _ptr(c), _stream_ptr(stream, a_codes)))
+    return c

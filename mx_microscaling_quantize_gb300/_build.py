@@ -18,8 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmxq.so")
-SOURCES = ("mx_api.cu", "mx_stream.cu", "mx_dequant.cu", "mx_rotate.cu", "mx_hadamard.cu")
-HEADERS = ("mx_device.cuh", "mx_launch.h")
+SOURCES = ("mx_api.cu", "mx_stream.cu", "mx_dequant.cu", "mx_rotate.cu", "mx_hadamard.cu",
+           "mx_gemm.cu")
+HEADERS = ("mx_device.cuh", "mx_launch.h", "mx_tcgen05.cuh")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

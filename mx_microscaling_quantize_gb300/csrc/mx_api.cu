@@ -426,6 +426,38 @@ mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, in
                                       static_cast<cudaStream_t>(stream)));
 }
 
+mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes,
+                  const void* b_scales, int64_t M, int64_t N, int64_t K, int fmt, int group,
+                  int layout, float alpha, void* c, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return MX_ERR_SHAPE;
+  if (group != 32 || !valid_fmt(fmt) || !valid_layout(layout)) return MX_ERR_UNSUPPORTED;
+  if (K == 0 || K % 64 != 0 || N % 8 != 0) return MX_ERR_SHAPE;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return MX_ERR_SHAPE;
+  if (M > (int64_t(1) << 40) / K || N > (int64_t(1) << 40) / K) return MX_ERR_SHAPE;
+  if (ceil_div(M, 128) > 65535) return MX_ERR_SHAPE;  // 128-row tiles on the grid's y axis
+  if (M == 0 || N == 0) return MX_OK;
+  if (!a_codes || !a_scales || !b_codes || !b_scales || !c) return MX_ERR_NULL;
+  if (!aligned16(a_codes) || !aligned16(b_codes) || !aligned16(c)) return MX_ERR_ALIGN;
+  if (layout == MX_SCALES_SWIZZLED && (!aligned16(a_scales) || !aligned16(b_scales))) {
+    return MX_ERR_ALIGN;
+  }
+  mxq::GemmArgs a{};
+  a.a_codes = a_codes;
+  a.a_scales = static_cast<const uint8_t*>(a_scales);
+  a.b_codes = b_codes;
+  a.b_scales = static_cast<const uint8_t*>(b_scales);
+  a.c = c;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.a_scale_cols = a.b_scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : ceil_div(K, mxq::kTileCols) * 4;
+  a.alpha = alpha;
+  cudaError_t err = mxq::device_error_word(&a.err);
+  if (err != cudaSuccess) return from_cuda(err);
+  return from_cuda(mxq::launch_gemm(fmt, layout == MX_SCALES_SWIZZLED, a,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
 mx_status mx_selftest_bounded_wait(int64_t limit_ns, void* stream) {
   if (limit_ns <= 0 || limit_ns > 100000000) return MX_ERR_SHAPE;
   return from_cuda(mxq::launch_wait_selftest((unsigned long long)limit_ns,

@@ -90,6 +90,28 @@ struct RotArgs {
 cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const RotArgs& a,
                           cudaStream_t stream);
 
+struct GemmArgs {
+  const void* a_codes;      // A: E2M1 [M, K/2] or E4M3 [M, K] codes
+  const uint8_t* a_scales;  // A's E8M0 scales, linear [M, K/32] or swizzled
+  const void* b_codes;      // B: [N, K/2] or [N, K] codes
+  const uint8_t* b_scales;
+  void* c;                  // bf16 [M, N]
+  int64_t M;
+  int64_t N;
+  int64_t K;
+  int64_t a_scale_cols;     // columns of A's / B's scale matrix (linear: K/32; swizzled: padded)
+  int64_t b_scale_cols;
+  float alpha;
+  unsigned int* err;        // device error word (device_error_word)
+};
+
+// C = alpha * dequant(A) * dequant(B)^T on the tensor cores (fmt: 1 = E2M1, 2 = E4M3).
+cudaError_t launch_gemm(int fmt, bool swizzled, const GemmArgs& a, cudaStream_t stream);
+
+// Device address of the current device's error word, for kernels outside the file that defines
+// it (looked up once per device).
+cudaError_t device_error_word(unsigned int** word);
+
 // Reads and clears the device error word of the current device (synchronizes).
 cudaError_t read_device_errors(unsigned int* flags);
 

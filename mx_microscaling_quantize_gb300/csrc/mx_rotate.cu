@@ -39,12 +39,15 @@
 
 #include "mx_device.cuh"
 #include "mx_launch.h"
+#include "mx_tcgen05.cuh"
 
 namespace mxq {
 
 __device__ unsigned int g_device_errors;
 
 namespace {
+
+using namespace tc;
 
 constexpr int kAcc = 4;  // fp32 accumulators in TMEM (128 columns each)
 constexpr int kBoxCols = 64;                  // bf16 per 128-byte swizzled row
@@ -54,7 +57,6 @@ constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue
 constexpr int kTmemCols = 128 * kAcc;             // all 512 columns of the SM
-constexpr uint32_t kErrWaitTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 // Tiles per CTA prefetched into L2 before pdl_wait (64 KiB per SM). Measured on GB300 (steady,
 // back to back, rotate+quantize E2M1 g = 32): 1.0-1.2 us less per launch with 2 tiles
@@ -62,71 +64,14 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 // less on most shapes, all 6 ring stages nothing (they compete with the previous kernel).
 constexpr int kPrefetchTiles = 2;
 
-// ------------------------------------------------------------------------------------------
-// PTX wrappers
-// ------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t slot_addr, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_addr),
-               "r"(ncols));
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, P;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-// Wait for the phase of the given parity; gives up after limit_ns (kWaitLimitNs in the
-// kernels), and at once once this thread has given up before (*failed). A give-up sets the
+// Bounded mbarrier wait of this file's kernels: gives up after limit_ns (kWaitLimitNs by
+// default), and at once once this thread has given up before (*failed); a give-up sets the
 // device error word.
 __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, bool* failed,
                                           unsigned long long limit_ns = kWaitLimitNs) {
-  if (*failed || mbar_try_wait(bar, parity)) return;
-  const unsigned long long t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > limit_ns) {
-      *failed = true;
-      atomicOr(&g_device_errors, kErrWaitTimeout);
-      return;
-    }
-  }
+  tc::mbar_wait(bar, parity, failed, limit_ns, &g_device_errors);
 }
+
 // L2 policy for data touched once (inputs read once, outputs written once): evict first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
@@ -182,53 +127,6 @@ __device__ __forceinline__ void load_tile(const RotArgs& a, const CUtensorMap* m
   tma_load_2d(dst + kBoxBytes, map, (int)(cb * kTileCols + kBoxCols), (int)(rb * kTileRows), bar);
 }
 
-// Shared-memory matrix descriptors (5th-generation tensor core format: start >> 4 at bits
-// 0-13, leading byte offset >> 4 at 16-29, stride byte offset >> 4 at 32-45, bit 46 set,
-// swizzle mode at 61-63).
-__device__ __forceinline__ uint64_t desc_noswizzle(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
-         ((uint64_t)(sbo >> 4) << 32) | (1ull << 46);
-}
-// K-major, 128-byte swizzle: 8-row groups 1024 bytes apart (the leading offset is unused).
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
-  return (uint64_t)((addr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         (1ull << 46) | (2ull << 61);
-}
-// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B bf16 (bits 7-9
-// and 10-12 = 1), both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::
-                   "r"(bar)
-               : "memory");
-}
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* y) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(r[i]);
-}
 __device__ __forceinline__ void epilogue_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }
@@ -935,6 +833,24 @@ cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const Rot
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream) {
   mx_wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
   return cudaGetLastError();
+}
+
+cudaError_t device_error_word(unsigned int** word) {
+  static std::mutex mu;
+  static unsigned int* cache[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_device_errors);
+    if (err != cudaSuccess) return err;
+    cache[dev] = static_cast<unsigned int*>(p);
+  }
+  *word = cache[dev];
+  return cudaSuccess;
 }
 
 cudaError_t read_device_errors(unsigned int* flags) {

@@ -265,6 +265,23 @@ def quantize_grouped(x_bits, offsets, fmt: int, layout: int, scale_rows: int | N
     return codes, scales
 
 
+def bf16_bits_to_double(bits) -> np.ndarray:
+    """bf16 bit patterns -> float64 values (exact: a bf16 is the upper half of an fp32)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def gemm(a_codes, a_scales, b_codes, b_scales, K: int, fmt: int, layout: int,
+         alpha: float = 1.0) -> np.ndarray:
+    """Block-scaled GEMM of stored MX data, float64 [M, N]:
+    alpha * dequantize(A) @ dequantize(B)^T, A and B dequantized by ``dequantize`` (each value
+    decode(code) * 2^(scale byte - 127) rounded to bf16 once) and multiplied in float64 (the
+    QuTLASS MXFP4 test's reference: the matmul of the dequantized operands)."""
+    da = bf16_bits_to_double(dequantize(a_codes, a_scales, K, fmt, layout))
+    db = bf16_bits_to_double(dequantize(b_codes, b_scales, K, fmt, layout))
+    return alpha * (da @ db.T)
+
+
 # ----------------------------------------------------------------------------------------------
 # NVFP4: E2M1 codes in blocks of 16, E4M3 block scales under an fp32 global scale gs
 # ----------------------------------------------------------------------------------------------

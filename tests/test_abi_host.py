@@ -246,6 +246,31 @@ def test_selftest_rotate_give_up_validation(L):
     assert f(P + 16, 128, 256, P, 32, P, P, 1000, None) == ALIGN    # x 32-byte aligned
 
 
+def test_gemm_validation(L):
+    f = L.mx_gemm  # (a_codes, a_scales, b_codes, b_scales, M, N, K, fmt, group, layout, alpha, c, stream)
+    assert f(P, P, P, P, 128, 128, 96, 1, 32, 1, 1.0, P, None) == SHAPE     # K % 64
+    assert f(P, P, P, P, 128, 128, 0, 1, 32, 1, 1.0, P, None) == SHAPE      # K == 0
+    assert f(P, P, P, P, 128, 100, 64, 1, 32, 1, 1.0, P, None) == SHAPE     # N % 8
+    assert f(P, P, P, P, -1, 128, 64, 1, 32, 1, 1.0, P, None) == SHAPE
+    assert f(P, P, P, P, 65535 * 128 + 1, 8, 64, 1, 32, 1, 1.0, P, None) == SHAPE
+    assert f(P, P, P, P, 1 << 34, 8, 64, 1, 32, 1, 1.0, P, None) == SHAPE
+    assert f(P, P, P, P, 128, 128, 64, 3, 32, 1, 1.0, P, None) == UNSUP     # fmt (NVFP4 is 3)
+    assert f(P, P, P, P, 128, 128, 64, 1, 16, 1, 1.0, P, None) == UNSUP     # group
+    assert f(P, P, P, P, 128, 128, 64, 1, 32, 2, 1.0, P, None) == UNSUP     # layout
+    for i in range(5):
+        args = [P, P, P, P]
+        if i < 4:
+            args[i] = None
+        assert f(*args, 128, 128, 64, 1, 32, 1, 1.0, None if i == 4 else P, None) == NULL
+    assert f(P + 8, P, P, P, 128, 128, 64, 1, 32, 1, 1.0, P, None) == ALIGN
+    assert f(P, P, P + 8, P, 128, 128, 64, 2, 32, 1, 1.0, P, None) == ALIGN
+    assert f(P, P, P, P, 128, 128, 64, 1, 32, 1, 1.0, P + 2, None) == ALIGN
+    assert f(P, P + 1, P, P, 128, 128, 64, 1, 32, 1, 1.0, P, None) == ALIGN  # swizzled scales
+    assert f(P, P, P, P + 4, 128, 128, 64, 1, 32, 1, 1.0, P, None) == ALIGN
+    assert f(None, None, None, None, 0, 128, 64, 1, 32, 1, 1.0, None, None) == OK
+    assert f(None, None, None, None, 128, 0, 64, 2, 32, 0, 1.0, None, None) == OK
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mxq, "_lib", None)
     monkeypatch.setattr(mxq, "LIB_PATH", str(tmp_path / "missing.so"))

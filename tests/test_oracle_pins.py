@@ -670,3 +670,66 @@ def test_rotation_orientation_with_non_symmetric_matrix(g):
     hd = W.bf16_bits_to_float(H).astype(np.float64)
     np.testing.assert_allclose(y, (xd @ hd).reshape(5, 2 * g), rtol=0, atol=1e-12)
     assert np.abs(y - (xd @ hd.T).reshape(5, 2 * g)).max() > 1e-3
+
+
+
+# ---------------------------------------------------------------------------------------------
+# block-scaled GEMM of stored MX data: dequantize, then matmul
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("fmt", [O.E2M1, O.E4M3])
+def test_gemm_of_unit_codes_is_k_times_alpha(fmt):
+    """Every code 1.0 (E2M1 nibble 0x2, E4M3 byte 0x38) under scale byte 127 (2^0): each
+    entry of C is alpha * K; under scale bytes 129 (A) and 126 (B) it is alpha * K * 2."""
+    M, N, K = 3, 5, 128
+    byte = 0x22 if fmt == O.E2M1 else 0x38
+    cols = O.code_bytes_per_row(fmt, K)
+    a = np.full((M, cols), byte, dtype=np.uint8)
+    b = np.full((N, cols), byte, dtype=np.uint8)
+    sa = np.full((M, K // 32), 127, dtype=np.uint8)
+    sb = np.full((N, K // 32), 127, dtype=np.uint8)
+    np.testing.assert_array_equal(O.gemm(a, sa, b, sb, K, fmt, O.LINEAR, alpha=0.5),
+                                  np.full((M, N), 0.5 * K))
+    sa[:] = 129
+    sb[:] = 126
+    np.testing.assert_array_equal(O.gemm(a, sa, b, sb, K, fmt, O.LINEAR), np.full((M, N), 2.0 * K))
+
+
+@pytest.mark.parametrize("layout", [O.LINEAR, O.SWIZZLED])
+@pytest.mark.parametrize("fmt", [O.E2M1, O.E4M3])
+def test_gemm_matches_a_brute_force_sum(fmt, layout):
+    """Random codes and scale bytes: each entry equals alpha * sum_k of the products of the
+    element-by-element dequantized values (oracle scalar dequant), summed in Python."""
+    rng = np.random.default_rng(fmt * 10 + layout)
+    M, N, K = 3, 4, 64
+    cols = O.code_bytes_per_row(fmt, K)
+    a = rng.integers(0, 256, (M, cols), dtype=np.uint8)
+    b = rng.integers(0, 256, (N, cols), dtype=np.uint8)
+    if fmt == O.E4M3:  # no NaN codes
+        a[(a & 0x7F) == 0x7F] ^= 0x01
+        b[(b & 0x7F) == 0x7F] ^= 0x01
+    la = rng.integers(120, 135, (M, K // 32), dtype=np.uint8)
+    lb = rng.integers(120, 135, (N, K // 32), dtype=np.uint8)
+
+    def stored(lin, rows):
+        if layout == O.LINEAR:
+            return lin
+        sw = np.zeros(O.scales_shape(rows, K, O.SWIZZLED), dtype=np.uint8).reshape(-1)
+        cp = O.scales_shape(rows, K, O.SWIZZLED)[1]
+        for r in range(rows):
+            for j in range(K // 32):
+                sw[O.swizzled_offset(r, j, cp)] = lin[r, j]
+        return sw.reshape(O.scales_shape(rows, K, O.SWIZZLED))
+
+    def value(codes, lin, r, k):
+        if fmt == O.E4M3:
+            code = int(codes[r, k])
+        else:
+            byte = int(codes[r, k // 2])
+            code = byte & 0xF if k % 2 == 0 else byte >> 4
+        return O.bf16_to_double(O.dequant_bf16(fmt, code, int(lin[r, k // 32])))
+
+    C = O.gemm(a, stored(la, M), b, stored(lb, N), K, fmt, layout, alpha=1.5)
+    for i in range(M):
+        for j in range(N):
+            want = 1.5 * sum(value(a, la, i, k) * value(b, lb, j, k) for k in range(K))
+            assert C[i, j] == pytest.approx(want, rel=1e-15, abs=1e-300)
