@@ -244,7 +244,8 @@ mx_status mx_dequantize_nvfp4(const void* codes, const void* scales, int64_t M, 
  * scales [M, K/32] (linear) or the 128x4 blocked layout of mx_scales_shape(M, K) (swizzled), as
  * mx_quantize writes them; B likewise with N rows; both in the same fmt and layout. C: bf16
  * [M, N] row-major, must not overlap the inputs. K % 64 == 0 (K > 0), N % 8 == 0; codes and C
- * 16-byte aligned, swizzled scales 16-byte aligned. A scale byte 0xFF makes its 32 values NaN.
+ * 16-byte aligned, linear scales 2-byte aligned, swizzled scales 16-byte aligned. A scale byte
+ * 0xFF makes its 32 values NaN.
  * M <= 8,388,480 (65,535 tiles of 128 rows). M == 0 or N == 0 is a no-op returning MX_OK.
  * Errors: see conventions; K not a positive multiple of 64, N % 8 or M too large ->
  * MX_ERR_SHAPE.

@@ -441,6 +441,7 @@ mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes
   if (layout == MX_SCALES_SWIZZLED && (!aligned16(a_scales) || !aligned16(b_scales))) {
     return MX_ERR_ALIGN;
   }
+  if (((uintptr_t)a_scales | (uintptr_t)b_scales) & 1) return MX_ERR_ALIGN;  // 2-byte reads
   mxq::GemmArgs a{};
   a.a_codes = a_codes;
   a.a_scales = static_cast<const uint8_t*>(a_scales);

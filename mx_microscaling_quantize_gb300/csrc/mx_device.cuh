@@ -229,18 +229,6 @@ __device__ __forceinline__ uint4 load_v4(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t load_u32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.b32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint2 load_u64(const void* p) {
-  uint2 v;
-  asm volatile("ld.global.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
-
 __device__ __forceinline__ float load_f32(const float* p) {
   float v;
   asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));

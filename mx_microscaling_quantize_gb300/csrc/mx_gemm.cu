@@ -7,22 +7,37 @@
 // matmul_mxf4_bf16_tn(a_e2m1, b_e2m1, a_e8m0, b_e8m0, alpha) compared with the matmul of the
 // dequantized operands).
 //
-// Each CTA computes one 128 x 128 tile of C, K in steps of 64:
-//   warps 0..7   producers: each K step they read the tile's A and B codes (16 or 32 bytes of
-//                codes per 32-element block) and their scale bytes from global memory and write
-//                the dequantized values decode(code) * 2^(byte - 127), rounded once to bf16 (exact
-//                for every E2M1 code and for E4M3 codes unless the product falls below the bf16
-//                range), into a stage of shared memory: A and B as 128 rows x 64 bf16, K-major,
-//                in the 128-byte swizzled layout (16-byte chunk c of row r at chunk c ^ (r % 8)),
-//                the form a tensor-core shared-memory descriptor reads;
-//   warp 8       allocates 128 tensor-memory columns and, from one lane, issues per stage four
-//                tcgen05.mma kind::f16 (M = 128, N = 128, K = 16, bf16 x bf16 -> fp32 in tensor
-//                memory) and commits them to the stage's "empty" barrier;
-//   warps 8..11  epilogue: tcgen05.ld of the accumulator (warp w reads lanes 32 (w % 4) .. +31,
-//                the tile's rows), times alpha, rounded to bf16, 16-byte stores.
-// Three stages in flight; two CTAs per SM. Every mbarrier wait is bounded as in the rotation
-// kernel: a wait that runs out sets the device error word and its role stops issuing work, and
-// the MMA thread waits for its MMAs before the tensor memory is freed.
+// Each CTA computes one 128 x 256 tile of C, K in steps of 64:
+//   warp 12      one thread loads each step's raw codes with the tensor-memory accelerator: A's
+//                128 rows and B's 256 rows of 32 (E2M1) or 64 (E4M3) code bytes, 32- or
+//                64-byte swizzled so that a thread reading its own row hits distinct banks,
+//                into a ring of four stages;
+//   warps 0..3   A converters, one thread per row of A: the step's 64 codes and two scale bytes
+//                -> 64 bf16 values decode(code) * 2^(byte - 127) (rounded once to bf16; exact for
+//                every E2M1 code and for E4M3 unless below the bf16 range), written straight
+//                into tensor memory (tcgen05.st; row i in lane i, two values per column), the
+//                form in which the MMA reads its A operand;
+//   warps 4..11  B converters, one thread per row of B: the same values written to shared
+//                memory as 256 rows x 128 bytes, K-major, 128-byte swizzled (16-byte chunk c of
+//                row r at chunk c ^ (r % 8)), the layout a shared-memory descriptor reads;
+//   warp 13      allocates the tensor memory (accumulator: 256 fp32 columns; A: three stages of
+//                32 columns) and, from one lane, issues per step four tcgen05.mma kind::f16
+//                (M = 128, N = 256, K = 16, A from tensor memory, B from shared memory,
+//                bf16 x bf16 -> fp32) and commits them to the step's "empty" barrier;
+//   warps 0..7   epilogue: tcgen05.ld of the accumulator, times alpha, rounded to bf16, 16-byte
+//                stores (warps 0-3 columns 0-127, warps 4-7 columns 128-255).
+// Operand type. When every scale byte of the CTA's rows lies in the window where every value
+// decode(code) * 2^X (X = byte - 127) is exact in f16 (E2M1: X in [-23, 13]; E4M3: [-15, 7]),
+// the operands are f16: two codes take one hardware conversion to f16x2 (exact) and one f16x2
+// multiply by 2^X (exact). Otherwise they are bf16: the f16 patterns are moved to bf16 position
+// (the values times 2^-112, still exact), then one bf16x2 multiply by 2^(X + 112) (rounded
+// once) and a second one only when X > 15 (2^(X + 112) is then beyond the bf16 range). In the
+// window both give the same operand values, so the choice changes no product. The converters
+// check the window over the CTA's scale bytes before the first step (one CTA-wide vote).
+// Scale bytes are read by each converter from global memory two steps ahead.
+// Every mbarrier wait is bounded: a wait that runs out sets the device error word and its role
+// stops issuing work; the loads in flight and the MMAs issued are waited for before the CTA
+// frees its tensor memory and exits.
 #include "mx_device.cuh"
 #include "mx_launch.h"
 #include "mx_tcgen05.cuh"
@@ -33,173 +48,409 @@ namespace {
 
 using namespace tc;
 
-constexpr int kBM = 128, kBN = 128, kBK = 64;
-constexpr int kStages = 3;
-constexpr int kOperandBytes = kBM * kBK * 2;  // 16 KiB of bf16 per operand and stage
-constexpr int kGemmStageBytes = 2 * kOperandBytes;
-constexpr int kProducerWarps = 8;
-constexpr int kGemmThreads = (kProducerWarps + 4) * 32;
-constexpr int kChunksPerThread = 2 * kBM * (kBK / 8) / (kProducerWarps * 32);  // 8
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kRawStages = 4;   // raw code stages (tensor-memory-accelerator ring)
+constexpr int kOpStages = 3;    // operand stages (A in tensor memory, B in shared memory)
+constexpr int kAWarps = 4, kBWarps = 8, kConvWarps = kAWarps + kBWarps;
+constexpr int kTmaWarp = kConvWarps, kMmaWarp = kConvWarps + 1;
+constexpr int kGemmThreads = (kConvWarps + 2) * 32;  // 448
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = kBN;            // fp32 accumulator columns
+constexpr uint32_t kAStageCols = kBK / 2;     // bf16 pairs of a 64-wide K step
+constexpr int kBOpBytes = kBN * kBK * 2;      // 32 KiB of bf16 per B stage
 constexpr unsigned long long kGemmWaitNs = 2000000000ull;  // 2 s
-constexpr int kGemmSmem = 1024 + kStages * kGemmStageBytes + (2 * kStages + 1) * 8 + 16;
 
-// Eight codes (8 E2M1 nibbles in a 32-bit word, lower K first; or 8 E4M3 bytes in two words)
-// under the E8M0 byte `sb` -> 8 bf16 (4 words), each decode(code) * 2^(sb - 127) rounded once.
-// Scale byte 0xFF (E8M0 NaN) gives the bf16 NaN 0x7FC0, as the dequantize kernel does.
 template <int FMT>
-__device__ __forceinline__ uint4 dequant8(uint32_t w0, uint32_t w1, uint32_t sb) {
-  const float sc = scale_of(sb);
-  uint32_t o[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t h;  // two codes decoded exactly to f16x2 (lower K in the low half)
-    if (FMT == kFmtE2M1) {
-      const uint32_t byte = (w0 >> (8 * i)) & 0xFFu;
-      asm("{\n\t.reg .b8 c;\n\tcvt.u8.u32 c, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, c;\n\t}"
-          : "=r"(h)
-          : "r"(byte));
-    } else {
-      const uint32_t pair = ((i < 2 ? w0 : w1) >> (16 * (i & 1))) & 0xFFFFu;
-      asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
-          : "=r"(h)
-          : "r"(pair));
-    }
-    float lo, hi;
-    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(h));
-    lo *= sc;  // exact: a power of two times a code value, inside the fp32 range
-    hi *= sc;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[i]) : "f"(hi), "f"(lo));
-  }
-  if (sb == 255u) return make_uint4(kBf16NaNx2, kBf16NaNx2, kBf16NaNx2, kBf16NaNx2);
-  return make_uint4(o[0], o[1], o[2], o[3]);
+struct RawLayout {
+  static constexpr int kRowBytes = FMT == kFmtE2M1 ? 32 : 64;  // code bytes of a row per step
+  static constexpr int kABytes = kBM * kRowBytes;
+  static constexpr int kStageBytes = (kBM + kBN) * kRowBytes;  // 12 or 24 KiB
+};
+
+template <int FMT>
+constexpr int gemm_smem() {
+  return 1024 + kOpStages * kBOpBytes + kRawStages * RawLayout<FMT>::kStageBytes +
+         (2 * kRawStages + 2 * kOpStages + 1) * 8 + 16;  // + tmem slot, vote
 }
 
-template <int FMT, bool SWZ>
-__global__ void __launch_bounds__(kGemmThreads, 2) mx_gemm_kernel(GemmArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kGemmStageBytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t m0 = (int64_t)blockIdx.y * kBM, n0 = (int64_t)blockIdx.x * kBN;
-  const int nk = (int)(a.K / kBK);
-  constexpr int kCodeBytesPer8 = FMT == kFmtE2M1 ? 4 : 8;  // code bytes of 8 elements
-  const int64_t code_row = FMT == kFmtE2M1 ? a.K / 2 : a.K;
+__device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 
-  pdl_launch_dependents();
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(full + s), kProducerWarps);
-      mbar_init(smem_u32(empty + s), 1);
-    }
-    mbar_init(smem_u32(acc_full), 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  pdl_wait();  // also: the kernel before may still hold this SM's tensor memory until then
-  if (warp == kProducerWarps) {
-    tmem_alloc(smem_u32(tmem_slot), kBN);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  bool failed = false;
+// f16x2 pattern of two code values (exact: each normal or zero with the low 7 mantissa bits
+// zero) -> bf16x2 pattern of the same values times 2^-112: exponent and top mantissa bits move
+// down three places into bf16 position, the signs stay.
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2_lowered(uint32_t h) {
+  return ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
+}
 
-  if (warp < kProducerWarps) {
-    // ---------------- producers ----------------
-    // chunk q in [0, 2048): operand q / 1024 (A, B), row (q % 1024) / 8, 8 elements
-    // 8 (q % 8) .. +7 of the K step; this thread takes q = tid + 256 j.
-    uint32_t w0[kChunksPerThread], w1[kChunksPerThread], sb[kChunksPerThread];
-    auto load_step = [&](int kk) {
+// Per 32-element block with scale byte sb: f1 = 2^(min(X, 15) + 112) in both bf16 halves and,
+// when X > 15, f2 = 2^(X - 15) (bf16 NaN for the E8M0 NaN byte 0xFF), X = sb - 127.
+struct BlockFactors {
+  uint32_t f1, f2;
+  bool big;
+};
+__device__ __forceinline__ BlockFactors block_factors(uint32_t sb) {
+  BlockFactors f;
+  f.f1 = ((min(sb, 142u) + 112u) << 7) * 0x00010001u;
+  f.big = sb > 142u;
+  f.f2 = sb == 255u ? kBf16NaNx2 : ((sb - 15u) << 7) * 0x00010001u;
+  return f;
+}
+
+// One row's 64 codes of a step (raw[]: E2M1 8 words, E4M3 16 words, lower K first) under the
+// scale bytes sb0 (elements 0-31) and sb1 (32-63) -> 32 bf16x2 words, lower K in the low half.
+template <int FMT>
+__device__ __forceinline__ void convert_row(const uint32_t* raw, uint32_t sb0, uint32_t sb1,
+                                            uint32_t* out) {
+  const BlockFactors b0 = block_factors(sb0), b1 = block_factors(sb1);
+  if (FMT == kFmtE2M1) {
 #pragma unroll
-      for (int j = 0; j < kChunksPerThread; ++j) {
-        const int q = tid + 256 * j;
-        const bool is_b = q >= 1024;
-        const int r = (q & 1023) >> 3, c = q & 7;
-        const int64_t row = (is_b ? n0 : m0) + r;
-        const int64_t rows = is_b ? a.N : a.M;
-        w0[j] = 0u;
-        w1[j] = 0u;
-        sb[j] = 0u;
-        if (row < rows) {
-          const int64_t k = (int64_t)kk * kBK + 8 * c;
-          const uint8_t* codes = static_cast<const uint8_t*>(is_b ? a.b_codes : a.a_codes) +
-                                 row * code_row + k * kCodeBytesPer8 / 8;
-          if (FMT == kFmtE2M1) {
-            w0[j] = load_u32(codes);
-          } else {
-            const uint2 v = load_u64(codes);
-            w0[j] = v.x;
-            w1[j] = v.y;
-          }
-          const int64_t scols = is_b ? a.b_scale_cols : a.a_scale_cols;
-          const int64_t kb = k >> 5;
-          const uint8_t* sc = is_b ? a.b_scales : a.a_scales;
-          sb[j] = load_u8(sc + (SWZ ? swizzled_offset(row, kb, scols) : row * scols + kb));
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t f = j < 4 ? b0.f1 : b1.f1;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        uint32_t h;
+        asm("{\n\t.reg .b8 c;\n\tcvt.u8.u32 c, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, c;\n\t}"
+            : "=r"(h)
+            : "r"(raw[j] >> (8 * t)));
+        out[4 * j + t] = hmul2_bf16(f16x2_to_bf16x2_lowered(h), f);
+      }
+    }
+  } else {
+    uint32_t nan = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t f = j < 8 ? b0.f1 : b1.f1;
+      const uint32_t w = raw[j];
+      nan |= (w & 0x7F7F7F7Fu) + 0x01010101u;  // a byte reaches 0x80 iff it is S.1111.111
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        uint32_t h;
+        asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+            : "=r"(h)
+            : "r"(w >> (16 * t)));
+        out[2 * j + t] = hmul2_bf16(f16x2_to_bf16x2_lowered(h), f);
+      }
+    }
+    if (nan & 0x80808080u) {  // E4M3 NaN codes: their values are the bf16 NaN
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t n = ((raw[j] & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t lo = (n >> (16 * t + 7)) & 1u, hi = (n >> (16 * t + 15)) & 1u;
+          uint32_t v = out[2 * j + t];
+          if (lo) v = (v & 0xFFFF0000u) | 0x7FC0u;
+          if (hi) v = (v & 0x0000FFFFu) | 0x7FC00000u;
+          out[2 * j + t] = v;
         }
       }
-    };
-    load_step(0);
-    for (int kk = 0; kk < nk; ++kk) {
-      const int s = kk % kStages;
-      if (kk >= kStages) {
-        mbar_wait(smem_u32(empty + s), ((kk / kStages) & 1) ^ 1, &failed, kGemmWaitNs, a.err);
-        failed = __any_sync(0xFFFFFFFFu, failed);  // the warp leaves together (__syncwarp below)
-      }
-      if (failed) break;
-      uint8_t* stage = smem + s * kGemmStageBytes;
-#pragma unroll
-      for (int j = 0; j < kChunksPerThread; ++j) {
-        const int q = tid + 256 * j;
-        const int r = (q & 1023) >> 3, c = q & 7;
-        const uint4 v = dequant8<FMT>(w0[j], w1[j], sb[j]);
-        *reinterpret_cast<uint4*>(stage + (q >= 1024 ? kOperandBytes : 0) + r * 128 +
-                                  ((c ^ (r & 7)) << 4)) = v;
-      }
-      if (kk + 1 < nk) load_step(kk + 1);  // next step's codes in flight during the wait
-      fence_proxy_async_smem();            // the writes are visible to the tensor cores
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(full + s));
     }
-  } else if (warp == kProducerWarps && lane == 0) {
-    // ---------------- MMA issuer ----------------
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+  }
+  if (b0.big) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) out[i] = hmul2_bf16(out[i], b0.f2);
+  }
+  if (b1.big) {
+#pragma unroll
+    for (int i = 16; i < 32; ++i) out[i] = hmul2_bf16(out[i], b1.f2);
+  }
+}
+
+// Scale-byte window in which every value decode(code) * 2^(byte - 127) is exact in f16.
+template <int FMT>
+struct F16Window {
+  static constexpr uint32_t kLo = FMT == kFmtE2M1 ? 104u : 112u;  // X >= -23 / -15
+  static constexpr uint32_t kHi = FMT == kFmtE2M1 ? 140u : 134u;  // X <= 13 / 7
+};
+
+__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// 2^(sb - 127) as f16 in both halves, sb inside the window (2^-23 .. 2^-15 are subnormal).
+__device__ __forceinline__ uint32_t f16_pow2x2(uint32_t sb) {
+  const int x = (int)sb - 127;
+  const uint32_t h = x >= -14 ? (uint32_t)(x + 15) << 10 : 1u << (x + 24);
+  return h * 0x00010001u;
+}
+
+// The f16 form of convert_row, scale bytes inside the window: values exact, lower K low half.
+template <int FMT>
+__device__ __forceinline__ void convert_row_f16(const uint32_t* raw, uint32_t sb0, uint32_t sb1,
+                                                uint32_t* out) {
+  const uint32_t m0 = f16_pow2x2(sb0), m1 = f16_pow2x2(sb1);
+  if (FMT == kFmtE2M1) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t h[4];
+      asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\tmov.b32 {c0, c1, c2, c3}, %4;\n\t"
+          "cvt.rn.f16x2.e2m1x2 %0, c0;\n\tcvt.rn.f16x2.e2m1x2 %1, c1;\n\t"
+          "cvt.rn.f16x2.e2m1x2 %2, c2;\n\tcvt.rn.f16x2.e2m1x2 %3, c3;\n\t}"
+          : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+          : "r"(raw[j]));
+#pragma unroll
+      for (int t = 0; t < 4; ++t) out[4 * j + t] = hmul2_f16(h[t], j < 4 ? m0 : m1);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      uint32_t h[2];
+      asm("{\n\t.reg .b16 c0, c1;\n\tmov.b32 {c0, c1}, %2;\n\t"
+          "cvt.rn.f16x2.e4m3x2 %0, c0;\n\tcvt.rn.f16x2.e4m3x2 %1, c1;\n\t}"
+          : "=r"(h[0]), "=r"(h[1])
+          : "r"(raw[j]));
+      out[2 * j] = hmul2_f16(h[0], j < 8 ? m0 : m1);
+      out[2 * j + 1] = hmul2_f16(h[1], j < 8 ? m0 : m1);
+    }
+  }
+}
+
+// Running byte-wise min / max of 4-byte words (bytes of rows or blocks that do not exist are
+// passed as `fill`).
+struct ByteRange {
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  __device__ __forceinline__ void add(uint32_t w) {
+    lo = __vminu4(lo, w);
+    hi = __vmaxu4(hi, w);
+  }
+  __device__ __forceinline__ bool inside(uint32_t wlo, uint32_t whi) const {
+    const uint32_t l = min(min(lo & 0xFFu, (lo >> 8) & 0xFFu), min((lo >> 16) & 0xFFu, lo >> 24));
+    const uint32_t h = max(max(hi & 0xFFu, (hi >> 8) & 0xFFu), max((hi >> 16) & 0xFFu, hi >> 24));
+    return l >= wlo && h <= whi;
+  }
+};
+
+__device__ __forceinline__ uint32_t load_scale_pair(const uint8_t* p) {
+  uint16_t v;
+  asm volatile("ld.global.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// Shared-memory carve-up and per-CTA constants of one GEMM CTA.
+template <int FMT>
+struct GemmCta {
+  uint8_t* bop;       // kOpStages x 32 KiB: B operand stages
+  uint8_t* raw;       // kRawStages x RawLayout<FMT>::kStageBytes: raw code stages
+  uint64_t* raw_full;
+  uint64_t* raw_empty;
+  uint64_t* op_full;
+  uint64_t* op_empty;
+  uint64_t* acc_full;
+  uint32_t tmem;
+  int64_t m0, n0;
+  int nk;
+};
+
+__device__ __forceinline__ uint4 load_scale_chunk(const uint8_t* p) {  // 16-byte aligned
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Whether every scale byte of this converter's share of the CTA's rows (A: the row block of
+// 128 rows; B: two) lies inside [lo, hi]. Rows past M / N, and the padding columns of the
+// swizzled layout, are not looked at.
+template <bool SWZ>
+__device__ __forceinline__ bool scales_inside(const GemmArgs& a, bool is_a, int r, int64_t grow,
+                                              uint32_t lo, uint32_t hi) {
+  ByteRange br;
+  const uint8_t* sc = is_a ? a.a_scales : a.b_scales;
+  const int64_t scols = is_a ? a.a_scale_cols : a.b_scale_cols;
+  const int64_t rows = is_a ? a.M : a.N;
+  const uint32_t fill = lo * 0x01010101u;
+  if (SWZ) {
+    // the 128-row block's 512-byte tiles are contiguous: chunk i (16 bytes) of the block holds
+    // rows q, q + 32, q + 64, q + 96 (q = i % 32) of tile i / 32, 4 blocks each
+    const int64_t row0 = (is_a ? 0 : (r >> 7) * 128) + grow - r;  // first row of the block
+    const int u = is_a ? r : (r & 127);
+    if (row0 < rows) {
+      const int64_t ctiles = scols >> 2;
+      const int kb_last = (int)((a.K / 32) & 3);  // 2 when the last tile holds 2 pad columns
+      const uint8_t* base = sc + (row0 >> 7) * ctiles * 512;
+      for (int64_t i = u; i < ctiles * 32; i += 128) {
+        const uint4 v = load_scale_chunk(base + i * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const bool last = i / 32 == ctiles - 1 && kb_last != 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t x = row0 + (i & 31) + 32 * g < rows ? w[g] : fill;
+          if (last) x = (x & 0x0000FFFFu) | (fill & 0xFFFF0000u);
+          br.add(x);
+        }
+      }
+    }
+  } else if (grow < rows) {
+    const uint8_t* p = sc + grow * scols;
+    if ((scols & 15) == 0 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+      for (int64_t i = 0; i < scols; i += 16) {
+        const uint4 v = load_scale_chunk(p + i);
+        br.add(v.x);
+        br.add(v.y);
+        br.add(v.z);
+        br.add(v.w);
+      }
+    } else {
+      for (int64_t i = 0; i < scols; i += 2) br.add(load_scale_pair(p + i) * 0x00010001u);
+    }
+  }
+  return br.inside(lo, hi);  // nothing looked at: lo 0xFF.., hi 0 -> inside
+}
+
+// Raw code loads (one thread of warp kTmaWarp): runs from the start, independent of the operand
+// type, so that the first stages are in flight while the converters vote.
+template <int FMT>
+__device__ __forceinline__ void gemm_loads(const CUtensorMap& amap, const CUtensorMap& bmap,
+                                           const GemmArgs& a, const GemmCta<FMT>& c) {
+  using R = RawLayout<FMT>;
+  const int nk = c.nk;
+  bool failed = false;
+  int issued = 0;
+  for (int kk = 0; kk < nk; ++kk) {
+    const int s = kk % kRawStages;
+    if (kk >= kRawStages) {
+      mbar_wait(smem_u32(c.raw_empty + s), ((kk / kRawStages) & 1) ^ 1, &failed,
+                kGemmWaitNs, a.err);
+    }
+    if (failed) break;
+    const uint32_t dst = smem_u32(c.raw + s * R::kStageBytes);
+    mbar_arrive_expect_tx(smem_u32(c.raw_full + s), R::kStageBytes);
+    tma_load_box(dst, &amap, kk * R::kRowBytes, (int)c.m0, smem_u32(c.raw_full + s));
+    tma_load_box(dst + R::kABytes, &bmap, kk * R::kRowBytes, (int)c.n0,
+                 smem_u32(c.raw_full + s));
+    issued = kk + 1;
+  }
+  // loads still in flight land before the CTA's shared memory goes away
+  bool drain_failed = false;
+  for (int kk = issued > kRawStages ? issued - kRawStages : 0; kk < issued; ++kk) {
+    mbar_wait(smem_u32(c.raw_full + kk % kRawStages), (kk / kRawStages) & 1, &drain_failed,
+              kGemmWaitNs, a.err);
+  }
+}
+
+template <int FMT, bool SWZ, bool F16>
+__device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>& c) {
+  using R = RawLayout<FMT>;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t tmem = c.tmem;
+  const int nk = c.nk;
+  bool failed = false;
+
+  if (warp < kConvWarps) {
+    // ---------------- converters: one row each ----------------
+    const bool is_a = warp < kAWarps;
+    const int r = is_a ? tid : tid - kAWarps * 32;
+    const int64_t grow = (is_a ? c.m0 : c.n0) + r;
+    const bool valid = grow < (is_a ? a.M : a.N);
+    const uint8_t* sc = is_a ? a.a_scales : a.b_scales;
+    const int64_t scols = is_a ? a.a_scale_cols : a.b_scale_cols;
+    // scale bytes of step kk (two blocks): linear row-major, or the row's 4-byte slot of the
+    // 512-byte tile holding blocks 4t .. 4t + 3 (t = kk / 2)
+    const uint8_t* sbase =
+        SWZ ? sc + ((grow >> 7) * (scols >> 2)) * 512 + (grow & 31) * 16 + ((grow >> 5) & 3) * 4
+            : sc + grow * scols;
+    auto scale_at = [&](int kk) -> uint32_t {
+      if (!valid || kk >= nk) return 0x7F7Fu;
+      return load_scale_pair(SWZ ? sbase + (int64_t)(kk >> 1) * 512 + (kk & 1) * 2
+                                 : sbase + 2 * (int64_t)kk);
+    };
+    uint32_t sc_next = scale_at(0), sc_after = scale_at(1);
+    const uint32_t raw_row = (is_a ? 0u : (uint32_t)R::kABytes) + (uint32_t)r * R::kRowBytes;
     for (int kk = 0; kk < nk; ++kk) {
-      const int s = kk % kStages;
-      mbar_wait(smem_u32(full + s), (kk / kStages) & 1, &failed, kGemmWaitNs, a.err);
+      const int sr = kk % kRawStages, so = kk % kOpStages;
+      const uint32_t scv = sc_next;
+      sc_next = sc_after;
+      sc_after = scale_at(kk + 2);
+      mbar_wait(smem_u32(c.raw_full + sr), (kk / kRawStages) & 1, &failed, kGemmWaitNs, a.err);
+      failed = __any_sync(0xFFFFFFFFu, failed);
+      if (failed) break;
+      uint32_t w[R::kRowBytes / 4];
+      const uint8_t* row = c.raw + sr * R::kStageBytes + raw_row;
+#pragma unroll
+      for (int q = 0; q < R::kRowBytes / 16; ++q) {
+        // swizzled box: 16-byte chunk q of row r at q ^ (r / 4 % 2) (32-byte rows) or
+        // q ^ (r / 2 % 4) (64-byte rows)
+        const int pq = FMT == kFmtE2M1 ? (q ^ ((r >> 2) & 1)) : (q ^ ((r >> 1) & 3));
+        const uint4 v = *reinterpret_cast<const uint4*>(row + pq * 16);
+        w[4 * q] = v.x;
+        w[4 * q + 1] = v.y;
+        w[4 * q + 2] = v.z;
+        w[4 * q + 3] = v.w;
+      }
+      uint32_t out[32];
+      if (F16) {
+        convert_row_f16<FMT>(w, scv & 0xFFu, scv >> 8, out);
+      } else {
+        convert_row<FMT>(w, scv & 0xFFu, scv >> 8, out);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(c.raw_empty + sr));  // raw bytes consumed
+      if (kk >= kOpStages) {
+        mbar_wait(smem_u32(c.op_empty + so), ((kk / kOpStages) & 1) ^ 1, &failed, kGemmWaitNs,
+                  a.err);
+        failed = __any_sync(0xFFFFFFFFu, failed);
+        if (failed) break;
+      }
+      if (is_a) {
+        tmem_st32(tmem + ((uint32_t)(warp * 32) << 16) + kAccCols + so * kAStageCols, out);
+        tc_fence_before();
+      } else {
+        uint8_t* dst = c.bop + so * kBOpBytes + r * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          *reinterpret_cast<uint4*>(dst + ((q ^ (r & 7)) << 4)) =
+              make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+        }
+        fence_proxy_async_smem();  // visible to the tensor cores
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(c.op_full + so));
+    }
+  } else if (warp == kMmaWarp && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t idesc = F16 ? idesc_f16_f32(kBM, kBN) : idesc_bf16_f32(kBM, kBN);
+    for (int kk = 0; kk < nk; ++kk) {
+      const int s = kk % kOpStages;
+      mbar_wait(smem_u32(c.op_full + s), (kk / kOpStages) & 1, &failed, kGemmWaitNs, a.err);
       if (failed) break;
       tc_fence_after();
-      const uint32_t sa = smem_u32(smem + s * kGemmStageBytes), sbb = sa + kOperandBytes;
+      const uint32_t b0 = smem_u32(c.bop + s * kBOpBytes);
 #pragma unroll
       for (int k16 = 0; k16 < kBK / 16; ++k16) {
-        mma_bf16(tmem, desc_sw128(sa + 32 * k16), desc_sw128(sbb + 32 * k16), idesc,
-                 (kk > 0 || k16 > 0) ? 1u : 0u);
+        mma_bf16_ts(tmem, tmem + kAccCols + s * kAStageCols + k16 * 8, desc_sw128(b0 + 32 * k16),
+                    idesc, (kk > 0 || k16 > 0) ? 1u : 0u);
       }
-      mma_commit(smem_u32(empty + s));  // stage free once these MMAs have read it
+      mma_commit(smem_u32(c.op_empty + s));  // stage free once these MMAs have read it
     }
-    mma_commit(smem_u32(acc_full));  // tracks every MMA issued above
+    mma_commit(smem_u32(c.acc_full));  // tracks every MMA issued above
+    bool drain_failed = false;         // the MMAs complete before the tensor memory is freed
+    mbar_wait(smem_u32(c.acc_full), 0, &drain_failed, kGemmWaitNs, a.err);
   }
-  if (warp >= kProducerWarps) {
+
+  if (warp < 8) {
     // ---------------- epilogue ----------------
-    bool efailed = false;
-    mbar_wait(smem_u32(acc_full), 0, &efailed, kGemmWaitNs, a.err);
-    efailed = __any_sync(0xFFFFFFFFu, efailed || failed);
+    bool efailed = failed;
+    mbar_wait(smem_u32(c.acc_full), 0, &efailed, kGemmWaitNs, a.err);
+    efailed = __any_sync(0xFFFFFFFFu, efailed);
     tc_fence_after();
     const int quarter = warp & 3;
-    const int64_t row = m0 + quarter * 32 + lane;
+    const uint32_t col0 = (uint32_t)(warp >> 2) * 128;
+    const int64_t row = c.m0 + quarter * 32 + lane;
 #pragma unroll 1
-    for (int cb = 0; cb < kBN / 32; ++cb) {
+    for (int cb = 0; cb < 4; ++cb) {
       float y[32];
-      if (!efailed) tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(cb * 32), y);
+      if (!efailed) tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col0 + cb * 32, y);
       if (efailed || row >= a.M) continue;
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const int64_t col = n0 + cb * 32 + g * 8;
+        const int64_t col = c.n0 + col0 + cb * 32 + g * 8;
         if (col >= a.N) break;
         uint32_t o[4];
 #pragma unroll
@@ -213,18 +464,97 @@ __global__ void __launch_bounds__(kGemmThreads, 2) mx_gemm_kernel(GemmArgs a) {
       }
     }
   }
+}
+
+template <int FMT, bool SWZ>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap amap,
+                   const __grid_constant__ CUtensorMap bmap, GemmArgs a) {
+  using R = RawLayout<FMT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  GemmCta<FMT> c;
+  c.bop = smem;
+  c.raw = smem + kOpStages * kBOpBytes;
+  c.raw_full = reinterpret_cast<uint64_t*>(c.raw + kRawStages * R::kStageBytes);
+  c.raw_empty = c.raw_full + kRawStages;
+  c.op_full = c.raw_empty + kRawStages;
+  c.op_empty = c.op_full + kOpStages;
+  c.acc_full = c.op_empty + kOpStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(c.acc_full + 1);
+  uint32_t* outside = tmem_slot + 1;  // count of converters with a scale byte outside the window
+  const int tid = threadIdx.x, warp = tid >> 5;
+  c.m0 = (int64_t)blockIdx.y * kBM;
+  c.n0 = (int64_t)blockIdx.x * kBN;
+  c.nk = (int)(a.K / kBK);
+
+  pdl_launch_dependents();
+  if (tid == 0) {
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(smem_u32(c.raw_full + s), 1);
+      mbar_init(smem_u32(c.raw_empty + s), kConvWarps);
+    }
+    for (int s = 0; s < kOpStages; ++s) {
+      mbar_init(smem_u32(c.op_full + s), kConvWarps);
+      mbar_init(smem_u32(c.op_empty + s), 1);
+    }
+    mbar_init(smem_u32(c.acc_full), 1);
+    *outside = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  pdl_wait();  // inputs written by the kernel before; its tensor memory freed
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();  // barriers initialised, tensor memory allocated
+  tc_fence_after();
+  c.tmem = *tmem_slot;
+  if (warp == kTmaWarp) {
+    if ((tid & 31) == 0) gemm_loads<FMT>(amap, bmap, a, c);
+  } else {
+    if (warp < kConvWarps) {  // f16 window vote over the CTA's scale bytes
+      const bool is_a = warp < kAWarps;
+      const int r = is_a ? tid : tid - kAWarps * 32;
+      const int64_t grow = (is_a ? c.m0 : c.n0) + r;
+      const bool in =
+          scales_inside<SWZ>(a, is_a, r, grow, F16Window<FMT>::kLo, F16Window<FMT>::kHi);
+      if (!__all_sync(0xFFFFFFFFu, in) && (tid & 31) == 0) atomicAdd(outside, 1u);
+    }
+    // converters and the MMA warp (the load warp is already running)
+    asm volatile("bar.sync 1, %0;" ::"n"((kConvWarps + 1) * 32) : "memory");
+    if (*outside == 0) {
+      gemm_roles<FMT, SWZ, true>(a, c);
+    } else {
+      gemm_roles<FMT, SWZ, false>(a, c);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kProducerWarps) tmem_dealloc(tmem, kBN);
+  if (warp == kMmaWarp) tmem_dealloc(c.tmem, kTmemCols);
 }
 
 template <int FMT, bool SWZ>
 cudaError_t launch_t(const GemmArgs& a, cudaStream_t stream) {
+  using R = RawLayout<FMT>;
   const void* k = reinterpret_cast<const void*>(&mx_gemm_kernel<FMT, SWZ>);
-  if (resident_ctas(k, kGemmThreads, kGemmSmem, 0) <= 0) return cudaErrorInvalidConfiguration;
+  constexpr int smem = gemm_smem<FMT>();
+  if (resident_ctas(k, kGemmThreads, smem, 1) <= 0) return cudaErrorInvalidConfiguration;
+  const int64_t code_row = FMT == kFmtE2M1 ? a.K / 2 : a.K;
+  const CUtensorMapSwizzle swz =
+      FMT == kFmtE2M1 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUtensorMap amap, bmap;
+  cudaError_t err = make_tensor_map_2d(&amap, a.a_codes, a.M, code_row,
+                                       CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, R::kRowBytes, kBM, swz);
+  if (err != cudaSuccess) return err;
+  err = make_tensor_map_2d(&bmap, a.b_codes, a.N, code_row, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                           R::kRowBytes, kBN, swz);
+  if (err != cudaSuccess) return err;
   const dim3 grid((unsigned)((a.N + kBN - 1) / kBN), (unsigned)((a.M + kBM - 1) / kBM));
-  return launch_pdl(&mx_gemm_kernel<FMT, SWZ>, grid, dim3(kGemmThreads), kGemmSmem, stream, a);
+  return launch_pdl(&mx_gemm_kernel<FMT, SWZ>, grid, dim3(kGemmThreads), smem, stream, amap,
+                    bmap, a);
 }
 
 }  // namespace

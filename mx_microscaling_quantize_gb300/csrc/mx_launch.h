@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <utility>
 
@@ -104,6 +105,12 @@ struct GemmArgs {
   float alpha;
   unsigned int* err;        // device error word (device_error_word)
 };
+
+// Tensor map of a row-major [rows, cols] matrix of 1- or 2-byte elements, boxes of box_rows x
+// box_cols, the given swizzle; loads read zeros out of bounds, stores drop what falls outside.
+cudaError_t make_tensor_map_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                               CUtensorMapDataType type, int elem_bytes, int box_cols,
+                               int box_rows, CUtensorMapSwizzle swizzle);
 
 // C = alpha * dequant(A) * dequant(B)^T on the tensor cores (fmt: 1 = E2M1, 2 = E4M3).
 cudaError_t launch_gemm(int fmt, bool swizzled, const GemmArgs& a, cudaStream_t stream);

@@ -742,31 +742,11 @@ __global__ void mx_wait_selftest_kernel(unsigned long long limit_ns) {
 // ------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------
-// Tensor map of a row-major [rows, cols] matrix of 1- or 2-byte elements, boxes of box_rows x
-// box_cols, the given swizzle; loads read zeros out of bounds, stores drop what falls outside.
+// Tensor map of a row-major [rows, cols] matrix, boxes of kTileRows x box_cols.
 cudaError_t make_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
                             CUtensorMapDataType type, int elem_bytes, int box_cols,
                             CUtensorMapSwizzle swizzle) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess) {
-      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-  });
-  if (!encode) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * elem_bytes};
-  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)kTileRows};
-  const cuuint32_t elem_strides[2] = {1, 1};
-  const CUresult r = encode(map, type, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  return make_tensor_map_2d(map, base, rows, cols, type, elem_bytes, box_cols, kTileRows, swizzle);
 }
 
 template <int FMT, int OUT, bool SWZ, int G>
@@ -821,6 +801,34 @@ cudaError_t launch_fmt(int out_kind, bool swz, int g, const RotArgs& a, cudaStre
 }
 
 }  // namespace
+
+// Tensor map of a row-major [rows, cols] matrix of 1- or 2-byte elements, boxes of box_rows x
+// box_cols, the given swizzle; loads read zeros out of bounds, stores drop what falls outside.
+cudaError_t make_tensor_map_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                               CUtensorMapDataType type, int elem_bytes, int box_cols,
+                               int box_rows, CUtensorMapSwizzle swizzle) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  });
+  if (!encode) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * elem_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = encode(map, type, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 
 cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const RotArgs& a,
                           cudaStream_t stream) {

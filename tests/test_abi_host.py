@@ -267,6 +267,8 @@ def test_gemm_validation(L):
     assert f(P, P, P, P, 128, 128, 64, 1, 32, 1, 1.0, P + 2, None) == ALIGN
     assert f(P, P + 1, P, P, 128, 128, 64, 1, 32, 1, 1.0, P, None) == ALIGN  # swizzled scales
     assert f(P, P, P, P + 4, 128, 128, 64, 1, 32, 1, 1.0, P, None) == ALIGN
+    assert f(P, P + 1, P, P, 128, 128, 64, 1, 32, 0, 1.0, P, None) == ALIGN   # linear: 2 bytes
+    assert f(P, P, P, P + 3, 128, 128, 64, 2, 32, 0, 1.0, P, None) == ALIGN
     assert f(None, None, None, None, 0, 128, 64, 1, 32, 1, 1.0, None, None) == OK
     assert f(None, None, None, None, 128, 0, 64, 2, 32, 0, 1.0, None, None) == OK
 

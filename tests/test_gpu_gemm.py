@@ -148,6 +148,72 @@ def test_gemm_times_identity_is_the_dequantized_operand(fmt, layout, M, K):
         np.testing.assert_array_equal(zero_sign_free(T.bf16_bits(c2)), want.T)
 
 
+# scale-byte windows in which every dequantized value is exact in f16 (the kernel then uses f16
+# operands; outside, bf16 operands, with a second multiply above 2^15)
+F16_WINDOW = {O.E2M1: (104, 140), O.E4M3: (112, 134)}
+
+
+@pytest.mark.parametrize("where", ["inside", "edges", "below", "above", "some_rows"])
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemm_scale_ranges(fmt, layout, where):
+    """Scale bytes inside the f16 window, on its edges, below it, above it (X up to 32), and
+    outside it in a few rows only (one CTA row block takes bf16 operands, the others f16)."""
+    M, N, K = 300, 264, 640
+    lo, hi = F16_WINDOW[fmt]
+    kinds = ["inside", "edges", "below", "above", "some_rows"]
+    rng = np.random.default_rng(100 * fmt + 10 * layout + kinds.index(where))
+    ranges = {"inside": (lo, hi + 1), "edges": (lo, hi + 1), "below": (lo - 20, lo + 2),
+              "above": (hi - 2, 160), "some_rows": (lo, hi + 1)}
+    a, sa = random_operand(rng, M, K, fmt, layout, *ranges[where])
+    b, sb = random_operand(rng, N, K, fmt, layout, *ranges[where])
+    if where in ("edges", "some_rows"):
+        la = T.unswizzle(sa, M, K) if layout == O.SWIZZLED else sa
+        lb = T.unswizzle(sb, N, K) if layout == O.SWIZZLED else sb
+        if where == "edges":
+            la[::2, ::3] = lo
+            la[1::2, ::3] = hi
+            lb[::3, 1::2] = hi
+        else:
+            la[200:210] = rng.integers(hi + 1, hi + 20, la[200:210].shape)
+        if layout == O.SWIZZLED:
+            sa = swizzle(la, M, K)
+            sb = swizzle(lb, N, K)
+    C_gpu = bf16_to_f64(mxq.mx_gemm(dev(a), dev(sa), dev(b), dev(sb), K, fmt, layout))
+    C_ref = O.gemm(a, sa, b, sb, K, fmt, layout)
+    S = exact_S(a, sa, b, sb, K, fmt, layout)
+    assert_gemm_close(C_gpu, C_ref, gemm_tolerance(C_ref, K, 1.0, S), where)
+
+
+def swizzle(lin, rows, K):
+    """Linear [rows, K/32] scale bytes -> the swizzled layout (pads 0), by the oracle's offset."""
+    shape = O.scales_shape(rows, K, O.SWIZZLED)
+    out = np.zeros(shape, dtype=np.uint8).reshape(-1)
+    r, c = np.meshgrid(np.arange(rows), np.arange(K // 32), indexing="ij")
+    off = np.vectorize(O.swizzled_offset)(r, c, shape[1])
+    out[off.reshape(-1)] = lin.reshape(-1)
+    return out.reshape(shape)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemm_times_identity_inside_the_f16_window(fmt, layout):
+    """The identity product with every scale byte inside the f16 window (f16 operands): C equals
+    the oracle's dequantize bit for bit."""
+    M, K = 256, 1024
+    lo, hi = F16_WINDOW[fmt]
+    rng = np.random.default_rng(77 + fmt + 3 * layout)
+    a, sa = random_operand(rng, M, K, fmt, layout, lo=lo, hi=hi + 1)
+    if layout == O.SWIZZLED:  # pads inside the window too, though never read
+        sa[:] = np.where(sa == 0, lo, sa)
+    ident, si = identity_operand(K, fmt, layout)
+    want = zero_sign_free(O.dequantize(a, sa, K, fmt, layout))
+    c1 = mxq.mx_gemm(dev(a), dev(sa), dev(ident), dev(si), K, fmt, layout)
+    np.testing.assert_array_equal(zero_sign_free(T.bf16_bits(c1)), want)
+    c2 = mxq.mx_gemm(dev(ident), dev(si), dev(a), dev(sa), K, fmt, layout)
+    np.testing.assert_array_equal(zero_sign_free(T.bf16_bits(c2)), want.T)
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_gemm_nan_scale_poisons_its_rows_and_columns(fmt):
     M, N, K = 160, 144, 256
