@@ -7,25 +7,28 @@
 // matmul_mxf4_bf16_tn(a_e2m1, b_e2m1, a_e8m0, b_e8m0, alpha) compared with the matmul of the
 // dequantized operands).
 //
-// Each CTA computes one 128 x 256 tile of C, K in steps of 64:
-//   warp 12      one thread loads each step's raw codes with the tensor-memory accelerator: A's
-//                128 rows and B's 256 rows of 32 (E2M1) or 64 (E4M3) code bytes, 32- or
-//                64-byte swizzled so that a thread reading its own row hits distinct banks,
-//                into a ring of four stages;
-//   warps 0..3   A converters, one thread per row of A: the step's 64 codes and two scale bytes
-//                -> 64 bf16 values decode(code) * 2^(byte - 127) (rounded once to bf16; exact for
-//                every E2M1 code and for E4M3 unless below the bf16 range), written straight
-//                into tensor memory (tcgen05.st; row i in lane i, two values per column), the
-//                form in which the MMA reads its A operand;
+// Each CTA computes one 128 x 256 tile of C, K in steps of 64 (warp numbers for the default of
+// one converter thread per row, MX_GEMM_SPLIT 1; with 2, two threads share a row, one block
+// each, and there are twice as many converter warps):
+//   warp 12      one thread loads the raw codes with the tensor-memory accelerator, 128 code
+//                bytes of each of A's 128 and B's 256 rows per stage (4 steps of E2M1, 2 of
+//                E4M3: one full line per row), 128-byte swizzled so that threads reading their
+//                own rows hit distinct banks, into a ring of two stages;
+//   warps 0..3   A converters, one thread per row of A (warp w: rows 32 w .. +31): the step's 64
+//                codes and two scale bytes -> 64 values decode(code) * 2^(byte - 127) (rounded
+//                once to bf16; exact for every E2M1 code and for E4M3 unless below the bf16
+//                range), written straight into tensor memory (tcgen05.st; row i in lane i, two
+//                values per column), the form in which the MMA reads its A operand;
 //   warps 4..11  B converters, one thread per row of B: the same values written to shared
 //                memory as 256 rows x 128 bytes, K-major, 128-byte swizzled (16-byte chunk c of
 //                row r at chunk c ^ (r % 8)), the layout a shared-memory descriptor reads;
-//   warp 13      allocates the tensor memory (accumulator: 256 fp32 columns; A: three stages of
+//   warp 13      allocates the tensor memory (accumulator: 256 fp32 columns; A: four stages of
 //                32 columns) and, from one lane, issues per step four tcgen05.mma kind::f16
 //                (M = 128, N = 256, K = 16, A from tensor memory, B from shared memory,
-//                bf16 x bf16 -> fp32) and commits them to the step's "empty" barrier;
+//                f16 or bf16 products summed in fp32) and commits them to the step's "empty"
+//                barrier;
 //   warps 0..7   epilogue: tcgen05.ld of the accumulator, times alpha, rounded to bf16, 16-byte
-//                stores (warps 0-3 columns 0-127, warps 4-7 columns 128-255).
+//                stores (warp w: rows 32 (w % 4) .. +31, columns 128 (w / 4) .. +127).
 // Operand type. When every scale byte of the CTA's rows lies in the window where every value
 // decode(code) * 2^X (X = byte - 127) is exact in f16 (E2M1: X in [-23, 13]; E4M3: [-15, 7]),
 // the operands are f16: two codes take one hardware conversion to f16x2 (exact) and one f16x2
@@ -49,22 +52,37 @@ namespace {
 using namespace tc;
 
 constexpr int kBM = 128, kBN = 256, kBK = 64;
-constexpr int kRawStages = 4;   // raw code stages (tensor-memory-accelerator ring)
-constexpr int kOpStages = 3;    // operand stages (A in tensor memory, B in shared memory)
-constexpr int kAWarps = 4, kBWarps = 8, kConvWarps = kAWarps + kBWarps;
+constexpr int kRawStages = 2;   // raw code stages (tensor-memory-accelerator ring)
+constexpr int kOpStages = 4;    // operand stages (A in tensor memory, B in shared memory)
+// kSplit converter threads per row, each taking 2 / kSplit of the step's two 32-element blocks.
+#ifndef MX_GEMM_SPLIT
+#define MX_GEMM_SPLIT 1
+#endif
+constexpr int kSplit = MX_GEMM_SPLIT;
+constexpr int kBlocksPerThread = 2 / kSplit;
+constexpr int kAWarps = 4 * kSplit, kBWarps = 8 * kSplit, kConvWarps = kAWarps + kBWarps;
 constexpr int kTmaWarp = kConvWarps, kMmaWarp = kConvWarps + 1;
-constexpr int kGemmThreads = (kConvWarps + 2) * 32;  // 448
+constexpr int kGemmThreads = (kConvWarps + 2) * 32;
+// epilogue: 4 lane quarters x kEpiCols column slices of the accumulator, one warp each
+constexpr int kEpiWarps = kConvWarps >= 16 ? 16 : 8;
+constexpr int kEpiCols = kBN / (kEpiWarps / 4);
+static_assert(kEpiWarps <= kConvWarps, "the epilogue runs on converter warps");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kBN;            // fp32 accumulator columns
 constexpr uint32_t kAStageCols = kBK / 2;     // bf16 pairs of a 64-wide K step
 constexpr int kBOpBytes = kBN * kBK * 2;      // 32 KiB of bf16 per B stage
 constexpr unsigned long long kGemmWaitNs = 2000000000ull;  // 2 s
 
+// A raw stage holds 128 code bytes of each row (kSteps K steps: 4 of E2M1, 2 of E4M3), so that
+// every row of a box is one full 128-byte line; rows 128-byte swizzled (16-byte chunk q of row
+// r at q ^ (r % 8)).
 template <int FMT>
 struct RawLayout {
   static constexpr int kRowBytes = FMT == kFmtE2M1 ? 32 : 64;  // code bytes of a row per step
-  static constexpr int kABytes = kBM * kRowBytes;
-  static constexpr int kStageBytes = (kBM + kBN) * kRowBytes;  // 12 or 24 KiB
+  static constexpr int kPitch = 128;                           // code bytes of a row per stage
+  static constexpr int kSteps = kPitch / kRowBytes;
+  static constexpr int kABytes = kBM * kPitch;
+  static constexpr int kStageBytes = (kBM + kBN) * kPitch;     // 48 KiB
 };
 
 template <int FMT>
@@ -100,30 +118,27 @@ __device__ __forceinline__ BlockFactors block_factors(uint32_t sb) {
   return f;
 }
 
-// One row's 64 codes of a step (raw[]: E2M1 8 words, E4M3 16 words, lower K first) under the
-// scale bytes sb0 (elements 0-31) and sb1 (32-63) -> 32 bf16x2 words, lower K in the low half.
+// One block of a row (32 codes, raw[]: E2M1 4 words, E4M3 8 words, lower K first) under the
+// scale byte sb -> 16 bf16x2 words, lower K in the low half.
 template <int FMT>
-__device__ __forceinline__ void convert_row(const uint32_t* raw, uint32_t sb0, uint32_t sb1,
-                                            uint32_t* out) {
-  const BlockFactors b0 = block_factors(sb0), b1 = block_factors(sb1);
+__device__ __forceinline__ void convert_block(const uint32_t* raw, uint32_t sb, uint32_t* out) {
+  const BlockFactors b = block_factors(sb);
   if (FMT == kFmtE2M1) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t f = j < 4 ? b0.f1 : b1.f1;
+    for (int j = 0; j < 4; ++j) {
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         uint32_t h;
         asm("{\n\t.reg .b8 c;\n\tcvt.u8.u32 c, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, c;\n\t}"
             : "=r"(h)
             : "r"(raw[j] >> (8 * t)));
-        out[4 * j + t] = hmul2_bf16(f16x2_to_bf16x2_lowered(h), f);
+        out[4 * j + t] = hmul2_bf16(f16x2_to_bf16x2_lowered(h), b.f1);
       }
     }
   } else {
     uint32_t nan = 0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t f = j < 8 ? b0.f1 : b1.f1;
+    for (int j = 0; j < 8; ++j) {
       const uint32_t w = raw[j];
       nan |= (w & 0x7F7F7F7Fu) + 0x01010101u;  // a byte reaches 0x80 iff it is S.1111.111
 #pragma unroll
@@ -132,12 +147,12 @@ __device__ __forceinline__ void convert_row(const uint32_t* raw, uint32_t sb0, u
         asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
             : "=r"(h)
             : "r"(w >> (16 * t)));
-        out[2 * j + t] = hmul2_bf16(f16x2_to_bf16x2_lowered(h), f);
+        out[2 * j + t] = hmul2_bf16(f16x2_to_bf16x2_lowered(h), b.f1);
       }
     }
     if (nan & 0x80808080u) {  // E4M3 NaN codes: their values are the bf16 NaN
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < 8; ++j) {
         const uint32_t n = ((raw[j] & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -150,13 +165,9 @@ __device__ __forceinline__ void convert_row(const uint32_t* raw, uint32_t sb0, u
       }
     }
   }
-  if (b0.big) {
+  if (b.big) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) out[i] = hmul2_bf16(out[i], b0.f2);
-  }
-  if (b1.big) {
-#pragma unroll
-    for (int i = 16; i < 32; ++i) out[i] = hmul2_bf16(out[i], b1.f2);
+    for (int i = 0; i < 16; ++i) out[i] = hmul2_bf16(out[i], b.f2);
   }
 }
 
@@ -180,14 +191,13 @@ __device__ __forceinline__ uint32_t f16_pow2x2(uint32_t sb) {
   return h * 0x00010001u;
 }
 
-// The f16 form of convert_row, scale bytes inside the window: values exact, lower K low half.
+// The f16 form of convert_block, scale byte inside the window: values exact.
 template <int FMT>
-__device__ __forceinline__ void convert_row_f16(const uint32_t* raw, uint32_t sb0, uint32_t sb1,
-                                                uint32_t* out) {
-  const uint32_t m0 = f16_pow2x2(sb0), m1 = f16_pow2x2(sb1);
+__device__ __forceinline__ void convert_block_f16(const uint32_t* raw, uint32_t sb, uint32_t* out) {
+  const uint32_t m = f16_pow2x2(sb);
   if (FMT == kFmtE2M1) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 4; ++j) {
       uint32_t h[4];
       asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\tmov.b32 {c0, c1, c2, c3}, %4;\n\t"
           "cvt.rn.f16x2.e2m1x2 %0, c0;\n\tcvt.rn.f16x2.e2m1x2 %1, c1;\n\t"
@@ -195,18 +205,18 @@ __device__ __forceinline__ void convert_row_f16(const uint32_t* raw, uint32_t sb
           : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
           : "r"(raw[j]));
 #pragma unroll
-      for (int t = 0; t < 4; ++t) out[4 * j + t] = hmul2_f16(h[t], j < 4 ? m0 : m1);
+      for (int t = 0; t < 4; ++t) out[4 * j + t] = hmul2_f16(h[t], m);
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < 8; ++j) {
       uint32_t h[2];
       asm("{\n\t.reg .b16 c0, c1;\n\tmov.b32 {c0, c1}, %2;\n\t"
           "cvt.rn.f16x2.e4m3x2 %0, c0;\n\tcvt.rn.f16x2.e4m3x2 %1, c1;\n\t}"
           : "=r"(h[0]), "=r"(h[1])
           : "r"(raw[j]));
-      out[2 * j] = hmul2_f16(h[0], j < 8 ? m0 : m1);
-      out[2 * j + 1] = hmul2_f16(h[1], j < 8 ? m0 : m1);
+      out[2 * j] = hmul2_f16(h[0], m);
+      out[2 * j + 1] = hmul2_f16(h[1], m);
     }
   }
 }
@@ -255,12 +265,14 @@ __device__ __forceinline__ uint4 load_scale_chunk(const uint8_t* p) {  // 16-byt
   return v;
 }
 
-// Whether every scale byte of this converter's share of the CTA's rows (A: the row block of
-// 128 rows; B: two) lies inside [lo, hi]. Rows past M / N, and the padding columns of the
-// swizzled layout, are not looked at.
+// Whether every scale byte of this converter's share of the CTA's rows (A: one block of 128
+// rows; B: two) lies inside [lo, hi]. Swizzled: the 128 kSplit threads of a row block share
+// its contiguous tiles (t: the thread's index within the block, row0 its first row); linear:
+// thread (row, part 0) takes the row (grow), the others nothing. Rows past M / N, and the padding columns of
+// the swizzled layout, are not looked at.
 template <bool SWZ>
-__device__ __forceinline__ bool scales_inside(const GemmArgs& a, bool is_a, int r, int64_t grow,
-                                              uint32_t lo, uint32_t hi) {
+__device__ __forceinline__ bool scales_inside(const GemmArgs& a, bool is_a, int t, int64_t row0,
+                                              int64_t grow, int part, uint32_t lo, uint32_t hi) {
   ByteRange br;
   const uint8_t* sc = is_a ? a.a_scales : a.b_scales;
   const int64_t scols = is_a ? a.a_scale_cols : a.b_scale_cols;
@@ -269,13 +281,13 @@ __device__ __forceinline__ bool scales_inside(const GemmArgs& a, bool is_a, int 
   if (SWZ) {
     // the 128-row block's 512-byte tiles are contiguous: chunk i (16 bytes) of the block holds
     // rows q, q + 32, q + 64, q + 96 (q = i % 32) of tile i / 32, 4 blocks each
-    const int64_t row0 = (is_a ? 0 : (r >> 7) * 128) + grow - r;  // first row of the block
-    const int u = is_a ? r : (r & 127);
+    const int u = t;
     if (row0 < rows) {
       const int64_t ctiles = scols >> 2;
       const int kb_last = (int)((a.K / 32) & 3);  // 2 when the last tile holds 2 pad columns
       const uint8_t* base = sc + (row0 >> 7) * ctiles * 512;
-      for (int64_t i = u; i < ctiles * 32; i += 128) {
+#pragma unroll 8
+      for (int64_t i = u; i < ctiles * 32; i += 128 * kSplit) {
         const uint4 v = load_scale_chunk(base + i * 16);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         const bool last = i / 32 == ctiles - 1 && kb_last != 0;
@@ -287,9 +299,10 @@ __device__ __forceinline__ bool scales_inside(const GemmArgs& a, bool is_a, int 
         }
       }
     }
-  } else if (grow < rows) {
+  } else if (grow < rows && part == 0) {
     const uint8_t* p = sc + grow * scols;
     if ((scols & 15) == 0 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+#pragma unroll 8
       for (int64_t i = 0; i < scols; i += 16) {
         const uint4 v = load_scale_chunk(p + i);
         br.add(v.x);
@@ -312,25 +325,25 @@ __device__ __forceinline__ void gemm_loads(const CUtensorMap& amap, const CUtens
   using R = RawLayout<FMT>;
   const int nk = c.nk;
   bool failed = false;
+  const int nstages = (nk + R::kSteps - 1) / R::kSteps;
   int issued = 0;
-  for (int kk = 0; kk < nk; ++kk) {
-    const int s = kk % kRawStages;
-    if (kk >= kRawStages) {
-      mbar_wait(smem_u32(c.raw_empty + s), ((kk / kRawStages) & 1) ^ 1, &failed,
-                kGemmWaitNs, a.err);
+  for (int rs = 0; rs < nstages; ++rs) {
+    const int s = rs % kRawStages;
+    if (rs >= kRawStages) {
+      mbar_wait(smem_u32(c.raw_empty + s), ((rs / kRawStages) & 1) ^ 1, &failed, kGemmWaitNs,
+                a.err);
     }
     if (failed) break;
     const uint32_t dst = smem_u32(c.raw + s * R::kStageBytes);
     mbar_arrive_expect_tx(smem_u32(c.raw_full + s), R::kStageBytes);
-    tma_load_box(dst, &amap, kk * R::kRowBytes, (int)c.m0, smem_u32(c.raw_full + s));
-    tma_load_box(dst + R::kABytes, &bmap, kk * R::kRowBytes, (int)c.n0,
-                 smem_u32(c.raw_full + s));
-    issued = kk + 1;
+    tma_load_box(dst, &amap, rs * R::kPitch, (int)c.m0, smem_u32(c.raw_full + s));
+    tma_load_box(dst + R::kABytes, &bmap, rs * R::kPitch, (int)c.n0, smem_u32(c.raw_full + s));
+    issued = rs + 1;
   }
   // loads still in flight land before the CTA's shared memory goes away
   bool drain_failed = false;
-  for (int kk = issued > kRawStages ? issued - kRawStages : 0; kk < issued; ++kk) {
-    mbar_wait(smem_u32(c.raw_full + kk % kRawStages), (kk / kRawStages) & 1, &drain_failed,
+  for (int rs = issued > kRawStages ? issued - kRawStages : 0; rs < issued; ++rs) {
+    mbar_wait(smem_u32(c.raw_full + rs % kRawStages), (rs / kRawStages) & 1, &drain_failed,
               kGemmWaitNs, a.err);
   }
 }
@@ -344,74 +357,104 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
   bool failed = false;
 
   if (warp < kConvWarps) {
-    // ---------------- converters: one row each ----------------
+    // ---------------- converters: blocks part * kBlocksPerThread .. of row r ----------------
     const bool is_a = warp < kAWarps;
-    const int r = is_a ? tid : tid - kAWarps * 32;
+    const int wq = is_a ? warp : warp - kAWarps;
+    const int r = (wq & (is_a ? 3 : 7)) * 32 + lane;  // A: lane quarter = warp % 4
+    const int part = is_a ? wq >> 2 : wq >> 3;
     const int64_t grow = (is_a ? c.m0 : c.n0) + r;
     const bool valid = grow < (is_a ? a.M : a.N);
     const uint8_t* sc = is_a ? a.a_scales : a.b_scales;
     const int64_t scols = is_a ? a.a_scale_cols : a.b_scale_cols;
-    // scale bytes of step kk (two blocks): linear row-major, or the row's 4-byte slot of the
-    // 512-byte tile holding blocks 4t .. 4t + 3 (t = kk / 2)
+    // scale bytes of blocks 2 kk + part * kBlocksPerThread ..: linear row-major, or bytes
+    // (2 kk + ..) % 4 of the row's 4-byte slot in the 512-byte tile holding blocks 4t .. 4t + 3
+    // (t = kk / 2)
     const uint8_t* sbase =
-        SWZ ? sc + ((grow >> 7) * (scols >> 2)) * 512 + (grow & 31) * 16 + ((grow >> 5) & 3) * 4
-            : sc + grow * scols;
+        SWZ ? sc + ((grow >> 7) * (scols >> 2)) * 512 + (grow & 31) * 16 + ((grow >> 5) & 3) * 4 +
+                  part * kBlocksPerThread
+            : sc + grow * scols + part * kBlocksPerThread;
     auto scale_at = [&](int kk) -> uint32_t {
-      if (!valid || kk >= nk) return 0x7F7Fu;
-      return load_scale_pair(SWZ ? sbase + (int64_t)(kk >> 1) * 512 + (kk & 1) * 2
-                                 : sbase + 2 * (int64_t)kk);
+      if (!valid || kk >= nk) return kBlocksPerThread == 2 ? 0x7F7Fu : 0x7Fu;
+      const uint8_t* p = SWZ ? sbase + (int64_t)(kk >> 1) * 512 + (kk & 1) * 2
+                             : sbase + 2 * (int64_t)kk;
+      return kBlocksPerThread == 2 ? load_scale_pair(p) : load_u8(p);
     };
-    uint32_t sc_next = scale_at(0), sc_after = scale_at(1);
-    const uint32_t raw_row = (is_a ? 0u : (uint32_t)R::kABytes) + (uint32_t)r * R::kRowBytes;
-    for (int kk = 0; kk < nk; ++kk) {
-      const int sr = kk % kRawStages, so = kk % kOpStages;
-      const uint32_t scv = sc_next;
-      sc_next = sc_after;
-      sc_after = scale_at(kk + 2);
-      mbar_wait(smem_u32(c.raw_full + sr), (kk / kRawStages) & 1, &failed, kGemmWaitNs, a.err);
-      failed = __any_sync(0xFFFFFFFFu, failed);
-      if (failed) break;
-      uint32_t w[R::kRowBytes / 4];
+    constexpr int kPartBytes = R::kRowBytes / kSplit;  // code bytes this thread converts
+    constexpr int kBlockWords = R::kRowBytes / 8;      // 32-bit words of codes of one block
+    const uint32_t raw_row = (is_a ? 0u : (uint32_t)R::kABytes) + (uint32_t)r * R::kPitch;
+    // one step; returns false once a wait has run out (warp-uniform)
+    auto step = [&](int kk, uint32_t sb) -> bool {
+      const int rs = kk / R::kSteps, sub = kk % R::kSteps;  // raw stage, step within it
+      const int sr = rs % kRawStages, so = kk % kOpStages;
+      if (sub == 0) {
+        mbar_wait(smem_u32(c.raw_full + sr), (rs / kRawStages) & 1, &failed, kGemmWaitNs, a.err);
+        failed = __any_sync(0xFFFFFFFFu, failed);
+        if (failed) return false;
+      }
+      uint32_t w[kPartBytes / 4];
       const uint8_t* row = c.raw + sr * R::kStageBytes + raw_row;
 #pragma unroll
-      for (int q = 0; q < R::kRowBytes / 16; ++q) {
-        // swizzled box: 16-byte chunk q of row r at q ^ (r / 4 % 2) (32-byte rows) or
-        // q ^ (r / 2 % 4) (64-byte rows)
-        const int pq = FMT == kFmtE2M1 ? (q ^ ((r >> 2) & 1)) : (q ^ ((r >> 1) & 3));
-        const uint4 v = *reinterpret_cast<const uint4*>(row + pq * 16);
-        w[4 * q] = v.x;
-        w[4 * q + 1] = v.y;
-        w[4 * q + 2] = v.z;
-        w[4 * q + 3] = v.w;
+      for (int j = 0; j < kPartBytes / 16; ++j) {
+        const int q = sub * (R::kRowBytes / 16) + part * (kPartBytes / 16) + j;
+        const uint4 v = *reinterpret_cast<const uint4*>(row + ((q ^ (r & 7)) * 16));  // 128-B swizzle
+        w[4 * j] = v.x;
+        w[4 * j + 1] = v.y;
+        w[4 * j + 2] = v.z;
+        w[4 * j + 3] = v.w;
       }
-      uint32_t out[32];
-      if (F16) {
-        convert_row_f16<FMT>(w, scv & 0xFFu, scv >> 8, out);
-      } else {
-        convert_row<FMT>(w, scv & 0xFFu, scv >> 8, out);
+      uint32_t out[16 * kBlocksPerThread];
+#pragma unroll
+      for (int i = 0; i < kBlocksPerThread; ++i) {
+        const uint32_t b = (sb >> (8 * i)) & 0xFFu;
+        if (F16) {
+          convert_block_f16<FMT>(w + i * kBlockWords, b, out + 16 * i);
+        } else {
+          convert_block<FMT>(w + i * kBlockWords, b, out + 16 * i);
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(c.raw_empty + sr));  // raw bytes consumed
+      if (sub == R::kSteps - 1 || kk == nk - 1) {  // the stage's raw bytes are consumed
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(c.raw_empty + sr));
+      }
       if (kk >= kOpStages) {
         mbar_wait(smem_u32(c.op_empty + so), ((kk / kOpStages) & 1) ^ 1, &failed, kGemmWaitNs,
                   a.err);
         failed = __any_sync(0xFFFFFFFFu, failed);
-        if (failed) break;
+        if (failed) return false;
       }
       if (is_a) {
-        tmem_st32(tmem + ((uint32_t)(warp * 32) << 16) + kAccCols + so * kAStageCols, out);
+        const uint32_t ta = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kAccCols +
+                            so * kAStageCols + part * (kAStageCols / kSplit);
+        if (kBlocksPerThread == 2) {
+          tmem_st32_async(ta, out);
+        } else {
+          tmem_st16_async(ta, out);
+        }
+        tmem_wait_st();
         tc_fence_before();
       } else {
         uint8_t* dst = c.bop + so * kBOpBytes + r * 128;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int j = 0; j < 8 / kSplit; ++j) {
+          const int q = part * (8 / kSplit) + j;
           *reinterpret_cast<uint4*>(dst + ((q ^ (r & 7)) << 4)) =
-              make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+              make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
         }
         fence_proxy_async_smem();  // visible to the tensor cores
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(c.op_full + so));
+      return true;
+    };
+    // two steps per iteration, each with its own scale register, reloaded right after its use
+    // for the step two later (no register move waits on a load in flight)
+    uint32_t sc0 = scale_at(0), sc1 = scale_at(1);
+    for (int kk = 0; kk < nk; kk += 2) {
+      if (!step(kk, sc0)) break;
+      sc0 = scale_at(kk + 2);
+      if (kk + 1 >= nk) break;
+      if (!step(kk + 1, sc1)) break;
+      sc1 = scale_at(kk + 3);
     }
   } else if (warp == kMmaWarp && lane == 0) {
     // ---------------- MMA issuer ----------------
@@ -434,17 +477,17 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
     mbar_wait(smem_u32(c.acc_full), 0, &drain_failed, kGemmWaitNs, a.err);
   }
 
-  if (warp < 8) {
+  if (warp < kEpiWarps) {
     // ---------------- epilogue ----------------
     bool efailed = failed;
     mbar_wait(smem_u32(c.acc_full), 0, &efailed, kGemmWaitNs, a.err);
     efailed = __any_sync(0xFFFFFFFFu, efailed);
     tc_fence_after();
     const int quarter = warp & 3;
-    const uint32_t col0 = (uint32_t)(warp >> 2) * 128;
+    const uint32_t col0 = (uint32_t)(warp >> 2) * kEpiCols;
     const int64_t row = c.m0 + quarter * 32 + lane;
 #pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
+    for (int cb = 0; cb < kEpiCols / 32; ++cb) {
       float y[32];
       if (!efailed) tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col0 + cb * 32, y);
       if (efailed || row >= a.M) continue;
@@ -516,10 +559,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     if (warp < kConvWarps) {  // f16 window vote over the CTA's scale bytes
       const bool is_a = warp < kAWarps;
-      const int r = is_a ? tid : tid - kAWarps * 32;
-      const int64_t grow = (is_a ? c.m0 : c.n0) + r;
-      const bool in =
-          scales_inside<SWZ>(a, is_a, r, grow, F16Window<FMT>::kLo, F16Window<FMT>::kHi);
+      const int wq = is_a ? warp : warp - kAWarps;
+      const int r = (wq & (is_a ? 3 : 7)) * 32 + (tid & 31);
+      const int part = is_a ? wq >> 2 : wq >> 3;
+      // thread within its row block (128 * kSplit threads per block)
+      const int bt = is_a ? tid : tid - kAWarps * 32;
+      const int t = bt % (128 * kSplit);
+      const int64_t row0 = is_a ? c.m0 : c.n0 + (bt / (128 * kSplit)) * 128;
+      const bool in = scales_inside<SWZ>(a, is_a, t, row0, (is_a ? c.m0 : c.n0) + r, part,
+                                         F16Window<FMT>::kLo, F16Window<FMT>::kHi);
       if (!__all_sync(0xFFFFFFFFu, in) && (tid & 31) == 0) atomicAdd(outside, 1u);
     }
     // converters and the MMA warp (the load warp is already running)
@@ -543,14 +591,13 @@ cudaError_t launch_t(const GemmArgs& a, cudaStream_t stream) {
   constexpr int smem = gemm_smem<FMT>();
   if (resident_ctas(k, kGemmThreads, smem, 1) <= 0) return cudaErrorInvalidConfiguration;
   const int64_t code_row = FMT == kFmtE2M1 ? a.K / 2 : a.K;
-  const CUtensorMapSwizzle swz =
-      FMT == kFmtE2M1 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B;
   CUtensorMap amap, bmap;
   cudaError_t err = make_tensor_map_2d(&amap, a.a_codes, a.M, code_row,
-                                       CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, R::kRowBytes, kBM, swz);
+                                       CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, R::kPitch, kBM, swz);
   if (err != cudaSuccess) return err;
   err = make_tensor_map_2d(&bmap, a.b_codes, a.N, code_row, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                           R::kRowBytes, kBN, swz);
+                           R::kPitch, kBN, swz);
   if (err != cudaSuccess) return err;
   const dim3 grid((unsigned)((a.N + kBN - 1) / kBN), (unsigned)((a.M + kBM - 1) / kBM));
   return launch_pdl(&mx_gemm_kernel<FMT, SWZ>, grid, dim3(kGemmThreads), smem, stream, amap,
