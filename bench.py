@@ -56,6 +56,8 @@ def parse_args():
     p.add_argument("--case", choices=sorted(CASES), default=None,
                    help="run one other workload only (for profiler captures): warmup + steps "
                         "launches, one JSON line with its kernel-only GB/s")
+    p.add_argument("--gemm-shapes", default="o_proj,down_proj,square,decode",
+                   help="--case gemm: comma-separated subset of o_proj, down_proj, square, decode")
     p.add_argument("--tiles-per-sm", type=int, default=8,
                    help="rotate_quant_tiles: x[128, 128 * SMs * n] gives exactly n tiles per SM")
     return p.parse_args()
@@ -889,6 +891,8 @@ def run_gemm_case(args, dev):
     peak = peaks.get("bf16_tflops", 1900.0)
     shapes = [("o_proj", 4096, 8192, 8192), ("down_proj", 1024, 8192, 28672),
               ("square", 8192, 8192, 8192), ("decode", 16, 8192, 8192)]
+    wanted = set(args.gemm_shapes.split(","))
+    shapes = [sh for sh in shapes if sh[0] in wanted]
     steps = max(1, args.steps)
 
     def clock(fn):
