@@ -880,6 +880,29 @@ def run_case(args):
           flush=True)
 
 
+def time_oracle_gemm(ca, sa, cw, sw, K, fmt, layout, rows, min_seconds=2.0):
+    """The oracle's GEMM (dequantize, then a float64 matmul) of A's first `rows` rows (one
+    128-row block of the swizzled scales) against the whole B, repeated until min_seconds."""
+    import oracle as O
+    O.build()
+    a = ca[:rows].cpu().numpy()
+    s_a = sa[:128].cpu().numpy() if layout == 1 else sa[:rows].cpu().numpy()
+    b, s_b = cw.cpu().numpy(), sw.cpu().numpy()
+    N = b.shape[0]
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        O.gemm(a, s_a, b, s_b, K, fmt, layout)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    return {"TFLOP/s": 2.0 * rows * N * K * passes / dt / 1e12, "kind": "oracle",
+            "cores": os.cpu_count() or 1,
+            "sample": f"C rows 0..{rows - 1} (A[{rows},{K}] x B[{N},{K}]^T), {passes} passes in "
+                      f"{dt:.1f} s: C dequantize of both operands + numpy float64 matmul"}
+
+
 def run_gemm_case(args, dev):
     """TFLOP/s (2 M N K per call) of mx_gemm, launches back to back after --warmup, against the
     measured bf16 tensor peak; the same product through cuBLAS on bf16 operands for context."""
@@ -933,6 +956,9 @@ def run_gemm_case(args, dev):
                 "frac_of_bf16_peak": flops / t / 1e12 / peak,
                 "cublas_bf16_us": t_mm * 1e6, "cublas_bf16_TFLOP/s": flops / t_mm / 1e12,
                 "dequant_then_cublas_us": t_two * 1e6}
+            if name == shapes[0][0]:  # the oracle beside it, on a bounded sample of C's rows
+                res[f"{name}_{fname}"]["cpu_baseline"] = time_oracle_gemm(
+                    ca, sa, cw, sw, K, fmt, mxq.SWIZZLED, rows=min(M, 128))
             del ca, sa, cw, sw, c, da, dw
         del xa, xw
         torch.cuda.empty_cache()
