@@ -51,7 +51,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kBM = 128, kBK = 64;
 constexpr int kRawStages = 2;   // raw code stages (tensor-memory-accelerator ring)
 constexpr int kOpStages = 4;    // operand stages (A in tensor memory, B in shared memory)
 // kSplit converter threads per row, each taking 2 / kSplit of the step's two 32-element blocks.
@@ -60,34 +60,44 @@ constexpr int kOpStages = 4;    // operand stages (A in tensor memory, B in shar
 #endif
 constexpr int kSplit = MX_GEMM_SPLIT;
 constexpr int kBlocksPerThread = 2 / kSplit;
-constexpr int kAWarps = 4 * kSplit, kBWarps = 8 * kSplit, kConvWarps = kAWarps + kBWarps;
-constexpr int kTmaWarp = kConvWarps, kMmaWarp = kConvWarps + 1;
-constexpr int kGemmThreads = (kConvWarps + 2) * 32;
-// epilogue: 4 lane quarters x kEpiCols column slices of the accumulator, one warp each
-constexpr int kEpiWarps = kConvWarps >= 16 ? 16 : 8;
-constexpr int kEpiCols = kBN / (kEpiWarps / 4);
-static_assert(kEpiWarps <= kConvWarps, "the epilogue runs on converter warps");
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = kBN;            // fp32 accumulator columns
+constexpr int kAWarps = 4 * kSplit;
 constexpr uint32_t kAStageCols = kBK / 2;     // bf16 pairs of a 64-wide K step
-constexpr int kBOpBytes = kBN * kBK * 2;      // 32 KiB of bf16 per B stage
+
+// Everything that depends on the tile's width BN (columns of C, rows of B): 256 for large
+// problems, 64 when 128 x 256 tiles would not fill the SMs (two CTAs per SM then).
+template <int BN>
+struct Tile {
+  static constexpr int kBRowWarps = BN / 32;  // warps covering B's rows once
+  static constexpr int kBWarps = kBRowWarps * kSplit, kConvWarps = kAWarps + kBWarps;
+  static constexpr int kTmaWarp = kConvWarps, kMmaWarp = kConvWarps + 1;
+  static constexpr int kThreads = (kConvWarps + 2) * 32;
+  // epilogue: 4 lane quarters x column slices of the accumulator, one converter warp each
+  static constexpr int kEpiWarps = kConvWarps >= 16 ? 16 : (kConvWarps >= 8 && BN >= 128 ? 8 : 4);
+  static constexpr int kEpiCols = BN / (kEpiWarps / 4);
+  static constexpr uint32_t kAccCols = BN;  // fp32 accumulator columns
+  static constexpr uint32_t kTmemCols = BN + kOpStages * kAStageCols <= 256 ? 256 : 512;
+  static constexpr int kBOpBytes = BN * kBK * 2;  // bf16 of one B stage (32 or 8 KiB)
+  static constexpr int kMinCtas = BN <= 64 ? 2 : 1;
+  static_assert(kEpiWarps <= kConvWarps, "the epilogue runs on converter warps");
+  static_assert(kEpiCols % 32 == 0, "32-column accumulator loads");
+};
 constexpr unsigned long long kGemmWaitNs = 2000000000ull;  // 2 s
 
 // A raw stage holds 128 code bytes of each row (kSteps K steps: 4 of E2M1, 2 of E4M3), so that
 // every row of a box is one full 128-byte line; rows 128-byte swizzled (16-byte chunk q of row
 // r at q ^ (r % 8)).
-template <int FMT>
+template <int FMT, int BN>
 struct RawLayout {
   static constexpr int kRowBytes = FMT == kFmtE2M1 ? 32 : 64;  // code bytes of a row per step
   static constexpr int kPitch = 128;                           // code bytes of a row per stage
   static constexpr int kSteps = kPitch / kRowBytes;
   static constexpr int kABytes = kBM * kPitch;
-  static constexpr int kStageBytes = (kBM + kBN) * kPitch;     // 48 KiB
+  static constexpr int kStageBytes = (kBM + BN) * kPitch;      // 48 or 24 KiB
 };
 
-template <int FMT>
+template <int FMT, int BN>
 constexpr int gemm_smem() {
-  return 1024 + kOpStages * kBOpBytes + kRawStages * RawLayout<FMT>::kStageBytes +
+  return 1024 + kOpStages * Tile<BN>::kBOpBytes + kRawStages * RawLayout<FMT, BN>::kStageBytes +
          (2 * kRawStages + 2 * kOpStages + 1) * 8 + 16;  // + tmem slot, vote
 }
 
@@ -245,8 +255,8 @@ __device__ __forceinline__ uint32_t load_scale_pair(const uint8_t* p) {
 // Shared-memory carve-up and per-CTA constants of one GEMM CTA.
 template <int FMT>
 struct GemmCta {
-  uint8_t* bop;       // kOpStages x 32 KiB: B operand stages
-  uint8_t* raw;       // kRawStages x RawLayout<FMT>::kStageBytes: raw code stages
+  uint8_t* bop;       // kOpStages x Tile::kBOpBytes: B operand stages
+  uint8_t* raw;       // kRawStages x RawLayout::kStageBytes: raw code stages
   uint64_t* raw_full;
   uint64_t* raw_empty;
   uint64_t* op_full;
@@ -266,13 +276,14 @@ __device__ __forceinline__ uint4 load_scale_chunk(const uint8_t* p) {  // 16-byt
 }
 
 // Whether every scale byte of this converter's share of the CTA's rows (A: one block of 128
-// rows; B: two) lies inside [lo, hi]. Swizzled: the 128 kSplit threads of a row block share
-// its contiguous tiles (t: the thread's index within the block, row0 its first row); linear:
-// thread (row, part 0) takes the row (grow), the others nothing. Rows past M / N, and the padding columns of
+// rows; B: the one or two blocks its rows lie in) lies inside [lo, hi]. Swizzled: the nthreads
+// threads of a row block share its contiguous tiles (t: the thread's index within the block,
+// row0 its first row); linear: thread (row, part 0) takes the row (grow), the others nothing. Rows past M / N, and the padding columns of
 // the swizzled layout, are not looked at.
 template <bool SWZ>
-__device__ __forceinline__ bool scales_inside(const GemmArgs& a, bool is_a, int t, int64_t row0,
-                                              int64_t grow, int part, uint32_t lo, uint32_t hi) {
+__device__ __forceinline__ bool scales_inside(const GemmArgs& a, bool is_a, int t, int nthreads,
+                                              int64_t row0, int64_t grow, int part, uint32_t lo,
+                                              uint32_t hi) {
   ByteRange br;
   const uint8_t* sc = is_a ? a.a_scales : a.b_scales;
   const int64_t scols = is_a ? a.a_scale_cols : a.b_scale_cols;
@@ -287,7 +298,7 @@ __device__ __forceinline__ bool scales_inside(const GemmArgs& a, bool is_a, int 
       const int kb_last = (int)((a.K / 32) & 3);  // 2 when the last tile holds 2 pad columns
       const uint8_t* base = sc + (row0 >> 7) * ctiles * 512;
 #pragma unroll 8
-      for (int64_t i = u; i < ctiles * 32; i += 128 * kSplit) {
+      for (int64_t i = u; i < ctiles * 32; i += nthreads) {
         const uint4 v = load_scale_chunk(base + i * 16);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         const bool last = i / 32 == ctiles - 1 && kb_last != 0;
@@ -319,10 +330,10 @@ __device__ __forceinline__ bool scales_inside(const GemmArgs& a, bool is_a, int 
 
 // Raw code loads (one thread of warp kTmaWarp): runs from the start, independent of the operand
 // type, so that the first stages are in flight while the converters vote.
-template <int FMT>
+template <int FMT, int BN>
 __device__ __forceinline__ void gemm_loads(const CUtensorMap& amap, const CUtensorMap& bmap,
                                            const GemmArgs& a, const GemmCta<FMT>& c) {
-  using R = RawLayout<FMT>;
+  using R = RawLayout<FMT, BN>;
   const int nk = c.nk;
   bool failed = false;
   const int nstages = (nk + R::kSteps - 1) / R::kSteps;
@@ -348,22 +359,28 @@ __device__ __forceinline__ void gemm_loads(const CUtensorMap& amap, const CUtens
   }
 }
 
-template <int FMT, bool SWZ, bool F16>
+template <int FMT, bool SWZ, bool F16, int BN>
 __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>& c) {
-  using R = RawLayout<FMT>;
+  using R = RawLayout<FMT, BN>;
+  using T = Tile<BN>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t tmem = c.tmem;
   const int nk = c.nk;
   bool failed = false;
 
-  if (warp < kConvWarps) {
+  if (warp < T::kConvWarps) {
     // ---------------- converters: blocks part * kBlocksPerThread .. of row r ----------------
     const bool is_a = warp < kAWarps;
     const int wq = is_a ? warp : warp - kAWarps;
-    const int r = (wq & (is_a ? 3 : 7)) * 32 + lane;  // A: lane quarter = warp % 4
-    const int part = is_a ? wq >> 2 : wq >> 3;
+    const int row_warps = is_a ? 4 : T::kBRowWarps;
+    const int r = (wq % row_warps) * 32 + lane;  // A: lane quarter = warp % 4
+    const int part = wq / row_warps;
     const int64_t grow = (is_a ? c.m0 : c.n0) + r;
     const bool valid = grow < (is_a ? a.M : a.N);
+    // narrow tiles (small M): a warp whose rows all lie past M (N) converts nothing; the MMA
+    // then reads stale operand rows, which only reach rows (columns) of C that are not stored.
+    // Wide tiles convert every row (the test costs them registers and 7 %).
+    const bool live = BN > 64 || grow - lane < (is_a ? a.M : a.N);
     const uint8_t* sc = is_a ? a.a_scales : a.b_scales;
     const int64_t scols = is_a ? a.a_scale_cols : a.b_scale_cols;
     // scale bytes of blocks 2 kk + part * kBlocksPerThread ..: linear row-major, or bytes
@@ -391,25 +408,27 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
         failed = __any_sync(0xFFFFFFFFu, failed);
         if (failed) return false;
       }
-      uint32_t w[kPartBytes / 4];
-      const uint8_t* row = c.raw + sr * R::kStageBytes + raw_row;
-#pragma unroll
-      for (int j = 0; j < kPartBytes / 16; ++j) {
-        const int q = sub * (R::kRowBytes / 16) + part * (kPartBytes / 16) + j;
-        const uint4 v = *reinterpret_cast<const uint4*>(row + ((q ^ (r & 7)) * 16));  // 128-B swizzle
-        w[4 * j] = v.x;
-        w[4 * j + 1] = v.y;
-        w[4 * j + 2] = v.z;
-        w[4 * j + 3] = v.w;
-      }
       uint32_t out[16 * kBlocksPerThread];
+      if (live) {
+        uint32_t w[kPartBytes / 4];
+        const uint8_t* row = c.raw + sr * R::kStageBytes + raw_row;
 #pragma unroll
-      for (int i = 0; i < kBlocksPerThread; ++i) {
-        const uint32_t b = (sb >> (8 * i)) & 0xFFu;
-        if (F16) {
-          convert_block_f16<FMT>(w + i * kBlockWords, b, out + 16 * i);
-        } else {
-          convert_block<FMT>(w + i * kBlockWords, b, out + 16 * i);
+        for (int j = 0; j < kPartBytes / 16; ++j) {
+          const int q = sub * (R::kRowBytes / 16) + part * (kPartBytes / 16) + j;
+          const uint4 v = *reinterpret_cast<const uint4*>(row + ((q ^ (r & 7)) * 16));  // 128-B swizzle
+          w[4 * j] = v.x;
+          w[4 * j + 1] = v.y;
+          w[4 * j + 2] = v.z;
+          w[4 * j + 3] = v.w;
+        }
+#pragma unroll
+        for (int i = 0; i < kBlocksPerThread; ++i) {
+          const uint32_t b = (sb >> (8 * i)) & 0xFFu;
+          if (F16) {
+            convert_block_f16<FMT>(w + i * kBlockWords, b, out + 16 * i);
+          } else {
+            convert_block<FMT>(w + i * kBlockWords, b, out + 16 * i);
+          }
         }
       }
       if (sub == R::kSteps - 1 || kk == nk - 1) {  // the stage's raw bytes are consumed
@@ -422,8 +441,10 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
         failed = __any_sync(0xFFFFFFFFu, failed);
         if (failed) return false;
       }
-      if (is_a) {
-        const uint32_t ta = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kAccCols +
+      if (!live) {
+        // nothing to store
+      } else if (is_a) {
+        const uint32_t ta = tmem + ((uint32_t)((warp & 3) * 32) << 16) + T::kAccCols +
                             so * kAStageCols + part * (kAStageCols / kSplit);
         if (kBlocksPerThread == 2) {
           tmem_st32_async(ta, out);
@@ -433,7 +454,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
         tmem_wait_st();
         tc_fence_before();
       } else {
-        uint8_t* dst = c.bop + so * kBOpBytes + r * 128;
+        uint8_t* dst = c.bop + so * T::kBOpBytes + r * 128;
 #pragma unroll
         for (int j = 0; j < 8 / kSplit; ++j) {
           const int q = part * (8 / kSplit) + j;
@@ -456,18 +477,18 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
       if (!step(kk + 1, sc1)) break;
       sc1 = scale_at(kk + 3);
     }
-  } else if (warp == kMmaWarp && lane == 0) {
+  } else if (warp == T::kMmaWarp && lane == 0) {
     // ---------------- MMA issuer ----------------
-    constexpr uint32_t idesc = F16 ? idesc_f16_f32(kBM, kBN) : idesc_bf16_f32(kBM, kBN);
+    constexpr uint32_t idesc = F16 ? idesc_f16_f32(kBM, BN) : idesc_bf16_f32(kBM, BN);
     for (int kk = 0; kk < nk; ++kk) {
       const int s = kk % kOpStages;
       mbar_wait(smem_u32(c.op_full + s), (kk / kOpStages) & 1, &failed, kGemmWaitNs, a.err);
       if (failed) break;
       tc_fence_after();
-      const uint32_t b0 = smem_u32(c.bop + s * kBOpBytes);
+      const uint32_t b0 = smem_u32(c.bop + s * T::kBOpBytes);
 #pragma unroll
       for (int k16 = 0; k16 < kBK / 16; ++k16) {
-        mma_bf16_ts(tmem, tmem + kAccCols + s * kAStageCols + k16 * 8, desc_sw128(b0 + 32 * k16),
+        mma_bf16_ts(tmem, tmem + T::kAccCols + s * kAStageCols + k16 * 8, desc_sw128(b0 + 32 * k16),
                     idesc, (kk > 0 || k16 > 0) ? 1u : 0u);
       }
       mma_commit(smem_u32(c.op_empty + s));  // stage free once these MMAs have read it
@@ -477,17 +498,17 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
     mbar_wait(smem_u32(c.acc_full), 0, &drain_failed, kGemmWaitNs, a.err);
   }
 
-  if (warp < kEpiWarps) {
+  if (warp < T::kEpiWarps) {
     // ---------------- epilogue ----------------
     bool efailed = failed;
     mbar_wait(smem_u32(c.acc_full), 0, &efailed, kGemmWaitNs, a.err);
     efailed = __any_sync(0xFFFFFFFFu, efailed);
     tc_fence_after();
     const int quarter = warp & 3;
-    const uint32_t col0 = (uint32_t)(warp >> 2) * kEpiCols;
+    const uint32_t col0 = (uint32_t)(warp >> 2) * T::kEpiCols;
     const int64_t row = c.m0 + quarter * 32 + lane;
 #pragma unroll 1
-    for (int cb = 0; cb < kEpiCols / 32; ++cb) {
+    for (int cb = 0; cb < T::kEpiCols / 32; ++cb) {
       float y[32];
       if (!efailed) tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col0 + cb * 32, y);
       if (efailed || row >= a.M) continue;
@@ -509,16 +530,17 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
   }
 }
 
-template <int FMT, bool SWZ>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <int FMT, bool SWZ, int BN>
+__global__ void __launch_bounds__(Tile<BN>::kThreads, Tile<BN>::kMinCtas)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap amap,
                    const __grid_constant__ CUtensorMap bmap, GemmArgs a) {
-  using R = RawLayout<FMT>;
+  using R = RawLayout<FMT, BN>;
+  using T = Tile<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   GemmCta<FMT> c;
   c.bop = smem;
-  c.raw = smem + kOpStages * kBOpBytes;
+  c.raw = smem + kOpStages * T::kBOpBytes;
   c.raw_full = reinterpret_cast<uint64_t*>(c.raw + kRawStages * R::kStageBytes);
   c.raw_empty = c.raw_full + kRawStages;
   c.op_full = c.raw_empty + kRawStages;
@@ -528,17 +550,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* outside = tmem_slot + 1;  // count of converters with a scale byte outside the window
   const int tid = threadIdx.x, warp = tid >> 5;
   c.m0 = (int64_t)blockIdx.y * kBM;
-  c.n0 = (int64_t)blockIdx.x * kBN;
+  c.n0 = (int64_t)blockIdx.x * BN;
   c.nk = (int)(a.K / kBK);
 
   pdl_launch_dependents();
   if (tid == 0) {
     for (int s = 0; s < kRawStages; ++s) {
       mbar_init(smem_u32(c.raw_full + s), 1);
-      mbar_init(smem_u32(c.raw_empty + s), kConvWarps);
+      mbar_init(smem_u32(c.raw_empty + s), T::kConvWarps);
     }
     for (int s = 0; s < kOpStages; ++s) {
-      mbar_init(smem_u32(c.op_full + s), kConvWarps);
+      mbar_init(smem_u32(c.op_full + s), T::kConvWarps);
       mbar_init(smem_u32(c.op_empty + s), 1);
     }
     mbar_init(smem_u32(c.acc_full), 1);
@@ -546,50 +568,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   pdl_wait();  // inputs written by the kernel before; its tensor memory freed
-  if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if (warp == T::kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), T::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();  // barriers initialised, tensor memory allocated
   tc_fence_after();
   c.tmem = *tmem_slot;
-  if (warp == kTmaWarp) {
-    if ((tid & 31) == 0) gemm_loads<FMT>(amap, bmap, a, c);
+  if (warp == T::kTmaWarp) {
+    if ((tid & 31) == 0) gemm_loads<FMT, BN>(amap, bmap, a, c);
   } else {
-    if (warp < kConvWarps) {  // f16 window vote over the CTA's scale bytes
+    if (warp < T::kConvWarps) {  // f16 window vote over the CTA's scale bytes
       const bool is_a = warp < kAWarps;
       const int wq = is_a ? warp : warp - kAWarps;
-      const int r = (wq & (is_a ? 3 : 7)) * 32 + (tid & 31);
-      const int part = is_a ? wq >> 2 : wq >> 3;
-      // thread within its row block (128 * kSplit threads per block)
+      const int row_warps = is_a ? 4 : T::kBRowWarps;
+      const int r = (wq % row_warps) * 32 + (tid & 31);
+      const int part = wq / row_warps;
+      // swizzled: the 128-row blocks holding the CTA's rows (A: one; B: one or two), each
+      // shared by nthr threads
+      const int nblocks = is_a ? 1 : (BN + 127) / 128;
+      const int nthr = (is_a ? kAWarps * 32 : T::kBWarps * 32) / nblocks;
       const int bt = is_a ? tid : tid - kAWarps * 32;
-      const int t = bt % (128 * kSplit);
-      const int64_t row0 = is_a ? c.m0 : c.n0 + (bt / (128 * kSplit)) * 128;
-      const bool in = scales_inside<SWZ>(a, is_a, t, row0, (is_a ? c.m0 : c.n0) + r, part,
-                                         F16Window<FMT>::kLo, F16Window<FMT>::kHi);
+      const int64_t row0 = ((is_a ? c.m0 : c.n0) >> 7 << 7) + (bt / nthr) * 128;
+      const bool in = scales_inside<SWZ>(a, is_a, bt % nthr, nthr, row0,
+                                         (is_a ? c.m0 : c.n0) + r, part, F16Window<FMT>::kLo,
+                                         F16Window<FMT>::kHi);
       if (!__all_sync(0xFFFFFFFFu, in) && (tid & 31) == 0) atomicAdd(outside, 1u);
     }
     // converters and the MMA warp (the load warp is already running)
-    asm volatile("bar.sync 1, %0;" ::"n"((kConvWarps + 1) * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"((T::kConvWarps + 1) * 32) : "memory");
     if (*outside == 0) {
-      gemm_roles<FMT, SWZ, true>(a, c);
+      gemm_roles<FMT, SWZ, true, BN>(a, c);
     } else {
-      gemm_roles<FMT, SWZ, false>(a, c);
+      gemm_roles<FMT, SWZ, false, BN>(a, c);
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(c.tmem, kTmemCols);
+  if (warp == T::kMmaWarp) tmem_dealloc(c.tmem, T::kTmemCols);
 }
 
-template <int FMT, bool SWZ>
-cudaError_t launch_t(const GemmArgs& a, cudaStream_t stream) {
-  using R = RawLayout<FMT>;
-  const void* k = reinterpret_cast<const void*>(&mx_gemm_kernel<FMT, SWZ>);
-  constexpr int smem = gemm_smem<FMT>();
-  if (resident_ctas(k, kGemmThreads, smem, 1) <= 0) return cudaErrorInvalidConfiguration;
+template <int FMT, bool SWZ, int BN>
+cudaError_t launch_tile(const GemmArgs& a, cudaStream_t stream) {
+  using R = RawLayout<FMT, BN>;
+  using T = Tile<BN>;
+  const void* k = reinterpret_cast<const void*>(&mx_gemm_kernel<FMT, SWZ, BN>);
+  constexpr int smem = gemm_smem<FMT, BN>();
+  if (resident_ctas(k, T::kThreads, smem, T::kMinCtas) <= 0) return cudaErrorInvalidConfiguration;
   const int64_t code_row = FMT == kFmtE2M1 ? a.K / 2 : a.K;
   const CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B;
   CUtensorMap amap, bmap;
@@ -597,11 +624,28 @@ cudaError_t launch_t(const GemmArgs& a, cudaStream_t stream) {
                                        CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, R::kPitch, kBM, swz);
   if (err != cudaSuccess) return err;
   err = make_tensor_map_2d(&bmap, a.b_codes, a.N, code_row, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                           R::kPitch, kBN, swz);
+                           R::kPitch, BN, swz);
   if (err != cudaSuccess) return err;
-  const dim3 grid((unsigned)((a.N + kBN - 1) / kBN), (unsigned)((a.M + kBM - 1) / kBM));
-  return launch_pdl(&mx_gemm_kernel<FMT, SWZ>, grid, dim3(kGemmThreads), smem, stream, amap,
+  const dim3 grid((unsigned)((a.N + BN - 1) / BN), (unsigned)((a.M + kBM - 1) / kBM));
+  return launch_pdl(&mx_gemm_kernel<FMT, SWZ, BN>, grid, dim3(T::kThreads), smem, stream, amap,
                     bmap, a);
+}
+
+// 128 x 256 tiles, or 128 x 64 tiles (two CTAs per SM) when the 128 x 256 tiles would leave
+// SMs idle and the narrow tiles fit in one wave. Measured (E2M1, M x 8192 x 8192): M = 16
+// 73 -> 59 us, M = 128 77 -> 58 us with narrow tiles; M = 512 (512 narrow tiles, 1.7 waves)
+// 78 -> 153 us, so narrow tiles beyond one wave are not taken.
+template <int FMT, bool SWZ>
+cudaError_t launch_t(const GemmArgs& a, cudaStream_t stream) {
+  const void* k = reinterpret_cast<const void*>(&mx_gemm_kernel<FMT, SWZ, 256>);
+  const int sms = resident_ctas(k, Tile<256>::kThreads, gemm_smem<FMT, 256>(), 1);
+  const int64_t row_tiles = (a.M + kBM - 1) / kBM;
+  const int64_t wide_tiles = row_tiles * ((a.N + 255) / 256);
+  const int64_t narrow_tiles = row_tiles * ((a.N + 63) / 64);
+  if (sms > 0 && wide_tiles < sms && narrow_tiles <= 2 * (int64_t)sms) {
+    return launch_tile<FMT, SWZ, 64>(a, stream);
+  }
+  return launch_tile<FMT, SWZ, 256>(a, stream);
 }
 
 }  // namespace

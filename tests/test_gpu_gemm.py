@@ -28,7 +28,9 @@ LAYOUTS = [O.LINEAR, O.SWIZZLED]
 GUARD = 4096
 CANARY = 0x5A
 BF16_MIN_SUB = 2.0 ** -133
-# (M, N, K): one tile, ragged rows and columns (N % 8 == 0), several K steps and tiles
+# (M, N, K): one tile, ragged rows and columns (N % 8 == 0), several K steps and tiles (these
+# take the kernel's 128 x 64 tiles; test_gemm_wide_tiles_ragged and the full-size tests its
+# 128 x 256 tiles)
 SHAPES = [(1, 8, 64), (3, 16, 128), (128, 128, 64), (129, 136, 192), (300, 264, 1024),
           (257, 520, 4096)]
 
@@ -94,6 +96,30 @@ def test_gemm_random_codes(fmt, layout, shape):
     C_ref = O.gemm(a, sa, b, sb, K, fmt, layout, alpha)
     S = exact_S(a, sa, b, sb, K, fmt, layout)
     assert_gemm_close(C_gpu, C_ref, gemm_tolerance(C_ref, K, alpha, S), "C")
+    f = full.cpu().numpy()
+    assert (f[:GUARD] == CANARY).all() and (f[GUARD + M * N * 2:] == CANARY).all()
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemm_wide_tiles_ragged(fmt, layout):
+    """A problem with enough 128 x 256 tiles to fill the SMs (so the kernel takes its wide
+    tiles; most small shapes above take 128 x 64 tiles), ragged in M and N, inside canaries;
+    random scale bytes partly outside the f16 window in one row block (bf16 operands there)."""
+    M, N, K = 641, 7944, 256
+    rng = np.random.default_rng(5 + fmt + 2 * layout)
+    a, sa = random_operand(rng, M, K, fmt, layout)
+    b, sb = random_operand(rng, N, K, fmt, layout)
+    la = T.unswizzle(sa, M, K) if layout == O.SWIZZLED else sa
+    la[300:310] = 150
+    if layout == O.SWIZZLED:
+        sa = swizzle(la, M, K)
+    full = torch.full((M * N * 2 + 2 * GUARD,), CANARY, dtype=torch.uint8, device="cuda")
+    c = full[GUARD:GUARD + M * N * 2].view(torch.bfloat16).view(M, N)
+    mxq.mx_gemm(dev(a), dev(sa), dev(b), dev(sb), K, fmt, layout, 0.75, c=c)
+    C_ref = O.gemm(a, sa, b, sb, K, fmt, layout, 0.75)
+    S = exact_S(a, sa, b, sb, K, fmt, layout)
+    assert_gemm_close(bf16_to_f64(c), C_ref, gemm_tolerance(C_ref, K, 0.75, S), "C")
     f = full.cpu().numpy()
     assert (f[:GUARD] == CANARY).all() and (f[GUARD + M * N * 2:] == CANARY).all()
 
