@@ -940,8 +940,9 @@ def test_dependent_calls_keep_stream_order():
     """Every kernel is launched with programmatic stream serialization (it may be scheduled
     while the kernel before it finishes) and waits for that kernel before touching global
     memory. A chain of calls in which each reads what the one before wrote (and some overwrite
-    what an earlier one read) gives the same bytes back to back, eagerly and in a CUDA graph, as
-    with a synchronization after every call."""
+    what an earlier one read; GEMMs read codes written just before them and a QDQ reads a GEMM's
+    output) gives the same bytes back to back, eagerly and in a CUDA graph, as with a
+    synchronization after every call."""
     M, K = 4096, 8192
     x = T.to_gpu(W.rotation_sweep_input("attn_in", M, K))
     H = T.to_gpu(rotation(32))
@@ -963,16 +964,28 @@ def test_dependent_calls_keep_stream_order():
     cg, sg = mxq.mx_quantize_grouped(x, off_src, mxq.E4M3, mxq.SWIZZLED)
     cgl, sgl = mxq.mx_quantize_grouped(x, off_src, mxq.E4M3, mxq.LINEAR)
     cng, sng = mxq.mx_quantize_nvfp4_grouped(x, off_src, gse, mxq.SWIZZLED)
-    outs = (a, b, d, c4, s4, c8, s8, cn, sn, small, cs, ss, offs, cg, sg, cgl, sgl, cng, sng)
+    # GEMM consumers of codes written earlier in the chain; a QDQ then reads a GEMM's output
+    cw, sw = mxq.mx_quantize(x[:512], mxq.E2M1, mxq.SWIZZLED)
+    cw8, sw8 = mxq.mx_quantize(x[:256], mxq.E4M3, mxq.LINEAR)
+    g1 = torch.empty((M, 512), dtype=torch.bfloat16, device="cuda")
+    g2 = torch.empty_like(g1)
+    g3 = torch.empty((M, 256), dtype=torch.bfloat16, device="cuda")
+    outs = (a, b, d, c4, s4, c8, s8, cn, sn, small, cs, ss, offs, cg, sg, cgl, sgl, cng, sng,
+            cw, sw, cw8, sw8, g1, g2, g3)
 
     def chain(sync):
         steps = [
             lambda: mxq.mx_qdq(x, mxq.E4M3, H128, y=a),
             lambda: mxq.mx_qdq(a, mxq.E2M1, y=b),
             lambda: mxq.mx_rotate_quantize(b, H, mxq.E2M1, mxq.SWIZZLED, codes=c4, scales=s4),
+            lambda: mxq.mx_quantize(a[:512], mxq.E2M1, mxq.SWIZZLED, codes=cw, scales=sw),
+            lambda: mxq.mx_gemm(c4, s4, cw, sw, K, mxq.E2M1, mxq.SWIZZLED, c=g1),
+            lambda: mxq.mx_qdq(g1, mxq.E4M3, y=g2),
             lambda: mxq.mx_dequantize(c4, s4, K, mxq.E2M1, mxq.SWIZZLED, y=d),
             lambda: mxq.mx_qdq(d, mxq.E4M3, H, y=a),
             lambda: mxq.mx_quantize(a, mxq.E4M3, mxq.LINEAR, codes=c8, scales=s8),
+            lambda: mxq.mx_quantize(d[:256], mxq.E4M3, mxq.LINEAR, codes=cw8, scales=sw8),
+            lambda: mxq.mx_gemm(c8, s8, cw8, sw8, K, mxq.E4M3, mxq.LINEAR, c=g3),
             lambda: mxq.mx_dequantize(c8, s8, K, mxq.E4M3, mxq.LINEAR, y=b),
             lambda: mxq.mx_quantize_nvfp4(b, gs, mxq.SWIZZLED, codes=cn, scales=sn),
             lambda: mxq.mx_dequantize_nvfp4(cn, sn, K, gs, mxq.SWIZZLED, y=d),
