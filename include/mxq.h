@@ -294,6 +294,20 @@ mx_status mx_selftest_bounded_wait(int64_t limit_ns, void* stream);
 mx_status mx_selftest_rotate_give_up(const void* x, int64_t M, int64_t K, const void* H, int g,
                                      void* codes, void* scales, int64_t limit_ns, void* stream);
 
+/*
+ * Give-up self-test of the GEMM kernel (no counterpart on the pages): the call
+ * mx_gemm(a_codes, a_scales, b_codes, b_scales, M, N, K, fmt, 32, layout, 1.0f, c, stream)
+ * makes, with every pipeline wait of the kernel limited to limit_ns nanoseconds
+ * (1 .. 100,000,000) instead of 2 s. A role whose wait ran out stops issuing work; the loads in
+ * flight and the MMAs issued are still waited for (2 s) before the kernel frees its tensor
+ * memory and exits: the call ends, the device error word reports the give-up
+ * (mx_device_errors) and the context stays usable. c then holds unspecified bytes. Shapes and
+ * errors as mx_gemm, except that M == 0 or N == 0 is MX_ERR_SHAPE.
+ */
+mx_status mx_selftest_gemm_give_up(const void* a_codes, const void* a_scales, const void* b_codes,
+                                   const void* b_scales, int64_t M, int64_t N, int64_t K, int fmt,
+                                   int layout, void* c, int64_t limit_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

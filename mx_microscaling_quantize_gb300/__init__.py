@@ -34,6 +34,7 @@ EXPORTS = (
     "mx_quantize_nvfp4", "mx_qdq_nvfp4", "mx_dequantize_nvfp4", "mx_nvfp4_grouped_scales_shape",
     "mx_quantize_nvfp4_grouped", "mx_rotate_debug", "mx_device_errors",
     "mx_selftest_bounded_wait", "mx_selftest_rotate_give_up", "mx_gemm",
+    "mx_selftest_gemm_give_up",
 )
 
 
@@ -75,6 +76,7 @@ def lib() -> ctypes.CDLL:
         "mx_selftest_bounded_wait": (i32, [i64, p]),
         "mx_selftest_rotate_give_up": (i32, [p, i64, i64, p, i32, p, p, i64, p]),
         "mx_gemm": (i32, [p, p, p, p, i64, i64, i64, i32, i32, i32, ctypes.c_float, p, p]),
+        "mx_selftest_gemm_give_up": (i32, [p, p, p, p, i64, i64, i64, i32, i32, p, i64, p]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -375,10 +377,7 @@ def mx_selftest_rotate_give_up(x, H, limit_ns: int, *, stream=None):
     return codes, scales
 
 
-def mx_gemm(a_codes, a_scales, b_codes, b_scales, K: int, fmt, layout=SWIZZLED, alpha: float = 1.0,
-            *, c=None, group=GROUP, stream=None):
-    """C[M, N] = alpha * dequant(A) @ dequant(B)^T (bf16) from MX codes and E8M0 scales as
-    mx_quantize returns them (A: [M, K/2 or K] codes, B: [N, ...])."""
+def _gemm_operands(a_codes, a_scales, b_codes, b_scales, K, fmt, c):
     for t in (a_codes, a_scales, b_codes, b_scales):
         if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.uint8
                 and t.is_contiguous()):
@@ -389,6 +388,26 @@ def mx_gemm(a_codes, a_scales, b_codes, b_scales, K: int, fmt, layout=SWIZZLED, 
         raise ValueError("codes do not match K and the format")
     if c is None:
         c = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
+    return M, N, c
+
+
+def mx_selftest_gemm_give_up(a_codes, a_scales, b_codes, b_scales, K: int, fmt, layout, limit_ns: int,
+                             *, stream=None):
+    """mx_gemm with every pipeline wait of the kernel limited to limit_ns: the kernel stops
+    issuing work, drains what is in flight and returns; the device error word reports it.
+    Returns the (unspecified) C buffer."""
+    M, N, c = _gemm_operands(a_codes, a_scales, b_codes, b_scales, K, fmt, None)
+    _check(lib().mx_selftest_gemm_give_up(_ptr(a_codes), _ptr(a_scales), _ptr(b_codes),
+                                          _ptr(b_scales), M, N, K, fmt, layout, _ptr(c), limit_ns,
+                                          _stream_ptr(stream, a_codes)))
+    return c
+
+
+def mx_gemm(a_codes, a_scales, b_codes, b_scales, K: int, fmt, layout=SWIZZLED, alpha: float = 1.0,
+            *, c=None, group=GROUP, stream=None):
+    """C[M, N] = alpha * dequant(A) @ dequant(B)^T (bf16) from MX codes and E8M0 scales as
+    mx_quantize returns them (A: [M, K/2 or K] codes, B: [N, ...])."""
+    M, N, c = _gemm_operands(a_codes, a_scales, b_codes, b_scales, K, fmt, c)
     _check(lib().mx_gemm(_ptr(a_codes), _ptr(a_scales), _ptr(b_codes), _ptr(b_scales), M, N, K,
                          fmt, group, layout, alpha, _ptr(c), _stream_ptr(stream, a_codes)))
     return c

@@ -426,9 +426,11 @@ mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, in
                                       static_cast<cudaStream_t>(stream)));
 }
 
-mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes,
-                  const void* b_scales, int64_t M, int64_t N, int64_t K, int fmt, int group,
-                  int layout, float alpha, void* c, void* stream) {
+namespace {
+mx_status gemm_call(const void* a_codes, const void* a_scales, const void* b_codes,
+                    const void* b_scales, int64_t M, int64_t N, int64_t K, int fmt, int group,
+                    int layout, float alpha, void* c, unsigned long long wait_limit_ns,
+                    void* stream) {
   if (M < 0 || N < 0 || K < 0) return MX_ERR_SHAPE;
   if (group != 32 || !valid_fmt(fmt) || !valid_layout(layout)) return MX_ERR_UNSUPPORTED;
   if (K == 0 || K % 64 != 0 || N % 8 != 0) return MX_ERR_SHAPE;
@@ -453,10 +455,28 @@ mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes
   a.K = K;
   a.a_scale_cols = a.b_scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : ceil_div(K, mxq::kTileCols) * 4;
   a.alpha = alpha;
+  a.wait_limit_ns = wait_limit_ns;
   cudaError_t err = mxq::device_error_word(&a.err);
   if (err != cudaSuccess) return from_cuda(err);
   return from_cuda(mxq::launch_gemm(fmt, layout == MX_SCALES_SWIZZLED, a,
                                     static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes,
+                  const void* b_scales, int64_t M, int64_t N, int64_t K, int fmt, int group,
+                  int layout, float alpha, void* c, void* stream) {
+  return gemm_call(a_codes, a_scales, b_codes, b_scales, M, N, K, fmt, group, layout, alpha, c,
+                   2000000000ull, stream);
+}
+
+mx_status mx_selftest_gemm_give_up(const void* a_codes, const void* a_scales, const void* b_codes,
+                                   const void* b_scales, int64_t M, int64_t N, int64_t K, int fmt,
+                                   int layout, void* c, int64_t limit_ns, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 100000000) return MX_ERR_SHAPE;
+  if (M == 0 || N == 0) return MX_ERR_SHAPE;  // a launch is the point
+  return gemm_call(a_codes, a_scales, b_codes, b_scales, M, N, K, fmt, 32, layout, 1.0f, c,
+                   (unsigned long long)limit_ns, stream);
 }
 
 mx_status mx_selftest_bounded_wait(int64_t limit_ns, void* stream) {

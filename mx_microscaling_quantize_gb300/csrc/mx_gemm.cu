@@ -38,9 +38,10 @@
 // window both give the same operand values, so the choice changes no product. The converters
 // check the window over the CTA's scale bytes before the first step (one CTA-wide vote).
 // Scale bytes are read by each converter from global memory two steps ahead.
-// Every mbarrier wait is bounded: a wait that runs out sets the device error word and its role
-// stops issuing work; the loads in flight and the MMAs issued are waited for before the CTA
-// frees its tensor memory and exits.
+// Every mbarrier wait is bounded (pipeline waits by GemmArgs::wait_limit_ns, 2 s unless a
+// self-test sets it shorter): a wait that runs out sets the device error word and its role
+// stops issuing work; the loads in flight and the MMAs issued are waited for (always with the
+// 2 s limit) before the CTA frees its tensor memory and exits.
 #include "mx_device.cuh"
 #include "mx_launch.h"
 #include "mx_tcgen05.cuh"
@@ -341,8 +342,8 @@ __device__ __forceinline__ void gemm_loads(const CUtensorMap& amap, const CUtens
   for (int rs = 0; rs < nstages; ++rs) {
     const int s = rs % kRawStages;
     if (rs >= kRawStages) {
-      mbar_wait(smem_u32(c.raw_empty + s), ((rs / kRawStages) & 1) ^ 1, &failed, kGemmWaitNs,
-                a.err);
+      mbar_wait(smem_u32(c.raw_empty + s), ((rs / kRawStages) & 1) ^ 1, &failed,
+                a.wait_limit_ns, a.err);
     }
     if (failed) break;
     const uint32_t dst = smem_u32(c.raw + s * R::kStageBytes);
@@ -404,7 +405,8 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
       const int rs = kk / R::kSteps, sub = kk % R::kSteps;  // raw stage, step within it
       const int sr = rs % kRawStages, so = kk % kOpStages;
       if (sub == 0) {
-        mbar_wait(smem_u32(c.raw_full + sr), (rs / kRawStages) & 1, &failed, kGemmWaitNs, a.err);
+        mbar_wait(smem_u32(c.raw_full + sr), (rs / kRawStages) & 1, &failed, a.wait_limit_ns,
+                  a.err);
         failed = __any_sync(0xFFFFFFFFu, failed);
         if (failed) return false;
       }
@@ -436,8 +438,8 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
         if (lane == 0) mbar_arrive(smem_u32(c.raw_empty + sr));
       }
       if (kk >= kOpStages) {
-        mbar_wait(smem_u32(c.op_empty + so), ((kk / kOpStages) & 1) ^ 1, &failed, kGemmWaitNs,
-                  a.err);
+        mbar_wait(smem_u32(c.op_empty + so), ((kk / kOpStages) & 1) ^ 1, &failed,
+                  a.wait_limit_ns, a.err);
         failed = __any_sync(0xFFFFFFFFu, failed);
         if (failed) return false;
       }
@@ -482,7 +484,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
     constexpr uint32_t idesc = F16 ? idesc_f16_f32(kBM, BN) : idesc_bf16_f32(kBM, BN);
     for (int kk = 0; kk < nk; ++kk) {
       const int s = kk % kOpStages;
-      mbar_wait(smem_u32(c.op_full + s), (kk / kOpStages) & 1, &failed, kGemmWaitNs, a.err);
+      mbar_wait(smem_u32(c.op_full + s), (kk / kOpStages) & 1, &failed, a.wait_limit_ns, a.err);
       if (failed) break;
       tc_fence_after();
       const uint32_t b0 = smem_u32(c.bop + s * T::kBOpBytes);
@@ -501,7 +503,7 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
   if (warp < T::kEpiWarps) {
     // ---------------- epilogue ----------------
     bool efailed = failed;
-    mbar_wait(smem_u32(c.acc_full), 0, &efailed, kGemmWaitNs, a.err);
+    mbar_wait(smem_u32(c.acc_full), 0, &efailed, a.wait_limit_ns, a.err);
     efailed = __any_sync(0xFFFFFFFFu, efailed);
     tc_fence_after();
     const int quarter = warp & 3;

@@ -104,6 +104,7 @@ struct GemmArgs {
   int64_t b_scale_cols;
   float alpha;
   unsigned int* err;        // device error word (device_error_word)
+  unsigned long long wait_limit_ns;  // pipeline waits (drains always allow 2 s)
 };
 
 // Tensor map of a row-major [rows, cols] matrix of 1- or 2-byte elements, boxes of box_rows x

@@ -273,6 +273,18 @@ def test_gemm_validation(L):
     assert f(None, None, None, None, 128, 0, 64, 2, 32, 0, 1.0, None, None) == OK
 
 
+def test_selftest_gemm_give_up_validation(L):
+    f = L.mx_selftest_gemm_give_up  # (a, sa, b, sb, M, N, K, fmt, layout, c, limit_ns, stream)
+    assert f(P, P, P, P, 128, 128, 64, 1, 1, P, 0, None) == SHAPE             # limit out of range
+    assert f(P, P, P, P, 128, 128, 64, 1, 1, P, 100_000_001, None) == SHAPE
+    assert f(P, P, P, P, 0, 128, 64, 1, 1, P, 1000, None) == SHAPE            # empty
+    assert f(P, P, P, P, 128, 0, 64, 1, 1, P, 1000, None) == SHAPE
+    assert f(P, P, P, P, 128, 128, 96, 1, 1, P, 1000, None) == SHAPE          # K % 64
+    assert f(P, P, P, P, 128, 128, 64, 3, 1, P, 1000, None) == UNSUP
+    assert f(None, P, P, P, 128, 128, 64, 1, 1, P, 1000, None) == NULL
+    assert f(P, P, P, P, 128, 128, 64, 1, 1, P + 8, 1000, None) == ALIGN
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mxq, "_lib", None)
     monkeypatch.setattr(mxq, "LIB_PATH", str(tmp_path / "missing.so"))

@@ -260,6 +260,34 @@ def test_gemm_nan_scale_poisons_its_rows_and_columns(fmt):
     assert_gemm_close(np.where(nan, 0, C_gpu), np.where(nan, 0, C_ref), np.where(nan, 1, tol), "C")
 
 
+@pytest.mark.parametrize("limit_ns", [1, 20_000, 1_000_000])
+def test_gemm_give_up_drains_and_reports(limit_ns):
+    """Failure detection without a fault: the GEMM with every pipeline wait limited to a few
+    ns .. 1 ms. Each call ends; the 1 ns call reports the give-up in the device error word;
+    the same context then computes a GEMM equal (within tolerance) to the oracle's."""
+    M, N, K = 2048, 4096, 4096
+    rng = np.random.default_rng(limit_ns)
+    a, sa = random_operand(rng, M, K, O.E2M1, O.SWIZZLED)
+    b, sb = random_operand(rng, N, K, O.E2M1, O.SWIZZLED)
+    ga, gsa, gb, gsb = dev(a), dev(sa), dev(b), dev(sb)
+    assert mxq.mx_device_errors() == 0
+    mxq.mx_selftest_gemm_give_up(ga, gsa, gb, gsb, K, O.E2M1, O.SWIZZLED, limit_ns)
+    torch.cuda.synchronize()
+    flags = mxq.mx_device_errors()
+    if limit_ns == 1:
+        assert flags == 1
+    assert flags in (0, 1)
+    # the context still computes: a small GEMM against the oracle
+    m, n, k = 130, 264, 512
+    a2, sa2 = random_operand(rng, m, k, O.E4M3, O.LINEAR)
+    b2, sb2 = random_operand(rng, n, k, O.E4M3, O.LINEAR)
+    C_gpu = bf16_to_f64(mxq.mx_gemm(dev(a2), dev(sa2), dev(b2), dev(sb2), k, O.E4M3, O.LINEAR))
+    C_ref = O.gemm(a2, sa2, b2, sb2, k, O.E4M3, O.LINEAR)
+    S = exact_S(a2, sa2, b2, sb2, k, O.E4M3, O.LINEAR)
+    assert_gemm_close(C_gpu, C_ref, gemm_tolerance(C_ref, k, 1.0, S), "after give-up")
+    assert mxq.mx_device_errors() == 0
+
+
 def test_gemm_empty_calls():
     u = torch.zeros(1024, dtype=torch.uint8, device="cuda")
     c = mxq.mx_gemm(u[:0], u, u[:256].view(8, 32), u, 64, O.E2M1, O.LINEAR)
