@@ -232,19 +232,18 @@ __device__ __forceinline__ void convert_block_f16(const uint32_t* raw, uint32_t 
   }
 }
 
-// Running byte-wise min / max of 4-byte words (bytes of rows or blocks that do not exist are
-// passed as `fill`).
-struct ByteRange {
-  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+// Whether any byte of w lies outside [lo, hi] (lo <= 128, hi >= 127): a byte b < lo borrows
+// into its top bit in w - lo * 0x01010101 while its own top bit is clear ("has a byte less
+// than n", exact for n <= 128 as an existence test), and b > hi is 255 - b < 255 - hi, the
+// same test on ~w. Bytes of rows or blocks that do not exist are passed as lo.
+struct ByteWindow {
+  uint32_t lo_n, hi_n, bad = 0u;
+  __device__ __forceinline__ ByteWindow(uint32_t lo, uint32_t hi)
+      : lo_n(lo * 0x01010101u), hi_n((255u - hi) * 0x01010101u) {}
   __device__ __forceinline__ void add(uint32_t w) {
-    lo = __vminu4(lo, w);
-    hi = __vmaxu4(hi, w);
+    bad |= ((w - lo_n) & ~w) | ((~w - hi_n) & w);
   }
-  __device__ __forceinline__ bool inside(uint32_t wlo, uint32_t whi) const {
-    const uint32_t l = min(min(lo & 0xFFu, (lo >> 8) & 0xFFu), min((lo >> 16) & 0xFFu, lo >> 24));
-    const uint32_t h = max(max(hi & 0xFFu, (hi >> 8) & 0xFFu), max((hi >> 16) & 0xFFu, hi >> 24));
-    return l >= wlo && h <= whi;
-  }
+  __device__ __forceinline__ bool inside() const { return (bad & 0x80808080u) == 0u; }
 };
 
 __device__ __forceinline__ uint32_t load_scale_pair(const uint8_t* p) {
@@ -285,7 +284,7 @@ template <bool SWZ>
 __device__ __forceinline__ bool scales_inside(const GemmArgs& a, bool is_a, int t, int nthreads,
                                               int64_t row0, int64_t grow, int part, uint32_t lo,
                                               uint32_t hi) {
-  ByteRange br;
+  ByteWindow br(lo, hi);
   const uint8_t* sc = is_a ? a.a_scales : a.b_scales;
   const int64_t scols = is_a ? a.a_scale_cols : a.b_scale_cols;
   const int64_t rows = is_a ? a.M : a.N;
@@ -326,7 +325,7 @@ __device__ __forceinline__ bool scales_inside(const GemmArgs& a, bool is_a, int 
       for (int64_t i = 0; i < scols; i += 2) br.add(load_scale_pair(p + i) * 0x00010001u);
     }
   }
-  return br.inside(lo, hi);  // nothing looked at: lo 0xFF.., hi 0 -> inside
+  return br.inside();
 }
 
 // Raw code loads (one thread of warp kTmaWarp): runs from the start, independent of the operand
