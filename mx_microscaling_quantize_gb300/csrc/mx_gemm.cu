@@ -27,8 +27,9 @@
 //                (M = 128, N = 256, K = 16, A from tensor memory, B from shared memory,
 //                f16 or bf16 products summed in fp32) and commits them to the step's "empty"
 //                barrier;
-//   warps 0..7   epilogue: tcgen05.ld of the accumulator, times alpha, rounded to bf16, 16-byte
-//                stores (warp w: rows 32 (w % 4) .. +31, columns 128 (w / 4) .. +127).
+//   warps 0..7   epilogue: tcgen05.ld of the accumulator (warp w: rows 32 (w % 4) .. +31,
+//                columns 128 (w / 4) .. +127), times alpha, rounded to bf16, staged in shared
+//                memory and written with tensor-map stores.
 // Operand type. When every scale byte of the CTA's rows lies in the window where every value
 // decode(code) * 2^X (X = byte - 127) is exact in f16 (E2M1: X in [-23, 13]; E4M3: [-15, 7]),
 // the operands are f16: two codes take one hardware conversion to f16x2 (exact) and one f16x2
@@ -81,6 +82,7 @@ struct Tile {
   static constexpr int kMinCtas = BN <= 64 ? 2 : 1;
   static_assert(kEpiWarps <= kConvWarps, "the epilogue runs on converter warps");
   static_assert(kEpiCols % 32 == 0, "32-column accumulator loads");
+  static_assert((BN / 64) * kBM * 128 <= kOpStages * kBOpBytes, "C staging fits the B stages");
 };
 constexpr unsigned long long kGemmWaitNs = 2000000000ull;  // 2 s
 
@@ -360,7 +362,8 @@ __device__ __forceinline__ void gemm_loads(const CUtensorMap& amap, const CUtens
 }
 
 template <int FMT, bool SWZ, bool F16, int BN>
-__device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>& c) {
+__device__ __forceinline__ void gemm_roles(const CUtensorMap& cmap, const GemmArgs& a,
+                                           const GemmCta<FMT>& c) {
   using R = RawLayout<FMT, BN>;
   using T = Tile<BN>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -501,22 +504,25 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
 
   if (warp < T::kEpiWarps) {
     // ---------------- epilogue ----------------
+    // The bf16 tile is staged in the (now idle) B operand stages as 64-column boxes of
+    // 128 rows x 128 bytes, 128-byte swizzled (16-byte chunk q of row r at q ^ (r % 8)), and
+    // written with tensor-map stores, which drop what lies past M and N.
     bool efailed = failed;
     mbar_wait(smem_u32(c.acc_full), 0, &efailed, a.wait_limit_ns, a.err);
     efailed = __any_sync(0xFFFFFFFFu, efailed);
     tc_fence_after();
     const int quarter = warp & 3;
     const uint32_t col0 = (uint32_t)(warp >> 2) * T::kEpiCols;
-    const int64_t row = c.m0 + quarter * 32 + lane;
+    const int r = quarter * 32 + lane;  // row of the tile
 #pragma unroll 1
     for (int cb = 0; cb < T::kEpiCols / 32; ++cb) {
+      if (efailed) break;
       float y[32];
-      if (!efailed) tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col0 + cb * 32, y);
-      if (efailed || row >= a.M) continue;
+      tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col0 + cb * 32, y);
+      const uint32_t col = col0 + cb * 32;  // first of 32 columns: half of a 64-column box
+      uint8_t* box = c.bop + (col / 64) * (kBM * 128) + r * 128;
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const int64_t col = c.n0 + col0 + cb * 32 + g * 8;
-        if (col >= a.N) break;
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -524,9 +530,20 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
               : "=r"(o[i])
               : "f"(a.alpha * y[g * 8 + 2 * i + 1]), "f"(a.alpha * y[g * 8 + 2 * i]));
         }
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.c) + row * a.N + col) =
-            make_uint4(o[0], o[1], o[2], o[3]);
+        const int q = (int)((col % 64) / 8) + g;
+        *reinterpret_cast<uint4*>(box + ((q ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
+    }
+    fence_proxy_async_smem();  // the staged tile is visible to the tensor-map stores
+    asm volatile("bar.sync 2, %0;" ::"n"(T::kEpiWarps * 32) : "memory");
+    if (warp == 0 && lane == 0 && !efailed) {
+#pragma unroll 1
+      for (int bx = 0; bx < BN / 64 && c.n0 + bx * 64 < a.N; ++bx) {  // boxes inside N only
+        tma_store_box(&cmap, (int)c.n0 + bx * 64, (int)c.m0,
+                      smem_u32(c.bop + bx * (kBM * 128)));
+      }
+      bulk_commit_group();
+      bulk_wait_read_all();  // the staging is read before the CTA's shared memory goes away
     }
   }
 }
@@ -534,7 +551,8 @@ __device__ __forceinline__ void gemm_roles(const GemmArgs& a, const GemmCta<FMT>
 template <int FMT, bool SWZ, int BN>
 __global__ void __launch_bounds__(Tile<BN>::kThreads, Tile<BN>::kMinCtas)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap amap,
-                   const __grid_constant__ CUtensorMap bmap, GemmArgs a) {
+                   const __grid_constant__ CUtensorMap bmap,
+                   const __grid_constant__ CUtensorMap cmap, GemmArgs a) {
   using R = RawLayout<FMT, BN>;
   using T = Tile<BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -600,9 +618,9 @@ __global__ void __launch_bounds__(Tile<BN>::kThreads, Tile<BN>::kMinCtas)
     // converters and the MMA warp (the load warp is already running)
     asm volatile("bar.sync 1, %0;" ::"n"((T::kConvWarps + 1) * 32) : "memory");
     if (*outside == 0) {
-      gemm_roles<FMT, SWZ, true, BN>(a, c);
+      gemm_roles<FMT, SWZ, true, BN>(cmap, a, c);
     } else {
-      gemm_roles<FMT, SWZ, false, BN>(a, c);
+      gemm_roles<FMT, SWZ, false, BN>(cmap, a, c);
     }
   }
   tc_fence_before();
@@ -627,9 +645,13 @@ cudaError_t launch_tile(const GemmArgs& a, cudaStream_t stream) {
   err = make_tensor_map_2d(&bmap, a.b_codes, a.N, code_row, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
                            R::kPitch, BN, swz);
   if (err != cudaSuccess) return err;
+  CUtensorMap cmap;  // C: bf16 [M, N], boxes of 128 rows x 64 columns
+  err = make_tensor_map_2d(&cmap, a.c, a.M, a.N, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, kBM,
+                           swz);
+  if (err != cudaSuccess) return err;
   const dim3 grid((unsigned)((a.N + BN - 1) / BN), (unsigned)((a.M + kBM - 1) / kBM));
   return launch_pdl(&mx_gemm_kernel<FMT, SWZ, BN>, grid, dim3(T::kThreads), smem, stream, amap,
-                    bmap, a);
+                    bmap, cmap, a);
 }
 
 // 128 x 256 tiles, or 128 x 64 tiles (two CTAs per SM) when the 128 x 256 tiles would leave

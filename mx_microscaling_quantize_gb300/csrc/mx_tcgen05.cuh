@@ -123,6 +123,19 @@ __device__ __forceinline__ void tma_load_box(uint32_t dst, const void* map, int 
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// 2-D tensor-map store of one box from shared memory (bulk-group completion: bulk_commit, then
+// bulk_wait_read before the shared memory is reused or the CTA exits).
+__device__ __forceinline__ void tma_store_box(const void* map, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 // 32 consecutive 32-bit columns of this thread's TMEM lane from registers, issued only: the
 // thread's tcgen05.wait::st (tmem_wait_st) completes it.
 __device__ __forceinline__ void tmem_st32_async(uint32_t taddr, const uint32_t* r) {
