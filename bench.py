@@ -578,7 +578,8 @@ CASES = {
     "gemm": "block-scaled GEMM consumer C = dequant(A) dequant(B)^T (bf16 out) on the quantized "
             "activation and weight workloads, MXFP4 and MXFP8, swizzled scales, at the o_proj, "
             "down_proj, square and decode shapes; beside it torch.matmul (cuBLAS bf16) of the "
-            "dequantized operands, alone and after the two mx_dequantize calls",
+            "dequantized operands, alone and after the two mx_dequantize calls, and for MXFP8 "
+            "cuBLAS's block-scaled GEMM (torch._scaled_mm) on the same codes and scales",
     "nonrotated_sweep": "every non-rotated kernel at full workload size (quantize, QDQ, "
                         "dequantize, NVFP4, grouped MoE, the x[128,4096] MXFP8 quantize), each "
                         "launched --steps times back to back over buffer copies that exceed 3x "
@@ -950,12 +951,25 @@ def run_gemm_case(args, dev):
                 torch.matmul(da, dw.t(), out=c)
             t_two = clock(two_step)
             launches += 4 + 3 * (max(3, args.warmup) + steps)
+            t_bs = None
+            if fmt == mxq.E4M3:  # cuBLAS's own MXFP8 block-scaled GEMM on the same bytes
+                a8, w8 = ca.view(torch.float8_e4m3fn), cw.view(torch.float8_e4m3fn)
+                sa8 = sa.view(torch.float8_e8m0fnu).reshape(-1)
+                sw8 = sw.view(torch.float8_e8m0fnu).reshape(-1)
+                try:
+                    t_bs = clock(lambda: torch._scaled_mm(a8, w8.t(), scale_a=sa8, scale_b=sw8,
+                                                          out_dtype=torch.bfloat16))
+                except Exception:  # not offered by this torch build on this GPU
+                    t_bs = None
             flops = 2.0 * M * N * K
             res[f"{name}_{fname}"] = {
                 "M": M, "N": N, "K": K, "us": t * 1e6, "TFLOP/s": flops / t / 1e12,
                 "frac_of_bf16_peak": flops / t / 1e12 / peak,
                 "cublas_bf16_us": t_mm * 1e6, "cublas_bf16_TFLOP/s": flops / t_mm / 1e12,
                 "dequant_then_cublas_us": t_two * 1e6}
+            if t_bs is not None:
+                res[f"{name}_{fname}"]["cublas_mxfp8_block_scaled_us"] = t_bs * 1e6
+                res[f"{name}_{fname}"]["cublas_mxfp8_block_scaled_TFLOP/s"] = flops / t_bs / 1e12
             if name == shapes[0][0]:  # the oracle beside it, on a bounded sample of C's rows
                 res[f"{name}_{fname}"]["cpu_baseline"] = time_oracle_gemm(
                     ca, sa, cw, sw, K, fmt, mxq.SWIZZLED, rows=min(M, 128))
