@@ -56,19 +56,20 @@ using namespace tc;
 constexpr int kBM = 128, kBK = 64;
 constexpr int kRawStages = 2;   // raw code stages (tensor-memory-accelerator ring)
 constexpr int kOpStages = 4;    // operand stages (A in tensor memory, B in shared memory)
-// kSplit converter threads per row, each taking 2 / kSplit of the step's two 32-element blocks.
+// Converter threads per row of wide tiles (each taking 2 / split of the step's two 32-element
+// blocks); narrow tiles always use two (their CTAs are few, so more warps per CTA pay).
 #ifndef MX_GEMM_SPLIT
 #define MX_GEMM_SPLIT 1
 #endif
-constexpr int kSplit = MX_GEMM_SPLIT;
-constexpr int kBlocksPerThread = 2 / kSplit;
-constexpr int kAWarps = 4 * kSplit;
 constexpr uint32_t kAStageCols = kBK / 2;     // bf16 pairs of a 64-wide K step
 
 // Everything that depends on the tile's width BN (columns of C, rows of B): 256 for large
 // problems, 64 when 128 x 256 tiles would not fill the SMs (two CTAs per SM then).
 template <int BN>
 struct Tile {
+  static constexpr int kSplit = BN <= 64 ? 2 : MX_GEMM_SPLIT;  // converter threads per row
+  static constexpr int kBlocksPerThread = 2 / kSplit;
+  static constexpr int kAWarps = 4 * kSplit;
   static constexpr int kBRowWarps = BN / 32;  // warps covering B's rows once
   static constexpr int kBWarps = kBRowWarps * kSplit, kConvWarps = kAWarps + kBWarps;
   static constexpr int kTmaWarp = kConvWarps, kMmaWarp = kConvWarps + 1;
@@ -79,7 +80,7 @@ struct Tile {
   static constexpr uint32_t kAccCols = BN;  // fp32 accumulator columns
   static constexpr uint32_t kTmemCols = BN + kOpStages * kAStageCols <= 256 ? 256 : 512;
   static constexpr int kBOpBytes = BN * kBK * 2;  // bf16 of one B stage (32 or 8 KiB)
-  static constexpr int kMinCtas = BN <= 64 ? 2 : 1;
+  static constexpr int kMinCtas = 1;
   static_assert(kEpiWarps <= kConvWarps, "the epilogue runs on converter warps");
   static_assert(kEpiCols % 32 == 0, "32-column accumulator loads");
   static_assert((BN / 64) * kBM * 128 <= kOpStages * kBOpBytes, "C staging fits the B stages");
@@ -366,6 +367,7 @@ __device__ __forceinline__ void gemm_roles(const CUtensorMap& cmap, const GemmAr
                                            const GemmCta<FMT>& c) {
   using R = RawLayout<FMT, BN>;
   using T = Tile<BN>;
+  constexpr int kSplit = T::kSplit, kBlocksPerThread = T::kBlocksPerThread, kAWarps = T::kAWarps;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t tmem = c.tmem;
   const int nk = c.nk;
@@ -599,6 +601,7 @@ __global__ void __launch_bounds__(Tile<BN>::kThreads, Tile<BN>::kMinCtas)
     if ((tid & 31) == 0) gemm_loads<FMT, BN>(amap, bmap, a, c);
   } else {
     if (warp < T::kConvWarps) {  // f16 window vote over the CTA's scale bytes
+      constexpr int kAWarps = T::kAWarps;
       const bool is_a = warp < kAWarps;
       const int wq = is_a ? warp : warp - kAWarps;
       const int row_warps = is_a ? 4 : T::kBRowWarps;
@@ -654,18 +657,18 @@ cudaError_t launch_tile(const GemmArgs& a, cudaStream_t stream) {
                     bmap, cmap, a);
 }
 
-// 128 x 256 tiles, or 128 x 64 tiles (two CTAs per SM) when the 128 x 256 tiles would leave
-// SMs idle and the narrow tiles fit in one wave. Measured (E2M1, M x 8192 x 8192): M = 16
-// 73 -> 59 us, M = 128 77 -> 58 us with narrow tiles; M = 512 (512 narrow tiles, 1.7 waves)
-// 78 -> 153 us, so narrow tiles beyond one wave are not taken.
+// 128 x 256 tiles, or 128 x 64 tiles when the 128 x 256 tiles would leave SMs idle and the
+// narrow tiles fit in one wave (narrow tiles beyond one wave measured 2x slower at M = 512).
 template <int FMT, bool SWZ>
 cudaError_t launch_t(const GemmArgs& a, cudaStream_t stream) {
   const void* k = reinterpret_cast<const void*>(&mx_gemm_kernel<FMT, SWZ, 256>);
   const int sms = resident_ctas(k, Tile<256>::kThreads, gemm_smem<FMT, 256>(), 1);
+  const void* kn = reinterpret_cast<const void*>(&mx_gemm_kernel<FMT, SWZ, 64>);
+  const int narrow_slots = resident_ctas(kn, Tile<64>::kThreads, gemm_smem<FMT, 64>(), 4);
   const int64_t row_tiles = (a.M + kBM - 1) / kBM;
   const int64_t wide_tiles = row_tiles * ((a.N + 255) / 256);
   const int64_t narrow_tiles = row_tiles * ((a.N + 63) / 64);
-  if (sms > 0 && wide_tiles < sms && narrow_tiles <= 2 * (int64_t)sms) {
+  if (sms > 0 && wide_tiles < sms && narrow_tiles <= narrow_slots) {
     return launch_tile<FMT, SWZ, 64>(a, stream);
   }
   return launch_tile<FMT, SWZ, 256>(a, stream);
