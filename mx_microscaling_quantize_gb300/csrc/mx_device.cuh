@@ -80,38 +80,34 @@ __device__ __forceinline__ uint32_t absmax_bf16x8(const uint4& v) {
   return max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
 }
 
+// max(|a|, |b|, |c|) in one instruction; NaN if any input is NaN.
+__device__ __forceinline__ float absmax3(float a, float b, float c) {
+  float d;
+  asm("max.NaN.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // abs-max of 16 fp32 values as sign-free fp32 bits; NaN propagates.
 __device__ __forceinline__ uint32_t absmax_f32x16(const float* y) {
-  float m[8];
+  // three-input tree: 16 -> 6 -> 2 -> 1 in 8 instructions
+  float m[6];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(m[i]) : "f"(y[2 * i]), "f"(y[2 * i + 1]));
-  }
-#pragma unroll
-  for (int w = 4; w >= 1; w >>= 1) {
-#pragma unroll
-    for (int i = 0; i < w; ++i) {
-      asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(m[i]) : "f"(m[i]), "f"(m[i + w]));
-    }
-  }
-  return __float_as_uint(m[0]) & 0x7FFFFFFFu;
+  for (int i = 0; i < 5; ++i) m[i] = absmax3(y[3 * i], y[3 * i + 1], y[3 * i + 2]);
+  m[5] = y[15];
+  const float p = absmax3(m[0], m[1], m[2]), q = absmax3(m[3], m[4], m[5]);
+  return __float_as_uint(absmax3(p, q, q)) & 0x7FFFFFFFu;
 }
 
 // abs-max of 32 fp32 values as sign-free fp32 bits; NaN propagates.
 __device__ __forceinline__ uint32_t absmax_f32x32(const float* y) {
-  float m[16];
+  // three-input tree: 32 -> 11 -> 4 -> 1 in 17 instructions
+  float m[11];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(m[i]) : "f"(y[2 * i]), "f"(y[2 * i + 1]));
-  }
-#pragma unroll
-  for (int w = 8; w >= 1; w >>= 1) {
-#pragma unroll
-    for (int i = 0; i < w; ++i) {
-      asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(m[i]) : "f"(m[i]), "f"(m[i + w]));
-    }
-  }
-  return __float_as_uint(m[0]) & 0x7FFFFFFFu;
+  for (int i = 0; i < 10; ++i) m[i] = absmax3(y[3 * i], y[3 * i + 1], y[3 * i + 2]);
+  m[10] = absmax3(y[30], y[31], y[31]);
+  const float p0 = absmax3(m[0], m[1], m[2]), p1 = absmax3(m[3], m[4], m[5]);
+  const float p2 = absmax3(m[6], m[7], m[8]), p3 = absmax3(m[9], m[10], m[10]);
+  return __float_as_uint(absmax3(absmax3(p0, p1, p2), p3, p3)) & 0x7FFFFFFFu;
 }
 
 // ------------------------------------------------------------------------------------------
