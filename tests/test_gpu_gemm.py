@@ -240,6 +240,39 @@ def test_gemm_times_identity_inside_the_f16_window(fmt, layout):
     np.testing.assert_array_equal(zero_sign_free(T.bf16_bits(c2)), want.T)
 
 
+def identity_operand_fast(n, fmt, layout):
+    """identity_operand built with array indexing (n = 8192 in the wide-tile tests)."""
+    codes = np.zeros((n, O.code_bytes_per_row(fmt, n)), dtype=np.uint8)
+    i = np.arange(n)
+    if fmt == O.E4M3:
+        codes[i, i] = 0x38
+    else:
+        codes[i, i // 2] = np.where(i % 2 == 0, 0x02, 0x20)
+    return codes, np.full(O.scales_shape(n, n, layout), 127, dtype=np.uint8)
+
+
+@pytest.mark.parametrize("window", ["bf16", "f16"])
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemm_times_identity_wide_tiles(fmt, layout, window):
+    """The identity products at a size that takes the 128 x 256 tiles (A [640, 8192] against
+    the 8192 x 8192 identity, both operand orders): bit-exact against the oracle's dequantize,
+    with scale bytes 0..239 (bf16 operands) or inside the f16 window (f16 operands)."""
+    M, K = 640, 8192
+    rng = np.random.default_rng(11 + fmt + 2 * layout + (window == "f16"))
+    lo, hi = (0, 240) if window == "bf16" else (F16_WINDOW[fmt][0], F16_WINDOW[fmt][1] + 1)
+    a, sa = random_operand(rng, M, K, fmt, layout, lo=lo, hi=hi)
+    if layout == O.SWIZZLED and window == "f16":
+        sa[:] = np.where(sa == 0, lo, sa)
+    ident, si = identity_operand_fast(K, fmt, layout)
+    want = zero_sign_free(O.dequantize(a, sa, K, fmt, layout))
+    ga, gsa, gi, gsi = dev(a), dev(sa), dev(ident), dev(si)
+    c1 = mxq.mx_gemm(ga, gsa, gi, gsi, K, fmt, layout)
+    np.testing.assert_array_equal(zero_sign_free(T.bf16_bits(c1)), want)
+    c2 = mxq.mx_gemm(gi, gsi, ga, gsa, K, fmt, layout)
+    np.testing.assert_array_equal(zero_sign_free(T.bf16_bits(c2)), want.T)
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_gemm_nan_scale_poisons_its_rows_and_columns(fmt):
     M, N, K = 160, 144, 256
