@@ -67,6 +67,11 @@ def _load():
         "mxo_quantize_values": (None, [p, i64, i64, i32, i32, p, p]),
         "mxo_qdq_values": (None, [p, i64, i64, i32, p]),
         "mxo_nvfp4_values": (None, [p, i64, i64, ctypes.c_float, i32, p, p, p]),
+        "mxo_quest_alpha": (dbl, []),
+        "mxo_quest_scale_byte": (i32, [p, i32]),
+        "mxo_quest_quantize_block": (i32, [p, i32, p]),
+        "mxo_quest_quantize_values": (None, [p, i64, i64, i32, p, p]),
+        "mxo_quest_qdq_values": (None, [p, i64, i64, p]),
         "mxo_quantize_grouped": (None, [p, p, i32, i64, i32, i32, i64, p, p]),
         "mxo_nvfp4_scales_shape": (None, [i64, i64, i32, p, p]),
         "mxo_nvfp4_block": (i32, [p, i32, ctypes.c_float, p]),
@@ -245,6 +250,62 @@ def qdq_values(v, fmt: int) -> np.ndarray:
     out = np.zeros((M, K), dtype=np.uint16)
     _load().mxo_qdq_values(_ptr(v), M, K, fmt, _ptr(out))
     return out
+
+
+# ----------------------------------------------------------------------------------------------
+# Quest-like scale (MXFP4): E8M0 scale from the clip point alpha * RMS of the block instead of its
+# abs-max (mx_oracle.cpp, quest_scale_byte, states the reading); E2M1 elements.
+# ----------------------------------------------------------------------------------------------
+def quest_alpha() -> float:
+    """The clip ratio alpha the oracle uses (clip point over the block's RMS)."""
+    return _load().mxo_quest_alpha()
+
+
+def quest_scale_byte(values) -> int:
+    """E8M0 byte of one block of finite values under the Quest-like rule."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    return _load().mxo_quest_scale_byte(_ptr(v), v.size)
+
+
+def quest_quantize_block(values):
+    """-> (scale byte, unpacked E2M1 codes uint8 [n]) of one block under the Quest-like rule."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    codes = np.zeros(v.size, dtype=np.uint8)
+    byte = _load().mxo_quest_quantize_block(_ptr(v), v.size, _ptr(codes))
+    return byte, codes
+
+
+def quest_quantize_values(v, layout: int):
+    """Quest-like MXFP4 quantize of float64 values [M, K] -> (codes [M, K/2], scales)."""
+    v = _values(v)
+    M, K = v.shape
+    codes = np.zeros((M, K // 2), dtype=np.uint8)
+    scales = np.zeros(scales_shape(M, K, layout), dtype=np.uint8)
+    _load().mxo_quest_quantize_values(_ptr(v), M, K, layout, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def quest_qdq_values(v) -> np.ndarray:
+    """Quest-like MXFP4 QDQ of float64 values [M, K] -> bf16 bits [M, K]."""
+    v = _values(v)
+    M, K = v.shape
+    out = np.zeros((M, K), dtype=np.uint16)
+    _load().mxo_quest_qdq_values(_ptr(v), M, K, _ptr(out))
+    return out
+
+
+def _quest_inputs(x_bits, H_bits):
+    return bf16_bits_to_double(_bits(x_bits)) if H_bits is None else rotate(x_bits, H_bits)
+
+
+def quest_quantize(x_bits, layout: int, H_bits=None):
+    """Quest-like MXFP4 quantize of bf16 x [M, K], rotated first by H when given."""
+    return quest_quantize_values(_quest_inputs(x_bits, H_bits), layout)
+
+
+def quest_qdq(x_bits, H_bits=None) -> np.ndarray:
+    """Quest-like MXFP4 QDQ of bf16 x [M, K] (in the rotated basis when H is given)."""
+    return quest_qdq_values(_quest_inputs(x_bits, H_bits))
 
 
 def quantize_grouped(x_bits, offsets, fmt: int, layout: int, scale_rows: int | None = None):

@@ -21,6 +21,8 @@
 //   scale exponent s = floor(log2(amax)) - emax, clamped to [-127, 127], stored as s + 127;
 //   element code = nearest member of the format's finite grid to x / 2^s, ties to the code
 //   with an even mantissa, magnitudes above the grid maximum saturate to it, sign kept.
+// The Quest-like MXFP4 scale (quest_scale_byte) is a further reading, stated where it is defined:
+// the pages name the scheme but give no rule.
 // Parity of this file is pinned by the CPU tests (format definitions, closed forms, brute force,
 // torch's float8_e4m3fn casts, invariants); see tests/test_oracle_pins.py.
 
@@ -189,6 +191,50 @@ int quantize_block(const ElementFormat& f, const double* v, int n, int forced_by
   return byte;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Quartet / "Quest-like" block scale for MXFP4. The QuTLASS page names the scheme (feature list,
+// "Multiple quantization schemes": "Quartet (i.e., Quest-like)") and its call (review thread on
+// vllm/_custom_ops.py: fusedQuantizeMxQuest(a, b, xh_e2m1, xh_e8m0) writes the E2M1 codes and
+// E8M0 scales of the rotated input), but prints no rule. Reading taken: the shared scale follows
+// the MX rule with the block's clip point c in place of its abs-max,
+//   RMS = sqrt(sum_i v_i^2 / n),  c = alpha * RMS,
+//   s = floor(log2 c) - emax(E2M1) clamped to [-127, 127], stored as s + 127 (c == 0: byte 0),
+// where alpha is the clip ratio (clip point over standard deviation) that minimises the mean
+// squared error of the E2M1 grid, stretched so that its largest value 6 sits at the clip point,
+// on a standard normal variable (the Gaussian clipping of the QuEST method). The elements then
+// follow quantize_block under that byte: values above 6 * 2^s saturate, which is the clipping.
+// ---------------------------------------------------------------------------------------------
+const double kQuestAlpha = 2.922475;  // the minimiser, to 7 significant digits
+
+// Scale byte of a block of n finite values under the reading above.
+int quest_scale_byte(const double* v, int n) {
+  double sum_sq = 0.0;
+  for (int i = 0; i < n; ++i) sum_sq += v[i] * v[i];
+  const double c = kQuestAlpha * std::sqrt(sum_sq / n);
+  if (c == 0.0) return 0;
+  int ex;
+  std::frexp(c, &ex);
+  int s = (ex - 1) - kE2M1.emax;  // floor(log2 c) - emax
+  if (s < -127) s = -127;
+  if (s > 127) s = 127;
+  return s + 127;
+}
+
+// quantize_block with the scale from quest_scale_byte (E2M1 elements). A block holding a NaN or
+// an infinity gets byte 0xFF and codes 0, as in quantize_block.
+int quantize_block_quest(const double* v, int n, uint8_t* codes) {
+  for (int i = 0; i < n; ++i) {
+    if (std::isnan(v[i]) || std::isinf(v[i])) return quantize_block(kE2M1, v, n, -1, codes);
+  }
+  return quantize_block(kE2M1, v, n, quest_scale_byte(v, n), codes);
+}
+
+// Scale schemes of the tensor operations below: 0 = abs-max (quantize_block), 1 = Quest-like
+// (quantize_block_quest, E2M1 only).
+int block_with_scheme(const ElementFormat& f, int scheme, const double* v, uint8_t* codes) {
+  return scheme == 1 ? quantize_block_quest(v, 32, codes) : quantize_block(f, v, 32, -1, codes);
+}
+
 // Value of one code at scale 2^0. E4M3 S.1111.111 (0x7F, 0xFF) is the format's NaN.
 double decode_code(const ElementFormat& f, int code) {
   int magnitude_code = code & (f.sign_bit - 1);
@@ -221,12 +267,13 @@ int64_t swizzled_offset(int64_t r, int64_t c, int64_t padded_cols) {
 // Quantize `rows` rows of `v` (doubles, row-major [rows, K]) whose first row is row `row0` of the
 // scale matrix. layout 0 = linear [*, K/32], 1 = swizzled.
 void quantize_rows(const ElementFormat& f, const double* v, int64_t rows, int64_t K, int64_t row0,
-                   int layout, int64_t padded_cols, uint8_t* codes, uint8_t* scales) {
+                   int layout, int64_t padded_cols, uint8_t* codes, uint8_t* scales,
+                   int scheme = 0) {
   const int64_t groups = K / 32;
   uint8_t block_codes[32];
   for (int64_t r = 0; r < rows; ++r) {
     for (int64_t j = 0; j < groups; ++j) {
-      int byte = quantize_block(f, v + r * K + j * 32, 32, -1, block_codes);
+      int byte = block_with_scheme(f, scheme, v + r * K + j * 32, block_codes);
       if (layout == 0) {
         scales[(row0 + r) * groups + j] = (uint8_t)byte;
       } else {
@@ -247,11 +294,12 @@ void quantize_rows(const ElementFormat& f, const double* v, int64_t rows, int64_
   }
 }
 
-void qdq_rows(const ElementFormat& f, const double* v, int64_t rows, int64_t K, uint16_t* out) {
+void qdq_rows(const ElementFormat& f, const double* v, int64_t rows, int64_t K, uint16_t* out,
+              int scheme = 0) {
   uint8_t block_codes[32];
   for (int64_t r = 0; r < rows; ++r) {
     for (int64_t j = 0; j < K / 32; ++j) {
-      int byte = quantize_block(f, v + r * K + j * 32, 32, -1, block_codes);
+      int byte = block_with_scheme(f, scheme, v + r * K + j * 32, block_codes);
       for (int i = 0; i < 32; ++i) {
         out[r * K + j * 32 + i] = dequant_to_bf16(f, block_codes[i], byte);
       }
@@ -495,6 +543,29 @@ void mxo_quantize_values(const double* v, int64_t M, int64_t K, int fmt, int lay
 
 void mxo_qdq_values(const double* v, int64_t M, int64_t K, int fmt, uint16_t* out) {
   qdq_rows(*format_of(fmt), v, M, K, out);
+}
+
+// Quest-like scale (see quest_scale_byte): the constant, the byte of one block of n finite
+// values, one block's codes, and the tensor operations on float64 values [M, K] (bf16 inputs
+// decoded, or the rotated values of mxo_rotate), E2M1 elements.
+double mxo_quest_alpha() { return kQuestAlpha; }
+
+int mxo_quest_scale_byte(const double* v, int n) { return quest_scale_byte(v, n); }
+
+int mxo_quest_quantize_block(const double* v, int n, uint8_t* codes) {
+  return quantize_block_quest(v, n, codes);
+}
+
+void mxo_quest_quantize_values(const double* v, int64_t M, int64_t K, int layout, uint8_t* codes,
+                               uint8_t* scales) {
+  int64_t srows, scols;
+  mxo_scales_shape(M, K, layout, &srows, &scols);
+  std::memset(scales, 0, (size_t)(srows * scols));
+  quantize_rows(kE2M1, v, M, K, 0, layout, scols, codes, scales, 1);
+}
+
+void mxo_quest_qdq_values(const double* v, int64_t M, int64_t K, uint16_t* out) {
+  qdq_rows(kE2M1, v, M, K, out, 1);
 }
 
 // Grouped (MoE) quantize: rows [offsets[e], offsets[e+1]) belong to expert e. Codes stay

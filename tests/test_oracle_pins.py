@@ -733,3 +733,178 @@ def test_gemm_matches_a_brute_force_sum(fmt, layout):
         for j in range(N):
             want = 1.5 * sum(value(a, la, i, k) * value(b, lb, j, k) for k in range(K))
             assert C[i, j] == pytest.approx(want, rel=1e-15, abs=1e-300)
+
+
+# ---------------------------------------------------------------------------------------------
+# Quest-like MXFP4 scale (clip point alpha * RMS in place of the abs-max)
+# ---------------------------------------------------------------------------------------------
+E2M1_GRID = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)  # the format's magnitudes (1 sign, E2M1)
+
+
+def gaussian_grid_mse(alpha: float) -> float:
+    """E[(Z - q(Z))^2] for Z ~ N(0, 1) and q the E2M1 grid stretched so that 6 sits at alpha
+    (nearest grid point, saturating), integrated piecewise between the decision points."""
+    from scipy import integrate, stats
+    t = alpha / 6.0
+    mids = [(a + b) / 2 for a, b in zip(E2M1_GRID, E2M1_GRID[1:])]
+    edges = [0.0] + [t * m for m in mids] + [math.inf]
+    total = 0.0
+    for k, level in enumerate(E2M1_GRID):
+        f = lambda z, q=level * t: (z - q) ** 2 * stats.norm.pdf(z)
+        total += integrate.quad(f, edges[k], edges[k + 1], epsabs=1e-14, epsrel=1e-13)[0]
+    return 2.0 * total
+
+
+def test_quest_alpha_minimises_gaussian_mse_of_e2m1_grid():
+    """The oracle's clip ratio is the minimiser of the grid's mean squared error on a standard
+    normal variable (the Gaussian clipping of the QuEST method), found here by quadrature."""
+    from scipy import optimize
+    res = optimize.minimize_scalar(gaussian_grid_mse, bounds=(1.0, 6.0), method="bounded",
+                                   options={"xatol": 1e-10})
+    alpha = O.quest_alpha()
+    assert abs(alpha - res.x) < 2e-6
+    best = gaussian_grid_mse(alpha)
+    assert best <= res.fun * (1 + 1e-9)
+    for d in (-0.05, -0.01, 0.01, 0.05):  # a minimum, not a flat stretch
+        assert gaussian_grid_mse(alpha + d) > best
+
+
+def _read_quest_blocks():
+    blocks = []
+    for line in open(os.path.join(GOLDEN, "quest_worked_blocks.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        parts = line.split()
+        if parts[0] == "block":
+            blocks.append((parts[1], int(parts[2]), []))
+        else:
+            blocks[-1][2].append((int(parts[0]), float(parts[1]), int(parts[2], 16)))
+    return blocks
+
+
+@pytest.mark.parametrize("case", _read_quest_blocks(), ids=lambda c: c[0])
+def test_quest_worked_blocks(case):
+    name, byte, entries = case
+    v = np.zeros(32)
+    want = np.zeros(32, dtype=np.uint8)
+    i = 0
+    for count, val, code in entries:
+        v[i:i + count] = val
+        want[i:i + count] = code
+        i += count
+    assert (W.bf16_bits_to_float(bf16(v)) == v.astype(np.float32)).all(), name
+    got_byte, got = O.quest_quantize_block(v)
+    assert got_byte == byte, name
+    np.testing.assert_array_equal(got, want, err_msg=name)
+    assert O.quest_scale_byte(v) == byte
+    codes, scales = O.quest_quantize(bf16(v).reshape(1, 32), O.LINEAR)
+    assert scales[0, 0] == byte
+    np.testing.assert_array_equal(codes[0] & 0xF, want[0::2])
+    np.testing.assert_array_equal(codes[0] >> 4, want[1::2])
+
+
+def _quest_byte_exact(v) -> int:
+    """Scale byte by exact rational arithmetic: k = floor(log2 c) is the k with
+    4^k <= c^2 < 4^(k+1), c^2 = alpha^2 * sum(v^2) / 32, alpha taken as the decimal 2.922475."""
+    from fractions import Fraction
+    alpha = Fraction(2922475, 10 ** 6)
+    c2 = alpha * alpha * sum(Fraction(float(x)) ** 2 for x in v) / 32
+    if c2 == 0:
+        return 0
+    k = (c2.numerator.bit_length() - c2.denominator.bit_length()) // 2 - 2
+    while Fraction(4) ** (k + 1) <= c2:
+        k += 1
+    while Fraction(4) ** k > c2:
+        k -= 1
+    return min(max(k - 2, -127), 127) + 127
+
+
+def test_quest_scale_byte_matches_exact_arithmetic():
+    rng = np.random.default_rng(11)
+    blocks = []
+    for e in (-140, -126, -60, -3, 0, 5, 60, 120, 126):  # spread over the whole exponent range
+        blocks.append(rng.standard_normal(32) * 2.0 ** e)
+        blocks.append(rng.uniform(-1, 1, 32) * 2.0 ** e)
+    for e in range(-130, 128, 7):  # blocks whose c sits next to a power of two, every binade
+        blocks.append(np.full(32, 1.375 * 2.0 ** e))
+        blocks.append(np.full(32, 1.3671875 * 2.0 ** e))
+    for _ in range(300):
+        blocks.append(rng.standard_normal(32) * 2.0 ** rng.integers(-20, 20))
+    for v in blocks:
+        v = W.bf16_bits_to_float(bf16(v)).astype(np.float64)  # bf16 inputs, as on the path
+        assert O.quest_scale_byte(v) == _quest_byte_exact(v), v
+
+
+def test_quest_scale_invariants():
+    """Power-of-two equivariance, sign symmetry, and the bounds RMS in [amax/sqrt(32), amax]
+    give against the abs-max byte: floor(log2 c) - floor(log2 amax) in [-1, 2]."""
+    rng = np.random.default_rng(12)
+    cases = [rng.standard_normal(32) for _ in range(200)]
+    cases += [np.eye(32)[i] * rng.uniform(1, 2) for i in range(32)]       # one-hot (RMS low)
+    cases += [np.full(32, rng.uniform(1, 2)) * rng.choice([-1, 1], 32) for _ in range(32)]
+    for v in cases:
+        v = W.bf16_bits_to_float(bf16(v)).astype(np.float64)
+        b, codes = O.quest_quantize_block(v)
+        b_abs = O.scale_byte(O.E2M1, float(np.abs(v).max()))
+        assert -1 <= b - b_abs <= 2
+        for k in (-40, -1, 3, 50):
+            b2, codes2 = O.quest_quantize_block(v * 2.0 ** k)
+            assert b2 == b + k
+            np.testing.assert_array_equal(codes2, codes)
+        bn, codesn = O.quest_quantize_block(-v)
+        assert bn == b
+        np.testing.assert_array_equal(codesn ^ 8, codes)
+    nan_block = np.ones(32)
+    nan_block[5] = np.nan
+    assert O.quest_quantize_block(nan_block)[0] == 0xFF
+    inf_block = np.ones(32)
+    inf_block[7] = -np.inf
+    b, codes = O.quest_quantize_block(inf_block)
+    assert b == 0xFF and not codes.any()
+
+
+def test_quest_gaussian_qdq_error_reaches_the_optimum():
+    """On normal data the Quest-like scale's QDQ error is within 1.5% of the continuous
+    optimum (the grid's Gaussian MSE at alpha) and below the abs-max scale's."""
+    rng = np.random.default_rng(13)
+    v = rng.standard_normal((2000, 320))
+    qd = W.bf16_bits_to_float(O.quest_qdq_values(v)).astype(np.float64)
+    qa = W.bf16_bits_to_float(O.qdq_values(v, O.E2M1)).astype(np.float64)
+    mse_q = float(((qd - v) ** 2).mean())
+    mse_a = float(((qa - v) ** 2).mean())
+    optimum = gaussian_grid_mse(O.quest_alpha())
+    assert abs(mse_q / optimum - 1) < 0.015
+    assert mse_q < 0.98 * mse_a
+
+
+def test_quest_tensor_entry_points_assemble_the_blocks():
+    """Tensor calls (linear / swizzled scales, QDQ, rotated input) against block-by-block calls
+    and the dequantize definition."""
+    rng = np.random.default_rng(14)
+    M, K = 130, 192
+    x = bf16(rng.standard_normal((M, K)) * np.exp(rng.uniform(-3, 3, (M, 1))))
+    v = W.bf16_bits_to_float(x).astype(np.float64)
+    codes_l, scales_l = O.quest_quantize(x, O.LINEAR)
+    codes_s, scales_s = O.quest_quantize(x, O.SWIZZLED)
+    np.testing.assert_array_equal(codes_l, codes_s)
+    rows, cols = O.scales_shape(M, K, O.SWIZZLED)
+    for r in range(M):
+        for j in range(K // 32):
+            b, c = O.quest_quantize_block(v[r, 32 * j:32 * j + 32])
+            assert scales_l[r, j] == b
+            assert scales_s.reshape(-1)[O.swizzled_offset(r, j, cols)] == b
+            packed = codes_l[r, 16 * j:16 * j + 16]
+            np.testing.assert_array_equal(packed & 0xF, c[0::2])
+            np.testing.assert_array_equal(packed >> 4, c[1::2])
+    np.testing.assert_array_equal(O.quest_qdq(x), O.dequantize(codes_l, scales_l, K, O.E2M1,
+                                                                O.LINEAR))
+    g = 32
+    h = np.array([[1.0]])
+    while h.shape[0] < g:
+        h = np.block([[h, h], [h, -h]])
+    H = bf16(h / math.sqrt(g))
+    y = O.rotate(x, H)
+    np.testing.assert_array_equal(O.quest_quantize(x, O.SWIZZLED, H)[1],
+                                  O.quest_quantize_values(y, O.SWIZZLED)[1])
+    np.testing.assert_array_equal(O.quest_qdq(x, H), O.quest_qdq_values(y))
