@@ -436,6 +436,36 @@ def extra_workloads(dev, peak):
             del c, s
         del x
 
+    # the Quest-like MXFP4 scale (rounding QUEST): plain quantize and QDQ of the QDQ weight,
+    # rotate(g = 32) + quantize of the rotate + quantize activation, both rotation kinds
+    x = to_gpu(W.mxfp4_qdq_weight(), dev)
+    c, s = mxq.mx_quantize(x, mxq.E2M1, mxq.SWIZZLED, rounding=mxq.QUEST)
+
+    def make(k, x=x, c=c, s=s):
+        xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+        return lambda: mxq.mx_quantize(xk, mxq.E2M1, mxq.SWIZZLED, codes=ck, scales=sk,
+                                       rounding=mxq.QUEST)
+    nb = 2 * x.numel() + c.numel() + s.numel()
+    measure("quest_quant_mxfp4_swizzled[8192,8192]", nb, x.numel(), make, nb)
+    y = torch.empty_like(x)
+
+    def make(k, x=x, y=y):
+        xk, yk = copy_of(x, k), empty_of(y, k)
+        return lambda: mxq.mx_qdq(xk, mxq.E2M1, y=yk, rounding=mxq.QUEST)
+    measure("quest_qdq_mxfp4[8192,8192]", 4 * x.numel(), x.numel(), make, 4 * x.numel())
+    del x, y, c, s
+    for M, K in ((8192, 8192), (8192, 28672)):
+        x = to_gpu(W.rotate_quant_activation(M, K), dev)
+        c, s = mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, rounding=mxq.QUEST)
+        for rk, kname in kinds:
+            def make(k, x=x, c=c, s=s, rk=rk):
+                xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+                return lambda: mxq.mx_rotate_quantize(xk, H, mxq.E2M1, mxq.SWIZZLED, codes=ck,
+                                                      scales=sk, rot_kind=rk, rounding=mxq.QUEST)
+            nb = 2 * x.numel() + c.numel() + s.numel()
+            measure(f"quest_rotate_quant_mxfp4_g32{kname}[{M},{K}]", nb, x.numel(), make, nb)
+        del x, c, s
+
     # dequantize stored codes + scales of the QDQ weight x[8192, 8192]
     x = to_gpu(W.mxfp4_qdq_weight(), dev)
     y = torch.empty_like(x)
@@ -568,6 +598,9 @@ CASES = {
     "nvfp4_rotate_quant": "NVFP4 rotate(g=16)+quantize, swizzled, x[8192,28672]",
     "nvfp4_dequant": "NVFP4 dequantize, swizzled E4M3 scales, codes of the weight x[8192,8192]",
     "rotate_quant_decode": "E2M1 rotate(g=32)+quantize, swizzled, x[16,28672] (FMA kernel)",
+    "rotate_quant_quest": "E2M1 rotate(g=32 Hadamard)+quantize under the Quest-like scale, "
+                          "swizzled, x[8192,8192] (tensor-core kernel)",
+    "qdq_quest": "E2M1 QDQ under the Quest-like scale, weight x[8192,8192] (streaming kernel)",
     "moe_quant_nvfp4": "NVFP4 grouped quantize, swizzled, 128 experts, per-expert scales, x[16384,2048]",
     "qdq_vs_copy": "MXFP4 QDQ of the weight and activation, each followed by an elementwise "
                    "copy of the same bytes (torch.mul(x, 1, out=y)) for profiler comparisons",
@@ -752,6 +785,18 @@ def run_case(args):
         c, s = mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED)
         fn = lambda: mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, codes=c, scales=s)
         nbytes = 2 * x.numel() + c.numel() + s.numel()
+    elif args.case == "rotate_quant_quest":
+        x = to_gpu(W.rotate_quant_activation(8192, 8192), dev)
+        H = to_gpu(W.normalized_hadamard_bf16(32), dev)
+        c, s = mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, rounding=mxq.QUEST)
+        fn = lambda: mxq.mx_rotate_quantize(x, H, mxq.E2M1, mxq.SWIZZLED, codes=c, scales=s,
+                                            rounding=mxq.QUEST)
+        nbytes = 2 * x.numel() + c.numel() + s.numel()
+    elif args.case == "qdq_quest":
+        x = to_gpu(W.mxfp4_qdq_weight(), dev)
+        y = torch.empty_like(x)
+        fn = lambda: mxq.mx_qdq(x, mxq.E2M1, y=y, rounding=mxq.QUEST)
+        nbytes = 4 * x.numel()
     elif args.case == "rotate_quant_hadamard":
         x = to_gpu(W.rotate_quant_activation(8192, 8192), dev)
         H = to_gpu(W.normalized_hadamard_bf16(32), dev)

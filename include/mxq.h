@@ -69,8 +69,26 @@ typedef int mx_status;
 #define MX_SCALES_LINEAR 0   /* [M, K/32] row-major */
 #define MX_SCALES_SWIZZLED 1 /* 128x4 blocked tiles, padded (see above) */
 
-/* rounding schemes */
-#define MX_ROUND_RNE 0 /* abs-max floor scale, round to nearest even, saturate */
+/*
+ * Rounding schemes (argument `rounding`): how the block scale is chosen. The elements are always
+ * rounded to nearest even with saturation under the chosen scale.
+ *  MX_ROUND_RNE: the abs-max scale above (the QuTLASS feature list's "Abs-Max" scheme).
+ *  MX_ROUND_QUEST: the Quartet / "Quest-like" scale (QuTLASS feature list: "Multiple
+ *    quantization schemes ... Quartet (i.e., Quest-like)"; the review thread on
+ *    vllm/_custom_ops.py names its call fusedQuantizeMxQuest(a, b, xh_e2m1, xh_e8m0)). MXFP4
+ *    (MX_FMT_E2M1) only; not for grouped calls. The pages print no rule; the reading is the
+ *    rule above with the block's clip point c in place of amax:
+ *      c = alpha * sqrt(sum_i v_i^2 / 32),  s = clamp(floor(log2 c) - 2, -127, 127),
+ *    alpha = 2.922475, the ratio of clip point to standard deviation that minimises the mean
+ *    squared error of the E2M1 grid (its largest value 6 at the clip point) on a normally
+ *    distributed input; values above 6 * 2^s saturate (the clipping). An all-zero block gets
+ *    byte 0, a block with a NaN or an infinity 0xFF as above. The sum of squares is formed in
+ *    fp32 after an exact power-of-two scaling (no overflow or underflow for any finite input),
+ *    so s can differ from the real-number rule only where c lies within about 2^-20 relative of
+ *    a power of two.
+ */
+#define MX_ROUND_RNE 0
+#define MX_ROUND_QUEST 1
 
 /*
  * Rotation kinds (argument rot_kind of the rotating calls; ignored where H is NULL).
@@ -106,7 +124,7 @@ mx_status mx_scales_shape(int64_t M, int64_t K, int group, int layout, int64_t* 
 /*
  * Block quantize (pages: fusedQuantizeMx without the rotation; mxfp8_quantize).
  * x: bf16 [M, K]. codes: see layouts. scales: per `layout`. fmt: MX_FMT_*. group: must be 32.
- * rounding: MX_ROUND_RNE. Errors: see conventions.
+ * rounding: MX_ROUND_RNE, or MX_ROUND_QUEST with MX_FMT_E2M1. Errors: see conventions.
  */
 mx_status mx_quantize(const void* x, int64_t M, int64_t K, int fmt, int group, int layout,
                       int rounding, void* codes, void* scales, void* stream);
@@ -117,6 +135,7 @@ mx_status mx_quantize(const void* x, int64_t M, int64_t K, int fmt, int group, i
  * (H: bf16 [g, g] row-major device matrix, g in {16, 32, 64, 128}, K % g == 0, rot_kind an
  * MX_ROT_* value), and the rotated values are quantized; the output stays in the rotated
  * basis. If H is NULL, g and rot_kind are ignored. y: bf16 [M, K], must not overlap x.
+ * rounding as in mx_quantize.
  */
 mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int rounding,
                  const void* H, int g, int rot_kind, void* y, void* stream);
@@ -164,7 +183,7 @@ mx_status mx_grouped_scales_shape(int64_t M_total, int E, int64_t K, int group, 
  * rows start at padded row P_e = sum_{e' < e} ceil(n_e'/128) * 128; the buffer has
  * mx_grouped_scales_shape() rows and all of it is written (rows past the last expert: zero).
  * 1 <= E <= 1024. Offsets that break the contract give unspecified values but every access
- * stays inside x, codes and scales.
+ * stays inside x, codes and scales. rounding: MX_ROUND_RNE (MX_ROUND_QUEST: MX_ERR_UNSUPPORTED).
  */
 mx_status mx_quantize_grouped(const void* x, const int64_t* row_offsets, int E, int64_t M_total,
                               int64_t K, int fmt, int group, int layout, int rounding,

@@ -19,7 +19,8 @@ E2M1 = MXFP4 = 1
 E4M3 = MXFP8 = 2
 LINEAR = 0
 SWIZZLED = 1
-RNE = 0
+RNE = 0    # abs-max block scale
+QUEST = 1  # Quest-like block scale (clip point alpha * RMS), MXFP4 only, not grouped
 GROUP = 32
 ROT_DENSE = 0     # any H: tensor-core product
 ROT_HADAMARD = 1  # H = H[0][0] * Sylvester (stated by the caller, checked on the device)

@@ -22,13 +22,20 @@ bool valid_rot_kind(int k) { return k == MX_ROT_DENSE || k == MX_ROT_HADAMARD; }
 // those calls run there (which takes any H).
 bool use_fwht(int rot_kind, int g) { return rot_kind == MX_ROT_HADAMARD && g <= 64; }
 
+// Kernel format id of an MX call: the Quest-like scale is its own instantiation of the kernels.
+int kernel_fmt(int fmt, int rounding) {
+  return rounding == MX_ROUND_QUEST ? mxq::kFmtE2M1Quest : fmt;
+}
+
 // Checks shared by every call on an [M, K] bf16 input. Returns MX_OK to go on; *empty is set
 // when there is nothing to compute.
 mx_status check_common(int64_t M, int64_t K, int fmt, int group, int rounding, bool* empty) {
   if (M < 0 || K < 0) return MX_ERR_SHAPE;
   if (group != 32) return MX_ERR_UNSUPPORTED;
   if (!valid_fmt(fmt)) return MX_ERR_UNSUPPORTED;
-  if (rounding != MX_ROUND_RNE) return MX_ERR_UNSUPPORTED;
+  if (rounding != MX_ROUND_RNE && !(rounding == MX_ROUND_QUEST && fmt == MX_FMT_E2M1)) {
+    return MX_ERR_UNSUPPORTED;
+  }
   if (K % 32 != 0) return MX_ERR_SHAPE;
   // element indices are formed in int64: keep M * K far from overflow
   if (K > 0 && M > (int64_t(1) << 40) / K) return MX_ERR_SHAPE;
@@ -122,7 +129,8 @@ mx_status mx_quantize(const void* x, int64_t M, int64_t K, int fmt, int group, i
   a.scales = static_cast<uint8_t*>(scales);
   a.scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : ceil_div(K, mxq::kTileCols) * 4;
   a.scale_rows = layout == MX_SCALES_LINEAR ? M : ceil_div(M, mxq::kTileRows) * mxq::kTileRows;
-  return from_cuda(mxq::launch_stream(fmt, false, layout == MX_SCALES_SWIZZLED, false, a,
+  return from_cuda(mxq::launch_stream(kernel_fmt(fmt, rounding), false, layout == MX_SCALES_SWIZZLED,
+                                      false, a,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -143,13 +151,15 @@ mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int ro
     if (use_fwht(rot_kind, g)) {
       mxq::StreamArgs a = stream_args(x, M, K, y);
       a.H = H;
-      return from_cuda(mxq::launch_hadamard(fmt, mxq::kRotQdq, false, g, a,
+      return from_cuda(mxq::launch_hadamard(kernel_fmt(fmt, rounding), mxq::kRotQdq, false, g, a,
                                             static_cast<cudaStream_t>(stream)));
     }
-    return from_cuda(mxq::launch_rotate(fmt, mxq::kRotQdq, false, g, rot_args(x, M, K, H, y),
+    return from_cuda(mxq::launch_rotate(kernel_fmt(fmt, rounding), mxq::kRotQdq, false, g,
+                                        rot_args(x, M, K, H, y),
                                         static_cast<cudaStream_t>(stream)));
   }
-  return from_cuda(mxq::launch_stream(fmt, true, false, false, stream_args(x, M, K, y),
+  return from_cuda(mxq::launch_stream(kernel_fmt(fmt, rounding), true, false, false,
+                                      stream_args(x, M, K, y),
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -193,13 +203,15 @@ mx_status mx_rotate_quantize(const void* x, int64_t M, int64_t K, const void* H,
     a.scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : ceil_div(K, mxq::kTileCols) * 4;
     a.scale_rows = layout == MX_SCALES_LINEAR ? M : ceil_div(M, mxq::kTileRows) * mxq::kTileRows;
     a.H = H;
-    return from_cuda(mxq::launch_hadamard(fmt, mxq::kRotCodes, layout == MX_SCALES_SWIZZLED, g, a,
+    return from_cuda(mxq::launch_hadamard(kernel_fmt(fmt, rounding), mxq::kRotCodes,
+                                          layout == MX_SCALES_SWIZZLED, g, a,
                                           static_cast<cudaStream_t>(stream)));
   }
   mxq::RotArgs a = rot_args(x, M, K, H, codes);
   a.scales = static_cast<uint8_t*>(scales);
   a.scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : a.col_tiles * 4;
-  return from_cuda(mxq::launch_rotate(fmt, mxq::kRotCodes, layout == MX_SCALES_SWIZZLED, g, a,
+  return from_cuda(mxq::launch_rotate(kernel_fmt(fmt, rounding), mxq::kRotCodes,
+                                      layout == MX_SCALES_SWIZZLED, g, a,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -209,6 +221,7 @@ mx_status mx_quantize_grouped(const void* x, const int64_t* row_offsets, int E, 
   bool empty = false;
   mx_status st = check_common(M_total, K, fmt, group, rounding, &empty);
   if (st != MX_OK) return st;
+  if (rounding != MX_ROUND_RNE) return MX_ERR_UNSUPPORTED;  // no grouped Quest-like scale
   if (!valid_layout(layout)) return MX_ERR_UNSUPPORTED;
   if (E < 1 || E > 1024) return MX_ERR_SHAPE;
   int64_t srows = 0, scols = 0;

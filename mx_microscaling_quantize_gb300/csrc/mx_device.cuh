@@ -19,6 +19,13 @@ namespace mxq {
 constexpr int kFmtE2M1 = 1;
 constexpr int kFmtE4M3 = 2;
 constexpr int kFmtNVFP4 = 3;  // E2M1 elements, 16-element blocks, E4M3 scales, fp32 global scale
+constexpr int kFmtE2M1Quest = 4;  // MXFP4 with the Quest-like scale (quest_byte_from_sum)
+
+// MX formats with E2M1 elements (4-bit codes, two per byte) and E8M0 block scales.
+template <int FMT>
+__host__ __device__ constexpr bool mx_e2m1() {
+  return FMT == kFmtE2M1 || FMT == kFmtE2M1Quest;
+}
 
 template <int FMT>
 struct FormatTraits;
@@ -34,6 +41,10 @@ template <>
 struct FormatTraits<kFmtNVFP4> {  // element format E2M1; the block scale is not a power of two
   static constexpr uint32_t emax = 2;
 };
+template <>
+struct FormatTraits<kFmtE2M1Quest> {
+  static constexpr uint32_t emax = 2;
+};
 
 // ------------------------------------------------------------------------------------------
 // scales
@@ -45,10 +56,56 @@ __device__ __forceinline__ uint32_t scale_byte_from_amax_bits(uint32_t amax_f32_
   return E == 255u ? 255u : (E > emax ? E - emax : 0u);
 }
 
-// 2^-(byte - 127) as fp32 (exact, normal for byte <= 253).
+// 2^-(byte - 127) as fp32, exact: normal for byte <= 253, the subnormal 2^-127 for 254 (reached
+// only by the Quest-like scale; multiplying by it is exact wherever the product is normal). 255
+// (NaN blocks, whose outputs are replaced) gives 2^-127 too.
 __device__ __forceinline__ float inv_scale_of(uint32_t byte) {
-  const uint32_t b = byte > 253u ? 253u : byte;
-  return __uint_as_float((254u - b) << 23);
+  return byte >= 254u ? __uint_as_float(0x00400000u) : __uint_as_float((254u - byte) << 23);
+}
+
+// Quest-like block scale (QuTLASS page, feature list: "Quartet (i.e., Quest-like)"; the pages
+// print no rule, so the reading is the MX rule with the block's clip point c in place of its
+// abs-max): c = alpha * sqrt(sum v_i^2 / 32), alpha = 2.922475 the clip ratio minimising the
+// E2M1 grid's mean squared error on a standard normal variable; byte = floor(log2 c) - 2 + 127
+// clamped to [0, 254]; an all-zero block gives 0 and a block with a NaN or an infinity 0xFF.
+// Every kernel first adds the plain squares of the block's values with fp32 FMAs in one fixed
+// order (sq_sum); when that sum lies in [2^-80, 2^100] it is accurate to a few units in the last
+// place (no overflow, and squares below 2^-126 are negligible against it) and decides the byte
+// with e = 127. Otherwise (a NaN or an infinity, an overflow, a tiny block) the squares are
+// summed again after an exact scaling by quest_prescale(E), E the abs-max's exponent field,
+// which neither overflows nor loses bits for any finite input. The decision needs no square
+// root: floor(log2 c) = (e - 127) + floor(floor(log2 p) / 2) for p = sum * alpha^2 / 32, the sum
+// taken over the values times 2^(127 - e).
+constexpr float kQuestBeta = (float)(2.922475 * 2.922475 / 32.0);  // alpha^2 / 32
+
+// 2^(127 - e), e = E clamped to [1, 253] (normal): the block's largest scaled value lies in [1, 4)
+// (below 1 only for a subnormal abs-max), so the scaled squares lie in [2^-46, 16).
+__device__ __forceinline__ float quest_prescale(uint32_t E) {
+  const uint32_t e = E < 1u ? 1u : (E > 253u ? 253u : E);
+  return __uint_as_float((254u - e) << 23);
+}
+
+// The range in which the plain sum of squares decides the byte: [2^-80, 2^100] (NaN excluded).
+__device__ __forceinline__ bool quest_sum_in_range(float sum_sq) {
+  return __float_as_uint(sum_sq) - 0x17800000u <= 0x71800000u - 0x17800000u;
+}
+
+__device__ __forceinline__ uint32_t quest_byte_from_sum(float sum_scaled_sq, uint32_t E) {
+  if (E == 255u) return 255u;
+  if (sum_scaled_sq == 0.0f) return 0u;
+  const int e = E < 1u ? 1 : (E > 253u ? 253 : (int)E);
+  const float p = sum_scaled_sq * kQuestBeta;  // normal: in [2^-48, 2^8)
+  const int lp = (int)(__float_as_uint(p) >> 23) - 127;  // floor(log2 p)
+  const int b = e - 2 + (lp >> 1);                        // arithmetic shift: floor(lp / 2)
+  return b < 0 ? 0u : (b > 254 ? 254u : (uint32_t)b);
+}
+
+// (lo, hi) <- (lo, hi) + (a, b)^2, one packed fp32 FMA per pair
+__device__ __forceinline__ void fma_sq2(float& lo, float& hi, float a, float b) {
+  asm("{\n\t.reg .b64 p, q;\n\tmov.b64 p, {%2, %3};\n\tmov.b64 q, {%0, %1};\n\t"
+      "fma.rn.f32x2 q, p, p, q;\n\tmov.b64 {%0, %1}, q;\n\t}"
+      : "+f"(lo), "+f"(hi)
+      : "f"(a), "f"(b));
 }
 
 // 2^(byte - 127) as fp32 (byte 0 -> 2^-127, an fp32 subnormal).
@@ -108,6 +165,44 @@ __device__ __forceinline__ uint32_t absmax_f32x32(const float* y) {
   const float p0 = absmax3(m[0], m[1], m[2]), p1 = absmax3(m[3], m[4], m[5]);
   const float p2 = absmax3(m[6], m[7], m[8]), p3 = absmax3(m[9], m[10], m[10]);
   return __float_as_uint(absmax3(absmax3(p0, p1, p2), p3, p3)) & 0x7FFFFFFFu;
+}
+
+// Sum of the squares of n fp32 values (n % 4 == 0): four interleaved chains (value i goes to
+// chain i % 4), then (c0 + c1) + (c2 + c3). Every kernel adds a 32-value block in this order.
+template <int N>
+__device__ __forceinline__ float sq_sum(const float* y) {
+  float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < N; i += 4) {
+    fma_sq2(s0, s1, y[i], y[i + 1]);
+    fma_sq2(s2, s3, y[i + 2], y[i + 3]);
+  }
+  return (s0 + s1) + (s2 + s3);
+}
+
+// The same sum with every value scaled by m first (exact: m is a power of two).
+template <int N>
+__device__ __forceinline__ float scaled_sq_sum(const float* y, float m) {
+  float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < N; i += 4) {
+    float a = y[i], b = y[i + 1], c = y[i + 2], d = y[i + 3];
+    mul2(a, b, m);
+    mul2(c, d, m);
+    fma_sq2(s0, s1, a, b);
+    fma_sq2(s2, s3, c, d);
+  }
+  return (s0 + s1) + (s2 + s3);
+}
+
+// Quest-like scale byte of one block of 32 fp32 values, given their plain sum of squares.
+__device__ __forceinline__ uint32_t quest_byte_f32x32(const float* y, float sum_sq) {
+  if (quest_sum_in_range(sum_sq)) return quest_byte_from_sum(sum_sq, 127u);
+  const uint32_t E = absmax_f32x32(y) >> 23;
+  return quest_byte_from_sum(scaled_sq_sum<32>(y, quest_prescale(E)), E);
+}
+__device__ __forceinline__ uint32_t quest_byte_f32x32(const float* y) {
+  return quest_byte_f32x32(y, sq_sum<32>(y));
 }
 
 // ------------------------------------------------------------------------------------------
@@ -175,7 +270,7 @@ __device__ __forceinline__ uint32_t qdq2_e4m3(float tlo, float thi, float sc) {
 
 template <int FMT>
 __device__ __forceinline__ uint32_t qdq2(float tlo, float thi, float sc) {
-  return FMT == kFmtE2M1 ? qdq2_e2m1(tlo, thi, sc) : qdq2_e4m3(tlo, thi, sc);
+  return mx_e2m1<FMT>() ? qdq2_e2m1(tlo, thi, sc) : qdq2_e4m3(tlo, thi, sc);
 }
 
 // 16-byte bf16 vector -> 8 fp32 values times `inv` (= 2^-s)
@@ -340,40 +435,6 @@ __device__ __forceinline__ NvScales nv_scales_tab(uint32_t amax0, uint32_t amax1
 // ------------------------------------------------------------------------------------------
 // One thread's 32 fp32 values (rotated values, lower K index first) -> output words.
 // ------------------------------------------------------------------------------------------
-// MX: one 32-element block. Writes 16 words of bf16 QDQ output or the block's codes (E2M1: 4
-// words, E4M3: 8) into out; returns the E8M0 byte. A block holding a NaN or an infinity gets
-// byte 0xFF and the fill outputs (QDQ 0x7FC0, E2M1 codes 0, E4M3 codes 0x7F). Every lane of
-// the warp must call it (the NaN check is a warp vote).
-template <int FMT, bool QDQ>
-__device__ __forceinline__ uint32_t mx_block_f32(float* y, uint32_t* out) {
-  const uint32_t byte = scale_byte_from_amax_bits<FMT>(absmax_f32x32(y));
-  const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);
-  const float inv = inv_scale_of(byte);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) mul2(y[2 * i], y[2 * i + 1], inv);  // y <- y / 2^s
-  if (QDQ) {
-    const float sc = scale_of(byte);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) out[i] = qdq2<FMT>(y[2 * i], y[2 * i + 1], sc);
-  } else if (FMT == kFmtE2M1) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) out[i] = codes8_e2m1(y + 8 * i);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint2 c = codes8_e4m3(y + 8 * i);
-      out[2 * i] = c.x;
-      out[2 * i + 1] = c.y;
-    }
-  }
-  if (special && byte == 255u) {
-    const uint32_t fill = QDQ ? kBf16NaNx2 : (FMT == kFmtE2M1 ? 0u : kE4M3NaNx4);
-#pragma unroll
-    for (int i = 0; i < (QDQ ? 16 : (FMT == kFmtE2M1 ? 4 : 8)); ++i) out[i] = fill;
-  }
-  return byte;
-}
-
 // NVFP4: two 16-element blocks under the scales n (from nv_scales or nv_scales_tab). Writes 16
 // words of bf16 QDQ output or 4 words of E2M1 codes; a NaN/Inf block gets 0x7FC0 / codes 0.
 // Every lane of the warp must call it.

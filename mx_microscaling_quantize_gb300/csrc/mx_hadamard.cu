@@ -154,15 +154,33 @@ __device__ __forceinline__ void dense_rotate(float* v, const uint16_t* H, int la
 // and symmetric, so this is max_j |fl(c s_j)|), and the values are scaled by q = c * 2^-s in one
 // multiplication: fl(s_j q) = fl(c s_j) * 2^-s exactly while q is a normal number (the scaling
 // by a power of two is exact); otherwise the two multiplications are done in turn.
+// The Quest-like scale (FMT kFmtE2M1Quest) takes the sum of the squares of y as c^2 times that of
+// s (one rounding more than summing the squares of y itself); where that product leaves the
+// plain-sum range, y = c * s is formed and the scaled sum of quest_byte_f32x32 taken instead.
 template <int FMT, bool QDQ>
 __device__ __forceinline__ uint32_t mx_hadamard_block(float* v, float c, uint32_t* out) {
-  const float amax_s = __uint_as_float(absmax_f32x32(v));
-  const float amax = __fmul_rn(fabsf(c), amax_s);
-  const uint32_t byte = scale_byte_from_amax_bits<FMT>(__float_as_uint(amax) & 0x7FFFFFFFu);
+  uint32_t byte;
+  bool c_applied = false;  // v already holds y = c * s
+  if constexpr (FMT == kFmtE2M1Quest) {
+    const float sum = __fmul_rn(__fmul_rn(c, c), sq_sum<32>(v));
+    if (quest_sum_in_range(sum)) {
+      byte = quest_byte_from_sum(sum, 127u);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mul2(v[2 * i], v[2 * i + 1], c);
+      c_applied = true;
+      const uint32_t E = absmax_f32x32(v) >> 23;
+      byte = quest_byte_from_sum(scaled_sq_sum<32>(v, quest_prescale(E)), E);
+    }
+  } else {
+    const float amax_s = __uint_as_float(absmax_f32x32(v));
+    const float amax = __fmul_rn(fabsf(c), amax_s);
+    byte = scale_byte_from_amax_bits<FMT>(__float_as_uint(amax) & 0x7FFFFFFFu);
+  }
   const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);
   const float inv = inv_scale_of(byte);
-  const float q = __fmul_rn(c, inv);
-  if (fabsf(q) >= 1.17549435e-38f || c == 0.0f) {  // q normal (or zero): one exact step
+  const float q = c_applied ? inv : __fmul_rn(c, inv);
+  if (c_applied || fabsf(q) >= 1.17549435e-38f || c == 0.0f) {  // one exact step
 #pragma unroll
     for (int i = 0; i < 16; ++i) mul2(v[2 * i], v[2 * i + 1], q);
   } else {
@@ -176,7 +194,7 @@ __device__ __forceinline__ uint32_t mx_hadamard_block(float* v, float c, uint32_
     const float sc = scale_of(byte);
 #pragma unroll
     for (int i = 0; i < 16; ++i) out[i] = qdq2<FMT>(v[2 * i], v[2 * i + 1], sc);
-  } else if (FMT == kFmtE2M1) {
+  } else if (mx_e2m1<FMT>()) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) out[i] = codes8_e2m1(v + 8 * i);
   } else {
@@ -188,9 +206,9 @@ __device__ __forceinline__ uint32_t mx_hadamard_block(float* v, float c, uint32_
     }
   }
   if (special && byte == 255u) {
-    const uint32_t fill = QDQ ? kBf16NaNx2 : (FMT == kFmtE2M1 ? 0u : kE4M3NaNx4);
+    const uint32_t fill = QDQ ? kBf16NaNx2 : (mx_e2m1<FMT>() ? 0u : kE4M3NaNx4);
 #pragma unroll
-    for (int i = 0; i < (QDQ ? 16 : (FMT == kFmtE2M1 ? 4 : 8)); ++i) out[i] = fill;
+    for (int i = 0; i < (QDQ ? 16 : (mx_e2m1<FMT>() ? 4 : 8)); ++i) out[i] = fill;
   }
   return byte;
 }
@@ -364,6 +382,7 @@ cudaError_t launch_hadamard(int fmt, int out_kind, bool swizzled, int g, const S
                             cudaStream_t stream) {
   if (out_kind == kRotDebug) return launch_g<kFmtE2M1, kRotDebug, false>(g, a, stream);
   if (fmt == kFmtE2M1) return launch_fmt<kFmtE2M1>(out_kind, swizzled, g, a, stream);
+  if (fmt == kFmtE2M1Quest) return launch_fmt<kFmtE2M1Quest>(out_kind, swizzled, g, a, stream);
   if (fmt == kFmtNVFP4) return launch_fmt<kFmtNVFP4>(out_kind, swizzled, g, a, stream);
   return launch_fmt<kFmtE4M3>(out_kind, swizzled, g, a, stream);
 }

@@ -46,8 +46,8 @@ struct StreamArgs {
   const void* H;           // Hadamard-rotated calls only: bf16 [g, g] row-major
 };
 
-// fmt: 1 = E2M1, 2 = E4M3, 3 = NVFP4. qdq: write bf16 QDQ instead of codes +
-// scales.
+// fmt: 1 = E2M1, 2 = E4M3, 3 = NVFP4, 4 = E2M1 under the Quest-like scale (not grouped). qdq:
+// write bf16 QDQ instead of codes + scales.
 cudaError_t launch_stream(int fmt, bool qdq, bool swizzled, bool grouped, const StreamArgs& a,
                           cudaStream_t stream);
 

@@ -172,7 +172,8 @@ __device__ __forceinline__ uint32_t nv_block_outputs(float* y, uint32_t* out, fl
 
 template <int FMT, int OUT>
 __device__ __forceinline__ uint32_t block_outputs(float* y, uint32_t* out) {
-  const uint32_t byte = scale_byte_from_amax_bits<FMT>(absmax_f32x32(y));
+  const uint32_t byte = FMT == kFmtE2M1Quest ? quest_byte_f32x32(y)
+                                             : scale_byte_from_amax_bits<FMT>(absmax_f32x32(y));
   const bool special = __any_sync(0xFFFFFFFFu, byte == 255u);  // a NaN / Inf block in the warp
   const float inv = inv_scale_of(byte);
 #pragma unroll
@@ -181,7 +182,7 @@ __device__ __forceinline__ uint32_t block_outputs(float* y, uint32_t* out) {
     const float sc = scale_of(byte);
 #pragma unroll
     for (int i = 0; i < 16; ++i) out[i] = qdq2<FMT>(y[2 * i], y[2 * i + 1], sc);
-  } else if (FMT == kFmtE2M1) {
+  } else if (mx_e2m1<FMT>()) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) out[i] = codes8_e2m1(y + 8 * i);
   } else {
@@ -193,7 +194,7 @@ __device__ __forceinline__ uint32_t block_outputs(float* y, uint32_t* out) {
     }
   }
   if (special && byte == 255u) {
-    const uint32_t fill = OUT == kRotQdq ? kBf16NaNx2 : (FMT == kFmtE2M1 ? 0u : kE4M3NaNx4);
+    const uint32_t fill = OUT == kRotQdq ? kBf16NaNx2 : (mx_e2m1<FMT>() ? 0u : kE4M3NaNx4);
 #pragma unroll
     for (int i = 0; i < block_out_words<FMT, OUT>(); ++i) out[i] = fill;
   }
@@ -653,10 +654,26 @@ __global__ void __launch_bounds__(kSmallThreads)
     return;
   }
 
-  // block scale: abs-max over the 4 threads of a 32-element block (2 of a 16-element block)
+  // block scale: abs-max over the 4 threads of a 32-element block (2 of a 16-element block);
+  // the Quest-like scale adds the 4 threads' scaled sums of squares as well
   uint32_t amax = absmax_f32x8(acc);
   amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
   if (!kNv) amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  uint32_t quest_byte = 0;
+  if constexpr (FMT == kFmtE2M1Quest) {  // the plain sum first, the scaled one where needed
+    float sum = sq_sum<8>(acc);
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+    const bool plain = quest_sum_in_range(sum);
+    quest_byte = quest_byte_from_sum(sum, 127u);
+    if (__any_sync(0xFFFFFFFFu, !plain)) {  // every lane takes part in the shuffles
+      const uint32_t E = amax >> 23;
+      float scaled = scaled_sq_sum<8>(acc, quest_prescale(E));
+      scaled += __shfl_xor_sync(0xFFFFFFFFu, scaled, 1);
+      scaled += __shfl_xor_sync(0xFFFFFFFFu, scaled, 2);
+      if (!plain) quest_byte = quest_byte_from_sum(scaled, E);
+    }
+  }
   uint32_t byte;
   uint32_t o[4];
   if constexpr (kNv) {
@@ -673,7 +690,7 @@ __global__ void __launch_bounds__(kSmallThreads)
       o[0] = n.special[0] ? 0u : codes8_e2m1(acc);
     }
   } else {
-    byte = scale_byte_from_amax_bits<FMT>(amax);
+    byte = FMT == kFmtE2M1Quest ? quest_byte : scale_byte_from_amax_bits<FMT>(amax);
     const float inv = inv_scale_of(byte);
 #pragma unroll
     for (int i = 0; i < 4; ++i) mul2(acc[2 * i], acc[2 * i + 1], inv);
@@ -685,7 +702,7 @@ __global__ void __launch_bounds__(kSmallThreads)
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[i] = kBf16NaNx2;
       }
-    } else if (FMT == kFmtE2M1) {
+    } else if (mx_e2m1<FMT>()) {
       o[0] = byte == 255u ? 0u : codes8_e2m1(acc);
     } else {
       const uint2 c = codes8_e4m3(acc);
@@ -834,6 +851,7 @@ cudaError_t launch_rotate(int fmt, int out_kind, bool swizzled, int g, const Rot
                           cudaStream_t stream) {
   if (out_kind == kRotDebug) return launch_g<kFmtE2M1, kRotDebug, false>(g, a, stream);
   if (fmt == kFmtE2M1) return launch_fmt<kFmtE2M1>(out_kind, swizzled, g, a, stream);
+  if (fmt == kFmtE2M1Quest) return launch_fmt<kFmtE2M1Quest>(out_kind, swizzled, g, a, stream);
   if (fmt == kFmtNVFP4) return launch_fmt<kFmtNVFP4>(out_kind, swizzled, g, a, stream);
   return launch_fmt<kFmtE4M3>(out_kind, swizzled, g, a, stream);
 }

@@ -47,11 +47,36 @@ __device__ __forceinline__ uint32_t absmax_block(const uint32_t* w) {
   return max(m[0] & 0x7FFFu, (m[0] >> 16) & 0x7FFFu);
 }
 
+// Sum of the squares of one block held in w[16] (bf16 pairs), each value scaled by m, in the
+// order of sq_sum<32> (element i of the block to chain i % 4); the values are widened on the fly.
+__device__ __forceinline__ float sq_sum_bf16x32(const uint32_t* w, float m) {
+  float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    float a = bf16_lo(w[i]), b = bf16_hi(w[i]), c = bf16_lo(w[i + 1]), d = bf16_hi(w[i + 1]);
+    mul2(a, b, m);
+    mul2(c, d, m);
+    fma_sq2(s0, s1, a, b);
+    fma_sq2(s2, s3, c, d);
+  }
+  return (s0 + s1) + (s2 + s3);
+}
+
+// Quest-like scale byte of one block held in w[16], with the arithmetic and the order of
+// quest_byte_f32x32 on the widened values (the plain sum is the scaled one with m = 1).
+__device__ __forceinline__ uint32_t quest_byte_bf16x32(const uint32_t* w) {
+  const float s = sq_sum_bf16x32(w, 1.0f);
+  if (quest_sum_in_range(s)) return quest_byte_from_sum(s, 127u);
+  const uint32_t E = (absmax_block(w) << 16) >> 23;
+  return quest_byte_from_sum(sq_sum_bf16x32(w, quest_prescale(E)), E);
+}
+
 // Quantize (or QDQ) one block held in w[16]; writes codes / bf16 through `out` when `ok`.
 // Returns the scale byte.
 template <int FMT, bool QDQ>
 __device__ __forceinline__ uint32_t block_kernel(const uint32_t* w, bool ok, void* out) {
-  const uint32_t byte = scale_byte_from_amax_bits<FMT>(absmax_block(w) << 16);
+  const uint32_t byte = FMT == kFmtE2M1Quest ? quest_byte_bf16x32(w)
+                                             : scale_byte_from_amax_bits<FMT>(absmax_block(w) << 16);
   const float inv = inv_scale_of(byte);
   const bool special = __any_sync(__activemask(), byte == 255u);  // a NaN / Inf block nearby
   if (QDQ) {
@@ -82,7 +107,7 @@ __device__ __forceinline__ uint32_t block_kernel(const uint32_t* w, bool ok, voi
         t[2 * i + 1] = bf16_hi(w[4 * q + i]);
         mul2(t[2 * i], t[2 * i + 1], inv);
       }
-      if (FMT == kFmtE2M1) {
+      if (mx_e2m1<FMT>()) {
         c[q] = codes8_e2m1(t);
       } else {
         const uint2 p = codes8_e4m3(t);
@@ -92,10 +117,10 @@ __device__ __forceinline__ uint32_t block_kernel(const uint32_t* w, bool ok, voi
     }
     if (special && byte == 255u) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) c[i] = FMT == kFmtE2M1 ? 0u : kE4M3NaNx4;
+      for (int i = 0; i < 8; ++i) c[i] = mx_e2m1<FMT>() ? 0u : kE4M3NaNx4;
     }
     if (ok) {
-      if (FMT == kFmtE2M1) {
+      if (mx_e2m1<FMT>()) {
         __stcs(static_cast<uint4*>(out), make_uint4(c[0], c[1], c[2], c[3]));
       } else {
         store32B(out, c);
@@ -244,10 +269,11 @@ __device__ __forceinline__ void zero_grouped_pads(const StreamArgs& a, const int
 // kernels are given room for more registers (66, 3 CTAs per SM), which measured 2-3% faster
 // than the 50-register, 4-CTA build (x[8192,8192] 44.9 -> 44.0 us, x[4096,8192] 22.8 -> 22.1 us
 // back to back); quantize kernels keep <= 64 registers and 4 CTAs per SM; grouped NVFP4 needs
-// 78 and 3 CTAs (forcing 64 spills and measured 14% slower).
+// 78 and 3 CTAs (forcing 64 spills and measured 14% slower), and so does the Quest-like
+// quantize (its sum of squares and scaled fallback spilled 40-132 bytes at 64).
 template <int FMT, bool QDQ, bool GROUPED>
 __host__ __device__ constexpr int stream_min_ctas() {
-  return QDQ ? 1 : ((GROUPED && FMT == kFmtNVFP4) ? 3 : 4);
+  return QDQ ? 1 : (((GROUPED && FMT == kFmtNVFP4) || FMT == kFmtE2M1Quest) ? 3 : 4);
 }
 
 // First blocks of each warp prefetched into L2 before pdl_wait: one 2 KiB span (the warp's
@@ -465,7 +491,11 @@ template <int FMT>
 cudaError_t launch_fmt(bool qdq, bool swz, bool grouped, const StreamArgs& a, cudaStream_t st) {
   if (qdq) return launch_t<FMT, true, false, false>(a, st);
   if (grouped) {
-    return swz ? launch_t<FMT, false, true, true>(a, st) : launch_t<FMT, false, false, true>(a, st);
+    if constexpr (FMT == kFmtE2M1Quest) {
+      return cudaErrorInvalidValue;  // no grouped variant of the Quest-like scale
+    } else {
+      return swz ? launch_t<FMT, false, true, true>(a, st) : launch_t<FMT, false, false, true>(a, st);
+    }
   }
   return swz ? launch_t<FMT, false, true, false>(a, st) : launch_t<FMT, false, false, false>(a, st);
 }
@@ -475,6 +505,7 @@ cudaError_t launch_fmt(bool qdq, bool swz, bool grouped, const StreamArgs& a, cu
 cudaError_t launch_stream(int fmt, bool qdq, bool swizzled, bool grouped, const StreamArgs& a,
                           cudaStream_t stream) {
   if (fmt == kFmtE2M1) return launch_fmt<kFmtE2M1>(qdq, swizzled, grouped, a, stream);
+  if (fmt == kFmtE2M1Quest) return launch_fmt<kFmtE2M1Quest>(qdq, swizzled, grouped, a, stream);
   if (fmt == kFmtNVFP4) return launch_fmt<kFmtNVFP4>(qdq, swizzled, grouped, a, stream);
   return launch_fmt<kFmtE4M3>(qdq, swizzled, grouped, a, stream);
 }

@@ -232,9 +232,13 @@ def _allowed_bytes(fmt, yb, tb, ref_byte):
     return allowed
 
 
-def _block_ok(fmt, vals, yb, tb, gpu_codes, gpu_byte, ref_byte) -> tuple[bool, int]:
-    """Whether GPU codes + byte of one block satisfy the rules; returns (ok, #exempt codes)."""
-    if gpu_byte not in _allowed_bytes(fmt, yb, tb, ref_byte):
+def _block_ok(fmt, vals, yb, tb, gpu_codes, gpu_byte, ref_byte,
+              allowed=None) -> tuple[bool, int]:
+    """Whether GPU codes + byte of one block satisfy the rules; returns (ok, #exempt codes).
+    allowed: the scale bytes the GPU may give (default: the abs-max rule's)."""
+    if allowed is None:
+        allowed = _allowed_bytes(fmt, yb, tb, ref_byte)
+    if gpu_byte not in allowed:
         return False, 0
     byte, rc = O.quantize_block(fmt, yb, forced_byte=gpu_byte)
     diff = np.nonzero(rc != gpu_codes)[0]
@@ -441,3 +445,114 @@ def check_rotated_nvfp4(x_bits, H_bits, gs, codes_gpu, scales_gpu_linear):
 
 def check_rotated_nvfp4_qdq(x_bits, H_bits, gs, out_gpu_bits):
     return check_rotated_multi(x_bits, H_bits, nvfp4_qdq={gs: out_gpu_bits})[("nvfp4_qdq", gs)]
+
+
+# ---------------------------------------------------------------------------------------------
+# Quest-like MXFP4 scale: the same element rules; the scale decision is a threshold on the clip
+# point c = alpha * RMS instead of the abs-max
+# ---------------------------------------------------------------------------------------------
+# The kernel sums the squares in fp32 (after an exact power-of-two scaling) and multiplies by
+# alpha^2 / 32 rounded to fp32: about 12 roundings of 2^-24 each on c^2, well inside 2^-20 on c.
+QUEST_SUM_REL = 2.0 ** -20
+
+
+def quest_clip(yb) -> float:
+    yb = np.asarray(yb, dtype=np.float64)
+    return O.quest_alpha() * float(np.sqrt(np.dot(yb, yb) / yb.size))
+
+
+def quest_allowed_bytes(yb, tb, ref_byte):
+    """The oracle's byte, and one step off only where c lies within its tolerance of the power
+    of two that the step crosses (c in [2^k, 2^(k+1)) gives the oracle's byte). The tolerance:
+    alpha / sqrt(32) times the 2-norm of the values' tolerances (c is that Lipschitz in the
+    values) plus the kernel's relative error on the sum."""
+    c = quest_clip(yb)
+    allowed = {ref_byte}
+    if c > 0:
+        k = np.floor(np.log2(c))
+        tc = O.quest_alpha() / np.sqrt(yb.size) * float(np.linalg.norm(tb)) + QUEST_SUM_REL * c
+        if c - 2.0 ** k <= tc:
+            allowed.add(ref_byte - 1)
+        if 2.0 ** (k + 1) - c <= tc:
+            allowed.add(ref_byte + 1)
+    return allowed
+
+
+def _quest_codes_chunk(vals, y, tol, gc_packed, sg, r0):
+    n, K = y.shape
+    rc, rs = O.quest_quantize_values(y, O.LINEAR)
+    gc = unpack_codes(gc_packed, O.E2M1)
+    rce = unpack_codes(rc, O.E2M1)
+    bad = np.nonzero((rs != sg) | (gc != rce).reshape(n, K // 32, 32).any(axis=2))
+    exempt_codes = flips = 0
+    for r, j in zip(*bad):
+        sl = slice(32 * j, 32 * j + 32)
+        yb, tb = y[r, sl], tol[r, sl]
+        ok, k = _block_ok(O.E2M1, vals, yb, tb, gc[r, sl], int(sg[r, j]), int(rs[r, j]),
+                          quest_allowed_bytes(yb, tb, int(rs[r, j])))
+        assert ok, (f"Quest block (row {r0 + r}, block {j}) outside tolerance: gpu byte "
+                    f"{sg[r, j]} ref byte {rs[r, j]}")
+        exempt_codes += k
+        flips += int(sg[r, j] != rs[r, j])
+    return np.array([n * K // 32, len(bad[0]), exempt_codes, flips])
+
+
+def _quest_qdq_chunk(vals, y, tol, og, r0):
+    n, K = y.shape
+    ref = O.quest_qdq_values(y)
+    bad = np.nonzero((ref != og).reshape(n, K // 32, 32).any(axis=2))
+    for r, j in zip(*bad):
+        sl = slice(32 * j, 32 * j + 32)
+        yb, tb, ob = y[r, sl], tol[r, sl], og[r, sl]
+        ref_byte = O.quest_scale_byte(yb)
+        allowed = quest_allowed_bytes(yb, tb, ref_byte)
+        ok = False
+        for b in sorted(allowed):
+            _, rc = O.quantize_block(O.E2M1, yb, forced_byte=b)
+            table = dequant_table(O.E2M1, b)
+            codes = rc.copy()
+            good = True
+            for i in np.nonzero(table[rc] != ob)[0]:
+                cands = np.nonzero(table == ob[i])[0]
+                if not len(cands):
+                    good = False
+                    break
+                codes[i] = cands[0]
+            if good and _block_ok(O.E2M1, vals, yb, tb, codes, b, ref_byte, allowed)[0]:
+                ok = True
+                break
+        assert ok, f"Quest QDQ block (row {r0 + r}, block {j}) outside tolerance"
+    return np.array([n * K // 32, len(bad[0])])
+
+
+def check_quest(x_bits, H_bits=None, codes=None, qdq=None):
+    """Quest-like MXFP4 outputs of x (rotated by H when given) against the oracle over every
+    row: codes = (packed codes, linear scales), qdq = bf16 bits. Without H the values are the
+    exact bf16 inputs (tolerance 0: only the kernel's fp32 sum can move a scale, and only next
+    to a power of two). Returns {"codes": stats, "qdq": stats}."""
+    x = np.ascontiguousarray(x_bits)
+    M, K = x.shape
+    vals = grid_values(O.E2M1)
+
+    def job(r0, r1):
+        if H_bits is None:
+            y = O.bf16_bits_to_double(x[r0:r1])
+            tol = np.zeros_like(y)
+        else:
+            y = O.rotate(x[r0:r1], H_bits)
+            tol = rotation_tolerance(y, H_bits.shape[0])
+        out = {}
+        if codes is not None:
+            out["codes"] = _quest_codes_chunk(vals, y, tol, codes[0][r0:r1], codes[1][r0:r1], r0)
+        if qdq is not None:
+            out["qdq"] = _quest_qdq_chunk(vals, y, tol, qdq[r0:r1], r0)
+        return out
+
+    parts = map_row_chunks(job, M, K, target_elems=1 << 20)
+    stats = {}
+    for k in parts[0]:
+        v = sum(p[k] for p in parts)
+        stats[k] = {"blocks": int(v[0]), "exempt_blocks": int(v[1])}
+        if k == "codes":
+            stats[k].update(exempt_codes=int(v[2]), scale_flips=int(v[3]))
+    return stats

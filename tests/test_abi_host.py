@@ -50,6 +50,7 @@ def test_macros_match_binding():
     assert int(macros["MX_SCALES_LINEAR"]) == mxq.LINEAR
     assert int(macros["MX_SCALES_SWIZZLED"]) == mxq.SWIZZLED
     assert int(macros["MX_ROUND_RNE"]) == mxq.RNE
+    assert int(macros["MX_ROUND_QUEST"]) == mxq.QUEST
     assert int(macros["MX_ROT_DENSE"]) == mxq.ROT_DENSE
     assert int(macros["MX_ROT_HADAMARD"]) == mxq.ROT_HADAMARD
 
@@ -98,7 +99,10 @@ def test_quantize_validation(L):
     assert q(P, 4, 64, 3, 32, 0, 0, P, P, None) == UNSUP
     assert q(P, 4, 64, 1, 16, 0, 0, P, P, None) == UNSUP
     assert q(P, 4, 64, 1, 32, 2, 0, P, P, None) == UNSUP
-    assert q(P, 4, 64, 1, 32, 0, 1, P, P, None) == UNSUP
+    assert q(P, 4, 64, 1, 32, 0, 2, P, P, None) == UNSUP  # unknown rounding
+    assert q(P, 4, 64, 2, 32, 0, 1, P, P, None) == UNSUP  # Quest-like scale: MXFP4 only
+    assert q(P, 4, 48, 1, 32, 0, 1, P, P, None) == SHAPE  # the other checks still apply
+    assert q(None, 4, 64, 1, 32, 0, 1, P, P, None) == NULL
     assert q(None, 4, 64, 1, 32, 0, 0, P, P, None) == NULL
     assert q(P, 4, 64, 1, 32, 0, 0, None, P, None) == NULL
     assert q(P, 4, 64, 1, 32, 0, 0, P, None, None) == NULL
@@ -122,6 +126,9 @@ def test_qdq_and_rotation_validation(L):
         assert q(P, 4, 64, 1, 32, 0, P + 1, 32, rk, P, None) == ALIGN
         assert q(P, 4, 64, 1, 32, 0, P + 8, 32, rk, P, None) == ALIGN
     assert q(P, 4, 64, 1, 32, 0, P, 32, 2, P, None) == UNSUP         # unknown rot_kind
+    assert q(P, 4, 64, 2, 32, 1, P, 32, 0, P, None) == UNSUP         # Quest-like: MXFP4 only
+    assert q(P, 4, 64, 2, 32, 1, None, 0, 0, P, None) == UNSUP
+    assert q(P, 4, 64, 1, 32, 3, None, 0, 0, P, None) == UNSUP       # unknown rounding
     assert q(P, 4, 64, 1, 32, 0, None, 0, 7, None, None) == NULL     # no H: rot_kind ignored
     assert q(P, 4, 64, 1, 32, 0, None, 0, 0, P + 2, None) == ALIGN
     assert q(P, 4, 64, 1, 32, 0, None, 0, 0, P + 16, None) == ALIGN
@@ -133,6 +140,8 @@ def test_qdq_and_rotation_validation(L):
         assert r(P, 4, 64, P, 32, rk, 1, 32, 1, 0, P, P + 8, None) == ALIGN
         assert r(None, 0, 64, None, 32, rk, 1, 32, 1, 0, None, None, None) == OK
     assert r(P, 4, 64, P, 32, -1, 1, 32, 1, 0, P, P, None) == UNSUP
+    assert r(P, 4, 64, P, 32, 0, 2, 32, 1, 1, P, P, None) == UNSUP  # Quest-like: MXFP4 only
+    assert r(P, 4, 64, P, 32, 0, 1, 32, 1, 1, P, P + 8, None) == ALIGN
     d = L.mx_rotate_debug  # (x, M, K, H, g, rot_kind, y, stream)
     assert d(P, 4, 64, P, 24, 0, P, None) == UNSUP
     assert d(P, 4, 64, P, 32, 3, P, None) == UNSUP
@@ -149,6 +158,7 @@ def test_grouped_validation(L):
     assert g(P, P, 4, 16, 64, 1, 32, 1, 0, P, P + 8, None) == ALIGN
     assert g(P, P, 4, 16, 48, 1, 32, 1, 0, P, P, None) == SHAPE
     assert g(None, None, 4, 0, 64, 1, 32, 1, 0, None, None, None) == OK
+    assert g(P, P, 4, 16, 64, 1, 32, 1, 1, P, P, None) == UNSUP  # no grouped Quest-like scale
 
 
 def test_dequantize_validation(L):

@@ -194,3 +194,56 @@ def test_chunked_checks_cover_every_row():
     q[96, 255] ^= 1
     with pytest.raises(AssertionError, match="rows"):
         T.assert_rows_equal(q, T.oracle_qdq_rows(x, O.E2M1))
+
+
+# ---------------------------------------------------------------------------------------------
+# Quest-like scale checker
+# ---------------------------------------------------------------------------------------------
+def _packed(codes):
+    return (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("rotated", [False, True])
+def test_quest_rules_accept_oracle_and_reject_planted_errors(rotated):
+    x = W.rotate_quant_activation(6, 256)
+    H = W.normalized_hadamard_bf16(32) if rotated else None
+    c, s = O.quest_quantize(x, O.LINEAR, H)
+    q = O.quest_qdq(x, H)
+    stats = T.check_quest(x, H, codes=(c, s), qdq=q)
+    assert stats["codes"]["exempt_blocks"] == 0 and stats["qdq"]["exempt_blocks"] == 0
+    assert stats["codes"]["blocks"] == 6 * 8
+    bad_s = s.copy()
+    bad_s[2, 5] += 1
+    with pytest.raises(AssertionError):
+        T.check_quest(x, H, codes=(c, bad_s))
+    bad_c = c.copy()
+    bad_c[4, 9] ^= 0x22  # two codes two grid steps off: never a midpoint exemption
+    with pytest.raises(AssertionError):
+        T.check_quest(x, H, codes=(bad_c, s))
+    bad_q = q.copy()
+    bad_q[1, 77] ^= 0x0080
+    with pytest.raises(AssertionError):
+        T.check_quest(x, H, qdq=bad_q)
+
+
+def test_quest_scale_flip_only_toward_the_nearby_power_of_two():
+    """A block with c = 3.99995 (1.2e-5 below 4): under a rotation (tolerance about 6e-5 of c
+    here) the byte may step up to 127 but never down to 125; without a rotation (exact inputs,
+    only the kernel's fp32 sum can move it) it must stay 126."""
+    v = np.full(32, 1.375)
+    v[0] = 1.15625
+    x = W.to_bf16_bits(v.reshape(1, 32))
+    assert abs(T.quest_clip(v) / 4 - 1) < 2e-5 and T.quest_clip(v) < 4
+    ref_byte, _ = O.quest_quantize_block(v)
+    assert ref_byte == 126
+    H = identity(32)
+    for b, ok_rot in ((127, True), (125, False)):
+        _, codes = O.quantize_block(O.E2M1, v, forced_byte=b)
+        got = (_packed(codes).reshape(1, 16), np.array([[b]], dtype=np.uint8))
+        if ok_rot:
+            assert T.check_quest(x, H, codes=got)["codes"]["scale_flips"] == 1
+        else:
+            with pytest.raises(AssertionError):
+                T.check_quest(x, H, codes=got)
+        with pytest.raises(AssertionError):
+            T.check_quest(x, None, codes=got)
