@@ -531,6 +531,15 @@ def extra_workloads(dev, peak):
     nb = 3 * x.numel() + used_rows * s.shape[1]
     measure("moe_quant_mxfp8[16384,2048]x128", nb, x.numel(), make, nb)
     del c, s
+    c, s = mxq.mx_quantize_grouped(x, offs, mxq.E4M3, mxq.LINEAR)
+
+    def make(k, x=x, c=c, s=s):
+        xk, ck, sk = copy_of(x, k), empty_of(c, k), empty_of(s, k)
+        return lambda: mxq.mx_quantize_grouped(xk, offs, mxq.E4M3, mxq.LINEAR, codes=ck,
+                                               scales=sk)
+    nb = 3 * x.numel() + s.numel()
+    measure("moe_quant_mxfp8_linear[16384,2048]x128", nb, x.numel(), make, nb)
+    del c, s
     gse = torch.stack([448.0 * 6.0 / x[int(off[e]):int(off[e + 1])].float().abs().max()
                        if off[e + 1] > off[e] else torch.ones((), device=dev)
                        for e in range(len(off) - 1)]).float().contiguous()

@@ -179,7 +179,8 @@ mx_status mx_grouped_scales_shape(int64_t M_total, int E, int64_t K, int group, 
  * Grouped (MoE expert) quantize. Rows [row_offsets[e], row_offsets[e+1]) of x belong to
  * expert e (row_offsets: DEVICE int64 [E+1], row_offsets[0] = 0, row_offsets[E] = M_total,
  * non-decreasing). Codes stay contiguous as for mx_quantize on the whole x. Linear scales are
- * [M_total, K/32]. Swizzled scales give each expert its own run of 128-row tiles: expert e's
+ * [M_total, K/32]: the call is then mx_quantize on the whole x and does not read row_offsets.
+ * Swizzled scales give each expert its own run of 128-row tiles: expert e's
  * rows start at padded row P_e = sum_{e' < e} ceil(n_e'/128) * 128; the buffer has
  * mx_grouped_scales_shape() rows and all of it is written (rows past the last expert: zero).
  * 1 <= E <= 1024. Offsets that break the contract give unspecified values but every access

@@ -236,9 +236,14 @@ mx_status mx_quantize_grouped(const void* x, const int64_t* row_offsets, int E, 
   a.scales = static_cast<uint8_t*>(scales);
   a.scale_cols = scols;
   a.scale_rows = srows;
-  a.offsets = row_offsets;
-  a.E = E;
-  return from_cuda(mxq::launch_stream(fmt, false, layout == MX_SCALES_SWIZZLED, true, a,
+  // Linear scales of a grouped call are [M_total, K/32] and the codes stay contiguous: exactly
+  // the plain quantize of the whole x, which needs no expert offsets.
+  const bool grouped = layout == MX_SCALES_SWIZZLED;
+  if (grouped) {
+    a.offsets = row_offsets;
+    a.E = E;
+  }
+  return from_cuda(mxq::launch_stream(fmt, false, layout == MX_SCALES_SWIZZLED, grouped, a,
                                       static_cast<cudaStream_t>(stream)));
 }
 

@@ -493,8 +493,10 @@ cudaError_t launch_fmt(bool qdq, bool swz, bool grouped, const StreamArgs& a, cu
   if (grouped) {
     if constexpr (FMT == kFmtE2M1Quest) {
       return cudaErrorInvalidValue;  // no grouped variant of the Quest-like scale
-    } else {
+    } else if constexpr (FMT == kFmtNVFP4) {
       return swz ? launch_t<FMT, false, true, true>(a, st) : launch_t<FMT, false, false, true>(a, st);
+    } else {  // MX grouped calls with linear scales run as plain calls (mx_api.cu)
+      return swz ? launch_t<FMT, false, true, true>(a, st) : cudaErrorInvalidValue;
     }
   }
   return swz ? launch_t<FMT, false, true, false>(a, st) : launch_t<FMT, false, false, false>(a, st);
