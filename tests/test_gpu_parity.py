@@ -517,12 +517,12 @@ def test_nvfp4_grouped_edge_counts(counts):
             np.testing.assert_array_equal(c, rc)
 
 
-def test_grouped_swizzled_on_both_sides_of_the_row_table_limit():
+def test_grouped_on_both_sides_of_the_row_table_limit():
     """MX grouped calls with swizzled scales run on the grid-stride kernel with a per-CTA table
     of its rows' padded-row shifts while the table fits (2048 entries), else on the
     contiguous-range kernel. K = 32 puts 258 rows in each CTA iteration: 300,000 rows stay
     within the table on a GB300 (2 iterations) and 1,300,000 rows exceed it (9); both formats
-    against the oracle."""
+    against the oracle, and NVFP4 grouped (the contiguous-range kernel) at the same sizes."""
     for M in (300_000, 1_300_000):
         counts = W.moe_counts(E=96, tokens=M, stream=M % 1000)
         off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
@@ -530,6 +530,12 @@ def test_grouped_swizzled_on_both_sides_of_the_row_table_limit():
         for fmt in FMTS:
             c, s = grouped(xb, off, fmt, O.SWIZZLED)
             rc, rs = O.quantize_grouped(xb, off, fmt, O.SWIZZLED, scale_rows=s.shape[0])
+            np.testing.assert_array_equal(s, rs)
+            np.testing.assert_array_equal(c, rc)
+        gs = expert_global_scales(xb, off)
+        for layout in LAYOUTS:
+            c, s = nv_grouped(xb, off, gs, layout)
+            rc, rs = O.nvfp4_quantize_grouped(xb, off, gs, layout, scale_rows=s.shape[0])
             np.testing.assert_array_equal(s, rs)
             np.testing.assert_array_equal(c, rc)
 
