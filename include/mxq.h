@@ -103,11 +103,18 @@ typedef int mx_status;
  *    hold the call computes sum_i x_i H[i][j] with fp32 FMAs instead, so the results are
  *    correct for any H (only slower). For g = 128 the call runs as MX_ROT_DENSE (faster
  *    there).
- * Both kinds compute the same rotation up to fp32 rounding (well inside the 1e-5 normwise
+ *  MX_ROT_AUTO: the same statement as MX_ROT_HADAMARD; the library takes whichever of the two
+ *    kernels measured faster on GB300 for the call: the fp32-FMA kernel for decode-sized calls
+ *    (M <= 16, M * g <= 512) and the tensor cores for g = 128; otherwise the Walsh-Hadamard
+ *    kernel below 4096 rows, and from 4096 rows the tensor cores for 4-bit codes (MXFP4, NVFP4)
+ *    and for MXFP8 codes or QDQ outputs while M * K <= 3 * 2^25, the Walsh-Hadamard kernel above.
+ *    mx_rotate_debug treats it as MX_ROT_HADAMARD.
+ * The kinds compute the same rotation up to fp32 rounding (well inside the 1e-5 normwise
  * tolerance of the rotated path).
  */
 #define MX_ROT_DENSE 0
 #define MX_ROT_HADAMARD 1
+#define MX_ROT_AUTO 2
 
 /* Text of a status code (static storage). */
 const char* mx_status_string(mx_status status);

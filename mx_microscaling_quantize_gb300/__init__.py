@@ -24,6 +24,7 @@ QUEST = 1  # Quest-like block scale (clip point alpha * RMS), MXFP4 only, not gr
 GROUP = 32
 ROT_DENSE = 0     # any H: tensor-core product
 ROT_HADAMARD = 1  # H = H[0][0] * Sylvester (stated by the caller, checked on the device)
+ROT_AUTO = 2      # the same statement; the library takes the kernel measured faster for the call
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmxq.so")
@@ -181,7 +182,7 @@ def mx_quantize(x, fmt, layout=LINEAR, *, codes=None, scales=None, group=GROUP, 
 def mx_qdq(x, fmt, H=None, *, y=None, group=GROUP, rounding=RNE, rot_kind=ROT_DENSE,
            stream=None):
     """Quantize-dequantize bf16 [M, K] -> bf16 [M, K]; with H, rotate each g-chunk first
-    (rot_kind: ROT_DENSE or ROT_HADAMARD)."""
+    (rot_kind: ROT_DENSE, ROT_HADAMARD or ROT_AUTO)."""
     M, K = _input(x)
     g = _rotation(H) if H is not None else 0
     if y is None:

@@ -16,11 +16,27 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool valid_fmt(int fmt) { return fmt == MX_FMT_E2M1 || fmt == MX_FMT_E4M3; }
 bool valid_layout(int layout) { return layout == MX_SCALES_LINEAR || layout == MX_SCALES_SWIZZLED; }
 bool valid_g(int g) { return g == 16 || g == 32 || g == 64 || g == 128; }
-bool valid_rot_kind(int k) { return k == MX_ROT_DENSE || k == MX_ROT_HADAMARD; }
-// The Walsh-Hadamard kernel takes MX_ROT_HADAMARD calls for g <= 64. For g = 128 its two
-// shuffle stages made it 19-42% slower than the tensor-core kernel on every measured shape, so
-// those calls run there (which takes any H).
-bool use_fwht(int rot_kind, int g) { return rot_kind == MX_ROT_HADAMARD && g <= 64; }
+bool valid_rot_kind(int k) {
+  return k == MX_ROT_DENSE || k == MX_ROT_HADAMARD || k == MX_ROT_AUTO;
+}
+// Whether a rotated call runs on the Walsh-Hadamard kernel. MX_ROT_HADAMARD: always for g <= 64
+// (for g = 128 its two shuffle stages made it 19-42% slower than the tensor-core kernel on every
+// measured shape, so those calls run there, which takes any H). MX_ROT_AUTO: the kernel that
+// measured faster on GB300 (steady, back to back) for the call's output and shape: the FMA kernel
+// for decode-sized calls (M <= 16, M * g <= 512); the Walsh-Hadamard kernel below 4096 rows
+// (x[1024, 8192] MXFP4 codes: 6.6 against 7.5 us); from 4096 rows the tensor cores for 4-bit codes
+// (x[8192, 8192]: 29.7 against 31.0 us; x[8192, 28672]: 91.3 against 97.3) and, for the wider
+// outputs (MXFP8 codes, bf16 QDQ), up to 3 * 2^25 elements (QDQ x[4096, 8192]: 22.6-23.0
+// against 23.5-24.5; MXFP8 x[8192, 8192]: 34.1 against 34.8), the Walsh-Hadamard kernel above
+// (QDQ x[4096, 28672]: 73.3-74.5 against 77.3-78.4; MXFP8 x[8192, 28672]: 112.3 against 115.6).
+// wide_out: MXFP8 codes or QDQ.
+bool use_fwht(int rot_kind, int g, bool wide_out, int64_t M, int64_t K) {
+  if (g > 64 || rot_kind == MX_ROT_DENSE) return false;
+  if (rot_kind == MX_ROT_HADAMARD) return true;
+  if (M <= 16 && M * g <= 512) return false;
+  if (M < 4096) return true;
+  return wide_out && M * K > (int64_t(3) << 25);
+}
 
 // Kernel format id of an MX call: the Quest-like scale is its own instantiation of the kernels.
 int kernel_fmt(int fmt, int rounding) {
@@ -148,7 +164,7 @@ mx_status mx_qdq(const void* x, int64_t M, int64_t K, int fmt, int group, int ro
   if (!aligned32(x) || !aligned32(y)) return MX_ERR_ALIGN;
   if (H) {
     if (!aligned16(H)) return MX_ERR_ALIGN;
-    if (use_fwht(rot_kind, g)) {
+    if (use_fwht(rot_kind, g, true, M, K)) {
       mxq::StreamArgs a = stream_args(x, M, K, y);
       a.H = H;
       return from_cuda(mxq::launch_hadamard(kernel_fmt(fmt, rounding), mxq::kRotQdq, false, g, a,
@@ -197,7 +213,7 @@ mx_status mx_rotate_quantize(const void* x, int64_t M, int64_t K, const void* H,
   if (!aligned32(x) || !aligned32(codes)) return MX_ERR_ALIGN;
   if (layout == MX_SCALES_SWIZZLED && !aligned16(scales)) return MX_ERR_ALIGN;
   if (!aligned16(H)) return MX_ERR_ALIGN;
-  if (use_fwht(rot_kind, g)) {
+  if (use_fwht(rot_kind, g, fmt == MX_FMT_E4M3, M, K)) {
     mxq::StreamArgs a = stream_args(x, M, K, codes);
     a.scales = static_cast<uint8_t*>(scales);
     a.scale_cols = layout == MX_SCALES_LINEAR ? K / 32 : ceil_div(K, mxq::kTileCols) * 4;
@@ -298,7 +314,7 @@ mx_status mx_quantize_nvfp4(const void* x, int64_t M, int64_t K, const void* H, 
   int64_t srows = 0, scols = 0;
   mx_nvfp4_scales_shape(M, K, layout, &srows, &scols);
   const bool swz = layout == MX_SCALES_SWIZZLED;
-  if (H && use_fwht(rot_kind, g)) {
+  if (H && use_fwht(rot_kind, g, false, M, K)) {
     mxq::StreamArgs a = stream_args(x, M, K, codes);
     a.scales = static_cast<uint8_t*>(scales);
     a.scale_cols = scols;
@@ -332,7 +348,7 @@ mx_status mx_qdq_nvfp4(const void* x, int64_t M, int64_t K, const void* H, int g
   if (st != MX_OK || empty) return st;
   if (!y) return MX_ERR_NULL;
   if (!aligned32(y)) return MX_ERR_ALIGN;
-  if (H && use_fwht(rot_kind, g)) {
+  if (H && use_fwht(rot_kind, g, true, M, K)) {
     mxq::StreamArgs a = stream_args(x, M, K, y);
     a.gscale = global_scale;
     a.H = H;
@@ -433,7 +449,7 @@ mx_status mx_rotate_debug(const void* x, int64_t M, int64_t K, const void* H, in
   if (!x || !H || !y_f32) return MX_ERR_NULL;
   if (!aligned32(x) || !aligned32(y_f32)) return MX_ERR_ALIGN;
   if (!aligned16(H)) return MX_ERR_ALIGN;
-  if (use_fwht(rot_kind, g)) {
+  if (use_fwht(rot_kind == MX_ROT_AUTO ? MX_ROT_HADAMARD : rot_kind, g, false, M, K)) {
     mxq::StreamArgs a = stream_args(x, M, K, y_f32);
     a.H = H;
     return from_cuda(mxq::launch_hadamard(MX_FMT_E2M1, mxq::kRotDebug, false, g, a,

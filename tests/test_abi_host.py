@@ -53,6 +53,7 @@ def test_macros_match_binding():
     assert int(macros["MX_ROUND_QUEST"]) == mxq.QUEST
     assert int(macros["MX_ROT_DENSE"]) == mxq.ROT_DENSE
     assert int(macros["MX_ROT_HADAMARD"]) == mxq.ROT_HADAMARD
+    assert int(macros["MX_ROT_AUTO"]) == mxq.ROT_AUTO
 
 
 def test_status_strings(L):
@@ -120,12 +121,12 @@ def test_quantize_validation(L):
 
 def test_qdq_and_rotation_validation(L):
     q = L.mx_qdq  # (x, M, K, fmt, group, rounding, H, g, rot_kind, y, stream)
-    for rk in (0, 1):  # MX_ROT_DENSE, MX_ROT_HADAMARD
+    for rk in (0, 1, 2):  # MX_ROT_DENSE, MX_ROT_HADAMARD, MX_ROT_AUTO
         assert q(P, 4, 64, 1, 32, 0, P, 8, rk, P, None) == UNSUP     # g = 8
         assert q(P, 4, 96, 1, 32, 0, P, 64, rk, P, None) == SHAPE    # K % g
         assert q(P, 4, 64, 1, 32, 0, P + 1, 32, rk, P, None) == ALIGN
         assert q(P, 4, 64, 1, 32, 0, P + 8, 32, rk, P, None) == ALIGN
-    assert q(P, 4, 64, 1, 32, 0, P, 32, 2, P, None) == UNSUP         # unknown rot_kind
+    assert q(P, 4, 64, 1, 32, 0, P, 32, 3, P, None) == UNSUP         # unknown rot_kind
     assert q(P, 4, 64, 2, 32, 1, P, 32, 0, P, None) == UNSUP         # Quest-like: MXFP4 only
     assert q(P, 4, 64, 2, 32, 1, None, 0, 0, P, None) == UNSUP
     assert q(P, 4, 64, 1, 32, 3, None, 0, 0, P, None) == UNSUP       # unknown rounding
@@ -133,13 +134,14 @@ def test_qdq_and_rotation_validation(L):
     assert q(P, 4, 64, 1, 32, 0, None, 0, 0, P + 2, None) == ALIGN
     assert q(P, 4, 64, 1, 32, 0, None, 0, 0, P + 16, None) == ALIGN
     r = L.mx_rotate_quantize  # (x, M, K, H, g, rot_kind, fmt, group, layout, rnd, codes, scales, s)
-    for rk in (0, 1):
+    for rk in (0, 1, 2):
         assert r(P, 4, 64, P, 48, rk, 1, 32, 1, 0, P, P, None) == UNSUP
         assert r(P, 4, 192, P, 128, rk, 1, 32, 1, 0, P, P, None) == SHAPE
         assert r(P, 4, 64, None, 32, rk, 1, 32, 1, 0, P, P, None) == NULL
         assert r(P, 4, 64, P, 32, rk, 1, 32, 1, 0, P, P + 8, None) == ALIGN
         assert r(None, 0, 64, None, 32, rk, 1, 32, 1, 0, None, None, None) == OK
     assert r(P, 4, 64, P, 32, -1, 1, 32, 1, 0, P, P, None) == UNSUP
+    assert r(P, 4, 64, P, 32, 3, 1, 32, 1, 0, P, P, None) == UNSUP
     assert r(P, 4, 64, P, 32, 0, 2, 32, 1, 1, P, P, None) == UNSUP  # Quest-like: MXFP4 only
     assert r(P, 4, 64, P, 32, 0, 1, 32, 1, 1, P, P + 8, None) == ALIGN
     d = L.mx_rotate_debug  # (x, M, K, H, g, rot_kind, y, stream)
@@ -186,7 +188,7 @@ def test_nvfp4_shapes_and_validation(L):
     assert q(P, 4, 48, None, 0, 0, P, 0, P, P, None) == SHAPE
     assert q(P, 4, 64, None, 0, 0, P, 2, P, P, None) == UNSUP
     assert q(P, 4, 64, P, 8, 0, P, 0, P, P, None) == UNSUP
-    assert q(P, 4, 64, P, 32, 2, P, 0, P, P, None) == UNSUP          # unknown rot_kind
+    assert q(P, 4, 64, P, 32, 3, P, 0, P, P, None) == UNSUP          # unknown rot_kind
     assert q(P, 4, 96, P, 64, 1, P, 0, P, P, None) == SHAPE
     assert q(P, 4, 64, None, 0, 0, None, 0, P, P, None) == NULL
     assert q(None, 4, 64, None, 0, 0, P, 0, P, P, None) == NULL
@@ -195,7 +197,7 @@ def test_nvfp4_shapes_and_validation(L):
     assert q(P, 4, 64, None, 0, 0, P, 0, P + 16, P, None) == ALIGN
     assert q(P, 4, 64, None, 0, 0, P, 0, P, P + 1, None) == ALIGN
     assert q(P, 4, 64, None, 0, 0, P, 1, P, P + 2, None) == ALIGN
-    for rk in (0, 1):
+    for rk in (0, 1, 2):
         assert q(P, 4, 64, P + 8, 32, rk, P, 1, P, P, None) == ALIGN
     assert q(None, 0, 64, None, 0, 0, None, 1, None, None, None) == OK
     d = L.mx_qdq_nvfp4  # (x, M, K, H, g, rot_kind, gs, y, stream)

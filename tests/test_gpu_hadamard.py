@@ -292,3 +292,47 @@ def test_hadamard_weight_and_nvfp4_full_size():
     q = T.bf16_bits(mxq.mx_qdq_nvfp4(xg, gst, T.to_gpu(H), rot_kind=HAD))
     within(T.check_rotated_multi(xa, H, nvfp4={gs: (T.u8(c), T.unswizzle(T.u8(s), 8192, 2 * 28672))},
                                  nvfp4_qdq={gs: q}))
+
+
+# (what, fmt, M, K, g, kernel ROT_AUTO must take)
+AUTO_CASES = [
+    ("codes", O.E2M1, 1, 8192, 32, "dense"),        # decode-sized: FMA kernel
+    ("codes", O.E2M1, 1024, 8192, 32, "hadamard"),  # below 4096 rows
+    ("codes", O.E2M1, 4096, 8192, 32, "dense"),     # 4-bit codes from 4096 rows
+    ("codes", O.E4M3, 4096, 8192, 32, "dense"),     # wide output, M * K <= 3 * 2^25
+    ("codes", O.E4M3, 4096, 32768, 64, "hadamard"),  # wide output above it
+    ("qdq", O.E2M1, 4096, 8192, 16, "dense"),
+    ("qdq", O.E4M3, 4096, 28672, 32, "hadamard"),
+    ("codes", O.E2M1, 1024, 8192, 128, "dense"),    # g = 128: tensor cores
+    ("nvfp4", None, 4096, 8192, 16, "dense"),
+    ("nvfp4", None, 1024, 8192, 16, "hadamard"),
+    ("quest", O.E2M1, 4096, 8192, 32, "dense"),
+]
+
+
+@pytest.mark.parametrize("case", AUTO_CASES, ids=lambda c: f"{c[0]}-{c[1]}-{c[2]}x{c[3]}-g{c[4]}")
+def test_rot_auto_takes_the_faster_kernel_of_the_table(case):
+    """ROT_AUTO gives exactly the output of the kernel its table names for the call. The two
+    kernels round the rotation differently, so on these sizes their codes or QDQ outputs differ in
+    a few blocks next to rounding midpoints; where they happen to agree the case still checks that
+    ROT_AUTO computes a correct result."""
+    what, fmt, M, K, g, want = case
+    x = T.to_gpu(W.rotate_quant_activation(M, K, stream=g))
+    H = T.to_gpu(W.normalized_hadamard_bf16(g))
+    gs = torch.tensor([448.0 * 6.0 / 8.0], device="cuda")
+
+    def run(rk):
+        if what == "codes":
+            c, s = mxq.mx_rotate_quantize(x, H, fmt, mxq.SWIZZLED, rot_kind=rk)
+            return torch.cat([c.view(-1), s.view(-1)])
+        if what == "quest":
+            c, s = mxq.mx_rotate_quantize(x, H, fmt, mxq.SWIZZLED, rot_kind=rk, rounding=mxq.QUEST)
+            return torch.cat([c.view(-1), s.view(-1)])
+        if what == "qdq":
+            return mxq.mx_qdq(x, fmt, H, rot_kind=rk).view(torch.uint8).view(-1)
+        c, s = mxq.mx_quantize_nvfp4(x, gs, mxq.SWIZZLED, H, rot_kind=rk)
+        return torch.cat([c.view(-1), s.view(-1)])
+
+    auto = run(mxq.ROT_AUTO)
+    ref = run(mxq.ROT_DENSE if want == "dense" else mxq.ROT_HADAMARD)
+    assert torch.equal(auto, ref)
