@@ -540,6 +540,27 @@ def test_grouped_on_both_sides_of_the_row_table_limit():
             np.testing.assert_array_equal(c, rc)
 
 
+@pytest.mark.parametrize("K", [8224, 28672])
+def test_grouped_wide_rows(K):
+    """Rows of more than 256 blocks (K = 8224: 257 blocks, the column wrap not a power of two;
+    K = 28672: 896): each CTA iteration then spans at most two rows of the row table. 22 experts:
+    Zipf counts with two empty experts inserted, both MX formats and NVFP4, both layouts."""
+    counts = np.insert(W.moe_counts(E=20, tokens=600, stream=K % 97), [3, 11], 0)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    xb = W.mxfp8_linear_quant(int(off[-1]), K, stream=K)
+    for layout in LAYOUTS:
+        for fmt in FMTS:
+            c, s = grouped(xb, off, fmt, layout)
+            rc, rs = O.quantize_grouped(xb, off, fmt, layout, scale_rows=s.shape[0])
+            np.testing.assert_array_equal(s, rs)
+            np.testing.assert_array_equal(c, rc)
+        gs = expert_global_scales(xb, off)
+        c, s = nv_grouped(xb, off, gs, layout)
+        rc, rs = O.nvfp4_quantize_grouped(xb, off, gs, layout, scale_rows=s.shape[0])
+        np.testing.assert_array_equal(s, rs)
+        np.testing.assert_array_equal(c, rc)
+
+
 def test_grouped_maximum_expert_count():
     """1024 experts (the limit; the prologue's per-thread share of the expert scan is then
     full), random counts with many empty experts, MXFP8 and NVFP4, both layouts."""
