@@ -14,7 +14,10 @@
 // expert's padded row). After the main loop a pass spread over the whole grid writes zeros
 // into the pad bytes.
 // NVFP4 (E2M1 codes, one E4M3 scale per 16 elements under an fp32 global scale) runs on the
-// same kernel: a thread's 32 elements are two NVFP4 blocks.
+// same kernel: a thread's 32 elements are two NVFP4 blocks; so does MXFP4 under the Quest-like
+// scale (FMT kFmtE2M1Quest: the scale from the block's sum of squares instead of its abs-max).
+// Grouped MX calls with swizzled scales take a grid-stride kernel with a per-CTA table of row
+// shifts (mx_grouped_table_kernel, below) while that table fits.
 #include <algorithm>
 #include <map>
 #include <mutex>

@@ -171,6 +171,18 @@ def test_quest_full_size_rotate_quantize_and_qdq():
     assert stats["qdq"]["exempt_blocks"] <= 4, stats
 
 
+@pytest.mark.parametrize("rot_kind", [mxq.ROT_DENSE, mxq.ROT_HADAMARD])
+def test_quest_full_size_wide_rows(rot_kind):
+    """Quest-like rotate + quantize of x[8192, 28672] (g = 32), the size the benchmark times,
+    whole outputs, on the tensor-core and the Walsh-Hadamard kernels."""
+    xb = W.rotate_quant_activation(8192, 28672)
+    H = W.normalized_hadamard_bf16(32)
+    x, Hd = T.to_gpu(xb), T.to_gpu(H)
+    c, s = mxq.mx_rotate_quantize(x, Hd, mxq.E2M1, mxq.LINEAR, rounding=Q, rot_kind=rot_kind)
+    stats = T.check_quest(xb, H, codes=(T.u8(c), T.u8(s)))
+    assert stats["codes"]["exempt_blocks"] <= 0.01 * stats["codes"]["blocks"], stats
+
+
 def test_quest_rejected_where_unsupported():
     x = torch.zeros(128, 256, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(mxq.MXError):
