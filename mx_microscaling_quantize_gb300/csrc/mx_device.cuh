@@ -127,16 +127,6 @@ __device__ __forceinline__ void mul2(float& lo, float& hi, float s) {
       : "f"(s));
 }
 
-// abs-max of the 8 bf16 of a 16-byte vector as sign-free bf16 bits; NaN propagates (0x7FFF
-// sorts above every other pattern, Inf 0x7F80 above every finite one).
-__device__ __forceinline__ uint32_t absmax_bf16x8(const uint4& v) {
-  uint32_t a, b, m;
-  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x), "r"(v.y));
-  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z), "r"(v.w));
-  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
-  return max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
-}
-
 // max(|a|, |b|, |c|) in one instruction; NaN if any input is NaN.
 __device__ __forceinline__ float absmax3(float a, float b, float c) {
   float d;
@@ -271,17 +261,6 @@ __device__ __forceinline__ uint32_t qdq2_e4m3(float tlo, float thi, float sc) {
 template <int FMT>
 __device__ __forceinline__ uint32_t qdq2(float tlo, float thi, float sc) {
   return mx_e2m1<FMT>() ? qdq2_e2m1(tlo, thi, sc) : qdq2_e4m3(tlo, thi, sc);
-}
-
-// 16-byte bf16 vector -> 8 fp32 values times `inv` (= 2^-s)
-__device__ __forceinline__ void scaled8_bf16(const uint4& v, float inv, float* t) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    t[2 * i] = bf16_lo(w[i]);
-    t[2 * i + 1] = bf16_hi(w[i]);
-    mul2(t[2 * i], t[2 * i + 1], inv);
-  }
 }
 
 constexpr uint32_t kE4M3NaNx4 = 0x7F7F7F7Fu;
